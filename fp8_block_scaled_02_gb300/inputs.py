@@ -1,0 +1,117 @@
+"""Seeded synthetic inputs shaped like the pages' workloads.
+
+This module holds random-number generation only -- none of the method's
+arithmetic -- so both the CUDA path and the CPU oracle can consume the very
+same tensors.  Every generator takes an explicit seed and a device; on a
+given device the output is a pure function of (shape, seed).
+
+Workloads (the weight shapes the pages measure):
+  * tiny ragged       W [320, 704] ~ N(0, 0.02^2), 4 outliers of +-1.5
+  * lm_head           W [152064, 4096], rows N(0, 0.02^2) * r_n,
+                      r_n log-uniform in [0.5, 2]          (FreeToken PR #636)
+  * rotation          48 layers x {[8192,2560], [2560,3072], [6656,2560],
+                      [2560,3072]} ~ N(0, 0.02^2)           (FreeToken PR #389)
+  * sweep / prefill   W [12288, 4096] ~ N(0, 0.02^2)
+  * MXFP8             W [18432, 7168] ~ N(0, 0.02^2) with 0.1% of entries
+                      replaced by 0.02 * t_3 (Student t, 3 d.o.f.)
+  * activations       x [M, K] ~ N(0, 1)
+All tensors are produced in fp32 and rounded once to bf16 (nearest-even).
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+WEIGHT_STD = 0.02
+
+TINY_SHAPE = (320, 704)
+LM_HEAD_SHAPE = (152064, 4096)
+ROTATION_SHAPES = ((8192, 2560), (2560, 3072), (6656, 2560), (2560, 3072))
+ROTATION_LAYERS = 48
+SWEEP_SHAPE = (12288, 4096)
+MX_SHAPE = (18432, 7168)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=torch.device(device))
+    g.manual_seed(int(seed))
+    return g
+
+
+def gaussian_bf16(shape, std: float, seed: int, device="cpu") -> torch.Tensor:
+    g = _gen(seed, device)
+    t = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(torch.bfloat16)
+
+
+def activations(m: int, k: int, seed: int, device="cpu") -> torch.Tensor:
+    """x [M, K] bf16 ~ N(0, 1)."""
+    return gaussian_bf16((m, k), 1.0, seed, device)
+
+
+def tiny_ragged_weight(seed: int = 0, device="cpu") -> torch.Tensor:
+    """[320, 704] ~ N(0, 0.02^2) with 4 outliers (+1.5, -1.5, +1.5, -1.5)
+    at seeded distinct positions."""
+    n, k = TINY_SHAPE
+    g = _gen(seed, device)
+    t = torch.randn((n, k), generator=g, device=device, dtype=torch.float32) * WEIGHT_STD
+    pos = torch.randperm(n * k, generator=g, device=device)[:4]
+    vals = torch.tensor([1.5, -1.5, 1.5, -1.5], device=device)
+    t.view(-1)[pos] = vals
+    return t.to(torch.bfloat16)
+
+
+def tiny_ragged_outliers(seed: int = 0):
+    """(row, col, value) of the 4 outliers of tiny_ragged_weight(seed) on CPU."""
+    n, k = TINY_SHAPE
+    g = _gen(seed, "cpu")
+    torch.randn((n, k), generator=g, dtype=torch.float32)
+    pos = torch.randperm(n * k, generator=g)[:4].tolist()
+    return [(p // k, p % k, v) for p, v in zip(pos, (1.5, -1.5, 1.5, -1.5))]
+
+
+def lm_head_weight(seed: int = 2, device="cpu", shape=LM_HEAD_SHAPE) -> torch.Tensor:
+    """rows N(0, 0.02^2) scaled by r_n, r_n log-uniform in [0.5, 2]."""
+    n, k = shape
+    g = _gen(seed, device)
+    t = torch.randn((n, k), generator=g, device=device, dtype=torch.float32)
+    u = torch.rand((n, 1), generator=g, device=device, dtype=torch.float32)
+    r = torch.exp(math.log(0.5) + u * (math.log(2.0) - math.log(0.5)))
+    t.mul_(WEIGHT_STD * r)
+    return t.to(torch.bfloat16)
+
+
+def rotation_weight(layer: int, j: int, device="cpu") -> torch.Tensor:
+    """Weight j (0..3) of rotation layer `layer`; each has its own seed."""
+    shape = ROTATION_SHAPES[j]
+    return gaussian_bf16(shape, WEIGHT_STD, 1000 + 4 * layer + j, device)
+
+
+def sweep_weight(copy: int = 0, device="cpu") -> torch.Tensor:
+    return gaussian_bf16(SWEEP_SHAPE, WEIGHT_STD, 4000 + copy, device)
+
+
+def heavy_tail_weight(seed: int = 5, device="cpu", shape=MX_SHAPE,
+                      frac: float = 0.001) -> torch.Tensor:
+    """N(0, 0.02^2) with round(frac*N*K) seeded positions replaced by
+    0.02 * t_3, where t_3 = z / sqrt(chi2_3 / 3)."""
+    n, k = shape
+    g = _gen(seed, device)
+    t = torch.randn((n, k), generator=g, device=device, dtype=torch.float32)
+    t.mul_(WEIGHT_STD)
+    cnt = max(1, int(round(frac * n * k)))
+    pos = torch.randint(0, n * k, (cnt,), generator=g, device=device)
+    z = torch.randn((cnt,), generator=g, device=device, dtype=torch.float32)
+    c = torch.randn((cnt, 3), generator=g, device=device, dtype=torch.float32)
+    t3 = z / torch.sqrt((c * c).sum(dim=1) / 3.0)
+    t.view(-1)[pos] = WEIGHT_STD * t3
+    return t.to(torch.bfloat16)
+
+
+def bf16_bits(t: torch.Tensor):
+    """CPU numpy uint16 view of a bf16 tensor (copying from the device if needed)."""
+    import numpy as np
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

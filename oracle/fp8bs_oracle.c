@@ -1,0 +1,296 @@
+/*
+ * fp8bs_oracle.c -- plain, slow CPU oracle (TEST INFRASTRUCTURE ONLY).
+ *
+ * Only tests/, the smoke check and the benchmark's CPU-baseline leg use this
+ * file.  It shares no code, table or constant generator with the CUDA
+ * library: everything here is derived from the definitions it cites.
+ *
+ * Parity pins for each function live in tests/test_oracle_*.py.
+ */
+#include "fp8bs_oracle.h"
+
+#include <assert.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define TILE 128   /* Atlas quantize_fp8_bs.rs: FP8_BLOCK = 128, both axes   */
+#define MXG 32     /* FreeToken issue #624: one e8m0 scale per 32 elements   */
+#define E4M3_MAX 448.0
+
+/* ---------------------------------------------------------------------
+ * e4m3fn ("E4M3 FN": 1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, S.1111.111 is NaN, so the largest finite value is
+ * 1.75 * 2^8 = 448).  This is the OCP 8-bit floating point E4M3 encoding
+ * the pages call "e4m3" / "FP8 E4M3".
+ * ------------------------------------------------------------------- */
+double oracle_e4m3_decode(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double mag;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);          /* subnormal: m/8 * 2^(1-7) */
+    else
+        mag = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7)     */
+    return sign ? -mag : mag;
+}
+
+/*
+ * Round to the nearest finite e4m3fn value by brute force: scan all 127
+ * non-negative finite magnitudes (codes 0x00..0x7E, increasing in value) and
+ * keep the closest; on a tie between two neighbours keep the one whose code
+ * is even (even mantissa LSB = round-half-to-even).  |v| >= 448 saturates to
+ * 448 ("satfinite").  The sign is reattached, so -0.0 and tiny negatives give
+ * 0x80.
+ *
+ * Exactness of the distances: callers pass either a binary32 value or a
+ * binary64 value with at most 8 significant bits.  For |v| >= 2^-10 both
+ * |dec - |v|| are exact in binary64 (their bits span at most 2^8..2^-33);
+ * below 2^-10 the nearest value is 0, whose distance |v| is exact, and every
+ * other distance exceeds 2^-10 by far more than its rounding error.
+ */
+uint8_t oracle_e4m3_encode(double v)
+{
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    int best = 0;
+    double bestd;
+    int c;
+    assert(!isnan(v) && !isinf(v));
+    if (a >= E4M3_MAX)
+        return (uint8_t)(0x7E | (neg << 7));
+    bestd = a; /* distance to code 0x00 (= 0.0) */
+    for (c = 1; c <= 0x7E; ++c) {
+        double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        if (d < bestd || (d == bestd && (c & 1) == 0)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)(best | (neg << 7));
+}
+
+void oracle_e4m3_encode_f32_array(const float *v, int64_t n, uint8_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_encode((double)v[i]);
+}
+
+/* ---------------------------------------------------------------------
+ * bf16: the top 16 bits of an IEEE binary32.
+ * ------------------------------------------------------------------- */
+static float bf16_to_float(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+double oracle_bf16_to_double(uint16_t bits)
+{
+    return (double)bf16_to_float(bits);
+}
+
+/*
+ * Round a double to bf16 (8 significant bits, exponent range of binary32,
+ * subnormal quantum 2^-133), ties to even, overflow to infinity.
+ */
+uint16_t oracle_double_to_bf16(double v)
+{
+    int e2;
+    double a, q, fl, frac, r;
+    float f;
+    uint32_t u;
+    int neg = signbit(v) ? 1 : 0;
+    if (isnan(v))
+        return 0x7FC0;
+    a = fabs(v);
+    if (isinf(a) || a == 0.0) {
+        r = a;
+    } else {
+        /* a = f * 2^e2 with f in [0.5, 1): the leading bit has weight
+         * 2^(e2-1); bf16 keeps 8 bits, so the quantum is 2^(e2-8), but
+         * never below the subnormal quantum 2^-133. */
+        frexp(a, &e2);
+        if (e2 - 8 < -133)
+            e2 = -133 + 8;
+        q = ldexp(a, -(e2 - 8));      /* exact: power-of-two scaling */
+        fl = floor(q);
+        frac = q - fl;                /* exact: q < 2^9 */
+        if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) != 0.0))
+            fl += 1.0;
+        r = ldexp(fl, e2 - 8);
+        /* largest finite bf16 is (2 - 2^-7) * 2^127 */
+        if (r > ldexp(255.0, 120))
+            r = INFINITY;
+    }
+    f = (float)r; /* exact: r is a bf16 value (or inf) */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)((u >> 16) | (neg ? 0x8000u : 0u));
+}
+
+/* ---------------------------------------------------------------------
+ * Block-FP8 quantization (128 x 128 tiles, fp32 scales).
+ * ------------------------------------------------------------------- */
+static int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+void oracle_block_quantize_tile(const uint16_t *w, int64_t n, int64_t k,
+                                int64_t bn, int64_t bk,
+                                uint8_t *codes, float *scales)
+{
+    int64_t kb = cdiv(k, TILE);
+    int64_t r0 = bn * TILE, c0 = bk * TILE;
+    int64_t r1 = r0 + TILE < n ? r0 + TILE : n;
+    int64_t c1 = c0 + TILE < k ? c0 + TILE : k;
+    int64_t r, c;
+    float amax = 0.0f, s;
+
+    /* amax over the real elements of the tile only (ragged edge tiles) */
+    for (r = r0; r < r1; ++r)
+        for (c = c0; c < c1; ++c) {
+            float a = fabsf(bf16_to_float(w[r * k + c]));
+            assert(!isnan(a) && !isinf(a));
+            if (a > amax)
+                amax = a;
+        }
+    /* s = amax / 448 in binary32; an all-zero tile takes s = 1 */
+    s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    scales[bn * kb + bk] = s;
+    for (r = r0; r < r1; ++r)
+        for (c = c0; c < c1; ++c) {
+            float q = bf16_to_float(w[r * k + c]) / s; /* binary32 quotient */
+            codes[r * k + c] = oracle_e4m3_encode((double)q);
+        }
+}
+
+void oracle_block_quantize(const uint16_t *w, int64_t n, int64_t k,
+                           uint8_t *codes, float *scales)
+{
+    int64_t bn, bk;
+    for (bn = 0; bn < cdiv(n, TILE); ++bn)
+        for (bk = 0; bk < cdiv(k, TILE); ++bk)
+            oracle_block_quantize_tile(w, n, k, bn, bk, codes, scales);
+}
+
+/* ---------------------------------------------------------------------
+ * MXFP8 quantization (groups of 32 consecutive K elements, e8m0 scales).
+ * ------------------------------------------------------------------- */
+static int mx_exponent(double amax)
+{
+    int e, E;
+    if (amax == 0.0)
+        return 127;
+    /* smallest integer e with 448 * 2^e >= amax, by exact comparisons */
+    frexp(amax, &e);
+    e -= 9;
+    while (ldexp(E4M3_MAX, e) < amax)
+        ++e;
+    while (ldexp(E4M3_MAX, e - 1) >= amax)
+        --e;
+    E = e + 127;
+    if (E < 0)
+        E = 0;
+    if (E > 254)
+        E = 254;
+    return E;
+}
+
+static void mx_quantize_row(const uint16_t *w, int64_t k, int64_t r,
+                            uint8_t *codes, uint8_t *e8m0)
+{
+    int64_t G = cdiv(k, MXG), g, c;
+    for (g = 0; g < G; ++g) {
+        int64_t c0 = g * MXG, c1 = c0 + MXG < k ? c0 + MXG : k;
+        double amax = 0.0, scale;
+        int E;
+        for (c = c0; c < c1; ++c) {
+            double a = fabs(oracle_bf16_to_double(w[r * k + c]));
+            assert(!isnan(a) && !isinf(a));
+            if (a > amax)
+                amax = a;
+        }
+        E = mx_exponent(amax);
+        e8m0[r * G + g] = (uint8_t)E;
+        scale = ldexp(1.0, E - 127);
+        for (c = c0; c < c1; ++c) /* w / 2^(E-127): exact in binary64 */
+            codes[r * k + c] =
+                oracle_e4m3_encode(oracle_bf16_to_double(w[r * k + c]) / scale);
+    }
+}
+
+void oracle_mx_quantize(const uint16_t *w, int64_t n, int64_t k,
+                        uint8_t *codes, uint8_t *e8m0)
+{
+    int64_t r;
+    for (r = 0; r < n; ++r)
+        mx_quantize_row(w, k, r, codes, e8m0);
+}
+
+void oracle_mx_quantize_rows(const uint16_t *w, int64_t n, int64_t k,
+                             const int64_t *rows, int64_t nrows,
+                             uint8_t *codes, uint8_t *e8m0)
+{
+    int64_t j;
+    (void)n;
+    for (j = 0; j < nrows; ++j)
+        mx_quantize_row(w, k, rows[j], codes, e8m0);
+}
+
+/* ---------------------------------------------------------------------
+ * W8A16 GEMV, y = x . dequant(W)^T, in binary64.  dec(q) * s is exact in
+ * binary64 (4 + 24 significant bits) and so is each product with a bf16 x
+ * (8 more bits); only the K-term sum rounds, at binary64 precision.
+ * ------------------------------------------------------------------- */
+void oracle_block_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
+                       const float *scales, int64_t n, int64_t k,
+                       const int64_t *rows, int64_t nrows, double *y64)
+{
+    double dec[256];
+    int64_t kb = cdiv(k, TILE), mi, j, c;
+    int i;
+    if (rows == NULL)
+        nrows = n;
+    for (i = 0; i < 256; ++i)
+        dec[i] = oracle_e4m3_decode((uint8_t)i);
+    for (mi = 0; mi < m; ++mi)
+        for (j = 0; j < nrows; ++j) {
+            int64_t r = rows ? rows[j] : j;
+            double sum = 0.0;
+            for (c = 0; c < k; ++c) {
+                double s = (double)scales[(r / TILE) * kb + c / TILE];
+                double wq = dec[codes[r * k + c]] * s;
+                sum += oracle_bf16_to_double(x[mi * k + c]) * wq;
+            }
+            y64[mi * nrows + j] = sum;
+        }
+}
+
+void oracle_mx_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
+                    const uint8_t *e8m0, int64_t n, int64_t k,
+                    const int64_t *rows, int64_t nrows, double *y64)
+{
+    double dec[256];
+    int64_t G = cdiv(k, MXG), mi, j, c;
+    int i;
+    if (rows == NULL)
+        nrows = n;
+    for (i = 0; i < 256; ++i)
+        dec[i] = oracle_e4m3_decode((uint8_t)i);
+    for (mi = 0; mi < m; ++mi)
+        for (j = 0; j < nrows; ++j) {
+            int64_t r = rows ? rows[j] : j;
+            double sum = 0.0;
+            for (c = 0; c < k; ++c) {
+                double s = ldexp(1.0, (int)e8m0[r * G + c / MXG] - 127);
+                double wq = dec[codes[r * k + c]] * s;
+                sum += oracle_bf16_to_double(x[mi * k + c]) * wq;
+            }
+            y64[mi * nrows + j] = sum;
+        }
+}

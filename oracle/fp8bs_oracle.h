@@ -1,0 +1,80 @@
+/*
+ * fp8bs_oracle.h -- plain, slow CPU oracle for block-scaled FP8 / MXFP8
+ * weight quantization and the W8A16 GEMV that consumes it.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This code is the independent statement of what
+ * the library computes; it exists so that tests, the smoke check and the
+ * benchmark's CPU baseline can compare against it.  No product code path may
+ * include, link or call it, and it shares no code with the CUDA library.
+ *
+ * Formats and layouts (all row-major, K contiguous):
+ *   w      bf16 [N,K]              (uint16_t bit patterns)
+ *   codes  e4m3fn [N,K]            one byte per weight
+ *   scales fp32 [ceil(N/128), ceil(K/128)]        128x128 block scales
+ *   e8m0   uint8 [N, ceil(K/32)]   MX power-of-two scale exponents (bias 127)
+ *   x      bf16 [M,K], y bf16 [M,N]
+ *
+ * Sources: FreeToken PR #636 "opt-in fp8-block QAT for the lm_head"
+ * (How it works, Changes, Validation); Atlas spark_model/weight_map/
+ * quantize_fp8_bs.rs (quantize_to_fp8_blockscaled: [n,k] bf16 weight,
+ * one byte per weight, one f32 per [128,128] tile, [n_blocks, k_blocks]
+ * grid); FreeToken issue #624 "Load-time MXFP8 requantization" (Proposed
+ * solution: e4m3 codes, one e8m0 scale per 32 elements, ceil-log2 of
+ * amax/448); InfiniLM PR #586 (Summary: 128x128 block scales, W8A16).
+ *
+ * Build: plain C11, no -ffast-math, -ffp-contract=off, so that every float
+ * operation below is one IEEE-754 binary32 or binary64 operation.
+ */
+#ifndef FP8BS_ORACLE_H
+#define FP8BS_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* e4m3fn code -> value (NaN for 0x7F / 0xFF). */
+double oracle_e4m3_decode(uint8_t code);
+/* nearest e4m3fn code, ties to even, saturating to +-448; sign kept for zero. */
+uint8_t oracle_e4m3_encode(double v);
+/* element-wise oracle_e4m3_encode over binary32 inputs. */
+void oracle_e4m3_encode_f32_array(const float *v, int64_t n, uint8_t *out);
+
+double oracle_bf16_to_double(uint16_t bits);
+/* round a double to the nearest bf16 (ties to even; overflow -> inf). */
+uint16_t oracle_double_to_bf16(double v);
+
+/* 128x128 block quantization: amax over the real elements of each tile,
+ * s = amax/448 in fp32 (s = 1 for an all-zero tile), q = e4m3(w/s) with the
+ * quotient formed in fp32. */
+void oracle_block_quantize(const uint16_t *w, int64_t n, int64_t k,
+                           uint8_t *codes, float *scales);
+/* the same for a single tile (bn, bk); writes only that tile's codes and
+ * its one scale into the full-size arrays. */
+void oracle_block_quantize_tile(const uint16_t *w, int64_t n, int64_t k,
+                                int64_t bn, int64_t bk,
+                                uint8_t *codes, float *scales);
+
+/* MXFP8: per row, per group of 32 consecutive K elements (the last group
+ * may be short): e = smallest integer with 448*2^e >= amax, E = e+127
+ * clamped to [0,254] (E = 127 for amax = 0), q = e4m3(w * 2^(127-E)). */
+void oracle_mx_quantize(const uint16_t *w, int64_t n, int64_t k,
+                        uint8_t *codes, uint8_t *e8m0);
+void oracle_mx_quantize_rows(const uint16_t *w, int64_t n, int64_t k,
+                             const int64_t *rows, int64_t nrows,
+                             uint8_t *codes, uint8_t *e8m0);
+
+/* y64[mi, j] = sum_k x[mi,k] * dec(q[rows[j],k]) * s(rows[j],k), in fp64.
+ * Output layout [m, nrows].  rows == NULL means all n rows in order. */
+void oracle_block_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
+                       const float *scales, int64_t n, int64_t k,
+                       const int64_t *rows, int64_t nrows, double *y64);
+void oracle_mx_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
+                    const uint8_t *e8m0, int64_t n, int64_t k,
+                    const int64_t *rows, int64_t nrows, double *y64);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
