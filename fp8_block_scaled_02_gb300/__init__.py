@@ -1,0 +1,174 @@
+"""fp8_block_scaled_02_gb300 -- block-scaled FP8 / MXFP8 W8A16 on GB300.
+
+A thin Python binding over the C ABI in ``include/fp8bs.h`` (``libfp8bs.so``,
+built from ``csrc/`` for sm_103a).  Every function here only marshals
+arguments -- device pointers, sizes and the current CUDA stream -- and calls
+the library; all computation runs in the library's kernels.  There is no CPU
+fallback: if the shared library has not been built, or a tensor is not on a
+CUDA device, the call raises.
+
+Functions (names follow the C entry points):
+    quantize(w)            -> (codes u8 [N,K], scales f32 [ceil(N/128), ceil(K/128)])
+    gemv(x, codes, scales) -> y bf16 [M,N]
+    mx_quantize(w)         -> (codes u8 [N,K], e8m0 u8 [N, ceil(K/32)])
+    mx_gemv(x, codes, e8m0)-> y bf16 [M,N]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PATH_AUTO, PATH_DECODE, PATH_PREFILL, PATH_GENERIC = 0, 1, 2, 3
+PATH_NAMES = {PATH_AUTO: "auto", PATH_DECODE: "decode", PATH_PREFILL: "prefill", PATH_GENERIC: "generic"}
+
+STATUS = {0: "FP8BS_OK", -1: "FP8BS_ERR_NULL", -2: "FP8BS_ERR_SHAPE", -3: "FP8BS_ERR_BLOCK",
+          -4: "FP8BS_ERR_ALIGN", -5: "FP8BS_ERR_CUDA", -6: "FP8BS_ERR_DEVICE", -7: "FP8BS_ERR_PATH"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfp8bs.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({strerror(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfp8bs.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "or `python fp8_block_scaled_02_gb300/build.py`")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.fp8bs_quantize.argtypes = [p, i64, i64, i32, p, p, p]
+        L.fp8bs_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
+        L.fp8bs_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
+        L.mxfp8_quantize.argtypes = [p, i64, i64, p, p, p]
+        L.mxfp8_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
+        L.mxfp8_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
+        L.fp8bs_select_path.argtypes = [i64, i64, i64, p, p, i32]
+        L.fp8bs_strerror.argtypes = [i32]
+        L.fp8bs_strerror.restype = ctypes.c_char_p
+        L.fp8bs_check_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+        L.fp8bs_version.argtypes = []
+        for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
+                  "mxfp8_gemv_ex", "fp8bs_select_path", "fp8bs_check_device_error", "fp8bs_version"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().fp8bs_strerror(int(status)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise Fp8bsError(status, what)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def cdiv(a: int, b: int) -> int:
+    return (a + b - 1) // b
+
+
+def quantize(w, block: int = 128, codes=None, scales=None, stream=None):
+    """Block-FP8 load-time quantization of a bf16 [N, K] CUDA tensor."""
+    import torch
+    n, k = w.shape
+    if codes is None:
+        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((cdiv(n, 128), cdiv(k, 128)), dtype=torch.float32, device=w.device)
+    _check(lib().fp8bs_quantize(_dev(w, torch.bfloat16, "w"), n, k, int(block), _dev(codes, torch.uint8, "codes"),
+                                _dev(scales, torch.float32, "scales"), _stream(stream)), "fp8bs_quantize")
+    return codes, scales
+
+
+def gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
+    """y[M, N] = x[M, K] . dequant(codes, scales)^T (bf16 out, fp32 accumulate)."""
+    import torch
+    m, k = x.shape
+    n = codes.shape[0]
+    if codes.shape[1] != k:
+        raise ValueError("codes and x disagree on K")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(lib().fp8bs_gemv_ex(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
+                               _dev(scales, torch.float32, "scales"), n, k, _dev(y, torch.bfloat16, "y"),
+                               int(path), _stream(stream)), "fp8bs_gemv")
+    return y
+
+
+def mx_quantize(w, codes=None, e8m0=None, stream=None):
+    """MXFP8 load-time quantization of a bf16 [N, K] CUDA tensor."""
+    import torch
+    n, k = w.shape
+    if codes is None:
+        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    if e8m0 is None:
+        e8m0 = torch.empty((n, cdiv(k, 32)), dtype=torch.uint8, device=w.device)
+    _check(lib().mxfp8_quantize(_dev(w, torch.bfloat16, "w"), n, k, _dev(codes, torch.uint8, "codes"),
+                                _dev(e8m0, torch.uint8, "e8m0"), _stream(stream)), "mxfp8_quantize")
+    return codes, e8m0
+
+
+def mx_gemv(x, codes, e8m0, y=None, path: int = PATH_AUTO, stream=None):
+    """y[M, N] = x[M, K] . dequant_mx(codes, e8m0)^T."""
+    import torch
+    m, k = x.shape
+    n = codes.shape[0]
+    if codes.shape[1] != k:
+        raise ValueError("codes and x disagree on K")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(lib().mxfp8_gemv_ex(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
+                               _dev(e8m0, torch.uint8, "e8m0"), n, k, _dev(y, torch.bfloat16, "y"),
+                               int(path), _stream(stream)), "mxfp8_gemv")
+    return y
+
+
+def select_path(m: int, n: int, k: int, x_ptr: int = 0, codes_ptr: int = 0, mx: bool = False) -> int:
+    """Path the AUTO dispatch would take (host-only; pointers only matter for alignment)."""
+    return lib().fp8bs_select_path(m, n, k, ctypes.c_void_p(x_ptr), ctypes.c_void_p(codes_ptr), int(mx))
+
+
+def check_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the kernels' error word."""
+    word = ctypes.c_uint32(0)
+    st = lib().fp8bs_check_device_error(_stream(stream), ctypes.byref(word))
+    if st not in (0, -6):
+        raise Fp8bsError(st, "fp8bs_check_device_error")
+    return int(word.value)

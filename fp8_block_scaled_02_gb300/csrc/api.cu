@@ -1,0 +1,154 @@
+// api.cu -- the C ABI (include/fp8bs.h): argument validation and shape-only
+// dispatch to the kernels.  Nothing here allocates, synchronises (except the
+// explicit debug query) or branches on tensor values.
+#include "../../include/fp8bs.h"
+#include "internal.h"
+
+namespace {
+
+using namespace fp8bs;
+
+constexpr int64_t kDecodeMaxM = 32;   // rows of x per decode launch
+constexpr int64_t kMaxDim = 1ll << 31;  // n, k and m must fit int32 for the kernels
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+
+// The TMA-staged kernels need 16-byte aligned x and codes with k % 16 == 0
+// (TMA row pitch and base address rules).
+inline bool tma_ok(int64_t k, const void *x, const void *codes) {
+    return (k % 16) == 0 && aligned(x, 16) && aligned(codes, 16);
+}
+
+int select_path(int64_t m, int64_t k, const void *x, const void *codes, bool mx) {
+    if (!tma_ok(k, x, codes)) return FP8BS_PATH_GENERIC;
+    if (mx || m <= kDecodeMaxM) return FP8BS_PATH_DECODE;
+    return FP8BS_PATH_PREFILL;
+}
+
+int check_gemv_args(const void *x, int64_t m, const uint8_t *codes, const void *scales, int64_t n,
+                    int64_t k, void *y, int path) {
+    if (m < 0 || n <= 0 || k <= 0 || m >= kMaxDim || n >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (path < FP8BS_PATH_AUTO || path > FP8BS_PATH_GENERIC) return FP8BS_ERR_PATH;
+    if (m == 0) return FP8BS_OK;
+    if (!x || !codes || !scales || !y) return FP8BS_ERR_NULL;
+    if (!aligned(x, 2) || !aligned(y, 2)) return FP8BS_ERR_ALIGN;
+    return FP8BS_OK;
+}
+
+int run_decode_chunks(const DecodeArgs &a, bool mx, cudaStream_t st) {
+    for (int64_t m0 = 0; m0 < a.m; m0 += kDecodeMaxM) {
+        DecodeArgs c = a;
+        c.m = a.m - m0 < kDecodeMaxM ? a.m - m0 : kDecodeMaxM;
+        c.x = static_cast<const char *>(a.x) + m0 * a.k * 2;
+        c.y = static_cast<char *>(a.y) + m0 * a.n * 2;
+        const cudaError_t e = launch_decode(c, mx, st);
+        if (e != cudaSuccess) return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
+}
+
+int gemv_dispatch(const DecodeArgs &a, bool mx, int path, cudaStream_t st) {
+    const bool tma = tma_ok(a.k, a.x, a.codes);
+    if (path == FP8BS_PATH_AUTO) path = select_path(a.m, a.k, a.x, a.codes, mx);
+    switch (path) {
+        case FP8BS_PATH_GENERIC:
+            return cuda_status(launch_generic_gemv(a, mx, st));
+        case FP8BS_PATH_DECODE:
+            if (!tma) return FP8BS_ERR_PATH;
+            return run_decode_chunks(a, mx, st);
+        case FP8BS_PATH_PREFILL: {
+            if (!tma || mx) return FP8BS_ERR_PATH;
+            const cudaError_t e = launch_prefill(a, st);
+            if (e == cudaErrorNotSupported) return run_decode_chunks(a, mx, st);
+            return cuda_status(e);
+        }
+        default:
+            return FP8BS_ERR_PATH;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8bs_version(void) { return 100; }
+
+const char *fp8bs_strerror(int status) {
+    switch (status) {
+        case FP8BS_OK: return "ok";
+        case FP8BS_ERR_NULL: return "a required pointer is NULL";
+        case FP8BS_ERR_SHAPE: return "shape out of range (need n > 0, k > 0, m >= 0, all < 2^31)";
+        case FP8BS_ERR_BLOCK: return "unsupported block size (only 128 is supported)";
+        case FP8BS_ERR_ALIGN: return "pointer not aligned to its element size";
+        case FP8BS_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case FP8BS_ERR_DEVICE: return "a kernel gave up a bounded wait (device error word set)";
+        case FP8BS_ERR_PATH: return "the requested kernel path cannot take this call";
+        default: return "unknown status";
+    }
+}
+
+int fp8bs_quantize(const void *w_bf16, int64_t n, int64_t k, int block, uint8_t *codes_u8, float *scales_f32,
+                   void *stream) {
+    if (n <= 0 || k <= 0 || n >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (block != 128) return FP8BS_ERR_BLOCK;
+    if (!w_bf16 || !codes_u8 || !scales_f32) return FP8BS_ERR_NULL;
+    if (!aligned(w_bf16, 2) || !aligned(scales_f32, 4)) return FP8BS_ERR_ALIGN;
+    const bool vec = (k % 8) == 0 && aligned(w_bf16, 16) && aligned(codes_u8, 8);
+    return cuda_status(
+        launch_block_quantize(w_bf16, n, k, codes_u8, scales_f32, vec, static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp8_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *codes_u8, uint8_t *scales_e8m0,
+                   void *stream) {
+    if (n <= 0 || k <= 0 || n >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (!w_bf16 || !codes_u8 || !scales_e8m0) return FP8BS_ERR_NULL;
+    if (!aligned(w_bf16, 2)) return FP8BS_ERR_ALIGN;
+    const bool vec = (k % 8) == 0 && aligned(w_bf16, 16) && aligned(codes_u8, 8);
+    return cuda_status(
+        launch_mx_quantize(w_bf16, n, k, codes_u8, scales_e8m0, vec, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scales, int64_t n,
+                  int64_t k, void *y_bf16, int path, void *stream) {
+    int st = check_gemv_args(x_bf16, m, codes, scales, n, k, y_bf16, path);
+    if (st != FP8BS_OK || m == 0) return st;
+    if (!aligned(scales, 4)) return FP8BS_ERR_ALIGN;
+    DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k};
+    return gemv_dispatch(a, false, path, static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scales, int64_t n, int64_t k,
+               void *y_bf16, void *stream) {
+    return fp8bs_gemv_ex(x_bf16, m, codes, scales, n, k, y_bf16, FP8BS_PATH_AUTO, stream);
+}
+
+int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const uint8_t *scales_e8m0, int64_t n,
+                  int64_t k, void *y_bf16, int path, void *stream) {
+    int st = check_gemv_args(x_bf16, m, codes, scales_e8m0, n, k, y_bf16, path);
+    if (st != FP8BS_OK || m == 0) return st;
+    if (path == FP8BS_PATH_PREFILL) return FP8BS_ERR_PATH;
+    DecodeArgs a{x_bf16, codes, nullptr, scales_e8m0, y_bf16, m, n, k};
+    return gemv_dispatch(a, true, path, static_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const uint8_t *scales_e8m0, int64_t n,
+               int64_t k, void *y_bf16, void *stream) {
+    return mxfp8_gemv_ex(x_bf16, m, codes, scales_e8m0, n, k, y_bf16, FP8BS_PATH_AUTO, stream);
+}
+
+int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16, const void *codes, int mx) {
+    (void)n;
+    if (m <= 0 || k <= 0) return FP8BS_ERR_SHAPE;
+    return select_path(m, k, x_bf16, codes, mx != 0);
+}
+
+int fp8bs_check_device_error(void *stream, uint32_t *word_out) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
+    const uint32_t w = take_decode_error() | take_prefill_error();
+    if (word_out) *word_out = w;
+    return w ? FP8BS_ERR_DEVICE : FP8BS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,359 @@
+// decode.cu -- W8A16 block-FP8 / MXFP8 GEMV and skinny GEMM for small m
+// (decode batches, m <= 32 per launch): y[m, n] = x[m, k] . dequant(W)^T.
+//
+// Design (sm_103a):
+//  * One CTA owns 128 weight rows (one row of 128x128 block scales) and a
+//    contiguous range of 128-wide K blocks.  When there are too few row
+//    tiles to fill the GPU, the K blocks are split over the CTAs of a thread
+//    block cluster (up to 8) and the partial sums are reduced through
+//    distributed shared memory -- no global workspace, a fixed summation
+//    order, and no waits on other CTAs beyond the hardware cluster barrier.
+//  * A producer warp streams each K block's 128x128 code tile (16 KB) and the
+//    matching x tile with 2-D TMA (128-byte swizzle) into a 4-stage shared
+//    memory ring guarded by mbarriers; 4 consumer warps split the K block
+//    32 columns each.  Every code byte is read from HBM once.
+//  * Consumers decode e4m3 pairs straight to exact bf16 pairs in registers
+//    (prmt + shift + one bf16x2 multiply) and run bf16 mma.sync m16n8k16
+//    with the weights as the 16-row A operand and x as the 8-wide B operand
+//    (swap-AB: m sits on the MMA's n axis, so m <= 32 needs at most four
+//    n8 tiles).  Each K block's fp32 MMA result starts from zero and is
+//    multiplied by that block's fp32 scale before it joins the accumulator
+//    ("promotion"), so the scale is never folded into a rounded bf16 weight.
+//    For MXFP8 the 32-column slice of a warp is exactly one e8m0 group, and
+//    each row's 2^(E-127) multiplies the slice's partial sum.
+//  * The logical k order inside each MMA is a fixed permutation of the
+//    physical columns, applied identically to A and B, so that every thread
+//    fetches 8 contiguous code bytes and 16 contiguous x bytes per K block
+//    with conflict-free shared-memory loads.
+//  * Programmatic dependent launch: a kernel may start (barrier init,
+//    tensor-map prefetch) while the previous kernel in the stream drains; it
+//    reads global memory only after griddepcontrol.wait.
+#include "common.cuh"
+#include "internal.h"
+
+#include <mutex>
+
+namespace fp8bs {
+
+namespace {
+
+__device__ uint32_t g_decode_err;
+
+constexpr int kKB = 128;             // K per stage (one scale block)
+constexpr int kConsumerWarps = 4;    // each owns 32 columns of the K block
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 4;
+constexpr int kMaxSplit = 8;         // portable cluster size limit
+
+template <int MT>
+struct Cfg {
+    // weight rows per CTA: a full block-scale row for m <= 16; half of one
+    // for wider x, which keeps the accumulators (BN/16 * MT * 4 fp32) in
+    // registers
+    static constexpr int kBN = MT <= 2 ? 128 : 64;
+    static constexpr int kXRows = 8 * MT;               // x rows staged (zero-padded)
+    static constexpr int kCodeBytes = kBN * kKB;        // 16 or 8 KB
+    static constexpr int kXPanelBytes = kXRows * 128;   // 64 bf16 of each row
+    static constexpr int kXBytes = 2 * kXPanelBytes;
+    static constexpr int kStageBytes = kCodeBytes + kXBytes;
+    static constexpr int kRedStride = kXRows + 1;       // padded fp32 row
+    static constexpr int kRedBytes = kBN * kRedStride * 4;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRedBytes + 2 * kStages * 8;
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+
+__device__ __forceinline__ float pow2_e8m0(uint32_t E) {
+    return E ? __uint_as_float(E << 23) : __uint_as_float(0x00400000u);
+}
+
+template <int MT, bool MX>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                                                          const __grid_constant__ CUtensorMap tm_x,
+                                                          const float *__restrict__ scales,
+                                                          const uint8_t *__restrict__ e8m0,
+                                                          __nv_bfloat16 *__restrict__ y, int m, int n,
+                                                          int kblocks, int groups, int splits) {
+    using C = Cfg<MT>;
+    constexpr int kBN = C::kBN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    float *red = reinterpret_cast<float *>(smem + kStages * C::kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * C::kStageBytes + C::kRedBytes);
+    uint64_t *empty = full + kStages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kBN;
+    const int split = blockIdx.y;
+    const int kb0 = static_cast<int>((static_cast<int64_t>(split) * kblocks) / splits);
+    const int kb1 = static_cast<int>((static_cast<int64_t>(split + 1) * kblocks) / splits);
+    const int nkb = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_mbarrier_init();
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        prefetch_tensormap(&tm_codes);
+        prefetch_tensormap(&tm_x);
+    }
+    __syncthreads();
+    pdl_wait();  // inputs may be produced by the previous kernel in the stream
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer
+        // The whole warp walks the ring (so it stays converged); lane 0
+        // waits for a free stage and issues the TMA copies.
+        const uint64_t stream_policy = policy_evict_first();
+        for (int it = 0; it < nkb; ++it) {
+            const int s = it % kStages;
+            int good = 1;
+            if (it >= kStages && lane == 0) good = mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1);
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                if (lane == 0) atomicOr(&g_decode_err, ERRBIT_EMPTY_WAIT);
+                break;
+            }
+            if (lane == 0) {
+                uint8_t *st = smem + s * C::kStageBytes;
+                const int kx = (kb0 + it) * kKB;
+                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                tma_load_2d_hint(st, &tm_codes, &full[s], kx, n0, stream_policy);
+                tma_load_2d(st + C::kCodeBytes, &tm_x, &full[s], kx, 0);
+                tma_load_2d(st + C::kCodeBytes + C::kXPanelBytes, &tm_x, &full[s], kx + 64, 0);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ------------------------------------------------------ consumers
+        const int g = lane >> 2, t = lane & 3;
+        float acc[kBN / 16][MT][4];
+#pragma unroll
+        for (int rt = 0; rt < kBN / 16; ++rt)
+#pragma unroll
+            for (int j = 0; j < MT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[rt][j][q] = 0.0f;
+
+        // x rows of this thread's B fragments: row 8j + pi(g) with
+        // pi(g) = (g >> 1) | ((g & 1) << 2) (bank-conflict-free swizzle use)
+        const int xrow_base = (g >> 1) | ((g & 1) << 2);
+        const int xpanel = warp >> 1;
+        const int xchunk = 4 * (warp & 1) + t;
+        // code rows of this thread's A fragments: 2g and 2g+1 of each 16-row tile
+        const int cchunk = 2 * warp + (t >> 1);
+        const int coff = (t & 1) * 8;
+        const float *srow = MX ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks;
+
+        for (int it = 0; it < nkb; ++it) {
+            const int s = it % kStages;
+            // every lane waits (acquire); the warp leaves together if any gave up
+            const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
+            if (!__all_sync(0xffffffffu, ready)) {
+                if (lane == 0) atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
+                break;
+            }
+            const uint8_t *cs = smem + s * C::kStageBytes;
+            const uint8_t *xs = cs + C::kCodeBytes + xpanel * C::kXPanelBytes;
+
+            uint32_t bx[MT][4];
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+                const int xr = 8 * j + xrow_base;
+                const uint4 v = *reinterpret_cast<const uint4 *>(xs + xr * 128 + ((xchunk ^ (xr & 7)) << 4));
+                bx[j][0] = v.x;
+                bx[j][1] = v.y;
+                bx[j][2] = v.z;
+                bx[j][3] = v.w;
+            }
+            const float sblk = MX ? 0.0f : __ldg(srow + kb0 + it);
+            const int grp = (kb0 + it) * 4 + warp;  // MX group of this warp's 32 columns
+
+#pragma unroll
+            for (int rt = 0; rt < kBN / 16; ++rt) {
+                const int ra = rt * 16 + 2 * g, rb = ra + 1;
+                const uint2 qa = *reinterpret_cast<const uint2 *>(cs + ra * 128 + ((cchunk ^ (ra & 7)) << 4) + coff);
+                const uint2 qb = *reinterpret_cast<const uint2 *>(cs + rb * 128 + ((cchunk ^ (rb & 7)) << 4) + coff);
+                const uint32_t a00 = e4m3x2_to_bf16x2(qa.x, 0x9180u), a01 = e4m3x2_to_bf16x2(qb.x, 0x9180u);
+                const uint32_t a02 = e4m3x2_to_bf16x2(qa.x, 0xB3A2u), a03 = e4m3x2_to_bf16x2(qb.x, 0xB3A2u);
+                const uint32_t a10 = e4m3x2_to_bf16x2(qa.y, 0x9180u), a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
+                const uint32_t a12 = e4m3x2_to_bf16x2(qa.y, 0xB3A2u), a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
+                float sa = sblk, sb = sblk;
+                if (MX) {
+                    const int64_t row_a = static_cast<int64_t>(n0) + ra;
+                    const bool gin = grp < groups;
+                    sa = (gin && row_a < n) ? pow2_e8m0(__ldg(e8m0 + row_a * groups + grp)) : 0.0f;
+                    sb = (gin && row_a + 1 < n) ? pow2_e8m0(__ldg(e8m0 + (row_a + 1) * groups + grp)) : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < MT; ++j) {
+                    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                    mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                    acc[rt][j][0] = fmaf(sa, c[0], acc[rt][j][0]);
+                    acc[rt][j][1] = fmaf(sa, c[1], acc[rt][j][1]);
+                    acc[rt][j][2] = fmaf(sb, c[2], acc[rt][j][2]);
+                    acc[rt][j][3] = fmaf(sb, c[3], acc[rt][j][3]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        // Cross-warp reduction, in warp order, into red[n_local][m].
+        // acc[rt][j][q] is y[m = 8j + t + 4(q&1)][n_local = 16rt + 2g + (q>>1)].
+#pragma unroll 1
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            if (warp == w) {
+#pragma unroll
+                for (int rt = 0; rt < kBN / 16; ++rt)
+#pragma unroll
+                    for (int j = 0; j < MT; ++j)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int nl = rt * 16 + 2 * g + (q >> 1);
+                            const int mc = 8 * j + t + 4 * (q & 1);
+                            float *p = red + nl * C::kRedStride + mc;
+                            *p = (w == 0) ? acc[rt][j][q] : *p + acc[rt][j][q];
+                        }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        }
+    }
+    pdl_launch_dependents();
+    __syncthreads();
+
+    // Split-K reduction across the cluster (fixed rank order) and bf16 store.
+    if (splits > 1) cluster_sync_all();
+    const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int rows_per = (kBN + splits - 1) / splits;
+    const int r_begin = rank * rows_per;
+    const int r_end = min(kBN, r_begin + rows_per);
+    const int my_rows = max(0, r_end - r_begin);
+    const int mm = min(m, C::kXRows);
+    const uint32_t red_addr = smem_u32(red);
+    for (int e = threadIdx.x; e < mm * my_rows; e += kThreads) {
+        const int mi = e / my_rows;
+        const int nl = r_begin + (e - mi * my_rows);
+        const int nn = n0 + nl;
+        if (nn >= n) continue;
+        const uint32_t off = static_cast<uint32_t>((nl * C::kRedStride + mi) * 4);
+        float sum;
+        if (splits > 1) {
+            sum = 0.0f;
+            for (int q = 0; q < splits; ++q) sum += dsmem_ld_f32(dsmem_map(red_addr + off, q));
+        } else {
+            sum = red[nl * C::kRedStride + mi];
+        }
+        y[static_cast<int64_t>(mi) * n + nn] = __float2bfloat16_rn(sum);
+    }
+    if (splits > 1) cluster_sync_all();  // keep shared memory alive for peers
+}
+
+// Per-device, per-instantiation launch setup (shared-memory opt-in and the
+// number of CTAs that fit on one SM), done once on first use.
+struct Setup {
+    std::mutex mu;
+    bool done[64] = {};
+    cudaError_t err[64] = {};
+    int resident[64] = {};
+};
+
+template <int MT, bool MX>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
+    using C = Cfg<MT>;
+    constexpr int kBN = C::kBN;
+    auto kern = decode_kernel<MT, MX>;
+    static Setup setup;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int resident = 1;
+    {
+        std::lock_guard<std::mutex> lock(setup.mu);
+        if (!setup.done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            int blocks = 0;
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kThreads, C::kSmemBytes);
+            setup.err[dev] = e;
+            setup.resident[dev] = blocks > 0 ? blocks : 1;
+            setup.done[dev] = true;
+        }
+        if (setup.err[dev] != cudaSuccess) return setup.err[dev];
+        resident = setup.resident[dev];
+    }
+
+    CUtensorMap tm_codes, tm_x;
+    const uint64_t n = static_cast<uint64_t>(a.n), k = static_cast<uint64_t>(a.k),
+                   m = static_cast<uint64_t>(a.m);
+    if (!encode_tensor_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, k, n, k, kKB, kBN,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64,
+                              C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+
+    const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
+    const int ntiles = static_cast<int>((a.n + kBN - 1) / kBN);
+    const int groups = static_cast<int>((a.k + 31) / 32);
+    const int capacity = device_sm_count() * resident;
+    int splits = 1;
+    if (ntiles < capacity) {
+        splits = capacity / ntiles;
+        if (splits > kMaxSplit) splits = kMaxSplit;
+        if (splits > kblocks) splits = kblocks;
+        if (splits < 1) splits = 1;
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>(splits), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (splits > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = static_cast<unsigned>(splits);
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, a.e8m0,
+                              static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m),
+                              static_cast<int>(a.n), kblocks, groups, splits);
+}
+
+template <bool MX>
+cudaError_t launch_mx(const DecodeArgs &a, cudaStream_t stream) {
+    switch ((a.m + 7) / 8) {
+        case 1: return launch_t<1, MX>(a, stream);
+        case 2: return launch_t<2, MX>(a, stream);
+        case 3: return launch_t<3, MX>(a, stream);
+        case 4: return launch_t<4, MX>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, bool mx, cudaStream_t stream) {
+    return mx ? launch_mx<true>(a, stream) : launch_mx<false>(a, stream);
+}
+
+uint32_t take_decode_error() {
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_err, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+    const uint32_t zero = 0;
+    cudaMemcpyToSymbol(g_decode_err, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,259 @@
+// quantize.cu -- load-time requantization kernels.
+//
+//  * block_quantize_kernel: bf16 [n,k] -> e4m3 codes + one fp32 scale per
+//    128x128 tile (Atlas spark_model/weight_map/quantize_fp8_bs.rs: one CTA
+//    per tile, grid [k_blocks, n_blocks], 256 threads; FreeToken PR #636
+//    per_block_quant_fp8).  Each thread keeps its 64 elements in registers
+//    between the amax reduction and the encode, so the tile is read from HBM
+//    exactly once.
+//  * mx_quantize_kernel: bf16 [n,k] -> e4m3 codes + one e8m0 exponent per 32
+//    consecutive k of a row (FreeToken issue #624).  Four lanes own one
+//    32-element group (16 bytes each, fully coalesced), the group amax comes
+//    from two shuffles, and no fp32 copy of the weight is ever formed.
+//  * *_generic kernels: scalar versions of the same arithmetic for shapes or
+//    pointers the vector kernels cannot take (k % 8 != 0, unaligned w).
+//
+// The arithmetic is fixed by the definition: amax in fp32, s = amax / 448.f
+// and w / s as IEEE fp32 divisions (nvcc's default -prec-div=true, no
+// -ftz), cvt.rn.satfinite to e4m3.  MX scales are exact powers of two, so
+// w * 2^(127-E) is exact wherever it matters.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8bs {
+
+namespace {
+
+constexpr int kTile = 128;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Encode 8 bf16 values (one uint4) divided by s into 8 e4m3 bytes (uint2).
+__device__ __forceinline__ uint2 encode8_div(const uint4 v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint16_t c0 = f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h]) / s, bf16hi_to_f32(w[2 * h]) / s);
+        const uint16_t c1 =
+            f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h + 1]) / s, bf16hi_to_f32(w[2 * h + 1]) / s);
+        out[h] = static_cast<uint32_t>(c0) | (static_cast<uint32_t>(c1) << 16);
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ uint2 encode8_mul(const uint4 v, float f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint16_t c0 = f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h]) * f, bf16hi_to_f32(w[2 * h]) * f);
+        const uint16_t c1 =
+            f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h + 1]) * f, bf16hi_to_f32(w[2 * h + 1]) * f);
+        out[h] = static_cast<uint32_t>(c0) | (static_cast<uint32_t>(c1) << 16);
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ float absmax8(const uint4 v, float m) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(bf16lo_to_f32(w[i])));
+        m = fmaxf(m, fabsf(bf16hi_to_f32(w[i])));
+    }
+    return m;
+}
+
+// MX exponent from the group amax (a non-negative bf16 value held in fp32):
+// e = smallest integer with 448 * 2^e >= amax.  Writing amax = m * 2^p with
+// m in [1, 2): 448 * 2^(p-8) = 1.75 * 2^p >= amax iff m <= 1.75, so
+// e = p - 8 + (m > 1.75).  In the fp32 encoding p = field - 127 and
+// m > 1.75 iff the 23-bit mantissa exceeds 0x600000.  Subnormal amax gives
+// e + 127 < 0 and clamps to E = 0; amax = 0 gives E = 127 by definition.
+__device__ __forceinline__ int mx_exponent(float amax) {
+    if (amax == 0.0f) return 127;
+    const uint32_t u = __float_as_uint(amax);
+    const int field = static_cast<int>(u >> 23);
+    if (field == 0) return 0;
+    const int E = field - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return E < 0 ? 0 : (E > 254 ? 254 : E);
+}
+
+// 2^(127 - E) as an fp32 value, exact for E in [0, 254].
+__device__ __forceinline__ float mx_inv_scale(int E) {
+    const int t = 254 - E;  // biased exponent of 2^(127-E)
+    return t >= 1 ? __uint_as_float(static_cast<uint32_t>(t) << 23) : __uint_as_float(0x00400000u);
+}
+
+// ------------------------------------------------------------ block, fast
+__global__ void __launch_bounds__(256) block_quantize_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                             uint8_t *__restrict__ codes,
+                                                             float *__restrict__ scales,
+                                                             int64_t n, int64_t k) {
+    __shared__ float warp_amax[8];
+    const int bk = blockIdx.x, bn = blockIdx.y;
+    const int chunk = threadIdx.x & 15;  // 8 bf16 = 16 bytes
+    const int rg = threadIdx.x >> 4;     // rows rg, rg+16, ..., rg+112
+    const int64_t col = static_cast<int64_t>(bk) * kTile + chunk * 8;
+    const bool col_ok = col < k;  // k % 8 == 0: a chunk is all in or all out
+
+    uint4 v[8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = static_cast<int64_t>(bn) * kTile + rg + 16 * i;
+        if (col_ok && row < n)
+            v[i] = ld_nc_v4(w + row * k + col);
+        else
+            v[i] = make_uint4(0, 0, 0, 0);  // padding: |0| never raises amax
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = absmax8(v[i], amax);
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) warp_amax[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = warp_amax[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_amax[i]);
+    const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    if (threadIdx.x == 0) scales[static_cast<int64_t>(bn) * gridDim.x + bk] = s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = static_cast<int64_t>(bn) * kTile + rg + 16 * i;
+        if (col_ok && row < n) {
+            const uint2 c = encode8_div(v[i], s);
+            *reinterpret_cast<uint2 *>(codes + row * k + col) = c;
+        }
+    }
+}
+
+// --------------------------------------------------------- block, generic
+__global__ void __launch_bounds__(256) block_quantize_generic_kernel(
+    const __nv_bfloat16 *__restrict__ w, uint8_t *__restrict__ codes, float *__restrict__ scales,
+    int64_t n, int64_t k) {
+    __shared__ float warp_amax[8];
+    const int bk = blockIdx.x, bn = blockIdx.y;
+    const int64_t r0 = static_cast<int64_t>(bn) * kTile, c0 = static_cast<int64_t>(bk) * kTile;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(kTile), n - r0));
+    const int cols = static_cast<int>(min(static_cast<int64_t>(kTile), k - c0));
+    const uint16_t *wb = reinterpret_cast<const uint16_t *>(w);
+    float amax = 0.0f;
+    for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
+        const int r = e / cols, c = e % cols;
+        amax = fmaxf(amax, fabsf(__uint_as_float(static_cast<uint32_t>(wb[(r0 + r) * k + c0 + c]) << 16)));
+    }
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) warp_amax[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = warp_amax[0];
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_amax[i]);
+    const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    if (threadIdx.x == 0) scales[static_cast<int64_t>(bn) * gridDim.x + bk] = s;
+    for (int e = threadIdx.x; e < rows * cols; e += blockDim.x) {
+        const int r = e / cols, c = e % cols;
+        const float q = __uint_as_float(static_cast<uint32_t>(wb[(r0 + r) * k + c0 + c]) << 16) / s;
+        codes[(r0 + r) * k + c0 + c] = static_cast<uint8_t>(f32x2_to_e4m3x2(q, 0.0f) & 0xFF);
+    }
+}
+
+// --------------------------------------------------------------- MX, fast
+// Thread layout: each row of k bf16 is cut into 4*G chunks of 8 elements
+// (G = ceil(k/32) groups); chunks past k are padding.  A block of 256 threads
+// covers 4 consecutive 256-chunk slabs (ILP: four independent 16-byte loads in
+// flight per thread).  Lanes 4j..4j+3 hold one group.
+constexpr int kMxThreads = 256;
+constexpr int kMxUnroll = 4;
+
+__global__ void __launch_bounds__(kMxThreads) mx_quantize_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                 uint8_t *__restrict__ codes,
+                                                                 uint8_t *__restrict__ e8m0,
+                                                                 int64_t n, int64_t k,
+                                                                 int64_t groups) {
+    const int64_t chunks_per_row = groups * 4;
+    const int64_t total = n * chunks_per_row;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * (kMxThreads * kMxUnroll) + threadIdx.x;
+    uint4 v[kMxUnroll];
+    int64_t row[kMxUnroll], col[kMxUnroll];
+    bool ok[kMxUnroll];
+#pragma unroll
+    for (int u = 0; u < kMxUnroll; ++u) {
+        const int64_t q = base + u * kMxThreads;
+        const bool in = q < total;
+        row[u] = in ? q / chunks_per_row : 0;
+        col[u] = in ? (q - row[u] * chunks_per_row) * 8 : 0;
+        ok[u] = in && col[u] < k;
+        v[u] = ok[u] ? ld_nc_v4(w + row[u] * k + col[u]) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kMxUnroll; ++u) {
+        float amax = absmax8(v[u], 0.0f);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int E = mx_exponent(amax);
+        if (ok[u]) {
+            const uint2 c = encode8_mul(v[u], mx_inv_scale(E));
+            *reinterpret_cast<uint2 *>(codes + row[u] * k + col[u]) = c;
+            if ((threadIdx.x & 3) == 0) e8m0[row[u] * groups + col[u] / 32] = static_cast<uint8_t>(E);
+        }
+    }
+}
+
+// ------------------------------------------------------------ MX, generic
+__global__ void __launch_bounds__(256) mx_quantize_generic_kernel(
+    const __nv_bfloat16 *__restrict__ w, uint8_t *__restrict__ codes, uint8_t *__restrict__ e8m0,
+    int64_t n, int64_t k, int64_t groups) {
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (g >= n * groups) return;
+    const int64_t r = g / groups, c0 = (g - r * groups) * 32;
+    const int len = static_cast<int>(min(static_cast<int64_t>(32), k - c0));
+    const uint16_t *wb = reinterpret_cast<const uint16_t *>(w) + r * k + c0;
+    float amax = 0.0f;
+    for (int i = 0; i < len; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(static_cast<uint32_t>(wb[i]) << 16)));
+    const int E = mx_exponent(amax);
+    const float f = mx_inv_scale(E);
+    for (int i = 0; i < len; ++i) {
+        const float q = __uint_as_float(static_cast<uint32_t>(wb[i]) << 16) * f;
+        codes[r * k + c0 + i] = static_cast<uint8_t>(f32x2_to_e4m3x2(q, 0.0f) & 0xFF);
+    }
+    e8m0[g] = static_cast<uint8_t>(E);
+}
+
+}  // namespace
+
+cudaError_t launch_block_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
+                                  float *scales, bool vector_ok, cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>((k + kTile - 1) / kTile),
+                    static_cast<unsigned>((n + kTile - 1) / kTile));
+    if (vector_ok)
+        block_quantize_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), codes,
+                                                        scales, n, k);
+    else
+        block_quantize_generic_kernel<<<grid, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(w), codes, scales, n, k);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
+                               uint8_t *e8m0, bool vector_ok, cudaStream_t stream) {
+    const int64_t groups = (k + 31) / 32;
+    if (vector_ok) {
+        const int64_t total = n * groups * 4;
+        const int64_t per_block = kMxThreads * kMxUnroll;
+        const unsigned blocks = static_cast<unsigned>((total + per_block - 1) / per_block);
+        mx_quantize_kernel<<<blocks, kMxThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w),
+                                                               codes, e8m0, n, k, groups);
+    } else {
+        const int64_t total = n * groups;
+        const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
+        mx_quantize_generic_kernel<<<blocks, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(w), codes, e8m0, n, k, groups);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

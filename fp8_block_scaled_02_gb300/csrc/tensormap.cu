@@ -1,0 +1,61 @@
+// tensormap.cu -- TMA descriptor encoding and device queries.
+//
+// cuTensorMapEncodeTiled is a driver API entry point; it is fetched once
+// through the runtime (cudaGetDriverEntryPointByVersion) so the library
+// needs no link against libcuda.  Encoding is pure host work (no device
+// call, no synchronisation), so it is safe inside stream capture.
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+namespace fp8bs {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void resolve_encode() {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices] = {};
+
+}  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, resolve_encode);
+    if (!g_encode) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+    int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c == 0) {
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 1;
+        g_sm_count[dev].store(c, std::memory_order_relaxed);
+    }
+    return c;
+}
+
+}  // namespace fp8bs

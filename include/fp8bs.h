@@ -1,0 +1,180 @@
+/*
+ * fp8bs.h -- C ABI of libfp8bs: block-scaled FP8 (E4M3) and MXFP8 weight
+ * quantization and the W8A16 GEMV / skinny GEMM / prefill GEMM that consumes
+ * it, for NVIDIA GB300 (sm_103a).
+ *
+ * Common conventions
+ * ------------------
+ *  - Every pointer argument is a DEVICE pointer owned by the caller; the
+ *    library never allocates, frees or keeps a pointer after the call
+ *    returns ("The BF16 source is the caller's to free -- this does not take
+ *    ownership", Atlas spark_model/weight_map/quantize_fp8_bs.rs).
+ *  - Matrices are row-major with the last index contiguous:
+ *      weight w   bf16  [n, k]   (n = output features, k = input features)
+ *      codes      e4m3  [n, k]   one byte per weight
+ *      scales     fp32  [ceil(n/128), ceil(k/128)]   one per 128x128 tile
+ *      e8m0       uint8 [n, ceil(k/32)]              one per 32 k of a row
+ *      x          bf16  [m, k]
+ *      y          bf16  [m, n]
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *    only enqueues work on `stream` and returns: no host synchronisation, no
+ *    allocation, and the kernel choice depends on shapes only, never on
+ *    values, so a sequence of calls can be captured into a CUDA graph.
+ *  - Arguments are validated before anything is enqueued; on a negative
+ *    status nothing was launched.  Launch failures report FP8BS_ERR_CUDA.
+ *  - Inputs must be finite (no NaN or Inf); results for non-finite inputs
+ *    are unspecified.
+ *  - Results are deterministic: for a given shape the reduction order is
+ *    fixed.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_NULL = -1,    /* a required pointer is NULL                     */
+    FP8BS_ERR_SHAPE = -2,   /* n, k or m out of range                         */
+    FP8BS_ERR_BLOCK = -3,   /* block size other than 128                      */
+    FP8BS_ERR_ALIGN = -4,   /* pointer not aligned to its element size        */
+    FP8BS_ERR_CUDA = -5,    /* a CUDA runtime/driver call or launch failed    */
+    FP8BS_ERR_DEVICE = -6,  /* a kernel gave up a bounded wait (see below)    */
+    FP8BS_ERR_PATH = -7     /* the requested kernel path cannot take the call */
+} fp8bs_status;
+
+/* Kernel paths for the *_ex entry points. */
+typedef enum {
+    FP8BS_PATH_AUTO = 0,     /* choose by shape (what fp8bs_gemv does)         */
+    FP8BS_PATH_DECODE = 1,   /* TMA-staged skinny kernel, m <= 32 per launch
+                                (larger m runs in chunks of 32 rows)          */
+    FP8BS_PATH_PREFILL = 2,  /* tcgen05 tensor-core kernel, block-FP8 only     */
+    FP8BS_PATH_GENERIC = 3   /* plain-load kernel for any shape / alignment    */
+} fp8bs_path;
+
+/*
+ * fp8bs_quantize -- load-time requantization of a bf16 [n, k] weight to FP8
+ * E4M3 codes with one fp32 scale per 128x128 tile.
+ *
+ * Defined by: Atlas spark_model/weight_map/quantize_fp8_bs.rs
+ * (quantize_to_fp8_blockscaled: [n, k] bf16 in, one byte per weight, one f32
+ * per [128,128] tile laid out [n_blocks, k_blocks], n > 0 && k > 0 required,
+ * launch grid [k_blocks, n_blocks]); FreeToken PR #636 "opt-in fp8-block QAT
+ * for the lm_head" (How it works: quantize to fp8 with a 128-block scale
+ * after load); FreeToken issue #624 (amax/448).
+ *
+ * For each tile (bn, bk), over the tile's real elements only (edge tiles may
+ * be partial): amax = max|w|, s = amax / 448 as an IEEE fp32 division, s = 1
+ * when amax = 0; codes[r, c] = e4m3(w[r, c] / s) with the quotient an IEEE
+ * fp32 division, rounded to nearest-even and saturated to +-448.
+ *
+ *   w_bf16      device, n*k bf16, 2-byte aligned
+ *   n, k        > 0 (else FP8BS_ERR_SHAPE)
+ *   block       must be 128, the tile edge the consumers hard-code
+ *               (else FP8BS_ERR_BLOCK)
+ *   codes_u8    device, n*k bytes, written
+ *   scales_f32  device, ceil(n/128)*ceil(k/128) floats, 4-byte aligned
+ *   stream      cudaStream_t
+ * Any alignment is accepted; 16-byte-aligned w with k % 8 == 0 takes the
+ * vectorised kernel, everything else a scalar kernel with identical results.
+ */
+int fp8bs_quantize(const void *w_bf16, int64_t n, int64_t k, int block,
+                   uint8_t *codes_u8, float *scales_f32, void *stream);
+
+/*
+ * fp8bs_gemv -- decode-time W8A16 block-FP8 linear:
+ *   y[i, j] = bf16_rn( sum_kb s[j/128, kb] * sum_{c in kb} x[i, c] * dec(q[j, c]) )
+ * with fp32 accumulation.  dec(q) is exact in bf16; the scale multiplies the
+ * fp32 partial sum of each 128-wide K block (it is never folded into a
+ * rounded bf16 weight).
+ *
+ * Defined by: InfiniLM PR #586 (Summary: 128x128 block-FP8 W8A16 weights run
+ * without materialising bf16 weights; decode routing by M); FreeToken PR #389
+ * (the decode GEMV micro-benchmark over M = 1/8/16, and testing the op
+ * against a linear on the dequantized weight); FreeToken PR #636 (the fp8
+ * lm_head served by the block-FP8 GEMV).
+ *
+ *   x_bf16   device, m*k bf16, 2-byte aligned
+ *   m        >= 0; m == 0 is a no-op returning FP8BS_OK
+ *   codes    device, n*k bytes from fp8bs_quantize
+ *   scales   device, fp32 [ceil(n/128), ceil(k/128)], 4-byte aligned
+ *   n, k     > 0
+ *   y_bf16   device, m*n bf16, written (must not overlap the inputs)
+ * Shape-only dispatch (FP8BS_PATH_AUTO): m <= 32 -> decode kernel; larger m
+ * -> tcgen05 prefill kernel; k % 16 != 0 or unaligned (non-16-byte) x/codes
+ * -> generic kernel.
+ */
+int fp8bs_gemv(const void *x_bf16, int64_t m, const uint8_t *codes,
+               const float *scales, int64_t n, int64_t k, void *y_bf16,
+               void *stream);
+
+/* fp8bs_gemv with an explicit kernel path (fp8bs_path).  A path that cannot
+ * take the call (e.g. DECODE with k % 16 != 0) returns FP8BS_ERR_PATH. */
+int fp8bs_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
+                  const float *scales, int64_t n, int64_t k, void *y_bf16,
+                  int path, void *stream);
+
+/*
+ * mxfp8_quantize -- load-time MXFP8 requantization: per row, per group of 32
+ * consecutive k (the last group may be shorter), e = the smallest integer with
+ * 448 * 2^e >= amax (i.e. 2^ceil(log2(amax/448))), E = clamp(e + 127, 0, 254)
+ * (E = 127 when amax = 0), codes = e4m3(w * 2^(127 - E)) rounded to
+ * nearest-even and saturated.
+ *
+ * Defined by: FreeToken issue #624 "Load-time MXFP8 requantization"
+ * (Proposed solution: e4m3 codes with one e8m0 scale per 32 elements, ceil-log2
+ * of amax/448, served by a W8A16 path).  This kernel streams bf16 straight to
+ * codes; it needs no fp32 staging buffer.
+ *
+ *   w_bf16       device, n*k bf16, 2-byte aligned
+ *   n, k         > 0
+ *   codes_u8     device, n*k bytes, written
+ *   scales_e8m0  device, n*ceil(k/32) bytes, written
+ */
+int mxfp8_quantize(const void *w_bf16, int64_t n, int64_t k,
+                   uint8_t *codes_u8, uint8_t *scales_e8m0, void *stream);
+
+/*
+ * mxfp8_gemv -- W8A16 linear over MXFP8 weights:
+ *   y[i, j] = bf16_rn( sum_g 2^(E[j,g]-127) * sum_{c in g} x[i, c] * dec(q[j, c]) )
+ * Same argument rules as fp8bs_gemv, with scales_e8m0 [n, ceil(k/32)].
+ * Defined by: FreeToken issue #624 (the "mxfp8_linear W8A16 path").
+ * m > 32 runs the decode kernel in chunks of 32 rows.
+ */
+int mxfp8_gemv(const void *x_bf16, int64_t m, const uint8_t *codes,
+               const uint8_t *scales_e8m0, int64_t n, int64_t k, void *y_bf16,
+               void *stream);
+
+/* mxfp8_gemv with an explicit path (AUTO, DECODE or GENERIC). */
+int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
+                  const uint8_t *scales_e8m0, int64_t n, int64_t k,
+                  void *y_bf16, int path, void *stream);
+
+/* Path FP8BS_PATH_AUTO would take for these shapes and pointers
+ * (host-only, launches nothing).  `mx` selects the MXFP8 GEMV. */
+int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16,
+                      const void *codes, int mx);
+
+/* Human-readable text for a status code (static storage). */
+const char *fp8bs_strerror(int status);
+
+/*
+ * Debug query: every wait inside the pipelined kernels is bounded; a kernel
+ * that gives up sets a device-side error word instead of hanging.  This
+ * synchronises `stream`, copies the word to *word_out (may be NULL), clears
+ * it, and returns FP8BS_ERR_DEVICE if it was non-zero, else FP8BS_OK (or
+ * FP8BS_ERR_CUDA if the synchronisation itself failed).
+ */
+int fp8bs_check_device_error(void *stream, uint32_t *word_out);
+
+/* ABI version (major * 100 + minor). */
+int fp8bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8BS_H */

@@ -53,6 +53,20 @@ double oracle_e4m3_decode(uint8_t code)
  * below 2^-10 the nearest value is 0, whose distance |v| is exact, and every
  * other distance exceeds 2^-10 by far more than its rounding error.
  */
+/* the 127 non-negative finite magnitudes, decoded once */
+static double g_mag[0x7F];
+static int g_mag_ready;
+
+static void init_magnitudes(void)
+{
+    int c;
+    if (g_mag_ready)
+        return;
+    for (c = 0; c < 0x7F; ++c)
+        g_mag[c] = oracle_e4m3_decode((uint8_t)c);
+    g_mag_ready = 1;
+}
+
 uint8_t oracle_e4m3_encode(double v)
 {
     int neg = signbit(v) ? 1 : 0;
@@ -63,9 +77,10 @@ uint8_t oracle_e4m3_encode(double v)
     assert(!isnan(v) && !isinf(v));
     if (a >= E4M3_MAX)
         return (uint8_t)(0x7E | (neg << 7));
+    init_magnitudes();
     bestd = a; /* distance to code 0x00 (= 0.0) */
     for (c = 1; c <= 0x7E; ++c) {
-        double d = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        double d = fabs(g_mag[c] - a);
         if (d < bestd || (d == bestd && (c & 1) == 0)) {
             best = c;
             bestd = d;

@@ -1,0 +1,103 @@
+"""The C ABI library builds, loads and exports every entry point declared in
+include/fp8bs.h; argument validation and path selection work without a GPU
+(these calls return before any CUDA call)."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8bs.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp8_block_scaled_02_gb300 import build
+    build.build()
+    import fp8_block_scaled_02_gb300 as pkg
+    return pkg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
+                 "mxfp8_gemv_ex", "fp8bs_select_path", "fp8bs_strerror", "fp8bs_check_device_error",
+                 "fp8bs_version"):
+        assert want in names, names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    from fp8_block_scaled_02_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(declared_functions()) <= exported
+
+
+def test_version_and_strerror(L):
+    assert L.fp8bs_version() == 100
+    import fp8_block_scaled_02_gb300 as pkg
+    for st in range(-7, 1):
+        assert pkg.strerror(st) and pkg.strerror(st) != "unknown status"
+    assert pkg.strerror(-99) == "unknown status"
+
+
+P = ctypes.c_void_p
+
+
+def test_quantize_validation(L):
+    w, c, s = P(0x10000), P(0x20000), P(0x30000)
+    assert L.fp8bs_quantize(w, 0, 10, 128, c, s, None) == -2
+    assert L.fp8bs_quantize(w, 10, -1, 128, c, s, None) == -2
+    assert L.fp8bs_quantize(w, 10, 10, 64, c, s, None) == -3
+    assert L.fp8bs_quantize(None, 10, 10, 128, c, s, None) == -1
+    assert L.fp8bs_quantize(w, 10, 10, 128, None, s, None) == -1
+    assert L.fp8bs_quantize(w, 10, 10, 128, c, None, None) == -1
+    assert L.fp8bs_quantize(P(0x10001), 10, 10, 128, c, s, None) == -4
+    assert L.fp8bs_quantize(w, 10, 10, 128, c, P(0x30002), None) == -4
+    assert L.mxfp8_quantize(w, 0, 10, c, s, None) == -2
+    assert L.mxfp8_quantize(w, 10, 10, None, s, None) == -1
+    assert L.mxfp8_quantize(P(0x10001), 10, 10, c, s, None) == -4
+
+
+def test_gemv_validation(L):
+    x, c, s, y = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    assert L.fp8bs_gemv(x, -1, c, s, 10, 10, y, None) == -2
+    assert L.fp8bs_gemv(x, 1, c, s, 0, 10, y, None) == -2
+    assert L.fp8bs_gemv(x, 1, c, s, 10, 0, y, None) == -2
+    assert L.fp8bs_gemv(x, 1, c, s, 1 << 31, 10, y, None) == -2
+    assert L.fp8bs_gemv(None, 0, None, None, 10, 10, None, None) == 0   # m == 0: no-op
+    assert L.fp8bs_gemv(None, 1, c, s, 10, 10, y, None) == -1
+    assert L.fp8bs_gemv(x, 1, c, s, 10, 10, None, None) == -1
+    assert L.fp8bs_gemv(P(0x10001), 1, c, s, 10, 10, y, None) == -4
+    assert L.fp8bs_gemv(x, 1, c, P(0x30002), 10, 10, y, None) == -4
+    assert L.fp8bs_gemv_ex(x, 1, c, s, 10, 10, y, 9, None) == -7
+    # an explicit path that cannot take the shape is refused before launch
+    assert L.fp8bs_gemv_ex(x, 1, c, s, 10, 10, y, 1, None) == -7    # decode needs k % 16 == 0
+    assert L.fp8bs_gemv_ex(x, 1, P(0x20001), s, 10, 32, y, 1, None) == -7  # decode needs aligned codes
+    assert L.mxfp8_gemv_ex(x, 1, c, s, 10, 32, y, 2, None) == -7    # no MX prefill path
+    assert L.mxfp8_gemv(x, 1, c, None, 10, 32, y, None) == -1
+
+
+def test_select_path(L):
+    a16, c16 = P(0x10000), P(0x20000)
+    assert L.fp8bs_select_path(1, 100, 4096, a16, c16, 0) == 1          # decode
+    assert L.fp8bs_select_path(32, 100, 4096, a16, c16, 0) == 1
+    assert L.fp8bs_select_path(33, 100, 4096, a16, c16, 0) == 2         # prefill
+    assert L.fp8bs_select_path(4096, 100, 4096, a16, c16, 1) == 1       # MX: decode in chunks
+    assert L.fp8bs_select_path(1, 100, 4100, a16, c16, 0) == 3          # k % 16 != 0 -> generic
+    assert L.fp8bs_select_path(1, 100, 4096, P(0x10008), c16, 0) == 3   # x not 16-byte aligned
+    assert L.fp8bs_select_path(0, 100, 4096, a16, c16, 0) == -2

@@ -1,0 +1,200 @@
+"""GPU parity: the W8A16 GEMV / skinny GEMM vs the CPU oracle's fp64 result.
+
+The GEMV's inputs (codes, scales, x) on every checked output come from the
+seeded generators and the oracle's own quantizer, never from the CUDA path.
+Exact checks: every e4m3 code decodes exactly (one-hot x), one-hot columns
+of ragged tiles give bf16(fl32(dec * s)), x = 0 gives 0.  Everything else is
+held to the tolerance in oracle/tolerance.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_02_gb300 import PATH_DECODE, PATH_GENERIC, PATH_PREFILL, inputs
+
+from gpu_helpers import (bits, check_block_gemv, check_mx_gemv, guard_intact, guarded_empty, install_block_rows,
+                         lib_or_skip, oracle_block_rows, table)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    return lib_or_skip()
+
+
+def to_dev_bits(a: np.ndarray, dtype=torch.uint8):
+    return torch.from_numpy(a).to(DEV)
+
+
+def bf16_dev(a_bits: np.ndarray):
+    return torch.from_numpy(a_bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+# ------------------------------------------------------------ exact checks
+@pytest.mark.parametrize("path", [PATH_DECODE, PATH_GENERIC])
+@pytest.mark.parametrize("m", [1, 5, 8, 9, 16, 17, 32])
+def test_every_code_decodes_exactly(pkg, path, m):
+    """Row i of W holds code i at column 3 (scales 1); x = e_3, so
+    y[:, i] = bf16(dec(i)) exactly for every finite code."""
+    codes_list = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    n, k = len(codes_list), 32
+    w = np.zeros((n, k), dtype=np.uint8)
+    w[:, 3] = codes_list
+    scales = np.ones((-(-n // 128), 1), dtype=np.float32)
+    x = np.zeros((m, k), dtype=np.uint16)
+    x[:, 3] = 0x3F80
+    y = pkg.gemv(bf16_dev(x), to_dev_bits(w), torch.from_numpy(scales).to(DEV), path=path)
+    torch.cuda.synchronize()
+    want = np.array([oracle.double_to_bf16(v) for v in table()[codes_list]], dtype=np.uint16)
+    got = bits(y.cpu())
+    for i in range(m):
+        assert np.array_equal(got[i], want), np.argwhere(got[i] != want)[:5]
+
+
+@pytest.mark.parametrize("path", [PATH_DECODE, PATH_GENERIC])
+def test_one_hot_columns_on_ragged_tiles(pkg, path):
+    w = inputs.tiny_ragged_weight(0)
+    n, k = w.shape
+    oc, os_ = oracle.block_quantize(bits(w))
+    codes, scales = to_dev_bits(oc), torch.from_numpy(os_).to(DEV)
+    cols = [0, 1, 127, 128, 300, 640, 703]
+    x = np.zeros((len(cols), k), dtype=np.uint16)
+    for i, c in enumerate(cols):
+        x[i, c] = 0x3F80
+    y = bits(pkg.gemv(bf16_dev(x), codes, scales, path=path).cpu())
+    for i, c in enumerate(cols):
+        prod = (table()[oc[:, c]].astype(np.float32) * os_[np.arange(n) // 128, c // 128]).astype(np.float32)
+        want = np.array([oracle.double_to_bf16(float(v)) for v in prod], dtype=np.uint16)
+        assert np.array_equal(y[i], want), (c, np.argwhere(y[i] != want)[:5])
+
+
+def test_zero_input_gives_zero(pkg):
+    w = inputs.gaussian_bf16((256, 512), 0.02, 3)
+    oc, os_ = oracle.block_quantize(bits(w))
+    for path in (PATH_DECODE, PATH_GENERIC):
+        y = pkg.gemv(torch.zeros((4, 512), dtype=torch.bfloat16, device=DEV), to_dev_bits(oc),
+                     torch.from_numpy(os_).to(DEV), path=path)
+        assert int((y.view(torch.int16) & 0x7FFF).abs().sum()) == 0
+
+
+# ----------------------------------------------------------- small, full
+def full_block_case(pkg, w, m, path, seed=7):
+    n, k = w.shape
+    oc, os_ = oracle.block_quantize(bits(w))
+    x = inputs.activations(m, k, seed)
+    y, raw = guarded_empty((m, n), torch.bfloat16, DEV)
+    pkg.gemv(x.to(DEV), to_dev_bits(oc), torch.from_numpy(os_).to(DEV), y=y, path=path)
+    torch.cuda.synchronize()
+    assert guard_intact(raw, m * n * 2)
+    rows_q = {rb: (oc[rb * 128:rb * 128 + 128], os_[rb]) for rb in range(-(-n // 128))}
+    return check_block_gemv(y, bits(x), rows_q)
+
+
+@pytest.mark.parametrize("path", [PATH_DECODE, PATH_GENERIC, PATH_PREFILL])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 7, 8, 9, 15, 16, 24, 31, 32, 33, 40, 64, 100])
+def test_tiny_ragged_all_m(pkg, m, path):
+    full_block_case(pkg, inputs.tiny_ragged_weight(0), m, path)
+
+
+SHAPES = [(1, 16), (1, 1), (5, 300), (37, 48), (128, 128), (129, 272), (300, 7), (513, 1024), (64, 4096)]
+
+
+@pytest.mark.parametrize("n,k", SHAPES)
+@pytest.mark.parametrize("m", [1, 8, 19, 32])
+def test_small_shapes(pkg, n, k, m):
+    full_block_case(pkg, inputs.gaussian_bf16((n, k), 0.02, n * 31 + k), m, 0)
+
+
+@pytest.mark.parametrize("n,k", [(37, 48), (300, 7), (129, 272), (5, 1)])
+@pytest.mark.parametrize("m", [1, 8, 33])
+def test_small_shapes_mx(pkg, n, k, m):
+    w = inputs.heavy_tail_weight(3, shape=(n, k), frac=0.01)
+    oc, oe = oracle.mx_quantize(bits(w))
+    x = inputs.activations(m, k, 5)
+    for path in (0, PATH_GENERIC) if k % 16 else (0, PATH_DECODE, PATH_GENERIC):
+        y = pkg.mx_gemv(x.to(DEV), to_dev_bits(oc), to_dev_bits(oe), path=path)
+        check_mx_gemv(y, bits(x), np.arange(n), oc, oe)
+
+
+# ------------------------------------------------------ full-size, sampled
+def sampled_block_case(pkg, w_dev, ms, row_blocks, seed=11, path=0, x_rows=None):
+    n, k = w_dev.shape
+    codes, scales = pkg.quantize(w_dev)
+    w_bits = None
+    rows_q = {}
+    for rb in row_blocks:
+        sub = bits(w_dev[rb * 128:rb * 128 + 128].cpu())
+        c, s = oracle.block_quantize(sub)
+        rows_q[int(rb)] = (c, s[0])
+    del w_bits
+    install_block_rows(codes, scales, rows_q)
+    stats = []
+    for m in ms:
+        x = inputs.activations(m, k, seed + m, device=DEV)
+        y = pkg.gemv(x, codes, scales, path=path)
+        torch.cuda.synchronize()
+        xr = None if x_rows is None else x_rows(m)
+        stats.append(check_block_gemv(y, bits(x.cpu()), rows_q, m_rows=xr))
+    return stats
+
+
+def _row_blocks(n, count, seed):
+    nb = -(-n // 128)
+    rng = np.random.default_rng(seed)
+    return sorted(set([0, nb - 1] + list(rng.integers(0, nb, count))))
+
+
+def test_lm_head_full_size(pkg):
+    w = inputs.lm_head_weight(2, device=DEV)
+    sampled_block_case(pkg, w, [1, 4, 8, 16], _row_blocks(w.shape[0], 4, 1))
+
+
+@pytest.mark.parametrize("j", range(4))
+def test_rotation_shapes(pkg, j):
+    w = inputs.rotation_weight(0, j, device=DEV)
+    sampled_block_case(pkg, w, [1, 8, 16, 32], _row_blocks(w.shape[0], 3, j))
+
+
+def test_sweep_shape_all_m(pkg):
+    w = inputs.sweep_weight(0, device=DEV)
+    sampled_block_case(pkg, w, list(range(1, 33)), _row_blocks(w.shape[0], 2, 5))
+
+
+def test_prefill_shapes_sampled(pkg):
+    w = inputs.sweep_weight(0, device=DEV)
+    rng = np.random.default_rng(9)
+    sampled_block_case(pkg, w, [64, 512], _row_blocks(w.shape[0], 1, 6),
+                       x_rows=lambda m: np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, 14)])))
+
+
+def test_mx_full_size(pkg):
+    w = inputs.heavy_tail_weight(5, device=DEV)
+    n, k = w.shape
+    codes, e8m0 = pkg.mx_quantize(w)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 254)]))
+    oc, oe = oracle.mx_quantize(bits(w[torch.from_numpy(rows).to(DEV)].cpu()))
+    ridx = torch.from_numpy(rows).to(DEV)
+    codes[ridx] = to_dev_bits(oc)
+    e8m0[ridx] = to_dev_bits(oe)
+    for m in (1, 8, 16):
+        x = inputs.activations(m, k, 40 + m, device=DEV)
+        y = pkg.mx_gemv(x, codes, e8m0)
+        torch.cuda.synchronize()
+        check_mx_gemv(y, bits(x.cpu()), rows, oc, oe)
+
+
+def test_repeat_is_deterministic(pkg):
+    w = inputs.rotation_weight(1, 1, device=DEV)
+    codes, scales = pkg.quantize(w)
+    x = inputs.activations(16, w.shape[1], 3, device=DEV)
+    y1 = pkg.gemv(x, codes, scales)
+    y2 = pkg.gemv(x, codes, scales)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_no_device_error(pkg):
+    assert pkg.check_device_error() == 0
