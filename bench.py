@@ -1,0 +1,471 @@
+"""Benchmark of the block-FP8 W8A16 decode GEMV on GB300.
+
+Default workload (one "step"): the lm_head weight [152064, 4096] quantized to
+128x128 block FP8 at load time, then one GEMV call at each of M = 1, 4, 8, 16
+(bf16 x, bf16 logits out).  The weight (623 MB of codes) is larger than L2,
+so every call streams it from HBM.  Metric: algorithmic HBM bytes
+(codes + scales + x + y) per second over the step, in GB/s; per-M us/call,
+GB/s and fraction of HBM bandwidth are reported alongside.
+
+Other workloads (--workload): rotation (48 layers x 4 projection weights,
+192 GEMVs per step, CUDA-graph captured), sweep ([12288, 4096], M = 1..32
+over 8 rotated copies), mx ([18432, 7168] MXFP8 GEMV, M = 1, 8, 16 over 4
+copies), quantize ([18432, 7168] block + MXFP8 load-time quantization).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload lm_head|rotation|sweep|mx|quantize] [--m M]
+
+N > 1 runs one independent replica per GPU (the path needs no collective);
+the reported value is the aggregate over ranks of bytes moved divided by the
+slowest rank's time.  --impl reference times the CPU oracle (plain C, one
+host core) on a bounded sample of the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HBM_NOMINAL_GBS = 8000.0
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def gemv_bytes(m, n, k, mx=False):
+    scales = n * ((k + 31) // 32) if mx else 4 * ((n + 127) // 128) * ((k + 127) // 128)
+    return n * k + scales + 2 * m * k + 2 * m * n
+
+
+# ----------------------------------------------------------- clocks sampler
+class Clocks:
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0],
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 9:
+                try:
+                    rows.append((float(p[1]), float(p[2]), p[5:9]))
+                except ValueError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ ranks
+def dist_setup(n_gpus):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, v):
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, v):
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- workloads
+def lm_head_workload(torch, fp8bs, inputs, dev):
+    ms = [1, 4, 8, 16]
+    w = inputs.lm_head_weight(2, device=dev)
+    n, k = w.shape
+    codes, scales = fp8bs.quantize(w)
+    del w
+    xs = {m: inputs.activations(m, k, 100 + m, device=dev) for m in ms}
+    ys = {m: torch.empty((m, n), dtype=torch.bfloat16, device=dev) for m in ms}
+    calls = [(f"M={m}", m, gemv_bytes(m, n, k), (lambda m=m: fp8bs.gemv(xs[m], codes, scales, y=ys[m])))
+             for m in ms]
+    cfg = {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call at each "
+                       "of M=1,4,8,16 per step", "n": n, "k": k, "ms": ms,
+           "l2": "inputs larger than L2 (623 MB of codes per call)"}
+    return dict(calls=calls, xs=xs, ys=ys, cfg=cfg, dominant=("decode_kernel<1,false>", [0, 1, 2]),
+                codes=codes, scales=scales, n=n, k=k, mx=False)
+
+
+def rotation_workload(torch, fp8bs, inputs, dev, m):
+    layers = inputs.ROTATION_LAYERS
+    weights = []
+    for l in range(layers):
+        for j in range(4):
+            w = inputs.rotation_weight(l, j, device=dev)
+            weights.append(fp8bs.quantize(w))
+            del w
+    shapes = [inputs.ROTATION_SHAPES[j] for _ in range(layers) for j in range(4)]
+    xs = [inputs.activations(m, k, 7 + i, device=dev) for i, (n, k) in enumerate(shapes)]
+    ys = [torch.empty((m, n), dtype=torch.bfloat16, device=dev) for (n, k) in shapes]
+
+    def step():
+        for i, (c, s) in enumerate(weights):
+            fp8bs.gemv(xs[i], c, s, y=ys[i])
+    total = sum(gemv_bytes(m, n, k) for (n, k) in shapes)
+    cfg = {"workload": f"decode dense-projection rotation: 48 layers x 4 block-FP8 weights "
+                       f"([8192,2560],[2560,3072],[6656,2560],[2560,3072]), M={m}, 192 GEMVs per step "
+                       "(CUDA graph)", "ms": [m], "l2": "inputs larger than L2 (2.58 GB of codes per step)"}
+    return dict(calls=[(f"rotation M={m}", m, total, step)], cfg=cfg, graph=True, launches_per_step=192,
+                dominant=("decode_kernel", [0]))
+
+
+def sweep_workload(torch, fp8bs, inputs, dev, ms):
+    copies = [fp8bs.quantize(inputs.sweep_weight(c, device=dev)) for c in range(8)]
+    n, k = inputs.SWEEP_SHAPE
+    calls = []
+    for m in ms:
+        x = inputs.activations(m, k, 300 + m, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+        def fn(x=x, y=y):
+            for c, s in copies:
+                fp8bs.gemv(x, c, s, y=y)
+        calls.append((f"M={m}", m, 8 * gemv_bytes(m, n, k), fn))
+    cfg = {"workload": "M sweep: block-FP8 [12288,4096], one GEMV per M over 8 rotated weight copies (403 MB)",
+           "n": n, "k": k, "ms": ms, "l2": "inputs larger than L2 (8 rotated copies)"}
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel", list(range(len(ms)))), launches_per_call=8)
+
+
+def mx_workload(torch, fp8bs, inputs, dev):
+    ms = [1, 8, 16]
+    copies = []
+    for c in range(4):
+        w = inputs.heavy_tail_weight(5 + c, device=dev)
+        copies.append(fp8bs.mx_quantize(w))
+        del w
+    n, k = inputs.MX_SHAPE
+    calls = []
+    for m in ms:
+        x = inputs.activations(m, k, 500 + m, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+        def fn(x=x, y=y):
+            for c, e in copies:
+                fp8bs.mx_gemv(x, c, e, y=y)
+        calls.append((f"M={m}", m, 4 * gemv_bytes(m, n, k, mx=True), fn))
+    cfg = {"workload": "MXFP8 [18432,7168] (e8m0 per 32 K) W8A16 GEMV, M=1,8,16, 4 rotated copies",
+           "n": n, "k": k, "ms": ms, "l2": "inputs larger than L2 (4 rotated copies, 528 MB)"}
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,true>", [0, 1]), launches_per_call=4)
+
+
+def quantize_workload(torch, fp8bs, inputs, dev):
+    w = inputs.heavy_tail_weight(5, device=dev)
+    n, k = w.shape
+    codes = torch.empty((n, k), dtype=torch.uint8, device=dev)
+    scales = torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=torch.float32, device=dev)
+    e8m0 = torch.empty((n, (k + 31) // 32), dtype=torch.uint8, device=dev)
+    bq = 3 * n * k + 4 * scales.numel()
+    mq = 3 * n * k + e8m0.numel()
+    calls = [("block quantize", 0, bq, lambda: fp8bs.quantize(w, codes=codes, scales=scales)),
+             ("mx quantize", 0, mq, lambda: fp8bs.mx_quantize(w, codes=codes, e8m0=e8m0))]
+    cfg = {"workload": "load-time quantize of bf16 [18432,7168] (0.1% Student-t entries) to block FP8 and "
+                       "MXFP8", "n": n, "k": k, "l2": "inputs larger than L2 (264 MB bf16 read per call)"}
+    return dict(calls=calls, cfg=cfg, dominant=("block_quantize_kernel", [0]))
+
+
+# ------------------------------------------------------------------ timing
+def time_calls(torch, calls, steps, warmup, pg, graph=False):
+    """Run `warmup` untimed steps, then `steps` timed ones.  Each call is
+    bracketed by CUDA events on the current stream; returns per-call mean
+    ms and the whole timed region in ms."""
+    stream = torch.cuda.current_stream()
+    run = [fn for _, _, _, fn in calls]
+    if graph:
+        g = []
+        s = torch.cuda.Stream()
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            for fn in run:
+                fn()
+        stream.wait_stream(s)
+        torch.cuda.synchronize()
+        for fn in run:
+            cg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(cg):
+                fn()
+            g.append(cg)
+        run = [cg.replay for cg in g]
+    for _ in range(warmup):
+        for fn in run:
+            fn()
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in run]
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(steps):
+        for i, fn in enumerate(run):
+            ev[s][i][0].record(stream)
+            fn()
+            ev[s][i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    total = t0.elapsed_time(t1)
+    per = [statistics.fmean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)) for i in range(len(run))]
+    return per, total
+
+
+def e2e_lm_head(torch, fp8bs, wl, steps, warmup, pg):
+    """Same step through the public API with host buffers: every step copies
+    each x from pinned host memory and reads each y back into pinned host
+    memory, inside the timed region."""
+    stream = torch.cuda.current_stream()
+    ms = wl["cfg"]["ms"]
+    hx = {m: wl["xs"][m].cpu().pin_memory() for m in ms}
+    hy = {m: torch.empty(tuple(wl["ys"][m].shape), dtype=torch.bfloat16).pin_memory() for m in ms}
+    dx = {m: torch.empty_like(wl["xs"][m]) for m in ms}
+
+    def step():
+        for m in ms:
+            dx[m].copy_(hx[m], non_blocking=True)
+            fp8bs.gemv(dx[m], wl["codes"], wl["scales"], y=wl["ys"][m])
+            hy[m].copy_(wl["ys"][m], non_blocking=True)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    h2d = sum(hx[m].numel() * 2 for m in ms)
+    d2h = sum(hy[m].numel() * 2 for m in ms)
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(rows=4096, ms=(1, 4, 8, 16)):
+    """Time the plain-C oracle (one host thread, as it stands) on a bounded
+    sample of the lm_head workload: `rows` weight rows, the same M sweep.
+    Returns (GB/s in the metric's units, seconds, description)."""
+    import numpy as np
+
+    import oracle
+    from fp8_block_scaled_02_gb300 import inputs
+    w = inputs.lm_head_weight(2, shape=(rows, 4096))
+    wb = inputs.bf16_bits(w)
+    t = time.perf_counter()
+    codes, scales = oracle.block_quantize(wb)
+    tq = time.perf_counter() - t
+    total_bytes, total_s = 0, 0.0
+    for m in ms:
+        xb = inputs.bf16_bits(inputs.activations(m, 4096, 100 + m))
+        t = time.perf_counter()
+        oracle.block_gemv(xb, codes, scales)
+        total_s += time.perf_counter() - t
+        total_bytes += gemv_bytes(m, rows, 4096)
+    _ = np.zeros(1)
+    desc = (f"oracle block_gemv (plain C, fp64, 1 thread) over {rows} of the 152064 lm_head rows, "
+            f"K=4096, one call at each of M={list(ms)}; its quantize of that sample took {tq:.2f} s")
+    return total_bytes / total_s / 1e9, total_s, desc
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+# -------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="lm_head", choices=["lm_head", "rotation", "sweep", "mx", "quantize"])
+    ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-file", default=os.path.join(ROOT, "gpurun_out", "bench_clocks.csv"))
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    peak, peak_kind = measured_peaks()
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        # each step is a bounded sample: about 24 s of oracle work in total
+        rows = 128 * max(1, round(32 * min(1.0, 24.0 / max(1, args.steps))))
+        for _ in range(warmup):
+            oracle_sample(rows=128)
+        per_step = []
+        desc = ""
+        for _ in range(args.steps):
+            v, s, desc = oracle_sample(rows=rows)
+            per_step.append((v, s))
+        value = statistics.fmean(v for v, _ in per_step)
+        ms_step = 1e3 * statistics.fmean(s for _, s in per_step)
+        line = {"impl": "reference", "metric": "block-FP8 W8A16 GEMV HBM-equivalent GB/s (lm_head, M=1,4,8,16)",
+                "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": len(per_step),
+                "warmup": warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call "
+                                       "at each of M=1,4,8,16 per step", "n": 152064, "k": 4096,
+                           "ms": [1, 4, 8, 16], "sample_rows_per_step": rows},
+                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import fp8_block_scaled_02_gb300 as fp8bs
+    from fp8_block_scaled_02_gb300 import inputs
+    fp8bs.lib()
+
+    if args.workload == "lm_head":
+        wl = lm_head_workload(torch, fp8bs, inputs, dev)
+    elif args.workload == "rotation":
+        wl = rotation_workload(torch, fp8bs, inputs, dev, args.m)
+    elif args.workload == "sweep":
+        wl = sweep_workload(torch, fp8bs, inputs, dev, list(range(1, 33)))
+    elif args.workload == "mx":
+        wl = mx_workload(torch, fp8bs, inputs, dev)
+    else:
+        wl = quantize_workload(torch, fp8bs, inputs, dev)
+    torch.cuda.synchronize()
+    if fp8bs.check_device_error() != 0:
+        raise RuntimeError("device error word set during set-up")
+
+    calls = wl["calls"]
+    os.makedirs(os.path.dirname(args.clocks_file), exist_ok=True)
+    with Clocks(args.clocks_file) as clk:
+        per, total_ms = time_calls(torch, calls, args.steps, warmup, pg, graph=wl.get("graph", False))
+    clocks = clk.summary() if rank == 0 else None
+    if fp8bs.check_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    step_bytes = sum(b for _, _, b, _ in calls)
+    total_ms = max_over_ranks(pg, total_ms)
+    all_bytes = sum_over_ranks(pg, step_bytes * args.steps)
+    value = all_bytes / (total_ms * 1e-3) / 1e9
+    per_call = {}
+    for (name, m, b, _), t in zip(calls, per):
+        lp = wl.get("launches_per_call", 1)
+        per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "gb_s": round(b / (t * 1e-3) / 1e9, 1),
+                          "frac_of_8TBps": round(b / (t * 1e-3) / 1e9 / HBM_NOMINAL_GBS, 4),
+                          "frac_of_measured": round(b / (t * 1e-3) / 1e9 / peak, 4)}
+    dom_name, dom_idx = wl["dominant"]
+    dom_bytes = sum(calls[i][2] for i in dom_idx)
+    dom_ms = sum(per[i] for i in dom_idx)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
+                "traffic": None}
+
+    e2e = None
+    if args.workload == "lm_head":
+        e2e_ms, h2d, d2h = e2e_lm_head(torch, fp8bs, wl, max(1, args.steps // 4), warmup, pg)
+        e2e_ms = max_over_ranks(pg, e2e_ms)
+        e_bytes = sum_over_ranks(pg, step_bytes * max(1, args.steps // 4))
+        e2e = {"value": round(e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "lm_head":
+        v, s, desc = oracle_sample()
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+               "host_cores_available": host_cores()}
+
+    launches = args.steps * sum(wl.get("launches_per_call", 1) for _ in calls) * wl.get("launches_per_step", 1)
+    if rank == 0:
+        line = {"metric": "block-FP8 W8A16 GEMV HBM GB/s (lm_head, M=1,4,8,16)" if args.workload == "lm_head"
+                else f"{args.workload} GB/s",
+                "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x bf16 -> fp32", "data": "synthetic",
+                "config": dict(wl["cfg"], parallelism=f"replicas x{world}"),
+                "per_call": per_call, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clocks, "gpu_launches": launches}
+        print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -40,7 +40,7 @@ namespace {
 __device__ uint32_t g_decode_err;
 
 constexpr int kKB = 128;             // K per stage (one scale block)
-constexpr int kConsumerWarps = 4;    // each owns 32 columns of the K block
+constexpr int kConsumerWarps = 8;    // 4 column slices x 2 row halves
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 4;
 constexpr int kMaxSplit = 8;         // portable cluster size limit
@@ -48,9 +48,9 @@ constexpr int kMaxSplit = 8;         // portable cluster size limit
 template <int MT>
 struct Cfg {
     // weight rows per CTA: a full block-scale row for m <= 16; half of one
-    // for wider x, which keeps the accumulators (BN/16 * MT * 4 fp32) in
-    // registers
+    // for wider x, which keeps the accumulators in registers
     static constexpr int kBN = MT <= 2 ? 128 : 64;
+    static constexpr int kRT = kBN / 32;                // 16-row tiles per warp
     static constexpr int kXRows = 8 * MT;               // x rows staged (zero-padded)
     static constexpr int kCodeBytes = kBN * kKB;        // 16 or 8 KB
     static constexpr int kXPanelBytes = kXRows * 128;   // 64 bf16 of each row
@@ -60,19 +60,30 @@ struct Cfg {
     static constexpr int kRedBytes = kBN * kRedStride * 4;
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRedBytes + 2 * kStages * 8;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+    static_assert(kRedBytes % 8 == 0, "barriers must stay 8-byte aligned");
 };
 
 __device__ __forceinline__ float pow2_e8m0(uint32_t E) {
     return E ? __uint_as_float(E << 23) : __uint_as_float(0x00400000u);
 }
 
+__device__ __forceinline__ void consumer_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// One CTA processes row tiles blockIdx.x, blockIdx.x + gridDim.x, ... (all
+// of them for its K range [kb0, kb1)).  With splits == 1 the grid is
+// persistent (about two CTAs per SM) and the TMA ring streams across tile
+// boundaries, so the next tile's codes are already arriving while the
+// consumers reduce and store the previous tile.  With splits > 1 each CTA
+// owns exactly one row tile and the cluster reduces over K.
 template <int MT, bool MX>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                                           const __grid_constant__ CUtensorMap tm_x,
                                                           const float *__restrict__ scales,
                                                           const uint8_t *__restrict__ e8m0,
                                                           __nv_bfloat16 *__restrict__ y, int m, int n,
-                                                          int kblocks, int groups, int splits) {
+                                                          int kblocks, int groups, int splits, int ntiles) {
     using C = Cfg<MT>;
     constexpr int kBN = C::kBN;
     extern __shared__ uint8_t smem_raw[];
@@ -83,13 +94,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     uint64_t *empty = full + kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kBN;
     const int split = blockIdx.y;
     const int kb0 = static_cast<int>((static_cast<int64_t>(split) * kblocks) / splits);
     const int kb1 = static_cast<int>((static_cast<int64_t>(split + 1) * kblocks) / splits);
     const int nkb = kb1 - kb0;
+    const int tile0 = blockIdx.x, tstep = gridDim.x;
+    const int my_tiles = tile0 < ntiles ? (ntiles - tile0 + tstep - 1) / tstep : 0;
+    const int mm = min(m, C::kXRows);
+    __shared__ int s_fail;  // a consumer warp gave up a wait: all consumers stop after this tile
 
     if (threadIdx.x == 0) {
+        s_fail = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
@@ -108,7 +123,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         // The whole warp walks the ring (so it stays converged); lane 0
         // waits for a free stage and issues the TMA copies.
         const uint64_t stream_policy = policy_evict_first();
-        for (int it = 0; it < nkb; ++it) {
+        const int total = my_tiles * nkb;
+        for (int it = 0; it < total; ++it) {
             const int s = it % kStages;
             int good = 1;
             if (it >= kStages && lane == 0) good = mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1);
@@ -118,8 +134,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 break;
             }
             if (lane == 0) {
+                const int ti = it / nkb;
+                const int n0 = (tile0 + ti * tstep) * kBN;
+                const int kx = (kb0 + (it - ti * nkb)) * kKB;
                 uint8_t *st = smem + s * C::kStageBytes;
-                const int kx = (kb0 + it) * kKB;
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
                 tma_load_2d_hint(st, &tm_codes, &full[s], kx, n0, stream_policy);
                 tma_load_2d(st + C::kCodeBytes, &tm_x, &full[s], kx, 0);
@@ -130,110 +148,141 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     } else {
         // ------------------------------------------------------ consumers
         const int g = lane >> 2, t = lane & 3;
-        float acc[kBN / 16][MT][4];
-#pragma unroll
-        for (int rt = 0; rt < kBN / 16; ++rt)
-#pragma unroll
-            for (int j = 0; j < MT; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[rt][j][q] = 0.0f;
-
+        const int cw = warp & 3;            // 32-column slice of each K block
+        const int rbase = (warp >> 2) * (kBN / 2);  // row half
         // x rows of this thread's B fragments: row 8j + pi(g) with
         // pi(g) = (g >> 1) | ((g & 1) << 2) (bank-conflict-free swizzle use)
         const int xrow_base = (g >> 1) | ((g & 1) << 2);
-        const int xpanel = warp >> 1;
-        const int xchunk = 4 * (warp & 1) + t;
+        const int xpanel = cw >> 1;
+        const int xchunk = 4 * (cw & 1) + t;
         // code rows of this thread's A fragments: 2g and 2g+1 of each 16-row tile
-        const int cchunk = 2 * warp + (t >> 1);
+        const int cchunk = 2 * cw + (t >> 1);
         const int coff = (t & 1) * 8;
-        const float *srow = MX ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks;
 
-        for (int it = 0; it < nkb; ++it) {
-            const int s = it % kStages;
-            // every lane waits (acquire); the warp leaves together if any gave up
-            const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
-            if (!__all_sync(0xffffffffu, ready)) {
-                if (lane == 0) atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
-                break;
-            }
-            const uint8_t *cs = smem + s * C::kStageBytes;
-            const uint8_t *xs = cs + C::kCodeBytes + xpanel * C::kXPanelBytes;
-
-            uint32_t bx[MT][4];
+        for (int ti = 0; ti < my_tiles; ++ti) {
+            const int n0 = (tile0 + ti * tstep) * kBN;
+            const float *srow = MX ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
+            float acc[C::kRT][MT][4];
 #pragma unroll
-            for (int j = 0; j < MT; ++j) {
-                const int xr = 8 * j + xrow_base;
-                const uint4 v = *reinterpret_cast<const uint4 *>(xs + xr * 128 + ((xchunk ^ (xr & 7)) << 4));
-                bx[j][0] = v.x;
-                bx[j][1] = v.y;
-                bx[j][2] = v.z;
-                bx[j][3] = v.w;
-            }
-            const float sblk = MX ? 0.0f : __ldg(srow + kb0 + it);
-            const int grp = (kb0 + it) * 4 + warp;  // MX group of this warp's 32 columns
-
+            for (int rt = 0; rt < C::kRT; ++rt)
 #pragma unroll
-            for (int rt = 0; rt < kBN / 16; ++rt) {
-                const int ra = rt * 16 + 2 * g, rb = ra + 1;
-                const uint2 qa = *reinterpret_cast<const uint2 *>(cs + ra * 128 + ((cchunk ^ (ra & 7)) << 4) + coff);
-                const uint2 qb = *reinterpret_cast<const uint2 *>(cs + rb * 128 + ((cchunk ^ (rb & 7)) << 4) + coff);
-                const uint32_t a00 = e4m3x2_to_bf16x2(qa.x, 0x9180u), a01 = e4m3x2_to_bf16x2(qb.x, 0x9180u);
-                const uint32_t a02 = e4m3x2_to_bf16x2(qa.x, 0xB3A2u), a03 = e4m3x2_to_bf16x2(qb.x, 0xB3A2u);
-                const uint32_t a10 = e4m3x2_to_bf16x2(qa.y, 0x9180u), a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
-                const uint32_t a12 = e4m3x2_to_bf16x2(qa.y, 0xB3A2u), a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
-                float sa = sblk, sb = sblk;
-                if (MX) {
-                    const int64_t row_a = static_cast<int64_t>(n0) + ra;
-                    const bool gin = grp < groups;
-                    sa = (gin && row_a < n) ? pow2_e8m0(__ldg(e8m0 + row_a * groups + grp)) : 0.0f;
-                    sb = (gin && row_a + 1 < n) ? pow2_e8m0(__ldg(e8m0 + (row_a + 1) * groups + grp)) : 0.0f;
+                for (int j = 0; j < MT; ++j)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[rt][j][q] = 0.0f;
+            float s_next = MX ? 0.0f : __ldg(srow);
+
+            for (int kbi = 0; kbi < nkb; ++kbi) {
+                const int it = ti * nkb + kbi;
+                const int s = it % kStages;
+                const float sblk = s_next;
+                if (!MX && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
+                // every lane waits (acquire); the warp leaves together if any gave up
+                const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
+                if (!__all_sync(0xffffffffu, ready)) {
+                    if (lane == 0) {
+                        atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
+                        s_fail = 1;
+                    }
+                    break;
                 }
+                const uint8_t *cs = smem + s * C::kStageBytes;
+                const uint8_t *xs = cs + C::kCodeBytes + xpanel * C::kXPanelBytes;
+
+                uint32_t bx[MT][4];
 #pragma unroll
                 for (int j = 0; j < MT; ++j) {
-                    float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
-                    mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
-                    acc[rt][j][0] = fmaf(sa, c[0], acc[rt][j][0]);
-                    acc[rt][j][1] = fmaf(sa, c[1], acc[rt][j][1]);
-                    acc[rt][j][2] = fmaf(sb, c[2], acc[rt][j][2]);
-                    acc[rt][j][3] = fmaf(sb, c[3], acc[rt][j][3]);
+                    const int xr = 8 * j + xrow_base;
+                    const uint4 v =
+                        *reinterpret_cast<const uint4 *>(xs + xr * 128 + ((xchunk ^ (xr & 7)) << 4));
+                    bx[j][0] = v.x;
+                    bx[j][1] = v.y;
+                    bx[j][2] = v.z;
+                    bx[j][3] = v.w;
                 }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-        }
+                const int grp = (kb0 + kbi) * 4 + cw;  // MX group of this warp's 32 columns
 
-        // Cross-warp reduction, in warp order, into red[n_local][m].
-        // acc[rt][j][q] is y[m = 8j + t + 4(q&1)][n_local = 16rt + 2g + (q>>1)].
-#pragma unroll 1
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            if (warp == w) {
 #pragma unroll
-                for (int rt = 0; rt < kBN / 16; ++rt)
+                for (int rt = 0; rt < C::kRT; ++rt) {
+                    const int ra = rbase + rt * 16 + 2 * g, rb = ra + 1;
+                    const uint2 qa =
+                        *reinterpret_cast<const uint2 *>(cs + ra * 128 + ((cchunk ^ (ra & 7)) << 4) + coff);
+                    const uint2 qb =
+                        *reinterpret_cast<const uint2 *>(cs + rb * 128 + ((cchunk ^ (rb & 7)) << 4) + coff);
+                    const uint32_t a00 = e4m3x2_to_bf16x2(qa.x, 0x9180u), a01 = e4m3x2_to_bf16x2(qb.x, 0x9180u);
+                    const uint32_t a02 = e4m3x2_to_bf16x2(qa.x, 0xB3A2u), a03 = e4m3x2_to_bf16x2(qb.x, 0xB3A2u);
+                    const uint32_t a10 = e4m3x2_to_bf16x2(qa.y, 0x9180u), a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
+                    const uint32_t a12 = e4m3x2_to_bf16x2(qa.y, 0xB3A2u), a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
+                    float sa = sblk, sb = sblk;
+                    if (MX) {
+                        const int64_t row_a = static_cast<int64_t>(n0) + ra;
+                        const bool gin = grp < groups;
+                        sa = (gin && row_a < n) ? pow2_e8m0(__ldg(e8m0 + row_a * groups + grp)) : 0.0f;
+                        sb = (gin && row_a + 1 < n) ? pow2_e8m0(__ldg(e8m0 + (row_a + 1) * groups + grp)) : 0.0f;
+                    }
 #pragma unroll
-                    for (int j = 0; j < MT; ++j)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int nl = rt * 16 + 2 * g + (q >> 1);
-                            const int mc = 8 * j + t + 4 * (q & 1);
-                            float *p = red + nl * C::kRedStride + mc;
-                            *p = (w == 0) ? acc[rt][j][q] : *p + acc[rt][j][q];
-                        }
+                    for (int j = 0; j < MT; ++j) {
+                        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                        mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                        acc[rt][j][0] = fmaf(sa, c[0], acc[rt][j][0]);
+                        acc[rt][j][1] = fmaf(sa, c[1], acc[rt][j][1]);
+                        acc[rt][j][2] = fmaf(sb, c[2], acc[rt][j][2]);
+                        acc[rt][j][3] = fmaf(sb, c[3], acc[rt][j][3]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
             }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+
+            // Cross-warp reduction over the 4 column slices, in slice order,
+            // into red[n_local][m]; the two row halves write disjoint rows.
+            // acc[rt][j][q] is y[m = 8j + t + 4(q&1)][n_local = rbase + 16rt + 2g + (q>>1)].
+#pragma unroll 1
+            for (int p = 0; p < 4; ++p) {
+                if (cw == p) {
+#pragma unroll
+                    for (int rt = 0; rt < C::kRT; ++rt)
+#pragma unroll
+                        for (int j = 0; j < MT; ++j)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int nl = rbase + rt * 16 + 2 * g + (q >> 1);
+                                const int mc = 8 * j + t + 4 * (q & 1);
+                                float *ptr = red + nl * C::kRedStride + mc;
+                                *ptr = (p == 0) ? acc[rt][j][q] : *ptr + acc[rt][j][q];
+                            }
+                }
+                consumer_bar();
+            }
+            // Every write of s_fail for this tile precedes the phase barriers
+            // above, and a write for the next tile can only follow the last
+            // barrier below, so all consumer warps read the same value.
+            const bool stop = *reinterpret_cast<volatile int *>(&s_fail) != 0;
+            if (splits == 1) {
+                // bf16 store of this tile, consecutive threads on consecutive n
+                for (int e = threadIdx.x; e < mm * kBN; e += kConsumerWarps * 32) {
+                    const int mi = e / kBN;
+                    const int nl = e - mi * kBN;
+                    if (n0 + nl < n)
+                        y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(red[nl * C::kRedStride + mi]);
+                }
+                consumer_bar();  // red is rewritten by the next tile
+            }
+            if (stop) break;
         }
     }
     pdl_launch_dependents();
-    __syncthreads();
+    if (splits == 1) return;
 
-    // Split-K reduction across the cluster (fixed rank order) and bf16 store.
-    if (splits > 1) cluster_sync_all();
-    const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    // Split-K: one row tile per CTA; reduce across the cluster in rank order.
+    __syncthreads();
+    cluster_sync_all();
+    const int n0 = tile0 * kBN;
+    const int rank = static_cast<int>(cluster_ctarank());
     const int rows_per = (kBN + splits - 1) / splits;
     const int r_begin = rank * rows_per;
     const int r_end = min(kBN, r_begin + rows_per);
     const int my_rows = max(0, r_end - r_begin);
-    const int mm = min(m, C::kXRows);
     const uint32_t red_addr = smem_u32(red);
     for (int e = threadIdx.x; e < mm * my_rows; e += kThreads) {
         const int mi = e / my_rows;
@@ -241,16 +290,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         const int nn = n0 + nl;
         if (nn >= n) continue;
         const uint32_t off = static_cast<uint32_t>((nl * C::kRedStride + mi) * 4);
-        float sum;
-        if (splits > 1) {
-            sum = 0.0f;
-            for (int q = 0; q < splits; ++q) sum += dsmem_ld_f32(dsmem_map(red_addr + off, q));
-        } else {
-            sum = red[nl * C::kRedStride + mi];
-        }
+        float sum = 0.0f;
+        for (int q = 0; q < splits; ++q) sum += dsmem_ld_f32(dsmem_map(red_addr + off, q));
         y[static_cast<int64_t>(mi) * n + nn] = __float2bfloat16_rn(sum);
     }
-    if (splits > 1) cluster_sync_all();  // keep shared memory alive for peers
+    cluster_sync_all();  // keep shared memory alive for peers
 }
 
 // Per-device, per-instantiation launch setup (shared-memory opt-in and the
@@ -306,9 +350,11 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
         if (splits > kblocks) splits = kblocks;
         if (splits < 1) splits = 1;
     }
+    // splits == 1: persistent grid; splits > 1: one CTA per (row tile, split)
+    const int gx = splits == 1 ? (ntiles < capacity ? ntiles : capacity) : ntiles;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>(splits), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(splits), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
@@ -328,7 +374,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, a.e8m0,
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m),
-                              static_cast<int>(a.n), kblocks, groups, splits);
+                              static_cast<int>(a.n), kblocks, groups, splits, ntiles);
 }
 
 template <bool MX>

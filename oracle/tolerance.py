@@ -11,6 +11,10 @@ bound applied is therefore the stated one plus half a bf16 ulp of the result:
     |y - y64| <= 1e-2 * ||x_m|| * max|deqW_n| / sqrt(K) + ulp_bf16(max(|y|, |y64|)) / 2
 
 The as-written ratio is still computed and reported.
+
+The relative-L2 bound is a statistic over many outputs; one bf16 rounding
+alone can reach 2^-8 (3.9e-3) relative, so it is applied to outputs of at
+least 256 elements, and smaller outputs are held to the element-wise bound.
 """
 from __future__ import annotations
 
@@ -49,11 +53,16 @@ def gemv_errors(y_bits, y64, x_bits, wmax_rows) -> dict:
         "rel_l2": rel_l2,
         "max_abs_err": float(err.max()) if err.size else 0.0,
         "finite": bool(np.all(np.isfinite(y))),
+        "count": int(y.size),
     }
 
 
+REL_L2_MIN_COUNT = 256
+
+
 def gemv_ok(stats: dict, rel_l2_max: float = 2e-3) -> bool:
-    return stats["finite"] and stats["max_ratio"] <= 1.0 and stats["rel_l2"] <= rel_l2_max
+    rel_ok = stats["rel_l2"] <= rel_l2_max or stats["count"] < REL_L2_MIN_COUNT
+    return stats["finite"] and stats["max_ratio"] <= 1.0 and rel_ok
 
 
 def block_wmax_rows(codes_rows, scales, rows, table) -> np.ndarray:

@@ -48,7 +48,8 @@ def test_every_code_decodes_exactly(pkg, path, m):
     x[:, 3] = 0x3F80
     y = pkg.gemv(bf16_dev(x), to_dev_bits(w), torch.from_numpy(scales).to(DEV), path=path)
     torch.cuda.synchronize()
-    want = np.array([oracle.double_to_bf16(v) for v in table()[codes_list]], dtype=np.uint16)
+    # a sum that starts from +0 turns the -0 of code 0x80 into +0 (IEEE)
+    want = np.array([oracle.double_to_bf16(0.0 + v) for v in table()[codes_list]], dtype=np.uint16)
     got = bits(y.cpu())
     for i in range(m):
         assert np.array_equal(got[i], want), np.argwhere(got[i] != want)[:5]
@@ -67,7 +68,7 @@ def test_one_hot_columns_on_ragged_tiles(pkg, path):
     y = bits(pkg.gemv(bf16_dev(x), codes, scales, path=path).cpu())
     for i, c in enumerate(cols):
         prod = (table()[oc[:, c]].astype(np.float32) * os_[np.arange(n) // 128, c // 128]).astype(np.float32)
-        want = np.array([oracle.double_to_bf16(float(v)) for v in prod], dtype=np.uint16)
+        want = np.array([oracle.double_to_bf16(0.0 + float(v)) for v in prod], dtype=np.uint16)
         assert np.array_equal(y[i], want), (c, np.argwhere(y[i] != want)[:5])
 
 
