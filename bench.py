@@ -45,6 +45,15 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured, burst"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def gemv_bytes(m, n, k, mx=False):
     scales = n * ((k + 31) // 32) if mx else 4 * ((n + 127) // 128) * ((k + 127) // 128)
     return n * k + scales + 2 * m * k + 2 * m * n
@@ -218,6 +227,20 @@ def mx_workload(torch, fp8bs, inputs, dev):
     return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,true>", [0, 1]), launches_per_call=4)
 
 
+def prefill_workload(torch, fp8bs, inputs, dev):
+    ms = [512, 2048, 4096]
+    codes, scales = fp8bs.quantize(inputs.sweep_weight(0, device=dev))
+    n, k = inputs.SWEEP_SHAPE
+    calls = []
+    for m in ms:
+        x = inputs.activations(m, k, 700 + m, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        calls.append((f"M={m}", m, 2 * m * n * k, (lambda x=x, y=y: fp8bs.gemv(x, codes, scales, y=y))))
+    cfg = {"workload": "prefill: block-FP8 [12288,4096] W8A16 GEMM on tcgen05, M=512,2048,4096", "n": n, "k": k,
+           "ms": ms, "l2": "weight (50 MB) and x fit in L2; compute-bound"}
+    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel", [0, 1, 2]), flops=True)
+
+
 def quantize_workload(torch, fp8bs, inputs, dev):
     w = inputs.heavy_tail_weight(5, device=dev)
     n, k = w.shape
@@ -353,7 +376,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="lm_head", choices=["lm_head", "rotation", "sweep", "mx", "quantize"])
+    ap.add_argument("--workload", default="lm_head",
+                    choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-file", default=os.path.join(ROOT, "gpurun_out", "bench_clocks.csv"))
@@ -405,6 +429,8 @@ def main():
         wl = sweep_workload(torch, fp8bs, inputs, dev, list(range(1, 33)))
     elif args.workload == "mx":
         wl = mx_workload(torch, fp8bs, inputs, dev)
+    elif args.workload == "prefill":
+        wl = prefill_workload(torch, fp8bs, inputs, dev)
     else:
         wl = quantize_workload(torch, fp8bs, inputs, dev)
     torch.cuda.synchronize()
@@ -422,20 +448,34 @@ def main():
     step_bytes = sum(b for _, _, b, _ in calls)
     total_ms = max_over_ranks(pg, total_ms)
     all_bytes = sum_over_ranks(pg, step_bytes * args.steps)
-    value = all_bytes / (total_ms * 1e-3) / 1e9
+    flops = wl.get("flops", False)
+    scale_unit = 1e12 if flops else 1e9
+    unit = "TFLOP/s" if flops else "GB/s"
+    tpeak, tpeak_kind = tensor_peak()
+    value = all_bytes / (total_ms * 1e-3) / scale_unit
     per_call = {}
     for (name, m, b, _), t in zip(calls, per):
         lp = wl.get("launches_per_call", 1)
-        per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "gb_s": round(b / (t * 1e-3) / 1e9, 1),
-                          "frac_of_8TBps": round(b / (t * 1e-3) / 1e9 / HBM_NOMINAL_GBS, 4),
-                          "frac_of_measured": round(b / (t * 1e-3) / 1e9 / peak, 4)}
+        rate = b / (t * 1e-3) / scale_unit
+        if flops:
+            per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "tflop_s": round(rate, 1),
+                              "frac_of_measured_bf16": round(rate / tpeak, 4)}
+        else:
+            per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "gb_s": round(rate, 1),
+                              "frac_of_8TBps": round(rate / HBM_NOMINAL_GBS, 4),
+                              "frac_of_measured": round(rate / peak, 4)}
     dom_name, dom_idx = wl["dominant"]
     dom_bytes = sum(calls[i][2] for i in dom_idx)
     dom_ms = sum(per[i] for i in dom_idx)
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
-                "traffic": None}
+    achieved = dom_bytes / (dom_ms * 1e-3) / scale_unit
+    if flops:
+        roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
+                    "peak_kind": f"bf16_tflops ({tpeak_kind})", "traffic": None}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
+                    "traffic": None}
 
     e2e = None
     if args.workload == "lm_head":
@@ -454,8 +494,8 @@ def main():
     launches = args.steps * sum(wl.get("launches_per_call", 1) for _ in calls) * wl.get("launches_per_step", 1)
     if rank == 0:
         line = {"metric": "block-FP8 W8A16 GEMV HBM GB/s (lm_head, M=1,4,8,16)" if args.workload == "lm_head"
-                else f"{args.workload} GB/s",
-                "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                else f"{args.workload} {unit}",
+                "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x bf16 -> fp32", "data": "synthetic",
                 "config": dict(wl["cfg"], parallelism=f"replicas x{world}"),

@@ -34,8 +34,8 @@ def bf16_dev(a_bits: np.ndarray):
 
 
 # ------------------------------------------------------------ exact checks
-@pytest.mark.parametrize("path", [PATH_DECODE, PATH_GENERIC])
-@pytest.mark.parametrize("m", [1, 5, 8, 9, 16, 17, 32])
+@pytest.mark.parametrize("path", [PATH_DECODE, PATH_GENERIC, PATH_PREFILL])
+@pytest.mark.parametrize("m", [1, 5, 8, 9, 16, 17, 32, 40, 130])
 def test_every_code_decodes_exactly(pkg, path, m):
     """Row i of W holds code i at column 3 (scales 1); x = e_3, so
     y[:, i] = bf16(dec(i)) exactly for every finite code."""
@@ -55,7 +55,7 @@ def test_every_code_decodes_exactly(pkg, path, m):
         assert np.array_equal(got[i], want), np.argwhere(got[i] != want)[:5]
 
 
-@pytest.mark.parametrize("path", [PATH_DECODE, PATH_GENERIC])
+@pytest.mark.parametrize("path", [PATH_DECODE, PATH_GENERIC, PATH_PREFILL])
 def test_one_hot_columns_on_ragged_tiles(pkg, path):
     w = inputs.tiny_ragged_weight(0)
     n, k = w.shape
@@ -75,7 +75,7 @@ def test_one_hot_columns_on_ragged_tiles(pkg, path):
 def test_zero_input_gives_zero(pkg):
     w = inputs.gaussian_bf16((256, 512), 0.02, 3)
     oc, os_ = oracle.block_quantize(bits(w))
-    for path in (PATH_DECODE, PATH_GENERIC):
+    for path in (PATH_DECODE, PATH_GENERIC, PATH_PREFILL):
         y = pkg.gemv(torch.zeros((4, 512), dtype=torch.bfloat16, device=DEV), to_dev_bits(oc),
                      torch.from_numpy(os_).to(DEV), path=path)
         assert int((y.view(torch.int16) & 0x7FFF).abs().sum()) == 0
@@ -118,6 +118,15 @@ def test_small_shapes_mx(pkg, n, k, m):
     for path in (0, PATH_GENERIC) if k % 16 else (0, PATH_DECODE, PATH_GENERIC):
         y = pkg.mx_gemv(x.to(DEV), to_dev_bits(oc), to_dev_bits(oe), path=path)
         check_mx_gemv(y, bits(x), np.arange(n), oc, oe)
+
+
+PREFILL_SHAPES = [(129, 272), (256, 1024), (64, 4096), (300, 16), (1, 128), (520, 640)]
+
+
+@pytest.mark.parametrize("n,k", PREFILL_SHAPES)
+@pytest.mark.parametrize("m", [33, 128, 130, 257])
+def test_prefill_small_shapes(pkg, n, k, m):
+    full_block_case(pkg, inputs.gaussian_bf16((n, k), 0.02, n * 17 + k), m, PATH_PREFILL, seed=m)
 
 
 # ------------------------------------------------------ full-size, sampled
@@ -167,7 +176,7 @@ def test_sweep_shape_all_m(pkg):
 def test_prefill_shapes_sampled(pkg):
     w = inputs.sweep_weight(0, device=DEV)
     rng = np.random.default_rng(9)
-    sampled_block_case(pkg, w, [64, 512], _row_blocks(w.shape[0], 1, 6),
+    sampled_block_case(pkg, w, [64, 512, 2048, 4096], _row_blocks(w.shape[0], 1, 6),
                        x_rows=lambda m: np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, 14)])))
 
 
