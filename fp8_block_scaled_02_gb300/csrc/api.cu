@@ -1,7 +1,7 @@
 // api.cu -- the C ABI (include/fp8bs.h): argument validation and shape-only
 // dispatch to the kernels.  Nothing here allocates, synchronises (except the
 // explicit debug query) or branches on tensor values.
-#include "../../include/fp8bs.h"
+#include "fp8bs.h"
 #include "internal.h"
 
 namespace {

@@ -3,26 +3,31 @@
 //
 // Design (sm_103a):
 //  * One CTA owns 128 weight rows (one row of 128x128 block scales) and a
-//    contiguous range of 128-wide K blocks.  When there are too few row
-//    tiles to fill the GPU, the K blocks are split over the CTAs of a thread
-//    block cluster (up to 8) and the partial sums are reduced through
-//    distributed shared memory -- no global workspace, a fixed summation
-//    order, and no waits on other CTAs beyond the hardware cluster barrier.
-//  * A producer warp streams each K block's 128x128 code tile (16 KB) and the
-//    matching x tile with 2-D TMA (128-byte swizzle) into a 4-stage shared
-//    memory ring guarded by mbarriers; 4 consumer warps split the K block
-//    32 columns each.  Every code byte is read from HBM once.
-//  * Consumers decode e4m3 pairs straight to exact bf16 pairs in registers
-//    (prmt + shift + one bf16x2 multiply) and run bf16 mma.sync m16n8k16
-//    with the weights as the 16-row A operand and x as the 8-wide B operand
-//    (swap-AB: m sits on the MMA's n axis, so m <= 32 needs at most four
-//    n8 tiles).  Each K block's fp32 MMA result starts from zero and is
-//    multiplied by that block's fp32 scale before it joins the accumulator
-//    ("promotion"), so the scale is never folded into a rounded bf16 weight.
-//    For MXFP8 the 32-column slice of a warp is exactly one e8m0 group, and
-//    each row's 2^(E-127) multiplies the slice's partial sum.
+//    contiguous range of 128-wide K blocks.  With enough row tiles the grid is
+//    persistent (about two CTAs per SM) and each CTA's TMA ring streams across
+//    row-tile boundaries; with too few, the K blocks are split over the CTAs
+//    of a thread-block cluster (up to 8) and the partial sums are reduced in
+//    rank order through distributed shared memory -- no global workspace and
+//    no waits on other CTAs beyond the hardware cluster barrier.
+//  * A TMA warp streams each K block's 128x128 code tile (16 KB) and the
+//    matching x tile (2-D TMA, 128-byte swizzle) into a shared-memory ring.
+//  * A converter warp rewrites each staged x tile in place from bf16 to f16
+//    with an exact power-of-two rescale per (row of x, 32-column slice): the
+//    slice maximum is moved into [2^14, 2^15), so every value within 2^-31 of
+//    the slice maximum converts exactly and nothing overflows; the inverse
+//    power of two is kept for the promotion step.  For MXFP8 it also stages
+//    the K block's e8m0 exponents as fp32 row scales.
+//  * Eight consumer warps (4 column slices x 2 row halves) convert code pairs
+//    with cvt.rn.f16x2.e4m3x2 (exact) and run f16 mma.sync m16n8k16 with the
+//    weights as the 16-row A operand and x as the 8-wide B operand (m on the
+//    MMA's n axis, so m <= 32 needs at most four n8 tiles).  Each K slice's
+//    fp32 MMA result starts from zero and is multiplied by (block scale x
+//    inverse x rescale) before it joins the accumulator, so the scale is
+//    applied once per 128-wide K block to an fp32 partial and is never folded
+//    into a rounded weight.  For MXFP8 a warp's 32-column slice is exactly
+//    one e8m0 group.
 //  * The logical k order inside each MMA is a fixed permutation of the
-//    physical columns, applied identically to A and B, so that every thread
+//    physical columns, applied identically to A and B, so every thread
 //    fetches 8 contiguous code bytes and 16 contiguous x bytes per K block
 //    with conflict-free shared-memory loads.
 //  * Programmatic dependent launch: a kernel may start (barrier init,
@@ -41,26 +46,41 @@ __device__ uint32_t g_decode_err;
 
 constexpr int kKB = 128;             // K per stage (one scale block)
 constexpr int kConsumerWarps = 8;    // 4 column slices x 2 row halves
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 4;
+constexpr int kWarpTma = kConsumerWarps;
+constexpr int kWarpConv0 = kConsumerWarps + 1;
 constexpr int kMaxSplit = 8;         // portable cluster size limit
 
-template <int MT>
+// F16: operands are f16 (codes via cvt.rn.f16x2.e4m3x2, x rescaled to f16 by
+// a converter warp); otherwise bf16 (codes decoded with integer ops, x used
+// as staged).  The f16 form halves the decode work and wins while the
+// consumers are bound by it (m <= 8); the bf16 form has no converter stage
+// and wins for wider x.  MXFP8 always uses the converter warp, which also
+// stages the e8m0 row scales.
+template <int MT, bool MX, bool F16>
 struct Cfg {
-    // weight rows per CTA: a full block-scale row for m <= 16; half of one
-    // for wider x, which keeps the accumulators in registers
+    // weight rows per CTA: a full block-scale row for m <= 16, half of one for
+    // wider x (keeps the accumulators of two CTAs per SM in registers)
     static constexpr int kBN = MT <= 2 ? 128 : 64;
-    static constexpr int kRT = kBN / 32;                // 16-row tiles per warp
+    static constexpr int kRT = kBN / 32;                // 16-row tiles per consumer warp
+    static constexpr int kStages = 4;
+    static constexpr bool kConv = F16 || MX;            // converter warp present
+    static constexpr int kConvWarps = kConv ? 1 : 0;
+    static constexpr int kThreads = (kConsumerWarps + 1 + kConvWarps) * 32;
     static constexpr int kXRows = 8 * MT;               // x rows staged (zero-padded)
-    static constexpr int kCodeBytes = kBN * kKB;        // 16 or 8 KB
-    static constexpr int kXPanelBytes = kXRows * 128;   // 64 bf16 of each row
-    static constexpr int kXBytes = 2 * kXPanelBytes;
-    static constexpr int kStageBytes = kCodeBytes + kXBytes;
+    static constexpr int kCodeBytes = kBN * kKB;        // 16 KB
+    static constexpr int kXPanelBytes = kXRows * 128;   // 64 columns of each row
+    static constexpr int kStageBytes = kCodeBytes + 2 * kXPanelBytes;
+    static constexpr int kXInvFloats = 4 * kXRows;      // per stage: [slice][row]
+    static constexpr int kRowScaleFloats = MX ? 4 * kBN : 0;  // per stage: [slice][weight row]
+    static constexpr int kAuxBytes = (kXInvFloats + kRowScaleFloats) * 4;
     static constexpr int kRedStride = kXRows + 1;       // padded fp32 row
     static constexpr int kRedBytes = kBN * kRedStride * 4;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kRedBytes + 2 * kStages * 8;
+    static constexpr int kSmemBytes =
+        1024 + kStages * kStageBytes + kStages * kAuxBytes + kRedBytes + 3 * kStages * 8;
+    static constexpr int kMinBlocks = 2;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static_assert(kRedBytes % 8 == 0, "barriers must stay 8-byte aligned");
+    static_assert((kStages * kAuxBytes + kRedBytes) % 8 == 0, "barriers must stay 8-byte aligned");
+    static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
 __device__ __forceinline__ float pow2_e8m0(uint32_t E) {
@@ -71,27 +91,72 @@ __device__ __forceinline__ void consumer_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// Position of x row r in the per-slice inverse-scale table: rows 8j+t and
+// 8j+t+4 sit next to each other, so a consumer thread reads both with one
+// 64-bit load.
+__device__ __forceinline__ int xinv_slot(int r) { return (r & ~7) | ((r & 3) << 1) | ((r >> 2) & 1); }
+
+// Rewrite one (x row r, 32-column slice sl) of a staged x tile from bf16 to
+// f16 in place with the exact power-of-two rescale described above.
+template <int kXPanelBytes, int kXRows>
+__device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r, int sl) {
+    uint8_t *base = xs + (sl >> 1) * kXPanelBytes + r * 128;
+    const int c0 = 4 * (sl & 1);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4 *>(base + (((c0 + i) ^ (r & 7)) << 4));
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        mx = max_u16x2(mx, v[i].x & 0x7FFF7FFFu);
+        mx = max_u16x2(mx, v[i].y & 0x7FFF7FFFu);
+        mx = max_u16x2(mx, v[i].z & 0x7FFF7FFFu);
+        mx = max_u16x2(mx, v[i].w & 0x7FFF7FFFu);
+    }
+    const uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);  // |max| as bf16 bits
+    int k = 0;                                          // scale 2^k
+    if (m16 != 0) {
+        const int field = static_cast<int>(m16 >> 7);
+        const int e = field ? field - 127 : -133;       // floor(log2 |max|) (subnormal: below -126)
+        k = min(126, max(-126, 14 - e));
+    }
+    const float mult = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 o;
+        o.x = f32x2_to_f16x2(bf16lo_to_f32(v[i].x) * mult, bf16hi_to_f32(v[i].x) * mult);
+        o.y = f32x2_to_f16x2(bf16lo_to_f32(v[i].y) * mult, bf16hi_to_f32(v[i].y) * mult);
+        o.z = f32x2_to_f16x2(bf16lo_to_f32(v[i].z) * mult, bf16hi_to_f32(v[i].z) * mult);
+        o.w = f32x2_to_f16x2(bf16lo_to_f32(v[i].w) * mult, bf16hi_to_f32(v[i].w) * mult);
+        *reinterpret_cast<uint4 *>(base + (((c0 + i) ^ (r & 7)) << 4)) = o;
+    }
+    xinv[sl * kXRows + xinv_slot(r)] = inv;
+}
+
 // One CTA processes row tiles blockIdx.x, blockIdx.x + gridDim.x, ... (all
 // of them for its K range [kb0, kb1)).  With splits == 1 the grid is
-// persistent (about two CTAs per SM) and the TMA ring streams across tile
-// boundaries, so the next tile's codes are already arriving while the
-// consumers reduce and store the previous tile.  With splits > 1 each CTA
-// owns exactly one row tile and the cluster reduces over K.
-template <int MT, bool MX>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tm_codes,
-                                                          const __grid_constant__ CUtensorMap tm_x,
-                                                          const float *__restrict__ scales,
-                                                          const uint8_t *__restrict__ e8m0,
-                                                          __nv_bfloat16 *__restrict__ y, int m, int n,
-                                                          int kblocks, int groups, int splits, int ntiles) {
-    using C = Cfg<MT>;
+// persistent and the TMA ring streams across tile boundaries, so the next
+// tile's codes are already arriving while the consumers reduce and store the
+// previous tile.  With splits > 1 each CTA owns exactly one row tile and the
+// cluster reduces over K.
+template <int MT, bool MX, bool F16>
+__global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::kMinBlocks) decode_kernel(
+    const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
+    const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y, int m,
+    int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec) {
+    using C = Cfg<MT, MX, F16>;
+    constexpr int kStages = C::kStages;
     constexpr int kBN = C::kBN;
+    constexpr int kRT = C::kRT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    float *red = reinterpret_cast<float *>(smem + kStages * C::kStageBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * C::kStageBytes + C::kRedBytes);
-    uint64_t *empty = full + kStages;
+    float *aux = reinterpret_cast<float *>(smem + kStages * C::kStageBytes);
+    float *red = aux + kStages * (C::kXInvFloats + C::kRowScaleFloats);
+    uint64_t *full = reinterpret_cast<uint64_t *>(red + kBN * C::kRedStride);
+    uint64_t *xready = full + kStages;
+    uint64_t *empty = xready + kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.y;
@@ -100,30 +165,31 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int nkb = kb1 - kb0;
     const int tile0 = blockIdx.x, tstep = gridDim.x;
     const int my_tiles = tile0 < ntiles ? (ntiles - tile0 + tstep - 1) / tstep : 0;
+    const int total = my_tiles * nkb;
     const int mm = min(m, C::kXRows);
-    __shared__ int s_fail;  // a consumer warp gave up a wait: all consumers stop after this tile
+    __shared__ int s_fail;  // a warp gave up a wait: consumers stop after this tile
 
     if (threadIdx.x == 0) {
         s_fail = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
+            mbar_init(&xready[s], C::kConv ? C::kConvWarps : 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
         fence_mbarrier_init();
     }
-    if (warp == kConsumerWarps && lane == 0) {
+    if (warp == kWarpTma && lane == 0) {
         prefetch_tensormap(&tm_codes);
         prefetch_tensormap(&tm_x);
     }
     __syncthreads();
     pdl_wait();  // inputs may be produced by the previous kernel in the stream
 
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------ producer
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------ TMA producer
         // The whole warp walks the ring (so it stays converged); lane 0
         // waits for a free stage and issues the TMA copies.
         const uint64_t stream_policy = policy_evict_first();
-        const int total = my_tiles * nkb;
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages;
             int good = 1;
@@ -145,10 +211,70 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             }
             __syncwarp();
         }
+    } else if (C::kConv && warp >= kWarpConv0) {
+        // ------------------------------------------------------ x converter
+        const int clane = (warp - kWarpConv0) * 32 + lane;
+        constexpr int kConvLanes = C::kConvWarps * 32;
+        for (int it = 0; it < total; ++it) {
+            const int s = it % kStages;
+            uint32_t ev[MX ? kBN / kConvLanes : 1];  // e8m0 of this lane's rows, 4 groups each
+            if (MX) {
+                const int ti = it / nkb;
+                const int n0 = (tile0 + ti * tstep) * kBN;
+                const int g0 = (kb0 + (it - ti * nkb)) * 4;
+#pragma unroll
+                for (int i = 0; i < (MX ? kBN / kConvLanes : 1); ++i) {
+                    const int64_t row = static_cast<int64_t>(n0) + clane + i * kConvLanes;
+                    uint32_t w = 0;
+                    if (row < n) {
+                        const uint8_t *p = e8m0 + row * groups + g0;
+                        if (e8m0_vec) {
+                            w = __ldg(reinterpret_cast<const uint32_t *>(p));
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                if (g0 + q < groups) w |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
+                        }
+                    }
+                    ev[i] = w;
+                }
+            }
+            const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
+            if (!__all_sync(0xffffffffu, ready)) {
+                if (lane == 0) {
+                    atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
+                    s_fail = 1;
+                }
+                break;
+            }
+            uint8_t *xs = smem + s * C::kStageBytes + C::kCodeBytes;
+            float *xinv = aux + s * (C::kXInvFloats + C::kRowScaleFloats);
+            if (F16) {
+                for (int u = clane; u < 4 * C::kXRows; u += kConvLanes)
+                    convert_x_slice<C::kXPanelBytes, C::kXRows>(xs, xinv, u >> 2, u & 3);
+            }
+            if (MX) {
+                const int ti = it / nkb;
+                const int n0 = (tile0 + ti * tstep) * kBN;
+                const int g0 = (kb0 + (it - ti * nkb)) * 4;
+                float *rs = xinv + C::kXInvFloats;
+#pragma unroll
+                for (int i = 0; i < (MX ? kBN / kConvLanes : 1); ++i) {
+                    const int r = clane + i * kConvLanes;
+                    const bool rin = n0 + r < n;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        rs[q * kBN + r] = (rin && g0 + q < groups) ? pow2_e8m0((ev[i] >> (8 * q)) & 0xFFu) : 0.0f;
+                }
+            }
+            fence_proxy_async_smem();  // the TMA will overwrite these bytes later
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xready[s]);
+        }
     } else {
         // ------------------------------------------------------ consumers
         const int g = lane >> 2, t = lane & 3;
-        const int cw = warp & 3;            // 32-column slice of each K block
+        const int cw = warp & 3;                    // 32-column slice of each K block
         const int rbase = (warp >> 2) * (kBN / 2);  // row half
         // x rows of this thread's B fragments: row 8j + pi(g) with
         // pi(g) = (g >> 1) | ((g & 1) << 2) (bank-conflict-free swizzle use)
@@ -162,9 +288,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         for (int ti = 0; ti < my_tiles; ++ti) {
             const int n0 = (tile0 + ti * tstep) * kBN;
             const float *srow = MX ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
-            float acc[C::kRT][MT][4];
+            float acc[kRT][MT][4];
 #pragma unroll
-            for (int rt = 0; rt < C::kRT; ++rt)
+            for (int rt = 0; rt < kRT; ++rt)
 #pragma unroll
                 for (int j = 0; j < MT; ++j)
 #pragma unroll
@@ -177,7 +303,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 const float sblk = s_next;
                 if (!MX && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
                 // every lane waits (acquire); the warp leaves together if any gave up
-                const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
+                const uint32_t par = (it / kStages) & 1;
+                const bool ready =
+                    mbar_wait_bounded(&full[s], par) && (!C::kConv || mbar_wait_bounded(&xready[s], par));
                 if (!__all_sync(0xffffffffu, ready)) {
                     if (lane == 0) {
                         atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
@@ -187,8 +315,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 }
                 const uint8_t *cs = smem + s * C::kStageBytes;
                 const uint8_t *xs = cs + C::kCodeBytes + xpanel * C::kXPanelBytes;
+                const float *xinv = aux + s * (C::kXInvFloats + C::kRowScaleFloats) + cw * C::kXRows;
 
                 uint32_t bx[MT][4];
+                float f0[MT], f1[MT];  // promotion factors of this thread's two C columns
 #pragma unroll
                 for (int j = 0; j < MT; ++j) {
                     const int xr = 8 * j + xrow_base;
@@ -198,36 +328,67 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                     bx[j][1] = v.y;
                     bx[j][2] = v.z;
                     bx[j][3] = v.w;
+                    if (F16) {
+                        const float2 iv = *reinterpret_cast<const float2 *>(xinv + 8 * j + 2 * t);
+                        f0[j] = MX ? iv.x : sblk * iv.x;
+                        f1[j] = MX ? iv.y : sblk * iv.y;
+                    } else {
+                        f0[j] = MX ? 1.0f : sblk;
+                        f1[j] = MX ? 1.0f : sblk;
+                    }
                 }
-                const int grp = (kb0 + kbi) * 4 + cw;  // MX group of this warp's 32 columns
 
 #pragma unroll
-                for (int rt = 0; rt < C::kRT; ++rt) {
+                for (int rt = 0; rt < kRT; ++rt) {
                     const int ra = rbase + rt * 16 + 2 * g, rb = ra + 1;
                     const uint2 qa =
                         *reinterpret_cast<const uint2 *>(cs + ra * 128 + ((cchunk ^ (ra & 7)) << 4) + coff);
                     const uint2 qb =
                         *reinterpret_cast<const uint2 *>(cs + rb * 128 + ((cchunk ^ (rb & 7)) << 4) + coff);
-                    const uint32_t a00 = e4m3x2_to_bf16x2(qa.x, 0x9180u), a01 = e4m3x2_to_bf16x2(qb.x, 0x9180u);
-                    const uint32_t a02 = e4m3x2_to_bf16x2(qa.x, 0xB3A2u), a03 = e4m3x2_to_bf16x2(qb.x, 0xB3A2u);
-                    const uint32_t a10 = e4m3x2_to_bf16x2(qa.y, 0x9180u), a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
-                    const uint32_t a12 = e4m3x2_to_bf16x2(qa.y, 0xB3A2u), a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
-                    float sa = sblk, sb = sblk;
+                    uint32_t a00, a02, a01, a03, a10, a12, a11, a13;
+                    if (F16) {
+                        e4m3x4_to_f16x2x2(qa.x, a00, a02);
+                        e4m3x4_to_f16x2x2(qb.x, a01, a03);
+                        e4m3x4_to_f16x2x2(qa.y, a10, a12);
+                        e4m3x4_to_f16x2x2(qb.y, a11, a13);
+                    } else {
+                        a00 = e4m3x2_to_bf16x2(qa.x, 0x9180u);
+                        a02 = e4m3x2_to_bf16x2(qa.x, 0xB3A2u);
+                        a01 = e4m3x2_to_bf16x2(qb.x, 0x9180u);
+                        a03 = e4m3x2_to_bf16x2(qb.x, 0xB3A2u);
+                        a10 = e4m3x2_to_bf16x2(qa.y, 0x9180u);
+                        a12 = e4m3x2_to_bf16x2(qa.y, 0xB3A2u);
+                        a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
+                        a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
+                    }
+                    float sa = 1.0f, sb = 1.0f;
                     if (MX) {
-                        const int64_t row_a = static_cast<int64_t>(n0) + ra;
-                        const bool gin = grp < groups;
-                        sa = (gin && row_a < n) ? pow2_e8m0(__ldg(e8m0 + row_a * groups + grp)) : 0.0f;
-                        sb = (gin && row_a + 1 < n) ? pow2_e8m0(__ldg(e8m0 + (row_a + 1) * groups + grp)) : 0.0f;
+                        const float2 rs = *reinterpret_cast<const float2 *>(xinv - cw * C::kXRows + C::kXInvFloats +
+                                                                            cw * kBN + ra);
+                        sa = rs.x;
+                        sb = rs.y;
                     }
 #pragma unroll
                     for (int j = 0; j < MT; ++j) {
                         float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
-                        mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
-                        acc[rt][j][0] = fmaf(sa, c[0], acc[rt][j][0]);
-                        acc[rt][j][1] = fmaf(sa, c[1], acc[rt][j][1]);
-                        acc[rt][j][2] = fmaf(sb, c[2], acc[rt][j][2]);
-                        acc[rt][j][3] = fmaf(sb, c[3], acc[rt][j][3]);
+                        if (F16) {
+                            mma_f16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                            mma_f16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                        } else {
+                            mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                            mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                        }
+                        if (MX) {
+                            acc[rt][j][0] = fmaf(sa * f0[j], c[0], acc[rt][j][0]);
+                            acc[rt][j][1] = fmaf(sa * f1[j], c[1], acc[rt][j][1]);
+                            acc[rt][j][2] = fmaf(sb * f0[j], c[2], acc[rt][j][2]);
+                            acc[rt][j][3] = fmaf(sb * f1[j], c[3], acc[rt][j][3]);
+                        } else {
+                            acc[rt][j][0] = fmaf(f0[j], c[0], acc[rt][j][0]);
+                            acc[rt][j][1] = fmaf(f1[j], c[1], acc[rt][j][1]);
+                            acc[rt][j][2] = fmaf(f0[j], c[2], acc[rt][j][2]);
+                            acc[rt][j][3] = fmaf(f1[j], c[3], acc[rt][j][3]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -241,7 +402,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
             for (int p = 0; p < 4; ++p) {
                 if (cw == p) {
 #pragma unroll
-                    for (int rt = 0; rt < C::kRT; ++rt)
+                    for (int rt = 0; rt < kRT; ++rt)
 #pragma unroll
                         for (int j = 0; j < MT; ++j)
 #pragma unroll
@@ -284,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     const int r_end = min(kBN, r_begin + rows_per);
     const int my_rows = max(0, r_end - r_begin);
     const uint32_t red_addr = smem_u32(red);
-    for (int e = threadIdx.x; e < mm * my_rows; e += kThreads) {
+    for (int e = threadIdx.x; e < mm * my_rows; e += C::kThreads) {
         const int mi = e / my_rows;
         const int nl = r_begin + (e - mi * my_rows);
         const int nn = n0 + nl;
@@ -306,11 +467,11 @@ struct Setup {
     int resident[64] = {};
 };
 
-template <int MT, bool MX>
+template <int MT, bool MX, bool F16>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
-    using C = Cfg<MT>;
+    using C = Cfg<MT, MX, F16>;
     constexpr int kBN = C::kBN;
-    auto kern = decode_kernel<MT, MX>;
+    auto kern = decode_kernel<MT, MX, F16>;
     static Setup setup;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -321,7 +482,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
             int blocks = 0;
             if (e == cudaSuccess)
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kThreads, C::kSmemBytes);
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, C::kThreads, C::kSmemBytes);
             setup.err[dev] = e;
             setup.resident[dev] = blocks > 0 ? blocks : 1;
             setup.done[dev] = true;
@@ -343,6 +504,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     const int ntiles = static_cast<int>((a.n + kBN - 1) / kBN);
     const int groups = static_cast<int>((a.k + 31) / 32);
     const int capacity = device_sm_count() * resident;
+    const int e8m0_vec = (groups % 4 == 0 && (reinterpret_cast<uintptr_t>(a.e8m0) & 3) == 0) ? 1 : 0;
     int splits = 1;
     if (ntiles < capacity) {
         splits = capacity / ntiles;
@@ -355,7 +517,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(splits), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
@@ -374,16 +536,17 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, a.e8m0,
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m),
-                              static_cast<int>(a.n), kblocks, groups, splits, ntiles);
+                              static_cast<int>(a.n), kblocks, groups, splits, ntiles, e8m0_vec);
 }
 
 template <bool MX>
 cudaError_t launch_mx(const DecodeArgs &a, cudaStream_t stream) {
+    // f16 operands for m <= 8 (and always for MXFP8), bf16 for wider x
     switch ((a.m + 7) / 8) {
-        case 1: return launch_t<1, MX>(a, stream);
-        case 2: return launch_t<2, MX>(a, stream);
-        case 3: return launch_t<3, MX>(a, stream);
-        case 4: return launch_t<4, MX>(a, stream);
+        case 1: return launch_t<1, MX, true>(a, stream);
+        case 2: return launch_t<2, MX, MX>(a, stream);
+        case 3: return launch_t<3, MX, MX>(a, stream);
+        case 4: return launch_t<4, MX, MX>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
