@@ -61,7 +61,12 @@ struct Cfg {
     // weight rows per CTA: a full block-scale row for m <= 16, half of one for
     // wider x (keeps the accumulators of two CTAs per SM in registers)
     static constexpr int kBN = MT <= 2 ? 128 : 64;
-    static constexpr int kRT = kBN / 32;                // 16-row tiles per consumer warp
+    static constexpr int kRT = kBN / 32;                // 16-row tiles per consumer warp (split layout)
+    // m <= 16: each consumer warp owns one 16-row tile across the whole K
+    // block, so row sums never cross warps (no reduction epilogue); wider x
+    // splits the K block over 4 warps to share each B fragment over 2 row
+    // tiles, and reduces across warps once per row tile.
+    static constexpr bool kFullRow = MT <= 2;
     static constexpr int kStages = 4;
     static constexpr bool kConv = F16 || MX;            // converter warp present
     static constexpr int kConvWarps = kConv ? 1 : 0;
@@ -270,6 +275,127 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
             fence_proxy_async_smem();  // the TMA will overwrite these bytes later
             __syncwarp();
             if (lane == 0) mbar_arrive(&xready[s]);
+        }
+    } else if (C::kFullRow) {
+        // ------------------------------------------- consumers, full rows
+        const int g = lane >> 2, t = lane & 3;
+        const int ra = warp * 16 + 2 * g, rb = ra + 1;  // this thread's two weight rows
+        // x rows of this thread's B fragments: row 8j + pi(g) with
+        // pi(g) = (g >> 1) | ((g & 1) << 2) (bank-conflict-free swizzle use)
+        const int xrow_base = (g >> 1) | ((g & 1) << 2);
+        const int coff = (t & 1) * 8;
+        for (int ti = 0; ti < my_tiles; ++ti) {
+            const int n0 = (tile0 + ti * tstep) * kBN;
+            const float *srow = MX ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
+            float acc[MT][4];
+#pragma unroll
+            for (int j = 0; j < MT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
+            float s_next = MX ? 0.0f : __ldg(srow);
+            bool failed = false;
+            for (int kbi = 0; kbi < nkb; ++kbi) {
+                const int it = ti * nkb + kbi;
+                const int s = it % kStages;
+                const float sblk = s_next;
+                if (!MX && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
+                const uint32_t par = (it / kStages) & 1;
+                const bool ready =
+                    mbar_wait_bounded(&full[s], par) && (!C::kConv || mbar_wait_bounded(&xready[s], par));
+                if (!__all_sync(0xffffffffu, ready)) {
+                    if (lane == 0) atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
+                    failed = true;
+                    break;
+                }
+                const uint8_t *cs = smem + s * C::kStageBytes;
+                const uint8_t *xbase = cs + C::kCodeBytes;
+                const float *xinv = aux + s * (C::kXInvFloats + C::kRowScaleFloats);
+#pragma unroll
+                for (int sl = 0; sl < 4; ++sl) {
+                    const uint8_t *xs = xbase + (sl >> 1) * C::kXPanelBytes;
+                    const int xchunk = 4 * (sl & 1) + t;
+                    uint32_t bx[MT][4];
+                    float f0[MT], f1[MT];
+#pragma unroll
+                    for (int j = 0; j < MT; ++j) {
+                        const int xr = 8 * j + xrow_base;
+                        const uint4 v =
+                            *reinterpret_cast<const uint4 *>(xs + xr * 128 + ((xchunk ^ (xr & 7)) << 4));
+                        bx[j][0] = v.x;
+                        bx[j][1] = v.y;
+                        bx[j][2] = v.z;
+                        bx[j][3] = v.w;
+                        if (F16) {
+                            const float2 iv =
+                                *reinterpret_cast<const float2 *>(xinv + sl * C::kXRows + 8 * j + 2 * t);
+                            f0[j] = MX ? iv.x : sblk * iv.x;
+                            f1[j] = MX ? iv.y : sblk * iv.y;
+                        } else {
+                            f0[j] = MX ? 1.0f : sblk;
+                            f1[j] = MX ? 1.0f : sblk;
+                        }
+                    }
+                    const int cchunk = 2 * sl + (t >> 1);
+                    const uint2 qa =
+                        *reinterpret_cast<const uint2 *>(cs + ra * 128 + ((cchunk ^ (ra & 7)) << 4) + coff);
+                    const uint2 qb =
+                        *reinterpret_cast<const uint2 *>(cs + rb * 128 + ((cchunk ^ (rb & 7)) << 4) + coff);
+                    uint32_t a00, a02, a01, a03, a10, a12, a11, a13;
+                    if (F16) {
+                        e4m3x4_to_f16x2x2(qa.x, a00, a02);
+                        e4m3x4_to_f16x2x2(qb.x, a01, a03);
+                        e4m3x4_to_f16x2x2(qa.y, a10, a12);
+                        e4m3x4_to_f16x2x2(qb.y, a11, a13);
+                    } else {
+                        a00 = e4m3x2_to_bf16x2(qa.x, 0x9180u);
+                        a02 = e4m3x2_to_bf16x2(qa.x, 0xB3A2u);
+                        a01 = e4m3x2_to_bf16x2(qb.x, 0x9180u);
+                        a03 = e4m3x2_to_bf16x2(qb.x, 0xB3A2u);
+                        a10 = e4m3x2_to_bf16x2(qa.y, 0x9180u);
+                        a12 = e4m3x2_to_bf16x2(qa.y, 0xB3A2u);
+                        a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
+                        a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
+                    }
+                    float sa = 1.0f, sb = 1.0f;
+                    if (MX) {
+                        const float2 rsc = *reinterpret_cast<const float2 *>(xinv + C::kXInvFloats + sl * kBN + ra);
+                        sa = rsc.x;
+                        sb = rsc.y;
+                    }
+#pragma unroll
+                    for (int j = 0; j < MT; ++j) {
+                        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        if (F16) {
+                            mma_f16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                            mma_f16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                        } else {
+                            mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                            mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                        }
+                        acc[j][0] = fmaf(sa * f0[j], c[0], acc[j][0]);
+                        acc[j][1] = fmaf(sa * f1[j], c[1], acc[j][1]);
+                        acc[j][2] = fmaf(sb * f0[j], c[2], acc[j][2]);
+                        acc[j][3] = fmaf(sb * f1[j], c[3], acc[j][3]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            if (failed) break;
+            // acc[j][q] is y[m = 8j + t + 4(q&1)][n_local = ra + (q>>1)]
+#pragma unroll
+            for (int j = 0; j < MT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int mi = 8 * j + t + 4 * (q & 1);
+                    const int nl = ra + (q >> 1);
+                    if (splits == 1) {
+                        if (mi < m && n0 + nl < n)
+                            y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(acc[j][q]);
+                    } else {
+                        red[nl * C::kRedStride + mi] = acc[j][q];
+                    }
+                }
         }
     } else {
         // ------------------------------------------------------ consumers

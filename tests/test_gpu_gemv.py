@@ -197,6 +197,33 @@ def test_mx_full_size(pkg):
         check_mx_gemv(y, bits(x.cpu()), rows, oc, oe)
 
 
+@pytest.mark.parametrize("m", [1, 4, 8, 16])
+@pytest.mark.parametrize("case", ["wide_range", "tiny", "huge", "single_spike"])
+def test_x_dynamic_range(pkg, m, case):
+    """Activations with extreme ranges inside one 32-column slice: the f16
+    operand path rescales each slice by a power of two (exact for values
+    within 2^-31 of the slice maximum), so results stay within tolerance."""
+    w = inputs.gaussian_bf16((384, 1024), 0.02, 77)
+    oc, os_ = oracle.block_quantize(bits(w))
+    g = torch.Generator().manual_seed(5)
+    base = torch.randn((m, 1024), generator=g)
+    if case == "wide_range":
+        expo = torch.randint(-30, 30, (m, 1024), generator=g).to(torch.float32)
+        x = base * torch.pow(10.0, expo)
+    elif case == "tiny":
+        x = base * 1e-35
+    elif case == "huge":
+        x = base * 1e30
+    else:
+        x = base.clone()
+        x[:, 37] = 3e20
+    x = x.to(torch.bfloat16)
+    for path in (0, PATH_GENERIC):
+        y = pkg.gemv(x.to(DEV), to_dev_bits(oc), torch.from_numpy(os_).to(DEV), path=path)
+        rows_q = {rb: (oc[rb * 128:rb * 128 + 128], os_[rb]) for rb in range(3)}
+        check_block_gemv(y, bits(x), rows_q)
+
+
 def test_repeat_is_deterministic(pkg):
     w = inputs.rotation_weight(1, 1, device=DEV)
     codes, scales = pkg.quantize(w)
