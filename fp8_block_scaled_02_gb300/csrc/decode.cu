@@ -76,7 +76,7 @@ struct Cfg {
     static constexpr int kXPanelBytes = kXRows * 128;   // 64 columns of each row
     static constexpr int kStageBytes = kCodeBytes + 2 * kXPanelBytes;
     static constexpr int kXInvFloats = 4 * kXRows;      // per stage: [slice][row]
-    static constexpr int kRowScaleFloats = MX ? 4 * kBN : 0;  // per stage: [slice][weight row]
+    static constexpr int kRowScaleFloats = (MX && MT > 2) ? 4 * kBN : 0;  // per stage: [slice][weight row]
     static constexpr int kAuxBytes = (kXInvFloats + kRowScaleFloats) * 4;
     static constexpr int kRedStride = kXRows + 1;       // padded fp32 row
     static constexpr int kRedBytes = kBN * kRedStride * 4;
@@ -220,30 +220,36 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
         // ------------------------------------------------------ x converter
         const int clane = (warp - kWarpConv0) * 32 + lane;
         constexpr int kConvLanes = C::kConvWarps * 32;
+        // e8m0 bytes of this lane's rows for stage `it` (4 groups per row),
+        // fetched one stage ahead so their latency hides behind the ring
+        constexpr bool kStageE8m0 = MX && !C::kFullRow;  // full-row consumers fetch their own
+        constexpr int kRowsPerLane = kStageE8m0 ? kBN / kConvLanes : 1;
+        auto load_e8m0 = [&](int it, uint32_t (&ev)[kRowsPerLane]) {
+            const int ti = it / nkb;
+            const int n0 = (tile0 + ti * tstep) * kBN;
+            const int g0 = (kb0 + (it - ti * nkb)) * 4;
+#pragma unroll
+            for (int i = 0; i < kRowsPerLane; ++i) {
+                const int64_t row = static_cast<int64_t>(n0) + clane + i * kConvLanes;
+                uint32_t w = 0;
+                if (row < n) {
+                    const uint8_t *p = e8m0 + row * groups + g0;
+                    if (e8m0_vec) {
+                        w = __ldg(reinterpret_cast<const uint32_t *>(p));
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (g0 + q < groups) w |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
+                    }
+                }
+                ev[i] = w;
+            }
+        };
+        uint32_t ev[kRowsPerLane], ev_next[kRowsPerLane];
+        if (kStageE8m0 && total > 0) load_e8m0(0, ev);
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages;
-            uint32_t ev[MX ? kBN / kConvLanes : 1];  // e8m0 of this lane's rows, 4 groups each
-            if (MX) {
-                const int ti = it / nkb;
-                const int n0 = (tile0 + ti * tstep) * kBN;
-                const int g0 = (kb0 + (it - ti * nkb)) * 4;
-#pragma unroll
-                for (int i = 0; i < (MX ? kBN / kConvLanes : 1); ++i) {
-                    const int64_t row = static_cast<int64_t>(n0) + clane + i * kConvLanes;
-                    uint32_t w = 0;
-                    if (row < n) {
-                        const uint8_t *p = e8m0 + row * groups + g0;
-                        if (e8m0_vec) {
-                            w = __ldg(reinterpret_cast<const uint32_t *>(p));
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                if (g0 + q < groups) w |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
-                        }
-                    }
-                    ev[i] = w;
-                }
-            }
+            if (kStageE8m0 && it + 1 < total) load_e8m0(it + 1, ev_next);
             const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
             if (!__all_sync(0xffffffffu, ready)) {
                 if (lane == 0) {
@@ -258,13 +264,13 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
                 for (int u = clane; u < 4 * C::kXRows; u += kConvLanes)
                     convert_x_slice<C::kXPanelBytes, C::kXRows>(xs, xinv, u >> 2, u & 3);
             }
-            if (MX) {
+            if (kStageE8m0) {
                 const int ti = it / nkb;
                 const int n0 = (tile0 + ti * tstep) * kBN;
                 const int g0 = (kb0 + (it - ti * nkb)) * 4;
                 float *rs = xinv + C::kXInvFloats;
 #pragma unroll
-                for (int i = 0; i < (MX ? kBN / kConvLanes : 1); ++i) {
+                for (int i = 0; i < kRowsPerLane; ++i) {
                     const int r = clane + i * kConvLanes;
                     const bool rin = n0 + r < n;
 #pragma unroll
@@ -275,6 +281,10 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
             fence_proxy_async_smem();  // the TMA will overwrite these bytes later
             __syncwarp();
             if (lane == 0) mbar_arrive(&xready[s]);
+            if (kStageE8m0) {
+#pragma unroll
+                for (int i = 0; i < kRowsPerLane; ++i) ev[i] = ev_next[i];
+            }
         }
     } else if (C::kFullRow) {
         // ------------------------------------------- consumers, full rows
@@ -293,12 +303,35 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
             float s_next = MX ? 0.0f : __ldg(srow);
+            // MX: lane l < 16 holds the e8m0 word (4 groups of this K block) of
+            // weight row 16*warp + l, fetched one K block ahead
+            auto load_e8m0_word = [&](int kbi) -> uint32_t {
+                const int64_t row = static_cast<int64_t>(n0) + warp * 16 + lane;
+                const int g0 = (kb0 + kbi) * 4;
+                uint32_t w = 0;
+                if (lane < 16 && row < n) {
+                    const uint8_t *p = e8m0 + row * groups + g0;
+                    if (e8m0_vec) {
+                        w = __ldg(reinterpret_cast<const uint32_t *>(p));
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (g0 + q < groups) w |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
+                    }
+                }
+                return w;
+            };
+            uint32_t e_next = MX ? load_e8m0_word(0) : 0u;
             bool failed = false;
             for (int kbi = 0; kbi < nkb; ++kbi) {
                 const int it = ti * nkb + kbi;
                 const int s = it % kStages;
                 const float sblk = s_next;
                 if (!MX && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
+                const uint32_t e_cur = e_next;
+                if (MX && kbi + 1 < nkb) e_next = load_e8m0_word(kbi + 1);
+                const uint32_t ewa = MX ? __shfl_sync(0xffffffffu, e_cur, 2 * g) : 0u;
+                const uint32_t ewb = MX ? __shfl_sync(0xffffffffu, e_cur, 2 * g + 1) : 0u;
                 const uint32_t par = (it / kStages) & 1;
                 const bool ready =
                     mbar_wait_bounded(&full[s], par) && (!C::kConv || mbar_wait_bounded(&xready[s], par));
@@ -358,9 +391,8 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
                     }
                     float sa = 1.0f, sb = 1.0f;
                     if (MX) {
-                        const float2 rsc = *reinterpret_cast<const float2 *>(xinv + C::kXInvFloats + sl * kBN + ra);
-                        sa = rsc.x;
-                        sb = rsc.y;
+                        sa = pow2_e8m0((ewa >> (8 * sl)) & 0xFFu);
+                        sb = pow2_e8m0((ewb >> (8 * sl)) & 0xFFu);
                     }
 #pragma unroll
                     for (int j = 0; j < MT; ++j) {
