@@ -1,28 +1,29 @@
 // prefill.cu -- block-FP8 W8A16 GEMM for prefill-shaped batches on the
 // 5th-generation tensor cores (tcgen05), y[M, N] = x[M, K] . dequant(W)^T.
 //
-// Design (sm_103a, one CTA per 128 weight rows x 128 rows of x):
-//  * Weights are the MMA's A operand and live in tensor memory: four
+// Design (sm_103a, one CTA per 128 weight rows x 128 rows of x, 18 warps):
+//  * Weights are the MMA's A operand and live in tensor memory: eight
 //    "decoder" warps stream their rows' e4m3 codes from global memory (each
-//    thread owns one weight row = one TMEM lane), convert them exactly to
-//    bf16 pairs in registers and tcgen05.st them into a double-buffered
-//    64-column A slot (128 K of bf16 per K block).  The decoded weight never
-//    touches shared memory or HBM.
+//    thread owns one weight row = one TMEM lane and one 64-wide K half,
+//    loading two K blocks ahead), convert them exactly to bf16 pairs in
+//    registers and tcgen05.st them into a double-buffered 64-column A slot
+//    (128 K of bf16 per K block).  The decoded weight never touches shared
+//    memory or HBM.
 //  * x is the B operand: one producer thread brings each K block's
 //    [128 rows x 128 K] bf16 tile in with 2-D TMA (128-byte swizzle, two
 //    64-column panels) into a 4-stage shared-memory ring.
 //  * One thread issues tcgen05.mma.kind::f16 (bf16 x bf16 -> fp32, M=128,
 //    N=128, K=16; 8 per K block).  Each K block accumulates from zero into
 //    one of two 128-column TMEM accumulators.
-//  * Four epilogue warps read each finished K-block accumulator with
-//    tcgen05.ld, multiply it by that block's fp32 scale and add it into
-//    128 fp32 registers per thread ("promotion"), so the scale is applied
-//    once per 128-wide K block to an fp32 partial and never folded into a
-//    rounded bf16 weight.  At the end each thread holds its weight row's
-//    128 outputs and stores them as bf16.
-//  * mbarriers: x_full/x_empty (TMA ring), a_full/a_empty (TMEM A slots),
-//    d_full/d_empty (TMEM accumulators).  tcgen05.commit signals MMA
-//    completion.  Every wait is bounded; a kernel that gives up sets an error
+//  * Eight epilogue warps (two per TMEM lane quarter, one per 64-column
+//    half) read each finished K-block accumulator with tcgen05.ld, multiply
+//    it by that block's fp32 scale and add it into 64 fp32 registers per
+//    thread ("promotion"), so the scale is applied once per 128-wide K
+//    block to an fp32 partial and never folded into a rounded bf16 weight.
+//    At the end each thread stores its weight row's outputs as bf16.
+//  * mbarriers: x_full (TMA ring), a_full (TMEM A slots), d_empty (TMEM
+//    accumulators), and a ring of "MMA done" barriers, one tcgen05.commit
+//    per K block, that frees x stages, A slots and accumulators alike.  Every wait is bounded; a kernel that gives up sets an error
 //    word, drains what it issued and still frees its TMEM.
 #include "common.cuh"
 #include "internal.h"
@@ -39,6 +40,8 @@ constexpr int kTileW = 128;       // weight rows per CTA (= one scale row block,
 constexpr int kTileX = 128;       // x rows per CTA (= MMA N)
 constexpr int kKB = 128;          // K per block
 constexpr int kXStages = 4;
+constexpr int kRing = 4;          // MMA-completion barriers (>= x stages, > A slots, > accumulators)
+static_assert(kXStages <= kRing, "the x producer waits on a block kXStages back");
 constexpr int kXPanel = kTileX * 128;     // 64 bf16 per row, 16 KB
 constexpr int kXStage = 2 * kXPanel;      // 32 KB
 constexpr int kTmemCols = 512;
@@ -48,9 +51,11 @@ constexpr int kColD = 128;                // accumulators: [128, 256) and [256, 
 // warp roles
 constexpr int kWarpMma = 0;       // also allocates / frees TMEM
 constexpr int kWarpTma = 1;
-constexpr int kWarpDec0 = 2;      // 2..5 decoders (lane quarter = warp % 4)
-constexpr int kWarpEpi0 = 6;      // 6..9 epilogue (lane quarter = warp % 4)
-constexpr int kThreads = 10 * 32;
+constexpr int kWarpDec0 = 2;      // 2..9 decoders: lane quarter warp % 4, K half (warp - 2) / 4
+constexpr int kNumDec = 8;
+constexpr int kWarpEpi0 = kWarpDec0 + kNumDec;  // 10..17 epilogue: lane quarter warp % 4, column half (warp - 10) / 4
+constexpr int kNumEpi = 8;
+constexpr int kThreads = (kWarpEpi0 + kNumEpi) * 32;
 constexpr int kSmemBytes = 1024 + kXStages * kXStage + 256;
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
@@ -112,6 +117,15 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         : "memory");
 }
 
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -134,29 +148,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kXStages * kXStage);
-    uint64_t *x_full = bars;                 // [4]
-    uint64_t *x_empty = bars + 4;            // [4]
-    uint64_t *a_full = bars + 8;             // [2]
-    uint64_t *a_empty = bars + 10;           // [2]
-    uint64_t *d_full = bars + 12;            // [2]
-    uint64_t *d_empty = bars + 14;           // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    int *s_fail = reinterpret_cast<int *>(bars + 17);
+    // done[kb % kRing] completes when the MMAs of K block kb have finished
+    // (one tcgen05.commit per block); the x producer, the decoders and the
+    // epilogue all wait on it, each before its ring slot could be reused
+    uint64_t *x_full = bars;                 // [kXStages]
+    uint64_t *done = bars + kXStages;        // [kRing]
+    uint64_t *a_full = done + kRing;         // [2]
+    uint64_t *d_empty = a_full + 2;          // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_empty + 2);
+    int *s_fail = reinterpret_cast<int *>(d_empty + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileW;
     const int m0 = blockIdx.y * kTileX;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kXStages; ++i) {
-            mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], 1);
-        }
+        for (int i = 0; i < kXStages; ++i) mbar_init(&x_full[i], 1);
+        for (int i = 0; i < kRing; ++i) mbar_init(&done[i], 1);  // tcgen05.commit
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&a_full[i], 4);   // one arrival per decoder warp
-            mbar_init(&a_empty[i], 1);  // tcgen05.commit
-            mbar_init(&d_full[i], 1);   // tcgen05.commit
-            mbar_init(&d_empty[i], 4);  // one arrival per epilogue warp
+            mbar_init(&a_full[i], kNumDec);   // one arrival per decoder warp
+            mbar_init(&d_empty[i], kNumEpi);  // one arrival per epilogue warp
         }
         *s_fail = 0;
         fence_mbarrier_init();
@@ -189,20 +200,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     break;
                 }
                 tc_fence_after();
-                const uint32_t xbase = smem_u32(smem + xs * kXStage);
+                // descriptor of the stage's first 16-column slice; the others
+                // are 32 bytes (2 in address/16 units) apart within a 64-column
+                // panel, and panels are kXPanel bytes apart
+                const uint64_t desc0 = sw128_desc(smem_u32(smem + xs * kXStage));
+                const uint32_t d_tmem = tmem + kColD + db * 128;
+                const uint32_t a_tmem = tmem + kColA + as * 64;
 #pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk) {
-                    const uint32_t b_addr = xbase + (kk >> 2) * kXPanel + (kk & 3) * 32;
-                    tc_mma(tmem + kColD + db * 128, tmem + kColA + as * 64 + kk * 8, sw128_desc(b_addr),
+                for (int kk = 0; kk < kKB / 16; ++kk)
+                    tc_mma(d_tmem, a_tmem + kk * 8, desc0 + (kk >> 2) * (kXPanel >> 4) + (kk & 3) * 2,
                            kk > 0 ? 1u : 0u);
-                }
-                tc_commit(&x_empty[xs]);
-                tc_commit(&a_empty[as]);
-                tc_commit(&d_full[db]);
+                tc_commit(&done[kb % kRing]);
                 issued = kb + 1;
             }
             // drain: wait for the last committed block before TMEM can be freed
-            if (issued > 0 && !mbar_wait_bounded(&d_full[(issued - 1) & 1], ((issued - 1) >> 1) & 1))
+            if (issued > 0 && !mbar_wait_bounded(&done[(issued - 1) % kRing], ((issued - 1) / kRing) & 1))
                 fail(ERRBIT_MMA_WAIT);
         }
         __syncwarp();
@@ -212,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             int issued = 0;
             for (int kb = 0; kb < kblocks; ++kb) {
                 const int xs = kb % kXStages;
-                if (kb >= kXStages && !mbar_wait_bounded(&x_empty[xs], ((kb / kXStages) - 1) & 1)) {
+                if (kb >= kXStages && !mbar_wait_bounded(&done[(kb - kXStages) % kRing], ((kb - kXStages) / kRing) & 1)) {
                     fail(ERRBIT_EMPTY_WAIT);
                     break;
                 }
@@ -230,92 +242,98 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         __syncwarp();
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------------------ decoders
+        // thread = one weight row (its TMEM lane); this warp converts the K
+        // half kh (64 codes) of its rows for every K block, two blocks ahead
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int kh = (warp - kWarpDec0) >> 2;
         const int row = n0 + q * 32 + lane;
         const bool row_ok = row < n;
-        const uint8_t *rp = codes + static_cast<int64_t>(row_ok ? row : 0) * k;
-        uint4 cur[8], nxt[8];
+        const uint8_t *rp = codes + static_cast<int64_t>(row_ok ? row : 0) * k + kh * 64;
+        auto load4 = [&](int kb, uint4 (&v)[4]) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int col = j * 16;
-            cur[j] = (row_ok && col < k) ? ld_codes16(rp + col) : make_uint4(0, 0, 0, 0);
-        }
+            for (int j = 0; j < 4; ++j) {
+                const int col = kb * kKB + kh * 64 + j * 16;
+                v[j] = (kb < kblocks && row_ok && col < k) ? ld_codes16(rp + kb * kKB + j * 16) : make_uint4(0, 0, 0, 0);
+            }
+        };
+        uint4 c0[4], c1[4], c2[4];
+        load4(0, c0);
+        load4(1, c1);
         for (int kb = 0; kb < kblocks; ++kb) {
             const int as = kb & 1;
-            // prefetch the next K block's codes while this one is converted
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int col = (kb + 1) * kKB + j * 16;
-                nxt[j] = (kb + 1 < kblocks && row_ok && col < k) ? ld_codes16(rp + col) : make_uint4(0, 0, 0, 0);
-            }
-            bool ok = kb < 2 || mbar_wait_bounded(&a_empty[as], ((kb >> 1) - 1) & 1);
+            load4(kb + 2, c2);  // in flight while this block is converted
+            bool ok = kb < 2 || mbar_wait_bounded(&done[(kb - 2) % kRing], ((kb - 2) / kRing) & 1);
             if (!__all_sync(0xffffffffu, ok) || *reinterpret_cast<volatile int *>(s_fail)) {
                 if (lane == 0) fail(ERRBIT_EMPTY_WAIT);
                 break;
             }
             tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kColA + as * 64;
+            uint32_t v[32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t v[32];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 c = cur[4 * h + j];
-                    v[8 * j + 0] = e4m3x2_to_bf16x2(c.x, 0x9180u);
-                    v[8 * j + 1] = e4m3x2_to_bf16x2(c.x, 0xB3A2u);
-                    v[8 * j + 2] = e4m3x2_to_bf16x2(c.y, 0x9180u);
-                    v[8 * j + 3] = e4m3x2_to_bf16x2(c.y, 0xB3A2u);
-                    v[8 * j + 4] = e4m3x2_to_bf16x2(c.z, 0x9180u);
-                    v[8 * j + 5] = e4m3x2_to_bf16x2(c.z, 0xB3A2u);
-                    v[8 * j + 6] = e4m3x2_to_bf16x2(c.w, 0x9180u);
-                    v[8 * j + 7] = e4m3x2_to_bf16x2(c.w, 0xB3A2u);
-                }
-                tc_st32(taddr + 32 * h, v);
+            for (int j = 0; j < 4; ++j) {
+                const uint4 c = c0[j];
+                v[8 * j + 0] = e4m3x2_to_bf16x2(c.x, 0x9180u);
+                v[8 * j + 1] = e4m3x2_to_bf16x2(c.x, 0xB3A2u);
+                v[8 * j + 2] = e4m3x2_to_bf16x2(c.y, 0x9180u);
+                v[8 * j + 3] = e4m3x2_to_bf16x2(c.y, 0xB3A2u);
+                v[8 * j + 4] = e4m3x2_to_bf16x2(c.z, 0x9180u);
+                v[8 * j + 5] = e4m3x2_to_bf16x2(c.z, 0xB3A2u);
+                v[8 * j + 6] = e4m3x2_to_bf16x2(c.w, 0x9180u);
+                v[8 * j + 7] = e4m3x2_to_bf16x2(c.w, 0xB3A2u);
             }
+            tc_st32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColA + as * 64 + kh * 32, v);
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[as]);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+            for (int j = 0; j < 4; ++j) {
+                c0[j] = c1[j];
+                c1[j] = c2[j];
+            }
         }
     } else {
         // ------------------------------------------------------ epilogue
+        // thread = one weight row (TMEM lane); this warp promotes the 64
+        // accumulator columns (rows of x) of half ch
         const int q = warp & 3;
-        float acc[kTileX];
+        const int ch = (warp - kWarpEpi0) >> 2;
+        float acc[kTileX / 2];
 #pragma unroll
-        for (int i = 0; i < kTileX; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < kTileX / 2; ++i) acc[i] = 0.0f;
         const float *srow = scales + static_cast<int64_t>(blockIdx.x) * kblocks;
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
             const int db = kb & 1;
             const float s = __ldg(srow + kb);
-            ok = mbar_wait_bounded(&d_full[db], (kb >> 1) & 1);
+            ok = mbar_wait_bounded(&done[kb % kRing], (kb / kRing) & 1);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) fail(ERRBIT_FULL_WAIT);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kColD + db * 128;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kColD + db * 128 + ch * 64;
 #pragma unroll
-            for (int c = 0; c < kTileX / 32; ++c) {
-                uint32_t v[32];
-                tc_ld32(taddr + 32 * c, v);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[16];
+                tc_ld16(taddr + 16 * c, v);
                 tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[32 * c + i] = fmaf(s, __uint_as_float(v[i]), acc[32 * c + i]);
+                for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(s, __uint_as_float(v[i]), acc[16 * c + i]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&d_empty[db]);
         }
-        // thread = weight row, acc[i] = y[m0 + i][row]
+        // thread = weight row, acc[i] = y[m0 + 64 ch + i][row]
         const int row = n0 + q * 32 + lane;
         if (ok && row < n) {
 #pragma unroll
-            for (int i = 0; i < kTileX; ++i)
-                if (m0 + i < m) y[static_cast<int64_t>(m0 + i) * n + row] = __float2bfloat16_rn(acc[i]);
+            for (int i = 0; i < kTileX / 2; ++i) {
+                const int mi = m0 + ch * 64 + i;
+                if (mi < m) y[static_cast<int64_t>(mi) * n + row] = __float2bfloat16_rn(acc[i]);
+            }
         }
     }
 
