@@ -2,8 +2,8 @@
 //
 //  * block_quantize_kernel: bf16 [n,k] -> e4m3 codes + one fp32 scale per
 //    128x128 tile (Atlas spark_model/weight_map/quantize_fp8_bs.rs: one CTA
-//    per tile, grid [k_blocks, n_blocks], 256 threads; FreeToken PR #636
-//    per_block_quant_fp8).  Each thread keeps its 64 elements in registers
+//    per tile, grid [k_blocks, n_blocks]; FreeToken PR #636
+//    per_block_quant_fp8).  Each thread keeps its 32 elements in registers
 //    between the amax reduction and the encode, so the tile is read from HBM
 //    exactly once.
 //  * mx_quantize_kernel: bf16 [n,k] -> e4m3 codes + one e8m0 exponent per 32
@@ -59,14 +59,15 @@ __device__ __forceinline__ uint2 encode8_mul(const uint4 v, float f) {
     return make_uint2(out[0], out[1]);
 }
 
+// max |w| over 8 bf16 values, folded into m.  Magnitudes of finite bf16
+// values order like their 15-bit patterns, so the maximum is taken on the
+// packed integer halves.
 __device__ __forceinline__ float absmax8(const uint4 v, float m) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        m = fmaxf(m, fabsf(bf16lo_to_f32(w[i])));
-        m = fmaxf(m, fabsf(bf16hi_to_f32(w[i])));
-    }
-    return m;
+    uint32_t mx = max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    mx = max_u16x2(mx, v.z & 0x7FFF7FFFu);
+    mx = max_u16x2(mx, v.w & 0x7FFF7FFFu);
+    const uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);
+    return fmaxf(m, __uint_as_float(m16 << 16));
 }
 
 // MX exponent from the group amax (a non-negative bf16 value held in fp32):
@@ -91,40 +92,47 @@ __device__ __forceinline__ float mx_inv_scale(int E) {
 }
 
 // ------------------------------------------------------------ block, fast
-__global__ void __launch_bounds__(256) block_quantize_kernel(const __nv_bfloat16 *__restrict__ w,
-                                                             uint8_t *__restrict__ codes,
-                                                             float *__restrict__ scales,
-                                                             int64_t n, int64_t k) {
-    __shared__ float warp_amax[8];
+// 512 threads per 128x128 tile: thread t owns the 16-byte chunk t % 16 of
+// rows t / 16 + 32 i (i < 4), i.e. 32 elements kept in registers between the
+// tile-amax reduction and the encode; at two to four CTAs per SM the load
+// phase of one tile overlaps the divide/encode phase of another.
+constexpr int kQThreads = 512;
+constexpr int kQRows = kQThreads / 16;  // rows covered per pass
+
+__global__ void __launch_bounds__(kQThreads, 2) block_quantize_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                    uint8_t *__restrict__ codes,
+                                                                    float *__restrict__ scales,
+                                                                    int64_t n, int64_t k) {
+    __shared__ float warp_amax[kQThreads / 32];
     const int bk = blockIdx.x, bn = blockIdx.y;
     const int chunk = threadIdx.x & 15;  // 8 bf16 = 16 bytes
-    const int rg = threadIdx.x >> 4;     // rows rg, rg+16, ..., rg+112
+    const int rg = threadIdx.x >> 4;     // rows rg, rg + 32, rg + 64, rg + 96
     const int64_t col = static_cast<int64_t>(bk) * kTile + chunk * 8;
     const bool col_ok = col < k;  // k % 8 == 0: a chunk is all in or all out
 
-    uint4 v[8];
+    uint4 v[kTile / kQRows];
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t row = static_cast<int64_t>(bn) * kTile + rg + 16 * i;
+    for (int i = 0; i < kTile / kQRows; ++i) {
+        const int64_t row = static_cast<int64_t>(bn) * kTile + rg + kQRows * i;
         if (col_ok && row < n)
             v[i] = ld_nc_v4(w + row * k + col);
         else
             v[i] = make_uint4(0, 0, 0, 0);  // padding: |0| never raises amax
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = absmax8(v[i], amax);
+    for (int i = 0; i < kTile / kQRows; ++i) amax = absmax8(v[i], amax);
     amax = warp_max(amax);
     if ((threadIdx.x & 31) == 0) warp_amax[threadIdx.x >> 5] = amax;
     __syncthreads();
     amax = warp_amax[0];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_amax[i]);
+    for (int i = 1; i < kQThreads / 32; ++i) amax = fmaxf(amax, warp_amax[i]);
     const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
     if (threadIdx.x == 0) scales[static_cast<int64_t>(bn) * gridDim.x + bk] = s;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int64_t row = static_cast<int64_t>(bn) * kTile + rg + 16 * i;
+    for (int i = 0; i < kTile / kQRows; ++i) {
+        const int64_t row = static_cast<int64_t>(bn) * kTile + rg + kQRows * i;
         if (col_ok && row < n) {
             const uint2 c = encode8_div(v[i], s);
             *reinterpret_cast<uint2 *>(codes + row * k + col) = c;
@@ -230,8 +238,8 @@ cudaError_t launch_block_quantize(const void *w, int64_t n, int64_t k, uint8_t *
     const dim3 grid(static_cast<unsigned>((k + kTile - 1) / kTile),
                     static_cast<unsigned>((n + kTile - 1) / kTile));
     if (vector_ok)
-        block_quantize_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), codes,
-                                                        scales, n, k);
+        block_quantize_kernel<<<grid, kQThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), codes,
+                                                              scales, n, k);
     else
         block_quantize_generic_kernel<<<grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(w), codes, scales, n, k);
