@@ -45,6 +45,38 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = {
+    "decode_kernel": ["decode.cu", "common.cuh"],
+    "prefill_kernel": ["prefill.cu", "common.cuh"],
+    "block_quantize_kernel": ["quantize.cu", "common.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    base = kernel.split("<")[0]
+    for f in KERNEL_SOURCES.get(base, []):
+        with open(os.path.join(ROOT, "fp8_block_scaled_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+    the committed ncu capture in profiles/traffic.json, or None if the kernel's
+    source has changed since those counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d[f"{kernel} {workload}"]
+        if e["source_sha256"] != kernel_source_hash(kernel):
+            return None
+        return int(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def tensor_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -161,7 +193,7 @@ def lm_head_workload(torch, fp8bs, inputs, dev):
     cfg = {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call at each "
                        "of M=1,4,8,16 per step", "n": n, "k": k, "ms": ms,
            "l2": "inputs larger than L2 (623 MB of codes per call)"}
-    return dict(calls=calls, xs=xs, ys=ys, cfg=cfg, dominant=("decode_kernel<1,false>", [0, 1, 2]),
+    return dict(calls=calls, xs=xs, ys=ys, cfg=cfg, dominant=("decode_kernel<1,false,true>", [0, 1, 2]),
                 codes=codes, scales=scales, n=n, k=k, mx=False)
 
 
@@ -476,7 +508,7 @@ def main():
     else:
         roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
-                    "traffic": None}
+                    "traffic": measured_traffic(dom_name, args.workload)}
 
     e2e = None
     if args.workload == "lm_head":
