@@ -146,6 +146,8 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t rank
     return r;
 }
 
+// Volatile keeps it after the cluster barrier; several can still be in
+// flight when the caller issues them before using any result.
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");

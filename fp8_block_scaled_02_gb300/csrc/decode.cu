@@ -602,15 +602,24 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
     const int r_begin = rank * rows_per;
     const int r_end = min(kBN, r_begin + rows_per);
     const int my_rows = max(0, r_end - r_begin);
-    const uint32_t red_addr = smem_u32(red);
+    // all of a thread's remote loads are issued before the first add, so a
+    // cluster of S costs one DSMEM round trip rather than S
+    uint32_t peer_red[kMaxSplit];
+#pragma unroll
+    for (int q = 0; q < kMaxSplit; ++q) peer_red[q] = q < splits ? dsmem_map(smem_u32(red), q) : 0u;
     for (int e = threadIdx.x; e < mm * my_rows; e += C::kThreads) {
         const int mi = e / my_rows;
         const int nl = r_begin + (e - mi * my_rows);
         const int nn = n0 + nl;
         if (nn >= n) continue;
         const uint32_t off = static_cast<uint32_t>((nl * C::kRedStride + mi) * 4);
+        float part[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q) part[q] = q < splits ? dsmem_ld_f32(peer_red[q] + off) : 0.0f;
         float sum = 0.0f;
-        for (int q = 0; q < splits; ++q) sum += dsmem_ld_f32(dsmem_map(red_addr + off, q));
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+            if (q < splits) sum += part[q];
         y[static_cast<int64_t>(mi) * n + nn] = __float2bfloat16_rn(sum);
     }
     cluster_sync_all();  // keep shared memory alive for peers

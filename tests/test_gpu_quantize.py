@@ -123,6 +123,30 @@ def test_special_values_mx(pkg):
     assert_mx_equal(pkg, special_weight())
 
 
+def test_quotients_on_rounding_midpoints(pkg):
+    """Tiles whose scale is a power of two (amax = 448 * 2^j) and whose
+    entries sit exactly on e4m3 rounding midpoints (and their bf16
+    neighbours) times that scale: every tie must resolve to the even code,
+    exactly as the oracle's IEEE quotient does."""
+    mags = oracle.e4m3_decode_table()[:0x7F]
+    mids = (mags[:-1] + mags[1:]) / 2
+    rng = np.random.default_rng(11)
+    w = np.zeros((256, 256), dtype=np.float64)
+    for bn in range(2):
+        for bk in range(2):
+            j = int(rng.integers(-20, 10))
+            tile = rng.choice(mids, size=(128, 128)) * rng.choice([-1.0, 1.0], size=(128, 128))
+            tile[0, 0] = 448.0
+            w[bn * 128:(bn + 1) * 128, bk * 128:(bk + 1) * 128] = tile * 2.0 ** j
+    wt = torch.from_numpy(w).to(torch.bfloat16)
+    # bf16 neighbours of some entries (one ulp up/down) for near-ties
+    bitsw = wt.view(torch.int16).numpy().view(np.uint16).copy()
+    bitsw[1::3, ::5] += 1
+    bitsw[2::3, 1::5] -= 1
+    wt = torch.from_numpy(bitsw.view(np.int16)).view(torch.bfloat16)
+    assert_block_equal(pkg, wt)
+
+
 def test_amax_448_tile_is_plain_cast(pkg):
     w = special_weight()
     c, s = run_block(pkg, w)
