@@ -69,9 +69,14 @@ def _load():
         lib.oracle_mx_quantize_rows.argtypes = [p, i64, i64, p, i64, p, p]
         lib.oracle_block_gemv.argtypes = [p, i64, p, p, i64, i64, p, i64, p]
         lib.oracle_mx_gemv.argtypes = [p, i64, p, p, i64, i64, p, i64, p]
+        lib.oracle_row_quantize_rows.argtypes = [p, i64, i64, p, i64, p, p]
+        lib.oracle_tensor_quantize_rows.argtypes = [p, i64, i64, p, i64, p, p]
+        lib.oracle_row_gemv.argtypes = [p, i64, p, p, i64, i64, i64, p, i64, p]
         for f in ("oracle_block_quantize", "oracle_block_quantize_tile",
                   "oracle_mx_quantize", "oracle_mx_quantize_rows",
-                  "oracle_block_gemv", "oracle_mx_gemv"):
+                  "oracle_block_gemv", "oracle_mx_gemv",
+                  "oracle_row_quantize_rows", "oracle_tensor_quantize_rows",
+                  "oracle_row_gemv"):
             getattr(lib, f).restype = None
         _lib = lib
         return lib
@@ -208,6 +213,54 @@ def mx_gemv(x, codes: np.ndarray, e8m0: np.ndarray, rows=None) -> np.ndarray:
     y = np.zeros((m, nrows), dtype=np.float64)
     _load().oracle_mx_gemv(_ptr(x), m, _ptr(codes), _ptr(e8m0), n, k,
                            None if rows is None else _ptr(rows), nrows, _ptr(y))
+    return y
+
+
+def row_quantize(w, rows=None) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row FP8: w [N,K] bf16 bits -> (codes u8 [N,K], scales f32 [N]).
+    With ``rows``, only those rows are quantized and returned (in order)."""
+    w = _bits16(w)
+    n, k = w.shape
+    rows, nrows = _rows_arg(rows, n)
+    codes = np.zeros((n, k), dtype=np.uint8)
+    scales = np.zeros((n,), dtype=np.float32)
+    _load().oracle_row_quantize_rows(_ptr(w), n, k, None if rows is None else _ptr(rows),
+                                     nrows, _ptr(codes), _ptr(scales))
+    if rows is None:
+        return codes, scales
+    return codes[rows], scales[rows]
+
+
+def tensor_quantize(w, rows=None) -> tuple[np.ndarray, np.ndarray]:
+    """Per-tensor FP8: w [N,K] bf16 bits -> (codes u8 [N,K], scale f32 [1]).
+    The amax is always taken over the whole tensor; with ``rows`` only
+    those rows are encoded and returned (in order)."""
+    w = _bits16(w)
+    n, k = w.shape
+    rows, nrows = _rows_arg(rows, n)
+    codes = np.zeros((n, k), dtype=np.uint8)
+    scale = np.zeros((1,), dtype=np.float32)
+    _load().oracle_tensor_quantize_rows(_ptr(w), n, k, None if rows is None else _ptr(rows),
+                                        nrows, _ptr(codes), _ptr(scale))
+    if rows is None:
+        return codes, scale
+    return codes[rows], scale
+
+
+def row_gemv(x, codes: np.ndarray, scales: np.ndarray, rows=None) -> np.ndarray:
+    """fp64 y[M, len(rows)] = x . (dec(codes) * s_row)^T.  ``scales`` is the
+    per-row vector [N] or the per-tensor scalar [1] (broadcast)."""
+    x = _bits16(x)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(np.asarray(scales, dtype=np.float32).ravel())
+    m, k = x.shape
+    n, k2 = codes.shape
+    assert k == k2 and scales.shape in ((n,), (1,))
+    stride = 1 if scales.shape == (n,) and n > 1 else 0
+    rows, nrows = _rows_arg(rows, n)
+    y = np.zeros((m, nrows), dtype=np.float64)
+    _load().oracle_row_gemv(_ptr(x), m, _ptr(codes), _ptr(scales), stride, n, k,
+                            None if rows is None else _ptr(rows), nrows, _ptr(y))
     return y
 
 

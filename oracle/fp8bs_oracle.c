@@ -309,3 +309,105 @@ void oracle_mx_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
             y64[mi * nrows + j] = sum;
         }
 }
+
+/* ---------------------------------------------------------------------
+ * Per-row and per-tensor FP8 (one fp32 scale per output row, or one for
+ * the whole weight).  FreeToken PR #389 "load-time per-tensor FP8 dense
+ * projections" (What this adds: e4m3 with one fp32 scale per weight; Why:
+ * the per-row W8A16 route of its decode table).  The scale follows the
+ * same rule as the 128x128 tiles: s = amax/448 in binary32 over the real
+ * elements of the row (or tensor), s = 1 when they are all zero, and
+ * q = e4m3(w/s) with the quotient formed in binary32.
+ * ------------------------------------------------------------------- */
+static float amax_of_rows(const uint16_t *w, int64_t k, int64_t r0, int64_t r1)
+{
+    float amax = 0.0f;
+    int64_t i;
+    for (i = r0 * k; i < r1 * k; ++i) {
+        float a = fabsf(bf16_to_float(w[i]));
+        assert(!isnan(a) && !isinf(a));
+        if (a > amax)
+            amax = a;
+    }
+    return amax;
+}
+
+static float scale_of_amax(float amax)
+{
+    return (amax == 0.0f) ? 1.0f : amax / 448.0f;
+}
+
+static void encode_row(const uint16_t *w, int64_t k, int64_t r, float s,
+                       uint8_t *codes)
+{
+    int64_t c;
+    for (c = 0; c < k; ++c) {
+        float q = bf16_to_float(w[r * k + c]) / s; /* binary32 quotient */
+        codes[r * k + c] = oracle_e4m3_encode((double)q);
+    }
+}
+
+void oracle_row_quantize_rows(const uint16_t *w, int64_t n, int64_t k,
+                              const int64_t *rows, int64_t nrows,
+                              uint8_t *codes, float *scales)
+{
+    int64_t j;
+    if (rows == NULL)
+        nrows = n;
+    for (j = 0; j < nrows; ++j) {
+        int64_t r = rows ? rows[j] : j;
+        float s = scale_of_amax(amax_of_rows(w, k, r, r + 1));
+        scales[r] = s;
+        encode_row(w, k, r, s, codes);
+    }
+}
+
+void oracle_row_quantize(const uint16_t *w, int64_t n, int64_t k,
+                         uint8_t *codes, float *scales)
+{
+    oracle_row_quantize_rows(w, n, k, NULL, 0, codes, scales);
+}
+
+void oracle_tensor_quantize_rows(const uint16_t *w, int64_t n, int64_t k,
+                                 const int64_t *rows, int64_t nrows,
+                                 uint8_t *codes, float *scale)
+{
+    int64_t j;
+    float s = scale_of_amax(amax_of_rows(w, k, 0, n));
+    *scale = s;
+    if (rows == NULL)
+        nrows = n;
+    for (j = 0; j < nrows; ++j)
+        encode_row(w, k, rows ? rows[j] : j, s, codes);
+}
+
+void oracle_tensor_quantize(const uint16_t *w, int64_t n, int64_t k,
+                            uint8_t *codes, float *scale)
+{
+    oracle_tensor_quantize_rows(w, n, k, NULL, 0, codes, scale);
+}
+
+/* y64[mi, j] = sum_k x[mi,k] * dec(q[r,k]) * scales[r * scale_stride] with
+ * r = rows[j], in binary64 (exact products, as for the block form). */
+void oracle_row_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
+                     const float *scales, int64_t scale_stride, int64_t n,
+                     int64_t k, const int64_t *rows, int64_t nrows,
+                     double *y64)
+{
+    double dec[256];
+    int64_t mi, j, c;
+    int i;
+    if (rows == NULL)
+        nrows = n;
+    for (i = 0; i < 256; ++i)
+        dec[i] = oracle_e4m3_decode((uint8_t)i);
+    for (mi = 0; mi < m; ++mi)
+        for (j = 0; j < nrows; ++j) {
+            int64_t r = rows ? rows[j] : j;
+            double s = (double)scales[r * scale_stride];
+            double sum = 0.0;
+            for (c = 0; c < k; ++c)
+                sum += oracle_bf16_to_double(x[mi * k + c]) * (dec[codes[r * k + c]] * s);
+            y64[mi * nrows + j] = sum;
+        }
+}

@@ -12,6 +12,7 @@
  *   codes  e4m3fn [N,K]            one byte per weight
  *   scales fp32 [ceil(N/128), ceil(K/128)]        128x128 block scales
  *   e8m0   uint8 [N, ceil(K/32)]   MX power-of-two scale exponents (bias 127)
+ *   row scales fp32 [N]; tensor scale fp32 [1]
  *   x      bf16 [M,K], y bf16 [M,N]
  *
  * Sources: FreeToken PR #636 "opt-in fp8-block QAT for the lm_head"
@@ -20,7 +21,9 @@
  * one byte per weight, one f32 per [128,128] tile, [n_blocks, k_blocks]
  * grid); FreeToken issue #624 "Load-time MXFP8 requantization" (Proposed
  * solution: e4m3 codes, one e8m0 scale per 32 elements, ceil-log2 of
- * amax/448); InfiniLM PR #586 (Summary: 128x128 block scales, W8A16).
+ * amax/448); InfiniLM PR #586 (Summary: 128x128 block scales, W8A16);
+ * FreeToken PR #389 "load-time per-tensor FP8 dense projections" (What
+ * this adds: one fp32 scale per weight; Why: the per-row W8A16 route).
  *
  * Build: plain C11, no -ffast-math, -ffp-contract=off, so that every float
  * operation below is one IEEE-754 binary32 or binary64 operation.
@@ -73,6 +76,30 @@ void oracle_block_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
 void oracle_mx_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
                     const uint8_t *e8m0, int64_t n, int64_t k,
                     const int64_t *rows, int64_t nrows, double *y64);
+
+/* Per-row FP8: one fp32 scale per output row, s_r = amax_r/448 in fp32
+ * (s = 1 for an all-zero row), q = e4m3(w/s_r) with the quotient in fp32.
+ * scales has n entries; the _rows form writes only the listed rows (NULL:
+ * all n rows in order). */
+void oracle_row_quantize(const uint16_t *w, int64_t n, int64_t k,
+                         uint8_t *codes, float *scales);
+void oracle_row_quantize_rows(const uint16_t *w, int64_t n, int64_t k,
+                              const int64_t *rows, int64_t nrows,
+                              uint8_t *codes, float *scales);
+/* Per-tensor FP8: the same with one scale over all n*k elements.  The _rows
+ * form still takes the amax over the whole tensor but encodes only the
+ * listed rows. */
+void oracle_tensor_quantize(const uint16_t *w, int64_t n, int64_t k,
+                            uint8_t *codes, float *scale);
+void oracle_tensor_quantize_rows(const uint16_t *w, int64_t n, int64_t k,
+                                 const int64_t *rows, int64_t nrows,
+                                 uint8_t *codes, float *scale);
+/* y64[mi, j] = sum_k x[mi,k] * dec(q[rows[j],k]) * scales[rows[j]*stride]
+ * in fp64; stride 1 for per-row scales, 0 for a per-tensor scale. */
+void oracle_row_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
+                     const float *scales, int64_t scale_stride, int64_t n,
+                     int64_t k, const int64_t *rows, int64_t nrows,
+                     double *y64);
 
 #ifdef __cplusplus
 }
