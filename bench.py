@@ -10,10 +10,15 @@ GB/s and fraction of HBM bandwidth are reported alongside.
 Other workloads (--workload): rotation (48 layers x 4 projection weights,
 192 GEMVs per step, CUDA-graph captured), sweep ([12288, 4096], M = 1..32
 over 8 rotated copies), mx ([18432, 7168] MXFP8 GEMV, M = 1, 8, 16 over 4
-copies), quantize ([18432, 7168] block + MXFP8 load-time quantization).
+copies), quantize ([18432, 7168] block, MXFP8, per-row and per-tensor
+load-time quantization), prefill ([12288, 4096] at M = 512, 2048, 4096 on the
+tensor cores), rowwise (the lm_head weight with one scale per row and with
+one per tensor, M = 1, 8, 16).  --scales row|tensor runs the rotation and
+prefill workloads on per-row / per-tensor FP8 instead of 128x128 blocks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload lm_head|rotation|sweep|mx|quantize] [--m M]
+                  [--workload lm_head|rotation|sweep|mx|quantize|prefill|rowwise]
+                  [--m M] [--scales block|row|tensor]
 
 N > 1 runs one independent replica per GPU (the path needs no collective);
 the reported value is the aggregate over ranks of bytes moved divided by the
@@ -86,9 +91,25 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
-def gemv_bytes(m, n, k, mx=False):
-    scales = n * ((k + 31) // 32) if mx else 4 * ((n + 127) // 128) * ((k + 127) // 128)
-    return n * k + scales + 2 * m * k + 2 * m * n
+def gemv_bytes(m, n, k, mx=False, scales="block"):
+    if mx:
+        sb = n * ((k + 31) // 32)
+    elif scales == "row":
+        sb = 4 * n
+    elif scales == "tensor":
+        sb = 4
+    else:
+        sb = 4 * ((n + 127) // 128) * ((k + 127) // 128)
+    return n * k + sb + 2 * m * k + 2 * m * n
+
+
+def quantizer(fp8bs, scales):
+    """(quantize, gemv) pair of the binding for a scale layout."""
+    if scales == "row":
+        return fp8bs.row_quantize, fp8bs.row_gemv
+    if scales == "tensor":
+        return fp8bs.tensor_quantize, fp8bs.row_gemv
+    return fp8bs.quantize, fp8bs.gemv
 
 
 # ----------------------------------------------------------- clocks sampler
@@ -193,17 +214,18 @@ def lm_head_workload(torch, fp8bs, inputs, dev):
     cfg = {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call at each "
                        "of M=1,4,8,16 per step", "n": n, "k": k, "ms": ms,
            "l2": "inputs larger than L2 (623 MB of codes per call)"}
-    return dict(calls=calls, xs=xs, ys=ys, cfg=cfg, dominant=("decode_kernel<1,false,true>", [0, 1, 2]),
+    return dict(calls=calls, xs=xs, ys=ys, cfg=cfg, dominant=("decode_kernel<1,0,true>", [0, 1, 2]),
                 codes=codes, scales=scales, n=n, k=k, mx=False)
 
 
-def rotation_workload(torch, fp8bs, inputs, dev, m):
+def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block"):
     layers = inputs.ROTATION_LAYERS
+    quant, gemv = quantizer(fp8bs, scales)
     weights = []
     for l in range(layers):
         for j in range(4):
             w = inputs.rotation_weight(l, j, device=dev)
-            weights.append(fp8bs.quantize(w))
+            weights.append(quant(w))
             del w
     shapes = [inputs.ROTATION_SHAPES[j] for _ in range(layers) for j in range(4)]
     xs = [inputs.activations(m, k, 7 + i, device=dev) for i, (n, k) in enumerate(shapes)]
@@ -211,9 +233,10 @@ def rotation_workload(torch, fp8bs, inputs, dev, m):
 
     def step():
         for i, (c, s) in enumerate(weights):
-            fp8bs.gemv(xs[i], c, s, y=ys[i])
-    total = sum(gemv_bytes(m, n, k) for (n, k) in shapes)
-    cfg = {"workload": f"decode dense-projection rotation: 48 layers x 4 block-FP8 weights "
+            gemv(xs[i], c, s, y=ys[i])
+    total = sum(gemv_bytes(m, n, k, scales=scales) for (n, k) in shapes)
+    kind = {"block": "block-FP8", "row": "per-row FP8", "tensor": "per-tensor FP8"}[scales]
+    cfg = {"workload": f"decode dense-projection rotation: 48 layers x 4 {kind} weights "
                        f"([8192,2560],[2560,3072],[6656,2560],[2560,3072]), M={m}, 192 GEMVs per step "
                        "(CUDA graph)", "ms": [m], "l2": "inputs larger than L2 (2.58 GB of codes per step)"}
     return dict(calls=[(f"rotation M={m}", m, total, step)], cfg=cfg, graph=True, launches_per_step=192,
@@ -256,21 +279,45 @@ def mx_workload(torch, fp8bs, inputs, dev):
         calls.append((f"M={m}", m, 4 * gemv_bytes(m, n, k, mx=True), fn))
     cfg = {"workload": "MXFP8 [18432,7168] (e8m0 per 32 K) W8A16 GEMV, M=1,8,16, 4 rotated copies",
            "n": n, "k": k, "ms": ms, "l2": "inputs larger than L2 (4 rotated copies, 528 MB)"}
-    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,true>", [0, 1]), launches_per_call=4)
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,1,true>", [0, 1]), launches_per_call=4)
 
 
-def prefill_workload(torch, fp8bs, inputs, dev):
+def prefill_workload(torch, fp8bs, inputs, dev, scales="block"):
     ms = [512, 2048, 4096]
-    codes, scales = fp8bs.quantize(inputs.sweep_weight(0, device=dev))
+    quant, gemv = quantizer(fp8bs, scales)
+    codes, sc = quant(inputs.sweep_weight(0, device=dev))
     n, k = inputs.SWEEP_SHAPE
     calls = []
     for m in ms:
         x = inputs.activations(m, k, 700 + m, device=dev)
         y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        calls.append((f"M={m}", m, 2 * m * n * k, (lambda x=x, y=y: fp8bs.gemv(x, codes, scales, y=y))))
-    cfg = {"workload": "prefill: block-FP8 [12288,4096] W8A16 GEMM on tcgen05, M=512,2048,4096", "n": n, "k": k,
+        calls.append((f"M={m}", m, 2 * m * n * k, (lambda x=x, y=y: gemv(x, codes, sc, y=y))))
+    kind = {"block": "block-FP8", "row": "per-row FP8", "tensor": "per-tensor FP8"}[scales]
+    cfg = {"workload": f"prefill: {kind} [12288,4096] W8A16 GEMM on tcgen05, M=512,2048,4096", "n": n, "k": k,
            "ms": ms, "l2": "weight (50 MB) and x fit in L2; compute-bound"}
-    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel", [0, 1, 2]), flops=True)
+    dom = "prefill_kernel<false>" if scales == "block" else "prefill_kernel<true>"
+    return dict(calls=calls, cfg=cfg, dominant=(dom, [0, 1, 2]), flops=True)
+
+
+def rowwise_workload(torch, fp8bs, inputs, dev):
+    """lm_head [152064, 4096] with one fp32 scale per row and with one per
+    tensor (FreeToken PR #389's per-row W8A16 route), M = 1, 8, 16."""
+    ms = [1, 8, 16]
+    w = inputs.lm_head_weight(2, device=dev)
+    n, k = w.shape
+    rq = fp8bs.row_quantize(w)
+    tq = fp8bs.tensor_quantize(w)
+    del w
+    xs = {m: inputs.activations(m, k, 100 + m, device=dev) for m in ms}
+    ys = {m: torch.empty((m, n), dtype=torch.bfloat16, device=dev) for m in ms}
+    calls = [(f"row M={m}", m, gemv_bytes(m, n, k, scales="row"),
+              (lambda m=m: fp8bs.row_gemv(xs[m], rq[0], rq[1], y=ys[m]))) for m in ms]
+    calls += [(f"tensor M={m}", m, gemv_bytes(m, n, k, scales="tensor"),
+               (lambda m=m: fp8bs.row_gemv(xs[m], tq[0], tq[1], y=ys[m]))) for m in ms]
+    cfg = {"workload": "lm_head [152064,4096] per-row and per-tensor FP8 W8A16 GEMV, one call at each of "
+                       "M=1,8,16 per layout per step", "n": n, "k": k, "ms": ms,
+           "l2": "inputs larger than L2 (623 MB of codes per call)"}
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,2,true>", [0, 1, 3, 4]))
 
 
 def quantize_workload(torch, fp8bs, inputs, dev):
@@ -279,13 +326,20 @@ def quantize_workload(torch, fp8bs, inputs, dev):
     codes = torch.empty((n, k), dtype=torch.uint8, device=dev)
     scales = torch.empty(((n + 127) // 128, (k + 127) // 128), dtype=torch.float32, device=dev)
     e8m0 = torch.empty((n, (k + 31) // 32), dtype=torch.uint8, device=dev)
+    rs = torch.empty((n,), dtype=torch.float32, device=dev)
+    ts = torch.empty((1,), dtype=torch.float32, device=dev)
     bq = 3 * n * k + 4 * scales.numel()
     mq = 3 * n * k + e8m0.numel()
     calls = [("block quantize", 0, bq, lambda: fp8bs.quantize(w, codes=codes, scales=scales)),
-             ("mx quantize", 0, mq, lambda: fp8bs.mx_quantize(w, codes=codes, e8m0=e8m0))]
-    cfg = {"workload": "load-time quantize of bf16 [18432,7168] (0.1% Student-t entries) to block FP8 and "
-                       "MXFP8", "n": n, "k": k, "l2": "inputs larger than L2 (264 MB bf16 read per call)"}
-    return dict(calls=calls, cfg=cfg, dominant=("block_quantize_kernel", [0]))
+             ("mx quantize", 0, mq, lambda: fp8bs.mx_quantize(w, codes=codes, e8m0=e8m0)),
+             ("row quantize", 0, 3 * n * k + 4 * n, lambda: fp8bs.row_quantize(w, codes=codes, scales=rs)),
+             # per tensor: the weight is read twice (amax pass, then encode), 5 bytes per element moved
+             ("tensor quantize", 0, 3 * n * k + 4, lambda: fp8bs.tensor_quantize(w, codes=codes, scale=ts))]
+    cfg = {"workload": "load-time quantize of bf16 [18432,7168] (0.1% Student-t entries) to block FP8, "
+                       "MXFP8, per-row and per-tensor FP8", "n": n, "k": k,
+           "l2": "inputs larger than L2 (264 MB bf16 read per call)"}
+    # per tensor: amax, encode and finalize kernels (plus a 4-byte memset)
+    return dict(calls=calls, cfg=cfg, dominant=("block_quantize_kernel", [0]), call_launches=[1, 1, 1, 3])
 
 
 # ------------------------------------------------------------------ timing
@@ -410,8 +464,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="lm_head",
-                    choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill"])
+                    choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill", "rowwise"])
     ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-file", default=os.path.join(ROOT, "gpurun_out", "bench_clocks.csv"))
     args = ap.parse_args()
@@ -457,13 +512,15 @@ def main():
     if args.workload == "lm_head":
         wl = lm_head_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "rotation":
-        wl = rotation_workload(torch, fp8bs, inputs, dev, args.m)
+        wl = rotation_workload(torch, fp8bs, inputs, dev, args.m, args.scales)
     elif args.workload == "sweep":
         wl = sweep_workload(torch, fp8bs, inputs, dev, list(range(1, 33)))
     elif args.workload == "mx":
         wl = mx_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "prefill":
-        wl = prefill_workload(torch, fp8bs, inputs, dev)
+        wl = prefill_workload(torch, fp8bs, inputs, dev, args.scales)
+    elif args.workload == "rowwise":
+        wl = rowwise_workload(torch, fp8bs, inputs, dev)
     else:
         wl = quantize_workload(torch, fp8bs, inputs, dev)
     torch.cuda.synchronize()
@@ -524,7 +581,8 @@ def main():
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
                "host_cores_available": host_cores()}
 
-    launches = args.steps * sum(wl.get("launches_per_call", 1) for _ in calls) * wl.get("launches_per_step", 1)
+    per_call_launches = wl.get("call_launches", [wl.get("launches_per_call", 1)] * len(calls))
+    launches = args.steps * sum(per_call_launches) * wl.get("launches_per_step", 1)
     if rank == 0:
         line = {"metric": "block-FP8 W8A16 GEMV HBM GB/s (lm_head, M=1,4,8,16)" if args.workload == "lm_head"
                 else f"{args.workload} {unit}",

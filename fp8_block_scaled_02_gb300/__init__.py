@@ -1,4 +1,4 @@
-"""fp8_block_scaled_02_gb300 -- block-scaled FP8 / MXFP8 W8A16 on GB300.
+"""fp8_block_scaled_02_gb300 -- block-scaled FP8 / MXFP8 / per-row FP8 W8A16 on GB300.
 
 A thin Python binding over the C ABI in ``include/fp8bs.h`` (``libfp8bs.so``,
 built from ``csrc/`` for sm_103a).  Every function here only marshals
@@ -12,6 +12,9 @@ Functions (names follow the C entry points):
     gemv(x, codes, scales) -> y bf16 [M,N]
     mx_quantize(w)         -> (codes u8 [N,K], e8m0 u8 [N, ceil(K/32)])
     mx_gemv(x, codes, e8m0)-> y bf16 [M,N]
+    row_quantize(w)        -> (codes u8 [N,K], scales f32 [N])       (fp8row_*)
+    tensor_quantize(w)     -> (codes u8 [N,K], scale f32 [1])        (fp8tensor_*)
+    row_gemv(x, codes, s)  -> y bf16 [M,N]; s is [N] (per row) or [1] (per tensor)
 """
 from __future__ import annotations
 
@@ -56,13 +59,21 @@ def lib() -> ctypes.CDLL:
         L.mxfp8_quantize.argtypes = [p, i64, i64, p, p, p]
         L.mxfp8_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
         L.mxfp8_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
+        L.fp8row_quantize.argtypes = [p, i64, i64, p, p, p]
+        L.fp8tensor_quantize.argtypes = [p, i64, i64, p, p, p]
+        L.fp8row_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
+        L.fp8row_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
+        L.fp8tensor_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
+        L.fp8tensor_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
         L.fp8bs_select_path.argtypes = [i64, i64, i64, p, p, i32]
         L.fp8bs_strerror.argtypes = [i32]
         L.fp8bs_strerror.restype = ctypes.c_char_p
         L.fp8bs_check_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
         L.fp8bs_version.argtypes = []
         for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
-                  "mxfp8_gemv_ex", "fp8bs_select_path", "fp8bs_check_device_error", "fp8bs_version"):
+                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
+                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8bs_select_path", "fp8bs_check_device_error",
+                  "fp8bs_version"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
         return L
@@ -157,6 +168,52 @@ def mx_gemv(x, codes, e8m0, y=None, path: int = PATH_AUTO, stream=None):
     _check(lib().mxfp8_gemv_ex(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
                                _dev(e8m0, torch.uint8, "e8m0"), n, k, _dev(y, torch.bfloat16, "y"),
                                int(path), _stream(stream)), "mxfp8_gemv")
+    return y
+
+
+def row_quantize(w, codes=None, scales=None, stream=None):
+    """Per-row FP8 load-time quantization: one fp32 scale per row of w."""
+    import torch
+    n, k = w.shape
+    if codes is None:
+        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((n,), dtype=torch.float32, device=w.device)
+    _check(lib().fp8row_quantize(_dev(w, torch.bfloat16, "w"), n, k, _dev(codes, torch.uint8, "codes"),
+                                 _dev(scales, torch.float32, "scales"), _stream(stream)), "fp8row_quantize")
+    return codes, scales
+
+
+def tensor_quantize(w, codes=None, scale=None, stream=None):
+    """Per-tensor FP8 load-time quantization: one fp32 scale for all of w."""
+    import torch
+    n, k = w.shape
+    if codes is None:
+        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    if scale is None:
+        scale = torch.empty((1,), dtype=torch.float32, device=w.device)
+    _check(lib().fp8tensor_quantize(_dev(w, torch.bfloat16, "w"), n, k, _dev(codes, torch.uint8, "codes"),
+                                    _dev(scale, torch.float32, "scale"), _stream(stream)), "fp8tensor_quantize")
+    return codes, scale
+
+
+def row_gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
+    """y[M, N] = x[M, K] . (dec(codes) * s_row)^T.  ``scales`` of shape [N]
+    calls fp8row_gemv, of shape [1] fp8tensor_gemv."""
+    import torch
+    m, k = x.shape
+    n = codes.shape[0]
+    if codes.shape[1] != k:
+        raise ValueError("codes and x disagree on K")
+    per_row = tuple(scales.shape) == (n,) and n > 1
+    if not per_row and tuple(scales.shape) not in ((1,), ()):
+        raise ValueError("scales must have shape [N] (per row) or [1] (per tensor)")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    fn = lib().fp8row_gemv_ex if per_row else lib().fp8tensor_gemv_ex
+    _check(fn(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
+              _dev(scales, torch.float32, "scales"), n, k, _dev(y, torch.bfloat16, "y"), int(path),
+              _stream(stream)), "fp8row_gemv" if per_row else "fp8tensor_gemv")
     return y
 
 

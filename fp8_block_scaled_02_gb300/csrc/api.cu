@@ -37,31 +37,32 @@ int check_gemv_args(const void *x, int64_t m, const uint8_t *codes, const void *
     return FP8BS_OK;
 }
 
-int run_decode_chunks(const DecodeArgs &a, bool mx, cudaStream_t st) {
+int run_decode_chunks(const DecodeArgs &a, cudaStream_t st) {
     for (int64_t m0 = 0; m0 < a.m; m0 += kDecodeMaxM) {
         DecodeArgs c = a;
         c.m = a.m - m0 < kDecodeMaxM ? a.m - m0 : kDecodeMaxM;
         c.x = static_cast<const char *>(a.x) + m0 * a.k * 2;
         c.y = static_cast<char *>(a.y) + m0 * a.n * 2;
-        const cudaError_t e = launch_decode(c, mx, st);
+        const cudaError_t e = launch_decode(c, st);
         if (e != cudaSuccess) return FP8BS_ERR_CUDA;
     }
     return FP8BS_OK;
 }
 
-int gemv_dispatch(const DecodeArgs &a, bool mx, int path, cudaStream_t st) {
+int gemv_dispatch(const DecodeArgs &a, int path, cudaStream_t st) {
+    const bool mx = a.kind == kScaleMx;
     const bool tma = tma_ok(a.k, a.x, a.codes);
     if (path == FP8BS_PATH_AUTO) path = select_path(a.m, a.k, a.x, a.codes, mx);
     switch (path) {
         case FP8BS_PATH_GENERIC:
-            return cuda_status(launch_generic_gemv(a, mx, st));
+            return cuda_status(launch_generic_gemv(a, st));
         case FP8BS_PATH_DECODE:
             if (!tma) return FP8BS_ERR_PATH;
-            return run_decode_chunks(a, mx, st);
+            return run_decode_chunks(a, st);
         case FP8BS_PATH_PREFILL: {
             if (!tma || mx) return FP8BS_ERR_PATH;
             const cudaError_t e = launch_prefill(a, st);
-            if (e == cudaErrorNotSupported) return run_decode_chunks(a, mx, st);
+            if (e == cudaErrorNotSupported) return run_decode_chunks(a, st);
             return cuda_status(e);
         }
         default:
@@ -73,7 +74,7 @@ int gemv_dispatch(const DecodeArgs &a, bool mx, int path, cudaStream_t st) {
 
 extern "C" {
 
-int fp8bs_version(void) { return 100; }
+int fp8bs_version(void) { return 101; }
 
 const char *fp8bs_strerror(int status) {
     switch (status) {
@@ -115,8 +116,8 @@ int fp8bs_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const flo
     int st = check_gemv_args(x_bf16, m, codes, scales, n, k, y_bf16, path);
     if (st != FP8BS_OK || m == 0) return st;
     if (!aligned(scales, 4)) return FP8BS_ERR_ALIGN;
-    DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k};
-    return gemv_dispatch(a, false, path, static_cast<cudaStream_t>(stream));
+    DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k, kScaleBlock, 0};
+    return gemv_dispatch(a, path, static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scales, int64_t n, int64_t k,
@@ -129,13 +130,62 @@ int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const uin
     int st = check_gemv_args(x_bf16, m, codes, scales_e8m0, n, k, y_bf16, path);
     if (st != FP8BS_OK || m == 0) return st;
     if (path == FP8BS_PATH_PREFILL) return FP8BS_ERR_PATH;
-    DecodeArgs a{x_bf16, codes, nullptr, scales_e8m0, y_bf16, m, n, k};
-    return gemv_dispatch(a, true, path, static_cast<cudaStream_t>(stream));
+    DecodeArgs a{x_bf16, codes, nullptr, scales_e8m0, y_bf16, m, n, k, kScaleMx, 0};
+    return gemv_dispatch(a, path, static_cast<cudaStream_t>(stream));
 }
 
 int mxfp8_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const uint8_t *scales_e8m0, int64_t n,
                int64_t k, void *y_bf16, void *stream) {
     return mxfp8_gemv_ex(x_bf16, m, codes, scales_e8m0, n, k, y_bf16, FP8BS_PATH_AUTO, stream);
+}
+
+static int rowwise_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *codes_u8, float *scales_f32,
+                            bool per_tensor, void *stream) {
+    if (n <= 0 || k <= 0 || n >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (!w_bf16 || !codes_u8 || !scales_f32) return FP8BS_ERR_NULL;
+    if (!aligned(w_bf16, 2) || !aligned(scales_f32, 4)) return FP8BS_ERR_ALIGN;
+    const bool vec = (k % 8) == 0 && aligned(w_bf16, 16) && aligned(codes_u8, 8);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(per_tensor ? launch_tensor_quantize(w_bf16, n, k, codes_u8, scales_f32, vec, st)
+                                  : launch_row_quantize(w_bf16, n, k, codes_u8, scales_f32, vec, st));
+}
+
+int fp8row_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *codes_u8, float *scales_f32, void *stream) {
+    return rowwise_quantize(w_bf16, n, k, codes_u8, scales_f32, false, stream);
+}
+
+int fp8tensor_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *codes_u8, float *scale_f32,
+                       void *stream) {
+    return rowwise_quantize(w_bf16, n, k, codes_u8, scale_f32, true, stream);
+}
+
+static int rowwise_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scales, int64_t n,
+                        int64_t k, void *y_bf16, int row_stride, int path, void *stream) {
+    int st = check_gemv_args(x_bf16, m, codes, scales, n, k, y_bf16, path);
+    if (st != FP8BS_OK || m == 0) return st;
+    if (!aligned(scales, 4)) return FP8BS_ERR_ALIGN;
+    DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k, kScaleRow, row_stride};
+    return gemv_dispatch(a, path, static_cast<cudaStream_t>(stream));
+}
+
+int fp8row_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scales, int64_t n, int64_t k,
+                   void *y_bf16, int path, void *stream) {
+    return rowwise_gemv(x_bf16, m, codes, scales, n, k, y_bf16, 1, path, stream);
+}
+
+int fp8row_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scales, int64_t n, int64_t k,
+                void *y_bf16, void *stream) {
+    return rowwise_gemv(x_bf16, m, codes, scales, n, k, y_bf16, 1, FP8BS_PATH_AUTO, stream);
+}
+
+int fp8tensor_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scale, int64_t n,
+                      int64_t k, void *y_bf16, int path, void *stream) {
+    return rowwise_gemv(x_bf16, m, codes, scale, n, k, y_bf16, 0, path, stream);
+}
+
+int fp8tensor_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scale, int64_t n, int64_t k,
+                   void *y_bf16, void *stream) {
+    return rowwise_gemv(x_bf16, m, codes, scale, n, k, y_bf16, 0, FP8BS_PATH_AUTO, stream);
 }
 
 int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16, const void *codes, int mx) {

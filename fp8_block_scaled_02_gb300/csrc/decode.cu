@@ -1,5 +1,6 @@
-// decode.cu -- W8A16 block-FP8 / MXFP8 GEMV and skinny GEMM for small m
-// (decode batches, m <= 32 per launch): y[m, n] = x[m, k] . dequant(W)^T.
+// decode.cu -- W8A16 block-FP8 / MXFP8 / per-row FP8 GEMV and skinny GEMM
+// for small m (decode batches, m <= 32 per launch):
+// y[m, n] = x[m, k] . dequant(W)^T.
 //
 // Design (sm_103a):
 //  * One CTA owns 128 weight rows (one row of 128x128 block scales) and a
@@ -25,7 +26,9 @@
 //    inverse x rescale) before it joins the accumulator, so the scale is
 //    applied once per 128-wide K block to an fp32 partial and is never folded
 //    into a rounded weight.  For MXFP8 a warp's 32-column slice is exactly
-//    one e8m0 group.
+//    one e8m0 group.  With one scale per row (or per tensor) the K blocks
+//    accumulate unscaled and the row's scale multiplies the fp32 sum once,
+//    just before the bf16 rounding.
 //  * The logical k order inside each MMA is a fixed permutation of the
 //    physical columns, applied identically to A and B, so every thread
 //    fetches 8 contiguous code bytes and 16 contiguous x bytes per K block
@@ -145,12 +148,19 @@ __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r,
 // tile's codes are already arriving while the consumers reduce and store the
 // previous tile.  With splits > 1 each CTA owns exactly one row tile and the
 // cluster reduces over K.
-template <int MT, bool MX, bool F16>
-__global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::kMinBlocks) decode_kernel(
-    const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
-    const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y, int m,
-    int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec) {
+// SC: how the weight is scaled (ScaleKind: 128x128 blocks, MX groups, rows)
+template <int MT, int SC, bool F16>
+__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
+                  const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
+                  int m, int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec, int row_stride) {
+    constexpr bool MX = SC == kScaleMx;
+    constexpr bool ROW = SC == kScaleRow;  // no per-K-block scale; scales[row * row_stride] at the end
     using C = Cfg<MT, MX, F16>;
+    // factor applied to a finished fp32 sum of weight row nn before rounding
+    auto out_scale = [&](int nn) -> float {
+        return ROW ? __ldg(scales + static_cast<int64_t>(nn) * row_stride) : 1.0f;
+    };
     constexpr int kStages = C::kStages;
     constexpr int kBN = C::kBN;
     constexpr int kRT = C::kRT;
@@ -296,13 +306,13 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
         const int coff = (t & 1) * 8;
         for (int ti = 0; ti < my_tiles; ++ti) {
             const int n0 = (tile0 + ti * tstep) * kBN;
-            const float *srow = MX ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
+            const float *srow = (MX || ROW) ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
             float acc[MT][4];
 #pragma unroll
             for (int j = 0; j < MT; ++j)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
-            float s_next = MX ? 0.0f : __ldg(srow);
+            float s_next = (MX || ROW) ? 1.0f : __ldg(srow);
             // MX: lane l < 16 holds the e8m0 word (4 groups of this K block) of
             // weight row 16*warp + l, fetched one K block ahead
             auto load_e8m0_word = [&](int kbi) -> uint32_t {
@@ -327,7 +337,7 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
                 const int it = ti * nkb + kbi;
                 const int s = it % kStages;
                 const float sblk = s_next;
-                if (!MX && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
+                if (!MX && !ROW && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
                 const uint32_t e_cur = e_next;
                 if (MX && kbi + 1 < nkb) e_next = load_e8m0_word(kbi + 1);
                 const uint32_t ewa = MX ? __shfl_sync(0xffffffffu, e_cur, 2 * g) : 0u;
@@ -423,7 +433,8 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
                     const int nl = ra + (q >> 1);
                     if (splits == 1) {
                         if (mi < m && n0 + nl < n)
-                            y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(acc[j][q]);
+                            y[static_cast<int64_t>(mi) * n + n0 + nl] =
+                                __float2bfloat16_rn(ROW ? acc[j][q] * out_scale(n0 + nl) : acc[j][q]);
                     } else {
                         red[nl * C::kRedStride + mi] = acc[j][q];
                     }
@@ -445,7 +456,7 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
 
         for (int ti = 0; ti < my_tiles; ++ti) {
             const int n0 = (tile0 + ti * tstep) * kBN;
-            const float *srow = MX ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
+            const float *srow = (MX || ROW) ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
             float acc[kRT][MT][4];
 #pragma unroll
             for (int rt = 0; rt < kRT; ++rt)
@@ -453,13 +464,13 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
                 for (int j = 0; j < MT; ++j)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) acc[rt][j][q] = 0.0f;
-            float s_next = MX ? 0.0f : __ldg(srow);
+            float s_next = (MX || ROW) ? 1.0f : __ldg(srow);
 
             for (int kbi = 0; kbi < nkb; ++kbi) {
                 const int it = ti * nkb + kbi;
                 const int s = it % kStages;
                 const float sblk = s_next;
-                if (!MX && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
+                if (!MX && !ROW && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
                 // every lane waits (acquire); the warp leaves together if any gave up
                 const uint32_t par = (it / kStages) & 1;
                 const bool ready =
@@ -582,8 +593,10 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
                 for (int e = threadIdx.x; e < mm * kBN; e += kConsumerWarps * 32) {
                     const int mi = e / kBN;
                     const int nl = e - mi * kBN;
-                    if (n0 + nl < n)
-                        y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(red[nl * C::kRedStride + mi]);
+                    if (n0 + nl < n) {
+                        const float v = red[nl * C::kRedStride + mi];
+                        y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(ROW ? v * out_scale(n0 + nl) : v);
+                    }
                 }
                 consumer_bar();  // red is rewritten by the next tile
             }
@@ -620,7 +633,7 @@ __global__ void __launch_bounds__(Cfg<MT, MX, F16>::kThreads, Cfg<MT, MX, F16>::
 #pragma unroll
         for (int q = 0; q < kMaxSplit; ++q)
             if (q < splits) sum += part[q];
-        y[static_cast<int64_t>(mi) * n + nn] = __float2bfloat16_rn(sum);
+        y[static_cast<int64_t>(mi) * n + nn] = __float2bfloat16_rn(ROW ? sum * out_scale(nn) : sum);
     }
     cluster_sync_all();  // keep shared memory alive for peers
 }
@@ -634,11 +647,11 @@ struct Setup {
     int resident[64] = {};
 };
 
-template <int MT, bool MX, bool F16>
+template <int MT, int SC, bool F16>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
-    using C = Cfg<MT, MX, F16>;
+    using C = Cfg<MT, SC == kScaleMx, F16>;
     constexpr int kBN = C::kBN;
-    auto kern = decode_kernel<MT, MX, F16>;
+    auto kern = decode_kernel<MT, SC, F16>;
     static Setup setup;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -703,25 +716,31 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, a.e8m0,
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m),
-                              static_cast<int>(a.n), kblocks, groups, splits, ntiles, e8m0_vec);
+                              static_cast<int>(a.n), kblocks, groups, splits, ntiles, e8m0_vec, a.row_stride);
 }
 
-template <bool MX>
-cudaError_t launch_mx(const DecodeArgs &a, cudaStream_t stream) {
+template <int SC>
+cudaError_t launch_sc(const DecodeArgs &a, cudaStream_t stream) {
     // f16 operands for m <= 8 (and always for MXFP8), bf16 for wider x
+    constexpr bool kMx = SC == kScaleMx;
     switch ((a.m + 7) / 8) {
-        case 1: return launch_t<1, MX, true>(a, stream);
-        case 2: return launch_t<2, MX, MX>(a, stream);
-        case 3: return launch_t<3, MX, MX>(a, stream);
-        case 4: return launch_t<4, MX, MX>(a, stream);
+        case 1: return launch_t<1, SC, true>(a, stream);
+        case 2: return launch_t<2, SC, kMx>(a, stream);
+        case 3: return launch_t<3, SC, kMx>(a, stream);
+        case 4: return launch_t<4, SC, kMx>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs &a, bool mx, cudaStream_t stream) {
-    return mx ? launch_mx<true>(a, stream) : launch_mx<false>(a, stream);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
+    switch (a.kind) {
+        case kScaleBlock: return launch_sc<kScaleBlock>(a, stream);
+        case kScaleMx: return launch_sc<kScaleMx>(a, stream);
+        case kScaleRow: return launch_sc<kScaleRow>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 uint32_t take_decode_error() {

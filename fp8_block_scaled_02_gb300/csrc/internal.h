@@ -13,23 +13,38 @@ cudaError_t launch_block_quantize(const void *w, int64_t n, int64_t k, uint8_t *
                                   float *scales, bool vector_ok, cudaStream_t stream);
 cudaError_t launch_mx_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
                                uint8_t *e8m0, bool vector_ok, cudaStream_t stream);
+// one fp32 scale per row (scales[n]) or per tensor (scales[1]); the
+// per-tensor form zeroes scales[0] and accumulates the amax there first.
+cudaError_t launch_row_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
+                                float *scales, bool vector_ok, cudaStream_t stream);
+cudaError_t launch_tensor_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
+                                   float *scale, bool vector_ok, cudaStream_t stream);
+
+// How the weight's scales are laid out.
+enum ScaleKind : int {
+    kScaleBlock = 0,  // fp32 [ceil(n/128), ceil(k/128)], one per 128x128 tile
+    kScaleMx = 1,     // e8m0 [n, ceil(k/32)], one per 32 consecutive k of a row
+    kScaleRow = 2,    // fp32 scales[r * row_stride]: per row (stride 1) or per tensor (stride 0)
+};
 
 // decode.cu -- TMA-staged skinny GEMM, m <= 32 per launch.
 struct DecodeArgs {
     const void *x;           // bf16 [m, k] (row offset already applied)
     const uint8_t *codes;    // e4m3 [n, k]
-    const float *scales;     // block scales [ceil(n/128), ceil(k/128)] or nullptr
-    const uint8_t *e8m0;     // MX exponents [n, ceil(k/32)] or nullptr
+    const float *scales;     // block or row scales (kScaleBlock / kScaleRow), else nullptr
+    const uint8_t *e8m0;     // MX exponents [n, ceil(k/32)] (kScaleMx), else nullptr
     void *y;                 // bf16 [m, n] (row offset already applied)
     int64_t m, n, k;
+    ScaleKind kind;
+    int row_stride;          // kScaleRow: 1 per row, 0 per tensor
 };
-cudaError_t launch_decode(const DecodeArgs &a, bool mx, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 uint32_t take_decode_error();  // reads and clears the decode kernels' error word
 
 // generic.cu -- plain-load kernels for any shape / alignment.
-cudaError_t launch_generic_gemv(const DecodeArgs &a, bool mx, cudaStream_t stream);
+cudaError_t launch_generic_gemv(const DecodeArgs &a, cudaStream_t stream);
 
-// prefill.cu -- tcgen05 block-FP8 GEMM for larger m.
+// prefill.cu -- tcgen05 block-FP8 / row-scaled FP8 GEMM for larger m.
 cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream);
 uint32_t take_prefill_error();
 

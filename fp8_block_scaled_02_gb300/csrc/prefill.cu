@@ -21,6 +21,10 @@
 //    thread ("promotion"), so the scale is applied once per 128-wide K
 //    block to an fp32 partial and never folded into a rounded bf16 weight.
 //    At the end each thread stores its weight row's outputs as bf16.
+//  * With one scale per weight row (or per tensor) there is nothing to
+//    promote per K block: all K blocks accumulate into one TMEM
+//    accumulator, and the epilogue reads it once after the last MMA,
+//    multiplies each row by its scale and stores bf16.
 //  * mbarriers: x_full (TMA ring), a_full (TMEM A slots), d_empty (TMEM
 //    accumulators), and a ring of "MMA done" barriers, one tcgen05.commit
 //    per K block, that frees x stages, A slots and accumulators alike.  Every wait is bounded; a kernel that gives up sets an error
@@ -139,11 +143,14 @@ __device__ __forceinline__ uint4 ld_codes16(const uint8_t *p) {
 
 __device__ __forceinline__ void fail(uint32_t bit) { atomicOr(&g_prefill_err, bit); }
 
+// ROW: scales[row * row_stride] per weight row (stride 0: one per tensor)
+// instead of 128x128 block scales.
+template <bool ROW>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                               const uint8_t *__restrict__ codes,
                                                               const float *__restrict__ scales,
                                                               __nv_bfloat16 *__restrict__ y, int m, int n,
-                                                              int k, int kblocks) {
+                                                              int k, int kblocks, int row_stride) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -155,8 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint64_t *done = bars + kXStages;        // [kRing]
     uint64_t *a_full = done + kRing;         // [2]
     uint64_t *d_empty = a_full + 2;          // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_empty + 2);
-    int *s_fail = reinterpret_cast<int *>(d_empty + 3);
+    uint64_t *d_full = d_empty + 2;          // ROW: all MMAs of the tile done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_full + 1);
+    int *s_fail = reinterpret_cast<int *>(d_full + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileW;
@@ -169,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             mbar_init(&a_full[i], kNumDec);   // one arrival per decoder warp
             mbar_init(&d_empty[i], kNumEpi);  // one arrival per epilogue warp
         }
+        mbar_init(d_full, 1);  // tcgen05.commit
         *s_fail = 0;
         fence_mbarrier_init();
     }
@@ -190,10 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         int issued = 0;  // K blocks whose MMAs were committed
         if (lane == 0) {
             for (int kb = 0; kb < kblocks; ++kb) {
-                const int xs = kb % kXStages, as = kb & 1, db = kb & 1;
+                const int xs = kb % kXStages, as = kb & 1, db = ROW ? 0 : (kb & 1);
                 bool ok = mbar_wait_bounded(&x_full[xs], (kb / kXStages) & 1) &&
                           mbar_wait_bounded(&a_full[as], (kb >> 1) & 1) &&
-                          (kb < 2 || mbar_wait_bounded(&d_empty[db], ((kb >> 1) - 1) & 1));
+                          (ROW || kb < 2 || mbar_wait_bounded(&d_empty[db], ((kb >> 1) - 1) & 1));
                 if (!ok) {
                     fail(ERRBIT_MMA_WAIT);
                     *reinterpret_cast<volatile int *>(s_fail) = 1;
@@ -209,10 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
                     tc_mma(d_tmem, a_tmem + kk * 8, desc0 + (kk >> 2) * (kXPanel >> 4) + (kk & 3) * 2,
-                           kk > 0 ? 1u : 0u);
+                           (kk > 0 || (ROW && kb > 0)) ? 1u : 0u);
                 tc_commit(&done[kb % kRing]);
                 issued = kb + 1;
             }
+            // ROW: the epilogue's single wait (also after a failure, so that
+            // it does not sit out its whole time limit)
+            if (ROW) tc_commit(d_full);
             // drain: wait for the last committed block before TMEM can be freed
             if (issued > 0 && !mbar_wait_bounded(&done[(issued - 1) % kRing], ((issued - 1) / kRing) & 1))
                 fail(ERRBIT_MMA_WAIT);
@@ -301,9 +313,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         float acc[kTileX / 2];
 #pragma unroll
         for (int i = 0; i < kTileX / 2; ++i) acc[i] = 0.0f;
-        const float *srow = scales + static_cast<int64_t>(blockIdx.x) * kblocks;
+        const float *srow = scales + (ROW ? 0 : static_cast<int64_t>(blockIdx.x) * kblocks);
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        if (ROW) {
+            ok = mbar_wait_bounded(d_full, 0);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) fail(ERRBIT_FULL_WAIT);
+                ok = false;
+            } else {
+                ok = *reinterpret_cast<volatile int *>(s_fail) == 0;
+                tc_fence_after();
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kColD + ch * 64;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[16];
+                    tc_ld16(taddr + 16 * c, v);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[16 * c + i] = __uint_as_float(v[i]);
+                }
+                const int row = n0 + q * 32 + lane;
+                const float rs = row < n ? __ldg(scales + static_cast<int64_t>(row) * row_stride) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < kTileX / 2; ++i) acc[i] *= rs;
+            }
+        }
+        for (int kb = 0; ROW ? false : kb < kblocks; ++kb) {
             const int db = kb & 1;
             const float s = __ldg(srow + kb);
             ok = mbar_wait_bounded(&done[kb % kRing], (kb / kRing) & 1);
@@ -354,13 +389,19 @@ cudaError_t g_setup_err[64] = {};
 }  // namespace
 
 cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
+    if (a.kind != kScaleBlock && a.kind != kScaleRow) return cudaErrorNotSupported;
+    const bool row = a.kind == kScaleRow;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lock(g_setup_mu);
         if (!g_setup_done[dev]) {
-            g_setup_err[dev] =
-                cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            cudaError_t e =
+                cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+            g_setup_err[dev] = e;
             g_setup_done[dev] = true;
         }
         if (g_setup_err[dev] != cudaSuccess) return g_setup_err[dev];
@@ -372,9 +413,10 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
     const dim3 grid(static_cast<unsigned>((a.n + kTileW - 1) / kTileW), static_cast<unsigned>((a.m + kTileX - 1) / kTileX));
-    prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, a.codes, a.scales, static_cast<__nv_bfloat16 *>(a.y),
-                                                           static_cast<int>(a.m), static_cast<int>(a.n),
-                                                           static_cast<int>(a.k), kblocks);
+    auto kern = row ? prefill_kernel<true> : prefill_kernel<false>;
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, a.codes, a.scales, static_cast<__nv_bfloat16 *>(a.y),
+                                                 static_cast<int>(a.m), static_cast<int>(a.n), static_cast<int>(a.k),
+                                                 kblocks, row ? a.row_stride : 0);
     return cudaGetLastError();
 }
 

@@ -10,6 +10,14 @@
 //    consecutive k of a row (FreeToken issue #624).  Four lanes own one
 //    32-element group (16 bytes each, fully coalesced), the group amax comes
 //    from two shuffles, and no fp32 copy of the weight is ever formed.
+//  * row_quantize_kernel / tensor_*_kernel: one fp32 scale per output row
+//    or per weight (FreeToken PR #389, What this adds / Why), the same rule
+//    as a tile: s = amax / 448 over the row (tensor), s = 1 if all zero.
+//    Per row is one CTA per row; per tensor is a grid-wide amax (atomicMax
+//    on the fp32 bit pattern, which orders like the value for |w| >= 0, so
+//    the result is the exact maximum whatever the order) into the scale
+//    slot, an encode pass that derives s from it, and a one-thread pass
+//    that replaces the amax by s.
 //  * *_generic kernels: scalar versions of the same arithmetic for shapes or
 //    pointers the vector kernels cannot take (k % 8 != 0, unaligned w).
 //
@@ -231,6 +239,124 @@ __global__ void __launch_bounds__(256) mx_quantize_generic_kernel(
     e8m0[g] = static_cast<uint8_t>(E);
 }
 
+// --------------------------------------------------------------- per row
+// One CTA per weight row.  The row's 16-byte chunks are dealt round-robin to
+// 256 threads; the first kRowHeld chunks of each thread stay in registers
+// between the amax reduction and the encode, so rows of up to
+// 256 * 8 * kRowHeld = 8192 elements are read from HBM once (longer rows
+// read the remainder a second time, from L2).
+constexpr int kRowThreads = 256;
+constexpr int kRowHeld = 4;
+
+__device__ __forceinline__ float cta_max(float v, float *warp_slots) {
+    v = warp_max(v);
+    if ((threadIdx.x & 31) == 0) warp_slots[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = warp_slots[0];
+    for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) v = fmaxf(v, warp_slots[i]);
+    return v;
+}
+
+__global__ void __launch_bounds__(kRowThreads) row_quantize_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                 uint8_t *__restrict__ codes,
+                                                                 float *__restrict__ scales, int64_t k) {
+    __shared__ float warp_amax[kRowThreads / 32];
+    const int64_t row = blockIdx.x;
+    const __nv_bfloat16 *wr = w + row * k;
+    uint8_t *cr = codes + row * k;
+    const int64_t chunks = k / 8;  // k % 8 == 0 on this path
+    uint4 v[kRowHeld];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kRowHeld; ++i) {
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kRowThreads;
+        v[i] = c < chunks ? ld_nc_v4(wr + c * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kRowHeld; ++i) amax = absmax8(v[i], amax);
+    for (int64_t c = threadIdx.x + kRowHeld * kRowThreads; c < chunks; c += kRowThreads)
+        amax = absmax8(ld_nc_v4(wr + c * 8), amax);
+    amax = cta_max(amax, warp_amax);
+    const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    if (threadIdx.x == 0) scales[row] = s;
+#pragma unroll
+    for (int i = 0; i < kRowHeld; ++i) {
+        const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kRowThreads;
+        if (c < chunks) *reinterpret_cast<uint2 *>(cr + c * 8) = encode8_div(v[i], s);
+    }
+    for (int64_t c = threadIdx.x + kRowHeld * kRowThreads; c < chunks; c += kRowThreads)
+        *reinterpret_cast<uint2 *>(cr + c * 8) = encode8_div(ld_nc_v4(wr + c * 8), s);
+}
+
+__global__ void __launch_bounds__(kRowThreads) row_quantize_generic_kernel(
+    const __nv_bfloat16 *__restrict__ w, uint8_t *__restrict__ codes, float *__restrict__ scales, int64_t k) {
+    __shared__ float warp_amax[kRowThreads / 32];
+    const int64_t row = blockIdx.x;
+    const uint16_t *wb = reinterpret_cast<const uint16_t *>(w) + row * k;
+    float amax = 0.0f;
+    for (int64_t c = threadIdx.x; c < k; c += kRowThreads)
+        amax = fmaxf(amax, fabsf(__uint_as_float(static_cast<uint32_t>(wb[c]) << 16)));
+    amax = cta_max(amax, warp_amax);
+    const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    if (threadIdx.x == 0) scales[row] = s;
+    for (int64_t c = threadIdx.x; c < k; c += kRowThreads) {
+        const float q = __uint_as_float(static_cast<uint32_t>(wb[c]) << 16) / s;
+        codes[row * k + c] = static_cast<uint8_t>(f32x2_to_e4m3x2(q, 0.0f) & 0xFF);
+    }
+}
+
+// ------------------------------------------------------------ per tensor
+// The weight is one flat array of total = n*k elements.  VEC: total % 8 == 0
+// and 16-byte aligned w / 8-byte aligned codes, 16-byte chunks.
+constexpr int kTensorThreads = 256;
+
+template <bool VEC>
+__global__ void __launch_bounds__(kTensorThreads) tensor_amax_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                   int64_t total,
+                                                                   uint32_t *__restrict__ amax_bits) {
+    __shared__ float warp_amax[kTensorThreads / 32];
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTensorThreads;
+    float amax = 0.0f;
+    if (VEC) {
+        for (int64_t c = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; c < total / 8; c += stride)
+            amax = absmax8(ld_nc_v4(w + c * 8), amax);
+    } else {
+        const uint16_t *wb = reinterpret_cast<const uint16_t *>(w);
+        for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; e < total; e += stride)
+            amax = fmaxf(amax, fabsf(__uint_as_float(static_cast<uint32_t>(wb[e]) << 16)));
+    }
+    amax = cta_max(amax, warp_amax);
+    if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(amax));
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kTensorThreads) tensor_encode_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                     int64_t total, uint8_t *__restrict__ codes,
+                                                                     const uint32_t *__restrict__ amax_bits) {
+    const float amax = __uint_as_float(*amax_bits);
+    const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTensorThreads;
+    if (VEC) {
+        for (int64_t c = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; c < total / 8; c += stride)
+            *reinterpret_cast<uint2 *>(codes + c * 8) = encode8_div(ld_nc_v4(w + c * 8), s);
+    } else {
+        const uint16_t *wb = reinterpret_cast<const uint16_t *>(w);
+        for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; e < total; e += stride) {
+            const float q = __uint_as_float(static_cast<uint32_t>(wb[e]) << 16) / s;
+            codes[e] = static_cast<uint8_t>(f32x2_to_e4m3x2(q, 0.0f) & 0xFF);
+        }
+    }
+}
+
+// Replace the accumulated amax in the scale slot by s (after every encode
+// CTA has read it: stream order).
+__global__ void tensor_finalize_kernel(float *scale) {
+    if (threadIdx.x == 0) {
+        const float amax = *scale;
+        *scale = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_block_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
@@ -261,6 +387,43 @@ cudaError_t launch_mx_quantize(const void *w, int64_t n, int64_t k, uint8_t *cod
         mx_quantize_generic_kernel<<<blocks, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16 *>(w), codes, e8m0, n, k, groups);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_row_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
+                                float *scales, bool vector_ok, cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>(n);
+    if (vector_ok)
+        row_quantize_kernel<<<blocks, kRowThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), codes,
+                                                                scales, k);
+    else
+        row_quantize_generic_kernel<<<blocks, kRowThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w),
+                                                                        codes, scales, k);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tensor_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
+                                   float *scale, bool vector_ok, cudaStream_t stream) {
+    const int64_t total = n * k;
+    const int64_t units = vector_ok ? total / 8 : total;
+    // enough CTAs to fill every SM several times over, never more than the work
+    int64_t blocks = static_cast<int64_t>(device_sm_count()) * 8;
+    const int64_t need = (units + kTensorThreads - 1) / kTensorThreads;
+    if (blocks > need) blocks = need;
+    if (blocks < 1) blocks = 1;
+    const __nv_bfloat16 *wb = static_cast<const __nv_bfloat16 *>(w);
+    uint32_t *amax_bits = reinterpret_cast<uint32_t *>(scale);
+    cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (vector_ok) {
+        tensor_amax_kernel<true><<<g, kTensorThreads, 0, stream>>>(wb, total, amax_bits);
+        tensor_encode_kernel<true><<<g, kTensorThreads, 0, stream>>>(wb, total, codes, amax_bits);
+    } else {
+        tensor_amax_kernel<false><<<g, kTensorThreads, 0, stream>>>(wb, total, amax_bits);
+        tensor_encode_kernel<false><<<g, kTensorThreads, 0, stream>>>(wb, total, codes, amax_bits);
+    }
+    tensor_finalize_kernel<<<1, 32, 0, stream>>>(scale);
     return cudaGetLastError();
 }
 

@@ -1,7 +1,7 @@
 /*
- * fp8bs.h -- C ABI of libfp8bs: block-scaled FP8 (E4M3) and MXFP8 weight
- * quantization and the W8A16 GEMV / skinny GEMM / prefill GEMM that consumes
- * it, for NVIDIA GB300 (sm_103a).
+ * fp8bs.h -- C ABI of libfp8bs: block-scaled FP8 (E4M3), MXFP8 and per-row /
+ * per-tensor FP8 weight quantization and the W8A16 GEMV / skinny GEMM /
+ * prefill GEMM that consumes it, for NVIDIA GB300 (sm_103a).
  *
  * Common conventions
  * ------------------
@@ -14,6 +14,7 @@
  *      codes      e4m3  [n, k]   one byte per weight
  *      scales     fp32  [ceil(n/128), ceil(k/128)]   one per 128x128 tile
  *      e8m0       uint8 [n, ceil(k/32)]              one per 32 k of a row
+ *      row scales fp32  [n] (per row) or [1] (per tensor)
  *      x          bf16  [m, k]
  *      y          bf16  [m, n]
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
@@ -52,7 +53,8 @@ typedef enum {
     FP8BS_PATH_AUTO = 0,     /* choose by shape (what fp8bs_gemv does)         */
     FP8BS_PATH_DECODE = 1,   /* TMA-staged skinny kernel, m <= 32 per launch
                                 (larger m runs in chunks of 32 rows)          */
-    FP8BS_PATH_PREFILL = 2,  /* tcgen05 tensor-core kernel, block-FP8 only     */
+    FP8BS_PATH_PREFILL = 2,  /* tcgen05 tensor-core kernel (block / row / tensor
+                                scales; not MXFP8)                           */
     FP8BS_PATH_GENERIC = 3   /* plain-load kernel for any shape / alignment    */
 } fp8bs_path;
 
@@ -154,8 +156,56 @@ int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
                   const uint8_t *scales_e8m0, int64_t n, int64_t k,
                   void *y_bf16, int path, void *stream);
 
+/*
+ * fp8row_quantize / fp8tensor_quantize -- load-time FP8 with one fp32 scale
+ * per output row (scales_f32[n]) or one for the whole weight (scale_f32[1]).
+ *
+ * Defined by: FreeToken PR #389 "load-time per-tensor FP8 dense projections"
+ * (What this adds: each weight quantized to e4m3 with one fp32 scale; Why:
+ * the per-row W8A16 route in its decode table).  The scale rule is the tile
+ * rule applied to a row / the tensor: amax over its elements, s = amax / 448
+ * as an IEEE fp32 division, s = 1 when amax = 0, codes = e4m3(w / s) with an
+ * IEEE fp32 quotient, nearest-even, saturated to +-448.
+ *
+ *   w_bf16      device, n*k bf16, 2-byte aligned
+ *   n, k        > 0 (else FP8BS_ERR_SHAPE)
+ *   codes_u8    device, n*k bytes, written
+ *   scales_f32  device, n floats (per row) / 1 float (per tensor), 4-byte
+ *               aligned, written.  The per-tensor form uses its one float as
+ *               the amax accumulator before it writes s there, so no other
+ *               work may read it until the call has completed on `stream`.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+int fp8row_quantize(const void *w_bf16, int64_t n, int64_t k,
+                    uint8_t *codes_u8, float *scales_f32, void *stream);
+int fp8tensor_quantize(const void *w_bf16, int64_t n, int64_t k,
+                       uint8_t *codes_u8, float *scale_f32, void *stream);
+
+/*
+ * fp8row_gemv / fp8tensor_gemv -- W8A16 linear over per-row / per-tensor FP8:
+ *   y[i, j] = bf16_rn( s_j * sum_c x[i, c] * dec(q[j, c]) )
+ * with the sum in fp32 and s_j = scales[j] (per row) or scale[0] (per
+ * tensor), applied once to the fp32 sum.  Same argument rules, paths and
+ * errors as fp8bs_gemv, with the scale arrays of the quantizers above.
+ * Defined by: FreeToken PR #389 (Why: the per-row W8A16 route of the decode
+ * micro-benchmark over M = 1/8/16).
+ */
+int fp8row_gemv(const void *x_bf16, int64_t m, const uint8_t *codes,
+                const float *scales, int64_t n, int64_t k, void *y_bf16,
+                void *stream);
+int fp8row_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
+                   const float *scales, int64_t n, int64_t k, void *y_bf16,
+                   int path, void *stream);
+int fp8tensor_gemv(const void *x_bf16, int64_t m, const uint8_t *codes,
+                   const float *scale, int64_t n, int64_t k, void *y_bf16,
+                   void *stream);
+int fp8tensor_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
+                      const float *scale, int64_t n, int64_t k, void *y_bf16,
+                      int path, void *stream);
+
 /* Path FP8BS_PATH_AUTO would take for these shapes and pointers
- * (host-only, launches nothing).  `mx` selects the MXFP8 GEMV. */
+ * (host-only, launches nothing).  `mx` selects the MXFP8 GEMV; the block,
+ * per-row and per-tensor GEMVs share the same paths (mx = 0). */
 int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16,
                       const void *codes, int mx);
 

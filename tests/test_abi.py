@@ -33,8 +33,9 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
-                 "mxfp8_gemv_ex", "fp8bs_select_path", "fp8bs_strerror", "fp8bs_check_device_error",
-                 "fp8bs_version"):
+                 "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
+                 "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8bs_select_path", "fp8bs_strerror",
+                 "fp8bs_check_device_error", "fp8bs_version"):
         assert want in names, names
 
 
@@ -48,7 +49,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strerror(L):
-    assert L.fp8bs_version() == 100
+    assert L.fp8bs_version() == 101
     import fp8_block_scaled_02_gb300 as pkg
     for st in range(-7, 1):
         assert pkg.strerror(st) and pkg.strerror(st) != "unknown status"
@@ -90,6 +91,26 @@ def test_gemv_validation(L):
     assert L.fp8bs_gemv_ex(x, 1, P(0x20001), s, 10, 32, y, 1, None) == -7  # decode needs aligned codes
     assert L.mxfp8_gemv_ex(x, 1, c, s, 10, 32, y, 2, None) == -7    # no MX prefill path
     assert L.mxfp8_gemv(x, 1, c, None, 10, 32, y, None) == -1
+
+
+def test_rowwise_validation(L):
+    w, c, s, x, y = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000)
+    for q in (L.fp8row_quantize, L.fp8tensor_quantize):
+        assert q(w, 0, 10, c, s, None) == -2
+        assert q(w, 10, 1 << 31, c, s, None) == -2
+        assert q(None, 10, 10, c, s, None) == -1
+        assert q(w, 10, 10, None, s, None) == -1
+        assert q(w, 10, 10, c, None, None) == -1
+        assert q(P(0x10001), 10, 10, c, s, None) == -4
+        assert q(w, 10, 10, c, P(0x30002), None) == -4
+    for g, gx in ((L.fp8row_gemv, L.fp8row_gemv_ex), (L.fp8tensor_gemv, L.fp8tensor_gemv_ex)):
+        assert g(x, -1, c, s, 10, 10, y, None) == -2
+        assert g(None, 0, None, None, 10, 10, None, None) == 0
+        assert g(x, 1, c, None, 10, 10, y, None) == -1
+        assert g(x, 1, c, P(0x30002), 10, 10, y, None) == -4
+        assert gx(x, 1, c, s, 10, 10, y, 9, None) == -7
+        assert gx(x, 1, c, s, 10, 10, y, 1, None) == -7   # decode needs k % 16 == 0
+        assert gx(x, 40, c, s, 10, 24, y, 2, None) == -7  # prefill needs k % 16 == 0
 
 
 def test_select_path(L):
