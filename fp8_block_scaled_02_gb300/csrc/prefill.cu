@@ -1,34 +1,37 @@
-// prefill.cu -- block-FP8 W8A16 GEMM for prefill-shaped batches on the
-// 5th-generation tensor cores (tcgen05), y[M, N] = x[M, K] . dequant(W)^T.
+// prefill.cu -- block-FP8 / per-row FP8 W8A16 GEMM for prefill-shaped
+// batches on the 5th-generation tensor cores (tcgen05),
+// y[M, N] = x[M, K] . dequant(W)^T.
 //
-// Design (sm_103a, one CTA per 128 weight rows x 128 rows of x, 18 warps):
-//  * Weights are the MMA's A operand and live in tensor memory: eight
-//    "decoder" warps stream their rows' e4m3 codes from global memory (each
-//    thread owns one weight row = one TMEM lane and one 64-wide K half,
-//    loading two K blocks ahead), convert them exactly to bf16 pairs in
-//    registers and tcgen05.st them into a double-buffered 64-column A slot
-//    (128 K of bf16 per K block).  The decoded weight never touches shared
-//    memory or HBM.
-//  * x is the B operand: one producer thread brings each K block's
+// Design (sm_103a, one CTA per 128 weight rows x 256 rows of x, 18 warps):
+//  * Weights are the MMA's A operand.  Eight "decoder" warps stream their
+//    rows' e4m3 codes from global memory (each thread owns one weight row
+//    and one 64-wide K half, loading two K blocks ahead), convert them
+//    exactly to bf16 pairs in registers and store them into a
+//    double-buffered shared-memory A slot in the 128-byte-swizzled K-major
+//    layout the tensor core reads.  The decoded weight never reaches HBM.
+//    Each decoded 128 x 128 block feeds two MMA groups (two 128-row halves
+//    of x), so the decode work per flop is half that of a 128 x 128 tile.
+//  * x is the B operand: one producer thread brings each (K block, half)
 //    [128 rows x 128 K] bf16 tile in with 2-D TMA (128-byte swizzle, two
 //    64-column panels) into a 4-stage shared-memory ring.
 //  * One thread issues tcgen05.mma.kind::f16 (bf16 x bf16 -> fp32, M=128,
-//    N=128, K=16; 8 per K block).  Each K block accumulates from zero into
-//    one of two 128-column TMEM accumulators.
-//  * Eight epilogue warps (two per TMEM lane quarter, one per 64-column
-//    half) read each finished K-block accumulator with tcgen05.ld, multiply
-//    it by that block's fp32 scale and add it into 64 fp32 registers per
-//    thread ("promotion"), so the scale is applied once per 128-wide K
-//    block to an fp32 partial and never folded into a rounded bf16 weight.
-//    At the end each thread stores its weight row's outputs as bf16.
-//  * With one scale per weight row (or per tensor) there is nothing to
-//    promote per K block: all K blocks accumulate into one TMEM
-//    accumulator, and the epilogue reads it once after the last MMA,
-//    multiplies each row by its scale and stores bf16.
-//  * mbarriers: x_full (TMA ring), a_full (TMEM A slots), d_empty (TMEM
-//    accumulators), and a ring of "MMA done" barriers, one tcgen05.commit
-//    per K block, that frees x stages, A slots and accumulators alike.  Every wait is bounded; a kernel that gives up sets an error
-//    word, drains what it issued and still frees its TMEM.
+//    N=128, K=16; 8 per K block and half), both operands from shared memory,
+//    and one tcgen05.commit per (K block, half) into a ring of "MMA done"
+//    barriers that frees x stages, A slots and accumulators alike.
+//  * Block scales: each (K block, half) accumulates from zero into that
+//    half's 128-column TMEM partial D_h; eight epilogue warps (one per TMEM
+//    lane quarter and half) read it with tcgen05.ld, multiply it by the
+//    block's fp32 scale and add it into the half's running total T_h, which
+//    also lives in TMEM (tcgen05.st), with packed fp32x2 FMAs ("promotion":
+//    the scale is applied once per 128-wide K block to an fp32 partial and
+//    never folded into a rounded bf16 weight).  TMEM: T_0, T_1, D_0, D_1 =
+//    512 columns.
+//  * With one scale per weight row (or per tensor) nothing is promoted per
+//    K block: the MMAs accumulate straight into T_h across all of K, and the
+//    epilogue reads it once after a final commit, multiplies each row by its
+//    scale and stores bf16.
+//  * Every wait is bounded; a kernel that gives up sets an error word,
+//    drains what it issued and still frees its TMEM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,31 +44,35 @@ namespace {
 __device__ uint32_t g_prefill_err;
 
 constexpr int kTileW = 128;       // weight rows per CTA (= one scale row block, = MMA M)
-constexpr int kTileX = 128;       // x rows per CTA (= MMA N)
+constexpr int kHalfX = 128;       // x rows per MMA group (= MMA N)
+constexpr int kTileX = 2 * kHalfX;  // x rows per CTA
 constexpr int kKB = 128;          // K per block
-constexpr int kXStages = 4;
-constexpr int kRing = 4;          // MMA-completion barriers (>= x stages, > A slots, > accumulators)
-static_assert(kXStages <= kRing, "the x producer waits on a block kXStages back");
-constexpr int kXPanel = kTileX * 128;     // 64 bf16 per row, 16 KB
-constexpr int kXStage = 2 * kXPanel;      // 32 KB
+constexpr int kPanel = 128 * 128;           // one 64-column bf16 panel of 128 rows, 16 KB
+constexpr int kXStages = 4;                 // x ring: one (K block, half) per stage
+constexpr int kXStage = 2 * kPanel;         // 32 KB
+constexpr int kASlots = 2;                  // decoded weight blocks in flight
+constexpr int kASlot = 2 * kPanel;          // 32 KB
+constexpr int kRing = 8;  // MMA-completion barriers, one per (K block, half); >= every look-back
+static_assert(kXStages <= kRing && 2 * kASlots <= kRing, "a wait must never reach back a full ring");
 constexpr int kTmemCols = 512;
-constexpr int kColA = 0;                  // A slots: [0, 64) and [64, 128)
-constexpr int kColD = 128;                // accumulators: [128, 256) and [256, 384)
+constexpr int kColT = 0;                  // running totals T_0, T_1: [0, 128), [128, 256)
+constexpr int kColD = 256;                // per-K-block partials D_0, D_1: [256, 384), [384, 512)
 
 // warp roles
 constexpr int kWarpMma = 0;       // also allocates / frees TMEM
 constexpr int kWarpTma = 1;
-constexpr int kWarpDec0 = 2;      // 2..9 decoders: lane quarter warp % 4, K half (warp - 2) / 4
+constexpr int kWarpDec0 = 2;      // 2..9 decoders: weight rows 32 (warp % 4) .. +31, K half (warp - 2) / 4
 constexpr int kNumDec = 8;
-constexpr int kWarpEpi0 = kWarpDec0 + kNumDec;  // 10..17 epilogue: lane quarter warp % 4, column half (warp - 10) / 4
+constexpr int kWarpEpi0 = kWarpDec0 + kNumDec;  // 10..17 epilogue: TMEM lane quarter warp % 4, half (warp - 10) / 4
 constexpr int kNumEpi = 8;
 constexpr int kThreads = (kWarpEpi0 + kNumEpi) * 32;
-constexpr int kSmemBytes = 1024 + kXStages * kXStage + 256;
+constexpr int kSmemBytes = 1024 + kXStages * kXStage + kASlots * kASlot + 256;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kTileX >> 3) << 17) |
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kHalfX >> 3) << 17) |
                             (static_cast<uint32_t>(kTileW >> 4) << 24);
 
 // Shared-memory matrix descriptor for a K-major operand stored in the
@@ -83,42 +90,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %3, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(accumulate), "r"(kIdesc)
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
-}
-
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr)
-        : "memory");
 }
 
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
@@ -143,6 +117,34 @@ __device__ __forceinline__ uint4 ld_codes16(const uint8_t *p) {
 
 __device__ __forceinline__ void fail(uint32_t bit) { atomicOr(&g_prefill_err, bit); }
 
+// Both operands from shared memory.
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %3, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(kIdesc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+// t = s * d + t on two packed fp32 lanes (one instruction for two outputs)
+__device__ __forceinline__ void ffma2(uint32_t &t_lo, uint32_t &t_hi, uint64_t s2, uint32_t d_lo, uint32_t d_hi) {
+    uint64_t t, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(t) : "r"(t_lo), "r"(t_hi));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(d_lo), "r"(d_hi));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(t) : "l"(s2), "l"(d));
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(t_lo), "=r"(t_hi) : "l"(t));
+}
+
 // ROW: scales[row * row_stride] per weight row (stride 0: one per tensor)
 // instead of 128x128 block scales.
 template <bool ROW>
@@ -154,30 +156,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kXStages * kXStage);
-    // done[kb % kRing] completes when the MMAs of K block kb have finished
-    // (one tcgen05.commit per block); the x producer, the decoders and the
-    // epilogue all wait on it, each before its ring slot could be reused
+    uint8_t *xring = smem;                              // [kXStages][2 panels][128 rows][128 B]
+    uint8_t *aring = smem + kXStages * kXStage;         // [kASlots][2 panels][128 rows][128 B]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(aring + kASlots * kASlot);
+    // done[u % kRing] completes when the MMAs of unit u = 2 * kb + half have
+    // finished (one tcgen05.commit per unit); the x producer, the decoders
+    // and the epilogue all wait on it, each before its slot could be reused
     uint64_t *x_full = bars;                 // [kXStages]
-    uint64_t *done = bars + kXStages;        // [kRing]
-    uint64_t *a_full = done + kRing;         // [2]
-    uint64_t *d_empty = a_full + 2;          // [2]
-    uint64_t *d_full = d_empty + 2;          // ROW: all MMAs of the tile done
+    uint64_t *done = x_full + kXStages;      // [kRing]
+    uint64_t *a_full = done + kRing;         // [kASlots]
+    uint64_t *d_empty = a_full + kASlots;    // [2] one per half
+    uint64_t *d_full = d_empty + 2;          // ROW: every MMA of the tile done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_full + 1);
     int *s_fail = reinterpret_cast<int *>(d_full + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileW;
     const int m0 = blockIdx.y * kTileX;
+    const int units = 2 * kblocks;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kXStages; ++i) mbar_init(&x_full[i], 1);
         for (int i = 0; i < kRing; ++i) mbar_init(&done[i], 1);  // tcgen05.commit
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&a_full[i], kNumDec);   // one arrival per decoder warp
-            mbar_init(&d_empty[i], kNumEpi);  // one arrival per epilogue warp
-        }
-        mbar_init(d_full, 1);  // tcgen05.commit
+        for (int i = 0; i < kASlots; ++i) mbar_init(&a_full[i], kNumDec);  // one arrival per decoder warp
+        for (int i = 0; i < 2; ++i) mbar_init(&d_empty[i], kNumEpi / 2);   // the half's epilogue warps
+        mbar_init(d_full, 1);
         *s_fail = 0;
         fence_mbarrier_init();
     }
@@ -196,36 +199,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     if (warp == kWarpMma) {
         // ------------------------------------------------------ MMA issuer
-        int issued = 0;  // K blocks whose MMAs were committed
+        int issued = 0;  // units whose MMAs were committed
         if (lane == 0) {
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int xs = kb % kXStages, as = kb & 1, db = ROW ? 0 : (kb & 1);
-                bool ok = mbar_wait_bounded(&x_full[xs], (kb / kXStages) & 1) &&
-                          mbar_wait_bounded(&a_full[as], (kb >> 1) & 1) &&
-                          (ROW || kb < 2 || mbar_wait_bounded(&d_empty[db], ((kb >> 1) - 1) & 1));
+            for (int u = 0; u < units; ++u) {
+                const int kb = u >> 1, h = u & 1, xs = u % kXStages, as = kb % kASlots;
+                bool ok = mbar_wait_bounded(&x_full[xs], (u / kXStages) & 1) &&
+                          (h == 1 || mbar_wait_bounded(&a_full[as], (kb / kASlots) & 1)) &&
+                          (ROW || kb == 0 || mbar_wait_bounded(&d_empty[h], (kb - 1) & 1));
                 if (!ok) {
                     fail(ERRBIT_MMA_WAIT);
                     *reinterpret_cast<volatile int *>(s_fail) = 1;
                     break;
                 }
                 tc_fence_after();
-                // descriptor of the stage's first 16-column slice; the others
-                // are 32 bytes (2 in address/16 units) apart within a 64-column
-                // panel, and panels are kXPanel bytes apart
-                const uint64_t desc0 = sw128_desc(smem_u32(smem + xs * kXStage));
-                const uint32_t d_tmem = tmem + kColD + db * 128;
-                const uint32_t a_tmem = tmem + kColA + as * 64;
+                // descriptors of the first 16-column slices; the others are 32
+                // bytes (2 in address/16 units) apart within a 64-column panel
+                const uint64_t adesc = sw128_desc(smem_u32(aring + as * kASlot));
+                const uint64_t bdesc = sw128_desc(smem_u32(xring + xs * kXStage));
+                const uint32_t d_tmem = tmem + (ROW ? kColT : kColD) + h * 128;
 #pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk)
-                    tc_mma(d_tmem, a_tmem + kk * 8, desc0 + (kk >> 2) * (kXPanel >> 4) + (kk & 3) * 2,
-                           (kk > 0 || (ROW && kb > 0)) ? 1u : 0u);
-                tc_commit(&done[kb % kRing]);
-                issued = kb + 1;
+                for (int kk = 0; kk < kKB / 16; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>((kk >> 2) * (kPanel >> 4) + (kk & 3) * 2);
+                    tc_mma_ss(d_tmem, adesc + off, bdesc + off, (kk > 0 || (ROW && kb > 0)) ? 1u : 0u);
+                }
+                tc_commit(&done[u % kRing]);
+                issued = u + 1;
             }
             // ROW: the epilogue's single wait (also after a failure, so that
             // it does not sit out its whole time limit)
             if (ROW) tc_commit(d_full);
-            // drain: wait for the last committed block before TMEM can be freed
+            // drain: wait for the last committed unit before TMEM can be freed
             if (issued > 0 && !mbar_wait_bounded(&done[(issued - 1) % kRing], ((issued - 1) / kRing) & 1))
                 fail(ERRBIT_MMA_WAIT);
         }
@@ -234,31 +237,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // ------------------------------------------------------ x producer
         if (lane == 0) {
             int issued = 0;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int xs = kb % kXStages;
-                if (kb >= kXStages && !mbar_wait_bounded(&done[(kb - kXStages) % kRing], ((kb - kXStages) / kRing) & 1)) {
+            for (int u = 0; u < units; ++u) {
+                const int xs = u % kXStages;
+                if (u >= kXStages &&
+                    !mbar_wait_bounded(&done[(u - kXStages) % kRing], ((u - kXStages) / kRing) & 1)) {
                     fail(ERRBIT_EMPTY_WAIT);
                     break;
                 }
                 if (*reinterpret_cast<volatile int *>(s_fail)) break;
-                uint8_t *st = smem + xs * kXStage;
+                uint8_t *st = xring + xs * kXStage;
+                const int kx = (u >> 1) * kKB, mx = m0 + (u & 1) * kHalfX;
                 mbar_arrive_expect_tx(&x_full[xs], kXStage);
-                tma_load_2d(st, &tm_x, &x_full[xs], kb * kKB, m0);
-                tma_load_2d(st + kXPanel, &tm_x, &x_full[xs], kb * kKB + 64, m0);
-                issued = kb + 1;
+                tma_load_2d(st, &tm_x, &x_full[xs], kx, mx);
+                tma_load_2d(st + kPanel, &tm_x, &x_full[xs], kx + 64, mx);
+                issued = u + 1;
             }
             // never leave with copies in flight: wait for the last stages issued
-            for (int kb = issued - kXStages < 0 ? 0 : issued - kXStages; kb < issued; ++kb)
-                if (!mbar_wait_bounded(&x_full[kb % kXStages], (kb / kXStages) & 1)) fail(ERRBIT_FULL_WAIT);
+            for (int u = issued - kXStages < 0 ? 0 : issued - kXStages; u < issued; ++u)
+                if (!mbar_wait_bounded(&x_full[u % kXStages], (u / kXStages) & 1)) fail(ERRBIT_FULL_WAIT);
         }
         __syncwarp();
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------------------ decoders
-        // thread = one weight row (its TMEM lane); this warp converts the K
-        // half kh (64 codes) of its rows for every K block, two blocks ahead
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // thread = one weight row r; this warp converts the K half kh (64
+        // codes = one 128-byte swizzled row of A panel kh) for every K block,
+        // two blocks ahead of the conversion
+        const int r = (warp & 3) * 32 + lane;
         const int kh = (warp - kWarpDec0) >> 2;
-        const int row = n0 + q * 32 + lane;
+        const int row = n0 + r;
         const bool row_ok = row < n;
         const uint8_t *rp = codes + static_cast<int64_t>(row_ok ? row : 0) * k + kh * 64;
         auto load4 = [&](int kb, uint4 (&v)[4]) {
@@ -272,30 +278,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         load4(0, c0);
         load4(1, c1);
         for (int kb = 0; kb < kblocks; ++kb) {
-            const int as = kb & 1;
+            const int as = kb % kASlots;
             load4(kb + 2, c2);  // in flight while this block is converted
-            bool ok = kb < 2 || mbar_wait_bounded(&done[(kb - 2) % kRing], ((kb - 2) / kRing) & 1);
+            // slot `as` was last read by the MMAs of K block kb - kASlots,
+            // whose last unit is 2 (kb - kASlots) + 1
+            const int prev = 2 * (kb - kASlots) + 1;
+            bool ok = kb < kASlots || mbar_wait_bounded(&done[prev % kRing], (prev / kRing) & 1);
             if (!__all_sync(0xffffffffu, ok) || *reinterpret_cast<volatile int *>(s_fail)) {
                 if (lane == 0) fail(ERRBIT_EMPTY_WAIT);
                 break;
             }
-            tc_fence_after();
-            uint32_t v[32];
+            uint8_t *arow = aring + as * kASlot + kh * kPanel + r * 128;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint4 c = c0[j];
-                v[8 * j + 0] = e4m3x2_to_bf16x2(c.x, 0x9180u);
-                v[8 * j + 1] = e4m3x2_to_bf16x2(c.x, 0xB3A2u);
-                v[8 * j + 2] = e4m3x2_to_bf16x2(c.y, 0x9180u);
-                v[8 * j + 3] = e4m3x2_to_bf16x2(c.y, 0xB3A2u);
-                v[8 * j + 4] = e4m3x2_to_bf16x2(c.z, 0x9180u);
-                v[8 * j + 5] = e4m3x2_to_bf16x2(c.z, 0xB3A2u);
-                v[8 * j + 6] = e4m3x2_to_bf16x2(c.w, 0x9180u);
-                v[8 * j + 7] = e4m3x2_to_bf16x2(c.w, 0xB3A2u);
+                // 16 codes -> two 16-byte chunks (2j, 2j + 1) of this row
+                uint4 lo, hi;
+                lo.x = e4m3x2_to_bf16x2(c.x, 0x9180u);
+                lo.y = e4m3x2_to_bf16x2(c.x, 0xB3A2u);
+                lo.z = e4m3x2_to_bf16x2(c.y, 0x9180u);
+                lo.w = e4m3x2_to_bf16x2(c.y, 0xB3A2u);
+                hi.x = e4m3x2_to_bf16x2(c.z, 0x9180u);
+                hi.y = e4m3x2_to_bf16x2(c.z, 0xB3A2u);
+                hi.z = e4m3x2_to_bf16x2(c.w, 0x9180u);
+                hi.w = e4m3x2_to_bf16x2(c.w, 0xB3A2u);
+                *reinterpret_cast<uint4 *>(arow + (((2 * j) ^ (r & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4 *>(arow + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
             }
-            tc_st32(tmem + (static_cast<uint32_t>(q * 32) << 16) + kColA + as * 64 + kh * 32, v);
-            tc_wait_st();
-            tc_fence_before();
+            fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[as]);
 #pragma unroll
@@ -306,14 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     } else {
         // ------------------------------------------------------ epilogue
-        // thread = one weight row (TMEM lane); this warp promotes the 64
-        // accumulator columns (rows of x) of half ch
+        // thread = one weight row (TMEM lane of quarter q); this warp owns
+        // the 128 accumulator columns (rows of x) of half h
         const int q = warp & 3;
-        const int ch = (warp - kWarpEpi0) >> 2;
-        float acc[kTileX / 2];
-#pragma unroll
-        for (int i = 0; i < kTileX / 2; ++i) acc[i] = 0.0f;
-        const float *srow = scales + (ROW ? 0 : static_cast<int64_t>(blockIdx.x) * kblocks);
+        const int h = (warp - kWarpEpi0) >> 2;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t t_addr = lane_base + kColT + h * 128;
+        const uint32_t d_addr = lane_base + kColD + h * 128;
+        const int row = n0 + q * 32 + lane;
         bool ok = true;
         if (ROW) {
             ok = mbar_wait_bounded(d_full, 0);
@@ -322,52 +332,68 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 ok = false;
             } else {
                 ok = *reinterpret_cast<volatile int *>(s_fail) == 0;
-                tc_fence_after();
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kColD + ch * 64;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[16];
-                    tc_ld16(taddr + 16 * c, v);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[16 * c + i] = __uint_as_float(v[i]);
+            }
+        } else {
+            const float *srow = scales + static_cast<int64_t>(blockIdx.x) * kblocks;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                const float s = __ldg(srow + kb);
+                uint64_t s2;
+                asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(s));
+                const int u = 2 * kb + h;
+                ok = mbar_wait_bounded(&done[u % kRing], (u / kRing) & 1);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) fail(ERRBIT_FULL_WAIT);
+                    ok = false;
+                    break;
                 }
-                const int row = n0 + q * 32 + lane;
-                const float rs = row < n ? __ldg(scales + static_cast<int64_t>(row) * row_stride) : 0.0f;
-#pragma unroll
-                for (int i = 0; i < kTileX / 2; ++i) acc[i] *= rs;
-            }
-        }
-        for (int kb = 0; ROW ? false : kb < kblocks; ++kb) {
-            const int db = kb & 1;
-            const float s = __ldg(srow + kb);
-            ok = mbar_wait_bounded(&done[kb % kRing], (kb / kRing) & 1);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) fail(ERRBIT_FULL_WAIT);
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kColD + db * 128 + ch * 64;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[16];
-                tc_ld16(taddr + 16 * c, v);
+                tc_fence_after();
+                // T_h += s * D_h, 16 columns at a time; the loads of chunk
+                // c + 1 are in flight while chunk c is combined and stored
+                uint32_t dv[2][16], tv[2][16];
+                tc_ld16(d_addr, dv[0]);
+                if (kb > 0) tc_ld16(t_addr, tv[0]);
                 tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[16 * c + i] = fmaf(s, __uint_as_float(v[i]), acc[16 * c + i]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&d_empty[db]);
-        }
-        // thread = weight row, acc[i] = y[m0 + 64 ch + i][row]
-        const int row = n0 + q * 32 + lane;
-        if (ok && row < n) {
+                for (int c = 0; c < 8; ++c) {
+                    const int cur = c & 1, nxt = cur ^ 1;
+                    if (c + 1 < 8) {
+                        tc_ld16(d_addr + 16 * (c + 1), dv[nxt]);
+                        if (kb > 0) tc_ld16(t_addr + 16 * (c + 1), tv[nxt]);
+                    }
+                    if (kb > 0) {
 #pragma unroll
-            for (int i = 0; i < kTileX / 2; ++i) {
-                const int mi = m0 + ch * 64 + i;
-                if (mi < m) y[static_cast<int64_t>(mi) * n + row] = __float2bfloat16_rn(acc[i]);
+                        for (int i = 0; i < 16; i += 2) ffma2(tv[cur][i], tv[cur][i + 1], s2, dv[cur][i], dv[cur][i + 1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) tv[cur][i] = __float_as_uint(s * __uint_as_float(dv[cur][i]));
+                    }
+                    tc_st16(t_addr + 16 * c, tv[cur]);
+                    tc_wait_ld();
+                }
+                // D_h has been read: the next unit of this half may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&d_empty[h]);
+                tc_wait_st();  // T_h is read again by the next K block
+            }
+        }
+        // thread = weight row, column j of T_h = y[m0 + 128 h + j][row]
+        if (ok) {
+            tc_fence_after();
+            const float rs = !ROW ? 1.0f : (row < n ? __ldg(scales + static_cast<int64_t>(row) * row_stride) : 0.0f);
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+                uint32_t v[16];
+                tc_ld16(t_addr + 16 * c, v);
+                tc_wait_ld();
+                if (row < n) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int mi = m0 + h * kHalfX + 16 * c + i;
+                        const float val = ROW ? __uint_as_float(v[i]) * rs : __uint_as_float(v[i]);
+                        if (mi < m) y[static_cast<int64_t>(mi) * n + row] = __float2bfloat16_rn(val);
+                    }
+                }
             }
         }
     }
@@ -408,7 +434,7 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
     }
     CUtensorMap tm_x;
     const uint64_t k = static_cast<uint64_t>(a.k), m = static_cast<uint64_t>(a.m);
-    if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64, kTileX,
+    if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64, kHalfX,
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
