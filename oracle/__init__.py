@@ -72,11 +72,12 @@ def _load():
         lib.oracle_row_quantize_rows.argtypes = [p, i64, i64, p, i64, p, p]
         lib.oracle_tensor_quantize_rows.argtypes = [p, i64, i64, p, i64, p, p]
         lib.oracle_row_gemv.argtypes = [p, i64, p, p, i64, i64, i64, p, i64, p]
+        lib.oracle_w8a8_gemv.argtypes = [p, i64, ctypes.c_float, p, ctypes.c_float, i64, i64, p, i64, p]
         for f in ("oracle_block_quantize", "oracle_block_quantize_tile",
                   "oracle_mx_quantize", "oracle_mx_quantize_rows",
                   "oracle_block_gemv", "oracle_mx_gemv",
                   "oracle_row_quantize_rows", "oracle_tensor_quantize_rows",
-                  "oracle_row_gemv"):
+                  "oracle_row_gemv", "oracle_w8a8_gemv"):
             getattr(lib, f).restype = None
         _lib = lib
         return lib
@@ -261,6 +262,27 @@ def row_gemv(x, codes: np.ndarray, scales: np.ndarray, rows=None) -> np.ndarray:
     y = np.zeros((m, nrows), dtype=np.float64)
     _load().oracle_row_gemv(_ptr(x), m, _ptr(codes), _ptr(scales), stride, n, k,
                             None if rows is None else _ptr(rows), nrows, _ptr(y))
+    return y
+
+
+def act_quantize(x) -> tuple[np.ndarray, np.ndarray]:
+    """Dynamic per-tensor activation quantization: x [M,K] bf16 bits ->
+    (codes u8 [M,K], scale f32 [1]); the per-tensor rule applied to x."""
+    return tensor_quantize(x)
+
+
+def w8a8_gemv(xcodes: np.ndarray, sx, wcodes: np.ndarray, sw, rows=None) -> np.ndarray:
+    """fp64 y[M, len(rows)] = sx * sw * dec(xcodes) . dec(wcodes)^T."""
+    xcodes = np.ascontiguousarray(xcodes, dtype=np.uint8)
+    wcodes = np.ascontiguousarray(wcodes, dtype=np.uint8)
+    m, k = xcodes.shape
+    n, k2 = wcodes.shape
+    assert k == k2
+    rows, nrows = _rows_arg(rows, n)
+    y = np.zeros((m, nrows), dtype=np.float64)
+    _load().oracle_w8a8_gemv(_ptr(xcodes), m, float(np.float32(np.ravel(sx)[0])), _ptr(wcodes),
+                             float(np.float32(np.ravel(sw)[0])), n, k,
+                             None if rows is None else _ptr(rows), nrows, _ptr(y))
     return y
 
 

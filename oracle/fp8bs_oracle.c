@@ -411,3 +411,33 @@ void oracle_row_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
             y64[mi * nrows + j] = sum;
         }
 }
+
+/* ---------------------------------------------------------------------
+ * W8A8 (FreeToken PR #389, What this adds: a dynamic per-tensor activation
+ * scale -- an amax pass, then the cast -- and a GEMM of the e4m3
+ * activations with the per-tensor e4m3 weight, scaled by both scales).
+ * The activation quantizer is oracle_tensor_quantize applied to x.
+ * y64[mi, j] = sx * sw * sum_k dec(qx[mi,k]) * dec(qw[r,k]), r = rows[j]:
+ * every product of two e4m3 values is exact in binary64, as is the
+ * multiplication by the two binary32 scales of an exact sum.
+ * ------------------------------------------------------------------- */
+void oracle_w8a8_gemv(const uint8_t *xcodes, int64_t m, float sx,
+                      const uint8_t *wcodes, float sw, int64_t n, int64_t k,
+                      const int64_t *rows, int64_t nrows, double *y64)
+{
+    double dec[256];
+    int64_t mi, j, c;
+    int i;
+    if (rows == NULL)
+        nrows = n;
+    for (i = 0; i < 256; ++i)
+        dec[i] = oracle_e4m3_decode((uint8_t)i);
+    for (mi = 0; mi < m; ++mi)
+        for (j = 0; j < nrows; ++j) {
+            int64_t r = rows ? rows[j] : j;
+            double sum = 0.0;
+            for (c = 0; c < k; ++c)
+                sum += dec[xcodes[mi * k + c]] * dec[wcodes[r * k + c]];
+            y64[mi * nrows + j] = sum * (double)sx * (double)sw;
+        }
+}

@@ -101,6 +101,13 @@ void oracle_row_gemv(const uint16_t *x, int64_t m, const uint8_t *codes,
                      int64_t k, const int64_t *rows, int64_t nrows,
                      double *y64);
 
+/* W8A8: x quantized per tensor (oracle_tensor_quantize of x gives xcodes,
+ * sx), weight per tensor (wcodes, sw).  y64[mi, j] = sx * sw *
+ * sum_k dec(qx[mi,k]) * dec(qw[rows[j],k]) in fp64; rows == NULL: all. */
+void oracle_w8a8_gemv(const uint8_t *xcodes, int64_t m, float sx,
+                      const uint8_t *wcodes, float sw, int64_t n, int64_t k,
+                      const int64_t *rows, int64_t nrows, double *y64);
+
 #ifdef __cplusplus
 }
 #endif
