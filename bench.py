@@ -320,6 +320,45 @@ def rowwise_workload(torch, fp8bs, inputs, dev):
     return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,2,true>", [0, 1, 3, 4]))
 
 
+def w8a8_workload(torch, fp8bs, inputs, dev):
+    """lm_head [152064, 4096] per-tensor e4m3 weight x dynamically quantized
+    e4m3 activations (FreeToken PR #389's W8A8 route), M = 1, 8, 16: the GEMM
+    alone on pre-quantized x, and the whole linear (activation quantize +
+    GEMM) per call."""
+    ms = [1, 8, 16]
+    w = inputs.lm_head_weight(2, device=dev)
+    n, k = w.shape
+    wq, sw = fp8bs.tensor_quantize(w)
+    del w
+    xs = {m: inputs.activations(m, k, 100 + m, device=dev) for m in ms}
+    xq = {m: fp8bs.act_quantize(xs[m]) for m in ms}
+    ys = {m: torch.empty((m, n), dtype=torch.bfloat16, device=dev) for m in ms}
+    gb = lambda m: n * k + 4 + m * k + 4 + 2 * m * n
+    calls = [(f"gemm M={m}", m, gb(m), (lambda m=m: fp8bs.w8a8_gemm(xq[m][0], xq[m][1], wq, sw, y=ys[m])))
+             for m in ms]
+    calls += [(f"linear M={m}", m, gb(m) + 2 * m * k,
+               (lambda m=m: fp8bs.w8a8_linear(xs[m], wq, sw, y=ys[m], xq=xq[m][0], sx=xq[m][1]))) for m in ms]
+    cfg = {"workload": "lm_head [152064,4096] W8A8 (per-tensor e4m3 weight, dynamic per-tensor e4m3 "
+                       "activations): GEMM alone and activation-quantize + GEMM, M=1,8,16", "n": n, "k": k,
+           "ms": ms, "l2": "inputs larger than L2 (623 MB of codes per call)"}
+    return dict(calls=calls, cfg=cfg, dominant=("w8a8_decode_kernel<1>", [0, 1]),
+                call_launches=[1, 1, 1, 2, 2, 2])
+
+
+def w8a8_prefill_workload(torch, fp8bs, inputs, dev):
+    ms = [512, 2048, 4096]
+    wq, sw = fp8bs.tensor_quantize(inputs.sweep_weight(0, device=dev))
+    n, k = inputs.SWEEP_SHAPE
+    calls = []
+    for m in ms:
+        xq, sx = fp8bs.act_quantize(inputs.activations(m, k, 700 + m, device=dev))
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        calls.append((f"M={m}", m, 2 * m * n * k, (lambda xq=xq, sx=sx, y=y: fp8bs.w8a8_gemm(xq, sx, wq, sw, y=y))))
+    cfg = {"workload": "prefill: W8A8 [12288,4096] e4m3 x e4m3 GEMM on tcgen05 (kind::f8f6f4), M=512,2048,4096",
+           "n": n, "k": k, "ms": ms, "l2": "weight (50 MB) and x fit in L2; compute-bound"}
+    return dict(calls=calls, cfg=cfg, dominant=("w8a8_prefill_kernel", [0, 1, 2]), flops=True, fp8=True)
+
+
 def quantize_workload(torch, fp8bs, inputs, dev):
     w = inputs.heavy_tail_weight(5, device=dev)
     n, k = w.shape
@@ -464,7 +503,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="lm_head",
-                    choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill", "rowwise"])
+                    choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill", "rowwise", "w8a8",
+                             "w8a8_prefill"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -521,6 +561,10 @@ def main():
         wl = prefill_workload(torch, fp8bs, inputs, dev, args.scales)
     elif args.workload == "rowwise":
         wl = rowwise_workload(torch, fp8bs, inputs, dev)
+    elif args.workload == "w8a8":
+        wl = w8a8_workload(torch, fp8bs, inputs, dev)
+    elif args.workload == "w8a8_prefill":
+        wl = w8a8_prefill_workload(torch, fp8bs, inputs, dev)
     else:
         wl = quantize_workload(torch, fp8bs, inputs, dev)
     torch.cuda.synchronize()
@@ -542,6 +586,10 @@ def main():
     scale_unit = 1e12 if flops else 1e9
     unit = "TFLOP/s" if flops else "GB/s"
     tpeak, tpeak_kind = tensor_peak()
+    if wl.get("fp8"):
+        # e4m3 tensor-core peak: the measured bf16 peak times the nominal
+        # fp8 : bf16 ratio (4.5 : 2.25 PFLOP/s dense)
+        tpeak, tpeak_kind = 2.0 * tpeak, tpeak_kind + " x 2 (fp8 : bf16 nominal)"
     value = all_bytes / (total_ms * 1e-3) / scale_unit
     per_call = {}
     for (name, m, b, _), t in zip(calls, per):
@@ -549,7 +597,7 @@ def main():
         rate = b / (t * 1e-3) / scale_unit
         if flops:
             per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "tflop_s": round(rate, 1),
-                              "frac_of_measured_bf16": round(rate / tpeak, 4)}
+                              "frac_of_peak": round(rate / tpeak, 4)}
         else:
             per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "gb_s": round(rate, 1),
                               "frac_of_8TBps": round(rate / HBM_NOMINAL_GBS, 4),
@@ -561,7 +609,8 @@ def main():
     if flops:
         roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1), "peak": tpeak,
                     "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
-                    "peak_kind": f"bf16_tflops ({tpeak_kind})", "traffic": None}
+                    "peak_kind": f"bf16_tflops ({tpeak_kind})", "traffic": None,
+                    "dtype": "e4m3" if wl.get("fp8") else "bf16"}
     else:
         roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",

@@ -15,6 +15,9 @@ Functions (names follow the C entry points):
     row_quantize(w)        -> (codes u8 [N,K], scales f32 [N])       (fp8row_*)
     tensor_quantize(w)     -> (codes u8 [N,K], scale f32 [1])        (fp8tensor_*)
     row_gemv(x, codes, s)  -> y bf16 [M,N]; s is [N] (per row) or [1] (per tensor)
+    act_quantize(x)        -> (x codes u8 [M,K], scale f32 [1])      (fp8act_quantize)
+    w8a8_gemm(xq, sx, wq, sw) -> y bf16 [M,N]                        (w8a8_gemm)
+    w8a8_linear(x, wq, sw) -> y bf16 [M,N]: act_quantize then w8a8_gemm
 """
 from __future__ import annotations
 
@@ -65,6 +68,9 @@ def lib() -> ctypes.CDLL:
         L.fp8row_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
         L.fp8tensor_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
         L.fp8tensor_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
+        L.fp8act_quantize.argtypes = [p, i64, i64, p, p, p]
+        L.w8a8_gemm.argtypes = [p, i64, p, p, p, i64, i64, p, p]
+        L.w8a8_gemm_ex.argtypes = [p, i64, p, p, p, i64, i64, p, i32, p]
         L.fp8bs_select_path.argtypes = [i64, i64, i64, p, p, i32]
         L.fp8bs_strerror.argtypes = [i32]
         L.fp8bs_strerror.restype = ctypes.c_char_p
@@ -72,7 +78,8 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_version.argtypes = []
         for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
-                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8bs_select_path", "fp8bs_check_device_error",
+                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
+                  "fp8bs_select_path", "fp8bs_check_device_error",
                   "fp8bs_version"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -215,6 +222,40 @@ def row_gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
               _dev(scales, torch.float32, "scales"), n, k, _dev(y, torch.bfloat16, "y"), int(path),
               _stream(stream)), "fp8row_gemv" if per_row else "fp8tensor_gemv")
     return y
+
+
+def act_quantize(x, codes=None, scale=None, stream=None):
+    """Dynamic per-tensor e4m3 quantization of bf16 activations [M, K]."""
+    import torch
+    m, k = x.shape
+    if codes is None:
+        codes = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _check(lib().fp8act_quantize(_dev(x, torch.bfloat16, "x"), m, k, _dev(codes, torch.uint8, "codes"),
+                                 _dev(scale, torch.float32, "scale"), _stream(stream)), "fp8act_quantize")
+    return codes, scale
+
+
+def w8a8_gemm(xq, sx, wq, sw, y=None, path: int = PATH_AUTO, stream=None):
+    """y[M, N] = sx * sw * dec(xq) . dec(wq)^T (e4m3 x e4m3, fp32 accumulate, bf16 out)."""
+    import torch
+    m, k = xq.shape
+    n = wq.shape[0]
+    if wq.shape[1] != k:
+        raise ValueError("x codes and weight codes disagree on K")
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device)
+    _check(lib().w8a8_gemm_ex(_dev(xq, torch.uint8, "xq"), m, _dev(sx, torch.float32, "sx"),
+                              _dev(wq, torch.uint8, "wq"), _dev(sw, torch.float32, "sw"), n, k,
+                              _dev(y, torch.bfloat16, "y"), int(path), _stream(stream)), "w8a8_gemm")
+    return y
+
+
+def w8a8_linear(x, wq, sw, y=None, xq=None, sx=None, path: int = PATH_AUTO, stream=None):
+    """The W8A8 route end to end: quantize x per tensor, then w8a8_gemm."""
+    xq, sx = act_quantize(x, codes=xq, scale=sx, stream=stream)
+    return w8a8_gemm(xq, sx, wq, sw, y=y, path=path, stream=stream)
 
 
 def select_path(m: int, n: int, k: int, x_ptr: int = 0, codes_ptr: int = 0, mx: bool = False) -> int:

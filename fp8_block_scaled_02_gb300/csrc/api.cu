@@ -70,11 +70,22 @@ int gemv_dispatch(const DecodeArgs &a, int path, cudaStream_t st) {
     }
 }
 
+int run_w8a8_decode_chunks(const W8A8Args &a, cudaStream_t st) {
+    for (int64_t m0 = 0; m0 < a.m; m0 += kDecodeMaxM) {
+        W8A8Args c = a;
+        c.m = a.m - m0 < kDecodeMaxM ? a.m - m0 : kDecodeMaxM;
+        c.xq = a.xq + m0 * a.k;
+        c.y = static_cast<char *>(a.y) + m0 * a.n * 2;
+        if (launch_w8a8_decode(c, st) != cudaSuccess) return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-int fp8bs_version(void) { return 101; }
+int fp8bs_version(void) { return 102; }
 
 const char *fp8bs_strerror(int status) {
     switch (status) {
@@ -188,6 +199,38 @@ int fp8tensor_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const fl
     return rowwise_gemv(x_bf16, m, codes, scale, n, k, y_bf16, 0, FP8BS_PATH_AUTO, stream);
 }
 
+int fp8act_quantize(const void *x_bf16, int64_t m, int64_t k, uint8_t *codes_u8, float *scale_f32, void *stream) {
+    if (m <= 0 || k <= 0 || m >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (!x_bf16 || !codes_u8 || !scale_f32) return FP8BS_ERR_NULL;
+    if (!aligned(x_bf16, 2) || !aligned(scale_f32, 4)) return FP8BS_ERR_ALIGN;
+    const bool vec = (k % 8) == 0 && aligned(x_bf16, 16) && aligned(codes_u8, 8);
+    return cuda_status(launch_act_quantize(x_bf16, m, k, codes_u8, scale_f32, vec, static_cast<cudaStream_t>(stream)));
+}
+
+int w8a8_gemm_ex(const uint8_t *x_codes, int64_t m, const float *x_scale, const uint8_t *w_codes,
+                 const float *w_scale, int64_t n, int64_t k, void *y_bf16, int path, void *stream) {
+    if (m < 0 || n <= 0 || k <= 0 || m >= kMaxDim || n >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (path < FP8BS_PATH_AUTO || path > FP8BS_PATH_GENERIC) return FP8BS_ERR_PATH;
+    if (m == 0) return FP8BS_OK;
+    if (!x_codes || !x_scale || !w_codes || !w_scale || !y_bf16) return FP8BS_ERR_NULL;
+    if (!aligned(x_scale, 4) || !aligned(w_scale, 4) || !aligned(y_bf16, 2)) return FP8BS_ERR_ALIGN;
+    const bool tma = tma_ok(k, x_codes, w_codes);
+    if (path == FP8BS_PATH_AUTO) path = !tma ? FP8BS_PATH_GENERIC : (m <= kDecodeMaxM ? FP8BS_PATH_DECODE : FP8BS_PATH_PREFILL);
+    const W8A8Args a{x_codes, x_scale, w_codes, w_scale, y_bf16, m, n, k};
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (path) {
+        case FP8BS_PATH_GENERIC: return cuda_status(launch_w8a8_generic(a, st));
+        case FP8BS_PATH_DECODE: return tma ? run_w8a8_decode_chunks(a, st) : FP8BS_ERR_PATH;
+        case FP8BS_PATH_PREFILL: return tma ? cuda_status(launch_w8a8_prefill(a, st)) : FP8BS_ERR_PATH;
+        default: return FP8BS_ERR_PATH;
+    }
+}
+
+int w8a8_gemm(const uint8_t *x_codes, int64_t m, const float *x_scale, const uint8_t *w_codes, const float *w_scale,
+              int64_t n, int64_t k, void *y_bf16, void *stream) {
+    return w8a8_gemm_ex(x_codes, m, x_scale, w_codes, w_scale, n, k, y_bf16, FP8BS_PATH_AUTO, stream);
+}
+
 int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16, const void *codes, int mx) {
     (void)n;
     if (m <= 0 || k <= 0) return FP8BS_ERR_SHAPE;
@@ -196,7 +239,7 @@ int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16, const
 
 int fp8bs_check_device_error(void *stream, uint32_t *word_out) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
-    const uint32_t w = take_decode_error() | take_prefill_error();
+    const uint32_t w = take_decode_error() | take_prefill_error() | take_w8a8_error();
     if (word_out) *word_out = w;
     return w ? FP8BS_ERR_DEVICE : FP8BS_OK;
 }

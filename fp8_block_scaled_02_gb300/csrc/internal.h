@@ -19,6 +19,11 @@ cudaError_t launch_row_quantize(const void *w, int64_t n, int64_t k, uint8_t *co
                                 float *scales, bool vector_ok, cudaStream_t stream);
 cudaError_t launch_tensor_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
                                    float *scale, bool vector_ok, cudaStream_t stream);
+// dynamic per-tensor activation quantization (the per-tensor rule); up to
+// kActSmall elements in one single-CTA launch, larger tensors grid-wide
+constexpr int64_t kActSmall = 65536;
+cudaError_t launch_act_quantize(const void *x, int64_t m, int64_t k, uint8_t *codes, float *scale,
+                                bool vector_ok, cudaStream_t stream);
 
 // How the weight's scales are laid out.
 enum ScaleKind : int {
@@ -47,6 +52,20 @@ cudaError_t launch_generic_gemv(const DecodeArgs &a, cudaStream_t stream);
 // prefill.cu -- tcgen05 block-FP8 / row-scaled FP8 GEMM for larger m.
 cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream);
 uint32_t take_prefill_error();
+
+// w8a8.cu -- e4m3 activations x e4m3 weight, both scaled per tensor.
+struct W8A8Args {
+    const uint8_t *xq;       // e4m3 [m, k] (row offset already applied)
+    const float *sx;         // activation scale [1]
+    const uint8_t *wq;       // e4m3 [n, k]
+    const float *sw;         // weight scale [1]
+    void *y;                 // bf16 [m, n] (row offset already applied)
+    int64_t m, n, k;
+};
+cudaError_t launch_w8a8_decode(const W8A8Args &a, cudaStream_t stream);   // m <= 32
+cudaError_t launch_w8a8_prefill(const W8A8Args &a, cudaStream_t stream);  // tcgen05
+cudaError_t launch_w8a8_generic(const W8A8Args &a, cudaStream_t stream);  // any shape / alignment
+uint32_t take_w8a8_error();
 
 // tensormap.cu -- cuTensorMapEncodeTiled through the runtime's driver entry
 // point (no link against libcuda).

@@ -357,6 +357,39 @@ __global__ void tensor_finalize_kernel(float *scale) {
     }
 }
 
+// ------------------------------------------------- small per-tensor (one CTA)
+// Activations at decode sizes: amax and cast in one launch of one CTA (the
+// per-call cost, not the bytes, dominates there); same arithmetic as the
+// grid-wide per-tensor path, so a tensor quantizes to the same bits either way.
+constexpr int kActThreads = 1024;
+
+template <bool VEC>
+__global__ void __launch_bounds__(kActThreads) tensor_quantize_small_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                          int64_t total, uint8_t *__restrict__ codes,
+                                                                          float *__restrict__ scale) {
+    __shared__ float warp_amax[kActThreads / 32];
+    const uint16_t *wb = reinterpret_cast<const uint16_t *>(w);
+    float amax = 0.0f;
+    if (VEC) {
+        for (int64_t c = threadIdx.x; c < total / 8; c += kActThreads) amax = absmax8(ld_nc_v4(w + c * 8), amax);
+    } else {
+        for (int64_t e = threadIdx.x; e < total; e += kActThreads)
+            amax = fmaxf(amax, fabsf(__uint_as_float(static_cast<uint32_t>(wb[e]) << 16)));
+    }
+    amax = cta_max(amax, warp_amax);
+    const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+    if (threadIdx.x == 0) *scale = s;
+    if (VEC) {
+        for (int64_t c = threadIdx.x; c < total / 8; c += kActThreads)
+            *reinterpret_cast<uint2 *>(codes + c * 8) = encode8_div(ld_nc_v4(w + c * 8), s);
+    } else {
+        for (int64_t e = threadIdx.x; e < total; e += kActThreads) {
+            const float q = __uint_as_float(static_cast<uint32_t>(wb[e]) << 16) / s;
+            codes[e] = static_cast<uint8_t>(f32x2_to_e4m3x2(q, 0.0f) & 0xFF);
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_block_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
@@ -424,6 +457,18 @@ cudaError_t launch_tensor_quantize(const void *w, int64_t n, int64_t k, uint8_t 
         tensor_encode_kernel<false><<<g, kTensorThreads, 0, stream>>>(wb, total, codes, amax_bits);
     }
     tensor_finalize_kernel<<<1, 32, 0, stream>>>(scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_act_quantize(const void *x, int64_t m, int64_t k, uint8_t *codes, float *scale,
+                                bool vector_ok, cudaStream_t stream) {
+    const int64_t total = m * k;
+    if (total > kActSmall) return launch_tensor_quantize(x, m, k, codes, scale, vector_ok, stream);
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
+    if (vector_ok)
+        tensor_quantize_small_kernel<true><<<1, kActThreads, 0, stream>>>(xb, total, codes, scale);
+    else
+        tensor_quantize_small_kernel<false><<<1, kActThreads, 0, stream>>>(xb, total, codes, scale);
     return cudaGetLastError();
 }
 

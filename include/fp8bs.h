@@ -1,7 +1,8 @@
 /*
  * fp8bs.h -- C ABI of libfp8bs: block-scaled FP8 (E4M3), MXFP8 and per-row /
- * per-tensor FP8 weight quantization and the W8A16 GEMV / skinny GEMM /
- * prefill GEMM that consumes it, for NVIDIA GB300 (sm_103a).
+ * per-tensor FP8 weight quantization, the W8A16 GEMV / skinny GEMM /
+ * prefill GEMM that consumes it, and the W8A8 route (dynamic per-tensor
+ * activation quantization + e4m3 x e4m3 GEMM), for NVIDIA GB300 (sm_103a).
  *
  * Common conventions
  * ------------------
@@ -202,6 +203,50 @@ int fp8tensor_gemv(const void *x_bf16, int64_t m, const uint8_t *codes,
 int fp8tensor_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
                       const float *scale, int64_t n, int64_t k, void *y_bf16,
                       int path, void *stream);
+
+/*
+ * fp8act_quantize -- dynamic per-tensor activation quantization for the
+ * W8A8 route: the per-tensor rule applied to x [m, k] (amax over all m*k
+ * elements, s = amax / 448 in fp32, s = 1 if all zero, codes = e4m3(x / s)
+ * with an IEEE fp32 quotient).  Up to 65536 elements run as one single-CTA
+ * launch (amax and cast fused; the per-call cost dominates at decode sizes),
+ * larger tensors as the grid-wide fp8tensor_quantize, bit for bit the same.
+ *
+ * Defined by: FreeToken PR #389 (What this adds: a dynamic per-tensor
+ * activation scale, an amax pass then the cast; the follow-up commit: a
+ * block-parallel partial amax plus a reduce and cast for large inputs).
+ *
+ *   x_bf16     device, m*k bf16
+ *   codes_u8   device, m*k bytes, written
+ *   scale_f32  device, 1 float, written (used as the amax accumulator by
+ *              the grid-wide form, see fp8tensor_quantize)
+ */
+int fp8act_quantize(const void *x_bf16, int64_t m, int64_t k,
+                    uint8_t *codes_u8, float *scale_f32, void *stream);
+
+/*
+ * w8a8_gemm -- W8A8 linear:
+ *   y[i, j] = bf16_rn( sx * sw * sum_c dec(qx[i, c]) * dec(qw[j, c]) )
+ * with e4m3 x e4m3 products (exact) summed in fp32 on the tensor cores.
+ *
+ * Defined by: FreeToken PR #389 (What this adds / Why: the per-tensor W8A8
+ * GEMM of the projections, raw scaled-mm row of its decode table).
+ *
+ *   x_codes   device, m*k e4m3 (fp8act_quantize), 16-byte aligned for the
+ *             TMA paths
+ *   x_scale   device, 1 float
+ *   w_codes   device, n*k e4m3 (fp8tensor_quantize), w_scale device, 1 float
+ *   y_bf16    device, m*n bf16, written
+ * Paths: m <= 32 -> DECODE (mma.sync e4m3, m > 32 in chunks of 32 rows);
+ * larger m -> PREFILL (tcgen05 kind::f8f6f4); k % 16 != 0 or unaligned
+ * codes -> GENERIC.  Errors as fp8bs_gemv.
+ */
+int w8a8_gemm(const uint8_t *x_codes, int64_t m, const float *x_scale,
+              const uint8_t *w_codes, const float *w_scale, int64_t n,
+              int64_t k, void *y_bf16, void *stream);
+int w8a8_gemm_ex(const uint8_t *x_codes, int64_t m, const float *x_scale,
+                 const uint8_t *w_codes, const float *w_scale, int64_t n,
+                 int64_t k, void *y_bf16, int path, void *stream);
 
 /* Path FP8BS_PATH_AUTO would take for these shapes and pointers
  * (host-only, launches nothing).  `mx` selects the MXFP8 GEMV; the block,

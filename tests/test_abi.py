@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
-                 "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8bs_select_path", "fp8bs_strerror",
+                 "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
+                 "fp8bs_select_path", "fp8bs_strerror",
                  "fp8bs_check_device_error", "fp8bs_version"):
         assert want in names, names
 
@@ -49,7 +50,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strerror(L):
-    assert L.fp8bs_version() == 101
+    assert L.fp8bs_version() == 102
     import fp8_block_scaled_02_gb300 as pkg
     for st in range(-7, 1):
         assert pkg.strerror(st) and pkg.strerror(st) != "unknown status"
@@ -111,6 +112,21 @@ def test_rowwise_validation(L):
         assert gx(x, 1, c, s, 10, 10, y, 9, None) == -7
         assert gx(x, 1, c, s, 10, 10, y, 1, None) == -7   # decode needs k % 16 == 0
         assert gx(x, 40, c, s, 10, 24, y, 2, None) == -7  # prefill needs k % 16 == 0
+
+
+def test_w8a8_validation(L):
+    x, c, s, y, w, t = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000), P(0x60000)
+    assert L.fp8act_quantize(x, 0, 10, c, s, None) == -2
+    assert L.fp8act_quantize(None, 1, 10, c, s, None) == -1
+    assert L.fp8act_quantize(x, 1, 10, c, P(0x30001), None) == -4
+    assert L.w8a8_gemm(c, -1, s, w, t, 10, 10, y, None) == -2
+    assert L.w8a8_gemm(None, 0, None, None, None, 10, 10, None, None) == 0
+    assert L.w8a8_gemm(c, 1, None, w, t, 10, 10, y, None) == -1
+    assert L.w8a8_gemm(c, 1, s, w, None, 10, 10, y, None) == -1
+    assert L.w8a8_gemm(c, 1, P(0x30002), w, t, 10, 10, y, None) == -4
+    assert L.w8a8_gemm_ex(c, 1, s, w, t, 10, 10, y, 9, None) == -7
+    assert L.w8a8_gemm_ex(c, 1, s, w, t, 10, 24, y, 1, None) == -7    # decode needs k % 16 == 0
+    assert L.w8a8_gemm_ex(c, 40, s, P(0x50008), t, 10, 32, y, 2, None) == -7  # prefill needs aligned codes
 
 
 def test_select_path(L):
