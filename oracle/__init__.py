@@ -73,11 +73,12 @@ def _load():
         lib.oracle_tensor_quantize_rows.argtypes = [p, i64, i64, p, i64, p, p]
         lib.oracle_row_gemv.argtypes = [p, i64, p, p, i64, i64, i64, p, i64, p]
         lib.oracle_w8a8_gemv.argtypes = [p, i64, ctypes.c_float, p, ctypes.c_float, i64, i64, p, i64, p]
+        lib.oracle_moe_gemv.argtypes = [p, i64, p, i64, p, p, i64, i64, i64, p, i64, p]
         for f in ("oracle_block_quantize", "oracle_block_quantize_tile",
                   "oracle_mx_quantize", "oracle_mx_quantize_rows",
                   "oracle_block_gemv", "oracle_mx_gemv",
                   "oracle_row_quantize_rows", "oracle_tensor_quantize_rows",
-                  "oracle_row_gemv", "oracle_w8a8_gemv"):
+                  "oracle_row_gemv", "oracle_w8a8_gemv", "oracle_moe_gemv"):
             getattr(lib, f).restype = None
         _lib = lib
         return lib
@@ -283,6 +284,24 @@ def w8a8_gemv(xcodes: np.ndarray, sx, wcodes: np.ndarray, sw, rows=None) -> np.n
     _load().oracle_w8a8_gemv(_ptr(xcodes), m, float(np.float32(np.ravel(sx)[0])), _ptr(wcodes),
                              float(np.float32(np.ravel(sw)[0])), n, k,
                              None if rows is None else _ptr(rows), nrows, _ptr(y))
+    return y
+
+
+def moe_gemv(x, ids, codes: np.ndarray, scales: np.ndarray, rows=None) -> np.ndarray:
+    """fp64 y[M, topk, len(rows)]: (token t, slot j) = block GEMV of x[t] with
+    expert ids[t, j]; codes [E, N, K], scales [E, ceil(N/128), ceil(K/128)]."""
+    x = _bits16(x)
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    m, k = x.shape
+    e, n, k2 = codes.shape
+    assert k == k2 and ids.shape[0] == m and scales.shape == (e, cdiv(n, TILE), cdiv(k, TILE))
+    topk = ids.shape[1]
+    rows, nrows = _rows_arg(rows, n)
+    y = np.zeros((m, topk, nrows), dtype=np.float64)
+    _load().oracle_moe_gemv(_ptr(x), m, _ptr(ids), topk, _ptr(codes), _ptr(scales), e, n, k,
+                            None if rows is None else _ptr(rows), nrows, _ptr(y))
     return y
 
 

@@ -441,3 +441,32 @@ void oracle_w8a8_gemv(const uint8_t *xcodes, int64_t m, float sx,
             y64[mi * nrows + j] = sum * (double)sx * (double)sw;
         }
 }
+
+/* ---------------------------------------------------------------------
+ * Grouped MoE GEMV (Atlas quantize_fp8_bs.rs, module notes: block-scaled
+ * FP8 experts read by a grouped MoE GEMM with [N/128, K/128] fp32 scales).
+ * Each (token t, slot j) output is the block GEMV of x[t] with expert
+ * ids[t*topk + j]; an id outside [0, num_experts) leaves its row at 0.
+ * y64 layout [m, topk, nrows].
+ * ------------------------------------------------------------------- */
+void oracle_moe_gemv(const uint16_t *x, int64_t m, const int32_t *ids,
+                     int64_t topk, const uint8_t *codes, const float *scales,
+                     int64_t num_experts, int64_t n, int64_t k,
+                     const int64_t *rows, int64_t nrows, double *y64)
+{
+    int64_t nb = cdiv(n, TILE), kb = cdiv(k, TILE), t, j, r;
+    if (rows == NULL)
+        nrows = n;
+    for (t = 0; t < m; ++t)
+        for (j = 0; j < topk; ++j) {
+            int32_t e = ids[t * topk + j];
+            double *out = y64 + (t * topk + j) * nrows;
+            if (e < 0 || e >= num_experts) {
+                for (r = 0; r < nrows; ++r)
+                    out[r] = 0.0;
+                continue;
+            }
+            oracle_block_gemv(x + t * k, 1, codes + (int64_t)e * n * k,
+                              scales + (int64_t)e * nb * kb, n, k, rows, nrows, out);
+        }
+}

@@ -108,6 +108,14 @@ void oracle_w8a8_gemv(const uint8_t *xcodes, int64_t m, float sx,
                       const uint8_t *wcodes, float sw, int64_t n, int64_t k,
                       const int64_t *rows, int64_t nrows, double *y64);
 
+/* Grouped MoE: y64[t, j, r] = block GEMV of x[t] with expert ids[t*topk+j]
+ * (codes [E, n, k], scales [E, ceil(n/128), ceil(k/128)]); out-of-range
+ * ids give 0.  Layout [m, topk, nrows]. */
+void oracle_moe_gemv(const uint16_t *x, int64_t m, const int32_t *ids,
+                     int64_t topk, const uint8_t *codes, const float *scales,
+                     int64_t num_experts, int64_t n, int64_t k,
+                     const int64_t *rows, int64_t nrows, double *y64);
+
 #ifdef __cplusplus
 }
 #endif
