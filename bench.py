@@ -359,6 +359,34 @@ def w8a8_prefill_workload(torch, fp8bs, inputs, dev):
     return dict(calls=calls, cfg=cfg, dominant=("w8a8_prefill_kernel", [0, 1, 2]), flops=True, fp8=True)
 
 
+def moe_workload(torch, fp8bs, inputs, dev):
+    """Grouped MoE decode: 256 block-FP8 experts of [2048, 4096] (2.1 GB of
+    codes), top-12 routing per token, M = 1, 8, 16 tokens.  Bytes per call
+    count the experts the call's routing selects (each streamed once)."""
+    E, (n, k), topk = inputs.MOE_EXPERTS, inputs.MOE_SHAPE, inputs.MOE_TOPK
+    codes = torch.empty((E, n, k), dtype=torch.uint8, device=dev)
+    scales = torch.empty((E, n // 128, k // 128), dtype=torch.float32, device=dev)
+    for e in range(E):
+        c, s_ = fp8bs.quantize(inputs.moe_expert_weight(e, device=dev))
+        codes[e] = c
+        scales[e] = s_
+    ms = [1, 8, 16]
+    calls = []
+    for m in ms:
+        ids_cpu = inputs.moe_routing(m, topk, E, seed=m)
+        distinct = int(torch.unique(ids_cpu).numel())
+        ids = ids_cpu.to(dev)
+        x = inputs.activations(m, k, 800 + m, device=dev)
+        y = torch.empty((m, topk, n), dtype=torch.bfloat16, device=dev)
+        b = distinct * (n * k + 4 * (n // 128) * (k // 128)) + 2 * m * k + 4 * m * topk + 2 * m * topk * n
+        calls.append((f"M={m} ({distinct} experts)", m, b,
+                      (lambda x=x, ids=ids, y=y: fp8bs.moe_gemv(x, ids, codes, scales, y=y))))
+    cfg = {"workload": "grouped MoE decode: 256 block-FP8 experts [2048,4096], top-12 routing, M=1,8,16",
+           "experts": E, "n": n, "k": k, "topk": topk, "ms": ms,
+           "l2": "inputs larger than L2 (12-144 experts x 8.4 MB selected per call)"}
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,0,true,true>", [0, 1]))
+
+
 def quantize_workload(torch, fp8bs, inputs, dev):
     w = inputs.heavy_tail_weight(5, device=dev)
     n, k = w.shape
@@ -504,7 +532,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="lm_head",
                     choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill", "rowwise", "w8a8",
-                             "w8a8_prefill"])
+                             "w8a8_prefill", "moe"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -565,6 +593,8 @@ def main():
         wl = w8a8_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "w8a8_prefill":
         wl = w8a8_prefill_workload(torch, fp8bs, inputs, dev)
+    elif args.workload == "moe":
+        wl = moe_workload(torch, fp8bs, inputs, dev)
     else:
         wl = quantize_workload(torch, fp8bs, inputs, dev)
     torch.cuda.synchronize()

@@ -18,6 +18,8 @@ Functions (names follow the C entry points):
     act_quantize(x)        -> (x codes u8 [M,K], scale f32 [1])      (fp8act_quantize)
     w8a8_gemm(xq, sx, wq, sw) -> y bf16 [M,N]                        (w8a8_gemm)
     w8a8_linear(x, wq, sw) -> y bf16 [M,N]: act_quantize then w8a8_gemm
+    moe_gemv(x, ids, codes, scales) -> y bf16 [M, topk, N]            (fp8bs_moe_gemv)
+        codes [E,N,K], scales [E, ceil(N/128), ceil(K/128)], ids int32 [M, topk]
 """
 from __future__ import annotations
 
@@ -69,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.fp8tensor_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
         L.fp8tensor_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
         L.fp8act_quantize.argtypes = [p, i64, i64, p, p, p]
+        L.fp8bs_moe_gemv.argtypes = [p, i64, p, i64, p, p, i64, i64, i64, p, p]
         L.w8a8_gemm.argtypes = [p, i64, p, p, p, i64, i64, p, p]
         L.w8a8_gemm_ex.argtypes = [p, i64, p, p, p, i64, i64, p, i32, p]
         L.fp8bs_select_path.argtypes = [i64, i64, i64, p, p, i32]
@@ -79,6 +82,7 @@ def lib() -> ctypes.CDLL:
         for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                   "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
+                  "fp8bs_moe_gemv",
                   "fp8bs_select_path", "fp8bs_check_device_error",
                   "fp8bs_version"):
             getattr(L, f).restype = ctypes.c_int
@@ -221,6 +225,22 @@ def row_gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
     _check(fn(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
               _dev(scales, torch.float32, "scales"), n, k, _dev(y, torch.bfloat16, "y"), int(path),
               _stream(stream)), "fp8row_gemv" if per_row else "fp8tensor_gemv")
+    return y
+
+
+def moe_gemv(x, ids, codes, scales, y=None, stream=None):
+    """Grouped block-FP8 GEMV over routed experts: y[t, j] = x[t] . dequant(W[ids[t, j]])^T."""
+    import torch
+    m, k = x.shape
+    e, n, k2 = codes.shape
+    topk = ids.shape[1]
+    if k2 != k or ids.shape[0] != m:
+        raise ValueError("x, ids and codes disagree on M or K")
+    if y is None:
+        y = torch.empty((m, topk, n), dtype=torch.bfloat16, device=x.device)
+    _check(lib().fp8bs_moe_gemv(_dev(x, torch.bfloat16, "x"), m, _dev(ids, torch.int32, "ids"), topk,
+                                _dev(codes, torch.uint8, "codes"), _dev(scales, torch.float32, "scales"), e, n, k,
+                                _dev(y, torch.bfloat16, "y"), _stream(stream)), "fp8bs_moe_gemv")
     return y
 
 

@@ -85,7 +85,7 @@ int run_w8a8_decode_chunks(const W8A8Args &a, cudaStream_t st) {
 
 extern "C" {
 
-int fp8bs_version(void) { return 102; }
+int fp8bs_version(void) { return 103; }
 
 const char *fp8bs_strerror(int status) {
     switch (status) {
@@ -197,6 +197,27 @@ int fp8tensor_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const
 int fp8tensor_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scale, int64_t n, int64_t k,
                    void *y_bf16, void *stream) {
     return rowwise_gemv(x_bf16, m, codes, scale, n, k, y_bf16, 0, FP8BS_PATH_AUTO, stream);
+}
+
+int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids, int64_t topk, const uint8_t *codes,
+                   const float *scales, int64_t num_experts, int64_t n, int64_t k, void *y_bf16, void *stream) {
+    if (m < 0 || n <= 0 || k <= 0 || m >= kMaxDim || n >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (topk < 1 || num_experts < 1 || num_experts > 1024 || topk > num_experts) return FP8BS_ERR_SHAPE;
+    if (num_experts * n >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (m == 0) return FP8BS_OK;
+    if (!x_bf16 || !expert_ids || !codes || !scales || !y_bf16) return FP8BS_ERR_NULL;
+    if (!aligned(x_bf16, 2) || !aligned(y_bf16, 2) || !aligned(scales, 4) || !aligned(expert_ids, 4))
+        return FP8BS_ERR_ALIGN;
+    if (!tma_ok(k, x_bf16, codes)) return FP8BS_ERR_PATH;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int64_t m0 = 0; m0 < m; m0 += kDecodeMaxM) {
+        const int64_t mc = m - m0 < kDecodeMaxM ? m - m0 : kDecodeMaxM;
+        DecodeArgs a{static_cast<const char *>(x_bf16) + m0 * k * 2, codes, scales, nullptr,
+                     static_cast<char *>(y_bf16) + m0 * topk * n * 2, mc, n, k, kScaleBlock, 0};
+        const MoeArgs g{expert_ids + m0 * topk, topk, num_experts};
+        if (launch_moe_decode(a, g, st) != cudaSuccess) return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
 }
 
 int fp8act_quantize(const void *x_bf16, int64_t m, int64_t k, uint8_t *codes_u8, float *scale_f32, void *stream) {

@@ -17,6 +17,7 @@ enum : uint32_t {
     ERRBIT_EMPTY_WAIT = 1u << 1,  // producer gave up waiting for a free stage
     ERRBIT_MMA_WAIT = 1u << 2,    // tensor-core pipeline wait expired
     ERRBIT_TMEM = 1u << 3,        // TMEM allocation problem
+    ERRBIT_INDEX = 1u << 4,       // an index argument (e.g. an expert id) was out of range
 };
 
 // Every spin on an mbarrier gives up after this much wall time (globaltimer

@@ -33,6 +33,13 @@
 //    physical columns, applied identically to A and B, so every thread
 //    fetches 8 contiguous code bytes and 16 contiguous x bytes per K block
 //    with conflict-free shared-memory loads.
+//  * Grouped MoE (MOE = true): grid.z enumerates "expert slots"; each CTA
+//    reads the routing ids, takes the blockIdx.z-th smallest expert that any
+//    token selected (or leaves at once if there are fewer), streams that
+//    expert's weight rows, runs every token's x through them (the MMA cost
+//    of the extra rows is nothing next to the weight stream at m <= 32) and
+//    stores only the outputs of tokens routed to it.  Each selected expert's
+//    weight is read once per call, whatever the number of its tokens.
 //  * Programmatic dependent launch: a kernel may start (barrier init,
 //    tensor-map prefetch) while the previous kernel in the stream drains; it
 //    reads global memory only after griddepcontrol.wait.
@@ -52,6 +59,7 @@ constexpr int kConsumerWarps = 8;    // 4 column slices x 2 row halves
 constexpr int kWarpTma = kConsumerWarps;
 constexpr int kWarpConv0 = kConsumerWarps + 1;
 constexpr int kMaxSplit = 8;         // portable cluster size limit
+constexpr int kMoeMaxExperts = 1024; // experts a grouped call may address (bitmap of 32 words)
 
 // F16: operands are f16 (codes via cvt.rn.f16x2.e4m3x2, x rescaled to f16 by
 // a converter warp); otherwise bf16 (codes decoded with integer ops, x used
@@ -149,11 +157,14 @@ __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r,
 // previous tile.  With splits > 1 each CTA owns exactly one row tile and the
 // cluster reduces over K.
 // SC: how the weight is scaled (ScaleKind: 128x128 blocks, MX groups, rows)
-template <int MT, int SC, bool F16>
+// MOE: grouped expert GEMV (block scales); n is the rows of one expert, the
+// codes / scales hold num_experts such weights back to back, ids [m, topk].
+template <int MT, int SC, bool F16, bool MOE = false>
 __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
                   const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
-                  int m, int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec, int row_stride) {
+                  int m, int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec, int row_stride,
+                  const int32_t *__restrict__ ids, int topk, int num_experts) {
     constexpr bool MX = SC == kScaleMx;
     constexpr bool ROW = SC == kScaleRow;  // no per-K-block scale; scales[row * row_stride] at the end
     using C = Cfg<MT, MX, F16>;
@@ -183,6 +194,9 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
     const int total = my_tiles * nkb;
     const int mm = min(m, C::kXRows);
     __shared__ int s_fail;  // a warp gave up a wait: consumers stop after this tile
+    __shared__ uint32_t s_bits[kMoeMaxExperts / 32];  // MOE: experts any token selected
+    __shared__ int s_expert;                          // MOE: this CTA's expert
+    __shared__ signed char s_route[32];               // MOE: slot j of x row mi for it, -1 if none
 
     if (threadIdx.x == 0) {
         s_fail = 0;
@@ -199,6 +213,63 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
     }
     __syncthreads();
     pdl_wait();  // inputs may be produced by the previous kernel in the stream
+
+    int expert = 0;
+    if (MOE) {
+        for (int i = threadIdx.x; i < kMoeMaxExperts / 32; i += blockDim.x) s_bits[i] = 0;
+        __syncthreads();
+        for (int i = threadIdx.x; i < m * topk; i += blockDim.x) {
+            const int e = __ldg(ids + i);
+            if (e >= 0 && e < num_experts)
+                atomicOr(&s_bits[e >> 5], 1u << (e & 31));
+            else
+                atomicOr(&g_decode_err, ERRBIT_INDEX);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // slot blockIdx.z -> the blockIdx.z-th smallest selected expert
+            const uint32_t word = s_bits[lane];
+            const int cnt = __popc(word);
+            int pre = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, pre, o);
+                if (lane >= o) pre += v;
+            }
+            const int target = static_cast<int>(blockIdx.z);
+            int found = -1;
+            if (target >= pre - cnt && target < pre) {
+                uint32_t w = word;
+                for (int r = target - (pre - cnt); r > 0; --r) w &= w - 1;  // drop the r lowest set bits
+                found = lane * 32 + __ffs(static_cast<int>(w)) - 1;
+            }
+            const unsigned holder = __ballot_sync(0xffffffffu, found >= 0);
+            found = holder ? __shfl_sync(0xffffffffu, found, __ffs(static_cast<int>(holder)) - 1) : -1;
+            if (lane == 0) s_expert = found;
+        }
+        __syncthreads();
+        expert = s_expert;
+        // fewer selected experts than slots: nothing was issued yet, and every
+        // CTA of a cluster shares blockIdx.z, so the whole cluster leaves
+        if (expert < 0) return;
+        if (threadIdx.x < 32) {
+            int r = -1;
+            if (threadIdx.x < m)
+                for (int j = topk - 1; j >= 0; --j)
+                    if (__ldg(ids + threadIdx.x * topk + j) == expert) r = j;
+            s_route[threadIdx.x] = static_cast<signed char>(r);
+        }
+        __syncthreads();
+    }
+    // flat index into y of output (x row mi, weight row nn), or -1 if not stored
+    auto out_at = [&](int mi, int nn) -> int64_t {
+        if (!MOE) return static_cast<int64_t>(mi) * n + nn;
+        const int j = s_route[mi];
+        return j < 0 ? -1 : (static_cast<int64_t>(mi) * topk + j) * n + nn;
+    };
+    const int row_base = MOE ? expert * n : 0;  // expert's first row in the stacked codes
+    const float *scale_base =
+        MOE ? scales + static_cast<int64_t>(expert) * ((n + 127) >> 7) * kblocks : scales;
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------ TMA producer
@@ -220,7 +291,7 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                 const int kx = (kb0 + (it - ti * nkb)) * kKB;
                 uint8_t *st = smem + s * C::kStageBytes;
                 mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                tma_load_2d_hint(st, &tm_codes, &full[s], kx, n0, stream_policy);
+                tma_load_2d_hint(st, &tm_codes, &full[s], kx, row_base + n0, stream_policy);
                 tma_load_2d(st + C::kCodeBytes, &tm_x, &full[s], kx, 0);
                 tma_load_2d(st + C::kCodeBytes + C::kXPanelBytes, &tm_x, &full[s], kx + 64, 0);
             }
@@ -306,7 +377,7 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
         const int coff = (t & 1) * 8;
         for (int ti = 0; ti < my_tiles; ++ti) {
             const int n0 = (tile0 + ti * tstep) * kBN;
-            const float *srow = (MX || ROW) ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
+            const float *srow = (MX || ROW) ? nullptr : scale_base + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
             float acc[MT][4];
 #pragma unroll
             for (int j = 0; j < MT; ++j)
@@ -432,9 +503,8 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                     const int mi = 8 * j + t + 4 * (q & 1);
                     const int nl = ra + (q >> 1);
                     if (splits == 1) {
-                        if (mi < m && n0 + nl < n)
-                            y[static_cast<int64_t>(mi) * n + n0 + nl] =
-                                __float2bfloat16_rn(ROW ? acc[j][q] * out_scale(n0 + nl) : acc[j][q]);
+                        const int64_t o = (mi < m && n0 + nl < n) ? out_at(mi, n0 + nl) : -1;
+                        if (o >= 0) y[o] = __float2bfloat16_rn(ROW ? acc[j][q] * out_scale(n0 + nl) : acc[j][q]);
                     } else {
                         red[nl * C::kRedStride + mi] = acc[j][q];
                     }
@@ -456,7 +526,7 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
 
         for (int ti = 0; ti < my_tiles; ++ti) {
             const int n0 = (tile0 + ti * tstep) * kBN;
-            const float *srow = (MX || ROW) ? nullptr : scales + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
+            const float *srow = (MX || ROW) ? nullptr : scale_base + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
             float acc[kRT][MT][4];
 #pragma unroll
             for (int rt = 0; rt < kRT; ++rt)
@@ -593,9 +663,10 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                 for (int e = threadIdx.x; e < mm * kBN; e += kConsumerWarps * 32) {
                     const int mi = e / kBN;
                     const int nl = e - mi * kBN;
-                    if (n0 + nl < n) {
+                    const int64_t o = n0 + nl < n ? out_at(mi, n0 + nl) : -1;
+                    if (o >= 0) {
                         const float v = red[nl * C::kRedStride + mi];
-                        y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(ROW ? v * out_scale(n0 + nl) : v);
+                        y[o] = __float2bfloat16_rn(ROW ? v * out_scale(n0 + nl) : v);
                     }
                 }
                 consumer_bar();  // red is rewritten by the next tile
@@ -624,7 +695,8 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
         const int mi = e / my_rows;
         const int nl = r_begin + (e - mi * my_rows);
         const int nn = n0 + nl;
-        if (nn >= n) continue;
+        const int64_t o = nn < n ? out_at(mi, nn) : -1;
+        if (o < 0) continue;
         const uint32_t off = static_cast<uint32_t>((nl * C::kRedStride + mi) * 4);
         float part[kMaxSplit];
 #pragma unroll
@@ -633,7 +705,7 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
 #pragma unroll
         for (int q = 0; q < kMaxSplit; ++q)
             if (q < splits) sum += part[q];
-        y[static_cast<int64_t>(mi) * n + nn] = __float2bfloat16_rn(ROW ? sum * out_scale(nn) : sum);
+        y[o] = __float2bfloat16_rn(ROW ? sum * out_scale(nn) : sum);
     }
     cluster_sync_all();  // keep shared memory alive for peers
 }
@@ -716,7 +788,78 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, a.e8m0,
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m),
-                              static_cast<int>(a.n), kblocks, groups, splits, ntiles, e8m0_vec, a.row_stride);
+                              static_cast<int>(a.n), kblocks, groups, splits, ntiles, e8m0_vec, a.row_stride,
+                              static_cast<const int32_t *>(nullptr), 0, 0);
+}
+
+// Grouped MoE launch: grid (row tiles of one expert, K splits, expert slots).
+template <int MT, bool F16>
+cudaError_t launch_moe_t(const DecodeArgs &a, const MoeArgs &g, cudaStream_t stream) {
+    using C = Cfg<MT, false, F16>;
+    constexpr int kBN = C::kBN;
+    auto kern = decode_kernel<MT, kScaleBlock, F16, true>;
+    static Setup setup;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int resident = 1;
+    {
+        std::lock_guard<std::mutex> lock(setup.mu);
+        if (!setup.done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            int blocks = 0;
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, C::kThreads, C::kSmemBytes);
+            setup.err[dev] = e;
+            setup.resident[dev] = blocks > 0 ? blocks : 1;
+            setup.done[dev] = true;
+        }
+        if (setup.err[dev] != cudaSuccess) return setup.err[dev];
+        resident = setup.resident[dev];
+    }
+    CUtensorMap tm_codes, tm_x;
+    const uint64_t rows = static_cast<uint64_t>(g.num_experts) * static_cast<uint64_t>(a.n);
+    const uint64_t k = static_cast<uint64_t>(a.k), m = static_cast<uint64_t>(a.m);
+    if (!encode_tensor_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, k, rows, k, kKB, kBN,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64, C::kXRows,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
+    const int ntiles = static_cast<int>((a.n + kBN - 1) / kBN);
+    const int64_t slots64 = a.m * g.topk < g.num_experts ? a.m * g.topk : g.num_experts;
+    const int slots = static_cast<int>(slots64);
+    // size the K split for the most tiles the call can have (every slot used)
+    const int capacity = device_sm_count() * resident;
+    int splits = 1;
+    if (static_cast<int64_t>(ntiles) * slots < capacity) {
+        splits = capacity / (ntiles * slots);
+        if (splits > kMaxSplit) splits = kMaxSplit;
+        if (splits > kblocks) splits = kblocks;
+        if (splits < 1) splits = 1;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>(splits), static_cast<unsigned>(slots));
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (splits > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = static_cast<unsigned>(splits);
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, static_cast<const uint8_t *>(nullptr),
+                              static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m), static_cast<int>(a.n),
+                              kblocks, 0, splits, ntiles, 0, 0, g.ids, static_cast<int>(g.topk),
+                              static_cast<int>(g.num_experts));
 }
 
 template <int SC>
@@ -733,6 +876,16 @@ cudaError_t launch_sc(const DecodeArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_t stream) {
+    switch ((a.m + 7) / 8) {
+        case 1: return launch_moe_t<1, true>(a, g, stream);
+        case 2: return launch_moe_t<2, false>(a, g, stream);
+        case 3: return launch_moe_t<3, false>(a, g, stream);
+        case 4: return launch_moe_t<4, false>(a, g, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     switch (a.kind) {

@@ -44,6 +44,13 @@ struct DecodeArgs {
     int row_stride;          // kScaleRow: 1 per row, 0 per tensor
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+// Grouped MoE: a.codes / a.scales hold num_experts block-FP8 weights of
+// [a.n, a.k] back to back; ids [a.m, topk]; a.y is [a.m, topk, a.n].
+struct MoeArgs {
+    const int32_t *ids;
+    int64_t topk, num_experts;
+};
+cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_t stream);
 uint32_t take_decode_error();  // reads and clears the decode kernels' error word
 
 // generic.cu -- plain-load kernels for any shape / alignment.

@@ -31,6 +31,9 @@ ROTATION_SHAPES = ((8192, 2560), (2560, 3072), (6656, 2560), (2560, 3072))
 ROTATION_LAYERS = 48
 SWEEP_SHAPE = (12288, 4096)
 MX_SHAPE = (18432, 7168)
+MOE_EXPERTS = 256            # routed experts; top-12 of 256 per token (Atlas quantize_fp8_bs.rs notes)
+MOE_TOPK = 12
+MOE_SHAPE = (2048, 4096)     # [n, k] of one expert's projection
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -109,6 +112,18 @@ def heavy_tail_weight(seed: int = 5, device="cpu", shape=MX_SHAPE,
     t3 = z / torch.sqrt((c * c).sum(dim=1) / 3.0)
     t.view(-1)[pos] = WEIGHT_STD * t3
     return t.to(torch.bfloat16)
+
+
+def moe_expert_weight(e: int, device="cpu", shape=MOE_SHAPE) -> torch.Tensor:
+    """Expert e's bf16 [n, k] weight ~ N(0, 0.02^2), seed 6000 + e."""
+    return gaussian_bf16(shape, 0.02, 6000 + e, device)
+
+
+def moe_routing(m: int, topk: int = MOE_TOPK, experts: int = MOE_EXPERTS, seed: int = 0) -> torch.Tensor:
+    """int32 [m, topk] expert ids, distinct within each token (a top-k
+    selection), uniformly random with the given seed."""
+    g = _gen(7000 + seed, "cpu")
+    return torch.stack([torch.randperm(experts, generator=g)[:topk] for _ in range(m)]).to(torch.int32)
 
 
 def bf16_bits(t: torch.Tensor):

@@ -205,6 +205,35 @@ int fp8tensor_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
                       int path, void *stream);
 
 /*
+ * fp8bs_moe_gemv -- grouped block-FP8 W8A16 GEMV over routed experts:
+ *   y[t, j, :] = x[t, :] . dequant(W[e])^T  with e = expert_ids[t, j],
+ * each expert a block-FP8 weight [n, k] (fp8bs_quantize), the num_experts
+ * weights stored back to back: codes [num_experts, n, k], scales
+ * [num_experts, ceil(n/128), ceil(k/128)].  Every expert any token selected
+ * is streamed once per call (whatever the number of its tokens); experts no
+ * token selected are not read.  Same arithmetic and tolerance as fp8bs_gemv.
+ *
+ * Defined by: Atlas spark_model/weight_map/quantize_fp8_bs.rs (module
+ * notes: the block-scaled quantizer exists for routed MoE experts; the
+ * grouped MoE GEMM reads [N/128, K/128] fp32 block scales; decode reads the
+ * top-12 of 256 experts per token).
+ *
+ *   x_bf16       device, m*k bf16, 16-byte aligned, k % 16 == 0
+ *   expert_ids   device, m*topk int32; ids of one token must be distinct;
+ *                an id outside [0, num_experts) selects nothing and sets
+ *                the device error word (fp8bs_check_device_error)
+ *   topk         1..num_experts;  num_experts 1..1024, num_experts*n < 2^31
+ *   y_bf16       device, m*topk*n bf16, written for every valid id
+ * The ids are read on the device (no host synchronisation); m > 32 runs in
+ * chunks of 32 tokens.  FP8BS_ERR_PATH if k % 16 != 0 or x / codes are not
+ * 16-byte aligned.
+ */
+int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids,
+                   int64_t topk, const uint8_t *codes, const float *scales,
+                   int64_t num_experts, int64_t n, int64_t k, void *y_bf16,
+                   void *stream);
+
+/*
  * fp8act_quantize -- dynamic per-tensor activation quantization for the
  * W8A8 route: the per-tensor rule applied to x [m, k] (amax over all m*k
  * elements, s = amax / 448 in fp32, s = 1 if all zero, codes = e4m3(x / s)

@@ -35,7 +35,7 @@ def test_header_declares_the_entry_points():
     for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
-                 "fp8bs_select_path", "fp8bs_strerror",
+                 "fp8bs_moe_gemv", "fp8bs_select_path", "fp8bs_strerror",
                  "fp8bs_check_device_error", "fp8bs_version"):
         assert want in names, names
 
@@ -50,7 +50,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strerror(L):
-    assert L.fp8bs_version() == 102
+    assert L.fp8bs_version() == 103
     import fp8_block_scaled_02_gb300 as pkg
     for st in range(-7, 1):
         assert pkg.strerror(st) and pkg.strerror(st) != "unknown status"
@@ -127,6 +127,19 @@ def test_w8a8_validation(L):
     assert L.w8a8_gemm_ex(c, 1, s, w, t, 10, 10, y, 9, None) == -7
     assert L.w8a8_gemm_ex(c, 1, s, w, t, 10, 24, y, 1, None) == -7    # decode needs k % 16 == 0
     assert L.w8a8_gemm_ex(c, 40, s, P(0x50008), t, 10, 32, y, 2, None) == -7  # prefill needs aligned codes
+
+
+def test_moe_validation(L):
+    x, i, c, s, y = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000)
+    f = L.fp8bs_moe_gemv
+    assert f(x, 1, i, 0, c, s, 8, 128, 128, y, None) == -2          # topk < 1
+    assert f(x, 1, i, 9, c, s, 8, 128, 128, y, None) == -2          # topk > experts
+    assert f(x, 1, i, 2, c, s, 1025, 128, 128, y, None) == -2       # too many experts
+    assert f(x, 1, i, 2, c, s, 1024, 1 << 21, 128, y, None) == -2   # E * n >= 2^31
+    assert f(None, 0, None, 2, None, None, 8, 128, 128, None, None) == 0
+    assert f(x, 1, None, 2, c, s, 8, 128, 128, y, None) == -1
+    assert f(x, 1, P(0x20002), 2, c, s, 8, 128, 128, y, None) == -4
+    assert f(x, 1, i, 2, c, s, 8, 128, 120, y, None) == -7          # k % 16 != 0
 
 
 def test_select_path(L):

@@ -1,0 +1,169 @@
+"""GPU parity for the grouped MoE block-FP8 GEMV (Atlas quantize_fp8_bs.rs:
+routed experts as block-FP8 weights): every (token, slot) output within the
+tolerance of oracle/tolerance.py against the oracle's per-expert fp64 GEMV,
+one-hot columns exact, out-of-range ids reported and left unwritten, and
+only the selected experts' outputs depend on their weights.
+
+The experts' codes and scales come from the oracle's quantizer (small
+cases) or are installed from it for the sampled experts (full size).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_block_scaled_02_gb300 import inputs
+from oracle import tolerance
+
+from gpu_helpers import bits, guard_intact, guarded_empty, lib_or_skip, table
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    return lib_or_skip()
+
+
+def experts(e, n, k, seed):
+    codes, scales = [], []
+    for i in range(e):
+        c, s = oracle.block_quantize(bits(inputs.gaussian_bf16((n, k), 0.02, seed + i)))
+        codes.append(c)
+        scales.append(s)
+    return np.stack(codes), np.stack(scales)
+
+
+def route(m, topk, e, seed):
+    """Distinct experts per token (top-k routing), seeded."""
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.choice(e, size=topk, replace=False) for _ in range(m)]).astype(np.int32)
+
+
+def check(y_dev, x_bits, ids, codes, scales):
+    m, topk = ids.shape
+    y64 = oracle.moe_gemv(x_bits, ids, codes, scales)
+    yb = bits(y_dev.cpu())
+    for t in range(m):
+        for j in range(topk):
+            e = ids[t, j]
+            s = np.repeat(scales[e].astype(np.float64), 128, axis=0)[:codes.shape[1]]
+            wmax = np.abs(table()[codes[e]] * np.repeat(s, 128, axis=1)[:, :codes.shape[2]]).max(axis=1)
+            st = tolerance.gemv_errors(yb[t, j][None, :], y64[t, j][None, :], x_bits[t][None, :], wmax)
+            assert tolerance.gemv_ok(st), (t, j, st)
+
+
+@pytest.mark.parametrize("m", [1, 2, 5, 8, 9, 16, 17, 32, 33])
+@pytest.mark.parametrize("E,n,k,topk", [(8, 256, 512, 2), (16, 320, 704, 4), (6, 130, 256, 6), (32, 128, 128, 12)])
+def test_moe_small(pkg, m, E, n, k, topk):
+    codes, scales = experts(E, n, k, 100 + E + n)
+    ids = route(m, topk, E, m + E)
+    x = inputs.activations(m, k, 3 + m)
+    y, raw = guarded_empty((m, topk, n), torch.bfloat16, DEV)
+    pkg.moe_gemv(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                 torch.from_numpy(scales).to(DEV), y=y)
+    torch.cuda.synchronize()
+    assert guard_intact(raw, m * topk * n * 2)
+    check(y, bits(x), ids, codes, scales)
+    assert pkg.check_device_error() == 0
+
+
+def test_one_hot_exact(pkg):
+    """x = e_c: y[t, j, r] = bf16(fl32(dec(q_e[r, c]) * s_e[r/128, c/128]))."""
+    E, n, k = 4, 200, 256
+    codes, scales = experts(E, n, k, 7)
+    ids = np.array([[3, 1], [0, 2], [2, 3]], dtype=np.int32)
+    cols = [5, 130, 255]
+    x = np.zeros((3, k), dtype=np.uint16)
+    for t, c in enumerate(cols):
+        x[t, c] = 0x3F80
+    y = pkg.moe_gemv(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(DEV), torch.from_numpy(ids).to(DEV),
+                     torch.from_numpy(codes).to(DEV), torch.from_numpy(scales).to(DEV))
+    yb = bits(y.cpu())
+    for t, c in enumerate(cols):
+        for j in range(2):
+            e = ids[t, j]
+            prod = (table()[codes[e][:, c]].astype(np.float32) * scales[e][np.arange(n) // 128, c // 128]).astype(np.float32)
+            want = np.array([oracle.double_to_bf16(0.0 + float(v)) for v in prod], dtype=np.uint16)
+            assert np.array_equal(yb[t, j], want), (t, j)
+
+
+def test_out_of_range_id_sets_error_and_skips(pkg):
+    E, n, k = 4, 128, 128
+    codes, scales = experts(E, n, k, 9)
+    ids = np.array([[1, 9], [-3, 2]], dtype=np.int32)
+    x = inputs.activations(2, k, 4)
+    y = torch.full((2, 2, n), 7.0, dtype=torch.bfloat16, device=DEV)
+    pkg.moe_gemv(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                 torch.from_numpy(scales).to(DEV), y=y)
+    assert pkg.check_device_error() != 0
+    yc = y.cpu().float()
+    assert torch.all(yc[0, 1] == 7.0) and torch.all(yc[1, 0] == 7.0)
+    y64 = oracle.moe_gemv(bits(x), np.where((ids >= 0) & (ids < E), ids, 0).astype(np.int32), codes, scales)
+    for t, j in ((0, 0), (1, 1)):
+        st = tolerance.gemv_errors(bits(y[t, j][None, :].cpu()), y64[t, j][None, :], bits(x)[t][None, :],
+                                   np.full(n, np.abs(table()[codes]).max() * scales.max()))
+        assert tolerance.gemv_ok(st)
+
+
+def test_unselected_experts_are_not_read(pkg):
+    """Poisoning the weights of experts no token selected changes nothing."""
+    E, n, k = 8, 128, 256
+    codes, scales = experts(E, n, k, 11)
+    ids = np.array([[0, 5], [5, 2]], dtype=np.int32)
+    x = inputs.activations(2, k, 6).to(DEV)
+    c = torch.from_numpy(codes).to(DEV)
+    s = torch.from_numpy(scales).to(DEV)
+    i = torch.from_numpy(ids).to(DEV)
+    y1 = pkg.moe_gemv(x, i, c, s)
+    for e in (1, 3, 4, 6, 7):
+        c[e] = 0x7E
+        s[e] = 1e30
+    y2 = pkg.moe_gemv(x, i, c, s)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_full_size_sampled(pkg):
+    """256 experts of [2048, 4096] (2.1 GB of codes), top-12, M = 1, 8, 16:
+    the oracle checks the slots of a few sampled experts, whose codes and
+    scales are installed from the oracle's quantizer."""
+    E, n, k, topk = 256, 2048, 4096, 12
+    w_all = torch.empty((E, n, k), dtype=torch.uint8, device=DEV)
+    s_all = torch.empty((E, n // 128, k // 128), dtype=torch.float32, device=DEV)
+    for e in range(E):
+        c, s = pkg.quantize(inputs.moe_expert_weight(e, device=DEV))
+        w_all[e] = c
+        s_all[e] = s
+    sample = [0, 17, 255]
+    oc, os_ = experts_from(sample)
+    for i, e in enumerate(sample):
+        w_all[e] = torch.from_numpy(oc[i]).to(DEV)
+        s_all[e] = torch.from_numpy(os_[i]).to(DEV)
+    for m in (1, 8, 16):
+        ids = inputs.moe_routing(m, topk, E, seed=m).numpy()
+        for i, e in enumerate(sample):  # make sure every sampled expert is selected
+            t = i % m
+            if e not in ids[t]:
+                ids[t, i] = e
+        x = inputs.activations(m, k, 60 + m)
+        y = pkg.moe_gemv(x.to(DEV), torch.from_numpy(ids).to(DEV), w_all, s_all)
+        torch.cuda.synchronize()
+        yb = bits(y.cpu())
+        xb = bits(x)
+        for i, e in enumerate(sample):
+            for t, j in zip(*np.nonzero(ids == e)):
+                y64 = oracle.block_gemv(xb[t][None, :], oc[i], os_[i])
+                wmax = tolerance.block_wmax_rows(oc[i], os_[i], np.arange(n), table())
+                st = tolerance.gemv_errors(yb[t, j][None, :], y64, xb[t][None, :], wmax)
+                assert tolerance.gemv_ok(st), (m, e, t, j, st)
+    assert pkg.check_device_error() == 0
+
+
+def experts_from(sample):
+    codes, scales = [], []
+    for e in sample:
+        c, s = oracle.block_quantize(bits(inputs.moe_expert_weight(e)))
+        codes.append(c)
+        scales.append(s)
+    return codes, scales
