@@ -126,6 +126,40 @@ def moe_routing(m: int, topk: int = MOE_TOPK, experts: int = MOE_EXPERTS, seed: 
     return torch.stack([torch.randperm(experts, generator=g)[:topk] for _ in range(m)]).to(torch.int32)
 
 
+# FP8 KV cache decode attention (InfiniLM PR #586's paged FP8 KV cache on a
+# Qwen3-8B-shaped layer: 32 query heads, 8 KV heads, head_dim 128).
+KV_Q_HEADS = 32
+KV_HEADS = 8
+KV_HEAD_DIM = 128
+KV_PAGE = 16
+
+
+def kv_layer(batch: int, seq_lens, num_blocks: int, q_heads: int = KV_Q_HEADS, kv_heads: int = KV_HEADS,
+             head_dim: int = KV_HEAD_DIM, page_size: int = KV_PAGE, seed: int = 0, device="cpu"):
+    """Seeded inputs of one decode-attention call: q [B, Hq, D] ~ N(0, 1),
+    bf16 keys / values [num_blocks, page_size, Hkv, D] ~ N(0, 1), and a block
+    table [B, max_blocks] int32 that gives every sequence its own randomly
+    chosen, randomly ordered blocks (max_blocks = the longest sequence's
+    block count; unused entries 0)."""
+    lens = [int(v) for v in seq_lens]
+    need = [(n + page_size - 1) // page_size for n in lens]
+    max_blocks = max(1, max(need))
+    assert sum(need) <= num_blocks
+    g = _gen(9000 + seed, "cpu")
+    q = torch.randn((batch, q_heads, head_dim), generator=g).to(torch.bfloat16)
+    k = torch.randn((num_blocks, page_size, kv_heads, head_dim), generator=g).to(torch.bfloat16)
+    v = torch.randn((num_blocks, page_size, kv_heads, head_dim), generator=g).to(torch.bfloat16)
+    perm = torch.randperm(num_blocks, generator=g)
+    table = torch.zeros((batch, max_blocks), dtype=torch.int32)
+    off = 0
+    for b in range(batch):
+        table[b, :need[b]] = perm[off:off + need[b]].to(torch.int32)
+        off += need[b]
+    dev = torch.device(device)
+    return (q.to(dev), k.to(dev), v.to(dev), table.to(dev),
+            torch.tensor(lens, dtype=torch.int32).to(dev))
+
+
 def bf16_bits(t: torch.Tensor):
     """CPU numpy uint16 view of a bf16 tensor (copying from the device if needed)."""
     import numpy as np

@@ -74,11 +74,15 @@ def _load():
         lib.oracle_row_gemv.argtypes = [p, i64, p, p, i64, i64, i64, p, i64, p]
         lib.oracle_w8a8_gemv.argtypes = [p, i64, ctypes.c_float, p, ctypes.c_float, i64, i64, p, i64, p]
         lib.oracle_moe_gemv.argtypes = [p, i64, p, i64, p, p, i64, i64, i64, p, i64, p]
+        f32, f64 = ctypes.c_float, ctypes.c_double
+        lib.oracle_kv_append.argtypes = [p, i64, i64, i64, p, f32, p]
+        lib.oracle_kv_attention.argtypes = [p, i64, i64, i64, i64, p, p, f32, f32, p, i64, p, i64, f64, p]
         for f in ("oracle_block_quantize", "oracle_block_quantize_tile",
                   "oracle_mx_quantize", "oracle_mx_quantize_rows",
                   "oracle_block_gemv", "oracle_mx_gemv",
                   "oracle_row_quantize_rows", "oracle_tensor_quantize_rows",
-                  "oracle_row_gemv", "oracle_w8a8_gemv", "oracle_moe_gemv"):
+                  "oracle_row_gemv", "oracle_w8a8_gemv", "oracle_moe_gemv", "oracle_kv_append",
+                  "oracle_kv_attention"):
             getattr(lib, f).restype = None
         _lib = lib
         return lib
@@ -303,6 +307,39 @@ def moe_gemv(x, ids, codes: np.ndarray, scales: np.ndarray, rows=None) -> np.nda
     _load().oracle_moe_gemv(_ptr(x), m, _ptr(ids), topk, _ptr(codes), _ptr(scales), e, n, k,
                             None if rows is None else _ptr(rows), nrows, _ptr(y))
     return y
+
+
+def kv_append(x, slots, scale, cache: np.ndarray) -> np.ndarray:
+    """Quantize x [T, Hkv, D] (bf16 bits) into a copy of cache
+    [num_blocks, page_size, Hkv, D] at the flat token slots."""
+    x = _bits16(x)
+    t, hkv, d = x.shape
+    slots = np.ascontiguousarray(np.asarray(slots, dtype=np.int32))
+    out = np.ascontiguousarray(cache, dtype=np.uint8).copy()
+    assert out.shape[2:] == (hkv, d) and slots.shape == (t,)
+    assert t == 0 or (slots.min() >= 0 and slots.max() < out.shape[0] * out.shape[1])
+    _load().oracle_kv_append(_ptr(x), t, hkv, d, _ptr(slots), float(np.float32(np.ravel(scale)[0])), _ptr(out))
+    return out
+
+
+def kv_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, sm_scale) -> np.ndarray:
+    """fp64 decode attention: q [B, Hq, D] bf16 bits, caches [num_blocks,
+    page_size, Hkv, D] e4m3, block_table [B, max_blocks] int32, seq_lens [B]."""
+    q = _bits16(q)
+    b, hq, d = q.shape
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    nb, page, hkv, d2 = k_cache.shape
+    assert d2 == d and v_cache.shape == k_cache.shape and hq % hkv == 0
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    assert bt.shape[0] == b and sl.shape == (b,)
+    assert np.all(sl <= bt.shape[1] * page)
+    o = np.zeros((b, hq, d), dtype=np.float64)
+    _load().oracle_kv_attention(_ptr(q), b, hq, hkv, d, _ptr(k_cache), _ptr(v_cache),
+                                float(np.float32(np.ravel(k_scale)[0])), float(np.float32(np.ravel(v_scale)[0])),
+                                _ptr(bt), bt.shape[1], _ptr(sl), page, float(sm_scale), _ptr(o))
+    return o
 
 
 def to_bf16_bits(y64: np.ndarray) -> np.ndarray:

@@ -470,3 +470,75 @@ void oracle_moe_gemv(const uint16_t *x, int64_t m, const int32_t *ids,
                               scales + (int64_t)e * nb * kb, n, k, rows, nrows, out);
         }
 }
+
+/* ---------------------------------------------------------------------
+ * FP8 E4M3 KV cache (InfiniLM PR #586, Summary: an F8 cache with per-layer
+ * F32 k_scale / v_scale for paged attention; Benchmark: split-KV decode).
+ * Paged layout: cache [num_blocks, page_size, num_kv_heads, head_dim] e4m3;
+ * token i of sequence b lives in block block_table[b][i / page_size] at
+ * offset i % page_size.  Appending quantizes like the per-tensor rule with
+ * the given (static) scale: code = e4m3(x / scale), binary32 quotient.
+ * ------------------------------------------------------------------- */
+void oracle_kv_append(const uint16_t *x, int64_t num_tokens, int64_t kv_heads,
+                      int64_t head_dim, const int32_t *slots, float scale,
+                      uint8_t *cache)
+{
+    int64_t t, i, row = kv_heads * head_dim;
+    for (t = 0; t < num_tokens; ++t)
+        for (i = 0; i < row; ++i) {
+            float q = bf16_to_float(x[t * row + i]) / scale; /* binary32 quotient */
+            cache[(int64_t)slots[t] * row + i] = oracle_e4m3_encode((double)q);
+        }
+}
+
+/* Decode attention over the cache, in binary64:
+ *   s_l = sm_scale * sum_d q[b,h,d] * dec(K[l,g,d]) * k_scale   (g = h / (Hq/Hkv))
+ *   p_l = exp(s_l - max s) / sum exp(s - max s)
+ *   o[b,h,:] = sum_l p_l * dec(V[l,g,:]) * v_scale
+ * over the seq_lens[b] tokens of sequence b.  o64 [batch, q_heads, head_dim];
+ * an empty sequence gives zeros. */
+void oracle_kv_attention(const uint16_t *q, int64_t batch, int64_t q_heads,
+                         int64_t kv_heads, int64_t head_dim,
+                         const uint8_t *k_cache, const uint8_t *v_cache,
+                         float k_scale, float v_scale, const int32_t *block_table,
+                         int64_t max_blocks, const int32_t *seq_lens,
+                         int64_t page_size, double sm_scale, double *o64)
+{
+    double dec[256];
+    int64_t b, h, l, d, group = q_heads / kv_heads, row = kv_heads * head_dim;
+    int i;
+    for (i = 0; i < 256; ++i)
+        dec[i] = oracle_e4m3_decode((uint8_t)i);
+    for (b = 0; b < batch; ++b)
+        for (h = 0; h < q_heads; ++h) {
+            int64_t g = h / group, len = seq_lens[b];
+            const uint16_t *qv = q + (b * q_heads + h) * head_dim;
+            double *out = o64 + (b * q_heads + h) * head_dim;
+            double *s = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1));
+            double mx = -INFINITY, sum = 0.0;
+            for (d = 0; d < head_dim; ++d)
+                out[d] = 0.0;
+            for (l = 0; l < len; ++l) {
+                int64_t slot = (int64_t)block_table[b * max_blocks + l / page_size] * page_size + l % page_size;
+                const uint8_t *kr = k_cache + slot * row + g * head_dim;
+                double dot = 0.0;
+                for (d = 0; d < head_dim; ++d)
+                    dot += oracle_bf16_to_double(qv[d]) * (dec[kr[d]] * (double)k_scale);
+                s[l] = sm_scale * dot;
+                if (s[l] > mx)
+                    mx = s[l];
+            }
+            for (l = 0; l < len; ++l) {
+                int64_t slot = (int64_t)block_table[b * max_blocks + l / page_size] * page_size + l % page_size;
+                const uint8_t *vr = v_cache + slot * row + g * head_dim;
+                double p = exp(s[l] - mx);
+                sum += p;
+                for (d = 0; d < head_dim; ++d)
+                    out[d] += p * (dec[vr[d]] * (double)v_scale);
+            }
+            if (len > 0)
+                for (d = 0; d < head_dim; ++d)
+                    out[d] /= sum;
+            free(s);
+        }
+}

@@ -116,6 +116,20 @@ void oracle_moe_gemv(const uint16_t *x, int64_t m, const int32_t *ids,
                      int64_t num_experts, int64_t n, int64_t k,
                      const int64_t *rows, int64_t nrows, double *y64);
 
+/* FP8 KV cache, paged: cache [num_blocks, page_size, kv_heads, head_dim]
+ * e4m3.  Append: cache[slots[t]] = e4m3(x[t] / scale) (binary32 quotient). */
+void oracle_kv_append(const uint16_t *x, int64_t num_tokens, int64_t kv_heads,
+                      int64_t head_dim, const int32_t *slots, float scale,
+                      uint8_t *cache);
+/* Decode attention in fp64 (softmax over seq_lens[b] tokens, GQA group =
+ * q_heads / kv_heads); o64 [batch, q_heads, head_dim]. */
+void oracle_kv_attention(const uint16_t *q, int64_t batch, int64_t q_heads,
+                         int64_t kv_heads, int64_t head_dim,
+                         const uint8_t *k_cache, const uint8_t *v_cache,
+                         float k_scale, float v_scale, const int32_t *block_table,
+                         int64_t max_blocks, const int32_t *seq_lens,
+                         int64_t page_size, double sm_scale, double *o64);
+
 #ifdef __cplusplus
 }
 #endif
