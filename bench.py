@@ -387,6 +387,40 @@ def moe_workload(torch, fp8bs, inputs, dev):
     return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,0,true,true>", [0, 1]))
 
 
+def kv_workload(torch, fp8bs, inputs, dev):
+    """FP8 KV-cache split-KV decode attention on a Qwen3-8B-shaped layer (32 q
+    heads, 8 kv heads, head_dim 128, page 16) at InfiniLM PR #586's decode
+    shapes: batch 1 x 1k / 4k / 16k tokens and batch 8 x 1k / 4k.  Each call
+    reads its sequences' K and V pages from a 2 GB cache pool through its own
+    block table (8 rotations per shape, so nothing is L2-resident)."""
+    hq, hkv, d, page = inputs.KV_Q_HEADS, inputs.KV_HEADS, inputs.KV_HEAD_DIM, inputs.KV_PAGE
+    blocks = (1 << 30) // (page * hkv * d)         # 1 GB for K, 1 GB for V
+    g = torch.Generator(device="cpu").manual_seed(11)
+    k_cache = torch.randint(0, 0x7F, (blocks, page, hkv, d), dtype=torch.uint8, generator=g).to(dev)
+    v_cache = torch.randint(0, 0x7F, (blocks, page, hkv, d), dtype=torch.uint8, generator=g).to(dev)
+    ks = torch.tensor([0.01], device=dev)
+    vs = torch.tensor([0.01], device=dev)
+    shapes = [(1, 1024), (1, 4096), (1, 16384), (8, 1024), (8, 4096)]
+    calls = []
+    for bsz, length in shapes:
+        nblk = (length + page - 1) // page
+        perm = torch.randperm(blocks, generator=g)
+        tables = [perm[r * bsz * nblk:(r + 1) * bsz * nblk].view(bsz, nblk).to(torch.int32).to(dev) for r in range(8)]
+        lens = torch.full((bsz,), length, dtype=torch.int32, device=dev)
+        q = inputs.activations(bsz * hq, d, 900 + length, device=dev).view(bsz, hq, d)
+        out = torch.empty((bsz, hq, d), dtype=torch.bfloat16, device=dev)
+        b = 8 * (2 * bsz * length * hkv * d + 4 * bsz * nblk + 4 * bsz * hq * d)
+
+        def fn(tables=tables, lens=lens, q=q, out=out, length=length):
+            for tb in tables:
+                fp8bs.kv_decode_attention(q, k_cache, v_cache, ks, vs, tb, lens, length, d ** -0.5, out=out)
+        calls.append((f"B={bsz} L={length}", bsz, b, fn))
+    cfg = {"workload": "FP8 E4M3 paged KV cache decode attention (split-KV), 32 q / 8 kv heads, head_dim 128, "
+                       "page 16; batch x context 1x1k, 1x4k, 1x16k, 8x1k, 8x4k", "q_heads": hq, "kv_heads": hkv,
+           "head_dim": d, "page": page, "l2": "8 rotated block tables per shape over a 2 GB cache pool"}
+    return dict(calls=calls, cfg=cfg, dominant=("kv_attn_kernel", [2, 4]), launches_per_call=8)
+
+
 def quantize_workload(torch, fp8bs, inputs, dev):
     w = inputs.heavy_tail_weight(5, device=dev)
     n, k = w.shape
@@ -532,7 +566,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="lm_head",
                     choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill", "rowwise", "w8a8",
-                             "w8a8_prefill", "moe"])
+                             "w8a8_prefill", "moe", "kv"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -595,6 +629,8 @@ def main():
         wl = w8a8_prefill_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "moe":
         wl = moe_workload(torch, fp8bs, inputs, dev)
+    elif args.workload == "kv":
+        wl = kv_workload(torch, fp8bs, inputs, dev)
     else:
         wl = quantize_workload(torch, fp8bs, inputs, dev)
     torch.cuda.synchronize()

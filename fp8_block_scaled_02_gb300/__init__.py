@@ -20,6 +20,9 @@ Functions (names follow the C entry points):
     w8a8_linear(x, wq, sw) -> y bf16 [M,N]: act_quantize then w8a8_gemm
     moe_gemv(x, ids, codes, scales) -> y bf16 [M, topk, N]            (fp8bs_moe_gemv)
         codes [E,N,K], scales [E, ceil(N/128), ceil(K/128)], ids int32 [M, topk]
+    kv_append(x, slots, scale, cache)    FP8 KV cache append (fp8kv_append), in place
+    kv_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                        max_seq_len, sm_scale) -> o bf16 [B, Hq, 128]   (fp8kv_decode_attention)
 """
 from __future__ import annotations
 
@@ -72,6 +75,9 @@ def lib() -> ctypes.CDLL:
         L.fp8tensor_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
         L.fp8act_quantize.argtypes = [p, i64, i64, p, p, p]
         L.fp8bs_moe_gemv.argtypes = [p, i64, p, i64, p, p, i64, i64, i64, p, p]
+        L.fp8kv_append.argtypes = [p, i64, i64, i64, p, p, p, i64, p]
+        L.fp8kv_decode_attention.argtypes = [p, p, p, p, p, p, i64, p, i64, i64, i64, i64, i64, i64, i64,
+                                             ctypes.c_float, p, p]
         L.w8a8_gemm.argtypes = [p, i64, p, p, p, i64, i64, p, p]
         L.w8a8_gemm_ex.argtypes = [p, i64, p, p, p, i64, i64, p, i32, p]
         L.fp8bs_select_path.argtypes = [i64, i64, i64, p, p, i32]
@@ -82,7 +88,7 @@ def lib() -> ctypes.CDLL:
         for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                   "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
-                  "fp8bs_moe_gemv",
+                  "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention",
                   "fp8bs_select_path", "fp8bs_check_device_error",
                   "fp8bs_version"):
             getattr(L, f).restype = ctypes.c_int
@@ -242,6 +248,40 @@ def moe_gemv(x, ids, codes, scales, y=None, stream=None):
                                 _dev(codes, torch.uint8, "codes"), _dev(scales, torch.float32, "scales"), e, n, k,
                                 _dev(y, torch.bfloat16, "y"), _stream(stream)), "fp8bs_moe_gemv")
     return y
+
+
+def kv_append(x, slots, scale, cache, stream=None):
+    """Quantize new keys or values x [T, Hkv, 128] bf16 into the e4m3 cache
+    [num_blocks, page_size, Hkv, 128] at flat token slots (in place)."""
+    import torch
+    t, hkv, d = x.shape
+    nb, page, hkv2, d2 = cache.shape
+    if (hkv2, d2) != (hkv, d):
+        raise ValueError("x and cache disagree on kv heads or head_dim")
+    _check(lib().fp8kv_append(_dev(x, torch.bfloat16, "x"), t, hkv, d, _dev(slots, torch.int32, "slots"),
+                              _dev(scale, torch.float32, "scale"), _dev(cache, torch.uint8, "cache"), nb * page,
+                              _stream(stream)), "fp8kv_append")
+    return cache
+
+
+def kv_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, max_seq_len: int,
+                        sm_scale: float, out=None, stream=None):
+    """Paged decode attention over the FP8 KV cache: q [B, Hq, 128] bf16."""
+    import torch
+    b, hq, d = q.shape
+    nb, page, hkv, d2 = k_cache.shape
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or block_table.shape[0] != b:
+        raise ValueError("q, caches and block table disagree")
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=q.device)
+    _check(lib().fp8kv_decode_attention(_dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.uint8, "k_cache"),
+                                        _dev(v_cache, torch.uint8, "v_cache"), _dev(k_scale, torch.float32, "k_scale"),
+                                        _dev(v_scale, torch.float32, "v_scale"),
+                                        _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
+                                        _dev(seq_lens, torch.int32, "seq_lens"), b, hq, hkv, d, page, nb,
+                                        int(max_seq_len), float(sm_scale), _dev(out, torch.bfloat16, "out"),
+                                        _stream(stream)), "fp8kv_decode_attention")
+    return out
 
 
 def act_quantize(x, codes=None, scale=None, stream=None):

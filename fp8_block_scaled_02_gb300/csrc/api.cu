@@ -85,7 +85,7 @@ int run_w8a8_decode_chunks(const W8A8Args &a, cudaStream_t st) {
 
 extern "C" {
 
-int fp8bs_version(void) { return 103; }
+int fp8bs_version(void) { return 104; }
 
 const char *fp8bs_strerror(int status) {
     switch (status) {
@@ -220,6 +220,44 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids, int
     return FP8BS_OK;
 }
 
+int fp8kv_append(const void *x_bf16, int64_t num_tokens, int64_t num_kv_heads, int64_t head_dim,
+                 const int32_t *slot_mapping, const float *scale, uint8_t *cache, int64_t num_slots, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_slots <= 0 || num_tokens >= kMaxDim || num_kv_heads >= 4096)
+        return FP8BS_ERR_SHAPE;
+    if (head_dim != 128) return FP8BS_ERR_SHAPE;
+    if (num_slots * num_kv_heads * head_dim >= (int64_t{1} << 40)) return FP8BS_ERR_SHAPE;
+    if (num_tokens == 0) return FP8BS_OK;
+    if (!x_bf16 || !slot_mapping || !scale || !cache) return FP8BS_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(cache, 8) || !aligned(slot_mapping, 4) || !aligned(scale, 4))
+        return FP8BS_ERR_ALIGN;
+    return cuda_status(launch_kv_append(x_bf16, num_tokens, num_kv_heads, slot_mapping, scale, cache, num_slots,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int fp8kv_decode_attention(const void *q_bf16, const uint8_t *k_cache, const uint8_t *v_cache, const float *k_scale,
+                           const float *v_scale, const int32_t *block_table, int64_t max_blocks_per_seq,
+                           const int32_t *seq_lens, int64_t batch, int64_t num_q_heads, int64_t num_kv_heads,
+                           int64_t head_dim, int64_t page_size, int64_t num_blocks, int64_t max_seq_len, float sm_scale,
+                           void *out_bf16, void *stream) {
+    if (batch < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0)
+        return FP8BS_ERR_SHAPE;
+    if (head_dim != 128 || num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > 8) return FP8BS_ERR_SHAPE;
+    if (page_size < 16 || page_size % 16 != 0 || page_size > 4096) return FP8BS_ERR_SHAPE;
+    if (num_blocks * page_size >= kMaxDim || batch * num_kv_heads >= kMaxDim || max_blocks_per_seq >= kMaxDim)
+        return FP8BS_ERR_SHAPE;
+    if (max_seq_len < 0 || max_seq_len > max_blocks_per_seq * page_size) return FP8BS_ERR_SHAPE;
+    if (!(sm_scale == sm_scale) || sm_scale > 3.0e38f || sm_scale < -3.0e38f) return FP8BS_ERR_SHAPE;
+    if (batch == 0) return FP8BS_OK;
+    if (!q_bf16 || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out_bf16)
+        return FP8BS_ERR_NULL;
+    if (!aligned(q_bf16, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out_bf16, 2) ||
+        !aligned(k_scale, 4) || !aligned(v_scale, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
+        return FP8BS_ERR_ALIGN;
+    KvAttnArgs a{q_bf16, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out_bf16,
+                 batch, num_q_heads, num_kv_heads, page_size, num_blocks, max_blocks_per_seq, max_seq_len, sm_scale};
+    return cuda_status(launch_kv_attention(a, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8act_quantize(const void *x_bf16, int64_t m, int64_t k, uint8_t *codes_u8, float *scale_f32, void *stream) {
     if (m <= 0 || k <= 0 || m >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
     if (!x_bf16 || !codes_u8 || !scale_f32) return FP8BS_ERR_NULL;
@@ -260,7 +298,7 @@ int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16, const
 
 int fp8bs_check_device_error(void *stream, uint32_t *word_out) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
-    const uint32_t w = take_decode_error() | take_prefill_error() | take_w8a8_error();
+    const uint32_t w = take_decode_error() | take_prefill_error() | take_w8a8_error() | take_kv_error();
     if (word_out) *word_out = w;
     return w ? FP8BS_ERR_DEVICE : FP8BS_OK;
 }

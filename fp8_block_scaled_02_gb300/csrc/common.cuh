@@ -98,6 +98,16 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 3-D tiled TMA load at element coordinates (x innermost, y, z).
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int32_t x,
+                                            int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // Same, with an L2 cache-policy hint (e.g. evict-first for streamed weights).
 __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorMap *map,
                                                  uint64_t *bar, int32_t x, int32_t y,
@@ -212,6 +222,21 @@ __device__ __forceinline__ float bf16lo_to_f32(uint32_t packed) { return __uint_
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) {
     return __uint_as_float(packed & 0xFFFF0000u);
 }
+
+// Encode 8 bf16 values (one uint4) divided by s into 8 e4m3 bytes (uint2).
+__device__ __forceinline__ uint2 encode8_div(const uint4 v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint16_t c0 = f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h]) / s, bf16hi_to_f32(w[2 * h]) / s);
+        const uint16_t c1 =
+            f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h + 1]) / s, bf16hi_to_f32(w[2 * h + 1]) / s);
+        out[h] = static_cast<uint32_t>(c0) | (static_cast<uint32_t>(c1) << 16);
+    }
+    return make_uint2(out[0], out[1]);
+}
+
 
 // ------------------------------------------------------------- mma.sync
 // D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col).

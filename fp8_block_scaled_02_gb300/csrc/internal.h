@@ -80,6 +80,28 @@ bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
                           uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
                           uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// 3-D variant: dims innermost first, strides of dims 1 and 2 in bytes.
+bool encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, const uint64_t (&dims)[3],
+                          const uint64_t (&strides_bytes)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle);
+
+// kvattn.cu -- FP8 E4M3 paged KV cache: append and split-KV decode attention.
+struct KvAttnArgs {
+    const void *q;               // bf16 [batch, q_heads, 128]
+    const uint8_t *k_cache;      // e4m3 [num_blocks, page_size, kv_heads, 128]
+    const uint8_t *v_cache;
+    const float *k_scale;        // [1]
+    const float *v_scale;        // [1]
+    const int32_t *block_table;  // [batch, max_blocks]
+    const int32_t *seq_lens;     // [batch]
+    void *out;                   // bf16 [batch, q_heads, 128]
+    int64_t batch, q_heads, kv_heads, page_size, num_blocks, max_blocks, max_seq_len;
+    float sm_scale;
+};
+cudaError_t launch_kv_attention(const KvAttnArgs &a, cudaStream_t stream);
+cudaError_t launch_kv_append(const void *x, int64_t num_tokens, int64_t kv_heads, const int32_t *slots,
+                             const float *scale, uint8_t *cache, int64_t num_slots, cudaStream_t stream);
+uint32_t take_kv_error();
+
 // Multiprocessor count of the current device (cached per device).
 int device_sm_count();
 

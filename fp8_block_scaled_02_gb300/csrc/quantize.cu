@@ -40,20 +40,6 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Encode 8 bf16 values (one uint4) divided by s into 8 e4m3 bytes (uint2).
-__device__ __forceinline__ uint2 encode8_div(const uint4 v, float s) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint16_t c0 = f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h]) / s, bf16hi_to_f32(w[2 * h]) / s);
-        const uint16_t c1 =
-            f32x2_to_e4m3x2(bf16lo_to_f32(w[2 * h + 1]) / s, bf16hi_to_f32(w[2 * h + 1]) / s);
-        out[h] = static_cast<uint32_t>(c0) | (static_cast<uint32_t>(c1) << 16);
-    }
-    return make_uint2(out[0], out[1]);
-}
-
 __device__ __forceinline__ uint2 encode8_mul(const uint4 v, float f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t out[2];

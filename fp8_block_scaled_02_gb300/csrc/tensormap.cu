@@ -47,6 +47,20 @@ bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, const uint64_t (&dims)[3],
+                          const uint64_t (&strides_bytes)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, resolve_encode);
+    if (!g_encode) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, dtype, 3, const_cast<void *>(base), d, st, bx, elem_strides,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;

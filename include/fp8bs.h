@@ -1,8 +1,10 @@
 /*
  * fp8bs.h -- C ABI of libfp8bs: block-scaled FP8 (E4M3), MXFP8 and per-row /
  * per-tensor FP8 weight quantization, the W8A16 GEMV / skinny GEMM /
- * prefill GEMM that consumes it, and the W8A8 route (dynamic per-tensor
- * activation quantization + e4m3 x e4m3 GEMM), for NVIDIA GB300 (sm_103a).
+ * prefill GEMM that consumes it, the W8A8 route (dynamic per-tensor
+ * activation quantization + e4m3 x e4m3 GEMM), the grouped MoE GEMV and an
+ * FP8 E4M3 paged KV cache with split-KV decode attention, for NVIDIA GB300
+ * (sm_103a).
  *
  * Common conventions
  * ------------------
@@ -232,6 +234,62 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids,
                    int64_t topk, const uint8_t *codes, const float *scales,
                    int64_t num_experts, int64_t n, int64_t k, void *y_bf16,
                    void *stream);
+
+/*
+ * FP8 E4M3 KV cache for paged decode attention.
+ *
+ * Defined by: InfiniLM PR #586 (Summary: an F8 cache with per-layer fp32
+ * k_scale / v_scale for paged attention; Benchmark: split-KV decode
+ * attention over the FP8 cache, "halves cache capacity and decode attention
+ * read bandwidth").
+ *
+ * Cache layout: [num_blocks, page_size, num_kv_heads, head_dim] e4m3, token
+ * i of sequence b in block block_table[b * max_blocks_per_seq +
+ * i / page_size] at offset i % page_size.  head_dim must be 128, page_size a
+ * multiple of 16, num_q_heads a multiple of num_kv_heads with at most 8
+ * query heads per kv head.
+ *
+ * fp8kv_append: cache[slot_mapping[t]] = e4m3(x[t] / scale) for the new
+ * tokens x [num_tokens, num_kv_heads, head_dim] bf16 (IEEE fp32 quotient,
+ * nearest-even, saturating); slot = block * page_size + offset;
+ * num_slots = num_blocks * page_size.  A slot outside [0, num_slots) is
+ * skipped and sets the device error word.  x 16-byte aligned.
+ */
+int fp8kv_append(const void *x_bf16, int64_t num_tokens, int64_t num_kv_heads,
+                 int64_t head_dim, const int32_t *slot_mapping,
+                 const float *scale, uint8_t *cache, int64_t num_slots,
+                 void *stream);
+
+/*
+ * fp8kv_decode_attention: one query token per sequence,
+ *   o[b, h, :] = sum_l p_l * dec(V[l, g]) * v_scale,
+ *   p = softmax_l( sm_scale * q[b, h, :] . dec(K[l, g]) * k_scale ),
+ * g = h / (num_q_heads / num_kv_heads), over the seq_lens[b] tokens of
+ * sequence b (0 tokens: o = 0).  K and V decode exactly; scores, the
+ * softmax and the sums are fp32 (the weights enter the V sum as f16); one
+ * bf16 rounding at the end.  The KV range of a sequence is split over a
+ * thread-block cluster and merged on chip (no workspace).
+ *
+ *   q_bf16       device, [batch, num_q_heads, 128] bf16, 16-byte aligned
+ *   k_cache, v_cache   device, e4m3 caches as above, 16-byte aligned
+ *   k_scale, v_scale   device, 1 float each
+ *   block_table  device, [batch, max_blocks_per_seq] int32
+ *   seq_lens     device, [batch] int32, each <= max_blocks_per_seq * page_size
+ *                (a larger or negative length is clamped and sets the device
+ *                error word, as does a block id outside [0, num_blocks))
+ *   max_seq_len  host upper bound of seq_lens (sizes the split), <=
+ *                max_blocks_per_seq * page_size
+ *   out_bf16     device, [batch, num_q_heads, 128] bf16, written
+ */
+int fp8kv_decode_attention(const void *q_bf16, const uint8_t *k_cache,
+                           const uint8_t *v_cache, const float *k_scale,
+                           const float *v_scale, const int32_t *block_table,
+                           int64_t max_blocks_per_seq, const int32_t *seq_lens,
+                           int64_t batch, int64_t num_q_heads,
+                           int64_t num_kv_heads, int64_t head_dim,
+                           int64_t page_size, int64_t num_blocks,
+                           int64_t max_seq_len, float sm_scale, void *out_bf16,
+                           void *stream);
 
 /*
  * fp8act_quantize -- dynamic per-tensor activation quantization for the

@@ -35,7 +35,7 @@ def test_header_declares_the_entry_points():
     for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
-                 "fp8bs_moe_gemv", "fp8bs_select_path", "fp8bs_strerror",
+                 "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention", "fp8bs_select_path", "fp8bs_strerror",
                  "fp8bs_check_device_error", "fp8bs_version"):
         assert want in names, names
 
@@ -50,7 +50,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strerror(L):
-    assert L.fp8bs_version() == 103
+    assert L.fp8bs_version() == 104
     import fp8_block_scaled_02_gb300 as pkg
     for st in range(-7, 1):
         assert pkg.strerror(st) and pkg.strerror(st) != "unknown status"
@@ -140,6 +140,33 @@ def test_moe_validation(L):
     assert f(x, 1, None, 2, c, s, 8, 128, 128, y, None) == -1
     assert f(x, 1, P(0x20002), 2, c, s, 8, 128, 128, y, None) == -4
     assert f(x, 1, i, 2, c, s, 8, 128, 120, y, None) == -7          # k % 16 != 0
+
+
+def test_kv_validation(L):
+    x, sl, s, c = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
+    a = L.fp8kv_append
+    assert a(x, 4, 8, 64, sl, s, c, 1024, None) == -2            # head_dim must be 128
+    assert a(x, 0, 8, 128, None, None, None, 1024, None) == 0
+    assert a(None, 4, 8, 128, sl, s, c, 1024, None) == -1
+    assert a(P(0x10008), 4, 8, 128, sl, s, c, 1024, None) == -4  # x 16-byte aligned
+    q, k, v, ks, vs, bt, lens, o = (P(0x10000 * i) for i in range(1, 9))
+    f = L.fp8kv_decode_attention
+    ok = dict(q=q, k=k, v=v, ks=ks, vs=vs, bt=bt, mb=4, lens=lens, b=2, hq=32, hkv=8, d=128, page=16, nb=64,
+              ml=64, sm=0.088, o=o)
+
+    def call(**kw):
+        a_ = dict(ok, **kw)
+        return f(a_["q"], a_["k"], a_["v"], a_["ks"], a_["vs"], a_["bt"], a_["mb"], a_["lens"], a_["b"], a_["hq"],
+                 a_["hkv"], a_["d"], a_["page"], a_["nb"], a_["ml"], ctypes.c_float(a_["sm"]), a_["o"], None)
+    assert call(d=64) == -2
+    assert call(hq=30) == -2                 # not a multiple of the kv heads
+    assert call(hq=80) == -2                 # more than 8 query heads per kv head
+    assert call(page=24) == -2
+    assert call(ml=65) == -2                 # beyond the block table
+    assert call(sm=float("nan")) == -2
+    assert call(b=0, q=None) == 0
+    assert call(q=None) == -1
+    assert call(q=P(0x10008)) == -4
 
 
 def test_select_path(L):
