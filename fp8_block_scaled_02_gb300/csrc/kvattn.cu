@@ -35,8 +35,6 @@ __device__ uint32_t g_kv_err;
 
 constexpr int kD = 128;                      // head_dim
 constexpr int kChunk = 16;                   // tokens per MMA tile / TMA box
-constexpr int kWarps = 4;                    // consumer warps per CTA
-constexpr int kStages = 5;                   // chunks in flight per warp
 constexpr int kGroup = 8;                    // query heads per kv head (MMA n)
 constexpr int kMaxSplit = 16;                // cluster size (non-portable above 8)
 constexpr int kTileBytes = kChunk * kD;      // 2 KB: one chunk of K or V
@@ -44,12 +42,17 @@ constexpr int kStageBytes = 2 * kTileBytes;  // K + V
 constexpr int kVStride = kD * 2 + 16;        // f16 V row in the transpose buffer, padded
 constexpr int kVScratch = kChunk * kVStride;
 constexpr int kMergeFloats = 2 * kGroup + kD * kGroup;  // m[8], l[8], O[128][8]
-// a warp's merge record (after its loop) reuses its own, then idle, stages
-static_assert(kMergeFloats * 4 <= kStages * kStageBytes, "merge record fits a warp's stages");
-constexpr int kSmemBytes =
-    1024 + kWarps * kStages * kStageBytes + kWarps * kVScratch + kMergeFloats * 4 + kWarps * kStages * 8;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-constexpr int kResident = kSmemBytes <= 113 * 1024 ? 2 : 1;  // CTAs per SM
+// W consumer warps per CTA, S chunks in flight per warp.  4 x 5 (two CTAs
+// per SM) measured fastest on every decode shape; 8 x 5, 8 x 3, 4 x 8, 4 x 10
+// (one CTA per SM) and 2 x 5 were all slower.
+template <int W, int S>
+struct KvCfg {
+    static constexpr int kSmemBytes = 1024 + W * S * kStageBytes + W * kVScratch + kMergeFloats * 4 + W * S * 8;
+    static constexpr int kResident = kSmemBytes <= 113 * 1024 ? 2 : 1;  // CTAs per SM
+    // a warp's merge record (after its loop) reuses its own, then idle, stages
+    static_assert(kMergeFloats * 4 <= S * kStageBytes, "merge record fits a warp's stages");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
@@ -60,12 +63,14 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
 
 __device__ __forceinline__ float dsmem_ld(uint32_t base, int idx) { return dsmem_ld_f32(base + 4u * idx); }
 
-__global__ void __launch_bounds__(kWarps * 32, kResident) kv_attn_kernel(
+template <int W, int S>
+__global__ void __launch_bounds__(W * 32, KvCfg<W, S>::kResident) kv_attn_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __nv_bfloat16 *__restrict__ q, const float *__restrict__ k_scale_p, const float *__restrict__ v_scale_p,
     const int32_t *__restrict__ table, const int32_t *__restrict__ seq_lens, __nv_bfloat16 *__restrict__ out,
     int kv_heads, int group, int page_size, int num_blocks, int max_blocks, int max_len, int splits,
     float sm_scale) {
+    constexpr int kWarps = W, kStages = S;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -430,59 +435,50 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const __nv_bf
     }
 }
 
-std::mutex g_setup_mu;
-bool g_setup_done[64] = {};
-cudaError_t g_setup_err[64] = {};
-int g_max_split[64] = {};
+struct KvSetup {
+    std::mutex mu;
+    bool done[64] = {};
+    cudaError_t err[64] = {};
+    int max_split[64] = {};
+};
 
-}  // namespace
-
-cudaError_t launch_kv_attention(const KvAttnArgs &a, cudaStream_t stream) {
+template <int W, int S>
+cudaError_t launch_kv_t(const KvAttnArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v, cudaStream_t stream) {
+    using C = KvCfg<W, S>;
+    auto kern = kv_attn_kernel<W, S>;
+    static KvSetup setup;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int max_split = 8;
     {
-        std::lock_guard<std::mutex> lock(g_setup_mu);
-        if (!g_setup_done[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(kv_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        std::lock_guard<std::mutex> lock(setup.mu);
+        if (!setup.done[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
             // clusters of up to 16 CTAs where the device allows them
-            g_max_split[dev] =
-                cudaFuncSetAttribute(kv_attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess
-                    ? kMaxSplit
-                    : 8;
+            setup.max_split[dev] =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess ? kMaxSplit
+                                                                                                             : 8;
             (void)cudaGetLastError();
-            g_setup_err[dev] = e;
-            g_setup_done[dev] = true;
+            setup.err[dev] = e;
+            setup.done[dev] = true;
         }
-        if (g_setup_err[dev] != cudaSuccess) return g_setup_err[dev];
-        max_split = g_max_split[dev];
+        if (setup.err[dev] != cudaSuccess) return setup.err[dev];
+        max_split = setup.max_split[dev];
     }
-    CUtensorMap tm_k, tm_v;
-    const uint64_t hkv = static_cast<uint64_t>(a.kv_heads);
-    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * static_cast<uint64_t>(a.page_size);
-    const uint64_t dims[3] = {static_cast<uint64_t>(kD), hkv, rows};
-    const uint64_t strides[2] = {static_cast<uint64_t>(kD), hkv * kD};
-    const uint32_t box[3] = {static_cast<uint32_t>(kD), 1u, static_cast<uint32_t>(kChunk)};
-    if (!encode_tensor_map_3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
     const int group = static_cast<int>(a.q_heads / a.kv_heads);
     const int64_t pairs = a.batch * a.kv_heads;
-    // enough CTAs to fill the SMs once, each warp with at least two chunks
+    // one wave of CTAs, each warp with at least two chunks
     const int64_t chunks = (a.max_seq_len + kChunk - 1) / kChunk;
-    // one wave
-    int64_t splits = (kResident * static_cast<int64_t>(device_sm_count())) / pairs;
-    const int64_t by_len = chunks / (2 * kWarps);
+    int64_t splits = (C::kResident * static_cast<int64_t>(device_sm_count())) / pairs;
+    const int64_t by_len = chunks / (2 * W);
     if (splits > by_len) splits = by_len;
     if (splits > max_split) splits = max_split;
     if (splits < 1) splits = 1;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pairs), static_cast<unsigned>(splits), 1);
-    cfg.blockDim = dim3(kWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.blockDim = dim3(W * 32, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -499,12 +495,11 @@ cudaError_t launch_kv_attention(const KvAttnArgs &a, cudaStream_t stream) {
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     auto launch = [&]() {
-        return cudaLaunchKernelEx(&cfg, kv_attn_kernel, tm_k, tm_v, static_cast<const __nv_bfloat16 *>(a.q),
-                                  a.k_scale, a.v_scale, a.block_table, a.seq_lens,
-                                  static_cast<__nv_bfloat16 *>(a.out), static_cast<int>(a.kv_heads), group,
-                                  static_cast<int>(a.page_size), static_cast<int>(a.num_blocks),
-                                  static_cast<int>(a.max_blocks), static_cast<int>(a.max_seq_len),
-                                  static_cast<int>(splits), a.sm_scale);
+        return cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, static_cast<const __nv_bfloat16 *>(a.q), a.k_scale,
+                                  a.v_scale, a.block_table, a.seq_lens, static_cast<__nv_bfloat16 *>(a.out),
+                                  static_cast<int>(a.kv_heads), group, static_cast<int>(a.page_size),
+                                  static_cast<int>(a.num_blocks), static_cast<int>(a.max_blocks),
+                                  static_cast<int>(a.max_seq_len), static_cast<int>(splits), a.sm_scale);
     };
     cudaError_t e = launch();
     if (e != cudaSuccess && splits > 8) {
@@ -513,11 +508,30 @@ cudaError_t launch_kv_attention(const KvAttnArgs &a, cudaStream_t stream) {
         splits = 8;
         cfg.gridDim.y = 8;
         attrs[1].val.clusterDim.y = 8;
-        std::lock_guard<std::mutex> lock(g_setup_mu);
-        g_max_split[dev] = 8;
+        {
+            std::lock_guard<std::mutex> lock(setup.mu);
+            setup.max_split[dev] = 8;
+        }
         e = launch();
     }
     return e;
+}
+
+}  // namespace
+
+cudaError_t launch_kv_attention(const KvAttnArgs &a, cudaStream_t stream) {
+    CUtensorMap tm_k, tm_v;
+    const uint64_t hkv = static_cast<uint64_t>(a.kv_heads);
+    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * static_cast<uint64_t>(a.page_size);
+    const uint64_t dims[3] = {static_cast<uint64_t>(kD), hkv, rows};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kD), hkv * kD};
+    const uint32_t box[3] = {static_cast<uint32_t>(kD), 1u, static_cast<uint32_t>(kChunk)};
+    if (!encode_tensor_map_3d(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_3d(&tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    return launch_kv_t<4, 5>(a, tm_k, tm_v, stream);
 }
 
 cudaError_t launch_kv_append(const void *x, int64_t num_tokens, int64_t kv_heads, const int32_t *slots,

@@ -164,3 +164,14 @@ def test_repeat_is_deterministic(pkg):
     o1 = run(pkg, q, kc, vc, ks, vs, tbl, sl, 0.09)
     o2 = run(pkg, q, kc, vc, ks, vs, tbl, sl, 0.09)
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_many_sequences(pkg):
+    """More (sequence, kv head) pairs than SMs: no KV split at all."""
+    rng = np.random.default_rng(14)
+    lens = [int(v) for v in rng.integers(0, 700, 24)]
+    blocks = sum((n + 15) // 16 for n in lens) + 4
+    q, kc, vc, ks, vs, tbl, sl = oracle_layer(24, lens, blocks, 32, 8, 16, 14)
+    o = run(pkg, q, kc, vc, ks, vs, tbl, sl, 0.0883)
+    check(o, q, kc, vc, ks, vs, tbl, sl, 0.0883)
+    assert pkg.check_device_error() == 0
