@@ -209,10 +209,11 @@ __global__ void __launch_bounds__(256) block_quantize_generic_kernel(
 // --------------------------------------------------------------- MX, fast
 // Thread layout: each row of k bf16 is cut into 4*G chunks of 8 elements
 // (G = ceil(k/32) groups); chunks past k are padding.  A block of 256 threads
-// covers 4 consecutive 256-chunk slabs (ILP: four independent 16-byte loads in
-// flight per thread).  Lanes 4j..4j+3 hold one group.
+// covers kMxUnroll consecutive 256-chunk slabs (that many independent 16-byte
+// loads in flight per thread; 2 measured faster than 4 or 8).  Lanes
+// 4j..4j+3 hold one group.
 constexpr int kMxThreads = 256;
-constexpr int kMxUnroll = 4;
+constexpr int kMxUnroll = 2;
 
 __global__ void __launch_bounds__(kMxThreads) mx_quantize_kernel(const __nv_bfloat16 *__restrict__ w,
                                                                  uint8_t *__restrict__ codes,
@@ -348,8 +349,15 @@ __global__ void __launch_bounds__(kTensorThreads) tensor_amax_kernel(const __nv_
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTensorThreads;
     float amax = 0.0f;
     if (VEC) {
-        for (int64_t c = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; c < total / 8; c += stride)
-            amax = absmax8(ld_nc_v4(w + c * 8), amax);
+        // four independent 16-byte loads in flight per thread per step
+        const int64_t n8 = total / 8;
+        for (int64_t c = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; c < n8; c += 4 * stride) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = c + u * stride < n8 ? ld_nc_v4(w + (c + u * stride) * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) amax = absmax8(v[u], amax);
+        }
     } else {
         const uint16_t *wb = reinterpret_cast<const uint16_t *>(w);
         for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; e < total; e += stride)
@@ -368,8 +376,15 @@ __global__ void __launch_bounds__(kTensorThreads) tensor_encode_kernel(const __n
     const float y = recip_for(s);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTensorThreads;
     if (VEC) {
-        for (int64_t c = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; c < total / 8; c += stride)
-            *reinterpret_cast<uint2 *>(codes + c * 8) = encode8_quot(ld_nc_v4(w + c * 8), s, y);
+        const int64_t n8 = total / 8;
+        for (int64_t c = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; c < n8; c += 4 * stride) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = c + u * stride < n8 ? ld_nc_v4(w + (c + u * stride) * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (c + u * stride < n8) *reinterpret_cast<uint2 *>(codes + (c + u * stride) * 8) = encode8_quot(v[u], s, y);
+        }
     } else {
         const uint16_t *wb = reinterpret_cast<const uint16_t *>(w);
         for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; e < total; e += stride) {
