@@ -119,6 +119,17 @@ __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// Ask for one 2-D box to be brought into L2 (no shared memory, no
+// completion).  L2 is the coherence point of device memory, so a prefetch
+// can never return stale data: it is safe even while the previous kernel in
+// the stream may still be writing the same addresses.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

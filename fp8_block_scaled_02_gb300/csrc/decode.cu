@@ -40,9 +40,13 @@
 //    of the extra rows is nothing next to the weight stream at m <= 32) and
 //    stores only the outputs of tokens routed to it.  Each selected expert's
 //    weight is read once per call, whatever the number of its tokens.
-//  * Programmatic dependent launch: a kernel may start (barrier init,
-//    tensor-map prefetch) while the previous kernel in the stream drains; it
-//    reads global memory only after griddepcontrol.wait.
+//  * Programmatic dependent launch: every CTA lets the next kernel in the
+//    stream be scheduled as soon as it has started, and may itself start
+//    (barrier init, tensor-map prefetch, an L2 prefetch of its first
+//    ring-depth of code tiles) while the previous kernel drains; it reads
+//    global memory only after griddepcontrol.wait.  An L2 prefetch cannot
+//    observe stale data, so it is safe even if the previous kernel writes the
+//    weight; on a chain of small GEMVs it hides the first DRAM latency.
 #include "common.cuh"
 #include "internal.h"
 
@@ -212,8 +216,23 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
     if (warp == kWarpTma && lane == 0) {
         prefetch_tensormap(&tm_codes);
         prefetch_tensormap(&tm_x);
+        // While the previous kernel drains, start this CTA's first ring-depth
+        // of weight tiles on their way into L2 (more would delay the first
+        // loads when there is nothing to overlap; MoE CTAs do not know their
+        // expert yet).
+        if (!MOE) {
+            const int npf = min(total, kStages);
+            for (int it = 0; it < npf; ++it) {
+                const int ti = it / nkb;
+                tma_prefetch_l2_2d(&tm_codes, (kb0 + (it - ti * nkb)) * kKB, (tile0 + ti * tstep) * kBN);
+            }
+        }
     }
     __syncthreads();
+    // Nothing before this point reads what an earlier kernel writes, so the
+    // next kernel in the stream may be scheduled now; it waits for this one
+    // to complete before it reads any input.
+    pdl_launch_dependents();
     pdl_wait();  // inputs may be produced by the previous kernel in the stream
 
     int expert = 0;
@@ -676,7 +695,6 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
             if (stop) break;
         }
     }
-    pdl_launch_dependents();
     if (splits == 1) return;
 
     // Split-K: one row tile per CTA; reduce across the cluster in rank order.
