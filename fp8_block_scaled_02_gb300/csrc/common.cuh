@@ -168,6 +168,13 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_addr, uint32_t rank
     return r;
 }
 
+// Store to the shared memory of a CTA of this cluster (an address from
+// dsmem_map); a later cluster barrier with release / acquire semantics makes
+// it visible to that CTA.
+__device__ __forceinline__ void dsmem_st_f32(uint32_t cluster_addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
 // Volatile keeps it after the cluster barrier; several can still be in
 // flight when the caller issues them before using any result.
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {

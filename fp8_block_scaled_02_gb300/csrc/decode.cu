@@ -97,11 +97,15 @@ struct Cfg {
     static constexpr int kAuxBytes = (kXInvFloats + kRowScaleFloats) * 4;
     static constexpr int kRedStride = kXRows + 1;       // padded fp32 row
     static constexpr int kRedBytes = kBN * kRedStride * 4;
+    // split-K receive buffer: [source rank][row of this CTA's slice][m];
+    // splits * ceil(kBN / splits) <= kBN + 7 rows (even, for alignment)
+    static constexpr int kRecvFloats = (kBN + kMaxSplit) * kRedStride;
+    static constexpr int kRecvBytes = kRecvFloats * 4;
     static constexpr int kSmemBytes =
-        1024 + kStages * kStageBytes + kStages * kAuxBytes + kRedBytes + 3 * kStages * 8;
+        1024 + kStages * kStageBytes + kStages * kAuxBytes + kRedBytes + kRecvBytes + 3 * kStages * 8;
     static constexpr int kMinBlocks = 2;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static_assert((kStages * kAuxBytes + kRedBytes) % 8 == 0, "barriers must stay 8-byte aligned");
+    static_assert((kStages * kAuxBytes + kRedBytes + kRecvBytes) % 8 == 0, "barriers must stay 8-byte aligned");
     static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
@@ -186,7 +190,8 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                                                 ~static_cast<uintptr_t>(1023));
     float *aux = reinterpret_cast<float *>(smem + kStages * C::kStageBytes);
     float *red = aux + kStages * (C::kXInvFloats + C::kRowScaleFloats);
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + kBN * C::kRedStride);
+    float *recv = red + kBN * C::kRedStride;
+    uint64_t *full = reinterpret_cast<uint64_t *>(recv + C::kRecvFloats);
     uint64_t *xready = full + kStages;
     uint64_t *empty = xready + kStages;
 
@@ -698,36 +703,42 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
     if (splits == 1) return;
 
     // Split-K: one row tile per CTA; reduce across the cluster in rank order.
-    __syncthreads();
-    cluster_sync_all();
+    // CTA r finishes rows [r * rows_per, (r + 1) * rows_per) of the tile.
+    // Every CTA pushes each row's partial straight into its finisher's
+    // receive buffer (DSMEM stores, slot = source rank), then one cluster
+    // barrier (release / acquire) makes all of them visible; each CTA sums
+    // its slots locally in rank order and leaves.  Nothing reads another
+    // CTA's shared memory, so no second barrier is needed before exit.
+    __syncthreads();  // local partials complete in red
     const int n0 = tile0 * kBN;
     const int rank = static_cast<int>(cluster_ctarank());
     const int rows_per = (kBN + splits - 1) / splits;
+    {
+        const uint32_t recv_base = smem_u32(recv) + static_cast<uint32_t>(rank * rows_per * C::kRedStride * 4);
+        for (int e = threadIdx.x; e < mm * kBN; e += C::kThreads) {
+            const int nl = e / mm;
+            const int mi = e - nl * mm;
+            const int owner = nl / rows_per;
+            const uint32_t off = static_cast<uint32_t>(((nl - owner * rows_per) * C::kRedStride + mi) * 4);
+            dsmem_st_f32(dsmem_map(recv_base + off, static_cast<uint32_t>(owner)), red[nl * C::kRedStride + mi]);
+        }
+    }
+    cluster_sync_all();
     const int r_begin = rank * rows_per;
     const int r_end = min(kBN, r_begin + rows_per);
     const int my_rows = max(0, r_end - r_begin);
-    // all of a thread's remote loads are issued before the first add, so a
-    // cluster of S costs one DSMEM round trip rather than S
-    uint32_t peer_red[kMaxSplit];
-#pragma unroll
-    for (int q = 0; q < kMaxSplit; ++q) peer_red[q] = q < splits ? dsmem_map(smem_u32(red), q) : 0u;
     for (int e = threadIdx.x; e < mm * my_rows; e += C::kThreads) {
         const int mi = e / my_rows;
-        const int nl = r_begin + (e - mi * my_rows);
-        const int nn = n0 + nl;
+        const int rl = e - mi * my_rows;
+        const int nn = n0 + r_begin + rl;
         const int64_t o = nn < n ? out_at(mi, nn) : -1;
         if (o < 0) continue;
-        const uint32_t off = static_cast<uint32_t>((nl * C::kRedStride + mi) * 4);
-        float part[kMaxSplit];
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q) part[q] = q < splits ? dsmem_ld_f32(peer_red[q] + off) : 0.0f;
         float sum = 0.0f;
 #pragma unroll
         for (int q = 0; q < kMaxSplit; ++q)
-            if (q < splits) sum += part[q];
+            if (q < splits) sum += recv[(q * rows_per + rl) * C::kRedStride + mi];
         y[o] = __float2bfloat16_rn(ROW ? sum * out_scale(nn) : sum);
     }
-    cluster_sync_all();  // keep shared memory alive for peers
 }
 
 // Per-device, per-instantiation launch setup (shared-memory opt-in and the
