@@ -55,11 +55,13 @@ struct DCfg {
     static constexpr int kXBytes = kXRows * kKB;          // 1-4 KB, a multiple of 1024
     static constexpr int kStageBytes = kCodeBytes + kXBytes;
     static constexpr int kRedStride = kXRows + 1;
-    static constexpr int kRedBytes = kDBN * kRedStride * 4;
+    // split-K receive buffer: [source rank][row of this CTA's slice][m];
+    // splits * ceil(128 / splits) <= 135 rows
+    static constexpr int kRecvFloats = (kDBN + kMaxSplit) * kRedStride;
     static constexpr int kThreads = (kDConsumers + 1) * 32;
-    static constexpr int kSmemBytes = 1024 + kDStages * kStageBytes + kRedBytes + 2 * kDStages * 8;
+    static constexpr int kSmemBytes = 1024 + kDStages * kStageBytes + kRecvFloats * 4 + 2 * kDStages * 8;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static_assert(kRedBytes % 8 == 0, "barriers must stay 8-byte aligned");
+    static_assert((kRecvFloats * 4) % 8 == 0, "barriers must stay 8-byte aligned");
     static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
@@ -81,8 +83,8 @@ __global__ void __launch_bounds__(DCfg<MT>::kThreads, 2) w8a8_decode_kernel(
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    float *red = reinterpret_cast<float *>(smem + kDStages * C::kStageBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(red + kDBN * C::kRedStride);
+    float *recv = reinterpret_cast<float *>(smem + kDStages * C::kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(recv + C::kRecvFloats);
     uint64_t *empty = full + kDStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,6 +96,9 @@ __global__ void __launch_bounds__(DCfg<MT>::kThreads, 2) w8a8_decode_kernel(
     const int my_tiles = tile0 < ntiles ? (ntiles - tile0 + tstep - 1) / tstep : 0;
     const int total = my_tiles * nkb;
     const int mm = min(m, C::kXRows);
+    // split-K: CTA r of the cluster finishes rows [r * rows_per, (r + 1) * rows_per)
+    const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int rows_per = (kDBN + splits - 1) / splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDStages; ++s) {
@@ -105,8 +110,18 @@ __global__ void __launch_bounds__(DCfg<MT>::kThreads, 2) w8a8_decode_kernel(
     if (warp == kDWarpTma && lane == 0) {
         prefetch_tensormap(&tm_w);
         prefetch_tensormap(&tm_x);
+        // the first ring-depth of weight tiles on their way into L2 while the
+        // previous kernel drains (an L2 prefetch never observes stale data)
+        const int npf = min(total, kDStages);
+        for (int it = 0; it < npf; ++it) {
+            const int ti = it / nkb;
+            tma_prefetch_l2_2d(&tm_w, (kb0 + (it - ti * nkb)) * kKB, (tile0 + ti * tstep) * kDBN);
+        }
     }
     __syncthreads();
+    // nothing above reads what an earlier kernel writes: let the next kernel
+    // in the stream be scheduled (it waits for this one before its reads)
+    pdl_launch_dependents();
     pdl_wait();  // x codes and s_x may come from the previous kernel in the stream
 
     if (warp == kDWarpTma) {
@@ -184,44 +199,40 @@ __global__ void __launch_bounds__(DCfg<MT>::kThreads, 2) w8a8_decode_kernel(
                     if (splits == 1) {
                         if (mi < m && n0 + nl < n)
                             y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(acc[j][q] * scale);
-                    } else {
-                        red[nl * C::kRedStride + mi] = acc[j][q];
+                    } else if (mi < mm) {
+                        // push the partial into its finisher's receive slot
+                        const int owner = nl / rows_per;
+                        const uint32_t dst = smem_u32(recv + ((rank * rows_per + nl - owner * rows_per) *
+                                                              C::kRedStride + mi));
+                        dsmem_st_f32(dsmem_map(dst, static_cast<uint32_t>(owner)), acc[j][q]);
                     }
                 }
         }
     }
-    pdl_launch_dependents();
     if (splits == 1) return;
 
     // Split-K: one row tile per CTA; reduce across the cluster in rank order.
-    __syncthreads();
+    // The consumers pushed each row's partial into its finisher's receive
+    // buffer (slot = source rank); one release / acquire cluster barrier
+    // makes them visible, and each CTA sums its rows locally in rank order
+    // (no remote reads, so no second barrier before exit).
+    const int n0 = tile0 * kDBN;
     cluster_sync_all();
     const float scale = __ldg(sx_p) * __ldg(sw_p);
-    const int n0 = tile0 * kDBN;
-    const int rank = static_cast<int>(cluster_ctarank());
-    const int rows_per = (kDBN + splits - 1) / splits;
     const int r_begin = rank * rows_per;
     const int r_end = min(kDBN, r_begin + rows_per);
     const int my_rows = max(0, r_end - r_begin);
-    uint32_t peer_red[kMaxSplit];
-#pragma unroll
-    for (int q = 0; q < kMaxSplit; ++q) peer_red[q] = q < splits ? dsmem_map(smem_u32(red), q) : 0u;
     for (int e = threadIdx.x; e < mm * my_rows; e += C::kThreads) {
         const int mi = e / my_rows;
-        const int nl = r_begin + (e - mi * my_rows);
-        const int nn = n0 + nl;
+        const int rl = e - mi * my_rows;
+        const int nn = n0 + r_begin + rl;
         if (nn >= n) continue;
-        const uint32_t off = static_cast<uint32_t>((nl * C::kRedStride + mi) * 4);
-        float part[kMaxSplit];
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q) part[q] = q < splits ? dsmem_ld_f32(peer_red[q] + off) : 0.0f;
         float sum = 0.0f;
 #pragma unroll
         for (int q = 0; q < kMaxSplit; ++q)
-            if (q < splits) sum += part[q];
+            if (q < splits) sum += recv[(q * rows_per + rl) * C::kRedStride + mi];
         y[static_cast<int64_t>(mi) * n + nn] = __float2bfloat16_rn(sum * scale);
     }
-    cluster_sync_all();  // keep shared memory alive for peers
 }
 
 struct Setup {
