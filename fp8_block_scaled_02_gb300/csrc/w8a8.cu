@@ -48,6 +48,11 @@ constexpr int kDConsumers = 8;     // one 16-row tile each
 constexpr int kDWarpTma = kDConsumers;
 constexpr int kMaxSplit = 8;       // portable cluster size limit
 
+// named barrier of the eight consumer warps (the TMA warp is not waited for)
+__device__ __forceinline__ void w8a8_consumer_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kDConsumers * 32) : "memory");
+}
+
 template <int MT>
 struct DCfg {
     static constexpr int kXRows = 8 * MT;                 // x rows staged (zero-padded by TMA)
@@ -62,6 +67,7 @@ struct DCfg {
     static constexpr int kSmemBytes = 1024 + kDStages * kStageBytes + kRecvFloats * 4 + 2 * kDStages * 8;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
     static_assert((kRecvFloats * 4) % 8 == 0, "barriers must stay 8-byte aligned");
+    static_assert(kDBN * kRedStride * 4 <= kStageBytes, "split-K partials fit in ring stage 0");
     static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
@@ -154,9 +160,9 @@ __global__ void __launch_bounds__(DCfg<MT>::kThreads, 2) w8a8_decode_kernel(
         const int coff = (t & 1) * 8;
         const float scale = __ldg(sx_p) * __ldg(sw_p);
         bool failed = false;
+        float acc[MT][4];  // split-K: read again after the tile loop
         for (int ti = 0; ti < my_tiles && !failed; ++ti) {
             const int n0 = (tile0 + ti * tstep) * kDBN;
-            float acc[MT][4];
 #pragma unroll
             for (int j = 0; j < MT; ++j)
 #pragma unroll
@@ -196,17 +202,34 @@ __global__ void __launch_bounds__(DCfg<MT>::kThreads, 2) w8a8_decode_kernel(
                 for (int q = 0; q < 4; ++q) {
                     const int mi = 8 * j + 2 * t + (q & 1);
                     const int nl = q < 2 ? ra : rb;
-                    if (splits == 1) {
-                        if (mi < m && n0 + nl < n)
-                            y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(acc[j][q] * scale);
-                    } else if (mi < mm) {
-                        // push the partial into its finisher's receive slot
-                        const int owner = nl / rows_per;
-                        const uint32_t dst = smem_u32(recv + ((rank * rows_per + nl - owner * rows_per) *
-                                                              C::kRedStride + mi));
-                        dsmem_st_f32(dsmem_map(dst, static_cast<uint32_t>(owner)), acc[j][q]);
-                    }
+                    if (splits == 1 && mi < m && n0 + nl < n)
+                        y[static_cast<int64_t>(mi) * n + n0 + nl] = __float2bfloat16_rn(acc[j][q] * scale);
                 }
+        }
+        if (splits > 1) {
+            // Split-K (one row tile): stage the partials in ring stage 0, free
+            // once every consumer has left the ring, then push each row's
+            // partial into its finisher's receive slot with coalesced DSMEM
+            // stores (faster than scattering them from the MMA fragments).
+            float *red = reinterpret_cast<float *>(smem);
+            w8a8_consumer_bar();
+#pragma unroll
+            for (int j = 0; j < MT; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int mi = 8 * j + 2 * t + (q & 1);
+                    red[(q < 2 ? ra : rb) * C::kRedStride + mi] = acc[j][q];
+                }
+            w8a8_consumer_bar();
+            const uint32_t recv_base =
+                smem_u32(recv) + static_cast<uint32_t>(rank * rows_per * C::kRedStride * 4);
+            for (int e = threadIdx.x; e < mm * kDBN; e += kDConsumers * 32) {
+                const int nl = e / mm;
+                const int mi = e - nl * mm;
+                const int owner = nl / rows_per;
+                const uint32_t off = static_cast<uint32_t>(((nl - owner * rows_per) * C::kRedStride + mi) * 4);
+                dsmem_st_f32(dsmem_map(recv_base + off, static_cast<uint32_t>(owner)), red[nl * C::kRedStride + mi]);
+            }
         }
     }
     if (splits == 1) return;
