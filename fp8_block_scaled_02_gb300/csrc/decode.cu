@@ -748,6 +748,7 @@ struct Setup {
     bool done[64] = {};
     cudaError_t err[64] = {};
     int resident[64] = {};
+    ClusterFit fit;
 };
 
 template <int MT, int SC, bool F16>
@@ -790,10 +791,12 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     const int e8m0_vec = (groups % 4 == 0 && (reinterpret_cast<uintptr_t>(a.e8m0) & 3) == 0) ? 1 : 0;
     int splits = 1;
     if (ntiles < capacity) {
-        splits = capacity / ntiles;
-        if (splits > kMaxSplit) splits = kMaxSplit;
-        if (splits > kblocks) splits = kblocks;
-        if (splits < 1) splits = 1;
+        // as many K splits as fill the SMs, but only a cluster size whose
+        // clusters all fit at once (a second wave would cost more)
+        int cap = capacity / ntiles;
+        if (cap > kMaxSplit) cap = kMaxSplit;
+        if (cap > kblocks) cap = kblocks;
+        splits = pick_split(setup.fit, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes, ntiles, cap);
     }
     // splits == 1: persistent grid; splits > 1: one CTA per (row tile, split)
     const int gx = splits == 1 ? (ntiles < capacity ? ntiles : capacity) : ntiles;
@@ -863,10 +866,11 @@ cudaError_t launch_moe_t(const DecodeArgs &a, const MoeArgs &g, cudaStream_t str
     const int capacity = device_sm_count() * resident;
     int splits = 1;
     if (static_cast<int64_t>(ntiles) * slots < capacity) {
-        splits = capacity / (ntiles * slots);
-        if (splits > kMaxSplit) splits = kMaxSplit;
-        if (splits > kblocks) splits = kblocks;
-        if (splits < 1) splits = 1;
+        int cap = capacity / (ntiles * slots);
+        if (cap > kMaxSplit) cap = kMaxSplit;
+        if (cap > kblocks) cap = kblocks;
+        splits = pick_split(setup.fit, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes,
+                            ntiles * slots, cap);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>(splits), static_cast<unsigned>(slots));

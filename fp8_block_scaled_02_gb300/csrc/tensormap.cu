@@ -61,6 +61,41 @@ bool encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
     return r == CUDA_SUCCESS;
 }
 
+int pick_split(ClusterFit &fit, const void *kern, int threads, int smem, int tiles, int max_split) {
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || dev >= 64) return 1;
+    if (max_split > 8) max_split = 8;
+    for (int s = max_split; s > 1; --s) {
+        int fits;
+        {
+            std::lock_guard<std::mutex> lock(mu);
+            fits = fit.max_clusters[dev][s];
+            if (fits == 0) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(1, static_cast<unsigned>(s), 1);
+                cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+                cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+                cudaLaunchAttribute attr;
+                attr.id = cudaLaunchAttributeClusterDimension;
+                attr.val.clusterDim.x = 1;
+                attr.val.clusterDim.y = static_cast<unsigned>(s);
+                attr.val.clusterDim.z = 1;
+                cfg.attrs = &attr;
+                cfg.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+                    (void)cudaGetLastError();
+                    n = -1;
+                }
+                fit.max_clusters[dev][s] = fits = n;
+            }
+        }
+        if (fits >= tiles) return s;
+    }
+    return 1;
+}
+
 int device_sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;

@@ -263,6 +263,7 @@ struct Setup {
     bool done[64] = {};
     cudaError_t err[64] = {};
     int resident[64] = {};
+    ClusterFit fit;
 };
 
 template <int MT>
@@ -299,10 +300,11 @@ cudaError_t launch_decode_t(const W8A8Args &a, cudaStream_t stream) {
     const int capacity = device_sm_count() * resident;
     int splits = 1;
     if (ntiles < capacity) {
-        splits = capacity / ntiles;
-        if (splits > kMaxSplit) splits = kMaxSplit;
-        if (splits > kblocks) splits = kblocks;
-        if (splits < 1) splits = 1;
+        // as many K splits as fill the SMs, in clusters that all fit at once
+        int cap = capacity / ntiles;
+        if (cap > kMaxSplit) cap = kMaxSplit;
+        if (cap > kblocks) cap = kblocks;
+        splits = pick_split(setup.fit, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes, ntiles, cap);
     }
     const int gx = splits == 1 ? (ntiles < capacity ? ntiles : capacity) : ntiles;
 
