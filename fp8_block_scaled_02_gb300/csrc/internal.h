@@ -106,14 +106,15 @@ uint32_t take_kv_error();
 int device_sm_count();
 
 // Split-K cluster size for `tiles` clusters of one launch: the largest
-// s <= max_split whose clusters of s CTAs (kernel `kern`, `threads` threads,
+// s <= max_split (<= 16; above 8 the kernel must allow non-portable cluster
+// sizes) whose clusters of s CTAs (kernel `kern`, `threads` threads,
 // `smem` dynamic shared memory, cluster dims (1, s, 1)) can all be resident
 // at once, so the launch runs as a single wave -- a cluster size that does
 // not pack onto the GPCs can halve the clusters that fit.  The per-device
 // answers of cudaOccupancyMaxActiveClusters are cached in `fit`, one per
 // kernel instantiation.  Returns 1 (no cluster) if none fits.
 struct ClusterFit {
-    int max_clusters[64][9] = {};  // 0: not asked yet; -1: the query failed
+    int max_clusters[64][17] = {};  // 0: not asked yet; -1: the query failed
 };
 int pick_split(ClusterFit &fit, const void *kern, int threads, int smem, int tiles, int max_split);
 

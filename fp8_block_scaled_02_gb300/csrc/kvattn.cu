@@ -440,6 +440,7 @@ struct KvSetup {
     bool done[64] = {};
     cudaError_t err[64] = {};
     int max_split[64] = {};
+    ClusterFit fit;
 };
 
 template <int W, int S>
@@ -473,6 +474,10 @@ cudaError_t launch_kv_t(const KvAttnArgs &a, const CUtensorMap &tm_k, const CUte
     const int64_t by_len = chunks / (2 * W);
     if (splits > by_len) splits = by_len;
     if (splits > max_split) splits = max_split;
+    // only a cluster size whose clusters all fit at once (one wave)
+    if (splits > 1)
+        splits = pick_split(setup.fit, reinterpret_cast<const void *>(kern), W * 32, C::kSmemBytes,
+                            static_cast<int>(pairs), static_cast<int>(splits));
     if (splits < 1) splits = 1;
 
     cudaLaunchConfig_t cfg = {};

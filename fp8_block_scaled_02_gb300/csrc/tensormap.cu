@@ -65,7 +65,7 @@ int pick_split(ClusterFit &fit, const void *kern, int threads, int smem, int til
     static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || dev >= 64) return 1;
-    if (max_split > 8) max_split = 8;
+    if (max_split > 16) max_split = 16;
     for (int s = max_split; s > 1; --s) {
         int fits;
         {
