@@ -42,12 +42,16 @@ constexpr int kStageBytes = 2 * kTileBytes;  // K + V
 constexpr int kVStride = kD * 2 + 16;        // f16 V row in the transpose buffer, padded
 constexpr int kVScratch = kChunk * kVStride;
 constexpr int kMergeFloats = 2 * kGroup + kD * kGroup;  // m[8], l[8], O[128][8]
+// split merge receive buffer: [source rank][m[8], l[8], this rank's share of
+// O]; splits * (16 + ceil(1024 / splits)) <= 16 * 16 + 1024 + 15 floats
+constexpr int kRecvFloats = kMaxSplit * 2 * kGroup + kD * kGroup + kMaxSplit;
 // W consumer warps per CTA, S chunks in flight per warp.  4 x 5 (two CTAs
 // per SM) measured fastest on every decode shape; 8 x 5, 8 x 3, 4 x 8, 4 x 10
 // (one CTA per SM) and 2 x 5 were all slower.
 template <int W, int S>
 struct KvCfg {
-    static constexpr int kSmemBytes = 1024 + W * S * kStageBytes + W * kVScratch + kMergeFloats * 4 + W * S * 8;
+    static constexpr int kSmemBytes =
+        1024 + W * S * kStageBytes + W * kVScratch + (kMergeFloats + kRecvFloats) * 4 + W * S * 8;
     static constexpr int kResident = kSmemBytes <= 113 * 1024 ? 2 : 1;  // CTAs per SM
     // a warp's merge record (after its loop) reuses its own, then idle, stages
     static_assert(kMergeFloats * 4 <= S * kStageBytes, "merge record fits a warp's stages");
@@ -60,8 +64,6 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
-
-__device__ __forceinline__ float dsmem_ld(uint32_t base, int idx) { return dsmem_ld_f32(base + 4u * idx); }
 
 template <int W, int S>
 __global__ void __launch_bounds__(W * 32, KvCfg<W, S>::kResident) kv_attn_kernel(
@@ -77,7 +79,8 @@ __global__ void __launch_bounds__(W * 32, KvCfg<W, S>::kResident) kv_attn_kernel
     uint8_t *stages = smem;                                         // [warp][stage][K | V]
     uint8_t *vscr = stages + kWarps * kStages * kStageBytes;        // [warp][16][kVStride]
     float *res = reinterpret_cast<float *>(vscr + kWarps * kVScratch);  // this CTA's m, l, O
-    uint64_t *full = reinterpret_cast<uint64_t *>(res + kMergeFloats);  // [warp][stage]
+    float *recv = res + kMergeFloats;                                   // split merge inputs
+    uint64_t *full = reinterpret_cast<uint64_t *>(recv + kRecvFloats);  // [warp][stage]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -376,37 +379,52 @@ __global__ void __launch_bounds__(W * 32, KvCfg<W, S>::kResident) kv_attn_kernel
         }
         return;
     }
-    cluster_sync_all();
+    // Every CTA pushes m, l and the share of O that rank q finishes into q's
+    // receive slot (DSMEM stores, slot = source rank); one release / acquire
+    // cluster barrier makes them visible and each rank merges locally in rank
+    // order.  Nothing reads another CTA's shared memory afterwards, so no
+    // second barrier is needed before exit.
     const int rank = static_cast<int>(cluster_ctarank());
-    const uint32_t res_addr = smem_u32(res);
-    const int per = (kD * group + splits - 1) / splits;  // (dim, head) outputs this rank finishes
+    const int per = (kD * group + splits - 1) / splits;  // (dim, head) outputs a rank finishes
+    const int slot = 2 * kGroup + per;
+    {
+        const uint32_t recv_base = smem_u32(recv) + static_cast<uint32_t>(rank * slot * 4);
+        for (int e = threadIdx.x; e < splits * slot; e += kWarps * 32) {
+            const int q = e / slot;
+            const int i = e - q * slot;
+            float v;
+            if (i < 2 * kGroup) {
+                v = res[i];
+            } else {
+                const int e2 = q * per + (i - 2 * kGroup);
+                if (e2 >= kD * group) continue;
+                const int h = e2 / kD, d = e2 - h * kD;
+                v = res[2 * kGroup + d * kGroup + h];
+            }
+            dsmem_st_f32(dsmem_map(recv_base + static_cast<uint32_t>(i * 4), static_cast<uint32_t>(q)), v);
+        }
+    }
+    cluster_sync_all();
     for (int e2 = rank * per + threadIdx.x; e2 < min(kD * group, (rank + 1) * per); e2 += kWarps * 32) {
         const int h = e2 / kD, d = e2 - h * kD;
-        // every remote load is issued before the first use, so a cluster of
-        // S costs two DSMEM round trips rather than 3S
-        float mr[kMaxSplit], lr[kMaxSplit], orr[kMaxSplit];
-#pragma unroll
-        for (int r = 0; r < kMaxSplit; ++r) {
-            const uint32_t pa = r < splits ? dsmem_map(res_addr, r) : 0u;
-            mr[r] = r < splits ? dsmem_ld(pa, h) : -INFINITY;
-            lr[r] = r < splits ? dsmem_ld(pa, kGroup + h) : 0.0f;
-            orr[r] = r < splits ? dsmem_ld(pa, 2 * kGroup + d * kGroup + h) : 0.0f;
-        }
+        const int i = 2 * kGroup + (e2 - rank * per);
         float M = -INFINITY;
 #pragma unroll
-        for (int r = 0; r < kMaxSplit; ++r) M = fmaxf(M, mr[r]);
+        for (int r = 0; r < kMaxSplit; ++r)
+            if (r < splits) M = fmaxf(M, recv[r * slot + h]);
         float L = 0.0f, O = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int r = 0; r < kMaxSplit; ++r) {
-                const float f = mr[r] == -INFINITY ? 0.0f : exp2f(mr[r] - M);
-                L += f * lr[r];
-                O += f * orr[r];
+                if (r >= splits) continue;
+                const float mr = recv[r * slot + h];
+                const float f = mr == -INFINITY ? 0.0f : exp2f(mr - M);
+                L += f * recv[r * slot + kGroup + h];
+                O += f * recv[r * slot + i];
             }
         }
         ob[static_cast<int64_t>(h) * kD + d] = __float2bfloat16_rn(L > 0.0f ? O / L * v_scale : 0.0f);
     }
-    cluster_sync_all();  // keep shared memory alive for peers
 }
 
 // ------------------------------------------------------------- cache append
