@@ -85,7 +85,8 @@ struct Cfg {
     // ring depth: a fifth stage keeps the m <= 8 stream fuller (the
     // lm_head-sized GEMV measured 1.6% faster); wider x keeps four
     static constexpr int kStages = MT == 1 ? 5 : 4;
-    static constexpr bool kConv = F16 || MX;            // converter warp present
+    // converter warp: f16 x, or the e8m0 staging of the split layout
+    static constexpr bool kConv = F16 || (MX && !kFullRow);
     static constexpr int kConvWarps = kConv ? 1 : 0;
     static constexpr int kThreads = (kConsumerWarps + 1 + kConvWarps) * 32;
     static constexpr int kXRows = 8 * MT;               // x rows staged (zero-padded)
@@ -903,7 +904,7 @@ cudaError_t launch_sc(const DecodeArgs &a, cudaStream_t stream) {
     constexpr bool kMx = SC == kScaleMx;
     switch ((a.m + 7) / 8) {
         case 1: return launch_t<1, SC, true>(a, stream);
-        case 2: return launch_t<2, SC, kMx>(a, stream);
+        case 2: return launch_t<2, SC, false>(a, stream);
         case 3: return launch_t<3, SC, kMx>(a, stream);
         case 4: return launch_t<4, SC, kMx>(a, stream);
         default: return cudaErrorInvalidValue;

@@ -110,7 +110,7 @@ def test_small_shapes(pkg, n, k, m):
 
 
 @pytest.mark.parametrize("n,k", [(37, 48), (300, 7), (129, 272), (5, 1)])
-@pytest.mark.parametrize("m", [1, 8, 33])
+@pytest.mark.parametrize("m", [1, 8, 12, 20, 33])
 def test_small_shapes_mx(pkg, n, k, m):
     w = inputs.heavy_tail_weight(3, shape=(n, k), frac=0.01)
     oc, oe = oracle.mx_quantize(bits(w))
