@@ -375,19 +375,24 @@ __global__ void __launch_bounds__(kTensorThreads) tensor_encode_kernel(const __n
     const float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
     const float y = recip_for(s);
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTensorThreads;
+    // Walk the tensor back to front: the amax pass just read it front to
+    // back, so its last part is still in L2 when this pass starts.
     if (VEC) {
         const int64_t n8 = total / 8;
         for (int64_t c = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; c < n8; c += 4 * stride) {
             uint4 v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = c + u * stride < n8 ? ld_nc_v4(w + (c + u * stride) * 8) : make_uint4(0, 0, 0, 0);
+            for (int u = 0; u < 4; ++u)
+                v[u] = c + u * stride < n8 ? ld_nc_v4(w + (n8 - 1 - (c + u * stride)) * 8) : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (c + u * stride < n8) *reinterpret_cast<uint2 *>(codes + (c + u * stride) * 8) = encode8_quot(v[u], s, y);
+                if (c + u * stride < n8)
+                    *reinterpret_cast<uint2 *>(codes + (n8 - 1 - (c + u * stride)) * 8) = encode8_quot(v[u], s, y);
         }
     } else {
         const uint16_t *wb = reinterpret_cast<const uint16_t *>(w);
-        for (int64_t e = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; e < total; e += stride) {
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * kTensorThreads + threadIdx.x; i < total; i += stride) {
+            const int64_t e = total - 1 - i;
             const float q = __uint_as_float(static_cast<uint32_t>(wb[e]) << 16) / s;
             codes[e] = static_cast<uint8_t>(f32x2_to_e4m3x2(q, 0.0f) & 0xFF);
         }
