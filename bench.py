@@ -445,9 +445,9 @@ def quantize_workload(torch, fp8bs, inputs, dev):
 
 # ------------------------------------------------------------------ timing
 def time_calls(torch, calls, steps, warmup, pg, graph=False):
-    """Run `warmup` untimed steps, then `steps` timed ones.  Each call is
-    bracketed by CUDA events on the current stream; returns per-call mean
-    ms and the whole timed region in ms."""
+    """Run `warmup` untimed steps, then `steps` timed ones bracketed by one
+    pair of CUDA events on the current stream (the whole timed region, ms),
+    then `steps` more with events around each call (per-call mean ms)."""
     stream = torch.cuda.current_stream()
     run = [fn for _, _, _, fn in calls]
     if graph:
@@ -471,21 +471,29 @@ def time_calls(torch, calls, steps, warmup, pg, graph=False):
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in run]
-          for _ in range(steps)]
+    # whole-job time: one event pair around all steps (an event between two
+    # calls would separate them and stop the next launch from overlapping the
+    # previous one's tail, which is not how the calls run in an application)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for s in range(steps):
-        for i, fn in enumerate(run):
-            ev[s][i][0].record(stream)
+        for fn in run:
             fn()
-            ev[s][i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
     total = t0.elapsed_time(t1)
+    # per-call breakdown: a second pass with events around every call
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in run]
+          for _ in range(steps)]
+    for s in range(steps):
+        for i, fn in enumerate(run):
+            ev[s][i][0].record(stream)
+            fn()
+            ev[s][i][1].record(stream)
+    torch.cuda.synchronize()
     per = [statistics.fmean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)) for i in range(len(run))]
     return per, total
 
@@ -493,32 +501,56 @@ def time_calls(torch, calls, steps, warmup, pg, graph=False):
 def e2e_lm_head(torch, fp8bs, wl, steps, warmup, pg):
     """Same step through the public API with host buffers: every step copies
     each x from pinned host memory and reads each y back into pinned host
-    memory, inside the timed region."""
+    memory, inside the timed region.  The copies run on their own streams
+    (one per direction), ordered against the GEMVs by events, with x and y
+    double-buffered across steps, so a call's read-back overlaps the next
+    call's GEMV; the region ends after the last read-back has landed."""
     stream = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     ms = wl["cfg"]["ms"]
     hx = {m: wl["xs"][m].cpu().pin_memory() for m in ms}
-    hy = {m: torch.empty(tuple(wl["ys"][m].shape), dtype=torch.bfloat16).pin_memory() for m in ms}
-    dx = {m: torch.empty_like(wl["xs"][m]) for m in ms}
+    hy = {m: [torch.empty(tuple(wl["ys"][m].shape), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+          for m in ms}
+    dx = {m: [torch.empty_like(wl["xs"][m]) for _ in range(2)] for m in ms}
+    dy = {m: [wl["ys"][m], torch.empty_like(wl["ys"][m])] for m in ms}
+    ev = {(m, b, kind): torch.cuda.Event() for m in ms for b in range(2) for kind in ("x", "gemv", "y")}
+    used = set()
 
-    def step():
+    def step(i):
+        b = i & 1
         for m in ms:
-            dx[m].copy_(hx[m], non_blocking=True)
-            fp8bs.gemv(dx[m], wl["codes"], wl["scales"], y=wl["ys"][m])
-            hy[m].copy_(wl["ys"][m], non_blocking=True)
-    for _ in range(warmup):
-        step()
+            if (m, b) in used:  # the GEMV that last read dx[m][b] has finished
+                h2d_s.wait_event(ev[(m, b, "gemv")])
+            with torch.cuda.stream(h2d_s):
+                dx[m][b].copy_(hx[m], non_blocking=True)
+                ev[(m, b, "x")].record(h2d_s)
+            stream.wait_event(ev[(m, b, "x")])
+            if (m, b) in used:  # dy[m][b]'s previous read-back has landed
+                stream.wait_event(ev[(m, b, "y")])
+            fp8bs.gemv(dx[m][b], wl["codes"], wl["scales"], y=dy[m][b])
+            ev[(m, b, "gemv")].record(stream)
+            d2h_s.wait_event(ev[(m, b, "gemv")])
+            with torch.cuda.stream(d2h_s):
+                hy[m][b].copy_(dy[m][b], non_blocking=True)
+                ev[(m, b, "y")].record(d2h_s)
+            used.add((m, b))
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     barrier(pg)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(steps):
-        step()
+    h2d_s.wait_stream(stream)
+    for i in range(steps):
+        step(warmup + i)
+    stream.wait_stream(h2d_s)
+    stream.wait_stream(d2h_s)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(pg)
     h2d = sum(hx[m].numel() * 2 for m in ms)
-    d2h = sum(hy[m].numel() * 2 for m in ms)
+    d2h = sum(hy[m][0].numel() * 2 for m in ms)
     return t0.elapsed_time(t1), h2d, d2h
 
 
