@@ -168,6 +168,15 @@ def test_rotation_shapes(pkg, j):
     sampled_block_case(pkg, w, [1, 8, 16, 32], _row_blocks(w.shape[0], 3, j))
 
 
+@pytest.mark.parametrize("n,ms", [(2560, [12, 17, 24, 32]), (3072, [17, 24, 32]), (5120, [17, 32])])
+def test_split_cluster_sizes(pkg, n, ms):
+    """Weights of 20 / 40 / 48 / 80 row tiles: the split-K cluster size is the
+    largest whose clusters all fit in one wave (not capacity / tiles, which
+    gives 6 or 7 here); every split count must give the same sums."""
+    w = inputs.gaussian_bf16((n, 2560), 0.02, n + 11, device=DEV)
+    sampled_block_case(pkg, w, ms, _row_blocks(n, 3, n))
+
+
 def test_sweep_shape_all_m(pkg):
     w = inputs.sweep_weight(0, device=DEV)
     sampled_block_case(pkg, w, list(range(1, 33)), _row_blocks(w.shape[0], 2, 5))
