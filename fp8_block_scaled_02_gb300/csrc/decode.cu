@@ -12,23 +12,26 @@
 //    no waits on other CTAs beyond the hardware cluster barrier.
 //  * A TMA warp streams each K block's 128x128 code tile (16 KB) and the
 //    matching x tile (2-D TMA, 128-byte swizzle) into a shared-memory ring.
-//  * A converter warp rewrites each staged x tile in place from bf16 to f16
-//    with an exact power-of-two rescale per (row of x, 32-column slice): the
-//    slice maximum is moved into [2^14, 2^15), so every value within 2^-31 of
-//    the slice maximum converts exactly and nothing overflows; the inverse
-//    power of two is kept for the promotion step.  For MXFP8 it also stages
-//    the K block's e8m0 exponents as fp32 row scales.
-//  * Eight consumer warps (4 column slices x 2 row halves) convert code pairs
-//    with cvt.rn.f16x2.e4m3x2 (exact) and run f16 mma.sync m16n8k16 with the
-//    weights as the 16-row A operand and x as the 8-wide B operand (m on the
-//    MMA's n axis, so m <= 32 needs at most four n8 tiles).  Each K slice's
-//    fp32 MMA result starts from zero and is multiplied by (block scale x
-//    inverse x rescale) before it joins the accumulator, so the scale is
-//    applied once per 128-wide K block to an fp32 partial and is never folded
-//    into a rounded weight.  For MXFP8 a warp's 32-column slice is exactly
-//    one e8m0 group.  With one scale per row (or per tensor) the K blocks
-//    accumulate unscaled and the row's scale multiplies the fp32 sum once,
-//    just before the bf16 rounding.
+//  * For m <= 8 a converter warp rewrites each staged x tile in place from
+//    bf16 to f16 with an exact power-of-two rescale per (row of x, 32-column
+//    slice): the slice maximum is moved into [2^14, 2^15), so every value
+//    within 2^-31 of the slice maximum converts exactly and nothing
+//    overflows; the inverse power of two is kept for the promotion step.
+//    Wider x keeps bf16 operands and needs no converter.
+//  * Eight consumer warps each own one 16-row tile of the weight across the
+//    whole 128-wide K block (so row sums never cross warps) and run
+//    mma.sync m16n8k16 with the weights as the 16-row A operand and x as the
+//    8-wide B operand (m on the MMA's n axis, so m <= 32 needs at most four
+//    n8 tiles).  Codes convert with cvt.rn.f16x2.e4m3x2 (f16 form) or decode
+//    to bf16 with integer ops, both exact.  Each 32-column K slice's fp32
+//    MMA result starts from zero and is multiplied by (block scale x inverse
+//    x rescale) before it joins the accumulator, so the scale is applied once
+//    per 128-wide K block to an fp32 partial and is never folded into a
+//    rounded weight.  For MXFP8 a 32-column slice is exactly one e8m0 group,
+//    whose exponents each warp fetches for its rows one K block ahead.  With
+//    one scale per row (or per tensor) the K blocks accumulate unscaled and
+//    the row's scale multiplies the fp32 sum once, just before the bf16
+//    rounding.
 //  * The logical k order inside each MMA is a fixed permutation of the
 //    physical columns, applied identically to A and B, so every thread
 //    fetches 8 contiguous code bytes and 16 contiguous x bytes per K block
@@ -59,7 +62,7 @@ namespace {
 __device__ uint32_t g_decode_err;
 
 constexpr int kKB = 128;             // K per stage (one scale block)
-constexpr int kConsumerWarps = 8;    // 4 column slices x 2 row halves
+constexpr int kConsumerWarps = 8;    // one 16-row tile of the 128 weight rows each
 constexpr int kWarpTma = kConsumerWarps;
 constexpr int kWarpConv0 = kConsumerWarps + 1;
 constexpr int kMaxSplit = 8;         // portable cluster size limit
@@ -68,25 +71,21 @@ constexpr int kMoeMaxExperts = 1024; // experts a grouped call may address (bitm
 // F16: operands are f16 (codes via cvt.rn.f16x2.e4m3x2, x rescaled to f16 by
 // a converter warp); otherwise bf16 (codes decoded with integer ops, x used
 // as staged).  The f16 form halves the decode work and wins while the
-// consumers are bound by it (m <= 8); the bf16 form has no converter stage
-// and wins for wider x.  MXFP8 always uses the converter warp, which also
-// stages the e8m0 row scales.
+// consumers are bound by it (m <= 8); beyond that the single converter warp
+// becomes the bottleneck and the bf16 form, which needs none, wins.
 template <int MT, bool MX, bool F16>
 struct Cfg {
-    // weight rows per CTA: a full block-scale row for m <= 16, half of one for
-    // wider x (keeps the accumulators of two CTAs per SM in registers)
-    static constexpr int kBN = MT <= 2 ? 128 : 64;
-    static constexpr int kRT = kBN / 32;                // 16-row tiles per consumer warp (split layout)
-    // m <= 16: each consumer warp owns one 16-row tile across the whole K
-    // block, so row sums never cross warps (no reduction epilogue); wider x
-    // splits the K block over 4 warps to share each B fragment over 2 row
-    // tiles, and reduces across warps once per row tile.
-    static constexpr bool kFullRow = MT <= 2;
+    // weight rows per CTA: one block-scale row.  Each of the 8 consumer
+    // warps owns one 16-row tile across the whole 128-wide K block, so row
+    // sums never cross warps; with m > 16 the x fragments of a K block are
+    // loaded by every warp, which costs shared-memory reads but no
+    // cross-warp reduction and only MT x 4 accumulators per thread.
+    static constexpr int kBN = 128;
     // ring depth: a fifth stage keeps the m <= 8 stream fuller (the
-    // lm_head-sized GEMV measured 1.6% faster); wider x keeps four
-    static constexpr int kStages = MT == 1 ? 5 : 4;
-    // converter warp: f16 x, or the e8m0 staging of the split layout
-    static constexpr bool kConv = F16 || (MX && !kFullRow);
+    // lm_head-sized GEMV measured 1.6% faster); wider x tiles leave room for
+    // four (m <= 16) or three stages within two CTAs per SM
+    static constexpr int kStages = MT == 1 ? 5 : (MT == 2 ? 4 : 3);
+    static constexpr bool kConv = F16;                  // converter warp present
     static constexpr int kConvWarps = kConv ? 1 : 0;
     static constexpr int kThreads = (kConsumerWarps + 1 + kConvWarps) * 32;
     static constexpr int kXRows = 8 * MT;               // x rows staged (zero-padded)
@@ -94,8 +93,7 @@ struct Cfg {
     static constexpr int kXPanelBytes = kXRows * 128;   // 64 columns of each row
     static constexpr int kStageBytes = kCodeBytes + 2 * kXPanelBytes;
     static constexpr int kXInvFloats = 4 * kXRows;      // per stage: [slice][row]
-    static constexpr int kRowScaleFloats = (MX && MT > 2) ? 4 * kBN : 0;  // per stage: [slice][weight row]
-    static constexpr int kAuxBytes = (kXInvFloats + kRowScaleFloats) * 4;
+    static constexpr int kAuxBytes = kXInvFloats * 4;
     static constexpr int kRedStride = kXRows + 1;       // padded fp32 row
     static constexpr int kRedBytes = kBN * kRedStride * 4;
     // split-K receive buffer: [source rank][row of this CTA's slice][m];
@@ -185,12 +183,11 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
     };
     constexpr int kStages = C::kStages;
     constexpr int kBN = C::kBN;
-    constexpr int kRT = C::kRT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     float *aux = reinterpret_cast<float *>(smem + kStages * C::kStageBytes);
-    float *red = aux + kStages * (C::kXInvFloats + C::kRowScaleFloats);
+    float *red = aux + kStages * C::kXInvFloats;
     float *recv = red + kBN * C::kRedStride;
     uint64_t *full = reinterpret_cast<uint64_t *>(recv + C::kRecvFloats);
     uint64_t *xready = full + kStages;
@@ -328,36 +325,8 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
         // ------------------------------------------------------ x converter
         const int clane = (warp - kWarpConv0) * 32 + lane;
         constexpr int kConvLanes = C::kConvWarps * 32;
-        // e8m0 bytes of this lane's rows for stage `it` (4 groups per row),
-        // fetched one stage ahead so their latency hides behind the ring
-        constexpr bool kStageE8m0 = MX && !C::kFullRow;  // full-row consumers fetch their own
-        constexpr int kRowsPerLane = kStageE8m0 ? kBN / kConvLanes : 1;
-        auto load_e8m0 = [&](int it, uint32_t (&ev)[kRowsPerLane]) {
-            const int ti = it / nkb;
-            const int n0 = (tile0 + ti * tstep) * kBN;
-            const int g0 = (kb0 + (it - ti * nkb)) * 4;
-#pragma unroll
-            for (int i = 0; i < kRowsPerLane; ++i) {
-                const int64_t row = static_cast<int64_t>(n0) + clane + i * kConvLanes;
-                uint32_t w = 0;
-                if (row < n) {
-                    const uint8_t *p = e8m0 + row * groups + g0;
-                    if (e8m0_vec) {
-                        w = __ldg(reinterpret_cast<const uint32_t *>(p));
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (g0 + q < groups) w |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
-                    }
-                }
-                ev[i] = w;
-            }
-        };
-        uint32_t ev[kRowsPerLane], ev_next[kRowsPerLane];
-        if (kStageE8m0 && total > 0) load_e8m0(0, ev);
         for (int it = 0; it < total; ++it) {
             const int s = it % kStages;
-            if (kStageE8m0 && it + 1 < total) load_e8m0(it + 1, ev_next);
             const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
             if (!__all_sync(0xffffffffu, ready)) {
                 if (lane == 0) {
@@ -367,35 +336,15 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                 break;
             }
             uint8_t *xs = smem + s * C::kStageBytes + C::kCodeBytes;
-            float *xinv = aux + s * (C::kXInvFloats + C::kRowScaleFloats);
-            if (F16) {
-                for (int u = clane; u < 4 * C::kXRows; u += kConvLanes)
-                    convert_x_slice<C::kXPanelBytes, C::kXRows>(xs, xinv, u >> 2, u & 3);
-            }
-            if (kStageE8m0) {
-                const int ti = it / nkb;
-                const int n0 = (tile0 + ti * tstep) * kBN;
-                const int g0 = (kb0 + (it - ti * nkb)) * 4;
-                float *rs = xinv + C::kXInvFloats;
-#pragma unroll
-                for (int i = 0; i < kRowsPerLane; ++i) {
-                    const int r = clane + i * kConvLanes;
-                    const bool rin = n0 + r < n;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        rs[q * kBN + r] = (rin && g0 + q < groups) ? pow2_e8m0((ev[i] >> (8 * q)) & 0xFFu) : 0.0f;
-                }
-            }
+            float *xinv = aux + s * C::kXInvFloats;
+            for (int u = clane; u < 4 * C::kXRows; u += kConvLanes)
+                convert_x_slice<C::kXPanelBytes, C::kXRows>(xs, xinv, u >> 2, u & 3);
             fence_proxy_async_smem();  // the TMA will overwrite these bytes later
             __syncwarp();
             if (lane == 0) mbar_arrive(&xready[s]);
-            if (kStageE8m0) {
-#pragma unroll
-                for (int i = 0; i < kRowsPerLane; ++i) ev[i] = ev_next[i];
-            }
         }
-    } else if (C::kFullRow) {
-        // ------------------------------------------- consumers, full rows
+    } else {
+        // ------------------------------------------------------ consumers
         const int g = lane >> 2, t = lane & 3;
         const int ra = warp * 16 + 2 * g, rb = ra + 1;  // this thread's two weight rows
         // x rows of this thread's B fragments: row 8j + pi(g) with
@@ -450,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                 }
                 const uint8_t *cs = smem + s * C::kStageBytes;
                 const uint8_t *xbase = cs + C::kCodeBytes;
-                const float *xinv = aux + s * (C::kXInvFloats + C::kRowScaleFloats);
+                const float *xinv = aux + s * C::kXInvFloats;
 #pragma unroll
                 for (int sl = 0; sl < 4; ++sl) {
                     const uint8_t *xs = xbase + (sl >> 1) * C::kXPanelBytes;
@@ -536,169 +485,6 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                         red[nl * C::kRedStride + mi] = acc[j][q];
                     }
                 }
-        }
-    } else {
-        // ------------------------------------------------------ consumers
-        const int g = lane >> 2, t = lane & 3;
-        const int cw = warp & 3;                    // 32-column slice of each K block
-        const int rbase = (warp >> 2) * (kBN / 2);  // row half
-        // x rows of this thread's B fragments: row 8j + pi(g) with
-        // pi(g) = (g >> 1) | ((g & 1) << 2) (bank-conflict-free swizzle use)
-        const int xrow_base = (g >> 1) | ((g & 1) << 2);
-        const int xpanel = cw >> 1;
-        const int xchunk = 4 * (cw & 1) + t;
-        // code rows of this thread's A fragments: 2g and 2g+1 of each 16-row tile
-        const int cchunk = 2 * cw + (t >> 1);
-        const int coff = (t & 1) * 8;
-
-        for (int ti = 0; ti < my_tiles; ++ti) {
-            const int n0 = (tile0 + ti * tstep) * kBN;
-            const float *srow = (MX || ROW) ? nullptr : scale_base + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
-            float acc[kRT][MT][4];
-#pragma unroll
-            for (int rt = 0; rt < kRT; ++rt)
-#pragma unroll
-                for (int j = 0; j < MT; ++j)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[rt][j][q] = 0.0f;
-            float s_next = (MX || ROW) ? 1.0f : __ldg(srow);
-
-            for (int kbi = 0; kbi < nkb; ++kbi) {
-                const int it = ti * nkb + kbi;
-                const int s = it % kStages;
-                const float sblk = s_next;
-                if (!MX && !ROW && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
-                // every lane waits (acquire); the warp leaves together if any gave up
-                const uint32_t par = (it / kStages) & 1;
-                const bool ready =
-                    mbar_wait_bounded(&full[s], par) && (!C::kConv || mbar_wait_bounded(&xready[s], par));
-                if (!__all_sync(0xffffffffu, ready)) {
-                    if (lane == 0) {
-                        atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
-                        s_fail = 1;
-                    }
-                    break;
-                }
-                const uint8_t *cs = smem + s * C::kStageBytes;
-                const uint8_t *xs = cs + C::kCodeBytes + xpanel * C::kXPanelBytes;
-                const float *xinv = aux + s * (C::kXInvFloats + C::kRowScaleFloats) + cw * C::kXRows;
-
-                uint32_t bx[MT][4];
-                float f0[MT], f1[MT];  // promotion factors of this thread's two C columns
-#pragma unroll
-                for (int j = 0; j < MT; ++j) {
-                    const int xr = 8 * j + xrow_base;
-                    const uint4 v =
-                        *reinterpret_cast<const uint4 *>(xs + xr * 128 + ((xchunk ^ (xr & 7)) << 4));
-                    bx[j][0] = v.x;
-                    bx[j][1] = v.y;
-                    bx[j][2] = v.z;
-                    bx[j][3] = v.w;
-                    if (F16) {
-                        const float2 iv = *reinterpret_cast<const float2 *>(xinv + 8 * j + 2 * t);
-                        f0[j] = MX ? iv.x : sblk * iv.x;
-                        f1[j] = MX ? iv.y : sblk * iv.y;
-                    } else {
-                        f0[j] = MX ? 1.0f : sblk;
-                        f1[j] = MX ? 1.0f : sblk;
-                    }
-                }
-
-#pragma unroll
-                for (int rt = 0; rt < kRT; ++rt) {
-                    const int ra = rbase + rt * 16 + 2 * g, rb = ra + 1;
-                    const uint2 qa =
-                        *reinterpret_cast<const uint2 *>(cs + ra * 128 + ((cchunk ^ (ra & 7)) << 4) + coff);
-                    const uint2 qb =
-                        *reinterpret_cast<const uint2 *>(cs + rb * 128 + ((cchunk ^ (rb & 7)) << 4) + coff);
-                    uint32_t a00, a02, a01, a03, a10, a12, a11, a13;
-                    if (F16) {
-                        e4m3x4_to_f16x2x2(qa.x, a00, a02);
-                        e4m3x4_to_f16x2x2(qb.x, a01, a03);
-                        e4m3x4_to_f16x2x2(qa.y, a10, a12);
-                        e4m3x4_to_f16x2x2(qb.y, a11, a13);
-                    } else {
-                        a00 = e4m3x2_to_bf16x2(qa.x, 0x9180u);
-                        a02 = e4m3x2_to_bf16x2(qa.x, 0xB3A2u);
-                        a01 = e4m3x2_to_bf16x2(qb.x, 0x9180u);
-                        a03 = e4m3x2_to_bf16x2(qb.x, 0xB3A2u);
-                        a10 = e4m3x2_to_bf16x2(qa.y, 0x9180u);
-                        a12 = e4m3x2_to_bf16x2(qa.y, 0xB3A2u);
-                        a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
-                        a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
-                    }
-                    float sa = 1.0f, sb = 1.0f;
-                    if (MX) {
-                        const float2 rs = *reinterpret_cast<const float2 *>(xinv - cw * C::kXRows + C::kXInvFloats +
-                                                                            cw * kBN + ra);
-                        sa = rs.x;
-                        sb = rs.y;
-                    }
-#pragma unroll
-                    for (int j = 0; j < MT; ++j) {
-                        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        if (F16) {
-                            mma_f16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
-                            mma_f16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
-                        } else {
-                            mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
-                            mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
-                        }
-                        if (MX) {
-                            acc[rt][j][0] = fmaf(sa * f0[j], c[0], acc[rt][j][0]);
-                            acc[rt][j][1] = fmaf(sa * f1[j], c[1], acc[rt][j][1]);
-                            acc[rt][j][2] = fmaf(sb * f0[j], c[2], acc[rt][j][2]);
-                            acc[rt][j][3] = fmaf(sb * f1[j], c[3], acc[rt][j][3]);
-                        } else {
-                            acc[rt][j][0] = fmaf(f0[j], c[0], acc[rt][j][0]);
-                            acc[rt][j][1] = fmaf(f1[j], c[1], acc[rt][j][1]);
-                            acc[rt][j][2] = fmaf(f0[j], c[2], acc[rt][j][2]);
-                            acc[rt][j][3] = fmaf(f1[j], c[3], acc[rt][j][3]);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-
-            // Cross-warp reduction over the 4 column slices, in slice order,
-            // into red[n_local][m]; the two row halves write disjoint rows.
-            // acc[rt][j][q] is y[m = 8j + t + 4(q&1)][n_local = rbase + 16rt + 2g + (q>>1)].
-#pragma unroll 1
-            for (int p = 0; p < 4; ++p) {
-                if (cw == p) {
-#pragma unroll
-                    for (int rt = 0; rt < kRT; ++rt)
-#pragma unroll
-                        for (int j = 0; j < MT; ++j)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int nl = rbase + rt * 16 + 2 * g + (q >> 1);
-                                const int mc = 8 * j + t + 4 * (q & 1);
-                                float *ptr = red + nl * C::kRedStride + mc;
-                                *ptr = (p == 0) ? acc[rt][j][q] : *ptr + acc[rt][j][q];
-                            }
-                }
-                consumer_bar();
-            }
-            // Every write of s_fail for this tile precedes the phase barriers
-            // above, and a write for the next tile can only follow the last
-            // barrier below, so all consumer warps read the same value.
-            const bool stop = *reinterpret_cast<volatile int *>(&s_fail) != 0;
-            if (splits == 1) {
-                // bf16 store of this tile, consecutive threads on consecutive n
-                for (int e = threadIdx.x; e < mm * kBN; e += kConsumerWarps * 32) {
-                    const int mi = e / kBN;
-                    const int nl = e - mi * kBN;
-                    const int64_t o = n0 + nl < n ? out_at(mi, n0 + nl) : -1;
-                    if (o >= 0) {
-                        const float v = red[nl * C::kRedStride + mi];
-                        y[o] = __float2bfloat16_rn(ROW ? v * out_scale(n0 + nl) : v);
-                    }
-                }
-                consumer_bar();  // red is rewritten by the next tile
-            }
-            if (stop) break;
         }
     }
     if (splits == 1) return;
@@ -900,13 +686,14 @@ cudaError_t launch_moe_t(const DecodeArgs &a, const MoeArgs &g, cudaStream_t str
 
 template <int SC>
 cudaError_t launch_sc(const DecodeArgs &a, cudaStream_t stream) {
-    // f16 operands for m <= 8 (and always for MXFP8), bf16 for wider x
-    constexpr bool kMx = SC == kScaleMx;
+    // f16 operands (converter warp) for m <= 8, bf16 for wider x: beyond
+    // eight rows one converter warp cannot keep up (lm_head M = 16: 129 us
+    // with f16, 113 with bf16; MXFP8 M = 32: 62 us with f16, 46 with bf16)
     switch ((a.m + 7) / 8) {
         case 1: return launch_t<1, SC, true>(a, stream);
         case 2: return launch_t<2, SC, false>(a, stream);
-        case 3: return launch_t<3, SC, kMx>(a, stream);
-        case 4: return launch_t<4, SC, kMx>(a, stream);
+        case 3: return launch_t<3, SC, false>(a, stream);
+        case 4: return launch_t<4, SC, false>(a, stream);
         default: return cudaErrorInvalidValue;
     }
 }
