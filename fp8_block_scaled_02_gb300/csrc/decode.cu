@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                   const int32_t *__restrict__ ids, int topk, int num_experts) {
     constexpr bool MX = SC == kScaleMx;
     constexpr bool ROW = SC == kScaleRow;  // no per-K-block scale; scales[row * row_stride] at the end
+    // bf16 operands and no per-slice factor (no x rescale, no e8m0 groups)
+    constexpr bool kWholeBlock = !F16 && !MX;
     using C = Cfg<MT, MX, F16>;
     // factor applied to a finished fp32 sum of weight row nn before rounding
     auto out_scale = [&](int nn) -> float {
@@ -400,6 +402,16 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                 const uint8_t *cs = smem + s * C::kStageBytes;
                 const uint8_t *xbase = cs + C::kCodeBytes;
                 const float *xinv = aux + s * C::kXInvFloats;
+                // bf16 operands with block scales: one promotion factor for
+                // the K block's four slices, so the MMAs accumulate the whole
+                // block and the scale is applied once after it
+                float cb[MT][4];
+                if (kWholeBlock && !ROW) {
+#pragma unroll
+                    for (int j = 0; j < MT; ++j)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) cb[j][q] = 0.0f;
+                }
 #pragma unroll
                 for (int sl = 0; sl < 4; ++sl) {
                     const uint8_t *xs = xbase + (sl >> 1) * C::kXPanelBytes;
@@ -453,19 +465,33 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                     }
 #pragma unroll
                     for (int j = 0; j < MT; ++j) {
-                        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        if (F16) {
-                            mma_f16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
-                            mma_f16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                        if constexpr (kWholeBlock) {
+                            // one scale per row (or tensor): straight into the
+                            // running sums; block scales: into the block's sums
+                            float(&d)[4] = ROW ? acc[j] : cb[j];
+                            mma_bf16_16816(d, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                            mma_bf16_16816(d, a10, a11, a12, a13, bx[j][2], bx[j][3]);
                         } else {
-                            mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
-                            mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            if (F16) {
+                                mma_f16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                                mma_f16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                            } else {
+                                mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                                mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                            }
+                            acc[j][0] = fmaf(sa * f0[j], c[0], acc[j][0]);
+                            acc[j][1] = fmaf(sa * f1[j], c[1], acc[j][1]);
+                            acc[j][2] = fmaf(sb * f0[j], c[2], acc[j][2]);
+                            acc[j][3] = fmaf(sb * f1[j], c[3], acc[j][3]);
                         }
-                        acc[j][0] = fmaf(sa * f0[j], c[0], acc[j][0]);
-                        acc[j][1] = fmaf(sa * f1[j], c[1], acc[j][1]);
-                        acc[j][2] = fmaf(sb * f0[j], c[2], acc[j][2]);
-                        acc[j][3] = fmaf(sb * f1[j], c[3], acc[j][3]);
                     }
+                }
+                if (kWholeBlock && !ROW) {
+#pragma unroll
+                    for (int j = 0; j < MT; ++j)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[j][q] = fmaf(sblk, cb[j][q], acc[j][q]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
