@@ -13,23 +13,24 @@
 //  * A TMA warp streams each K block's 128x128 code tile (16 KB) and the
 //    matching x tile (2-D TMA, 128-byte swizzle) into a shared-memory ring.
 //  * For m <= 8 a converter warp rewrites each staged x tile in place from
-//    bf16 to f16 with an exact power-of-two rescale per (row of x, 32-column
-//    slice): the slice maximum is moved into [2^14, 2^15), so every value
-//    within 2^-31 of the slice maximum converts exactly and nothing
-//    overflows; the inverse power of two is kept for the promotion step.
-//    Wider x keeps bf16 operands and needs no converter.
+//    bf16 to f16 with an exact power-of-two rescale per (row of x, 128-column
+//    K block; per 32-column slice for MXFP8): the maximum is moved into
+//    [2^14, 2^15), so every value within 2^-31 of it converts exactly and
+//    nothing overflows; the inverse power of two is kept for the promotion
+//    step.  Wider x keeps bf16 operands and needs no converter.
 //  * Eight consumer warps each own one 16-row tile of the weight across the
 //    whole 128-wide K block (so row sums never cross warps) and run
 //    mma.sync m16n8k16 with the weights as the 16-row A operand and x as the
 //    8-wide B operand (m on the MMA's n axis, so m <= 32 needs at most four
 //    n8 tiles).  Codes convert with cvt.rn.f16x2.e4m3x2 (f16 form) or decode
-//    to bf16 with integer ops, both exact.  Each 32-column K slice's fp32
-//    MMA result starts from zero and is multiplied by (block scale x inverse
-//    x rescale) before it joins the accumulator, so the scale is applied once
-//    per 128-wide K block to an fp32 partial and is never folded into a
-//    rounded weight.  For MXFP8 a 32-column slice is exactly one e8m0 group,
-//    whose exponents each warp fetches for its rows one K block ahead.  With
-//    one scale per row (or per tensor) the K blocks accumulate unscaled and
+//    to bf16 with integer ops, both exact.  The MMAs of a 128-wide K block
+//    accumulate from zero and the block's fp32 partial is multiplied by
+//    (block scale x inverse x rescale) once before it joins the running sum,
+//    so the scale is applied once per K block to an fp32 partial and is never
+//    folded into a rounded weight.  For MXFP8 each 32-column slice is one
+//    e8m0 group, promoted on its own, whose exponents each warp fetches for
+//    its rows one K block ahead.  With one scale per row (or per tensor) the
+//    K blocks accumulate unscaled (bf16 operands: straight in the MMA) and
 //    the row's scale multiplies the fp32 sum once, just before the bf16
 //    rounding.
 //  * The logical k order inside each MMA is a fixed permutation of the
@@ -112,10 +113,6 @@ __device__ __forceinline__ float pow2_e8m0(uint32_t E) {
     return E ? __uint_as_float(E << 23) : __uint_as_float(0x00400000u);
 }
 
-__device__ __forceinline__ void consumer_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-}
-
 // Position of x row r in the per-slice inverse-scale table: rows 8j+t and
 // 8j+t+4 sit next to each other, so a consumer thread reads both with one
 // 64-bit load.
@@ -123,7 +120,11 @@ __device__ __forceinline__ int xinv_slot(int r) { return (r & ~7) | ((r & 3) << 
 
 // Rewrite one (x row r, 32-column slice sl) of a staged x tile from bf16 to
 // f16 in place with the exact power-of-two rescale described above.
-template <int kXPanelBytes, int kXRows>
+// kBlock: one power of two for the row's whole 128-column K block (the four
+// slices of a row sit in four adjacent lanes, whose maxima are combined with
+// two shuffles; every lane of the warp must take part), so that the consumers
+// can accumulate the K block before promoting it once.
+template <int kXPanelBytes, int kXRows, bool kBlock>
 __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r, int sl) {
     uint8_t *base = xs + (sl >> 1) * kXPanelBytes + r * 128;
     const int c0 = 4 * (sl & 1);
@@ -138,7 +139,11 @@ __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r,
         mx = max_u16x2(mx, v[i].z & 0x7FFF7FFFu);
         mx = max_u16x2(mx, v[i].w & 0x7FFF7FFFu);
     }
-    const uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);  // |max| as bf16 bits
+    uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);        // |max| as bf16 bits
+    if (kBlock) {
+        m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, 1));
+        m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, 2));
+    }
     int k = 0;                                          // scale 2^k
     if (m16 != 0) {
         const int field = static_cast<int>(m16 >> 7);
@@ -176,8 +181,10 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                   const int32_t *__restrict__ ids, int topk, int num_experts) {
     constexpr bool MX = SC == kScaleMx;
     constexpr bool ROW = SC == kScaleRow;  // no per-K-block scale; scales[row * row_stride] at the end
-    // bf16 operands and no per-slice factor (no x rescale, no e8m0 groups)
-    constexpr bool kWholeBlock = !F16 && !MX;
+    // no per-slice factor (e8m0 groups): the MMAs accumulate a whole K block
+    constexpr bool kWholeBlock = !MX;
+    // ... and with bf16 operands and one scale per row, all of K
+    constexpr bool kDirect = kWholeBlock && ROW && !F16;
     using C = Cfg<MT, MX, F16>;
     // factor applied to a finished fp32 sum of weight row nn before rounding
     auto out_scale = [&](int nn) -> float {
@@ -339,8 +346,10 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
             }
             uint8_t *xs = smem + s * C::kStageBytes + C::kCodeBytes;
             float *xinv = aux + s * C::kXInvFloats;
+            static_assert(!C::kConv || MX || 4 * C::kXRows == kConvLanes,
+                          "a per-block rescale needs one slice per lane");
             for (int u = clane; u < 4 * C::kXRows; u += kConvLanes)
-                convert_x_slice<C::kXPanelBytes, C::kXRows>(xs, xinv, u >> 2, u & 3);
+                convert_x_slice<C::kXPanelBytes, C::kXRows, !MX>(xs, xinv, u >> 2, u & 3);
             fence_proxy_async_smem();  // the TMA will overwrite these bytes later
             __syncwarp();
             if (lane == 0) mbar_arrive(&xready[s]);
@@ -402,11 +411,12 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                 const uint8_t *cs = smem + s * C::kStageBytes;
                 const uint8_t *xbase = cs + C::kCodeBytes;
                 const float *xinv = aux + s * C::kXInvFloats;
-                // bf16 operands with block scales: one promotion factor for
-                // the K block's four slices, so the MMAs accumulate the whole
-                // block and the scale is applied once after it
+                // Without MX groups the promotion factor (block scale, times the
+                // x rescale for f16 operands) is the same for the K block's four
+                // slices: the MMAs accumulate the whole block and it is promoted
+                // once.  bf16 with one scale per row needs no promotion at all.
                 float cb[MT][4];
-                if (kWholeBlock && !ROW) {
+                if (kWholeBlock && !kDirect) {
 #pragma unroll
                     for (int j = 0; j < MT; ++j)
 #pragma unroll
@@ -417,7 +427,6 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                     const uint8_t *xs = xbase + (sl >> 1) * C::kXPanelBytes;
                     const int xchunk = 4 * (sl & 1) + t;
                     uint32_t bx[MT][4];
-                    float f0[MT], f1[MT];
 #pragma unroll
                     for (int j = 0; j < MT; ++j) {
                         const int xr = 8 * j + xrow_base;
@@ -427,15 +436,6 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                         bx[j][1] = v.y;
                         bx[j][2] = v.z;
                         bx[j][3] = v.w;
-                        if (F16) {
-                            const float2 iv =
-                                *reinterpret_cast<const float2 *>(xinv + sl * C::kXRows + 8 * j + 2 * t);
-                            f0[j] = MX ? iv.x : sblk * iv.x;
-                            f1[j] = MX ? iv.y : sblk * iv.y;
-                        } else {
-                            f0[j] = MX ? 1.0f : sblk;
-                            f1[j] = MX ? 1.0f : sblk;
-                        }
                     }
                     const int cchunk = 2 * sl + (t >> 1);
                     const uint2 qa =
@@ -458,20 +458,29 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                         a11 = e4m3x2_to_bf16x2(qb.y, 0x9180u);
                         a13 = e4m3x2_to_bf16x2(qb.y, 0xB3A2u);
                     }
-                    float sa = 1.0f, sb = 1.0f;
-                    if (MX) {
-                        sa = pow2_e8m0((ewa >> (8 * sl)) & 0xFFu);
-                        sb = pow2_e8m0((ewb >> (8 * sl)) & 0xFFu);
-                    }
 #pragma unroll
                     for (int j = 0; j < MT; ++j) {
                         if constexpr (kWholeBlock) {
-                            // one scale per row (or tensor): straight into the
-                            // running sums; block scales: into the block's sums
-                            float(&d)[4] = ROW ? acc[j] : cb[j];
-                            mma_bf16_16816(d, a00, a01, a02, a03, bx[j][0], bx[j][1]);
-                            mma_bf16_16816(d, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                            float(&d)[4] = kDirect ? acc[j] : cb[j];
+                            if (F16) {
+                                mma_f16_16816(d, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                                mma_f16_16816(d, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                            } else {
+                                mma_bf16_16816(d, a00, a01, a02, a03, bx[j][0], bx[j][1]);
+                                mma_bf16_16816(d, a10, a11, a12, a13, bx[j][2], bx[j][3]);
+                            }
                         } else {
+                            // MX: the slice is one e8m0 group of each row, and
+                            // (f16) x carries its own per-slice rescale
+                            float f0 = 1.0f, f1 = 1.0f;
+                            if (F16) {
+                                const float2 iv =
+                                    *reinterpret_cast<const float2 *>(xinv + sl * C::kXRows + 8 * j + 2 * t);
+                                f0 = iv.x;
+                                f1 = iv.y;
+                            }
+                            const float sa = pow2_e8m0((ewa >> (8 * sl)) & 0xFFu);
+                            const float sb = pow2_e8m0((ewb >> (8 * sl)) & 0xFFu);
                             float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                             if (F16) {
                                 mma_f16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
@@ -480,18 +489,28 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                                 mma_bf16_16816(c, a00, a01, a02, a03, bx[j][0], bx[j][1]);
                                 mma_bf16_16816(c, a10, a11, a12, a13, bx[j][2], bx[j][3]);
                             }
-                            acc[j][0] = fmaf(sa * f0[j], c[0], acc[j][0]);
-                            acc[j][1] = fmaf(sa * f1[j], c[1], acc[j][1]);
-                            acc[j][2] = fmaf(sb * f0[j], c[2], acc[j][2]);
-                            acc[j][3] = fmaf(sb * f1[j], c[3], acc[j][3]);
+                            acc[j][0] = fmaf(sa * f0, c[0], acc[j][0]);
+                            acc[j][1] = fmaf(sa * f1, c[1], acc[j][1]);
+                            acc[j][2] = fmaf(sb * f0, c[2], acc[j][2]);
+                            acc[j][3] = fmaf(sb * f1, c[3], acc[j][3]);
                         }
                     }
                 }
-                if (kWholeBlock && !ROW) {
+                if (kWholeBlock && !kDirect) {
+                    // promotion factor of x rows 8j + t (f0) and 8j + t + 4 (f1)
 #pragma unroll
-                    for (int j = 0; j < MT; ++j)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) acc[j][q] = fmaf(sblk, cb[j][q], acc[j][q]);
+                    for (int j = 0; j < MT; ++j) {
+                        float f0 = sblk, f1 = sblk;
+                        if (F16) {
+                            const float2 iv = *reinterpret_cast<const float2 *>(xinv + 8 * j + 2 * t);
+                            f0 *= iv.x;
+                            f1 *= iv.y;
+                        }
+                        acc[j][0] = fmaf(f0, cb[j][0], acc[j][0]);
+                        acc[j][1] = fmaf(f1, cb[j][1], acc[j][1]);
+                        acc[j][2] = fmaf(f0, cb[j][2], acc[j][2]);
+                        acc[j][3] = fmaf(f1, cb[j][3], acc[j][3]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
