@@ -215,23 +215,49 @@ __global__ void __launch_bounds__(256) block_quantize_generic_kernel(
 constexpr int kMxThreads = 256;
 constexpr int kMxUnroll = 2;
 
+// Unsigned 32-bit division by a divisor fixed for the launch, by a multiply
+// high and shifts (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", 1994, the round-down-with-add form): for divisor
+// d >= 2, l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1 (< 2^32), and
+// q / d = (t + ((q - t) >> 1)) >> (l - 1) with t = umulhi(m, q), exact for
+// every 32-bit q.  The host computes m and l (div_magic below).
+struct DivMagic {
+    uint32_t m, l;
+};
+
+DivMagic div_magic(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+    return {static_cast<uint32_t>(m), l};
+}
+
+__device__ __forceinline__ uint32_t div_by(uint32_t q, DivMagic dm) {
+    const uint32_t t = __umulhi(dm.m, q);
+    return (t + ((q - t) >> 1)) >> (dm.l - 1);
+}
+
+// One thread per 16-byte chunk (8 elements; four chunks = one 32-element
+// group, reduced with two shuffles).  The flat chunk index fits 32 bits
+// (the launcher sends larger tensors to the generic kernel).
 __global__ void __launch_bounds__(kMxThreads) mx_quantize_kernel(const __nv_bfloat16 *__restrict__ w,
                                                                  uint8_t *__restrict__ codes,
                                                                  uint8_t *__restrict__ e8m0,
                                                                  int64_t n, int64_t k,
-                                                                 int64_t groups) {
-    const int64_t chunks_per_row = groups * 4;
-    const int64_t total = n * chunks_per_row;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * (kMxThreads * kMxUnroll) + threadIdx.x;
+                                                                 int64_t groups, DivMagic per_row) {
+    const uint32_t chunks_per_row = static_cast<uint32_t>(groups * 4);
+    const uint32_t total = static_cast<uint32_t>(n * chunks_per_row);
+    const uint32_t base = blockIdx.x * (kMxThreads * kMxUnroll) + threadIdx.x;
     uint4 v[kMxUnroll];
     int64_t row[kMxUnroll], col[kMxUnroll];
     bool ok[kMxUnroll];
 #pragma unroll
     for (int u = 0; u < kMxUnroll; ++u) {
-        const int64_t q = base + u * kMxThreads;
+        const uint32_t q = base + u * kMxThreads;
         const bool in = q < total;
-        row[u] = in ? q / chunks_per_row : 0;
-        col[u] = in ? (q - row[u] * chunks_per_row) * 8 : 0;
+        const uint32_t r = in ? div_by(q, per_row) : 0u;
+        row[u] = r;
+        col[u] = in ? static_cast<int64_t>(q - r * chunks_per_row) * 8 : 0;
         ok[u] = in && col[u] < k;
         v[u] = ok[u] ? ld_nc_v4(w + row[u] * k + col[u]) : make_uint4(0, 0, 0, 0);
     }
@@ -460,12 +486,13 @@ cudaError_t launch_block_quantize(const void *w, int64_t n, int64_t k, uint8_t *
 cudaError_t launch_mx_quantize(const void *w, int64_t n, int64_t k, uint8_t *codes,
                                uint8_t *e8m0, bool vector_ok, cudaStream_t stream) {
     const int64_t groups = (k + 31) / 32;
-    if (vector_ok) {
-        const int64_t total = n * groups * 4;
-        const int64_t per_block = kMxThreads * kMxUnroll;
+    const int64_t per_block = kMxThreads * kMxUnroll;
+    const int64_t total = n * groups * 4;
+    if (vector_ok && total + per_block < (int64_t(1) << 32)) {
         const unsigned blocks = static_cast<unsigned>((total + per_block - 1) / per_block);
         mx_quantize_kernel<<<blocks, kMxThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w),
-                                                               codes, e8m0, n, k, groups);
+                                                               codes, e8m0, n, k, groups,
+                                                               div_magic(static_cast<uint32_t>(groups * 4)));
     } else {
         const int64_t total = n * groups;
         const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
