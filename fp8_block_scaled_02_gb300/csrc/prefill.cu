@@ -9,15 +9,18 @@
 //    exactly to bf16 pairs in registers and store them into a
 //    double-buffered shared-memory A slot in the 128-byte-swizzled K-major
 //    layout the tensor core reads.  The decoded weight never reaches HBM.
-//    Each decoded 128 x 128 block feeds two MMA groups (two 128-row halves
-//    of x), so the decode work per flop is half that of a 128 x 128 tile.
-//  * x is the B operand: one producer thread brings each (K block, half)
-//    [128 rows x 128 K] bf16 tile in with 2-D TMA (128-byte swizzle, two
-//    64-column panels) into a 4-stage shared-memory ring.
+//    Each decoded 128 x 128 block feeds both 128-row halves of x, so the
+//    decode work per flop is half that of a 128 x 128 tile.
+//  * x is the B operand: one producer thread brings each unit's x rows
+//    (block scales: one (K block, half), 128 rows; one scale per row: one K
+//    block, all 256 rows) with 2-D TMA (128-byte swizzle, two 64-column
+//    panels) into a 128 KB shared-memory ring.
 //  * One thread issues tcgen05.mma.kind::f16 (bf16 x bf16 -> fp32, M=128,
-//    N=128, K=16; 8 per K block and half), both operands from shared memory,
-//    and one tcgen05.commit per (K block, half) into a ring of "MMA done"
-//    barriers that frees x stages, A slots and accumulators alike.
+//    K=16, 8 per unit, both operands from shared memory; N = 128 per half
+//    with block scales, N = 256 with one scale per row, which reads each
+//    decoded A fragment once for both halves) and one tcgen05.commit per
+//    unit into a ring of "MMA done" barriers that frees x stages, A slots and
+//    accumulators alike.
 //  * Block scales: each (K block, half) accumulates from zero into that
 //    half's 128-column TMEM partial D_h; eight epilogue warps (one per TMEM
 //    lane quarter and half) read it with tcgen05.ld, multiply it by the
@@ -49,12 +52,25 @@ constexpr int kHalfX = 128;       // x rows per MMA group (= MMA N)
 constexpr int kTileX = 2 * kHalfX;  // x rows per CTA
 constexpr int kKB = 128;          // K per block
 constexpr int kPanel = 128 * 128;           // one 64-column bf16 panel of 128 rows, 16 KB
-constexpr int kXStages = 4;                 // x ring: one (K block, half) per stage
-constexpr int kXStage = 2 * kPanel;         // 32 KB
+constexpr int kXBytes = 4 * 2 * kPanel;     // x ring: 128 KB
+
+// The x ring and the MMA shape.  Block scales: one unit = (K block, half of
+// x), N = 128, into that half's partial D_h, so one half's promotion overlaps
+// the other half's MMAs.  One scale per row: nothing to promote, one unit =
+// K block, N = 256 straight into T = [T_0 | T_1]: each decoded A fragment is
+// read from shared memory once for both halves.
+template <bool ROW>
+struct PCfg {
+    static constexpr int kN = ROW ? kTileX : kHalfX;      // MMA N = x rows per unit
+    static constexpr int kUnitsPerKb = ROW ? 1 : 2;
+    static constexpr int kXPanel = kN * 128;              // one 64-column panel of the unit's x rows
+    static constexpr int kXStage = 2 * kXPanel;           // 32 KB / 64 KB
+    static constexpr int kXStages = kXBytes / kXStage;    // 4 / 2
+};
 constexpr int kASlots = 2;                  // decoded weight blocks in flight
 constexpr int kASlot = 2 * kPanel;          // 32 KB
-constexpr int kRing = 8;  // MMA-completion barriers, one per (K block, half); >= every look-back
-static_assert(kXStages <= kRing && 2 * kASlots <= kRing, "a wait must never reach back a full ring");
+constexpr int kRing = 8;  // MMA-completion barriers, one per unit; >= every look-back
+static_assert(4 <= kRing && 2 * kASlots <= kRing, "a wait must never reach back a full ring");
 constexpr int kTmemCols = 512;
 constexpr int kColT = 0;                  // running totals T_0, T_1: [0, 128), [128, 256)
 constexpr int kColD = 256;                // per-K-block partials D_0, D_1: [256, 384), [384, 512)
@@ -67,14 +83,17 @@ constexpr int kNumDec = 8;
 constexpr int kWarpEpi0 = kWarpDec0 + kNumDec;  // 10..17 epilogue: TMEM lane quarter warp % 4, half (warp - 10) / 4
 constexpr int kNumEpi = 8;
 constexpr int kThreads = (kWarpEpi0 + kNumEpi) * 32;
-constexpr int kSmemBytes = 1024 + kXStages * kXStage + kASlots * kASlot + 256;
+constexpr int kSmemBytes = 1024 + kXBytes + kASlots * kASlot + 256;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kHalfX >> 3) << 17) |
-                            (static_cast<uint32_t>(kTileW >> 4) << 24);
+template <int N>
+__host__ __device__ constexpr uint32_t idesc_f16() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(kTileW >> 4) << 24);
+}
 
 __device__ __forceinline__ uint4 ld_codes16(const uint8_t *p) {
     uint4 v;
@@ -87,12 +106,13 @@ __device__ __forceinline__ uint4 ld_codes16(const uint8_t *p) {
 __device__ __forceinline__ void fail(uint32_t bit) { atomicOr(&g_prefill_err, bit); }
 
 // Both operands from shared memory.
+template <uint32_t kIdesc>
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %3, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(kIdesc)
+        "l"(a_desc), "l"(b_desc), "r"(accumulate), "n"(kIdesc)
         : "memory");
 }
 
@@ -116,12 +136,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *xring = smem;                              // [kXStages][2 panels][128 rows][128 B]
-    uint8_t *aring = smem + kXStages * kXStage;         // [kASlots][2 panels][128 rows][128 B]
+    using P = PCfg<ROW>;
+    constexpr int kXStages = P::kXStages, kXStage = P::kXStage, kXPanel = P::kXPanel;
+    constexpr int kPerKb = P::kUnitsPerKb;
+    uint8_t *xring = smem;                              // [kXStages][2 panels][N rows][128 B]
+    uint8_t *aring = smem + kXBytes;                    // [kASlots][2 panels][128 rows][128 B]
     uint64_t *bars = reinterpret_cast<uint64_t *>(aring + kASlots * kASlot);
-    // done[u % kRing] completes when the MMAs of unit u = 2 * kb + half have
-    // finished (one tcgen05.commit per unit); the x producer, the decoders
-    // and the epilogue all wait on it, each before its slot could be reused
+    // done[u % kRing] completes when the MMAs of unit u have finished (one
+    // tcgen05.commit per unit; u = 2 kb + half with block scales, u = kb
+    // with one scale per row); the x producer, the decoders and the
+    // epilogue all wait on it, each before its slot could be reused
     uint64_t *x_full = bars;                 // [kXStages]
     uint64_t *done = x_full + kXStages;      // [kRing]
     uint64_t *a_full = done + kRing;         // [kASlots]
@@ -133,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kTileW;
     const int m0 = blockIdx.y * kTileX;
-    const int units = 2 * kblocks;
+    const int units = kPerKb * kblocks;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kXStages; ++i) mbar_init(&x_full[i], 1);
@@ -162,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         int issued = 0;  // units whose MMAs were committed
         if (lane == 0) {
             for (int u = 0; u < units; ++u) {
-                const int kb = u >> 1, h = u & 1, xs = u % kXStages, as = kb % kASlots;
+                const int kb = u / kPerKb, h = u % kPerKb, xs = u % kXStages, as = kb % kASlots;
                 bool ok = mbar_wait_bounded(&x_full[xs], (u / kXStages) & 1) &&
                           (h == 1 || mbar_wait_bounded(&a_full[as], (kb / kASlots) & 1)) &&
                           (ROW || kb == 0 || mbar_wait_bounded(&d_empty[h], (kb - 1) & 1));
@@ -176,11 +200,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 // bytes (2 in address/16 units) apart within a 64-column panel
                 const uint64_t adesc = sw128_desc(smem_u32(aring + as * kASlot));
                 const uint64_t bdesc = sw128_desc(smem_u32(xring + xs * kXStage));
-                const uint32_t d_tmem = tmem + (ROW ? kColT : kColD) + h * 128;
+                const uint32_t d_tmem = tmem + (ROW ? kColT : kColD + h * 128);
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>((kk >> 2) * (kPanel >> 4) + (kk & 3) * 2);
-                    tc_mma_ss(d_tmem, adesc + off, bdesc + off, (kk > 0 || (ROW && kb > 0)) ? 1u : 0u);
+                    const uint64_t aoff = static_cast<uint64_t>((kk >> 2) * (kPanel >> 4) + (kk & 3) * 2);
+                    const uint64_t boff = static_cast<uint64_t>((kk >> 2) * (kXPanel >> 4) + (kk & 3) * 2);
+                    tc_mma_ss<idesc_f16<P::kN>()>(d_tmem, adesc + aoff, bdesc + boff,
+                                                  (kk > 0 || (ROW && kb > 0)) ? 1u : 0u);
                 }
                 tc_commit(&done[u % kRing]);
                 issued = u + 1;
@@ -206,10 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 }
                 if (*reinterpret_cast<volatile int *>(s_fail)) break;
                 uint8_t *st = xring + xs * kXStage;
-                const int kx = (u >> 1) * kKB, mx = m0 + (u & 1) * kHalfX;
+                const int kx = (u / kPerKb) * kKB, mx = m0 + (u % kPerKb) * kHalfX;
                 mbar_arrive_expect_tx(&x_full[xs], kXStage);
                 tma_load_2d(st, &tm_x, &x_full[xs], kx, mx);
-                tma_load_2d(st + kPanel, &tm_x, &x_full[xs], kx + 64, mx);
+                tma_load_2d(st + kXPanel, &tm_x, &x_full[xs], kx + 64, mx);
                 issued = u + 1;
             }
             // never leave with copies in flight: wait for the last stages issued
@@ -241,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const int as = kb % kASlots;
             load4(kb + 2, c2);  // in flight while this block is converted
             // slot `as` was last read by the MMAs of K block kb - kASlots,
-            // whose last unit is 2 (kb - kASlots) + 1
-            const int prev = 2 * (kb - kASlots) + 1;
+            // whose last unit is kPerKb (kb - kASlots + 1) - 1
+            const int prev = kPerKb * (kb - kASlots + 1) - 1;
             bool ok = kb < kASlots || mbar_wait_bounded(&done[prev % kRing], (prev / kRing) & 1);
             if (!__all_sync(0xffffffffu, ok) || *reinterpret_cast<volatile int *>(s_fail)) {
                 if (lane == 0) fail(ERRBIT_EMPTY_WAIT);
@@ -394,7 +420,10 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
     }
     CUtensorMap tm_x;
     const uint64_t k = static_cast<uint64_t>(a.k), m = static_cast<uint64_t>(a.m);
-    if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64, kHalfX,
+    // one TMA box = the x rows of one MMA unit (a half with block scales, all
+    // 256 with one scale per row)
+    const uint32_t box_rows = row ? static_cast<uint32_t>(PCfg<true>::kN) : static_cast<uint32_t>(PCfg<false>::kN);
+    if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64, box_rows,
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
