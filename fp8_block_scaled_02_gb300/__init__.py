@@ -84,12 +84,13 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_strerror.argtypes = [i32]
         L.fp8bs_strerror.restype = ctypes.c_char_p
         L.fp8bs_check_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+        L.fp8bs_debug_wait_expiry.argtypes = [p]
         L.fp8bs_version.argtypes = []
         for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                   "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
                   "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention",
-                  "fp8bs_select_path", "fp8bs_check_device_error",
+                  "fp8bs_select_path", "fp8bs_check_device_error", "fp8bs_debug_wait_expiry",
                   "fp8bs_version"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -321,6 +322,12 @@ def w8a8_linear(x, wq, sw, y=None, xq=None, sx=None, path: int = PATH_AUTO, stre
 def select_path(m: int, n: int, k: int, x_ptr: int = 0, codes_ptr: int = 0, mx: bool = False) -> int:
     """Path the AUTO dispatch would take (host-only; pointers only matter for alignment)."""
     return lib().fp8bs_select_path(m, n, k, ctypes.c_void_p(x_ptr), ctypes.c_void_p(codes_ptr), int(mx))
+
+
+def debug_wait_expiry(stream=None) -> None:
+    """Launch the library's wait-expiry probe (fp8bs_debug_wait_expiry): one
+    thread gives up a bounded wait after about 2 s and sets the error word."""
+    _check(lib().fp8bs_debug_wait_expiry(_stream(stream)), "fp8bs_debug_wait_expiry")
 
 
 def check_device_error(stream=None) -> int:

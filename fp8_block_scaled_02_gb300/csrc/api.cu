@@ -296,6 +296,10 @@ int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16, const
     return select_path(m, k, x_bf16, codes, mx != 0);
 }
 
+int fp8bs_debug_wait_expiry(void *stream) {
+    return cuda_status(launch_wait_expiry_probe(static_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_check_device_error(void *stream, uint32_t *word_out) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
     const uint32_t w = take_decode_error() | take_prefill_error() | take_w8a8_error() | take_kv_error();

@@ -764,6 +764,21 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
     }
 }
 
+// One thread waits, with the same bounded wait every pipelined kernel uses,
+// on an mbarrier whose phase nothing completes; when the bound expires it
+// records ERRBIT_FULL_WAIT in the decode error word and returns.
+__global__ void wait_expiry_kernel() {
+    __shared__ uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    if (!mbar_wait_bounded(&bar, 0)) atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
+}
+
+cudaError_t launch_wait_expiry_probe(cudaStream_t stream) {
+    wait_expiry_kernel<<<1, 1, 0, stream>>>();
+    return cudaGetLastError();
+}
+
 uint32_t take_decode_error() {
     uint32_t v = 0;
     if (cudaMemcpyFromSymbol(&v, g_decode_err, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;

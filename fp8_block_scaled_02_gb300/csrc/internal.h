@@ -52,6 +52,9 @@ struct MoeArgs {
 };
 cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_t stream);
 uint32_t take_decode_error();  // reads and clears the decode kernels' error word
+// one thread waits on a barrier nothing completes until the bounded wait
+// gives up (about 2 s), then sets the decode error word
+cudaError_t launch_wait_expiry_probe(cudaStream_t stream);
 
 // generic.cu -- plain-load kernels for any shape / alignment.
 cudaError_t launch_generic_gemv(const DecodeArgs &a, cudaStream_t stream);

@@ -353,6 +353,20 @@ const char *fp8bs_strerror(int status);
  */
 int fp8bs_check_device_error(void *stream, uint32_t *word_out);
 
+/*
+ * Debug: exercise the give-up path of the bounded waits without a fault.
+ * Launches one thread on `stream` that waits, with the same bounded wait the
+ * pipelined kernels use, on a barrier nothing completes; after the bound
+ * (about 2 s) it sets the FULL_WAIT bit (1) of the device error word and
+ * returns, leaving the context usable.  Reads and writes no caller memory.
+ * Returns FP8BS_OK once launched (FP8BS_ERR_CUDA if the launch failed);
+ * fp8bs_check_device_error then reports FP8BS_ERR_DEVICE.
+ *
+ * Defined by: no passage of the source pages; this is the library's own
+ * test hook for its failure detection.
+ */
+int fp8bs_debug_wait_expiry(void *stream);
+
 /* ABI version (major * 100 + minor). */
 int fp8bs_version(void);
 

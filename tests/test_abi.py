@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
                  "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention", "fp8bs_select_path", "fp8bs_strerror",
-                 "fp8bs_check_device_error", "fp8bs_version"):
+                 "fp8bs_check_device_error", "fp8bs_debug_wait_expiry", "fp8bs_version"):
         assert want in names, names
 
 
