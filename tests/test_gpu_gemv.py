@@ -159,7 +159,7 @@ def _row_blocks(n, count, seed):
 
 def test_lm_head_full_size(pkg):
     w = inputs.lm_head_weight(2, device=DEV)
-    sampled_block_case(pkg, w, [1, 4, 8, 16], _row_blocks(w.shape[0], 4, 1))
+    sampled_block_case(pkg, w, [1, 4, 8, 16, 24, 32], _row_blocks(w.shape[0], 4, 1))
 
 
 @pytest.mark.parametrize("j", range(4))
@@ -199,7 +199,7 @@ def test_mx_full_size(pkg):
     ridx = torch.from_numpy(rows).to(DEV)
     codes[ridx] = to_dev_bits(oc)
     e8m0[ridx] = to_dev_bits(oe)
-    for m in (1, 8, 16):
+    for m in (1, 8, 16, 24, 32):
         x = inputs.activations(m, k, 40 + m, device=DEV)
         y = pkg.mx_gemv(x, codes, e8m0)
         torch.cuda.synchronize()
