@@ -85,13 +85,14 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_strerror.restype = ctypes.c_char_p
         L.fp8bs_check_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
         L.fp8bs_debug_wait_expiry.argtypes = [p]
+        L.fp8bs_debug_encode_f32.argtypes = [ctypes.c_uint32, i64, p, p]
         L.fp8bs_version.argtypes = []
         for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                   "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
                   "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention",
                   "fp8bs_select_path", "fp8bs_check_device_error", "fp8bs_debug_wait_expiry",
-                  "fp8bs_version"):
+                  "fp8bs_debug_encode_f32", "fp8bs_version"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
         return L
@@ -328,6 +329,20 @@ def debug_wait_expiry(stream=None) -> None:
     """Launch the library's wait-expiry probe (fp8bs_debug_wait_expiry): one
     thread gives up a bounded wait after about 2 s and sets the error word."""
     _check(lib().fp8bs_debug_wait_expiry(_stream(stream)), "fp8bs_debug_wait_expiry")
+
+
+def debug_encode_f32(first_bits: int, count: int, out=None, stream=None):
+    """The quantizers' e4m3 encode step on the binary32 bit patterns
+    first_bits .. first_bits + count - 1 (fp8bs_debug_encode_f32); returns
+    uint8 codes on the device."""
+    import torch
+    if out is None:
+        out = torch.empty(count, dtype=torch.uint8, device="cuda")
+    if out.numel() < count:
+        raise ValueError("out holds fewer than count bytes")
+    _check(lib().fp8bs_debug_encode_f32(first_bits, count, _dev(out, torch.uint8, "out"), _stream(stream)),
+           "fp8bs_debug_encode_f32")
+    return out
 
 
 def check_device_error(stream=None) -> int:

@@ -85,7 +85,7 @@ int run_w8a8_decode_chunks(const W8A8Args &a, cudaStream_t st) {
 
 extern "C" {
 
-int fp8bs_version(void) { return 104; }
+int fp8bs_version(void) { return 105; }
 
 const char *fp8bs_strerror(int status) {
     switch (status) {
@@ -298,6 +298,14 @@ int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16, const
 
 int fp8bs_debug_wait_expiry(void *stream) {
     return cuda_status(launch_wait_expiry_probe(static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_debug_encode_f32(uint32_t first_bits, int64_t count, uint8_t *codes_u8, void *stream) {
+    if (!codes_u8) return FP8BS_ERR_NULL;
+    if (count <= 0 || count % 4 != 0 || static_cast<uint64_t>(first_bits) + static_cast<uint64_t>(count) > (1ull << 32))
+        return FP8BS_ERR_SHAPE;
+    if (!aligned(codes_u8, 4)) return FP8BS_ERR_ALIGN;
+    return cuda_status(launch_encode_probe(first_bits, count, codes_u8, static_cast<cudaStream_t>(stream)));
 }
 
 int fp8bs_check_device_error(void *stream, uint32_t *word_out) {

@@ -55,6 +55,7 @@ uint32_t take_decode_error();  // reads and clears the decode kernels' error wor
 // one thread waits on a barrier nothing completes until the bounded wait
 // gives up (about 2 s), then sets the decode error word
 cudaError_t launch_wait_expiry_probe(cudaStream_t stream);
+cudaError_t launch_encode_probe(uint32_t first, int64_t count, uint8_t *codes, cudaStream_t stream);
 
 // generic.cu -- plain-load kernels for any shape / alignment.
 cudaError_t launch_generic_gemv(const DecodeArgs &a, cudaStream_t stream);

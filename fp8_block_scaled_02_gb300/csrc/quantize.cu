@@ -551,4 +551,30 @@ cudaError_t launch_act_quantize(const void *x, int64_t m, int64_t k, uint8_t *co
     return cudaGetLastError();
 }
 
+namespace {
+
+// Test hook: the quantizers' e4m3 encode step (f32x2_to_e4m3x2) over
+// consecutive binary32 bit patterns, four per thread and one 32-bit store.
+__global__ void encode_probe_kernel(uint32_t first, int64_t quads, uint32_t *__restrict__ out) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < quads; i += stride) {
+        const uint32_t b = first + static_cast<uint32_t>(4 * i);
+        const uint32_t lo = f32x2_to_e4m3x2(__uint_as_float(b), __uint_as_float(b + 1u));
+        const uint32_t hi = f32x2_to_e4m3x2(__uint_as_float(b + 2u), __uint_as_float(b + 3u));
+        out[i] = lo | (hi << 16);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_encode_probe(uint32_t first, int64_t count, uint8_t *codes, cudaStream_t stream) {
+    const int64_t quads = count / 4;
+    int64_t blocks = (quads + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+    if (blocks > cap) blocks = cap;
+    encode_probe_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(first, quads,
+                                                                          reinterpret_cast<uint32_t *>(codes));
+    return cudaGetLastError();
+}
+
 }  // namespace fp8bs

@@ -367,6 +367,28 @@ int fp8bs_check_device_error(void *stream, uint32_t *word_out);
  */
 int fp8bs_debug_wait_expiry(void *stream);
 
+/*
+ * Debug: the e4m3 encode step that every quantizer here applies to its
+ * fp32 quotients (round to nearest even, saturating to +-448, the sign kept
+ * on zero results), run on consecutive binary32 bit patterns:
+ * codes_u8[i] = e4m3(the float whose bits are first_bits + i), 0 <= i < count.
+ *
+ *   first_bits  first binary32 bit pattern
+ *   count       > 0, a multiple of 4, first_bits + count <= 2^32
+ *   codes_u8    device, count bytes, 4-byte aligned (written)
+ *
+ * Codes for NaN or Inf patterns are unspecified.  Asynchronous on `stream`.
+ * Returns FP8BS_ERR_NULL, FP8BS_ERR_SHAPE or FP8BS_ERR_ALIGN before any
+ * launch, FP8BS_ERR_CUDA if the launch failed.
+ *
+ * Defined by: the rounding of the block quantizer's codes (Atlas
+ * spark_model/weight_map/quantize_fp8_bs.rs, one e4m3 byte per weight;
+ * FreeToken PR #636, How it works: fp8 with a 128-block scale).  A test
+ * hook so that the encode step can be compared with an independent encoder
+ * over every finite binary32 value.
+ */
+int fp8bs_debug_encode_f32(uint32_t first_bits, int64_t count, uint8_t *codes_u8, void *stream);
+
 /* ABI version (major * 100 + minor). */
 int fp8bs_version(void);
 

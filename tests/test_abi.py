@@ -36,7 +36,8 @@ def test_header_declares_the_entry_points():
                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
                  "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention", "fp8bs_select_path", "fp8bs_strerror",
-                 "fp8bs_check_device_error", "fp8bs_debug_wait_expiry", "fp8bs_version"):
+                 "fp8bs_check_device_error", "fp8bs_debug_wait_expiry", "fp8bs_debug_encode_f32",
+                 "fp8bs_version"):
         assert want in names, names
 
 
@@ -50,7 +51,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strerror(L):
-    assert L.fp8bs_version() == 104
+    assert L.fp8bs_version() == 105
     import fp8_block_scaled_02_gb300 as pkg
     for st in range(-7, 1):
         assert pkg.strerror(st) and pkg.strerror(st) != "unknown status"
@@ -167,6 +168,16 @@ def test_kv_validation(L):
     assert call(b=0, q=None) == 0
     assert call(q=None) == -1
     assert call(q=P(0x10008)) == -4
+
+
+def test_encode_probe_validation(L):
+    c = P(0x10000)
+    f = L.fp8bs_debug_encode_f32
+    assert f(0, 16, None, None) == -1
+    assert f(0, 0, c, None) == -2
+    assert f(0, 6, c, None) == -2                     # not a multiple of 4
+    assert f(0xFFFFFFF0, 32, c, None) == -2           # runs past 2^32
+    assert f(0, 16, P(0x10002), None) == -4           # codes not 4-byte aligned
 
 
 def test_select_path(L):

@@ -198,5 +198,36 @@ def test_full_size_mx_sampled_rows(pkg):
     assert np.array_equal(codes[torch.from_numpy(rows).to(DEV)].cpu().numpy(), oc)
 
 
+def test_encode_step_every_finite_f32_matches_oracle(pkg):
+    """Exhaustive: the e4m3 encode step every quantizer applies to its fp32
+    quotients, run on the GPU (fp8bs_debug_encode_f32, 2^28 patterns per
+    launch), against the oracle's brute-force nearest-code encoder on every
+    finite binary32 value."""
+    from f32_sweep import ALL, FINITE, SLICE, f32_slice, sweep
+    chunk = 1 << 28
+    buf = torch.empty(chunk, dtype=torch.uint8, device=DEV)
+    bad = checked = 0
+    examples = []
+    for c0 in range(0, ALL, chunk):
+        pkg.debug_encode_f32(c0, chunk, out=buf)
+        host = buf.cpu().numpy()
+
+        def check(base, host=host, c0=c0):
+            f, fin = f32_slice(base)
+            got = host[base - c0:base - c0 + SLICE][fin]
+            ref = oracle.e4m3_encode_f32(f[fin])
+            wrong = np.nonzero(got != ref)[0]
+            if wrong.size:
+                i = wrong[0]
+                examples.append((hex(int(f[fin][i].view(np.uint32))), int(got[i]), int(ref[i])))
+            return int(wrong.size), int(ref.size)
+        b, n = sweep(check, range(c0, c0 + chunk, SLICE))
+        bad += b
+        checked += n
+    assert checked == FINITE
+    assert bad == 0, examples[:5]
+    assert pkg.check_device_error() == 0
+
+
 def test_no_device_error(pkg):
     assert pkg.check_device_error() == 0

@@ -168,3 +168,33 @@ def test_every_decoded_code_reencodes_to_itself(code):
     if math.isnan(v):
         return
     assert oracle.e4m3_encode(v) == code
+
+
+def test_encode_every_finite_f32_vs_torch():
+    """Exhaustive: the oracle's brute-force encoder against torch's
+    float8_e4m3fn cast on every finite binary32 value below 464 in magnitude
+    (above that torch gives NaN instead of saturating), and saturation to
+    +-448 with the sign kept for every finite value at or above it."""
+    import torch
+    from f32_sweep import FINITE, f32_slice, sweep
+
+    def check(base):
+        f, fin = f32_slice(base)
+        v = f[fin]
+        ours = oracle.e4m3_encode_f32(v)
+        small = np.abs(v) < 464.0
+        ref = torch.from_numpy(v[small]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        bad = int(np.count_nonzero(ours[small] != ref))
+        big = ~small
+        bad += int(np.count_nonzero((ours[big] & 0x7F) != 0x7E))
+        bad += int(np.count_nonzero((ours[big] >> 7) != np.signbit(v[big])))
+        return bad, v.size
+
+    threads = torch.get_num_threads()
+    torch.set_num_threads(1)
+    try:
+        bad, checked = sweep(check)
+    finally:
+        torch.set_num_threads(threads)
+    assert checked == FINITE
+    assert bad == 0
