@@ -275,6 +275,36 @@ __global__ void __launch_bounds__(kMxThreads) mx_quantize_kernel(const __nv_bflo
     }
 }
 
+// k a multiple of 32: chunk q of the flat [n, k] array starts at element 8q
+// and lies in 32-element group q / 4 of the flat [n, k / 32] exponent array,
+// so no row or column is formed (the per-chunk division and 64-bit index
+// arithmetic of the kernel above made it issue-bound).  The flat chunk index
+// fits 32 bits (the launcher checks).
+constexpr int kMxFlatUnroll = 4;
+__global__ void __launch_bounds__(kMxThreads) mx_quantize_flat_kernel(const __nv_bfloat16 *__restrict__ w,
+                                                                      uint8_t *__restrict__ codes,
+                                                                      uint8_t *__restrict__ e8m0, uint32_t total) {
+    const uint32_t base = blockIdx.x * (kMxThreads * kMxFlatUnroll) + threadIdx.x;
+    uint4 v[kMxFlatUnroll];
+#pragma unroll
+    for (int u = 0; u < kMxFlatUnroll; ++u) {
+        const uint32_t q = base + u * kMxThreads;
+        v[u] = q < total ? ld_nc_v4(w + 8 * static_cast<uint64_t>(q)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kMxFlatUnroll; ++u) {
+        const uint32_t q = base + u * kMxThreads;
+        float amax = absmax8(v[u], 0.0f);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int E = mx_exponent(amax);
+        if (q < total) {
+            *reinterpret_cast<uint2 *>(codes + 8 * static_cast<uint64_t>(q)) = encode8_mul(v[u], mx_inv_scale(E));
+            if ((threadIdx.x & 3) == 0) e8m0[q >> 2] = static_cast<uint8_t>(E);
+        }
+    }
+}
+
 // ------------------------------------------------------------ MX, generic
 __global__ void __launch_bounds__(256) mx_quantize_generic_kernel(
     const __nv_bfloat16 *__restrict__ w, uint8_t *__restrict__ codes, uint8_t *__restrict__ e8m0,
@@ -488,7 +518,12 @@ cudaError_t launch_mx_quantize(const void *w, int64_t n, int64_t k, uint8_t *cod
     const int64_t groups = (k + 31) / 32;
     const int64_t per_block = kMxThreads * kMxUnroll;
     const int64_t total = n * groups * 4;
-    if (vector_ok && total + per_block < (int64_t(1) << 32)) {
+    const int64_t flat_block = kMxThreads * kMxFlatUnroll;
+    if (vector_ok && k % 32 == 0 && total + flat_block < (int64_t(1) << 32)) {
+        const unsigned blocks = static_cast<unsigned>((total + flat_block - 1) / flat_block);
+        mx_quantize_flat_kernel<<<blocks, kMxThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w), codes,
+                                                                    e8m0, static_cast<uint32_t>(total));
+    } else if (vector_ok && total + per_block < (int64_t(1) << 32)) {
         const unsigned blocks = static_cast<unsigned>((total + per_block - 1) / per_block);
         mx_quantize_kernel<<<blocks, kMxThreads, 0, stream>>>(static_cast<const __nv_bfloat16 *>(w),
                                                                codes, e8m0, n, k, groups,
