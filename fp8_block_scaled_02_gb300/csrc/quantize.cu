@@ -50,22 +50,34 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// Encode 8 bf16 values divided by s (reciprocal y = RN(1/s)) into 8 e4m3
-// bytes, each quotient by Markstein's correction (see above).
-__device__ __forceinline__ float div_mk(float w, float s, float y) {
-    const float q0 = w * y;
-    const float r = __fmaf_rn(-s, q0, w);
-    return copysignf(__fmaf_rn(r, y, q0), w);
+// Two bf16 values (as fp32) divided by s with Markstein's correction (see
+// above), q0 = RN(w y), r = w - s q0, q = RN(q0 + r y), the sign copied from
+// w, on both values at once with packed fp32x2 fma (each lane rounds exactly
+// like the scalar fma; q0 = fma(w, y, -0) = RN(w y)): ns2 = (-s, -s),
+// y2 = (y, y), y = RN(1/s).  Returns the two e4m3 codes.
+__device__ __forceinline__ uint16_t encode2_mk(float wlo, float whi, uint64_t ns2, uint64_t y2) {
+    const uint64_t negzero2 = 0x8000000080000000ull;
+    uint64_t w2, q0, r, q;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w2) : "f"(wlo), "f"(whi));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q0) : "l"(w2), "l"(y2), "l"(negzero2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ns2), "l"(q0), "l"(w2));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(y2), "l"(q0));
+    float qlo, qhi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(qlo), "=f"(qhi) : "l"(q));
+    return f32x2_to_e4m3x2(copysignf(qlo, wlo), copysignf(qhi, whi));
 }
 
+// Encode 8 bf16 values divided by s into 8 e4m3 bytes.
 __device__ __forceinline__ uint2 encode8_mk(const uint4 v, float s, float y) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint64_t ns2, y2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(ns2) : "f"(-s));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y2) : "f"(y));
     uint32_t out[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const uint16_t c0 = f32x2_to_e4m3x2(div_mk(bf16lo_to_f32(w[2 * h]), s, y), div_mk(bf16hi_to_f32(w[2 * h]), s, y));
-        const uint16_t c1 =
-            f32x2_to_e4m3x2(div_mk(bf16lo_to_f32(w[2 * h + 1]), s, y), div_mk(bf16hi_to_f32(w[2 * h + 1]), s, y));
+        const uint16_t c0 = encode2_mk(bf16lo_to_f32(w[2 * h]), bf16hi_to_f32(w[2 * h]), ns2, y2);
+        const uint16_t c1 = encode2_mk(bf16lo_to_f32(w[2 * h + 1]), bf16hi_to_f32(w[2 * h + 1]), ns2, y2);
         out[h] = static_cast<uint32_t>(c0) | (static_cast<uint32_t>(c1) << 16);
     }
     return make_uint2(out[0], out[1]);
