@@ -211,13 +211,11 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
     const int my_tiles = tile0 < ntiles ? (ntiles - tile0 + tstep - 1) / tstep : 0;
     const int total = my_tiles * nkb;
     const int mm = min(m, C::kXRows);
-    __shared__ int s_fail;  // a warp gave up a wait: consumers stop after this tile
     __shared__ uint32_t s_bits[kMoeMaxExperts / 32];  // MOE: experts any token selected
     __shared__ int s_expert;                          // MOE: this CTA's expert
     __shared__ signed char s_route[32];               // MOE: slot j of x row mi for it, -1 if none
 
     if (threadIdx.x == 0) {
-        s_fail = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&xready[s], C::kConv ? C::kConvWarps : 1);
@@ -338,10 +336,8 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
             const int s = it % kStages;
             const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
             if (!__all_sync(0xffffffffu, ready)) {
-                if (lane == 0) {
-                    atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
-                    s_fail = 1;
-                }
+                // the consumers' own bounded waits on xready then give up too
+                if (lane == 0) atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
                 break;
             }
             uint8_t *xs = smem + s * C::kStageBytes + C::kCodeBytes;
