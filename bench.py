@@ -201,6 +201,15 @@ def sum_over_ranks(pg, v):
 
 
 # --------------------------------------------------------------- workloads
+LM_HEAD_METRIC = "block-FP8 W8A16 GEMV HBM GB/s (lm_head, M=1,4,8,16)"
+
+
+def lm_head_config(n, k, ms):
+    return {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call at each "
+                        "of M=1,4,8,16 per step", "n": n, "k": k, "ms": ms,
+            "l2": "inputs larger than L2 (623 MB of codes per call)"}
+
+
 def lm_head_workload(torch, fp8bs, inputs, dev):
     ms = [1, 4, 8, 16]
     w = inputs.lm_head_weight(2, device=dev)
@@ -211,9 +220,7 @@ def lm_head_workload(torch, fp8bs, inputs, dev):
     ys = {m: torch.empty((m, n), dtype=torch.bfloat16, device=dev) for m in ms}
     calls = [(f"M={m}", m, gemv_bytes(m, n, k), (lambda m=m: fp8bs.gemv(xs[m], codes, scales, y=ys[m])))
              for m in ms]
-    cfg = {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call at each "
-                       "of M=1,4,8,16 per step", "n": n, "k": k, "ms": ms,
-           "l2": "inputs larger than L2 (623 MB of codes per call)"}
+    cfg = lm_head_config(n, k, ms)
     return dict(calls=calls, xs=xs, ys=ys, cfg=cfg, dominant=("decode_kernel<1,0,true>", [0, 1, 2]),
                 codes=codes, scales=scales, n=n, k=k, mx=False)
 
@@ -622,15 +629,15 @@ def main():
             per_step.append((v, s))
         value = statistics.fmean(v for v, _ in per_step)
         ms_step = 1e3 * statistics.fmean(s for _, s in per_step)
-        line = {"impl": "reference", "metric": "block-FP8 W8A16 GEMV HBM-equivalent GB/s (lm_head, M=1,4,8,16)",
+        # the same metric, unit and config as this file's own lm_head line;
+        # the oracle processes a sample of the rows (cpu_baseline.sample)
+        line = {"impl": "reference", "metric": LM_HEAD_METRIC,
                 "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": len(per_step),
                 "warmup": warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call "
-                                       "at each of M=1,4,8,16 per step", "n": 152064, "k": 4096,
-                           "ms": [1, 4, 8, 16], "sample_rows_per_step": rows},
+                "config": dict(lm_head_config(152064, 4096, [1, 4, 8, 16]), parallelism=f"replicas x{args.gpus}"),
                 "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                 "sample": desc},
+                                 "sample": f"{desc}; {rows} rows per step"},
                 "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return 0
@@ -731,7 +738,7 @@ def main():
     per_call_launches = wl.get("call_launches", [wl.get("launches_per_call", 1)] * len(calls))
     launches = args.steps * sum(per_call_launches) * wl.get("launches_per_step", 1)
     if rank == 0:
-        line = {"metric": "block-FP8 W8A16 GEMV HBM GB/s (lm_head, M=1,4,8,16)" if args.workload == "lm_head"
+        line = {"metric": LM_HEAD_METRIC if args.workload == "lm_head"
                 else f"{args.workload} {unit}",
                 "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,

@@ -63,3 +63,8 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same metric and workload as the CUDA arm's default line
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["metric"] == bench.LM_HEAD_METRIC and d["higher_is_better"] is True
+    assert d["config"] == dict(bench.lm_head_config(152064, 4096, [1, 4, 8, 16]), parallelism="replicas x2")
