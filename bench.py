@@ -33,6 +33,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -609,7 +610,8 @@ def main():
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--clocks-file", default=os.path.join(ROOT, "gpurun_out", "bench_clocks.csv"))
+    ap.add_argument("--clocks-file", default=os.path.join(tempfile.gettempdir(), "fp8bs_bench_clocks.csv"),
+                    help="raw nvidia-smi samples taken during the timed region (summarised in the JSON line)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
     peak, peak_kind = measured_peaks()
