@@ -15,8 +15,10 @@
 //    blocks are split over a thread-block cluster and reduced through DSMEM
 //    in rank order, as in the W8A16 decode kernel.
 //  * w8a8_prefill_kernel: tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32),
-//    both operands loaded by TMA into a 4-stage ring, the fp32 accumulator
-//    in 256 TMEM columns for the whole K range, one epilogue pass.
+//    both operands loaded by TMA into a 4-stage ring; persistent CTAs (one
+//    per SM) loop over 128 x 256 output tiles, each tile accumulating over
+//    the whole K range in one of two 256-column TMEM accumulators, so one
+//    tile's epilogue overlaps the next tile's MMAs.
 //  * w8a8_generic_kernel: plain loads, any shape or alignment.
 #include "common.cuh"
 #include "internal.h"
@@ -338,7 +340,7 @@ constexpr int kPStages = 4;
 constexpr int kPABytes = kPTileW * kKB;   // 16 KB
 constexpr int kPBBytes = kPTileX * kKB;   // 32 KB
 constexpr int kPStage = kPABytes + kPBBytes;
-constexpr int kPTmemCols = 256;
+constexpr int kPTmemCols = 512;           // accumulators D_0, D_1: columns [0, 256), [256, 512)
 constexpr int kPWarpMma = 0, kPWarpTma = 1, kPWarpEpi0 = 2, kPNumEpi = 8;
 constexpr int kPThreads = (kPWarpEpi0 + kPNumEpi) * 32;
 constexpr int kPSmemBytes = 1024 + kPStages * kPStage + 256;
@@ -359,31 +361,39 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// Persistent: CTA b takes output tiles b, b + gridDim.x, ... (tile t = weight
+// tile t % tiles_w, x tile t / tiles_w).  The TMA ring streams straight across
+// tile boundaries and consecutive tiles accumulate into alternate TMEM
+// accumulators, so the epilogue of one tile overlaps the MMAs of the next.
 __global__ void __launch_bounds__(kPThreads, 1) w8a8_prefill_kernel(const __grid_constant__ CUtensorMap tm_w,
                                                                    const __grid_constant__ CUtensorMap tm_x,
                                                                    const float *__restrict__ sx_p,
                                                                    const float *__restrict__ sw_p,
                                                                    __nv_bfloat16 *__restrict__ y, int m, int n,
-                                                                   int kblocks) {
+                                                                   int kblocks, int tiles_w, int tiles) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kPStages * kPStage);  // [kPStages]
     uint64_t *empty = full + kPStages;                                         // [kPStages]
-    uint64_t *d_full = empty + kPStages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_full + 1);
-    int *s_fail = reinterpret_cast<int *>(d_full + 2);
+    uint64_t *d_full = empty + kPStages;                                       // [2] a tile's MMAs done
+    uint64_t *d_empty = d_full + 2;                                            // [2] a tile's epilogue done
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_empty + 2);
+    int *s_fail = reinterpret_cast<int *>(d_empty + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kPTileW;
-    const int m0 = blockIdx.y * kPTileX;
+    const int tile0 = blockIdx.x, tstep = gridDim.x;
+    const int my_tiles = tile0 < tiles ? (tiles - tile0 + tstep - 1) / tstep : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kPStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);  // tcgen05.commit
         }
-        mbar_init(d_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&d_full[i], 1);          // tcgen05.commit
+            mbar_init(&d_empty[i], kPNumEpi);  // every epilogue warp
+        }
         *s_fail = 0;
         fence_mbarrier_init();
     }
@@ -401,70 +411,95 @@ __global__ void __launch_bounds__(kPThreads, 1) w8a8_prefill_kernel(const __grid
     if (warp == kPWarpMma) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kPStages;
-                if (!mbar_wait_bounded(&full[s], (kb / kPStages) & 1)) {
+            int u = 0;  // stages consumed (all tiles)
+            bool failed = false;
+            for (int i = 0; i < my_tiles && !failed; ++i) {
+                const int b = i & 1;
+                // accumulator b was last read by the epilogue of tile i - 2
+                if (i >= 2 && !mbar_wait_bounded(&d_empty[b], ((i - 2) >> 1) & 1)) {
                     atomicOr(&g_w8a8_err, ERRBIT_MMA_WAIT);
-                    *reinterpret_cast<volatile int *>(s_fail) = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t adesc = sw128_desc(smem_u32(smem + s * kPStage));
-                const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kPStage + kPABytes));
+                    failed = true;
+                } else {
+                    tc_fence_after();
+                    const uint32_t d = tmem + 256 * b;
+                    for (int kb = 0; kb < kblocks; ++kb, ++u) {
+                        const int s = u % kPStages;
+                        if (!mbar_wait_bounded(&full[s], (u / kPStages) & 1)) {
+                            atomicOr(&g_w8a8_err, ERRBIT_MMA_WAIT);
+                            failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t adesc = sw128_desc(smem_u32(smem + s * kPStage));
+                        const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kPStage + kPABytes));
 #pragma unroll
-                for (int kk = 0; kk < kKB / 32; ++kk)
-                    tc_mma_f8(tmem, adesc + 2 * kk, bdesc + 2 * kk, (kb > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(&empty[s]);
-                issued = kb + 1;
+                        for (int kk = 0; kk < kKB / 32; ++kk)
+                            tc_mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(&empty[s]);
+                    }
+                }
+                if (failed) *reinterpret_cast<volatile int *>(s_fail) = 1;
+                // the epilogue's wait for this tile (also after a failure, so
+                // that it does not sit out its whole time limit)
+                tc_commit(&d_full[b]);
             }
-            tc_commit(d_full);  // the epilogue's single wait (also after a failure)
-            if (issued > 0 &&
-                !mbar_wait_bounded(&empty[(issued - 1) % kPStages], ((issued - 1) / kPStages) & 1))
+            // drain: wait for the last committed stage before TMEM can be freed
+            if (u > 0 && !mbar_wait_bounded(&empty[(u - 1) % kPStages], ((u - 1) / kPStages) & 1))
                 atomicOr(&g_w8a8_err, ERRBIT_MMA_WAIT);
         }
         __syncwarp();
     } else if (warp == kPWarpTma) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < kblocks; ++kb) {
-                const int s = kb % kPStages;
-                if (kb >= kPStages &&
-                    !mbar_wait_bounded(&empty[s], ((kb - kPStages) / kPStages) & 1)) {
-                    atomicOr(&g_w8a8_err, ERRBIT_EMPTY_WAIT);
-                    break;
+            int u = 0;  // stages issued (all tiles)
+            bool stop = false;
+            for (int i = 0; i < my_tiles && !stop; ++i) {
+                const int t = tile0 + i * tstep;
+                const int n0 = (t % tiles_w) * kPTileW, m0 = (t / tiles_w) * kPTileX;
+                for (int kb = 0; kb < kblocks; ++kb, ++u) {
+                    const int s = u % kPStages;
+                    if (u >= kPStages && !mbar_wait_bounded(&empty[s], ((u - kPStages) / kPStages) & 1)) {
+                        atomicOr(&g_w8a8_err, ERRBIT_EMPTY_WAIT);
+                        stop = true;
+                        break;
+                    }
+                    if (*reinterpret_cast<volatile int *>(s_fail)) {
+                        stop = true;
+                        break;
+                    }
+                    uint8_t *st = smem + s * kPStage;
+                    mbar_arrive_expect_tx(&full[s], kPStage);
+                    tma_load_2d(st, &tm_w, &full[s], kb * kKB, n0);
+                    tma_load_2d(st + kPABytes, &tm_x, &full[s], kb * kKB, m0);
                 }
-                if (*reinterpret_cast<volatile int *>(s_fail)) break;
-                uint8_t *st = smem + s * kPStage;
-                mbar_arrive_expect_tx(&full[s], kPStage);
-                tma_load_2d(st, &tm_w, &full[s], kb * kKB, n0);
-                tma_load_2d(st + kPABytes, &tm_x, &full[s], kb * kKB, m0);
-                issued = kb + 1;
             }
-            for (int kb = issued - kPStages < 0 ? 0 : issued - kPStages; kb < issued; ++kb)
-                if (!mbar_wait_bounded(&full[kb % kPStages], (kb / kPStages) & 1))
+            // never leave with copies in flight: wait for the last stages issued
+            for (int v = u - kPStages < 0 ? 0 : u - kPStages; v < u; ++v)
+                if (!mbar_wait_bounded(&full[v % kPStages], (v / kPStages) & 1))
                     atomicOr(&g_w8a8_err, ERRBIT_FULL_WAIT);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue
         // thread = one weight row (TMEM lane of quarter q); columns
-        // [128 ch, 128 ch + 128) are rows m0 + 128 ch + j of x
+        // [128 ch, 128 ch + 128) of a tile's accumulator are rows
+        // m0 + 128 ch + j of x
         const int q = warp & 3;
         const int ch = (warp - kPWarpEpi0) >> 2;
-        const int row = n0 + q * 32 + lane;
-        bool ok = mbar_wait_bounded(d_full, 0);
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) atomicOr(&g_w8a8_err, ERRBIT_FULL_WAIT);
-            ok = false;
-        } else {
-            ok = *reinterpret_cast<volatile int *>(s_fail) == 0;
-        }
-        if (ok) {
+        const float scale = __ldg(sx_p) * __ldg(sw_p);
+        for (int i = 0; i < my_tiles; ++i) {
+            const int b = i & 1;
+            const int t = tile0 + i * tstep;
+            const int n0 = (t % tiles_w) * kPTileW, m0 = (t / tiles_w) * kPTileX;
+            const int row = n0 + q * 32 + lane;
+            const bool ok = mbar_wait_bounded(&d_full[b], (i >> 1) & 1);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) atomicOr(&g_w8a8_err, ERRBIT_FULL_WAIT);
+                break;
+            }
+            if (*reinterpret_cast<volatile int *>(s_fail)) break;
             tc_fence_after();
-            const float scale = __ldg(sx_p) * __ldg(sw_p);
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ch * 128;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + 256 * b + ch * 128;
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
                 uint32_t v[16];
@@ -472,13 +507,17 @@ __global__ void __launch_bounds__(kPThreads, 1) w8a8_prefill_kernel(const __grid
                 tc_wait_ld();
                 if (row < n) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int mi = m0 + ch * 128 + 16 * c + i;
+                    for (int j = 0; j < 16; ++j) {
+                        const int mi = m0 + ch * 128 + 16 * c + j;
                         if (mi < m)
-                            y[static_cast<int64_t>(mi) * n + row] = __float2bfloat16_rn(__uint_as_float(v[i]) * scale);
+                            y[static_cast<int64_t>(mi) * n + row] = __float2bfloat16_rn(__uint_as_float(v[j]) * scale);
                     }
                 }
             }
+            // accumulator b has been read: the MMAs of tile i + 2 may reuse it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&d_empty[b]);
         }
     }
 
@@ -567,12 +606,18 @@ cudaError_t launch_w8a8_prefill(const W8A8Args &a, cudaStream_t stream) {
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
-    const dim3 grid(static_cast<unsigned>((a.n + kPTileW - 1) / kPTileW),
-                    static_cast<unsigned>((a.m + kPTileX - 1) / kPTileX));
+    const int64_t tiles_w = (a.n + kPTileW - 1) / kPTileW;
+    const int64_t tiles = tiles_w * ((a.m + kPTileX - 1) / kPTileX);
+    if (tiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    // one CTA per SM (the ring takes most of its shared memory), each looping
+    // over its tiles
+    const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
     w8a8_prefill_kernel<<<grid, kPThreads, kPSmemBytes, stream>>>(tm_w, tm_x, a.sx, a.sw,
                                                                   static_cast<__nv_bfloat16 *>(a.y),
                                                                   static_cast<int>(a.m), static_cast<int>(a.n),
-                                                                  kblocks);
+                                                                  kblocks, static_cast<int>(tiles_w),
+                                                                  static_cast<int>(tiles));
     return cudaGetLastError();
 }
 

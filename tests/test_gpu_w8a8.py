@@ -185,6 +185,20 @@ def test_prefill_shapes_sampled(pkg):
                  x_rows=lambda m: np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, 14)])))
 
 
+def test_prefill_more_tiles_than_ctas(pkg):
+    """180 output tiles of 128 weight rows x 256 x rows for at most 152
+    persistent CTAs: CTAs take a second tile into the other accumulator;
+    every output is checked."""
+    n, k, m = 20 * 128, 256, 9 * 256
+    w = inputs.gaussian_bf16((n, k), 0.02, 31)
+    owq, osw = oracle.tensor_quantize(bits(w))
+    x = inputs.activations(m, k, 32)
+    xq, sx = oracle.act_quantize(bits(x))
+    y = pkg.w8a8_gemm(dev(xq), dev(sx), dev(owq), dev(osw), path=PATH_PREFILL)
+    torch.cuda.synchronize()
+    check(y, xq, sx, owq, osw)
+
+
 def test_repeat_is_deterministic(pkg):
     w = inputs.rotation_weight(1, 1, device=DEV)
     wq, sw = pkg.tensor_quantize(w)
