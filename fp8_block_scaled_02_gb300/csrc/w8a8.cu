@@ -608,10 +608,11 @@ cudaError_t launch_w8a8_prefill(const W8A8Args &a, cudaStream_t stream) {
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
     const int64_t tiles_w = (a.n + kPTileW - 1) / kPTileW;
     const int64_t tiles = tiles_w * ((a.m + kPTileX - 1) / kPTileX);
-    if (tiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
     // one CTA per SM (the ring takes most of its shared memory), each looping
-    // over its tiles
+    // over its tiles; its stage counter runs over all of them (an int)
     const int64_t sms = device_sm_count() > 0 ? device_sm_count() : 1;
+    if (tiles >= (int64_t(1) << 31) || (tiles / sms + 1) * kblocks >= (int64_t(1) << 31))
+        return cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>(tiles < sms ? tiles : sms);
     w8a8_prefill_kernel<<<grid, kPThreads, kPSmemBytes, stream>>>(tm_w, tm_x, a.sx, a.sw,
                                                                   static_cast<__nv_bfloat16 *>(a.y),
