@@ -188,7 +188,7 @@ def test_worked_example_mx(golden):
 def _exact_ceil_log2(amax: Fraction) -> int:
     """ceil(log2(amax / 448)) by exact rational comparison."""
     r = amax / 448
-    e = 0
+    e = math.ceil(math.log2(r))  # a starting guess; the loops below make it exact
     while Fraction(2) ** e < r:
         e += 1
     while Fraction(2) ** (e - 1) >= r:
@@ -234,6 +234,34 @@ def test_mx_grid_values_roundtrip_exactly():
         assert e8m0[0, 0] == 127 + j
         back = table[codes[0]] * 2.0 ** (int(e8m0[0, 0]) - 127)
         assert np.array_equal(back, v)
+
+
+def test_mx_exponent_every_bf16_amax():
+    """Exhaustive over the group maximum: for every positive finite bf16
+    value as the amax of a 32-element group (the other elements smaller or
+    its negation), E = clamp(ceil(log2(amax / 448)) + 127, 0, 254) by exact
+    rational arithmetic; where E is not clamped, amax / 2^e lies in
+    (224, 448] (the group never saturates) and the amax element's code is the
+    independent bit-arithmetic encoder's code of that exact quotient, its
+    negation's the same code with the sign bit set."""
+    amax_bits = np.arange(0x0001, 0x7F80, dtype=np.uint32)          # every positive finite bf16
+    n = amax_bits.size
+    w = np.zeros((n, 32), dtype=np.uint16)
+    w[:, 13] = amax_bits
+    w[:, 20] = amax_bits >> 1                                        # a smaller element of each group
+    w[:, 27] = (amax_bits | 0x8000) & np.where(amax_bits > 1, 0xFFFF, 0x8000)  # -amax or -0
+    codes, e8m0 = oracle.mx_quantize(w)
+    vals = (amax_bits << 16).view(np.float32).astype(np.float64)
+    es = np.array([_exact_ceil_log2(Fraction(float(v))) for v in vals])
+    E = np.clip(es + 127, 0, 254)
+    assert np.array_equal(e8m0[:, 0].astype(np.int64), E)
+    free = (es + 127 >= 0) & (es + 127 <= 254)                           # E not clamped
+    ratio = vals[free] * np.exp2(-es[free].astype(np.float64))            # exact: power-of-two scaling
+    assert np.all((ratio > 224) & (ratio <= 448))
+    want = bitwise_e4m3_encode(ratio.astype(np.float32))
+    assert np.array_equal(codes[free, 13], want)
+    neg = free & (amax_bits > 1)
+    assert np.array_equal(codes[neg, 27], bitwise_e4m3_encode(ratio[(amax_bits > 1)[free]].astype(np.float32)) | 0x80)
 
 
 @pytest.mark.parametrize("amax_bits,E", [(0x43E0, 127), (0x43E1, 128), (0x4360, 126), (0x4361, 127),
