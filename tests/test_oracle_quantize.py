@@ -69,6 +69,29 @@ def test_amax_element_maps_to_448_and_scale_formula():
         assert codes[rs, cs][r, c] & 0x7F == 0x7E
 
 
+def test_block_scale_every_bf16_amax():
+    """Exhaustive over the tile maximum: one ragged 1 x 128 tile per positive
+    finite bf16 amax (with its negation and a smaller element beside it).
+    s is the IEEE fp32 quotient amax / 448; the codes are the independent
+    encoder's codes of the IEEE fp32 quotients w / s; and whenever s is a
+    normal fp32 value the amax element encodes to exactly +-448."""
+    amax_bits = np.arange(0x0001, 0x7F80, dtype=np.uint32)
+    t = amax_bits.size
+    w = np.zeros((1, 128 * t), dtype=np.uint16)
+    w[0, 0::128] = amax_bits
+    w[0, 1::128] = amax_bits | 0x8000
+    w[0, 2::128] = amax_bits >> 3
+    codes, scales = oracle.block_quantize(w)
+    amax = (amax_bits << 16).view(np.float32)
+    s = amax / np.float32(448.0)                                      # IEEE fp32 division
+    assert scales.shape == (1, t) and np.array_equal(scales[0].view(np.uint32), s.view(np.uint32))
+    for col in (0, 1, 2):
+        wv = (w[0, col::128].astype(np.uint32) << 16).view(np.float32)
+        assert np.array_equal(codes[0, col::128], bitwise_e4m3_encode(wv / s))
+    normal = s >= np.float32(2.0 ** -126)
+    assert np.all(codes[0, 0::128][normal] == 0x7E) and np.all(codes[0, 1::128][normal] == 0xFE)
+
+
 def test_tiny_ragged_outliers_set_their_tiles():
     w = bits_of(inputs.tiny_ragged_weight(0))
     codes, scales = oracle.block_quantize(w)
