@@ -78,3 +78,13 @@ def mx_wmax_rows(codes_rows, e8m0_rows, table) -> np.ndarray:
     k = codes_rows.shape[1]
     s = np.ldexp(1.0, np.repeat(np.asarray(e8m0_rows, dtype=np.int64) - 127, 32, axis=1)[:, :k])
     return np.abs(table[codes_rows] * s).max(axis=1)
+
+
+def kv_attention_bound(o, o64, vmax) -> np.ndarray:
+    """Element-wise bound for decode attention against the fp64 result:
+    2^-10 * max|V| + half a bf16 ulp.  o is a convex combination of the rows
+    of V, so every error term (f16 weights, fp32 sums, exp2) scales with
+    max|V|; the bf16 output adds its own rounding."""
+    o = np.asarray(o, dtype=np.float64)
+    o64 = np.asarray(o64, dtype=np.float64)
+    return 2.0 ** -10 * float(vmax) + 0.5 * ulp_bf16(np.maximum(np.abs(o), np.abs(o64)))

@@ -15,7 +15,8 @@ import torch
 
 import oracle
 from fp8_block_scaled_02_gb300 import inputs
-from oracle.tolerance import bf16_bits_to_f64, ulp_bf16
+from oracle import tolerance
+from oracle.tolerance import bf16_bits_to_f64
 
 from gpu_helpers import bits, lib_or_skip, table
 
@@ -52,7 +53,7 @@ def check(o_dev, q, kc, vc, ks, vs, tbl, sl, sm):
     o64 = oracle.kv_attention(bits(q), kc, vc, ks, vs, tbl.numpy(), sl.numpy(), sm)
     o = bf16_bits_to_f64(bits(o_dev.cpu()))
     vmax = np.nanmax(np.abs(table()[vc])) * float(vs[0])  # NaN codes may sit in unused slots
-    bound = 2.0 ** -10 * vmax + 0.5 * ulp_bf16(np.maximum(np.abs(o), np.abs(o64)))
+    bound = tolerance.kv_attention_bound(o, o64, vmax)
     err = np.abs(o - o64)
     assert np.all(np.isfinite(o))
     assert np.all(err <= bound), (err.max(), (err / bound).max())

@@ -1,11 +1,13 @@
-"""The GEMV acceptance test (oracle/tolerance.py) is tight enough to catch the
-mistakes a block-FP8 or MXFP8 GEMV kernel plausibly makes (CPU only).
+"""The acceptance tests (oracle/tolerance.py) are tight enough to catch the
+mistakes a block-FP8 / MXFP8 GEMV or an FP8 KV decode-attention kernel
+plausibly makes (CPU only).
 
-Each case builds a kernel-like result in numpy -- fp32 partial sums per K block
-(block scales) or per 32-element group (MX), the scale applied to the fp32
-partial, one bf16 rounding at the end -- once correctly and once with one
-planted mistake, and checks that the acceptance test passes the first and
-rejects the second, against the oracle's fp64 result.
+GEMV: a kernel-like result in numpy -- fp32 partial sums per K block (block
+scales) or per 32-element group (MX), the scale applied to the fp32 partial,
+one bf16 rounding at the end -- once correctly and once with one planted
+mistake.  Attention: the oracle's own result rounded to bf16, and the oracle
+run on inputs that carry one planted mistake.  The acceptance test must pass
+the first and reject the second, against the oracle's fp64 result.
 """
 import numpy as np
 import pytest
@@ -124,3 +126,53 @@ def test_mx_kernel_mistakes_fail(mx_case, bug):
     xb, codes, e8m0, y64, wmax = mx_case
     st = tolerance.gemv_errors(kernel_like_mx(xb, codes, e8m0, bug), y64, xb, wmax)
     assert not tolerance.gemv_ok(st), (bug, st)
+
+
+# ------------------------------------------------------ decode attention
+@pytest.fixture(scope="module")
+def kv_case():
+    hq, hkv, page, blocks = 8, 2, 16, 16
+    q, k, v, tbl, sl = inputs.kv_layer(2, [37, 70], blocks, hq, hkv, 128, page, seed=3)
+    kb = inputs.bf16_bits(k).reshape(-1, hkv, 128)
+    vb = inputs.bf16_bits(v).reshape(-1, hkv, 128)
+    _, ks = oracle.tensor_quantize(kb.reshape(-1, 128))
+    _, vs = oracle.tensor_quantize(vb.reshape(-1, 128))
+    slots = np.arange(blocks * page, dtype=np.int32)
+    empty = np.zeros((blocks, page, hkv, 128), dtype=np.uint8)
+    kc = oracle.kv_append(kb, slots, ks, empty)
+    vc = oracle.kv_append(vb, slots, vs, empty)
+    qb = inputs.bf16_bits(q)
+    sm = 128 ** -0.5
+    o64 = oracle.kv_attention(qb, kc, vc, ks, vs, tbl.numpy(), sl.numpy(), sm)
+    vmax = np.abs(oracle.e4m3_decode_table()[vc]).max() * float(vs[0])
+    return dict(q=qb, kc=kc, vc=vc, ks=ks, vs=vs, tbl=tbl.numpy(), sl=sl.numpy(), sm=sm, o64=o64, vmax=vmax)
+
+
+def kv_accepts(c, o):
+    o_bf16 = tolerance.bf16_bits_to_f64(to_bf16_bits(o))
+    return bool(np.all(np.abs(o_bf16 - c["o64"]) <= tolerance.kv_attention_bound(o_bf16, c["o64"], c["vmax"])))
+
+
+def test_correct_attention_passes(kv_case):
+    assert kv_accepts(kv_case, kv_case["o64"])
+
+
+@pytest.mark.parametrize("bug", ["k_scale_twice", "v_scale_missing", "last_token_dropped", "gqa_head_shifted",
+                                 "no_sm_scale", "block_table_shifted"])
+def test_attention_mistakes_fail(kv_case, bug):
+    c = dict(kv_case)
+    q, ks, vs, tbl, sl, sm = c["q"], c["ks"], c["vs"], c["tbl"].copy(), c["sl"].copy(), c["sm"]
+    if bug == "k_scale_twice":
+        ks = ks * ks
+    elif bug == "v_scale_missing":
+        vs = np.ones_like(vs)
+    elif bug == "last_token_dropped":
+        sl = sl - 1
+    elif bug == "gqa_head_shifted":
+        q = np.roll(q, 4, axis=1)          # query head h read as the group of head h + 4
+    elif bug == "no_sm_scale":
+        sm = 1.0
+    elif bug == "block_table_shifted":
+        tbl = np.roll(tbl, 1, axis=1)
+    o = oracle.kv_attention(q, c["kc"], c["vc"], ks, vs, tbl, sl, sm)
+    assert not kv_accepts(kv_case, o), bug
