@@ -23,6 +23,9 @@ Functions (names follow the C entry points):
     kv_append(x, slots, scale, cache)    FP8 KV cache append (fp8kv_append), in place
     kv_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                         max_seq_len, sm_scale) -> o bf16 [B, Hq, 128]   (fp8kv_decode_attention)
+    check_device_error()   -> the kernels' error word (synchronises; reading clears it)
+    select_path(m, n, k)   -> the kernel path an AUTO call takes (host only)
+    debug_wait_expiry(), debug_encode_f32(first_bits, count)   test hooks (fp8bs_debug_*)
 """
 from __future__ import annotations
 
