@@ -226,7 +226,10 @@ def lm_head_workload(torch, fp8bs, inputs, dev):
                 codes=codes, scales=scales, n=n, k=k, mx=False)
 
 
-def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block"):
+def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True):
+    """48 layers x 4 projection weights, one GEMV each per step.  batched:
+    the step is one fp8bs_gemv_batch call (the 192 GEMVs stream as two
+    persistent launches); otherwise one fp8bs_gemv call per weight."""
     layers = inputs.ROTATION_LAYERS
     quant, gemv = quantizer(fp8bs, scales)
     weights = []
@@ -238,17 +241,25 @@ def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block"):
     shapes = [inputs.ROTATION_SHAPES[j] for _ in range(layers) for j in range(4)]
     xs = [inputs.activations(m, k, 7 + i, device=dev) for i, (n, k) in enumerate(shapes)]
     ys = [torch.empty((m, n), dtype=torch.bfloat16, device=dev) for (n, k) in shapes]
+    batched = batched and scales == "block"
+    ops = [(xs[i], c, s, ys[i]) for i, (c, s) in enumerate(weights)]
 
     def step():
-        for i, (c, s) in enumerate(weights):
-            gemv(xs[i], c, s, y=ys[i])
+        if batched:
+            fp8bs.gemv_batch(ops)
+        else:
+            for i, (c, s) in enumerate(weights):
+                gemv(xs[i], c, s, y=ys[i])
     total = sum(gemv_bytes(m, n, k, scales=scales) for (n, k) in shapes)
     kind = {"block": "block-FP8", "row": "per-row FP8", "tensor": "per-tensor FP8"}[scales]
+    how = "one batched call (fp8bs_gemv_batch)" if batched else "one call per weight"
     cfg = {"workload": f"decode dense-projection rotation: 48 layers x 4 {kind} weights "
-                       f"([8192,2560],[2560,3072],[6656,2560],[2560,3072]), M={m}, 192 GEMVs per step "
-                       "(CUDA graph)", "ms": [m], "l2": "inputs larger than L2 (2.58 GB of codes per step)"}
-    return dict(calls=[(f"rotation M={m}", m, total, step)], cfg=cfg, graph=True, launches_per_step=192,
-                dominant=("decode_kernel", [0]))
+                       f"([8192,2560],[2560,3072],[6656,2560],[2560,3072]), M={m}, 192 GEMVs per step, "
+                       f"{how}, CUDA graph", "ms": [m], "l2": "inputs larger than L2 (2.58 GB of codes per step)"}
+    launches = 2 if batched else 192
+    dom = "gemv_batch_kernel" if batched else "decode_kernel"
+    return dict(calls=[(f"rotation M={m}", m, total, step)], cfg=cfg, graph=True, launches_per_step=launches,
+                dominant=(dom, [0]), xs=xs, ys=ys, weights=weights, ops=ops)
 
 
 def sweep_workload(torch, fp8bs, inputs, dev, ms):
@@ -608,6 +619,7 @@ def main():
                     choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill", "rowwise", "w8a8",
                              "w8a8_prefill", "moe", "kv"])
     ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--single", action="store_true", help="rotation: one GEMV call per weight, not one batch")
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-file", default=os.path.join(tempfile.gettempdir(), "fp8bs_bench_clocks.csv"),
@@ -655,7 +667,7 @@ def main():
     if args.workload == "lm_head":
         wl = lm_head_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "rotation":
-        wl = rotation_workload(torch, fp8bs, inputs, dev, args.m, args.scales)
+        wl = rotation_workload(torch, fp8bs, inputs, dev, args.m, args.scales, batched=not args.single)
     elif args.workload == "sweep":
         wl = sweep_workload(torch, fp8bs, inputs, dev, list(range(1, 33)))
     elif args.workload == "mx":

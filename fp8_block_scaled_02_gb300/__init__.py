@@ -12,6 +12,8 @@ Functions (names follow the C entry points):
     gemv(x, codes, scales) -> y bf16 [M,N]
     mx_quantize(w)         -> (codes u8 [N,K], e8m0 u8 [N, ceil(K/32)])
     mx_gemv(x, codes, e8m0)-> y bf16 [M,N]
+    gemv_batch([(x, codes, scales[, y]), ...]) -> [y, ...]   (fp8bs_gemv_batch)
+    mx_gemv_batch([(x, codes, e8m0[, y]), ...]) -> [y, ...]  (mxfp8_gemv_batch)
     row_quantize(w)        -> (codes u8 [N,K], scales f32 [N])       (fp8row_*)
     tensor_quantize(w)     -> (codes u8 [N,K], scale f32 [1])        (fp8tensor_*)
     row_gemv(x, codes, s)  -> y bf16 [M,N]; s is [N] (per row) or [1] (per tensor)
@@ -45,6 +47,12 @@ _lock = threading.Lock()
 _lib = None
 
 
+class GemvOp(ctypes.Structure):
+    """fp8bs_gemv_op: one GEMV of a batch (device pointers, sizes)."""
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("y_bf16", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
 class Fp8bsError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -67,6 +75,10 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_quantize.argtypes = [p, i64, i64, i32, p, p, p]
         L.fp8bs_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
         L.fp8bs_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
+        L.fp8bs_gemv_batch.argtypes = [p, i64, i64, p]
+        L.fp8bs_gemv_batch_ex.argtypes = [p, i64, i64, i32, p]
+        L.mxfp8_gemv_batch.argtypes = [p, i64, i64, p]
+        L.mxfp8_gemv_batch_ex.argtypes = [p, i64, i64, i32, p]
         L.mxfp8_quantize.argtypes = [p, i64, i64, p, p, p]
         L.mxfp8_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
         L.mxfp8_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
@@ -90,7 +102,8 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_debug_wait_expiry.argtypes = [p]
         L.fp8bs_debug_encode_f32.argtypes = [ctypes.c_uint32, i64, p, p]
         L.fp8bs_version.argtypes = []
-        for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
+        for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "fp8bs_gemv_batch", "fp8bs_gemv_batch_ex",
+                  "mxfp8_gemv_batch", "mxfp8_gemv_batch_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                   "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
                   "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention",
@@ -113,145 +126,252 @@ def _check(status: int, what: str):
         raise Fp8bsError(status, what)
 
 
-def _stream(stream):
+def _stream(stream, device=None):
     import torch
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
     if isinstance(stream, int):
         return ctypes.c_void_p(stream)
     return ctypes.c_void_p(stream.cuda_stream)
-
-
-def _dev(t, dtype, name):
-    import torch
-    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
-        raise TypeError(f"{name} must be a CUDA tensor")
-    if t.dtype != dtype:
-        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
 
 
 def cdiv(a: int, b: int) -> int:
     return (a + b - 1) // b
 
 
+class _Args:
+    """Checks one call's tensors before anything is launched.
+
+    ``need(name, t, dtype, numel=..., shape=...)`` records a tensor; sizes
+    are checked first (ValueError, for any device), then that every tensor
+    sits on the device of the first one (ValueError), then CUDA, dtype and
+    contiguity (TypeError / ValueError).  ``ptr(name)`` gives the device
+    address once ``check()`` has passed; ``device`` is where the call runs."""
+
+    def __init__(self):
+        self.items = []
+
+    def need(self, name, t, dtype, numel=None, shape=None):
+        import torch
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+        if numel is not None and t.numel() != numel:
+            raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
+        self.items.append((name, t, dtype))
+        return self
+
+    def check(self):
+        first = self.items[0][1].device
+        for name, t, _ in self.items:
+            if t.device != first:
+                raise ValueError(f"{name} is on {t.device}, the call's tensors on {first}")
+        for name, t, dtype in self.items:
+            if t.device.type != "cuda":
+                raise TypeError(f"{name} must be a CUDA tensor")
+            if t.dtype != dtype:
+                raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+        self.device = first
+        self.ptrs = {name: ctypes.c_void_p(t.data_ptr()) for name, t, _ in self.items}
+        return self
+
+    def ptr(self, name):
+        return self.ptrs[name]
+
+
+def _run(args: _Args, what: str, fn, *call_args, stream=None):
+    """Call the library on the device of the call's tensors, on that
+    device's current stream unless one is given."""
+    import torch
+    with torch.cuda.device(args.device):
+        _check(fn(*call_args, _stream(stream, args.device)), what)
+
+
+def _shape2(t, name):
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got {t.dim()}-D")
+    return t.shape
+
+
+def _new(t, shape, dtype, like):
+    import torch
+    return torch.empty(shape, dtype=dtype, device=like.device) if t is None else t
+
+
 def quantize(w, block: int = 128, codes=None, scales=None, stream=None):
     """Block-FP8 load-time quantization of a bf16 [N, K] CUDA tensor."""
     import torch
-    n, k = w.shape
-    if codes is None:
-        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
-    if scales is None:
-        scales = torch.empty((cdiv(n, 128), cdiv(k, 128)), dtype=torch.float32, device=w.device)
-    _check(lib().fp8bs_quantize(_dev(w, torch.bfloat16, "w"), n, k, int(block), _dev(codes, torch.uint8, "codes"),
-                                _dev(scales, torch.float32, "scales"), _stream(stream)), "fp8bs_quantize")
+    n, k = _shape2(w, "w")
+    codes = _new(codes, (n, k), torch.uint8, w)
+    scales = _new(scales, (cdiv(n, 128), cdiv(k, 128)), torch.float32, w)
+    a = _Args().need("w", w, torch.bfloat16).need("codes", codes, torch.uint8, numel=n * k) \
+        .need("scales", scales, torch.float32, numel=cdiv(n, 128) * cdiv(k, 128)).check()
+    _run(a, "fp8bs_quantize", lib().fp8bs_quantize, a.ptr("w"), n, k, int(block), a.ptr("codes"), a.ptr("scales"),
+         stream=stream)
     return codes, scales
+
+
+def _gemv_args(x, codes, y, scales, sdtype, snumel, check=True):
+    import torch
+    m, k = _shape2(x, "x")
+    n, k2 = _shape2(codes, "codes")
+    if k2 != k:
+        raise ValueError("codes and x disagree on K")
+    y = _new(y, (m, n), torch.bfloat16, x)
+    a = _Args().need("x", x, torch.bfloat16).need("codes", codes, torch.uint8) \
+        .need("scales", scales, sdtype, numel=snumel(n, k)).need("y", y, torch.bfloat16, numel=m * n)
+    return (a.check() if check else a), m, n, k, y
+
+
+def _block_numel(n, k):
+    return cdiv(n, 128) * cdiv(k, 128)
 
 
 def gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
     """y[M, N] = x[M, K] . dequant(codes, scales)^T (bf16 out, fp32 accumulate)."""
     import torch
-    m, k = x.shape
-    n = codes.shape[0]
-    if codes.shape[1] != k:
-        raise ValueError("codes and x disagree on K")
-    if y is None:
-        y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
-    _check(lib().fp8bs_gemv_ex(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
-                               _dev(scales, torch.float32, "scales"), n, k, _dev(y, torch.bfloat16, "y"),
-                               int(path), _stream(stream)), "fp8bs_gemv")
+    a, m, n, k, y = _gemv_args(x, codes, y, scales, torch.float32, _block_numel)
+    _run(a, "fp8bs_gemv", lib().fp8bs_gemv_ex, a.ptr("x"), m, a.ptr("codes"), a.ptr("scales"), n, k, a.ptr("y"),
+         int(path), stream=stream)
     return y
+
+
+def _batch_ops(ops, mx):
+    import torch
+    arr = (GemvOp * max(1, len(ops)))()
+    if not ops:
+        return arr, 0, [], None
+    m = _shape2(ops[0][0], "x")[0]
+    sdtype = torch.uint8 if mx else torch.float32
+    snumel = (lambda n, k: n * cdiv(k, 32)) if mx else _block_numel
+    # every op's sizes first (nothing about devices), then devices and dtypes
+    for i, op in enumerate(ops):
+        if _shape2(op[0], f"op {i} x")[0] != m:
+            raise ValueError("every op of a batch has the same M")
+        if len(op) > 3 and op[3] is not None:
+            _gemv_args(op[0], op[1], op[3], op[2], sdtype, snumel, check=False)
+        else:
+            n = _shape2(op[1], f"op {i} codes")[0]
+            _Args().need("scales", op[2], sdtype, numel=snumel(n, op[0].shape[1]))
+    first = ops[0][0].device
+    for i, op in enumerate(ops):
+        for name, tt in zip(("x", "codes", "scales", "y"), op):
+            if tt is not None and tt.device != first:
+                raise ValueError(f"op {i} {name} is on {tt.device}, the batch on {first}")
+    ys = []
+    device = None
+    for i, op in enumerate(ops):
+        y = op[3] if len(op) > 3 else None
+        a, _, n, k, y = _gemv_args(op[0], op[1], y, op[2], sdtype, snumel)
+        if device is None:
+            device = a.device
+        elif a.device != device:
+            raise ValueError(f"op {i} is on {a.device}, the batch on {device}")
+        ys.append(y)
+        arr[i] = GemvOp(a.ptr("x").value, a.ptr("codes").value, a.ptr("scales").value, a.ptr("y").value, n, k)
+    return arr, m, ys, device
+
+
+def _run_batch(fn, what, ops, mx, path, stream):
+    import torch
+    arr, m, ys, device = _batch_ops(ops, mx)
+    if not ops:
+        return ys
+    with torch.cuda.device(device):
+        _check(fn(ctypes.cast(arr, ctypes.c_void_p), len(ops), m, int(path), _stream(stream, device)), what)
+    return ys
+
+
+def gemv_batch(ops, path: int = PATH_AUTO, stream=None):
+    """A sequence of block-FP8 GEMVs (fp8bs_gemv_batch): ops is a list of
+    (x [M,K], codes, scales[, y]) with one M; returns the list of y.  Same
+    results as calling gemv on each op in order."""
+    return _run_batch(lib().fp8bs_gemv_batch_ex, "fp8bs_gemv_batch", ops, False, path, stream)
+
+
+def mx_gemv_batch(ops, path: int = PATH_AUTO, stream=None):
+    """A sequence of MXFP8 GEMVs (mxfp8_gemv_batch): ops is a list of
+    (x [M,K], codes, e8m0[, y]) with one M; returns the list of y."""
+    return _run_batch(lib().mxfp8_gemv_batch_ex, "mxfp8_gemv_batch", ops, True, path, stream)
 
 
 def mx_quantize(w, codes=None, e8m0=None, stream=None):
     """MXFP8 load-time quantization of a bf16 [N, K] CUDA tensor."""
     import torch
-    n, k = w.shape
-    if codes is None:
-        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
-    if e8m0 is None:
-        e8m0 = torch.empty((n, cdiv(k, 32)), dtype=torch.uint8, device=w.device)
-    _check(lib().mxfp8_quantize(_dev(w, torch.bfloat16, "w"), n, k, _dev(codes, torch.uint8, "codes"),
-                                _dev(e8m0, torch.uint8, "e8m0"), _stream(stream)), "mxfp8_quantize")
+    n, k = _shape2(w, "w")
+    codes = _new(codes, (n, k), torch.uint8, w)
+    e8m0 = _new(e8m0, (n, cdiv(k, 32)), torch.uint8, w)
+    a = _Args().need("w", w, torch.bfloat16).need("codes", codes, torch.uint8, numel=n * k) \
+        .need("e8m0", e8m0, torch.uint8, numel=n * cdiv(k, 32)).check()
+    _run(a, "mxfp8_quantize", lib().mxfp8_quantize, a.ptr("w"), n, k, a.ptr("codes"), a.ptr("e8m0"), stream=stream)
     return codes, e8m0
 
 
 def mx_gemv(x, codes, e8m0, y=None, path: int = PATH_AUTO, stream=None):
     """y[M, N] = x[M, K] . dequant_mx(codes, e8m0)^T."""
     import torch
-    m, k = x.shape
-    n = codes.shape[0]
-    if codes.shape[1] != k:
-        raise ValueError("codes and x disagree on K")
-    if y is None:
-        y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
-    _check(lib().mxfp8_gemv_ex(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
-                               _dev(e8m0, torch.uint8, "e8m0"), n, k, _dev(y, torch.bfloat16, "y"),
-                               int(path), _stream(stream)), "mxfp8_gemv")
+    a, m, n, k, y = _gemv_args(x, codes, y, e8m0, torch.uint8, lambda n, k: n * cdiv(k, 32))
+    _run(a, "mxfp8_gemv", lib().mxfp8_gemv_ex, a.ptr("x"), m, a.ptr("codes"), a.ptr("scales"), n, k, a.ptr("y"),
+         int(path), stream=stream)
     return y
+
+
+def _rowwise_quantize(fn, what, w, codes, scales, count, stream):
+    import torch
+    n, k = _shape2(w, "w")
+    codes = _new(codes, (n, k), torch.uint8, w)
+    scales = _new(scales, (count(n),), torch.float32, w)
+    a = _Args().need("w", w, torch.bfloat16).need("codes", codes, torch.uint8, numel=n * k) \
+        .need("scales", scales, torch.float32, numel=count(n)).check()
+    _run(a, what, fn, a.ptr("w"), n, k, a.ptr("codes"), a.ptr("scales"), stream=stream)
+    return codes, scales
 
 
 def row_quantize(w, codes=None, scales=None, stream=None):
     """Per-row FP8 load-time quantization: one fp32 scale per row of w."""
-    import torch
-    n, k = w.shape
-    if codes is None:
-        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
-    if scales is None:
-        scales = torch.empty((n,), dtype=torch.float32, device=w.device)
-    _check(lib().fp8row_quantize(_dev(w, torch.bfloat16, "w"), n, k, _dev(codes, torch.uint8, "codes"),
-                                 _dev(scales, torch.float32, "scales"), _stream(stream)), "fp8row_quantize")
-    return codes, scales
+    return _rowwise_quantize(lib().fp8row_quantize, "fp8row_quantize", w, codes, scales, lambda n: n, stream)
 
 
 def tensor_quantize(w, codes=None, scale=None, stream=None):
     """Per-tensor FP8 load-time quantization: one fp32 scale for all of w."""
-    import torch
-    n, k = w.shape
-    if codes is None:
-        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
-    if scale is None:
-        scale = torch.empty((1,), dtype=torch.float32, device=w.device)
-    _check(lib().fp8tensor_quantize(_dev(w, torch.bfloat16, "w"), n, k, _dev(codes, torch.uint8, "codes"),
-                                    _dev(scale, torch.float32, "scale"), _stream(stream)), "fp8tensor_quantize")
-    return codes, scale
+    return _rowwise_quantize(lib().fp8tensor_quantize, "fp8tensor_quantize", w, codes, scale, lambda n: 1, stream)
 
 
 def row_gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
     """y[M, N] = x[M, K] . (dec(codes) * s_row)^T.  ``scales`` of shape [N]
     calls fp8row_gemv, of shape [1] fp8tensor_gemv."""
     import torch
-    m, k = x.shape
-    n = codes.shape[0]
-    if codes.shape[1] != k:
-        raise ValueError("codes and x disagree on K")
+    n = _shape2(codes, "codes")[0]
     per_row = tuple(scales.shape) == (n,) and n > 1
     if not per_row and tuple(scales.shape) not in ((1,), ()):
         raise ValueError("scales must have shape [N] (per row) or [1] (per tensor)")
-    if y is None:
-        y = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    a, m, n, k, y = _gemv_args(x, codes, y, scales, torch.float32, lambda n, k: n if per_row else 1)
     fn = lib().fp8row_gemv_ex if per_row else lib().fp8tensor_gemv_ex
-    _check(fn(_dev(x, torch.bfloat16, "x"), m, _dev(codes, torch.uint8, "codes"),
-              _dev(scales, torch.float32, "scales"), n, k, _dev(y, torch.bfloat16, "y"), int(path),
-              _stream(stream)), "fp8row_gemv" if per_row else "fp8tensor_gemv")
+    _run(a, "fp8row_gemv" if per_row else "fp8tensor_gemv", fn, a.ptr("x"), m, a.ptr("codes"), a.ptr("scales"), n,
+         k, a.ptr("y"), int(path), stream=stream)
     return y
 
 
 def moe_gemv(x, ids, codes, scales, y=None, stream=None):
     """Grouped block-FP8 GEMV over routed experts: y[t, j] = x[t] . dequant(W[ids[t, j]])^T."""
     import torch
-    m, k = x.shape
+    m, k = _shape2(x, "x")
+    if codes.dim() != 3:
+        raise ValueError("codes must be [E, N, K]")
     e, n, k2 = codes.shape
-    topk = ids.shape[1]
+    topk = _shape2(ids, "ids")[1]
     if k2 != k or ids.shape[0] != m:
         raise ValueError("x, ids and codes disagree on M or K")
-    if y is None:
-        y = torch.empty((m, topk, n), dtype=torch.bfloat16, device=x.device)
-    _check(lib().fp8bs_moe_gemv(_dev(x, torch.bfloat16, "x"), m, _dev(ids, torch.int32, "ids"), topk,
-                                _dev(codes, torch.uint8, "codes"), _dev(scales, torch.float32, "scales"), e, n, k,
-                                _dev(y, torch.bfloat16, "y"), _stream(stream)), "fp8bs_moe_gemv")
+    y = _new(y, (m, topk, n), torch.bfloat16, x)
+    a = _Args().need("x", x, torch.bfloat16).need("ids", ids, torch.int32) \
+        .need("codes", codes, torch.uint8) \
+        .need("scales", scales, torch.float32, numel=e * cdiv(n, 128) * cdiv(k, 128)) \
+        .need("y", y, torch.bfloat16, numel=m * topk * n).check()
+    _run(a, "fp8bs_moe_gemv", lib().fp8bs_moe_gemv, a.ptr("x"), m, a.ptr("ids"), topk, a.ptr("codes"),
+         a.ptr("scales"), e, n, k, a.ptr("y"), stream=stream)
     return y
 
 
@@ -259,13 +379,16 @@ def kv_append(x, slots, scale, cache, stream=None):
     """Quantize new keys or values x [T, Hkv, 128] bf16 into the e4m3 cache
     [num_blocks, page_size, Hkv, 128] at flat token slots (in place)."""
     import torch
+    if x.dim() != 3 or cache.dim() != 4:
+        raise ValueError("x must be [T, Hkv, 128] and cache [num_blocks, page_size, Hkv, 128]")
     t, hkv, d = x.shape
     nb, page, hkv2, d2 = cache.shape
     if (hkv2, d2) != (hkv, d):
         raise ValueError("x and cache disagree on kv heads or head_dim")
-    _check(lib().fp8kv_append(_dev(x, torch.bfloat16, "x"), t, hkv, d, _dev(slots, torch.int32, "slots"),
-                              _dev(scale, torch.float32, "scale"), _dev(cache, torch.uint8, "cache"), nb * page,
-                              _stream(stream)), "fp8kv_append")
+    a = _Args().need("x", x, torch.bfloat16).need("slots", slots, torch.int32, numel=t) \
+        .need("scale", scale, torch.float32, numel=1).need("cache", cache, torch.uint8).check()
+    _run(a, "fp8kv_append", lib().fp8kv_append, a.ptr("x"), t, hkv, d, a.ptr("slots"), a.ptr("scale"),
+         a.ptr("cache"), nb * page, stream=stream)
     return cache
 
 
@@ -273,47 +396,49 @@ def kv_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_
                         sm_scale: float, out=None, stream=None):
     """Paged decode attention over the FP8 KV cache: q [B, Hq, 128] bf16."""
     import torch
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [B, Hq, 128] and the caches [num_blocks, page_size, Hkv, 128]")
     b, hq, d = q.shape
     nb, page, hkv, d2 = k_cache.shape
-    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or block_table.shape[0] != b:
+    bt_rows, max_blocks = _shape2(block_table, "block_table")
+    if d2 != d or tuple(v_cache.shape) != tuple(k_cache.shape) or bt_rows != b:
         raise ValueError("q, caches and block table disagree")
-    if out is None:
-        out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=q.device)
-    _check(lib().fp8kv_decode_attention(_dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.uint8, "k_cache"),
-                                        _dev(v_cache, torch.uint8, "v_cache"), _dev(k_scale, torch.float32, "k_scale"),
-                                        _dev(v_scale, torch.float32, "v_scale"),
-                                        _dev(block_table, torch.int32, "block_table"), block_table.shape[1],
-                                        _dev(seq_lens, torch.int32, "seq_lens"), b, hq, hkv, d, page, nb,
-                                        int(max_seq_len), float(sm_scale), _dev(out, torch.bfloat16, "out"),
-                                        _stream(stream)), "fp8kv_decode_attention")
+    out = _new(out, (b, hq, d), torch.bfloat16, q)
+    a = _Args().need("q", q, torch.bfloat16).need("k_cache", k_cache, torch.uint8) \
+        .need("v_cache", v_cache, torch.uint8).need("k_scale", k_scale, torch.float32, numel=1) \
+        .need("v_scale", v_scale, torch.float32, numel=1).need("block_table", block_table, torch.int32) \
+        .need("seq_lens", seq_lens, torch.int32, numel=b).need("out", out, torch.bfloat16, numel=b * hq * d).check()
+    _run(a, "fp8kv_decode_attention", lib().fp8kv_decode_attention, a.ptr("q"), a.ptr("k_cache"),
+         a.ptr("v_cache"), a.ptr("k_scale"), a.ptr("v_scale"), a.ptr("block_table"), max_blocks,
+         a.ptr("seq_lens"), b, hq, hkv, d, page, nb, int(max_seq_len), float(sm_scale), a.ptr("out"), stream=stream)
     return out
 
 
 def act_quantize(x, codes=None, scale=None, stream=None):
     """Dynamic per-tensor e4m3 quantization of bf16 activations [M, K]."""
     import torch
-    m, k = x.shape
-    if codes is None:
-        codes = torch.empty((m, k), dtype=torch.uint8, device=x.device)
-    if scale is None:
-        scale = torch.empty((1,), dtype=torch.float32, device=x.device)
-    _check(lib().fp8act_quantize(_dev(x, torch.bfloat16, "x"), m, k, _dev(codes, torch.uint8, "codes"),
-                                 _dev(scale, torch.float32, "scale"), _stream(stream)), "fp8act_quantize")
+    m, k = _shape2(x, "x")
+    codes = _new(codes, (m, k), torch.uint8, x)
+    scale = _new(scale, (1,), torch.float32, x)
+    a = _Args().need("x", x, torch.bfloat16).need("codes", codes, torch.uint8, numel=m * k) \
+        .need("scale", scale, torch.float32, numel=1).check()
+    _run(a, "fp8act_quantize", lib().fp8act_quantize, a.ptr("x"), m, k, a.ptr("codes"), a.ptr("scale"),
+         stream=stream)
     return codes, scale
 
 
 def w8a8_gemm(xq, sx, wq, sw, y=None, path: int = PATH_AUTO, stream=None):
     """y[M, N] = sx * sw * dec(xq) . dec(wq)^T (e4m3 x e4m3, fp32 accumulate, bf16 out)."""
     import torch
-    m, k = xq.shape
-    n = wq.shape[0]
-    if wq.shape[1] != k:
+    m, k = _shape2(xq, "xq")
+    n, k2 = _shape2(wq, "wq")
+    if k2 != k:
         raise ValueError("x codes and weight codes disagree on K")
-    if y is None:
-        y = torch.empty((m, n), dtype=torch.bfloat16, device=xq.device)
-    _check(lib().w8a8_gemm_ex(_dev(xq, torch.uint8, "xq"), m, _dev(sx, torch.float32, "sx"),
-                              _dev(wq, torch.uint8, "wq"), _dev(sw, torch.float32, "sw"), n, k,
-                              _dev(y, torch.bfloat16, "y"), int(path), _stream(stream)), "w8a8_gemm")
+    y = _new(y, (m, n), torch.bfloat16, xq)
+    a = _Args().need("xq", xq, torch.uint8).need("sx", sx, torch.float32, numel=1).need("wq", wq, torch.uint8) \
+        .need("sw", sw, torch.float32, numel=1).need("y", y, torch.bfloat16, numel=m * n).check()
+    _run(a, "w8a8_gemm", lib().w8a8_gemm_ex, a.ptr("xq"), m, a.ptr("sx"), a.ptr("wq"), a.ptr("sw"), n, k,
+         a.ptr("y"), int(path), stream=stream)
     return y
 
 
@@ -343,8 +468,8 @@ def debug_encode_f32(first_bits: int, count: int, out=None, stream=None):
         out = torch.empty(count, dtype=torch.uint8, device="cuda")
     if out.numel() < count:
         raise ValueError("out holds fewer than count bytes")
-    _check(lib().fp8bs_debug_encode_f32(first_bits, count, _dev(out, torch.uint8, "out"), _stream(stream)),
-           "fp8bs_debug_encode_f32")
+    a = _Args().need("out", out, torch.uint8).check()
+    _run(a, "fp8bs_debug_encode_f32", lib().fp8bs_debug_encode_f32, first_bits, count, a.ptr("out"), stream=stream)
     return out
 
 

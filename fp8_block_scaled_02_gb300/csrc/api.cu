@@ -70,6 +70,85 @@ int gemv_dispatch(const DecodeArgs &a, int path, cudaStream_t st) {
     }
 }
 
+// ------------------------------------------------------------ batches
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+inline Range range_of(const void *p, int64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+inline bool overlap(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// What one op of a batch reads and writes.
+struct OpSpan {
+    Range x, codes, scales, y;
+};
+OpSpan span_of(const fp8bs_gemv_op &o, int64_t m, bool mx) {
+    const int64_t sb = mx ? o.n * ((o.k + 31) / 32) : 4 * ((o.n + 127) / 128) * ((o.k + 127) / 128);
+    return OpSpan{range_of(o.x_bf16, 2 * m * o.k), range_of(o.codes, o.n * o.k), range_of(o.scales, sb),
+                  range_of(o.y_bf16, 2 * m * o.n)};
+}
+// b must wait for a if b writes what a reads or writes, or reads what a writes
+bool depends(const OpSpan &b, const OpSpan &a) {
+    return overlap(b.y, a.x) || overlap(b.y, a.codes) || overlap(b.y, a.scales) || overlap(b.y, a.y) ||
+           overlap(b.x, a.y) || overlap(b.codes, a.y) || overlap(b.scales, a.y);
+}
+
+int gemv_batch_impl(const fp8bs_gemv_op *ops, int64_t count, int64_t m, bool mx, int path, cudaStream_t st) {
+    if (count < 0 || count >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (path < FP8BS_PATH_AUTO || path > FP8BS_PATH_GENERIC) return FP8BS_ERR_PATH;
+    if (count == 0) return FP8BS_OK;
+    if (!ops) return FP8BS_ERR_NULL;
+    // validate everything before anything is enqueued
+    for (int64_t i = 0; i < count; ++i) {
+        const fp8bs_gemv_op &o = ops[i];
+        const int s = check_gemv_args(o.x_bf16, m, o.codes, o.scales, o.n, o.k, o.y_bf16, path);
+        if (s != FP8BS_OK) return s;
+        if (m == 0) continue;
+        if (!mx && !aligned(o.scales, 4)) return FP8BS_ERR_ALIGN;
+        const bool tma = tma_ok(o.k, o.x_bf16, o.codes);
+        if ((path == FP8BS_PATH_DECODE && !tma) || (path == FP8BS_PATH_PREFILL && (mx || !tma)))
+            return FP8BS_ERR_PATH;
+    }
+    if (m == 0) return FP8BS_OK;
+    const ScaleKind kind = mx ? kScaleMx : kScaleBlock;
+    const bool batchable_path = path == FP8BS_PATH_AUTO || path == FP8BS_PATH_DECODE;
+    BatchItem run[kBatchMaxOps];
+    OpSpan spans[kBatchMaxOps];
+    int nrun = 0;
+    auto flush = [&]() -> int {
+        if (nrun == 0) return FP8BS_OK;
+        const cudaError_t e = launch_decode_batch(run, nrun, m, kind, path == FP8BS_PATH_DECODE, st);
+        nrun = 0;
+        return cuda_status(e);
+    };
+    for (int64_t i = 0; i < count; ++i) {
+        const fp8bs_gemv_op &o = ops[i];
+        const bool eligible = batchable_path && m <= kDecodeMaxM && tma_ok(o.k, o.x_bf16, o.codes);
+        if (!eligible) {
+            int s = flush();
+            if (s != FP8BS_OK) return s;
+            const DecodeArgs a{o.x_bf16, o.codes, mx ? nullptr : static_cast<const float *>(o.scales),
+                               mx ? static_cast<const uint8_t *>(o.scales) : nullptr, o.y_bf16, m, o.n, o.k, kind, 0};
+            s = gemv_dispatch(a, path, st);
+            if (s != FP8BS_OK) return s;
+            continue;
+        }
+        const OpSpan sp = span_of(o, m, mx);
+        bool dep = nrun == kBatchMaxOps;
+        for (int j = 0; j < nrun && !dep; ++j) dep = depends(sp, spans[j]);
+        if (dep) {
+            const int s = flush();
+            if (s != FP8BS_OK) return s;
+        }
+        run[nrun] = BatchItem{o.x_bf16, o.codes, o.scales, o.y_bf16, o.n, o.k};
+        spans[nrun] = sp;
+        ++nrun;
+    }
+    return flush();
+}
+
 int run_w8a8_decode_chunks(const W8A8Args &a, cudaStream_t st) {
     for (int64_t m0 = 0; m0 < a.m; m0 += kDecodeMaxM) {
         W8A8Args c = a;
@@ -85,7 +164,7 @@ int run_w8a8_decode_chunks(const W8A8Args &a, cudaStream_t st) {
 
 extern "C" {
 
-int fp8bs_version(void) { return 105; }
+int fp8bs_version(void) { return 106; }
 
 const char *fp8bs_strerror(int status) {
     switch (status) {
@@ -148,6 +227,22 @@ int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const uin
 int mxfp8_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const uint8_t *scales_e8m0, int64_t n,
                int64_t k, void *y_bf16, void *stream) {
     return mxfp8_gemv_ex(x_bf16, m, codes, scales_e8m0, n, k, y_bf16, FP8BS_PATH_AUTO, stream);
+}
+
+int fp8bs_gemv_batch_ex(const fp8bs_gemv_op *ops, int64_t count, int64_t m, int path, void *stream) {
+    return gemv_batch_impl(ops, count, m, false, path, static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_gemv_batch(const fp8bs_gemv_op *ops, int64_t count, int64_t m, void *stream) {
+    return gemv_batch_impl(ops, count, m, false, FP8BS_PATH_AUTO, static_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_gemv_batch_ex(const fp8bs_gemv_op *ops, int64_t count, int64_t m, int path, void *stream) {
+    return gemv_batch_impl(ops, count, m, true, path, static_cast<cudaStream_t>(stream));
+}
+
+int mxfp8_gemv_batch(const fp8bs_gemv_op *ops, int64_t count, int64_t m, void *stream) {
+    return gemv_batch_impl(ops, count, m, true, FP8BS_PATH_AUTO, static_cast<cudaStream_t>(stream));
 }
 
 static int rowwise_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *codes_u8, float *scales_f32,

@@ -54,6 +54,7 @@
 #include "common.cuh"
 #include "internal.h"
 
+#include <cstring>
 #include <mutex>
 
 namespace fp8bs {
@@ -108,6 +109,27 @@ struct Cfg {
     static_assert((kStages * kAuxBytes + kRedBytes + kRecvBytes) % 8 == 0, "barriers must stay 8-byte aligned");
     static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
+
+// The op table of a batched launch.  It travels in the kernel's parameter
+// space (no device buffer to allocate or fill), so its size is bounded by the
+// 32 KB parameter limit: kBatchMaxOps ops per launch.  The tensor maps keep
+// their own arrays (128-byte aligned, no padding between them).
+struct BatchOp {
+    const float *scales;     // block or row scales, else nullptr
+    const uint8_t *e8m0;     // MX exponents, else nullptr
+    __nv_bfloat16 *y;        // bf16 [m, n]
+    int n, kblocks, groups;
+    int ntiles;              // 128-row tiles of this weight
+    int unit0;               // index of its first tile in the batch's unit list
+    int e8m0_vec, row_stride;
+};
+struct BatchParams {
+    CUtensorMap tm_codes[kBatchMaxOps];  // e4m3 [n, k], 128x128 boxes, 128-byte swizzle
+    CUtensorMap tm_x[kBatchMaxOps];      // bf16 [m, k], 64 x (8 * MT) boxes
+    BatchOp ops[kBatchMaxOps];
+    int count, units;
+};
+static_assert(sizeof(BatchParams) + 64 <= 32764, "the op table must fit the kernel parameter space");
 
 __device__ __forceinline__ float pow2_e8m0(uint32_t E) {
     return E ? __uint_as_float(E << 23) : __uint_as_float(0x00400000u);
@@ -164,32 +186,50 @@ __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r,
     xinv[sl * kXRows + xinv_slot(r)] = inv;
 }
 
-// One CTA processes row tiles blockIdx.x, blockIdx.x + gridDim.x, ... (all
-// of them for its K range [kb0, kb1)).  With splits == 1 the grid is
-// persistent and the TMA ring streams across tile boundaries, so the next
-// tile's codes are already arriving while the consumers reduce and store the
-// previous tile.  With splits > 1 each CTA owns exactly one row tile and the
-// cluster reduces over K.
+// The units a CTA works on.  A unit is one 128-row tile of one weight over a
+// range of its 128-wide K blocks.
+//  * One weight (BATCH = false): the CTA takes row tiles blockIdx.x,
+//    blockIdx.x + gridDim.x, ... over the K range of its split.  With
+//    splits == 1 the grid is persistent and the TMA ring streams across tile
+//    boundaries, so the next tile's codes are already arriving while the
+//    consumers store the previous tile; with splits > 1 each CTA owns one row
+//    tile and the cluster reduces over K.
+//  * A batch of weights (BATCH = true): the row tiles of all the ops, in op
+//    order, form one list of units, each over the whole of its weight's K;
+//    the CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...  The ring
+//    streams across unit and op boundaries alike, so a sequence of GEMVs runs
+//    as one continuous weight stream instead of one launch (with its start-up
+//    and tail) per weight.
+// Per-op view of what the roles read: the tensor maps and the scale and
+// output pointers and sizes of one weight.
+struct OpRef {
+    const CUtensorMap *tm_codes;
+    const CUtensorMap *tm_x;
+    const float *scales;     // block [ceil(n/128), kblocks] or row scales (scales[row * row_stride])
+    const uint8_t *e8m0;     // MX exponents [n, groups]
+    __nv_bfloat16 *y;        // [m, n]
+    int n, kblocks, groups, e8m0_vec, row_stride;
+};
+
 // SC: how the weight is scaled (ScaleKind: 128x128 blocks, MX groups, rows)
 // MOE: grouped expert GEMV (block scales); n is the rows of one expert, the
 // codes / scales hold num_experts such weights back to back, ids [m, topk].
-template <int MT, int SC, bool F16, bool MOE = false>
-__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
-                  const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
-                  int m, int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec, int row_stride,
-                  const int32_t *__restrict__ ids, int topk, int num_experts) {
+// BATCH: the ops come from `bp` (the single-weight arguments are unused).
+template <int MT, int SC, bool F16, bool MOE, bool BATCH>
+__device__ __forceinline__ void decode_body(const BatchParams *bp, const CUtensorMap *tm_codes,
+                                            const CUtensorMap *tm_x, const float *__restrict__ scales,
+                                            const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
+                                            int m, int n, int kblocks, int groups, int splits, int ntiles,
+                                            int e8m0_vec, int row_stride, const int32_t *__restrict__ ids,
+                                            int topk, int num_experts) {
     constexpr bool MX = SC == kScaleMx;
     constexpr bool ROW = SC == kScaleRow;  // no per-K-block scale; scales[row * row_stride] at the end
     // no per-slice factor (e8m0 groups): the MMAs accumulate a whole K block
     constexpr bool kWholeBlock = !MX;
     // ... and with bf16 operands and one scale per row, all of K
     constexpr bool kDirect = kWholeBlock && ROW && !F16;
+    static_assert(!(MOE && BATCH), "a grouped MoE call is one launch of its own");
     using C = Cfg<MT, MX, F16>;
-    // factor applied to a finished fp32 sum of weight row nn before rounding
-    auto out_scale = [&](int nn) -> float {
-        return ROW ? __ldg(scales + static_cast<int64_t>(nn) * row_stride) : 1.0f;
-    };
     constexpr int kStages = C::kStages;
     constexpr int kBN = C::kBN;
     extern __shared__ uint8_t smem_raw[];
@@ -203,17 +243,42 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
     uint64_t *empty = xready + kStages;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.y;
-    const int kb0 = static_cast<int>((static_cast<int64_t>(split) * kblocks) / splits);
-    const int kb1 = static_cast<int>((static_cast<int64_t>(split + 1) * kblocks) / splits);
-    const int nkb = kb1 - kb0;
+    // one weight: this CTA's K range (split-K); a batch: every unit runs all of K
+    const int split = BATCH ? 0 : static_cast<int>(blockIdx.y);
+    const int kb0 = BATCH ? 0 : static_cast<int>((static_cast<int64_t>(split) * kblocks) / splits);
+    const int kb1 = BATCH ? 0 : static_cast<int>((static_cast<int64_t>(split + 1) * kblocks) / splits);
     const int tile0 = blockIdx.x, tstep = gridDim.x;
-    const int my_tiles = tile0 < ntiles ? (ntiles - tile0 + tstep - 1) / tstep : 0;
-    const int total = my_tiles * nkb;
+    const int nunits = BATCH ? bp->units : ntiles;
+    const int my_units = tile0 < nunits ? (nunits - tile0 + tstep - 1) / tstep : 0;
     const int mm = min(m, C::kXRows);
     __shared__ uint32_t s_bits[kMoeMaxExperts / 32];  // MOE: experts any token selected
     __shared__ int s_expert;                          // MOE: this CTA's expert
     __shared__ signed char s_route[32];               // MOE: slot j of x row mi for it, -1 if none
+
+    // Unit i of this CTA: its op (BATCH: `op` is a cursor that only moves
+    // forward, units are visited in increasing order), first weight row and
+    // K blocks [kbb, kbb + nkb).
+    auto locate = [&](int i, int &op, int &n0, int &kbb, int &nkb) {
+        const int u = tile0 + i * tstep;
+        if (BATCH) {
+            while (u >= bp->ops[op].unit0 + bp->ops[op].ntiles) ++op;
+            n0 = (u - bp->ops[op].unit0) * kBN;
+            kbb = 0;
+            nkb = bp->ops[op].kblocks;
+        } else {
+            n0 = u * kBN;
+            kbb = kb0;
+            nkb = kb1 - kb0;
+        }
+    };
+    auto op_ref = [&](int op) -> OpRef {
+        if (BATCH) {
+            const BatchOp &o = bp->ops[op];
+            return OpRef{&bp->tm_codes[op], &bp->tm_x[op], o.scales, o.e8m0, o.y, o.n, o.kblocks, o.groups, o.e8m0_vec,
+                         o.row_stride};
+        }
+        return OpRef{tm_codes, tm_x, scales, e8m0, y, n, kblocks, groups, e8m0_vec, row_stride};
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -224,17 +289,27 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
         fence_mbarrier_init();
     }
     if (warp == kWarpTma && lane == 0) {
-        prefetch_tensormap(&tm_codes);
-        prefetch_tensormap(&tm_x);
+        if (!BATCH) {
+            prefetch_tensormap(tm_codes);
+            prefetch_tensormap(tm_x);
+        }
         // While the previous kernel drains, start this CTA's first ring-depth
         // of weight tiles on their way into L2 (more would delay the first
         // loads when there is nothing to overlap; MoE CTAs do not know their
         // expert yet).
         if (!MOE) {
-            const int npf = min(total, kStages);
-            for (int it = 0; it < npf; ++it) {
-                const int ti = it / nkb;
-                tma_prefetch_l2_2d(&tm_codes, (kb0 + (it - ti * nkb)) * kKB, (tile0 + ti * tstep) * kBN);
+            int left = kStages, op = 0, prev = -1;
+            for (int i = 0; i < my_units && left > 0; ++i) {
+                int n0, kbb, nkb;
+                locate(i, op, n0, kbb, nkb);
+                const OpRef o = op_ref(op);
+                if (BATCH && op != prev) {
+                    prefetch_tensormap(o.tm_codes);
+                    prefetch_tensormap(o.tm_x);
+                    prev = op;
+                }
+                for (int kb = 0; kb < nkb && left > 0; ++kb, --left)
+                    tma_prefetch_l2_2d(o.tm_codes, (kbb + kb) * kKB, n0);
             }
         }
     }
@@ -284,71 +359,90 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
         // CTA of a cluster shares blockIdx.z, so the whole cluster leaves
         if (expert < 0) return;
         if (threadIdx.x < 32) {
-            int r = -1;
+            int r = -1, hits = 0;
             if (threadIdx.x < m)
                 for (int j = topk - 1; j >= 0; --j)
-                    if (__ldg(ids + threadIdx.x * topk + j) == expert) r = j;
+                    if (__ldg(ids + threadIdx.x * topk + j) == expert) {
+                        r = j;
+                        ++hits;
+                    }
+            // a token that lists this expert twice breaks the distinct-ids
+            // precondition: only the lowest slot would be written
+            if (hits > 1) atomicOr(&g_decode_err, ERRBIT_INDEX);
             s_route[threadIdx.x] = static_cast<signed char>(r);
         }
         __syncthreads();
     }
-    // flat index into y of output (x row mi, weight row nn), or -1 if not stored
-    auto out_at = [&](int mi, int nn) -> int64_t {
-        if (!MOE) return static_cast<int64_t>(mi) * n + nn;
+    // flat index into y of output (x row mi, weight row nn) of a weight with
+    // `nrows` rows, or -1 if not stored
+    auto out_at = [&](int mi, int nn, int nrows) -> int64_t {
+        if (!MOE) return static_cast<int64_t>(mi) * nrows + nn;
         const int j = s_route[mi];
-        return j < 0 ? -1 : (static_cast<int64_t>(mi) * topk + j) * n + nn;
+        return j < 0 ? -1 : (static_cast<int64_t>(mi) * topk + j) * nrows + nn;
     };
     const int row_base = MOE ? expert * n : 0;  // expert's first row in the stacked codes
-    const float *scale_base =
-        MOE ? scales + static_cast<int64_t>(expert) * ((n + 127) >> 7) * kblocks : scales;
+    const int64_t scale_off = MOE ? static_cast<int64_t>(expert) * ((n + 127) >> 7) * kblocks : 0;
 
     if (warp == kWarpTma) {
         // ------------------------------------------------------ TMA producer
         // The whole warp walks the ring (so it stays converged); lane 0
         // waits for a free stage and issues the TMA copies.
         const uint64_t stream_policy = policy_evict_first();
-        for (int it = 0; it < total; ++it) {
-            const int s = it % kStages;
-            int good = 1;
-            if (it >= kStages && lane == 0) good = mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1);
-            good = __shfl_sync(0xffffffffu, good, 0);
-            if (!good) {
-                if (lane == 0) atomicOr(&g_decode_err, ERRBIT_EMPTY_WAIT);
-                break;
+        int it = 0, op = 0;
+        bool stop = false;
+        for (int i = 0; i < my_units && !stop; ++i) {
+            int n0, kbb, nkb;
+            locate(i, op, n0, kbb, nkb);
+            const OpRef o = op_ref(op);
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int s = it % kStages;
+                int good = 1;
+                if (it >= kStages && lane == 0) good = mbar_wait_bounded(&empty[s], ((it / kStages) - 1) & 1);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    if (lane == 0) atomicOr(&g_decode_err, ERRBIT_EMPTY_WAIT);
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    const int kx = (kbb + kb) * kKB;
+                    uint8_t *st = smem + s * C::kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                    tma_load_2d_hint(st, o.tm_codes, &full[s], kx, row_base + n0, stream_policy);
+                    tma_load_2d(st + C::kCodeBytes, o.tm_x, &full[s], kx, 0);
+                    tma_load_2d(st + C::kCodeBytes + C::kXPanelBytes, o.tm_x, &full[s], kx + 64, 0);
+                }
+                __syncwarp();
             }
-            if (lane == 0) {
-                const int ti = it / nkb;
-                const int n0 = (tile0 + ti * tstep) * kBN;
-                const int kx = (kb0 + (it - ti * nkb)) * kKB;
-                uint8_t *st = smem + s * C::kStageBytes;
-                mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-                tma_load_2d_hint(st, &tm_codes, &full[s], kx, row_base + n0, stream_policy);
-                tma_load_2d(st + C::kCodeBytes, &tm_x, &full[s], kx, 0);
-                tma_load_2d(st + C::kCodeBytes + C::kXPanelBytes, &tm_x, &full[s], kx + 64, 0);
-            }
-            __syncwarp();
         }
     } else if (C::kConv && warp >= kWarpConv0) {
         // ------------------------------------------------------ x converter
         const int clane = (warp - kWarpConv0) * 32 + lane;
         constexpr int kConvLanes = C::kConvWarps * 32;
-        for (int it = 0; it < total; ++it) {
-            const int s = it % kStages;
-            const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
-            if (!__all_sync(0xffffffffu, ready)) {
-                // the consumers' own bounded waits on xready then give up too
-                if (lane == 0) atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
-                break;
+        int it = 0, op = 0;
+        bool stop = false;
+        for (int i = 0; i < my_units && !stop; ++i) {
+            int n0, kbb, nkb;
+            locate(i, op, n0, kbb, nkb);
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const int s = it % kStages;
+                const bool ready = mbar_wait_bounded(&full[s], (it / kStages) & 1);
+                if (!__all_sync(0xffffffffu, ready)) {
+                    // the consumers' own bounded waits on xready then give up too
+                    if (lane == 0) atomicOr(&g_decode_err, ERRBIT_FULL_WAIT);
+                    stop = true;
+                    break;
+                }
+                uint8_t *xs = smem + s * C::kStageBytes + C::kCodeBytes;
+                float *xinv = aux + s * C::kXInvFloats;
+                static_assert(!C::kConv || MX || 4 * C::kXRows == kConvLanes,
+                              "a per-block rescale needs one slice per lane");
+                for (int u = clane; u < 4 * C::kXRows; u += kConvLanes)
+                    convert_x_slice<C::kXPanelBytes, C::kXRows, !MX>(xs, xinv, u >> 2, u & 3);
+                fence_proxy_async_smem();  // the TMA will overwrite these bytes later
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xready[s]);
             }
-            uint8_t *xs = smem + s * C::kStageBytes + C::kCodeBytes;
-            float *xinv = aux + s * C::kXInvFloats;
-            static_assert(!C::kConv || MX || 4 * C::kXRows == kConvLanes,
-                          "a per-block rescale needs one slice per lane");
-            for (int u = clane; u < 4 * C::kXRows; u += kConvLanes)
-                convert_x_slice<C::kXPanelBytes, C::kXRows, !MX>(xs, xinv, u >> 2, u & 3);
-            fence_proxy_async_smem();  // the TMA will overwrite these bytes later
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xready[s]);
         }
     } else {
         // ------------------------------------------------------ consumers
@@ -358,9 +452,18 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
         // pi(g) = (g >> 1) | ((g & 1) << 2) (bank-conflict-free swizzle use)
         const int xrow_base = (g >> 1) | ((g & 1) << 2);
         const int coff = (t & 1) * 8;
-        for (int ti = 0; ti < my_tiles; ++ti) {
-            const int n0 = (tile0 + ti * tstep) * kBN;
-            const float *srow = (MX || ROW) ? nullptr : scale_base + static_cast<int64_t>(n0 >> 7) * kblocks + kb0;
+        int it = 0, op = 0;
+        bool failed = false;
+        for (int ui = 0; ui < my_units && !failed; ++ui) {
+            int n0, kbb, nkb;
+            locate(ui, op, n0, kbb, nkb);
+            const OpRef o = op_ref(op);
+            // factor applied to a finished fp32 sum of weight row nn before rounding
+            auto out_scale = [&](int nn) -> float {
+                return ROW ? __ldg(o.scales + static_cast<int64_t>(nn) * o.row_stride) : 1.0f;
+            };
+            const float *srow = (MX || ROW) ? nullptr
+                                            : o.scales + scale_off + static_cast<int64_t>(n0 >> 7) * o.kblocks + kbb;
             float acc[MT][4];
 #pragma unroll
             for (int j = 0; j < MT; ++j)
@@ -371,24 +474,22 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
             // weight row 16*warp + l, fetched one K block ahead
             auto load_e8m0_word = [&](int kbi) -> uint32_t {
                 const int64_t row = static_cast<int64_t>(n0) + warp * 16 + lane;
-                const int g0 = (kb0 + kbi) * 4;
+                const int g0 = (kbb + kbi) * 4;
                 uint32_t w = 0;
-                if (lane < 16 && row < n) {
-                    const uint8_t *p = e8m0 + row * groups + g0;
-                    if (e8m0_vec) {
+                if (lane < 16 && row < o.n) {
+                    const uint8_t *p = o.e8m0 + row * o.groups + g0;
+                    if (o.e8m0_vec) {
                         w = __ldg(reinterpret_cast<const uint32_t *>(p));
                     } else {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            if (g0 + q < groups) w |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
+                            if (g0 + q < o.groups) w |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
                     }
                 }
                 return w;
             };
             uint32_t e_next = MX ? load_e8m0_word(0) : 0u;
-            bool failed = false;
-            for (int kbi = 0; kbi < nkb; ++kbi) {
-                const int it = ti * nkb + kbi;
+            for (int kbi = 0; kbi < nkb; ++kbi, ++it) {
                 const int s = it % kStages;
                 const float sblk = s_next;
                 if (!MX && !ROW && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
@@ -520,15 +621,16 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
                     const int mi = 8 * j + t + 4 * (q & 1);
                     const int nl = ra + (q >> 1);
                     if (splits == 1) {
-                        const int64_t o = (mi < m && n0 + nl < n) ? out_at(mi, n0 + nl) : -1;
-                        if (o >= 0) y[o] = __float2bfloat16_rn(ROW ? acc[j][q] * out_scale(n0 + nl) : acc[j][q]);
+                        const int64_t oi = (mi < m && n0 + nl < o.n) ? out_at(mi, n0 + nl, o.n) : -1;
+                        if (oi >= 0)
+                            o.y[oi] = __float2bfloat16_rn(ROW ? acc[j][q] * out_scale(n0 + nl) : acc[j][q]);
                     } else {
                         red[nl * C::kRedStride + mi] = acc[j][q];
                     }
                 }
         }
     }
-    if (splits == 1) return;
+    if (BATCH || splits == 1) return;
 
     // Split-K: one row tile per CTA; reduce across the cluster in rank order.
     // CTA r finishes rows [r * rows_per, (r + 1) * rows_per) of the tile.
@@ -559,14 +661,32 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
         const int mi = e / my_rows;
         const int rl = e - mi * my_rows;
         const int nn = n0 + r_begin + rl;
-        const int64_t o = nn < n ? out_at(mi, nn) : -1;
-        if (o < 0) continue;
+        const int64_t oi = nn < n ? out_at(mi, nn, n) : -1;
+        if (oi < 0) continue;
         float sum = 0.0f;
 #pragma unroll
         for (int q = 0; q < kMaxSplit; ++q)
             if (q < splits) sum += recv[(q * rows_per + rl) * C::kRedStride + mi];
-        y[o] = __float2bfloat16_rn(ROW ? sum * out_scale(nn) : sum);
+        y[oi] = __float2bfloat16_rn(ROW ? sum * __ldg(scales + static_cast<int64_t>(nn) * row_stride) : sum);
     }
+}
+
+template <int MT, int SC, bool F16, bool MOE = false>
+__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
+                  const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
+                  int m, int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec, int row_stride,
+                  const int32_t *__restrict__ ids, int topk, int num_experts) {
+    decode_body<MT, SC, F16, MOE, false>(nullptr, &tm_codes, &tm_x, scales, e8m0, y, m, n, kblocks, groups, splits,
+                                         ntiles, e8m0_vec, row_stride, ids, topk, num_experts);
+}
+
+// A batch of independent GEMVs with the same m in one persistent launch.
+template <int MT, int SC, bool F16>
+__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
+    gemv_batch_kernel(const __grid_constant__ BatchParams p, int m) {
+    decode_body<MT, SC, F16, false, true>(&p, nullptr, nullptr, nullptr, nullptr, nullptr, m, 0, 0, 0, 1, 0, 0, 0,
+                                          nullptr, 0, 0);
 }
 
 // Per-device, per-instantiation launch setup (shared-memory opt-in and the
@@ -579,28 +699,35 @@ struct Setup {
     ClusterFit fit;
 };
 
+// Shared-memory opt-in and resident CTAs per SM of one kernel instantiation
+// on the current device (done once per device).
+cudaError_t setup_once(Setup &setup, const void *kern, int threads, int smem, int &resident) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(setup.mu);
+    if (!setup.done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        int blocks = 0;
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, threads, smem);
+        setup.err[dev] = e;
+        setup.resident[dev] = blocks > 0 ? blocks : 1;
+        setup.done[dev] = true;
+    }
+    resident = setup.resident[dev];
+    return setup.err[dev];
+}
+
 template <int MT, int SC, bool F16>
 cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     using C = Cfg<MT, SC == kScaleMx, F16>;
     constexpr int kBN = C::kBN;
     auto kern = decode_kernel<MT, SC, F16>;
     static Setup setup;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int resident = 1;
     {
-        std::lock_guard<std::mutex> lock(setup.mu);
-        if (!setup.done[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-            int blocks = 0;
-            if (e == cudaSuccess)
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, C::kThreads, C::kSmemBytes);
-            setup.err[dev] = e;
-            setup.resident[dev] = blocks > 0 ? blocks : 1;
-            setup.done[dev] = true;
-        }
-        if (setup.err[dev] != cudaSuccess) return setup.err[dev];
-        resident = setup.resident[dev];
+        const cudaError_t e =
+            setup_once(setup, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes, resident);
+        if (e != cudaSuccess) return e;
     }
 
     CUtensorMap tm_codes, tm_x;
@@ -654,6 +781,76 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
                               static_cast<const int32_t *>(nullptr), 0, 0);
 }
 
+// A batch launch: one persistent grid over the row tiles of all the ops.
+template <int MT, int SC, bool F16>
+cudaError_t launch_batch_t(const BatchItem *ops, int count, int64_t m, bool force, cudaStream_t stream) {
+    using C = Cfg<MT, SC == kScaleMx, F16>;
+    constexpr int kBN = C::kBN;
+    auto kern = gemv_batch_kernel<MT, SC, F16>;
+    static Setup setup;
+    int resident = 1;
+    {
+        const cudaError_t e =
+            setup_once(setup, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes, resident);
+        if (e != cudaSuccess) return e;
+    }
+    int64_t units = 0;
+    for (int i = 0; i < count; ++i) units += (ops[i].n + kBN - 1) / kBN;
+    const int capacity = device_sm_count() * resident;
+    // One op, or too few row tiles to keep the SMs streaming with whole-K
+    // units: the single-weight launches (split-K clusters) do better.
+    if (!force && (count == 1 || units * 2 < capacity)) {
+        for (int i = 0; i < count; ++i) {
+            DecodeArgs a{ops[i].x, ops[i].codes, SC == kScaleMx ? nullptr : static_cast<const float *>(ops[i].scales),
+                         SC == kScaleMx ? static_cast<const uint8_t *>(ops[i].scales) : nullptr,
+                         ops[i].y, m, ops[i].n, ops[i].k, static_cast<ScaleKind>(SC), 0};
+            const cudaError_t e = launch_t<MT, SC, F16>(a, stream);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    if (units >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+
+    BatchParams p;
+    memset(&p, 0, sizeof p);
+    int unit0 = 0;
+    for (int i = 0; i < count; ++i) {
+        const BatchItem &it = ops[i];
+        BatchOp &o = p.ops[i];
+        const uint64_t n = static_cast<uint64_t>(it.n), k = static_cast<uint64_t>(it.k);
+        if (!encode_tensor_map_2d(&p.tm_codes[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, it.codes, k, n, k, kKB, kBN,
+                                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tensor_map_2d(&p.tm_x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, it.x, k, static_cast<uint64_t>(m),
+                                  k * 2, 64, C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        o.scales = SC == kScaleMx ? nullptr : static_cast<const float *>(it.scales);
+        o.e8m0 = SC == kScaleMx ? static_cast<const uint8_t *>(it.scales) : nullptr;
+        o.y = static_cast<__nv_bfloat16 *>(it.y);
+        o.n = static_cast<int>(it.n);
+        o.kblocks = static_cast<int>((it.k + kKB - 1) / kKB);
+        o.groups = static_cast<int>((it.k + 31) / 32);
+        o.ntiles = static_cast<int>((it.n + kBN - 1) / kBN);
+        o.unit0 = unit0;
+        unit0 += o.ntiles;
+        o.e8m0_vec = (o.groups % 4 == 0 && (reinterpret_cast<uintptr_t>(o.e8m0) & 3) == 0) ? 1 : 0;
+        o.row_stride = 0;
+    }
+    p.count = count;
+    p.units = unit0;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(unit0 < capacity ? unit0 : capacity), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, static_cast<int>(m));
+}
+
 // Grouped MoE launch: grid (row tiles of one expert, K splits, expert slots).
 template <int MT, bool F16>
 cudaError_t launch_moe_t(const DecodeArgs &a, const MoeArgs &g, cudaStream_t stream) {
@@ -661,22 +858,11 @@ cudaError_t launch_moe_t(const DecodeArgs &a, const MoeArgs &g, cudaStream_t str
     constexpr int kBN = C::kBN;
     auto kern = decode_kernel<MT, kScaleBlock, F16, true>;
     static Setup setup;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int resident = 1;
     {
-        std::lock_guard<std::mutex> lock(setup.mu);
-        if (!setup.done[dev]) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-            int blocks = 0;
-            if (e == cudaSuccess)
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, C::kThreads, C::kSmemBytes);
-            setup.err[dev] = e;
-            setup.resident[dev] = blocks > 0 ? blocks : 1;
-            setup.done[dev] = true;
-        }
-        if (setup.err[dev] != cudaSuccess) return setup.err[dev];
-        resident = setup.resident[dev];
+        const cudaError_t e =
+            setup_once(setup, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes, resident);
+        if (e != cudaSuccess) return e;
     }
     CUtensorMap tm_codes, tm_x;
     const uint64_t rows = static_cast<uint64_t>(g.num_experts) * static_cast<uint64_t>(a.n);
@@ -739,6 +925,17 @@ cudaError_t launch_sc(const DecodeArgs &a, cudaStream_t stream) {
     }
 }
 
+template <int SC>
+cudaError_t launch_batch_sc(const BatchItem *ops, int count, int64_t m, bool force, cudaStream_t stream) {
+    switch ((m + 7) / 8) {
+        case 1: return launch_batch_t<1, SC, true>(ops, count, m, force, stream);
+        case 2: return launch_batch_t<2, SC, false>(ops, count, m, force, stream);
+        case 3: return launch_batch_t<3, SC, false>(ops, count, m, force, stream);
+        case 4: return launch_batch_t<4, SC, false>(ops, count, m, force, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_t stream) {
@@ -756,6 +953,16 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {
         case kScaleBlock: return launch_sc<kScaleBlock>(a, stream);
         case kScaleMx: return launch_sc<kScaleMx>(a, stream);
         case kScaleRow: return launch_sc<kScaleRow>(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode_batch(const BatchItem *ops, int count, int64_t m, ScaleKind kind, bool force,
+                                cudaStream_t stream) {
+    if (count <= 0 || count > kBatchMaxOps || m <= 0 || m > 32) return cudaErrorInvalidValue;
+    switch (kind) {
+        case kScaleBlock: return launch_batch_sc<kScaleBlock>(ops, count, m, force, stream);
+        case kScaleMx: return launch_batch_sc<kScaleMx>(ops, count, m, force, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -51,6 +51,21 @@ struct MoeArgs {
     int64_t topk, num_experts;
 };
 cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_t stream);
+// A batch of GEMVs with one m <= 32, every op TMA-eligible (k % 16 == 0,
+// 16-byte aligned x and codes) and none reading or writing another's output:
+// one persistent launch streams all their weights (decode.cu).  count <=
+// kBatchMaxOps.  Unless `force`, a batch too small to fill the GPU's CTA
+// slots runs as one launch per op instead.
+constexpr int kBatchMaxOps = 96;
+struct BatchItem {
+    const void *x;           // bf16 [m, k]
+    const uint8_t *codes;    // e4m3 [n, k]
+    const void *scales;      // fp32 block scales (kScaleBlock) or e8m0 exponents (kScaleMx)
+    void *y;                 // bf16 [m, n]
+    int64_t n, k;
+};
+cudaError_t launch_decode_batch(const BatchItem *ops, int count, int64_t m, ScaleKind kind, bool force,
+                                cudaStream_t stream);
 uint32_t take_decode_error();  // reads and clears the decode kernels' error word
 // one thread waits on a barrier nothing completes until the bounded wait
 // gives up (about 2 s), then sets the decode error word

@@ -160,6 +160,62 @@ int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
                   void *y_bf16, int path, void *stream);
 
 /*
+ * fp8bs_gemv_batch / mxfp8_gemv_batch -- a sequence of W8A16 GEMVs with the
+ * same m, e.g. the dense projections of every layer of a decode step:
+ * the result is that of calling fp8bs_gemv (mxfp8_gemv) on ops[0],
+ * ops[1], ..., ops[count-1] in that order on `stream`.
+ *
+ * Defined by: FreeToken PR #389 (Why: the decode micro-benchmark streams a
+ * whole rotation of per-layer projection weights, 48 layers larger than L2,
+ * at M = 1/8/16, and times the rotation, not one weight); InfiniLM PR #586
+ * (Summary: block-FP8 W8A16 decode without bf16 weights) for the
+ * arithmetic, which is fp8bs_gemv's (mxfp8_gemv's) exactly.
+ *
+ * Runs of consecutive ops that are independent (no op reads or writes the
+ * bytes another op of the run writes) and fit the decode kernel (m <= 32,
+ * k % 16 == 0, 16-byte aligned x and codes) go to one persistent launch of
+ * up to 96 ops, which streams all their weights as one continuous sequence
+ * of 128-row tiles instead of paying each GEMV's start-up and tail.  An op
+ * that reads or writes an earlier op's output starts a new launch, so it
+ * sees that output complete (stream order); ops that the decode kernel
+ * cannot take run as their own fp8bs_gemv call in their place in the order.
+ * A run too small to fill the GPU (fewer 128-row tiles than half its CTA
+ * slots) runs as one launch per op.
+ *
+ *   ops      host array of count descriptors (read during the call only):
+ *              x_bf16  device, m*k bf16      codes  device, n*k e4m3
+ *              scales  device: fp32 [ceil(n/128), ceil(k/128)] (block) or
+ *                      e8m0 uint8 [n, ceil(k/32)] (MXFP8)
+ *              y_bf16  device, m*n bf16, written
+ *              n, k    > 0
+ *   count    >= 0 (0: no-op); m >= 0 (0: no-op), the same for every op
+ * Every op is validated as fp8bs_gemv / mxfp8_gemv validates its arguments
+ * before anything is enqueued; the first failure is returned and nothing
+ * is launched.  The launches' parameters hold the ops (no device memory is
+ * allocated or written besides y), so the call can be captured in a CUDA
+ * graph.  _ex: path AUTO as above; DECODE runs every eligible run through the
+ * batched kernel whatever its size (FP8BS_ERR_PATH if an op cannot take the
+ * decode kernel); PREFILL / GENERIC run every op as fp8bs_gemv_ex with that
+ * path.
+ */
+typedef struct fp8bs_gemv_op {
+    const void *x_bf16;
+    const uint8_t *codes;
+    const void *scales;
+    void *y_bf16;
+    int64_t n, k;
+} fp8bs_gemv_op;
+
+int fp8bs_gemv_batch(const fp8bs_gemv_op *ops, int64_t count, int64_t m,
+                     void *stream);
+int fp8bs_gemv_batch_ex(const fp8bs_gemv_op *ops, int64_t count, int64_t m,
+                        int path, void *stream);
+int mxfp8_gemv_batch(const fp8bs_gemv_op *ops, int64_t count, int64_t m,
+                     void *stream);
+int mxfp8_gemv_batch_ex(const fp8bs_gemv_op *ops, int64_t count, int64_t m,
+                        int path, void *stream);
+
+/*
  * fp8row_quantize / fp8tensor_quantize -- load-time FP8 with one fp32 scale
  * per output row (scales_f32[n]) or one for the whole weight (scale_f32[1]).
  *

@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "mxfp8_quantize", "mxfp8_gemv",
+    for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "fp8bs_gemv_batch", "fp8bs_gemv_batch_ex",
+                 "mxfp8_gemv_batch", "mxfp8_gemv_batch_ex", "mxfp8_quantize", "mxfp8_gemv",
                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
                  "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention", "fp8bs_select_path", "fp8bs_strerror",
@@ -51,7 +52,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_version_and_strerror(L):
-    assert L.fp8bs_version() == 105
+    assert L.fp8bs_version() == 106
     import fp8_block_scaled_02_gb300 as pkg
     for st in range(-7, 1):
         assert pkg.strerror(st) and pkg.strerror(st) != "unknown status"
@@ -93,6 +94,34 @@ def test_gemv_validation(L):
     assert L.fp8bs_gemv_ex(x, 1, P(0x20001), s, 10, 32, y, 1, None) == -7  # decode needs aligned codes
     assert L.mxfp8_gemv_ex(x, 1, c, s, 10, 32, y, 2, None) == -7    # no MX prefill path
     assert L.mxfp8_gemv(x, 1, c, None, 10, 32, y, None) == -1
+
+
+def batch(*ops):
+    from fp8_block_scaled_02_gb300 import GemvOp
+    arr = (GemvOp * max(1, len(ops)))()
+    for i, o in enumerate(ops):
+        arr[i] = GemvOp(*o)
+    return ctypes.cast(arr, ctypes.c_void_p)
+
+
+def test_gemv_batch_validation(L):
+    good = (0x10000, 0x20000, 0x30000, 0x40000, 128, 256)
+    for f, fx in ((L.fp8bs_gemv_batch, L.fp8bs_gemv_batch_ex), (L.mxfp8_gemv_batch, L.mxfp8_gemv_batch_ex)):
+        assert f(None, 0, 1, None) == 0                                   # empty batch: no-op
+        assert f(None, 2, 1, None) == -1                                  # no op array
+        assert f(batch(good, good), -1, 1, None) == -2
+        assert f(batch(good, good), 2, -1, None) == -2
+        assert f(batch(good, (0x10000, 0x20000, 0x30000, 0x40000, 0, 256)), 2, 1, None) == -2
+        assert f(batch(good, (0x10000, None, 0x30000, 0x40000, 128, 256)), 2, 1, None) == -1
+        assert f(batch(good, (0x10001, 0x20000, 0x30000, 0x40000, 128, 256)), 2, 1, None) == -4
+        assert f(batch(good, (None, None, None, None, 128, 256)), 2, 0, None) == 0   # m == 0: no-op
+        assert fx(batch(good), 1, 1, 9, None) == -7
+        # the decode path needs k % 16 == 0 and 16-byte aligned x and codes
+        assert fx(batch(good, (0x10000, 0x20000, 0x30000, 0x40000, 128, 200)), 2, 1, 1, None) == -7
+        assert fx(batch(good, (0x10008, 0x20000, 0x30000, 0x40000, 128, 256)), 2, 1, 1, None) == -7
+    # block scales must be 4-byte aligned; no MX prefill path
+    assert L.fp8bs_gemv_batch(batch(good, (0x10000, 0x20000, 0x30002, 0x40000, 128, 256)), 2, 1, None) == -4
+    assert L.mxfp8_gemv_batch_ex(batch(good), 1, 40, 2, None) == -7
 
 
 def test_rowwise_validation(L):
