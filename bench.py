@@ -226,18 +226,25 @@ def lm_head_workload(torch, fp8bs, inputs, dev):
                 codes=codes, scales=scales, n=n, k=k, mx=False)
 
 
-def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True):
+def rotation_weights(fp8bs, inputs, dev, scales="block"):
+    quant, _ = quantizer(fp8bs, scales)
+    weights = []
+    for l in range(inputs.ROTATION_LAYERS):
+        for j in range(4):
+            w = inputs.rotation_weight(l, j, device=dev)
+            weights.append(quant(w))
+            del w
+    return weights
+
+
+def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True, weights=None):
     """48 layers x 4 projection weights, one GEMV each per step.  batched:
     the step is one fp8bs_gemv_batch call (the 192 GEMVs stream as two
     persistent launches); otherwise one fp8bs_gemv call per weight."""
     layers = inputs.ROTATION_LAYERS
     quant, gemv = quantizer(fp8bs, scales)
-    weights = []
-    for l in range(layers):
-        for j in range(4):
-            w = inputs.rotation_weight(l, j, device=dev)
-            weights.append(quant(w))
-            del w
+    if weights is None:
+        weights = rotation_weights(fp8bs, inputs, dev, scales)
     shapes = [inputs.ROTATION_SHAPES[j] for _ in range(layers) for j in range(4)]
     xs = [inputs.activations(m, k, 7 + i, device=dev) for i, (n, k) in enumerate(shapes)]
     ys = [torch.empty((m, n), dtype=torch.bfloat16, device=dev) for (n, k) in shapes]
@@ -257,7 +264,8 @@ def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True
                        f"([8192,2560],[2560,3072],[6656,2560],[2560,3072]), M={m}, 192 GEMVs per step, "
                        f"{how}, CUDA graph", "ms": [m], "l2": "inputs larger than L2 (2.58 GB of codes per step)"}
     launches = 2 if batched else 192
-    dom = "gemv_batch_kernel" if batched else "decode_kernel"
+    mt = (m + 7) // 8
+    dom = f"gemv_batch_kernel<{mt},0,{'true' if mt == 1 else 'false'}>" if batched else "decode_kernel"
     return dict(calls=[(f"rotation M={m}", m, total, step)], cfg=cfg, graph=True, launches_per_step=launches,
                 dominant=(dom, [0]), xs=xs, ys=ys, weights=weights, ops=ops)
 
@@ -575,30 +583,118 @@ def e2e_lm_head(torch, fp8bs, wl, steps, warmup, pg):
 
 # ------------------------------------------------------------ CPU oracle
 _ORACLE_CACHE = {}
+ORACLE_GEMV_ROWS = 4096      # lm_head rows in the GEMV sample (M = 1, 4, 8, 16)
+ORACLE_QUANT_ROWS = 1024     # lm_head rows in the quantize sample
+ORACLE_ROT_ROWS = 1024       # rows of each rotation weight shape in the rotation GEMV sample
 
 
-def oracle_sample(rows=4096, ms=(1, 4, 8, 16)):
-    """Time the plain-C oracle (one host thread, as it stands) on a bounded
-    sample of the lm_head workload: `rows` weight rows, the same M sweep.
-    The sample is generated and quantized once (untimed).  Returns (GB/s in
-    the metric's units, seconds, description)."""
+def _oracle_samples():
+    """Seeded, bounded samples of the workloads (generated once, untimed):
+    the first rows of the lm_head weight (bf16 bits), x for M = 1, 4, 8, 16,
+    and for the rotation GEMV random finite e4m3 codes with positive scales
+    for the first rows of each of the four projection shapes (a GEMV's time
+    does not depend on its values)."""
+    if "s" in _ORACLE_CACHE:
+        return _ORACLE_CACHE["s"]
+    import numpy as np
     import oracle
     from fp8_block_scaled_02_gb300 import inputs
-    if rows not in _ORACLE_CACHE:
-        w = inputs.lm_head_weight(2, shape=(rows, 4096))
-        codes, scales = oracle.block_quantize(inputs.bf16_bits(w))
-        xs = {m: inputs.bf16_bits(inputs.activations(m, 4096, 100 + m)) for m in ms}
-        _ORACLE_CACHE[rows] = (codes, scales, xs)
-    codes, scales, xs = _ORACLE_CACHE[rows]
-    total_bytes, total_s = 0, 0.0
+    wq = inputs.bf16_bits(inputs.lm_head_weight(2, shape=(ORACLE_QUANT_ROWS, 4096)))
+    wg = inputs.bf16_bits(inputs.lm_head_weight(2, shape=(ORACLE_GEMV_ROWS, 4096)))
+    codes, scales = oracle.block_quantize(wg)
+    xs = {m: inputs.bf16_bits(inputs.activations(m, 4096, 100 + m)) for m in (1, 4, 8, 16)}
+    rng = np.random.default_rng(17)
+    rot = []
+    for j, (n, k) in enumerate(inputs.ROTATION_SHAPES):
+        r = min(n, ORACLE_ROT_ROWS)
+        c = rng.integers(0, 0x7F, size=(r, k), dtype=np.uint8) | (rng.integers(0, 2, size=(r, k), dtype=np.uint8) << 7)
+        s = rng.uniform(1e-5, 1e-3, size=(-(-r // 128), -(-k // 128))).astype(np.float32)
+        rot.append((c, s, inputs.bf16_bits(inputs.activations(1, k, 7 + j))))
+    _ORACLE_CACHE["s"] = dict(wq=wq, codes=codes, scales=scales, xs=xs, rot=rot)
+    return _ORACLE_CACHE["s"]
+
+
+def _row_chunks(rows, threads, align=128):
+    """Split [0, rows) into `threads` contiguous ranges on `align` boundaries."""
+    blocks = -(-rows // align)
+    per = -(-blocks // threads)
+    out = []
+    for t in range(threads):
+        r0, r1 = t * per * align, min(rows, (t + 1) * per * align)
+        if r0 < r1:
+            out.append((r0, r1))
+    return out
+
+
+def _parallel(fn, chunks, threads):
+    """Run fn(r0, r1) over the chunks on `threads` host threads (the oracle's
+    C calls release the GIL); returns the wall time in seconds."""
+    import concurrent.futures as cf
+    t = time.perf_counter()
+    if threads == 1:
+        for c in chunks:
+            fn(*c)
+    else:
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda c: fn(*c), chunks))
+    return time.perf_counter() - t
+
+
+def oracle_gemv_step(threads, ms=(1, 4, 8, 16)):
+    """The oracle's fp64 block GEMV on the lm_head sample, one call at each M
+    (the bench step's M sweep) with its rows split over `threads` host
+    threads.  Returns (GB/s in the metric's units, seconds)."""
+    import oracle
+    s = _oracle_samples()
+    rows = s["codes"].shape[0]
+    chunks = _row_chunks(rows, threads)
+    secs, nbytes = 0.0, 0
     for m in ms:
-        t = time.perf_counter()
-        oracle.block_gemv(xs[m], codes, scales)
-        total_s += time.perf_counter() - t
-        total_bytes += gemv_bytes(m, rows, 4096)
-    desc = (f"oracle block_gemv (plain C, fp64, 1 thread) over {rows} of the 152064 lm_head rows, "
-            f"K=4096, one call at each of M={list(ms)}")
-    return total_bytes / total_s / 1e9, total_s, desc
+        x = s["xs"][m]
+        secs += _parallel(lambda r0, r1: oracle.block_gemv(x, s["codes"][r0:r1], s["scales"][r0 // 128:-(-r1 // 128)]),
+                          chunks, threads)
+        nbytes += gemv_bytes(m, rows, 4096)
+    return nbytes / secs / 1e9, secs
+
+
+def oracle_runs(threads_list):
+    """The CPU oracle as it stands, timed on the host cores: block quantize
+    and MXFP8 quantize of the lm_head sample, the fp64 GEMV of the lm_head
+    sample at M = 1 and of the rotation sample at M = 1, each with 1 and with
+    all host threads (rows split into contiguous 128-row ranges)."""
+    import oracle
+    s = _oracle_samples()
+    out = []
+    rq = s["wq"].shape[0]
+    qbytes = 3 * rq * 4096
+    for t in threads_list:
+        chunks = _row_chunks(rq, t)
+        sec = _parallel(lambda r0, r1: oracle.block_quantize(s["wq"][r0:r1]), chunks, t)
+        out.append({"op": "block_quantize", "workload": f"lm_head [{rq} of 152064 rows, 4096]", "cores": t,
+                    "gb_s": round(qbytes / sec / 1e9, 5), "seconds": round(sec, 3)})
+        sec = _parallel(lambda r0, r1: oracle.mx_quantize(s["wq"][r0:r1]), chunks, t)
+        out.append({"op": "mx_quantize", "workload": f"lm_head [{rq} of 152064 rows, 4096]", "cores": t,
+                    "gb_s": round(qbytes / sec / 1e9, 5), "seconds": round(sec, 3)})
+        v, sec = oracle_gemv_step(t, ms=(1,))
+        out.append({"op": "block_gemv", "workload": f"lm_head M=1 [{s['codes'].shape[0]} of 152064 rows, 4096]",
+                    "cores": t, "gb_s": round(v, 5), "seconds": round(sec, 3)})
+        sec, nbytes = 0.0, 0
+        for c, sc, x in s["rot"]:
+            r, k = c.shape
+            sec += _parallel(lambda r0, r1: oracle.block_gemv(x, c[r0:r1], sc[r0 // 128:-(-r1 // 128)]),
+                             _row_chunks(r, t), t)
+            nbytes += gemv_bytes(1, r, k)
+        rate = nbytes / sec
+        out.append({"op": "block_gemv", "workload": "rotation M=1 (first 1024 rows of each projection shape)",
+                    "cores": t, "gb_s": round(rate / 1e9, 5), "seconds": round(sec, 3),
+                    "ms_per_rotation_step": round(1e3 * 2.5829e9 / rate, 1)})
+    return out
+
+
+def oracle_sample_desc(threads):
+    return (f"oracle block_gemv (plain C, fp64, as it stands) on {threads} host thread(s), rows split in 128-row "
+            f"ranges: the first {ORACLE_GEMV_ROWS} of the 152064 lm_head rows, K=4096, one call at each of "
+            "M=1,4,8,16")
 
 
 def host_cores():
@@ -606,6 +702,85 @@ def host_cores():
         return len(os.sched_getaffinity(0))
     except Exception:
         return os.cpu_count()
+
+
+# --------------------------------------------------------------- summaries
+def summarize(wl, per, total_ms, steps, workload):
+    """(value, unit, per_call, roofline) of one timed workload: per-call
+    rates from the per-call events; the roofline of the workload's dominant
+    kernel = its algorithmic bytes (flops) over its event time, against the
+    measured peak."""
+    peak, peak_kind = measured_peaks()
+    calls = wl["calls"]
+    flops = wl.get("flops", False)
+    scale_unit = 1e12 if flops else 1e9
+    unit = "TFLOP/s" if flops else "GB/s"
+    tpeak, tpeak_kind = tensor_peak()
+    if wl.get("fp8"):
+        # e4m3 tensor-core peak: the measured bf16 peak times the nominal
+        # fp8 : bf16 ratio (4.5 : 2.25 PFLOP/s dense)
+        tpeak, tpeak_kind = 2.0 * tpeak, tpeak_kind + " x 2 (fp8 : bf16 nominal)"
+    step_bytes = sum(b for _, _, b, _ in calls)
+    value = step_bytes * steps / (total_ms * 1e-3) / scale_unit
+    per_call = {}
+    for (name, m, b, _), t in zip(calls, per):
+        lp = wl.get("launches_per_call", 1)
+        rate = b / (t * 1e-3) / scale_unit
+        if flops:
+            per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "tflop_s": round(rate, 1),
+                              "frac_of_peak": round(rate / tpeak, 4)}
+        else:
+            per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "gb_s": round(rate, 1),
+                              "frac_of_8TBps": round(rate / HBM_NOMINAL_GBS, 4),
+                              "frac_of_measured": round(rate / peak, 4)}
+    dom_name, dom_idx = wl["dominant"]
+    dom_bytes = sum(calls[i][2] for i in dom_idx)
+    dom_ms = sum(per[i] for i in dom_idx)
+    achieved = dom_bytes / (dom_ms * 1e-3) / scale_unit
+    if flops:
+        roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1), "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
+                    "peak_kind": f"bf16_tflops ({tpeak_kind})", "traffic": None,
+                    "dtype": "e4m3" if wl.get("fp8") else "bf16"}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
+                    "traffic": measured_traffic(dom_name, workload)}
+    return value, unit, per_call, roofline
+
+
+def extra_configs(torch, fp8bs, inputs, dev, steps, warmup):
+    """The other measured configurations, each timed like the main workload
+    (warm-up, one event pair over the timed steps, then events around every
+    call) with its own roofline record: the 48-layer rotation at M = 1, 8,
+    16, 32 (one batched call per step), the [12288, 4096] M sweep at M = 1,
+    9, 17, 25, 32, the tcgen05 prefill at M = 512, 2048, 4096, the MXFP8
+    GEMV at M = 1, 8, 16 and the block / MXFP8 / per-row / per-tensor
+    load-time quantizers.  Returns ({name: record}, kernel launches)."""
+    out, launches = {}, 0
+
+    def run(name, wl, workload):
+        nonlocal launches
+        per, total = time_calls(torch, wl["calls"], steps, warmup, None, graph=wl.get("graph", False))
+        value, unit, per_call, roofline = summarize(wl, per, total, steps, workload)
+        out[name] = {"workload": wl["cfg"]["workload"], "value": round(value, 2), "unit": unit,
+                     "ms_per_step": round(total / steps, 4), "per_call": per_call, "roofline": roofline}
+        lpc = wl.get("call_launches", [wl.get("launches_per_call", 1)] * len(wl["calls"]))
+        launches += 2 * steps * sum(lpc) * wl.get("launches_per_step", 1)   # timed pass + per-call pass
+        torch.cuda.synchronize()
+        if fp8bs.check_device_error() != 0:
+            raise RuntimeError(f"device error word set while timing {name}")
+
+    weights = rotation_weights(fp8bs, inputs, dev)
+    for m in (1, 8, 16, 32):
+        run(f"rotation M={m}", rotation_workload(torch, fp8bs, inputs, dev, m, weights=weights), "rotation")
+    del weights
+    run("sweep", sweep_workload(torch, fp8bs, inputs, dev, [1, 9, 17, 25, 32]), "sweep")
+    run("prefill", prefill_workload(torch, fp8bs, inputs, dev), "prefill")
+    run("mx", mx_workload(torch, fp8bs, inputs, dev), "mx")
+    run("quantize", quantize_workload(torch, fp8bs, inputs, dev), "quantize")
+    torch.cuda.empty_cache()
+    return out, launches
 
 
 # -------------------------------------------------------------------- main
@@ -622,6 +797,8 @@ def main():
     ap.add_argument("--single", action="store_true", help="rotation: one GEMV call per weight, not one batch")
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="lm_head: skip the other configurations (rotation, sweep, prefill, MXFP8, quantize)")
     ap.add_argument("--clocks-file", default=os.path.join(tempfile.gettempdir(), "fp8bs_bench_clocks.csv"),
                     help="raw nvidia-smi samples taken during the timed region (summarised in the JSON line)")
     args = ap.parse_args()
@@ -632,15 +809,12 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return 0
-        # each step is a bounded sample: about 20 s of oracle GEMV work in total
-        rows = 128 * max(1, round(32 * min(1.0, 12.0 / max(1, args.steps))))
+        # the oracle as it stands on all host cores; each step is the bounded
+        # lm_head sample of oracle_gemv_step (the cpu_baseline leg's sample)
+        threads = host_cores()
         for _ in range(warmup):
-            oracle_sample(rows=128)
-        per_step = []
-        desc = ""
-        for _ in range(args.steps):
-            v, s, desc = oracle_sample(rows=rows)
-            per_step.append((v, s))
+            oracle_gemv_step(threads)
+        per_step = [oracle_gemv_step(threads) for _ in range(args.steps)]
         value = statistics.fmean(v for v, _ in per_step)
         ms_step = 1e3 * statistics.fmean(s for _, s in per_step)
         # the same metric, unit and config as this file's own lm_head line;
@@ -650,8 +824,8 @@ def main():
                 "warmup": warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": dict(lm_head_config(152064, 4096, [1, 4, 8, 16]), parallelism=f"replicas x{args.gpus}"),
-                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                 "sample": f"{desc}; {rows} rows per step"},
+                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                 "sample": oracle_sample_desc(threads)},
                 "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return 0
@@ -701,39 +875,8 @@ def main():
     step_bytes = sum(b for _, _, b, _ in calls)
     total_ms = max_over_ranks(pg, total_ms)
     all_bytes = sum_over_ranks(pg, step_bytes * args.steps)
-    flops = wl.get("flops", False)
-    scale_unit = 1e12 if flops else 1e9
-    unit = "TFLOP/s" if flops else "GB/s"
-    tpeak, tpeak_kind = tensor_peak()
-    if wl.get("fp8"):
-        # e4m3 tensor-core peak: the measured bf16 peak times the nominal
-        # fp8 : bf16 ratio (4.5 : 2.25 PFLOP/s dense)
-        tpeak, tpeak_kind = 2.0 * tpeak, tpeak_kind + " x 2 (fp8 : bf16 nominal)"
-    value = all_bytes / (total_ms * 1e-3) / scale_unit
-    per_call = {}
-    for (name, m, b, _), t in zip(calls, per):
-        lp = wl.get("launches_per_call", 1)
-        rate = b / (t * 1e-3) / scale_unit
-        if flops:
-            per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "tflop_s": round(rate, 1),
-                              "frac_of_peak": round(rate / tpeak, 4)}
-        else:
-            per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "gb_s": round(rate, 1),
-                              "frac_of_8TBps": round(rate / HBM_NOMINAL_GBS, 4),
-                              "frac_of_measured": round(rate / peak, 4)}
-    dom_name, dom_idx = wl["dominant"]
-    dom_bytes = sum(calls[i][2] for i in dom_idx)
-    dom_ms = sum(per[i] for i in dom_idx)
-    achieved = dom_bytes / (dom_ms * 1e-3) / scale_unit
-    if flops:
-        roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1), "peak": tpeak,
-                    "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
-                    "peak_kind": f"bf16_tflops ({tpeak_kind})", "traffic": None,
-                    "dtype": "e4m3" if wl.get("fp8") else "bf16"}
-    else:
-        roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
-                    "traffic": measured_traffic(dom_name, args.workload)}
+    _, unit, per_call, roofline = summarize(wl, per, total_ms, args.steps, args.workload)
+    value = all_bytes / (total_ms * 1e-3) / (1e12 if wl.get("flops", False) else 1e9)
 
     e2e = None
     if args.workload == "lm_head":
@@ -745,21 +888,34 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "lm_head":
-        v, s, desc = oracle_sample()
-        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
-               "host_cores_available": host_cores()}
+        threads = host_cores()
+        v, _ = oracle_gemv_step(threads)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": oracle_sample_desc(threads), "runs": oracle_runs(sorted({1, threads}))}
 
     per_call_launches = wl.get("call_launches", [wl.get("launches_per_call", 1)] * len(calls))
     launches = args.steps * sum(per_call_launches) * wl.get("launches_per_step", 1)
+    cfg = dict(wl["cfg"], parallelism=f"replicas x{world}")
+
+    extras = None
+    if args.workload == "lm_head" and world == 1 and not args.no_extras:
+        del wl, calls
+        torch.cuda.empty_cache()
+        with Clocks(args.clocks_file + ".extras") as clk2:
+            recs, extra_launches = extra_configs(torch, fp8bs, inputs, dev, min(args.steps, 20), warmup)
+        extras = {"clocks": clk2.summary(), "gpu_launches": extra_launches, **recs}
+
     if rank == 0:
         line = {"metric": LM_HEAD_METRIC if args.workload == "lm_head"
                 else f"{args.workload} {unit}",
                 "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x bf16 -> fp32", "data": "synthetic",
-                "config": dict(wl["cfg"], parallelism=f"replicas x{world}"),
+                "config": cfg,
                 "per_call": per_call, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "clocks": clocks, "gpu_launches": launches}
+        if extras is not None:
+            line["configs"] = extras
         print(json.dumps(line))
     if pg is not None:
         pg.destroy_process_group()

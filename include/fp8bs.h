@@ -277,9 +277,11 @@ int fp8tensor_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
  * top-12 of 256 experts per token).
  *
  *   x_bf16       device, m*k bf16, 16-byte aligned, k % 16 == 0
- *   expert_ids   device, m*topk int32; ids of one token must be distinct;
- *                an id outside [0, num_experts) selects nothing and sets
- *                the device error word (fp8bs_check_device_error)
+ *   expert_ids   device, m*topk int32; ids of one token must be distinct
+ *                (a token listing an expert twice gets only its lowest such
+ *                slot written and sets the device error word); an id
+ *                outside [0, num_experts) selects nothing and sets the
+ *                device error word (fp8bs_check_device_error)
  *   topk         1..num_experts;  num_experts 1..1024, num_experts*n < 2^31
  *   y_bf16       device, m*topk*n bf16, written for every valid id
  * The ids are read on the device (no host synchronisation); m > 32 runs in
@@ -397,7 +399,8 @@ int w8a8_gemm_ex(const uint8_t *x_codes, int64_t m, const float *x_scale,
 int fp8bs_select_path(int64_t m, int64_t n, int64_t k, const void *x_bf16,
                       const void *codes, int mx);
 
-/* Human-readable text for a status code (static storage). */
+/* Human-readable text for a status code (static storage).
+ * Defined by: no passage of the source pages (library infrastructure). */
 const char *fp8bs_strerror(int status);
 
 /*
@@ -406,6 +409,11 @@ const char *fp8bs_strerror(int status);
  * synchronises `stream`, copies the word to *word_out (may be NULL), clears
  * it, and returns FP8BS_ERR_DEVICE if it was non-zero, else FP8BS_OK (or
  * FP8BS_ERR_CUDA if the synchronisation itself failed).
+ *
+ * Defined by: no passage of the source pages (library infrastructure: the
+ * bounded waits' failure report).  Beyond a status, the call hands back the
+ * word itself (word_out) so that a caller can tell a wait expiry
+ * (bits 0-3) from a bad index argument (bit 4).
  */
 int fp8bs_check_device_error(void *stream, uint32_t *word_out);
 

@@ -107,6 +107,27 @@ def test_out_of_range_id_sets_error_and_skips(pkg):
         assert tolerance.gemv_ok(st)
 
 
+def test_duplicate_id_within_a_token_sets_error(pkg):
+    """ids of one token must be distinct (a top-k selection); a token that
+    lists an expert twice is flagged in the device error word (only its
+    lowest slot is written), and the other tokens' outputs are unaffected."""
+    E, n, k = 4, 128, 128
+    codes, scales = experts(E, n, k, 10)
+    ids = np.array([[2, 2], [0, 3]], dtype=np.int32)
+    x = inputs.activations(2, k, 5)
+    y = torch.full((2, 2, n), 7.0, dtype=torch.bfloat16, device=DEV)
+    pkg.moe_gemv(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                 torch.from_numpy(scales).to(DEV), y=y)
+    assert pkg.check_device_error() & 16       # ERRBIT_INDEX
+    y64 = oracle.moe_gemv(bits(x), ids, codes, scales)
+    for t, j in ((0, 0), (1, 0), (1, 1)):
+        st = tolerance.gemv_errors(bits(y[t, j][None, :].cpu()), y64[t, j][None, :], bits(x)[t][None, :],
+                                   np.full(n, np.abs(table()[codes]).max() * scales.max()))
+        assert tolerance.gemv_ok(st)
+    assert torch.all(y[0, 1].cpu().float() == 7.0)
+    assert pkg.check_device_error() == 0       # reading cleared it
+
+
 def test_unselected_experts_are_not_read(pkg):
     """Poisoning the weights of experts no token selected changes nothing."""
     E, n, k = 8, 128, 256
