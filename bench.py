@@ -270,9 +270,12 @@ def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True
                 dominant=(dom, [0]), xs=xs, ys=ys, weights=weights, ops=ops)
 
 
-def sweep_workload(torch, fp8bs, inputs, dev, ms):
+def sweep_workload(torch, fp8bs, inputs, dev, ms, ws=False):
+    """ws: every call goes through fp8bs_gemv_ws (x prepared once per call
+    in a caller-provided workspace, f16 operands at every M)."""
     copies = [fp8bs.quantize(inputs.sweep_weight(c, device=dev)) for c in range(8)]
     n, k = inputs.SWEEP_SHAPE
+    work = torch.empty((fp8bs.gemv_ws_bytes(32, k),), dtype=torch.uint8, device=dev) if ws else None
     calls = []
     for m in ms:
         x = inputs.activations(m, k, 300 + m, device=dev)
@@ -280,11 +283,16 @@ def sweep_workload(torch, fp8bs, inputs, dev, ms):
 
         def fn(x=x, y=y):
             for c, s in copies:
-                fp8bs.gemv(x, c, s, y=y)
+                if ws:
+                    fp8bs.gemv_ws(x, c, s, work, y=y)
+                else:
+                    fp8bs.gemv(x, c, s, y=y)
         calls.append((f"M={m}", m, 8 * gemv_bytes(m, n, k), fn))
-    cfg = {"workload": "M sweep: block-FP8 [12288,4096], one GEMV per M over 8 rotated weight copies (403 MB)",
+    how = " (fp8bs_gemv_ws: x prepared once per call)" if ws else ""
+    cfg = {"workload": f"M sweep: block-FP8 [12288,4096], one GEMV per M over 8 rotated weight copies (403 MB){how}",
            "n": n, "k": k, "ms": ms, "l2": "inputs larger than L2 (8 rotated copies)"}
-    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel", list(range(len(ms)))), launches_per_call=8)
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel", list(range(len(ms)))), gemvs_per_call=8,
+                launches_per_call=16 if ws else 8)
 
 
 def mx_workload(torch, fp8bs, inputs, dev):
@@ -322,8 +330,26 @@ def prefill_workload(torch, fp8bs, inputs, dev, scales="block"):
     kind = {"block": "block-FP8", "row": "per-row FP8", "tensor": "per-tensor FP8"}[scales]
     cfg = {"workload": f"prefill: {kind} [12288,4096] W8A16 GEMM on tcgen05, M=512,2048,4096", "n": n, "k": k,
            "ms": ms, "l2": "weight (50 MB) and x fit in L2; compute-bound"}
-    dom = "prefill_kernel<false>" if scales == "block" else "prefill_kernel<true>"
+    dom = "prefill_kernel<0>" if scales == "block" else "prefill_kernel<2>"
     return dict(calls=calls, cfg=cfg, dominant=(dom, [0, 1, 2]), flops=True)
+
+
+def mx_prefill_workload(torch, fp8bs, inputs, dev):
+    """MXFP8 [18432, 7168] (0.1% Student-t entries) at prefill sizes on the
+    tensor cores, the e8m0 group scales folded into the decoded weights."""
+    ms = [512, 2048, 4096]
+    w = inputs.heavy_tail_weight(5, device=dev)
+    codes, e8m0 = fp8bs.mx_quantize(w)
+    del w
+    n, k = inputs.MX_SHAPE
+    calls = []
+    for m in ms:
+        x = inputs.activations(m, k, 750 + m, device=dev)
+        y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        calls.append((f"M={m}", m, 2 * m * n * k, (lambda x=x, y=y: fp8bs.mx_gemv(x, codes, e8m0, y=y))))
+    cfg = {"workload": "prefill: MXFP8 [18432,7168] W8A16 GEMM on tcgen05, M=512,2048,4096", "n": n, "k": k,
+           "ms": ms, "l2": "weight (132 MB) about the size of L2; compute-bound"}
+    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel<1>", [0, 1, 2]), flops=True)
 
 
 def rowwise_workload(torch, fp8bs, inputs, dev):
@@ -724,7 +750,7 @@ def summarize(wl, per, total_ms, steps, workload):
     value = step_bytes * steps / (total_ms * 1e-3) / scale_unit
     per_call = {}
     for (name, m, b, _), t in zip(calls, per):
-        lp = wl.get("launches_per_call", 1)
+        lp = wl.get("gemvs_per_call", wl.get("launches_per_call", 1))   # us per GEMV / kernel call
         rate = b / (t * 1e-3) / scale_unit
         if flops:
             per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "tflop_s": round(rate, 1),
@@ -755,7 +781,8 @@ def extra_configs(torch, fp8bs, inputs, dev, steps, warmup):
     call) with its own roofline record: the 48-layer rotation at M = 1, 8,
     16, 32 (one batched call per step), the [12288, 4096] M sweep at M = 1,
     9, 17, 25, 32, the tcgen05 prefill at M = 512, 2048, 4096, the MXFP8
-    GEMV at M = 1, 8, 16 and the block / MXFP8 / per-row / per-tensor
+    GEMV at M = 1, 8, 16 and its tcgen05 prefill at M = 512, 2048, 4096,
+    and the block / MXFP8 / per-row / per-tensor
     load-time quantizers.  Returns ({name: record}, kernel launches)."""
     out, launches = {}, 0
 
@@ -778,6 +805,7 @@ def extra_configs(torch, fp8bs, inputs, dev, steps, warmup):
     run("sweep", sweep_workload(torch, fp8bs, inputs, dev, [1, 9, 17, 25, 32]), "sweep")
     run("prefill", prefill_workload(torch, fp8bs, inputs, dev), "prefill")
     run("mx", mx_workload(torch, fp8bs, inputs, dev), "mx")
+    run("mx_prefill", mx_prefill_workload(torch, fp8bs, inputs, dev), "mx_prefill")
     run("quantize", quantize_workload(torch, fp8bs, inputs, dev), "quantize")
     torch.cuda.empty_cache()
     return out, launches
@@ -791,10 +819,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="lm_head",
-                    choices=["lm_head", "rotation", "sweep", "mx", "quantize", "prefill", "rowwise", "w8a8",
+                    choices=["lm_head", "rotation", "sweep", "mx", "mx_prefill", "quantize", "prefill", "rowwise", "w8a8",
                              "w8a8_prefill", "moe", "kv"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--single", action="store_true", help="rotation: one GEMV call per weight, not one batch")
+    ap.add_argument("--ws", action="store_true", help="sweep: call fp8bs_gemv_ws (x prepared in a workspace)")
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
@@ -843,11 +872,13 @@ def main():
     elif args.workload == "rotation":
         wl = rotation_workload(torch, fp8bs, inputs, dev, args.m, args.scales, batched=not args.single)
     elif args.workload == "sweep":
-        wl = sweep_workload(torch, fp8bs, inputs, dev, list(range(1, 33)))
+        wl = sweep_workload(torch, fp8bs, inputs, dev, list(range(1, 33)), ws=args.ws)
     elif args.workload == "mx":
         wl = mx_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "prefill":
         wl = prefill_workload(torch, fp8bs, inputs, dev, args.scales)
+    elif args.workload == "mx_prefill":
+        wl = mx_prefill_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "rowwise":
         wl = rowwise_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "w8a8":

@@ -12,6 +12,7 @@ Functions (names follow the C entry points):
     gemv(x, codes, scales) -> y bf16 [M,N]
     mx_quantize(w)         -> (codes u8 [N,K], e8m0 u8 [N, ceil(K/32)])
     mx_gemv(x, codes, e8m0)-> y bf16 [M,N]
+    gemv_ws(x, codes, scales, workspace) -> y bf16 [M,N]        (fp8bs_gemv_ws)
     gemv_batch([(x, codes, scales[, y]), ...]) -> [y, ...]   (fp8bs_gemv_batch)
     mx_gemv_batch([(x, codes, e8m0[, y]), ...]) -> [y, ...]  (mxfp8_gemv_batch)
     row_quantize(w)        -> (codes u8 [N,K], scales f32 [N])       (fp8row_*)
@@ -75,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_quantize.argtypes = [p, i64, i64, i32, p, p, p]
         L.fp8bs_gemv.argtypes = [p, i64, p, p, i64, i64, p, p]
         L.fp8bs_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
+        L.fp8bs_gemv_ws_bytes.argtypes = [i64, i64]
+        L.fp8bs_gemv_ws_bytes.restype = i64
+        L.fp8bs_gemv_ws.argtypes = [p, i64, p, p, i64, i64, p, p, i64, p]
         L.fp8bs_gemv_batch.argtypes = [p, i64, i64, p]
         L.fp8bs_gemv_batch_ex.argtypes = [p, i64, i64, i32, p]
         L.mxfp8_gemv_batch.argtypes = [p, i64, i64, p]
@@ -102,7 +106,8 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_debug_wait_expiry.argtypes = [p]
         L.fp8bs_debug_encode_f32.argtypes = [ctypes.c_uint32, i64, p, p]
         L.fp8bs_version.argtypes = []
-        for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "fp8bs_gemv_batch", "fp8bs_gemv_batch_ex",
+        for f in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "fp8bs_gemv_ws", "fp8bs_gemv_batch",
+                  "fp8bs_gemv_batch_ex",
                   "mxfp8_gemv_batch", "mxfp8_gemv_batch_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                   "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
@@ -236,6 +241,26 @@ def gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
     a, m, n, k, y = _gemv_args(x, codes, y, scales, torch.float32, _block_numel)
     _run(a, "fp8bs_gemv", lib().fp8bs_gemv_ex, a.ptr("x"), m, a.ptr("codes"), a.ptr("scales"), n, k, a.ptr("y"),
          int(path), stream=stream)
+    return y
+
+
+def gemv_ws_bytes(m: int, k: int) -> int:
+    """Bytes of device workspace gemv_ws needs (fp8bs_gemv_ws_bytes)."""
+    v = lib().fp8bs_gemv_ws_bytes(m, k)
+    if v < 0:
+        raise Fp8bsError(int(v), "fp8bs_gemv_ws_bytes")
+    return int(v)
+
+
+def gemv_ws(x, codes, scales, workspace, y=None, stream=None):
+    """gemv with caller-provided device scratch (fp8bs_gemv_ws): x is
+    converted once per call to f16 in `workspace` (a uint8 CUDA tensor of at
+    least gemv_ws_bytes(M, K) bytes) and the decode kernel reads that copy."""
+    import torch
+    a, m, n, k, y = _gemv_args(x, codes, y, scales, torch.float32, _block_numel, check=False)
+    a.need("workspace", workspace, torch.uint8).check()
+    _run(a, "fp8bs_gemv_ws", lib().fp8bs_gemv_ws, a.ptr("x"), m, a.ptr("codes"), a.ptr("scales"), n, k, a.ptr("y"),
+         a.ptr("workspace"), workspace.numel(), stream=stream)
     return y
 
 

@@ -22,8 +22,9 @@ inline bool tma_ok(int64_t k, const void *x, const void *codes) {
 }
 
 int select_path(int64_t m, int64_t k, const void *x, const void *codes, bool mx) {
+    (void)mx;  // MXFP8 takes the same paths (its prefill folds the group scales into the decode)
     if (!tma_ok(k, x, codes)) return FP8BS_PATH_GENERIC;
-    if (mx || m <= kDecodeMaxM) return FP8BS_PATH_DECODE;
+    if (m <= kDecodeMaxM) return FP8BS_PATH_DECODE;
     return FP8BS_PATH_PREFILL;
 }
 
@@ -50,9 +51,8 @@ int run_decode_chunks(const DecodeArgs &a, cudaStream_t st) {
 }
 
 int gemv_dispatch(const DecodeArgs &a, int path, cudaStream_t st) {
-    const bool mx = a.kind == kScaleMx;
     const bool tma = tma_ok(a.k, a.x, a.codes);
-    if (path == FP8BS_PATH_AUTO) path = select_path(a.m, a.k, a.x, a.codes, mx);
+    if (path == FP8BS_PATH_AUTO) path = select_path(a.m, a.k, a.x, a.codes, a.kind == kScaleMx);
     switch (path) {
         case FP8BS_PATH_GENERIC:
             return cuda_status(launch_generic_gemv(a, st));
@@ -60,7 +60,7 @@ int gemv_dispatch(const DecodeArgs &a, int path, cudaStream_t st) {
             if (!tma) return FP8BS_ERR_PATH;
             return run_decode_chunks(a, st);
         case FP8BS_PATH_PREFILL: {
-            if (!tma || mx) return FP8BS_ERR_PATH;
+            if (!tma) return FP8BS_ERR_PATH;
             const cudaError_t e = launch_prefill(a, st);
             if (e == cudaErrorNotSupported) return run_decode_chunks(a, st);
             return cuda_status(e);
@@ -108,8 +108,7 @@ int gemv_batch_impl(const fp8bs_gemv_op *ops, int64_t count, int64_t m, bool mx,
         if (m == 0) continue;
         if (!mx && !aligned(o.scales, 4)) return FP8BS_ERR_ALIGN;
         const bool tma = tma_ok(o.k, o.x_bf16, o.codes);
-        if ((path == FP8BS_PATH_DECODE && !tma) || (path == FP8BS_PATH_PREFILL && (mx || !tma)))
-            return FP8BS_ERR_PATH;
+        if ((path == FP8BS_PATH_DECODE || path == FP8BS_PATH_PREFILL) && !tma) return FP8BS_ERR_PATH;
     }
     if (m == 0) return FP8BS_OK;
     const ScaleKind kind = mx ? kScaleMx : kScaleBlock;
@@ -215,11 +214,30 @@ int fp8bs_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const float 
     return fp8bs_gemv_ex(x_bf16, m, codes, scales, n, k, y_bf16, FP8BS_PATH_AUTO, stream);
 }
 
+int64_t fp8bs_gemv_ws_bytes(int64_t m, int64_t k) {
+    if (m < 0 || k <= 0 || m >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
+    return m == 0 ? 0 : xprep_bytes(m < kDecodeMaxM ? m : kDecodeMaxM, k);
+}
+
+int fp8bs_gemv_ws(const void *x_bf16, int64_t m, const uint8_t *codes, const float *scales, int64_t n, int64_t k,
+                  void *y_bf16, void *workspace, int64_t workspace_bytes, void *stream) {
+    int st = check_gemv_args(x_bf16, m, codes, scales, n, k, y_bf16, FP8BS_PATH_AUTO);
+    if (st != FP8BS_OK || m == 0) return st;
+    if (!aligned(scales, 4)) return FP8BS_ERR_ALIGN;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k, kScaleBlock, 0};
+    // only the decode path (m <= 32, TMA-eligible) uses the workspace
+    if (select_path(m, k, x_bf16, codes, false) != FP8BS_PATH_DECODE) return gemv_dispatch(a, FP8BS_PATH_AUTO, s);
+    if (!workspace) return FP8BS_ERR_NULL;
+    if (!aligned(workspace, 16)) return FP8BS_ERR_ALIGN;
+    if (workspace_bytes < xprep_bytes(m, k)) return FP8BS_ERR_SHAPE;
+    return cuda_status(launch_decode_xprep(a, workspace, s));
+}
+
 int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes, const uint8_t *scales_e8m0, int64_t n,
                   int64_t k, void *y_bf16, int path, void *stream) {
     int st = check_gemv_args(x_bf16, m, codes, scales_e8m0, n, k, y_bf16, path);
     if (st != FP8BS_OK || m == 0) return st;
-    if (path == FP8BS_PATH_PREFILL) return FP8BS_ERR_PATH;
     DecodeArgs a{x_bf16, codes, nullptr, scales_e8m0, y_bf16, m, n, k, kScaleMx, 0};
     return gemv_dispatch(a, path, static_cast<cudaStream_t>(stream));
 }

@@ -119,6 +119,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_load_g2s(void *smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Ask for one 2-D box to be brought into L2 (no shared memory, no
 // completion).  L2 is the coherence point of device memory, so a prefetch
 // can never return stale data: it is safe even while the previous kernel in
@@ -196,6 +205,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t word, uint32_t sel
     asm("prmt.b32 %0, %1, 0, %2;" : "=r"(v) : "r"(word), "r"(sel));
     v = (v << 4) & 0x87F087F0u;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(v), "r"(0x7B807B80u));
+    return out;
+}
+
+// Two e4m3 codes -> the bf16 pair (dec(c0), dec(c1)) * 2^-120 * f, given
+// mult = the bf16x2 pair (f, f): e4m3x2_to_bf16x2 with its final multiply
+// by 2^120 replaced by one by f (f = 2^120 gives the plain decode).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_mul(uint32_t word, uint32_t sel, uint32_t mult) {
+    uint32_t v, out;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(v) : "r"(word), "r"(sel));
+    v = (v << 4) & 0x87F087F0u;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(v), "r"(mult));
+    return out;
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t out;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(a), "r"(b));
     return out;
 }
 

@@ -75,7 +75,9 @@ constexpr int kMoeMaxExperts = 1024; // experts a grouped call may address (bitm
 // as staged).  The f16 form halves the decode work and wins while the
 // consumers are bound by it (m <= 8); beyond that the single converter warp
 // becomes the bottleneck and the bf16 form, which needs none, wins.
-template <int MT, bool MX, bool F16>
+// XP: x arrives prepared (an f16 copy with one power-of-two factor per row
+// and K block, written by xprep_kernel), so f16 operands need no converter.
+template <int MT, bool MX, bool F16, bool XP = false>
 struct Cfg {
     // weight rows per CTA: one block-scale row.  Each of the 8 consumer
     // warps owns one 16-row tile across the whole 128-wide K block, so row
@@ -87,7 +89,7 @@ struct Cfg {
     // lm_head-sized GEMV measured 1.6% faster); wider x tiles leave room for
     // four (m <= 16) or three stages within two CTAs per SM
     static constexpr int kStages = MT == 1 ? 5 : (MT == 2 ? 4 : 3);
-    static constexpr bool kConv = F16;                  // converter warp present
+    static constexpr bool kConv = F16 && !XP;           // converter warp present
     static constexpr int kConvWarps = kConv ? 1 : 0;
     static constexpr int kThreads = (kConsumerWarps + 1 + kConvWarps) * 32;
     static constexpr int kXRows = 8 * MT;               // x rows staged (zero-padded)
@@ -215,8 +217,9 @@ struct OpRef {
 // MOE: grouped expert GEMV (block scales); n is the rows of one expert, the
 // codes / scales hold num_experts such weights back to back, ids [m, topk].
 // BATCH: the ops come from `bp` (the single-weight arguments are unused).
-template <int MT, int SC, bool F16, bool MOE, bool BATCH>
-__device__ __forceinline__ void decode_body(const BatchParams *bp, const CUtensorMap *tm_codes,
+template <int MT, int SC, bool F16, bool MOE, bool BATCH, bool XP = false>
+__device__ __forceinline__ void decode_body(const BatchParams *bp, const float *__restrict__ xinv_g,
+                                            const CUtensorMap *tm_codes,
                                             const CUtensorMap *tm_x, const float *__restrict__ scales,
                                             const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
                                             int m, int n, int kblocks, int groups, int splits, int ntiles,
@@ -229,7 +232,8 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const CUtenso
     // ... and with bf16 operands and one scale per row, all of K
     constexpr bool kDirect = kWholeBlock && ROW && !F16;
     static_assert(!(MOE && BATCH), "a grouped MoE call is one launch of its own");
-    using C = Cfg<MT, MX, F16>;
+    static_assert(!XP || (F16 && !MX && !MOE && !BATCH), "prepared x feeds the single-weight f16 path");
+    using C = Cfg<MT, MX, F16, XP>;
     constexpr int kStages = C::kStages;
     constexpr int kBN = C::kBN;
     extern __shared__ uint8_t smem_raw[];
@@ -407,10 +411,14 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const CUtenso
                 if (lane == 0) {
                     const int kx = (kbb + kb) * kKB;
                     uint8_t *st = smem + s * C::kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+                    mbar_arrive_expect_tx(&full[s], C::kStageBytes + (XP ? C::kXRows * 4 : 0));
                     tma_load_2d_hint(st, o.tm_codes, &full[s], kx, row_base + n0, stream_policy);
                     tma_load_2d(st + C::kCodeBytes, o.tm_x, &full[s], kx, 0);
                     tma_load_2d(st + C::kCodeBytes + C::kXPanelBytes, o.tm_x, &full[s], kx + 64, 0);
+                    // prepared x: this K block's inverse factors, in the slot
+                    // order the consumers read (xprep_kernel)
+                    if (XP)
+                        bulk_load_g2s(aux + s * C::kXInvFloats, xinv_g + (kbb + kb) * 32, C::kXRows * 4, &full[s]);
                 }
                 __syncwarp();
             }
@@ -671,22 +679,64 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const CUtenso
     }
 }
 
-template <int MT, int SC, bool F16, bool MOE = false>
-__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
+template <int MT, int SC, bool F16, bool MOE = false, bool XP = false>
+__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16, XP>::kThreads,
+                                  Cfg<MT, SC == kScaleMx, F16, XP>::kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
                   const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
                   int m, int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec, int row_stride,
-                  const int32_t *__restrict__ ids, int topk, int num_experts) {
-    decode_body<MT, SC, F16, MOE, false>(nullptr, &tm_codes, &tm_x, scales, e8m0, y, m, n, kblocks, groups, splits,
-                                         ntiles, e8m0_vec, row_stride, ids, topk, num_experts);
+                  const int32_t *__restrict__ ids, int topk, int num_experts, const float *__restrict__ xinv) {
+    decode_body<MT, SC, F16, MOE, false, XP>(nullptr, xinv, &tm_codes, &tm_x, scales, e8m0, y, m, n, kblocks, groups,
+                                             splits, ntiles, e8m0_vec, row_stride, ids, topk, num_experts);
 }
 
 // A batch of independent GEMVs with the same m in one persistent launch.
 template <int MT, int SC, bool F16>
 __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
     gemv_batch_kernel(const __grid_constant__ BatchParams p, int m) {
-    decode_body<MT, SC, F16, false, true>(&p, nullptr, nullptr, nullptr, nullptr, nullptr, m, 0, 0, 0, 1, 0, 0, 0,
-                                          nullptr, 0, 0);
+    decode_body<MT, SC, F16, false, true>(&p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, m, 0, 0, 0, 1, 0,
+                                          0, 0, nullptr, 0, 0);
+}
+
+// ------------------------------------------------------------ x preparation
+// One warp per (row r < mpad, 128-column K block kb) of x bf16 [m, k]:
+// x16[r, kb*128 ..] = f16(x * 2^e), with the power of two 2^e that moves the
+// block's largest |x| into [2^14, 2^15) -- the converter warp's rescale,
+// done once per call instead of once per CTA -- and
+// inv[kb * 32 + slot(r)] = 2^-e in the slot order the consumer warps read.
+// Padding rows r in [m, mpad) get inv = 1 (their x rows load as zeros).
+__global__ void __launch_bounds__(256) xprep_kernel(const uint16_t *__restrict__ x, int m, int mpad, int k,
+                                                    int kblocks, uint16_t *__restrict__ x16,
+                                                    float *__restrict__ inv) {
+    pdl_launch_dependents();  // the GEMV's prologue may start; it waits for this grid before reading
+    pdl_wait();               // x may come from the previous kernel in the stream
+    const int gw = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    const int r = gw / kblocks, kb = gw - r * kblocks;
+    if (r >= mpad) return;
+    const int c = kb * kKB + lane * 4;
+    const bool in = r < m && c < k;  // k % 4 == 0: a lane's four values are all in or all out
+    uint2 v = make_uint2(0u, 0u);
+    if (in) v = *reinterpret_cast<const uint2 *>(x + static_cast<int64_t>(r) * k + c);
+    const uint32_t mx = max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);  // |max| as bf16 bits
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, o));
+    int e = 0;
+    if (m16 != 0) {
+        const int field = static_cast<int>(m16 >> 7);
+        const int lg = field ? field - 127 : -133;  // floor(log2 |max|) (subnormal: below -126)
+        e = min(126, max(-126, 14 - lg));
+    }
+    const float mult = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+    if (in) {
+        uint2 o;
+        o.x = f32x2_to_f16x2(bf16lo_to_f32(v.x) * mult, bf16hi_to_f32(v.x) * mult);
+        o.y = f32x2_to_f16x2(bf16lo_to_f32(v.y) * mult, bf16hi_to_f32(v.y) * mult);
+        *reinterpret_cast<uint2 *>(x16 + static_cast<int64_t>(r) * k + c) = o;
+    }
+    if (lane == 0)
+        inv[kb * 32 + xinv_slot(r)] = r < m ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 1.0f;
 }
 
 // Per-device, per-instantiation launch setup (shared-memory opt-in and the
@@ -717,11 +767,13 @@ cudaError_t setup_once(Setup &setup, const void *kern, int threads, int smem, in
     return setup.err[dev];
 }
 
-template <int MT, int SC, bool F16>
-cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
-    using C = Cfg<MT, SC == kScaleMx, F16>;
+// XP: a.x is the prepared f16 copy of x and xinv its inverse factors
+// (launch_decode_xprep).
+template <int MT, int SC, bool F16, bool XP = false>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream, const float *xinv = nullptr) {
+    using C = Cfg<MT, SC == kScaleMx, F16, XP>;
     constexpr int kBN = C::kBN;
-    auto kern = decode_kernel<MT, SC, F16>;
+    auto kern = decode_kernel<MT, SC, F16, false, XP>;
     static Setup setup;
     int resident = 1;
     {
@@ -735,8 +787,8 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
                    m = static_cast<uint64_t>(a.m);
     if (!encode_tensor_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, k, n, k, kKB, kBN,
                               CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64,
-                              C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_tensor_map_2d(&tm_x, XP ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x,
+                              k, m, k * 2, 64, C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
@@ -778,7 +830,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, a.e8m0,
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m),
                               static_cast<int>(a.n), kblocks, groups, splits, ntiles, e8m0_vec, a.row_stride,
-                              static_cast<const int32_t *>(nullptr), 0, 0);
+                              static_cast<const int32_t *>(nullptr), 0, 0, xinv);
 }
 
 // A batch launch: one persistent grid over the row tiles of all the ops.
@@ -908,7 +960,7 @@ cudaError_t launch_moe_t(const DecodeArgs &a, const MoeArgs &g, cudaStream_t str
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, static_cast<const uint8_t *>(nullptr),
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m), static_cast<int>(a.n),
                               kblocks, 0, splits, ntiles, 0, 0, g.ids, static_cast<int>(g.topk),
-                              static_cast<int>(g.num_experts));
+                              static_cast<int>(g.num_experts), static_cast<const float *>(nullptr));
 }
 
 template <int SC>
@@ -964,6 +1016,41 @@ cudaError_t launch_decode_batch(const BatchItem *ops, int count, int64_t m, Scal
         case kScaleBlock: return launch_batch_sc<kScaleBlock>(ops, count, m, force, stream);
         case kScaleMx: return launch_batch_sc<kScaleMx>(ops, count, m, force, stream);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+int64_t xprep_bytes(int64_t m, int64_t k) {
+    const int64_t x16 = (2 * m * k + 255) / 256 * 256;
+    return x16 + 128 * ((k + kKB - 1) / kKB);
+}
+
+cudaError_t launch_decode_xprep(const DecodeArgs &a, void *workspace, cudaStream_t stream) {
+    if (a.kind != kScaleBlock || a.m < 1 || a.m > 32) return cudaErrorInvalidValue;
+    const int mt = static_cast<int>((a.m + 7) / 8);
+    const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
+    uint16_t *x16 = static_cast<uint16_t *>(workspace);
+    float *inv = reinterpret_cast<float *>(static_cast<char *>(workspace) + (2 * a.m * a.k + 255) / 256 * 256);
+    const int mpad = 8 * mt;
+    const int64_t warps = static_cast<int64_t>(mpad) * kblocks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((warps + 7) / 8), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, xprep_kernel, static_cast<const uint16_t *>(a.x),
+                                       static_cast<int>(a.m), mpad, static_cast<int>(a.k), kblocks, x16, inv);
+    if (e != cudaSuccess) return e;
+    DecodeArgs b = a;
+    b.x = x16;
+    switch (mt) {
+        case 1: return launch_t<1, kScaleBlock, true, true>(b, stream, inv);
+        case 2: return launch_t<2, kScaleBlock, true, true>(b, stream, inv);
+        case 3: return launch_t<3, kScaleBlock, true, true>(b, stream, inv);
+        default: return launch_t<4, kScaleBlock, true, true>(b, stream, inv);
     }
 }
 

@@ -44,6 +44,13 @@ struct DecodeArgs {
     int row_stride;          // kScaleRow: 1 per row, 0 per tensor
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+// Block-scaled decode (m <= 32) with x prepared once per call: an f16 copy
+// of x with one power-of-two factor per (row, 128-column K block) is written
+// to the caller's workspace by a first kernel and read by every CTA of the
+// decode kernel in place of bf16 x (f16 weight decode at every m, no
+// converter warp).  Workspace: xprep_bytes(m, k) bytes, 16-byte aligned.
+int64_t xprep_bytes(int64_t m, int64_t k);
+cudaError_t launch_decode_xprep(const DecodeArgs &a, void *workspace, cudaStream_t stream);
 // Grouped MoE: a.codes / a.scales hold num_experts block-FP8 weights of
 // [a.n, a.k] back to back; ids [a.m, topk]; a.y is [a.m, topk, a.n].
 struct MoeArgs {

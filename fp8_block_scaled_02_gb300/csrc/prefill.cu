@@ -20,6 +20,13 @@
 //    frees x stages and A slots alike.  Consecutive K blocks write different
 //    partials, so the tensor core never waits on its own accumulator, and
 //    the MMAs of K block kb + 1 overlap the promotion of K block kb.
+//  * MXFP8 (one e8m0 exponent E per 32 K of a row): the decoders fold each
+//    group's 2^(E-127) into the exact bf16 decode -- dec(q) * 2^(E-127) is
+//    itself a bf16 value whenever 3 <= E <= 134 (at most four significant
+//    bits, exponent in range), and above 134 after a second exact multiply
+//    -- so the partials need no promotion and the epilogue sums them as they
+//    are.  Only groups with E < 3 (amax below 2^-116) lose exactness: their
+//    weights round to bf16's subnormal grid (|error| <= 2^-134 each).
 //  * Eight epilogue warps (one per TMEM lane quarter and 128-column half)
 //    read each partial with tcgen05.ld and add it, multiplied by the K
 //    block's fp32 scale, into running totals held in their registers
@@ -124,14 +131,19 @@ __device__ __forceinline__ void setmaxnreg_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// ROW: scales[row * row_stride] per weight row (stride 0: one per tensor)
-// instead of 128x128 block scales.
-template <bool ROW>
+// SC: kScaleBlock (128x128 block scales, promoted per K block), kScaleRow
+// (scales[row * row_stride] per weight row, stride 0: one per tensor,
+// applied to the total) or kScaleMx (e8m0 [n, groups], folded into the
+// decoded weights).
+template <int SC>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                               const uint8_t *__restrict__ codes,
                                                               const float *__restrict__ scales,
+                                                              const uint8_t *__restrict__ e8m0, int groups,
                                                               __nv_bfloat16 *__restrict__ y, int m, int n,
                                                               int k, int kblocks, int row_stride) {
+    constexpr bool ROW = SC == kScaleRow;
+    constexpr bool MX = SC == kScaleMx;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -243,11 +255,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 v[j] = (kb < kblocks && row_ok && col < k) ? ld_codes16(rp + kb * kKB + j * 16) : make_uint4(0, 0, 0, 0);
             }
         };
+        // MX: the row's exponents of the two 32-column groups of this K half
+        // (E = 127, scale 1, past the row's groups: those codes are zero)
+        const uint8_t *ep = MX ? e8m0 + static_cast<int64_t>(row_ok ? row : 0) * groups + 2 * kh : nullptr;
+        auto load_e = [&](int kb) -> uint32_t {
+            uint32_t e = 0x7F7Fu;
+            if (MX && row_ok && kb < kblocks) {
+                const int g = kb * 4 + 2 * kh;
+                if (g < groups) e = (e & 0xFF00u) | __ldg(ep + kb * 4);
+                if (g + 1 < groups) e = (e & 0x00FFu) | (static_cast<uint32_t>(__ldg(ep + kb * 4 + 1)) << 8);
+            }
+            return e;
+        };
         uint4 c0[4], c1[4];
         load4(0, c0);
+        uint32_t e0 = load_e(0), e1 = 0;
         for (int kb = 0; kb < kblocks; ++kb) {
             const int as = kb % kASlots;
             load4(kb + 1, c1);  // in flight while this block is converted
+            if (MX) e1 = load_e(kb + 1);
             // slot `as` was last read by the MMAs of K block kb - kASlots
             const int prev = kb - kASlots;
             bool ok = kb < kASlots || mbar_wait_bounded(&done[prev % kRing], (prev / kRing) & 1);
@@ -256,18 +282,49 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 break;
             }
             uint8_t *arow = aring + as * kASlot + kh * kPanel + r * 128;
+            // decode multiplier per group: 2^120 restores the plain decode;
+            // MX folds 2^(E-127) in: one multiply by 2^(E-7) when that is a
+            // normal bf16 and the result exact (3 <= E <= 134), else 2^120
+            // and a second multiply by 2^(E-127)
+            uint32_t m1[2] = {0x7B807B80u, 0x7B807B80u}, m2[2] = {0u, 0u};
+            bool two[2] = {false, false};
+            if (MX) {
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi) {
+                    const uint32_t E = (e0 >> (8 * gi)) & 0xFFu;
+                    if (E - 3u <= 131u) {
+                        const uint32_t f = (E + 120u) << 7;
+                        m1[gi] = f | (f << 16);
+                    } else {
+                        const uint32_t f = E ? E << 7 : 0x0040u;  // 2^(E-127); E = 0: subnormal 2^-127
+                        m2[gi] = f | (f << 16);
+                        two[gi] = true;
+                    }
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint4 c = c0[j];
+                const int gi = j >> 1;  // 16 codes of one 32-column group
                 uint4 lo, hi;
-                lo.x = e4m3x2_to_bf16x2(c.x, 0x9180u);
-                lo.y = e4m3x2_to_bf16x2(c.x, 0xB3A2u);
-                lo.z = e4m3x2_to_bf16x2(c.y, 0x9180u);
-                lo.w = e4m3x2_to_bf16x2(c.y, 0xB3A2u);
-                hi.x = e4m3x2_to_bf16x2(c.z, 0x9180u);
-                hi.y = e4m3x2_to_bf16x2(c.z, 0xB3A2u);
-                hi.z = e4m3x2_to_bf16x2(c.w, 0x9180u);
-                hi.w = e4m3x2_to_bf16x2(c.w, 0xB3A2u);
+                lo.x = e4m3x2_to_bf16x2_mul(c.x, 0x9180u, m1[gi]);
+                lo.y = e4m3x2_to_bf16x2_mul(c.x, 0xB3A2u, m1[gi]);
+                lo.z = e4m3x2_to_bf16x2_mul(c.y, 0x9180u, m1[gi]);
+                lo.w = e4m3x2_to_bf16x2_mul(c.y, 0xB3A2u, m1[gi]);
+                hi.x = e4m3x2_to_bf16x2_mul(c.z, 0x9180u, m1[gi]);
+                hi.y = e4m3x2_to_bf16x2_mul(c.z, 0xB3A2u, m1[gi]);
+                hi.z = e4m3x2_to_bf16x2_mul(c.w, 0x9180u, m1[gi]);
+                hi.w = e4m3x2_to_bf16x2_mul(c.w, 0xB3A2u, m1[gi]);
+                if (MX && two[gi]) {
+                    lo.x = mul_bf16x2(lo.x, m2[gi]);
+                    lo.y = mul_bf16x2(lo.y, m2[gi]);
+                    lo.z = mul_bf16x2(lo.z, m2[gi]);
+                    lo.w = mul_bf16x2(lo.w, m2[gi]);
+                    hi.x = mul_bf16x2(hi.x, m2[gi]);
+                    hi.y = mul_bf16x2(hi.y, m2[gi]);
+                    hi.z = mul_bf16x2(hi.z, m2[gi]);
+                    hi.w = mul_bf16x2(hi.w, m2[gi]);
+                }
                 *reinterpret_cast<uint4 *>(arow + (((2 * j) ^ (r & 7)) << 4)) = lo;
                 *reinterpret_cast<uint4 *>(arow + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
             }
@@ -276,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (lane == 0) mbar_arrive(&a_full[as]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) c0[j] = c1[j];
+            e0 = e1;
         }
     } else {
         setmaxnreg_inc<kRegEpi>();
@@ -287,16 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int h = (warp - kWarpEpi0) >> 2;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
         const int row = n0 + q * 32 + lane;
-        const float *srow = scales + static_cast<int64_t>(blockIdx.x) * kblocks;
+        const float *srow = (ROW || MX) ? nullptr : scales + static_cast<int64_t>(blockIdx.x) * kblocks;
         float tot[kHalfX];
 #pragma unroll
         for (int j = 0; j < kHalfX; ++j) tot[j] = 0.0f;
         bool ok = true;
         // K block scale (1 with one scale per row: the partials add unscaled)
-        float s_next = ROW ? 1.0f : __ldg(srow);
+        float s_next = (ROW || MX) ? 1.0f : __ldg(srow);
         for (int kb = 0; kb < kblocks; ++kb) {
             const float s = s_next;
-            if (!ROW && kb + 1 < kblocks) s_next = __ldg(srow + kb + 1);
+            if (!ROW && !MX && kb + 1 < kblocks) s_next = __ldg(srow + kb + 1);
             ok = mbar_wait_bounded(&done[kb % kRing], (kb / kRing) & 1);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) fail(ERRBIT_FULL_WAIT);
@@ -343,8 +401,7 @@ cudaError_t g_setup_err[64] = {};
 }  // namespace
 
 cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
-    if (a.kind != kScaleBlock && a.kind != kScaleRow) return cudaErrorNotSupported;
-    const bool row = a.kind == kScaleRow;
+    if (a.kind != kScaleBlock && a.kind != kScaleRow && a.kind != kScaleMx) return cudaErrorNotSupported;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     {
@@ -355,7 +412,7 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
             // fewer than the split was planned against (its epilogue warps
             // would wait forever for registers).
             cudaError_t e = cudaSuccess;
-            for (auto kern : {prefill_kernel<false>, prefill_kernel<true>}) {
+            for (auto kern : {prefill_kernel<kScaleBlock>, prefill_kernel<kScaleRow>, prefill_kernel<kScaleMx>}) {
                 cudaFuncAttributes fa = {};
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -377,9 +434,11 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>((a.n + kTileW - 1) / kTileW), static_cast<unsigned>((a.m + kTileX - 1) / kTileX));
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(a.y);
     const int mi = static_cast<int>(a.m), ni = static_cast<int>(a.n), ki = static_cast<int>(a.k);
-    auto kern = row ? prefill_kernel<true> : prefill_kernel<false>;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, a.codes, a.scales, y, mi, ni, ki, kblocks,
-                                                 row ? a.row_stride : 0);
+    auto kern = a.kind == kScaleRow ? prefill_kernel<kScaleRow>
+                                    : (a.kind == kScaleMx ? prefill_kernel<kScaleMx> : prefill_kernel<kScaleBlock>);
+    const int groups = static_cast<int>((a.k + 31) / 32);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, a.codes, a.scales, a.e8m0, groups, y, mi, ni, ki, kblocks,
+                                                 a.kind == kScaleRow ? a.row_stride : 0);
     return cudaGetLastError();
 }
 

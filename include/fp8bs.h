@@ -57,7 +57,7 @@ typedef enum {
     FP8BS_PATH_DECODE = 1,   /* TMA-staged skinny kernel, m <= 32 per launch
                                 (larger m runs in chunks of 32 rows)          */
     FP8BS_PATH_PREFILL = 2,  /* tcgen05 tensor-core kernel (block / row / tensor
-                                scales; not MXFP8)                           */
+                                scales, MXFP8)                               */
     FP8BS_PATH_GENERIC = 3   /* plain-load kernel for any shape / alignment    */
 } fp8bs_path;
 
@@ -124,6 +124,38 @@ int fp8bs_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
                   int path, void *stream);
 
 /*
+ * fp8bs_gemv_ws -- fp8bs_gemv with caller-provided device scratch, for the
+ * decode path (m <= 32, k % 16 == 0, 16-byte aligned x and codes): a first
+ * kernel writes an f16 copy of x with one power-of-two factor per (row,
+ * 128-column K block) -- the largest |x| of the block moved into
+ * [2^14, 2^15), every x within 2^-31 of it converting exactly -- into the
+ * workspace, and the GEMV reads it in place of x: e4m3 codes then enter the
+ * tensor cores as f16 (one conversion per code pair) at every m, where
+ * fp8bs_gemv decodes to bf16 above m = 8.  The result obeys the same
+ * definition and tolerance as fp8bs_gemv; the factor's inverse multiplies
+ * each K block's fp32 partial together with the block scale.
+ *
+ * Defined by: InfiniLM PR #586 (Notes for Reviewers: 9 <= M <= 32 decode
+ * batches on the tensor-core path) for the arithmetic, which is fp8bs_gemv's.
+ *
+ *   workspace        device, 16-byte aligned, >= fp8bs_gemv_ws_bytes(m, k)
+ *                    bytes; its contents on entry do not matter, and it may
+ *                    be reused once the call's work on `stream` is done
+ *   other arguments  as fp8bs_gemv
+ * Calls that do not take the decode path (m > 32: tensor-core prefill;
+ * unaligned or k % 16 != 0: generic kernel) ignore the workspace.
+ * FP8BS_ERR_NULL / FP8BS_ERR_ALIGN / FP8BS_ERR_SHAPE for a missing,
+ * misaligned or too small workspace, before anything is launched.
+ *
+ * fp8bs_gemv_ws_bytes: bytes of workspace fp8bs_gemv_ws needs for m rows
+ * of x with k columns (0 for m = 0), or FP8BS_ERR_SHAPE.  Host only.
+ */
+int64_t fp8bs_gemv_ws_bytes(int64_t m, int64_t k);
+int fp8bs_gemv_ws(const void *x_bf16, int64_t m, const uint8_t *codes,
+                  const float *scales, int64_t n, int64_t k, void *y_bf16,
+                  void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
  * mxfp8_quantize -- load-time MXFP8 requantization: per row, per group of 32
  * consecutive k (the last group may be shorter), e = the smallest integer with
  * 448 * 2^e >= amax (i.e. 2^ceil(log2(amax/448))), E = clamp(e + 127, 0, 254)
@@ -146,15 +178,20 @@ int mxfp8_quantize(const void *w_bf16, int64_t n, int64_t k,
 /*
  * mxfp8_gemv -- W8A16 linear over MXFP8 weights:
  *   y[i, j] = bf16_rn( sum_g 2^(E[j,g]-127) * sum_{c in g} x[i, c] * dec(q[j, c]) )
- * Same argument rules as fp8bs_gemv, with scales_e8m0 [n, ceil(k/32)].
- * Defined by: FreeToken issue #624 (the "mxfp8_linear W8A16 path").
- * m > 32 runs the decode kernel in chunks of 32 rows.
+ * Same argument rules and paths as fp8bs_gemv, with scales_e8m0
+ * [n, ceil(k/32)].  Defined by: FreeToken issue #624 (the "mxfp8_linear
+ * W8A16 path", which serves every batch size).
+ * m > 32 runs on the tensor cores (PREFILL): each group's 2^(E-127) is
+ * folded into the exact bf16 decode of its weights, which is exact for
+ * every group with 3 <= E (amax >= 2^-116); groups with a smaller E have
+ * their scaled weights rounded to bf16's subnormal grid (|error| <= 2^-134
+ * per weight).
  */
 int mxfp8_gemv(const void *x_bf16, int64_t m, const uint8_t *codes,
                const uint8_t *scales_e8m0, int64_t n, int64_t k, void *y_bf16,
                void *stream);
 
-/* mxfp8_gemv with an explicit path (AUTO, DECODE or GENERIC). */
+/* mxfp8_gemv with an explicit path (AUTO, DECODE, PREFILL or GENERIC). */
 int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
                   const uint8_t *scales_e8m0, int64_t n, int64_t k,
                   void *y_bf16, int path, void *stream);
@@ -195,8 +232,8 @@ int mxfp8_gemv_ex(const void *x_bf16, int64_t m, const uint8_t *codes,
  * allocated or written besides y), so the call can be captured in a CUDA
  * graph.  _ex: path AUTO as above; DECODE runs every eligible run through the
  * batched kernel whatever its size (FP8BS_ERR_PATH if an op cannot take the
- * decode kernel); PREFILL / GENERIC run every op as fp8bs_gemv_ex with that
- * path.
+ * decode kernel); PREFILL / GENERIC run every op as fp8bs_gemv_ex
+ * (mxfp8_gemv_ex) with that path.
  */
 typedef struct fp8bs_gemv_op {
     const void *x_bf16;

@@ -36,6 +36,7 @@ int main(void)
     void (*const entry_points[])(void) = {
         (void (*)(void))fp8bs_quantize,        (void (*)(void))fp8bs_gemv,
         (void (*)(void))fp8bs_gemv_ex,         (void (*)(void))fp8bs_gemv_batch,
+        (void (*)(void))fp8bs_gemv_ws,         (void (*)(void))fp8bs_gemv_ws_bytes,
         (void (*)(void))fp8bs_gemv_batch_ex,   (void (*)(void))mxfp8_quantize,
         (void (*)(void))mxfp8_gemv,            (void (*)(void))mxfp8_gemv_ex,
         (void (*)(void))mxfp8_gemv_batch,      (void (*)(void))mxfp8_gemv_batch_ex,
@@ -92,11 +93,19 @@ int main(void)
     EXPECT(fp8bs_gemv_ex(x, 1, c, s, 10, 10, y, 9, NULL), FP8BS_ERR_PATH);
     EXPECT(fp8bs_gemv_ex(x, 1, c, s, 10, 10, y, FP8BS_PATH_DECODE, NULL), FP8BS_ERR_PATH);
     EXPECT(mxfp8_gemv(x, 1, c, NULL, 10, 32, y, NULL), FP8BS_ERR_NULL);
-    EXPECT(mxfp8_gemv_ex(x, 1, c, c, 10, 32, y, FP8BS_PATH_PREFILL, NULL), FP8BS_ERR_PATH);
+    EXPECT(mxfp8_gemv_ex(x, 40, c, c, 10, 24, y, FP8BS_PATH_PREFILL, NULL), FP8BS_ERR_PATH);
     EXPECT(fp8row_gemv(x, 1, c, s, 0, 10, y, NULL), FP8BS_ERR_SHAPE);
     EXPECT(fp8row_gemv_ex(x, 40, c, s, 10, 24, y, FP8BS_PATH_PREFILL, NULL), FP8BS_ERR_PATH);
     EXPECT(fp8tensor_gemv(x, 1, NULL, s, 10, 10, y, NULL), FP8BS_ERR_NULL);
     EXPECT(fp8tensor_gemv_ex(x, 1, c, s, 10, 10, y, -1, NULL), FP8BS_ERR_PATH);
+
+    /* caller-provided workspace (decode path) */
+    const int64_t need = fp8bs_gemv_ws_bytes(16, 4096);
+    EXPECT(need == 2 * 16 * 4096 + 128 * 32, 1);
+    EXPECT((int)fp8bs_gemv_ws_bytes(-1, 4096), FP8BS_ERR_SHAPE);
+    EXPECT(fp8bs_gemv_ws(x, 16, c, s, 256, 4096, y, NULL, need, NULL), FP8BS_ERR_NULL);
+    EXPECT(fp8bs_gemv_ws(x, 16, c, s, 256, 4096, y, A(0x50008), need, NULL), FP8BS_ERR_ALIGN);
+    EXPECT(fp8bs_gemv_ws(x, 16, c, s, 256, 4096, y, A(0x50000), need - 1, NULL), FP8BS_ERR_SHAPE);
 
     /* batches: validated op by op before anything is launched */
     fp8bs_gemv_op ops[2] = {
@@ -114,6 +123,7 @@ int main(void)
     ops[1].k = 256;
     ops[1].scales = A(0x30002);
     EXPECT(fp8bs_gemv_batch(ops, 2, 1, NULL), FP8BS_ERR_ALIGN);
+    ops[1].k = 200;
     EXPECT(mxfp8_gemv_batch_ex(ops, 2, 40, FP8BS_PATH_PREFILL, NULL), FP8BS_ERR_PATH);
 
     /* W8A8, MoE, KV cache */

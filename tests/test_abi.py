@@ -32,7 +32,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "fp8bs_gemv_batch", "fp8bs_gemv_batch_ex",
+    for want in ("fp8bs_quantize", "fp8bs_gemv", "fp8bs_gemv_ex", "fp8bs_gemv_ws", "fp8bs_gemv_ws_bytes",
+                 "fp8bs_gemv_batch", "fp8bs_gemv_batch_ex",
                  "mxfp8_gemv_batch", "mxfp8_gemv_batch_ex", "mxfp8_quantize", "mxfp8_gemv",
                  "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                  "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
@@ -92,7 +93,7 @@ def test_gemv_validation(L):
     # an explicit path that cannot take the shape is refused before launch
     assert L.fp8bs_gemv_ex(x, 1, c, s, 10, 10, y, 1, None) == -7    # decode needs k % 16 == 0
     assert L.fp8bs_gemv_ex(x, 1, P(0x20001), s, 10, 32, y, 1, None) == -7  # decode needs aligned codes
-    assert L.mxfp8_gemv_ex(x, 1, c, s, 10, 32, y, 2, None) == -7    # no MX prefill path
+    assert L.mxfp8_gemv_ex(x, 40, c, s, 10, 24, y, 2, None) == -7   # the MX prefill needs k % 16 == 0
     assert L.mxfp8_gemv(x, 1, c, None, 10, 32, y, None) == -1
 
 
@@ -119,9 +120,24 @@ def test_gemv_batch_validation(L):
         # the decode path needs k % 16 == 0 and 16-byte aligned x and codes
         assert fx(batch(good, (0x10000, 0x20000, 0x30000, 0x40000, 128, 200)), 2, 1, 1, None) == -7
         assert fx(batch(good, (0x10008, 0x20000, 0x30000, 0x40000, 128, 256)), 2, 1, 1, None) == -7
-    # block scales must be 4-byte aligned; no MX prefill path
+    # block scales must be 4-byte aligned; the prefill path needs k % 16 == 0
     assert L.fp8bs_gemv_batch(batch(good, (0x10000, 0x20000, 0x30002, 0x40000, 128, 256)), 2, 1, None) == -4
-    assert L.mxfp8_gemv_batch_ex(batch(good), 1, 40, 2, None) == -7
+    assert L.mxfp8_gemv_batch_ex(batch((0x10000, 0x20000, 0x30000, 0x40000, 128, 200)), 1, 40, 2, None) == -7
+
+
+def test_gemv_ws_validation(L):
+    x, c, s, y, w = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000)
+    need = L.fp8bs_gemv_ws_bytes(16, 4096)
+    assert need == 2 * 16 * 4096 + 128 * 32               # f16 copy of x + one factor per (row slot, K block)
+    assert L.fp8bs_gemv_ws_bytes(0, 4096) == 0
+    assert L.fp8bs_gemv_ws_bytes(100, 4096) == L.fp8bs_gemv_ws_bytes(32, 4096)  # decode chunks of 32 rows
+    assert L.fp8bs_gemv_ws_bytes(-1, 4096) == -2 and L.fp8bs_gemv_ws_bytes(1, 0) == -2
+    assert L.fp8bs_gemv_ws(x, 16, c, s, 256, 4096, y, None, need, None) == -1        # decode path needs it
+    assert L.fp8bs_gemv_ws(x, 16, c, s, 256, 4096, y, P(0x50008), need, None) == -4  # 16-byte aligned
+    assert L.fp8bs_gemv_ws(x, 16, c, s, 256, 4096, y, w, need - 1, None) == -2       # too small
+    assert L.fp8bs_gemv_ws(x, -1, c, s, 256, 4096, y, w, need, None) == -2
+    assert L.fp8bs_gemv_ws(None, 0, None, None, 256, 4096, None, None, 0, None) == 0  # m == 0: no-op
+    assert L.fp8bs_gemv_ws(x, 16, c, P(0x30002), 256, 4096, y, w, need, None) == -4
 
 
 def test_rowwise_validation(L):
@@ -214,7 +230,7 @@ def test_select_path(L):
     assert L.fp8bs_select_path(1, 100, 4096, a16, c16, 0) == 1          # decode
     assert L.fp8bs_select_path(32, 100, 4096, a16, c16, 0) == 1
     assert L.fp8bs_select_path(33, 100, 4096, a16, c16, 0) == 2         # prefill
-    assert L.fp8bs_select_path(4096, 100, 4096, a16, c16, 1) == 1       # MX: decode in chunks
+    assert L.fp8bs_select_path(4096, 100, 4096, a16, c16, 1) == 2       # MX: tensor cores too
     assert L.fp8bs_select_path(1, 100, 4100, a16, c16, 0) == 3          # k % 16 != 0 -> generic
     assert L.fp8bs_select_path(1, 100, 4096, P(0x10008), c16, 0) == 3   # x not 16-byte aligned
     assert L.fp8bs_select_path(0, 100, 4096, a16, c16, 0) == -2

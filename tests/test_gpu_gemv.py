@@ -120,6 +120,84 @@ def test_small_shapes_mx(pkg, n, k, m):
         check_mx_gemv(y, bits(x), np.arange(n), oc, oe)
 
 
+@pytest.mark.parametrize("m", [1, 8, 16, 32, 40, 130])
+def test_mx_extreme_group_exponents(pkg, m):
+    """MXFP8 groups whose exponent E lies outside [3, 134] (amax below
+    2^-116 or above 57344) cannot carry their scale inside a bf16 weight; a
+    K block holding one takes the per-group fp32 promotion instead of the
+    folded decode.  Rows with tiny groups, huge groups, a single tiny group
+    among normal ones, and ordinary rows, at every path."""
+    g = torch.Generator().manual_seed(21)
+    w = torch.randn((256, 512), generator=g) * 0.02
+    w[0:16, :] *= 2.0 ** -115          # every group tiny: E = 0
+    w[16:32, 128:256] *= 2.0 ** 24     # one K block of huge groups: E > 134
+    w[32:48, 32:64] *= 2.0 ** -115     # one tiny group among normal ones
+    w = w.to(torch.bfloat16)
+    oc, oe = oracle.mx_quantize(bits(w))
+    assert oe[0:16].max() < 3 and oe[16:32, 4:8].min() > 134
+    x = inputs.activations(m, 512, 31 + m)
+    for path in (0, PATH_DECODE, PATH_GENERIC) + ((PATH_PREFILL,) if m > 32 else ()):
+        y = pkg.mx_gemv(x.to(DEV), to_dev_bits(oc), to_dev_bits(oe), path=path)
+        for rows in (np.arange(0, 16), np.arange(16, 32), np.arange(32, 48), np.arange(48, 256)):
+            check_mx_gemv(y[:, torch.from_numpy(rows).to(DEV)], bits(x), np.arange(len(rows)), oc[rows], oe[rows])
+
+
+@pytest.mark.parametrize("scale_e", [127, 130, 100, 140])
+def test_mx_prefill_every_code_exact(pkg, scale_e):
+    """The MX prefill folds 2^(E-127) into the decoded bf16 weight: with one
+    exponent for every group, row i holding code i at column 3 and x = e_3,
+    y[:, i] = bf16(dec(i) * 2^(E-127)) exactly (one multiply for E in
+    [3, 134], two above)."""
+    codes_list = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    n, k, m = len(codes_list), 64, 40
+    w = np.zeros((n, k), dtype=np.uint8)
+    w[:, 3] = codes_list
+    e8m0 = np.full((n, 2), scale_e, dtype=np.uint8)
+    x = np.zeros((m, k), dtype=np.uint16)
+    x[:, 3] = 0x3F80
+    y = pkg.mx_gemv(bf16_dev(x), to_dev_bits(w), to_dev_bits(e8m0), path=PATH_PREFILL)
+    want = np.array([oracle.double_to_bf16(0.0 + v * 2.0 ** (scale_e - 127)) for v in table()[codes_list]],
+                    dtype=np.uint16)
+    got = bits(y.cpu())
+    for i in range(m):
+        assert np.array_equal(got[i], want), np.argwhere(got[i] != want)[:5]
+
+
+MX_PREFILL_SHAPES = [(129, 272), (256, 1024), (520, 640), (300, 16), (1, 128), (37, 48)]
+
+
+@pytest.mark.parametrize("n,k", MX_PREFILL_SHAPES)
+@pytest.mark.parametrize("m", [33, 128, 130, 257])
+def test_mx_prefill_small_shapes(pkg, n, k, m):
+    w = inputs.heavy_tail_weight(7, shape=(n, k), frac=0.01)
+    oc, oe = oracle.mx_quantize(bits(w))
+    x = inputs.activations(m, k, 13 + m)
+    for path in (0, PATH_PREFILL):
+        y = pkg.mx_gemv(x.to(DEV), to_dev_bits(oc), to_dev_bits(oe), path=path)
+        check_mx_gemv(y, bits(x), np.arange(n), oc, oe)
+
+
+def test_mx_prefill_full_size_sampled(pkg):
+    """The MXFP8 [18432, 7168] weight (0.1% Student-t entries) at prefill
+    sizes: sampled weight rows (oracle codes installed) and sampled x rows."""
+    w = inputs.heavy_tail_weight(5, device=DEV)
+    n, k = w.shape
+    codes, e8m0 = pkg.mx_quantize(w)
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 126)]))
+    oc, oe = oracle.mx_quantize(bits(w[torch.from_numpy(rows).to(DEV)].cpu()))
+    ridx = torch.from_numpy(rows).to(DEV)
+    codes[ridx] = to_dev_bits(oc)
+    e8m0[ridx] = to_dev_bits(oe)
+    for m in (64, 512, 2048):
+        x = inputs.activations(m, k, 60 + m, device=DEV)
+        y = pkg.mx_gemv(x, codes, e8m0)
+        torch.cuda.synchronize()
+        xr = np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, 14)]))
+        xb = bits(x[torch.from_numpy(xr).to(DEV)].cpu())
+        check_mx_gemv(y[torch.from_numpy(xr).to(DEV)], xb, rows, oc, oe)
+
+
 PREFILL_SHAPES = [(129, 272), (256, 1024), (64, 4096), (300, 16), (1, 128), (520, 640)]
 
 
@@ -231,6 +309,96 @@ def test_x_dynamic_range(pkg, m, case):
         y = pkg.gemv(x.to(DEV), to_dev_bits(oc), torch.from_numpy(os_).to(DEV), path=path)
         rows_q = {rb: (oc[rb * 128:rb * 128 + 128], os_[rb]) for rb in range(3)}
         check_block_gemv(y, bits(x), rows_q)
+
+
+# ----------------------------------- prepared x (fp8bs_gemv_ws, workspace)
+def ws_for(pkg, m, k, fill=0xFF):
+    """A workspace of the size gemv_ws needs, filled with NaN bytes: its
+    contents on entry must not matter."""
+    return torch.full((pkg.gemv_ws_bytes(m, k),), fill, dtype=torch.uint8, device=DEV)
+
+
+@pytest.mark.parametrize("m", [1, 2, 5, 8, 9, 13, 16, 17, 24, 31, 32])
+def test_ws_tiny_ragged(pkg, m):
+    w = inputs.tiny_ragged_weight(0)
+    n, k = w.shape
+    oc, os_ = oracle.block_quantize(bits(w))
+    x = inputs.activations(m, k, 70 + m)
+    y, raw = guarded_empty((m, n), torch.bfloat16, DEV)
+    pkg.gemv_ws(x.to(DEV), to_dev_bits(oc), torch.from_numpy(os_).to(DEV), ws_for(pkg, m, k), y=y)
+    torch.cuda.synchronize()
+    assert guard_intact(raw, m * n * 2)
+    rows_q = {rb: (oc[rb * 128:rb * 128 + 128], os_[rb]) for rb in range(-(-n // 128))}
+    check_block_gemv(y, bits(x), rows_q)
+
+
+@pytest.mark.parametrize("n,k", [(37, 48), (129, 272), (513, 1024), (64, 4096), (300, 16)])
+@pytest.mark.parametrize("m", [1, 8, 19, 32])
+def test_ws_small_shapes(pkg, n, k, m):
+    w = inputs.gaussian_bf16((n, k), 0.02, n * 31 + k)
+    oc, os_ = oracle.block_quantize(bits(w))
+    x = inputs.activations(m, k, 7)
+    y = pkg.gemv_ws(x.to(DEV), to_dev_bits(oc), torch.from_numpy(os_).to(DEV), ws_for(pkg, m, k))
+    rows_q = {rb: (oc[rb * 128:rb * 128 + 128], os_[rb]) for rb in range(-(-n // 128))}
+    check_block_gemv(y, bits(x), rows_q)
+
+
+def test_ws_sweep_shape_all_m(pkg):
+    w = inputs.sweep_weight(0, device=DEV)
+    n, k = w.shape
+    codes, scales = pkg.quantize(w)
+    rows_q = {}
+    for rb in _row_blocks(n, 2, 5):
+        c, s = oracle.block_quantize(bits(w[rb * 128:rb * 128 + 128].cpu()))
+        rows_q[int(rb)] = (c, s[0])
+    install_block_rows(codes, scales, rows_q)
+    ws = ws_for(pkg, 32, k)
+    for m in range(1, 33):
+        x = inputs.activations(m, k, 11 + m, device=DEV)
+        y = pkg.gemv_ws(x, codes, scales, ws)   # one workspace reused by every call
+        torch.cuda.synchronize()
+        check_block_gemv(y, bits(x.cpu()), rows_q)
+
+
+@pytest.mark.parametrize("m", [4, 16, 32])
+@pytest.mark.parametrize("case", ["wide_range", "tiny", "huge", "single_spike"])
+def test_ws_x_dynamic_range(pkg, m, case):
+    """The prepared f16 copy of x takes one power of two per (row, K block):
+    activations spanning 60 decades, all tiny, all huge, or one spike per
+    row stay within tolerance."""
+    w = inputs.gaussian_bf16((384, 1024), 0.02, 77)
+    oc, os_ = oracle.block_quantize(bits(w))
+    g = torch.Generator().manual_seed(5)
+    base = torch.randn((m, 1024), generator=g)
+    if case == "wide_range":
+        x = base * torch.pow(10.0, torch.randint(-30, 30, (m, 1024), generator=g).to(torch.float32))
+    elif case == "tiny":
+        x = base * 1e-35
+    elif case == "huge":
+        x = base * 1e30
+    else:
+        x = base.clone()
+        x[:, 37] = 3e20
+    x = x.to(torch.bfloat16)
+    y = pkg.gemv_ws(x.to(DEV), to_dev_bits(oc), torch.from_numpy(os_).to(DEV), ws_for(pkg, m, 1024))
+    rows_q = {rb: (oc[rb * 128:rb * 128 + 128], os_[rb]) for rb in range(3)}
+    check_block_gemv(y, bits(x), rows_q)
+
+
+def test_ws_every_code_exact_and_prefill_ignores_it(pkg):
+    codes_list = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    n, k = len(codes_list), 32
+    w = np.zeros((n, k), dtype=np.uint8)
+    w[:, 3] = codes_list
+    scales = np.ones((-(-n // 128), 1), dtype=np.float32)
+    want = np.array([oracle.double_to_bf16(0.0 + v) for v in table()[codes_list]], dtype=np.uint16)
+    for m in (1, 9, 32, 40):   # 40: the prefill path, which needs no workspace
+        x = np.zeros((m, k), dtype=np.uint16)
+        x[:, 3] = 0x3F80
+        y = pkg.gemv_ws(bf16_dev(x), to_dev_bits(w), torch.from_numpy(scales).to(DEV), ws_for(pkg, m, k))
+        got = bits(y.cpu())
+        for i in range(m):
+            assert np.array_equal(got[i], want)
 
 
 def test_repeat_is_deterministic(pkg):
