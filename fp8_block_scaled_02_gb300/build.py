@@ -17,7 +17,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG_DIR), "include")
 OUT_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfp8bs.so")
 
-SOURCES = ["api.cu", "quantize.cu", "decode.cu", "generic.cu", "prefill.cu", "w8a8.cu", "kvattn.cu", "tensormap.cu"]
+SOURCES = ["api.cu", "quantize.cu", "decode.cu", "generic.cu", "prefill.cu", "w8a8.cu", "kvattn.cu", "tensormap.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I", CSRC, "-I", INCLUDE]

@@ -156,6 +156,39 @@ int fp8bs_gemv_ws(const void *x_bf16, int64_t m, const uint8_t *codes,
                   void *workspace, int64_t workspace_bytes, void *stream);
 
 /*
+ * fp8bs_gemv_noalloc -- fp8bs_gemv_ws without a caller workspace, for
+ * callers that cannot allocate device memory: a plugin whose host framework
+ * owns all device memory through its own pool, a real-time loop that cannot
+ * afford cudaMalloc / cudaFree (cudaFree synchronises the device), or a C
+ * caller with nowhere to keep a buffer.  The scratch fp8bs_gemv_ws would
+ * take from the caller (the f16 copy of x and its per-block factors) comes
+ * from a fixed array of FP8BS_NOALLOC_SCRATCH_BYTES in the library's own
+ * device memory; the call allocates and frees nothing.
+ *
+ * Defined by: no passage of the source pages has a counterpart; the
+ * arithmetic and tolerance are fp8bs_gemv's (fp8bs_gemv_ws's).
+ *
+ *   arguments  as fp8bs_gemv (x, codes, scales, y are the caller's)
+ *   returns    FP8BS_ERR_SHAPE, before anything is launched, when the
+ *              decode path would need more scratch than the array holds:
+ *              fp8bs_gemv_ws_bytes(m, k) > FP8BS_NOALLOC_SCRATCH_BYTES
+ *              (2 MiB: m = 32 with k up to 32,256).  Calls that do not take
+ *              the decode path (m > 32, unaligned, k % 16 != 0) need no
+ *              scratch and run as fp8bs_gemv.
+ * Every device that loads the library holds the array until the process
+ * exits.  The first call on each device looks up the array's device address
+ * once (cudaGetSymbolAddress, with that device current): make that first
+ * call before any stream capture.  Every call shares the one array and
+ * leaves its contents behind; each call writes all it reads, so nothing has
+ * to be cleared, but calls that overlap on the GPU (different streams, no
+ * ordering between them) race on it.  Calls on one stream are ordered.
+ */
+#define FP8BS_NOALLOC_SCRATCH_BYTES (2 * 1024 * 1024)
+int fp8bs_gemv_noalloc(const void *x_bf16, int64_t m, const uint8_t *codes,
+                       const float *scales, int64_t n, int64_t k, void *y_bf16,
+                       void *stream);
+
+/*
  * mxfp8_quantize -- load-time MXFP8 requantization: per row, per group of 32
  * consecutive k (the last group may be shorter), e = the smallest integer with
  * 448 * 2^e >= amax (i.e. 2^ceil(log2(amax/448))), E = clamp(e + 127, 0, 254)
