@@ -53,6 +53,7 @@ def measured_peaks():
 
 KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "common.cuh"],
+    "gemv_batch_kernel": ["decode.cu", "common.cuh"],
     "prefill_kernel": ["prefill.cu", "common.cuh"],
     "block_quantize_kernel": ["quantize.cu", "common.cuh"],
 }
@@ -207,8 +208,18 @@ LM_HEAD_METRIC = "block-FP8 W8A16 GEMV HBM GB/s (lm_head, M=1,4,8,16)"
 
 def lm_head_config(n, k, ms):
     return {"workload": "lm_head [152064,4096] block-FP8 (128x128 fp32 scales) W8A16 GEMV, one call at each "
-                        "of M=1,4,8,16 per step", "n": n, "k": k, "ms": ms,
+                        "of M=1,4,8,16 per step (M > 8 through fp8bs_gemv_ws: x prepared once per call in a "
+                        "workspace allocated before the timed region)", "n": n, "k": k, "ms": ms,
             "l2": "inputs larger than L2 (623 MB of codes per call)"}
+
+
+def lm_head_call(fp8bs, m, x, codes, scales, y, ws):
+    """The library's fastest call for this M: above M = 8 the workspace GEMV
+    (f16 operands at every M) beats the bf16 decode on this weight."""
+    if m > 8:
+        fp8bs.gemv_ws(x, codes, scales, ws, y=y)
+    else:
+        fp8bs.gemv(x, codes, scales, y=y)
 
 
 def lm_head_workload(torch, fp8bs, inputs, dev):
@@ -219,17 +230,19 @@ def lm_head_workload(torch, fp8bs, inputs, dev):
     del w
     xs = {m: inputs.activations(m, k, 100 + m, device=dev) for m in ms}
     ys = {m: torch.empty((m, n), dtype=torch.bfloat16, device=dev) for m in ms}
-    calls = [(f"M={m}", m, gemv_bytes(m, n, k), (lambda m=m: fp8bs.gemv(xs[m], codes, scales, y=ys[m])))
-             for m in ms]
+    ws = torch.empty((fp8bs.gemv_ws_bytes(max(ms), k),), dtype=torch.uint8, device=dev)
+    calls = [(f"M={m}", m, gemv_bytes(m, n, k),
+              (lambda m=m: lm_head_call(fp8bs, m, xs[m], codes, scales, ys[m], ws))) for m in ms]
     cfg = lm_head_config(n, k, ms)
     return dict(calls=calls, xs=xs, ys=ys, cfg=cfg, dominant=("decode_kernel<1,0,true>", [0, 1, 2]),
-                codes=codes, scales=scales, n=n, k=k, mx=False)
+                codes=codes, scales=scales, ws=ws, n=n, k=k, mx=False,
+                call_launches=[2 if m > 8 else 1 for m in ms])
 
 
-def rotation_weights(fp8bs, inputs, dev, scales="block"):
+def rotation_weights(fp8bs, inputs, dev, scales="block", layers=None):
     quant, _ = quantizer(fp8bs, scales)
     weights = []
-    for l in range(inputs.ROTATION_LAYERS):
+    for l in range(inputs.ROTATION_LAYERS if layers is None else layers):
         for j in range(4):
             w = inputs.rotation_weight(l, j, device=dev)
             weights.append(quant(w))
@@ -237,14 +250,15 @@ def rotation_weights(fp8bs, inputs, dev, scales="block"):
     return weights
 
 
-def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True, weights=None):
+def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True, weights=None, layers=None):
     """48 layers x 4 projection weights, one GEMV each per step.  batched:
     the step is one fp8bs_gemv_batch call (the 192 GEMVs stream as two
-    persistent launches); otherwise one fp8bs_gemv call per weight."""
-    layers = inputs.ROTATION_LAYERS
+    persistent launches); otherwise one fp8bs_gemv call per weight.
+    `layers` < 48 gives a smaller case of the same kernels (profiling)."""
+    layers = inputs.ROTATION_LAYERS if layers is None else layers
     quant, gemv = quantizer(fp8bs, scales)
     if weights is None:
-        weights = rotation_weights(fp8bs, inputs, dev, scales)
+        weights = rotation_weights(fp8bs, inputs, dev, scales, layers)
     shapes = [inputs.ROTATION_SHAPES[j] for _ in range(layers) for j in range(4)]
     xs = [inputs.activations(m, k, 7 + i, device=dev) for i, (n, k) in enumerate(shapes)]
     ys = [torch.empty((m, n), dtype=torch.bfloat16, device=dev) for (n, k) in shapes]
@@ -260,10 +274,11 @@ def rotation_workload(torch, fp8bs, inputs, dev, m, scales="block", batched=True
     total = sum(gemv_bytes(m, n, k, scales=scales) for (n, k) in shapes)
     kind = {"block": "block-FP8", "row": "per-row FP8", "tensor": "per-tensor FP8"}[scales]
     how = "one batched call (fp8bs_gemv_batch)" if batched else "one call per weight"
-    cfg = {"workload": f"decode dense-projection rotation: 48 layers x 4 {kind} weights "
-                       f"([8192,2560],[2560,3072],[6656,2560],[2560,3072]), M={m}, 192 GEMVs per step, "
-                       f"{how}, CUDA graph", "ms": [m], "l2": "inputs larger than L2 (2.58 GB of codes per step)"}
-    launches = 2 if batched else 192
+    cfg = {"workload": f"decode dense-projection rotation: {layers} layers x 4 {kind} weights "
+                       f"([8192,2560],[2560,3072],[6656,2560],[2560,3072]), M={m}, {4 * layers} GEMVs per step, "
+                       f"{how}, CUDA graph", "ms": [m],
+           "l2": f"inputs larger than L2 ({total / 1e9:.2f} GB of codes per step)"}
+    launches = -(-4 * layers // 96) if batched else 4 * layers
     mt = (m + 7) // 8
     dom = f"gemv_batch_kernel<{mt},0,{'true' if mt == 1 else 'false'}>" if batched else "decode_kernel"
     return dict(calls=[(f"rotation M={m}", m, total, step)], cfg=cfg, graph=True, launches_per_step=launches,
@@ -580,7 +595,7 @@ def e2e_lm_head(torch, fp8bs, wl, steps, warmup, pg):
             stream.wait_event(ev[(m, b, "x")])
             if (m, b) in used:  # dy[m][b]'s previous read-back has landed
                 stream.wait_event(ev[(m, b, "y")])
-            fp8bs.gemv(dx[m][b], wl["codes"], wl["scales"], y=dy[m][b])
+            lm_head_call(fp8bs, m, dx[m][b], wl["codes"], wl["scales"], dy[m][b], wl["ws"])
             ev[(m, b, "gemv")].record(stream)
             d2h_s.wait_event(ev[(m, b, "gemv")])
             with torch.cuda.stream(d2h_s):
@@ -822,6 +837,7 @@ def main():
                     choices=["lm_head", "rotation", "sweep", "mx", "mx_prefill", "quantize", "prefill", "rowwise", "w8a8",
                              "w8a8_prefill", "moe", "kv"])
     ap.add_argument("--m", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=None, help="rotation: fewer layers than 48 (a smaller case)")
     ap.add_argument("--single", action="store_true", help="rotation: one GEMV call per weight, not one batch")
     ap.add_argument("--ws", action="store_true", help="sweep: call fp8bs_gemv_ws (x prepared in a workspace)")
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
@@ -870,7 +886,8 @@ def main():
     if args.workload == "lm_head":
         wl = lm_head_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "rotation":
-        wl = rotation_workload(torch, fp8bs, inputs, dev, args.m, args.scales, batched=not args.single)
+        wl = rotation_workload(torch, fp8bs, inputs, dev, args.m, args.scales, batched=not args.single,
+                               layers=args.layers)
     elif args.workload == "sweep":
         wl = sweep_workload(torch, fp8bs, inputs, dev, list(range(1, 33)), ws=args.ws)
     elif args.workload == "mx":

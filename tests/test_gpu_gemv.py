@@ -267,6 +267,17 @@ def test_prefill_shapes_sampled(pkg):
                        x_rows=lambda m: np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, 14)])))
 
 
+def test_prefill_large_weight_tile_order(pkg):
+    """A weight whose codes exceed 64 MiB runs the prefill with the x tiles
+    fastest on the grid (the smaller weights above run weight tiles
+    fastest): block scales must still be read from the right tile row."""
+    w = inputs.gaussian_bf16((16512, 4096), 0.02, 404, device=DEV)
+    assert w.shape[0] * w.shape[1] > 64 << 20
+    rng = np.random.default_rng(12)
+    sampled_block_case(pkg, w, [64, 257, 600], _row_blocks(w.shape[0], 3, 12),
+                       x_rows=lambda m: np.unique(np.concatenate([[0, m - 1], rng.integers(0, m, 14)])))
+
+
 def test_mx_full_size(pkg):
     w = inputs.heavy_tail_weight(5, device=DEV)
     n, k = w.shape
