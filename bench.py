@@ -455,6 +455,35 @@ def moe_workload(torch, fp8bs, inputs, dev):
     return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,0,true,true>", [0, 1]))
 
 
+def moe_prefill_workload(torch, fp8bs, inputs, dev):
+    """Grouped MoE at prefill sizes: 256 block-FP8 experts of [2048, 4096],
+    top-12 routing, M = 512 and 2048 tokens through fp8bs_moe_gemv_ws (the
+    routing grouped on the device, one grouped tcgen05 GEMM).  Work per call:
+    2 * M * topk * N * K flops."""
+    E, (n, k), topk = inputs.MOE_EXPERTS, inputs.MOE_SHAPE, inputs.MOE_TOPK
+    codes = torch.empty((E, n, k), dtype=torch.uint8, device=dev)
+    scales = torch.empty((E, n // 128, k // 128), dtype=torch.float32, device=dev)
+    for e in range(E):
+        c, s_ = fp8bs.quantize(inputs.moe_expert_weight(e, device=dev))
+        codes[e] = c
+        scales[e] = s_
+    ms = [512, 2048]
+    calls = []
+    for m in ms:
+        ids = inputs.moe_routing(m, topk, E, seed=m).to(dev)
+        x = inputs.activations(m, k, 850 + m, device=dev)
+        y = torch.empty((m, topk, n), dtype=torch.bfloat16, device=dev)
+        work = torch.empty((fp8bs.moe_gemv_ws_bytes(m, topk, E, k),), dtype=torch.uint8, device=dev)
+        calls.append((f"M={m}", m, 2 * m * topk * n * k,
+                      (lambda x=x, ids=ids, y=y, work=work: fp8bs.moe_gemv_ws(x, ids, codes, scales, work, y=y))))
+    cfg = {"workload": "grouped MoE prefill: 256 block-FP8 experts [2048,4096], top-12 routing, M=512,2048 "
+                       "(fp8bs_moe_gemv_ws: routing grouped on the device, one grouped tcgen05 GEMM)",
+           "experts": E, "n": n, "k": k, "topk": topk, "ms": ms,
+           "l2": "inputs larger than L2 (2.1 GB of expert codes, nearly all selected)"}
+    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel<0,true>", [0, 1]), flops=True,
+                call_launches=[5, 5])
+
+
 def kv_workload(torch, fp8bs, inputs, dev):
     """FP8 KV-cache split-KV decode attention on a Qwen3-8B-shaped layer (32 q
     heads, 8 kv heads, head_dim 128, page 16) at InfiniLM PR #586's decode
@@ -835,6 +864,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="lm_head",
                     choices=["lm_head", "rotation", "sweep", "mx", "mx_prefill", "quantize", "prefill", "rowwise", "w8a8",
+                             "moe_prefill",
                              "w8a8_prefill", "moe", "kv"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--layers", type=int, default=None, help="rotation: fewer layers than 48 (a smaller case)")
@@ -904,6 +934,8 @@ def main():
         wl = w8a8_prefill_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "moe":
         wl = moe_workload(torch, fp8bs, inputs, dev)
+    elif args.workload == "moe_prefill":
+        wl = moe_prefill_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "kv":
         wl = kv_workload(torch, fp8bs, inputs, dev)
     else:

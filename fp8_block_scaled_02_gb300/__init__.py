@@ -14,6 +14,7 @@ Functions (names follow the C entry points):
     mx_gemv(x, codes, e8m0)-> y bf16 [M,N]
     gemv_ws(x, codes, scales, workspace) -> y bf16 [M,N]        (fp8bs_gemv_ws)
     gemv_batch([(x, codes, scales[, y]), ...]) -> [y, ...]   (fp8bs_gemv_batch)
+    GemvBatch(ops)() -> [y, ...]                  (fp8bs_gemv_batch, op table built once)
     mx_gemv_batch([(x, codes, e8m0[, y]), ...]) -> [y, ...]  (mxfp8_gemv_batch)
     row_quantize(w)        -> (codes u8 [N,K], scales f32 [N])       (fp8row_*)
     tensor_quantize(w)     -> (codes u8 [N,K], scale f32 [1])        (fp8tensor_*)
@@ -22,6 +23,7 @@ Functions (names follow the C entry points):
     w8a8_gemm(xq, sx, wq, sw) -> y bf16 [M,N]                        (w8a8_gemm)
     w8a8_linear(x, wq, sw) -> y bf16 [M,N]: act_quantize then w8a8_gemm
     moe_gemv(x, ids, codes, scales) -> y bf16 [M, topk, N]            (fp8bs_moe_gemv)
+    moe_gemv_ws(x, ids, codes, scales, workspace) -> y                (fp8bs_moe_gemv_ws)
         codes [E,N,K], scales [E, ceil(N/128), ceil(K/128)], ids int32 [M, topk]
     kv_append(x, slots, scale, cache)    FP8 KV cache append (fp8kv_append), in place
     kv_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
@@ -94,6 +96,9 @@ def lib() -> ctypes.CDLL:
         L.fp8tensor_gemv_ex.argtypes = [p, i64, p, p, i64, i64, p, i32, p]
         L.fp8act_quantize.argtypes = [p, i64, i64, p, p, p]
         L.fp8bs_moe_gemv.argtypes = [p, i64, p, i64, p, p, i64, i64, i64, p, p]
+        L.fp8bs_moe_gemv_ws.argtypes = [p, i64, p, i64, p, p, i64, i64, i64, p, p, i64, p]
+        L.fp8bs_moe_gemv_ws_bytes.argtypes = [i64, i64, i64, i64]
+        L.fp8bs_moe_gemv_ws_bytes.restype = i64
         L.fp8kv_append.argtypes = [p, i64, i64, i64, p, p, p, i64, p]
         L.fp8kv_decode_attention.argtypes = [p, p, p, p, p, p, i64, p, i64, i64, i64, i64, i64, i64, i64,
                                              ctypes.c_float, p, p]
@@ -111,7 +116,7 @@ def lib() -> ctypes.CDLL:
                   "mxfp8_gemv_batch", "mxfp8_gemv_batch_ex", "mxfp8_quantize", "mxfp8_gemv",
                   "mxfp8_gemv_ex", "fp8row_quantize", "fp8tensor_quantize", "fp8row_gemv", "fp8row_gemv_ex",
                   "fp8tensor_gemv", "fp8tensor_gemv_ex", "fp8act_quantize", "w8a8_gemm", "w8a8_gemm_ex",
-                  "fp8bs_moe_gemv", "fp8kv_append", "fp8kv_decode_attention",
+                  "fp8bs_moe_gemv", "fp8bs_moe_gemv_ws", "fp8kv_append", "fp8kv_decode_attention",
                   "fp8bs_select_path", "fp8bs_check_device_error", "fp8bs_debug_wait_expiry",
                   "fp8bs_debug_encode_f32", "fp8bs_version"):
             getattr(L, f).restype = ctypes.c_int
@@ -317,6 +322,27 @@ def gemv_batch(ops, path: int = PATH_AUTO, stream=None):
     return _run_batch(lib().fp8bs_gemv_batch_ex, "fp8bs_gemv_batch", ops, False, path, stream)
 
 
+class GemvBatch:
+    """A prepared sequence of block-FP8 GEMVs (fp8bs_gemv_batch): the op
+    table is built once, so calling it only enqueues the launches.  ops as
+    for gemv_batch."""
+
+    def __init__(self, ops, path: int = PATH_AUTO):
+        self.arr, self.m, self.ys, self.device = _batch_ops(ops, False)
+        self.count = len(ops)
+        self.path = path
+        self.ops = ops  # keeps the tensors alive
+
+    def __call__(self, stream=None):
+        import torch
+        if not self.count:
+            return self.ys
+        with torch.cuda.device(self.device):
+            _check(lib().fp8bs_gemv_batch_ex(ctypes.cast(self.arr, ctypes.c_void_p), self.count, self.m,
+                                             int(self.path), _stream(stream, self.device)), "fp8bs_gemv_batch")
+        return self.ys
+
+
 def mx_gemv_batch(ops, path: int = PATH_AUTO, stream=None):
     """A sequence of MXFP8 GEMVs (mxfp8_gemv_batch): ops is a list of
     (x [M,K], codes, e8m0[, y]) with one M; returns the list of y."""
@@ -380,8 +406,7 @@ def row_gemv(x, codes, scales, y=None, path: int = PATH_AUTO, stream=None):
     return y
 
 
-def moe_gemv(x, ids, codes, scales, y=None, stream=None):
-    """Grouped block-FP8 GEMV over routed experts: y[t, j] = x[t] . dequant(W[ids[t, j]])^T."""
+def _moe_args(x, ids, codes, scales, y):
     import torch
     m, k = _shape2(x, "x")
     if codes.dim() != 3:
@@ -394,9 +419,37 @@ def moe_gemv(x, ids, codes, scales, y=None, stream=None):
     a = _Args().need("x", x, torch.bfloat16).need("ids", ids, torch.int32) \
         .need("codes", codes, torch.uint8) \
         .need("scales", scales, torch.float32, numel=e * cdiv(n, 128) * cdiv(k, 128)) \
-        .need("y", y, torch.bfloat16, numel=m * topk * n).check()
+        .need("y", y, torch.bfloat16, numel=m * topk * n)
+    return a, m, topk, e, n, k, y
+
+
+def moe_gemv(x, ids, codes, scales, y=None, stream=None):
+    """Grouped block-FP8 GEMV over routed experts: y[t, j] = x[t] . dequant(W[ids[t, j]])^T."""
+    a, m, topk, e, n, k, y = _moe_args(x, ids, codes, scales, y)
+    a.check()
     _run(a, "fp8bs_moe_gemv", lib().fp8bs_moe_gemv, a.ptr("x"), m, a.ptr("ids"), topk, a.ptr("codes"),
          a.ptr("scales"), e, n, k, a.ptr("y"), stream=stream)
+    return y
+
+
+def moe_gemv_ws_bytes(m: int, topk: int, num_experts: int, k: int) -> int:
+    """Bytes of device workspace moe_gemv_ws needs (fp8bs_moe_gemv_ws_bytes)."""
+    v = lib().fp8bs_moe_gemv_ws_bytes(m, topk, num_experts, k)
+    if v < 0:
+        raise Fp8bsError(int(v), "fp8bs_moe_gemv_ws_bytes")
+    return int(v)
+
+
+def moe_gemv_ws(x, ids, codes, scales, workspace, y=None, stream=None):
+    """moe_gemv with caller-provided device scratch (fp8bs_moe_gemv_ws): more
+    than 32 tokens run as one grouped tensor-core GEMM over the routed
+    experts; `workspace` is a uint8 CUDA tensor of at least
+    moe_gemv_ws_bytes(M, topk, E, K) bytes."""
+    import torch
+    a, m, topk, e, n, k, y = _moe_args(x, ids, codes, scales, y)
+    a.need("workspace", workspace, torch.uint8).check()
+    _run(a, "fp8bs_moe_gemv_ws", lib().fp8bs_moe_gemv_ws, a.ptr("x"), m, a.ptr("ids"), topk, a.ptr("codes"),
+         a.ptr("scales"), e, n, k, a.ptr("y"), a.ptr("workspace"), workspace.numel(), stream=stream)
     return y
 
 

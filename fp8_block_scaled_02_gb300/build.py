@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfp8bs.so")
 
 SOURCES = ["api.cu", "quantize.cu", "decode.cu", "generic.cu", "prefill.cu", "w8a8.cu", "kvattn.cu", "tensormap.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I", CSRC, "-I", INCLUDE]

@@ -312,17 +312,22 @@ int fp8tensor_gemv(const void *x_bf16, int64_t m, const uint8_t *codes, const fl
     return rowwise_gemv(x_bf16, m, codes, scale, n, k, y_bf16, 0, FP8BS_PATH_AUTO, stream);
 }
 
-int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids, int64_t topk, const uint8_t *codes,
-                   const float *scales, int64_t num_experts, int64_t n, int64_t k, void *y_bf16, void *stream) {
+static int moe_check(const void *x_bf16, int64_t m, const int32_t *expert_ids, int64_t topk, const uint8_t *codes,
+                     const float *scales, int64_t num_experts, int64_t n, int64_t k, void *y_bf16) {
     if (m < 0 || n <= 0 || k <= 0 || m >= kMaxDim || n >= kMaxDim || k >= kMaxDim) return FP8BS_ERR_SHAPE;
     if (topk < 1 || num_experts < 1 || num_experts > 1024 || topk > num_experts) return FP8BS_ERR_SHAPE;
-    if (num_experts * n >= kMaxDim) return FP8BS_ERR_SHAPE;
+    if (num_experts * n >= kMaxDim || m * topk >= kMaxDim) return FP8BS_ERR_SHAPE;
     if (m == 0) return FP8BS_OK;
     if (!x_bf16 || !expert_ids || !codes || !scales || !y_bf16) return FP8BS_ERR_NULL;
     if (!aligned(x_bf16, 2) || !aligned(y_bf16, 2) || !aligned(scales, 4) || !aligned(expert_ids, 4))
         return FP8BS_ERR_ALIGN;
     if (!tma_ok(k, x_bf16, codes)) return FP8BS_ERR_PATH;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return FP8BS_OK;
+}
+
+static int moe_decode_chunks(const void *x_bf16, int64_t m, const int32_t *expert_ids, int64_t topk,
+                             const uint8_t *codes, const float *scales, int64_t num_experts, int64_t n, int64_t k,
+                             void *y_bf16, cudaStream_t st) {
     for (int64_t m0 = 0; m0 < m; m0 += kDecodeMaxM) {
         const int64_t mc = m - m0 < kDecodeMaxM ? m - m0 : kDecodeMaxM;
         DecodeArgs a{static_cast<const char *>(x_bf16) + m0 * k * 2, codes, scales, nullptr,
@@ -331,6 +336,44 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids, int
         if (launch_moe_decode(a, g, st) != cudaSuccess) return FP8BS_ERR_CUDA;
     }
     return FP8BS_OK;
+}
+
+int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids, int64_t topk, const uint8_t *codes,
+                   const float *scales, int64_t num_experts, int64_t n, int64_t k, void *y_bf16, void *stream) {
+    const int s = moe_check(x_bf16, m, expert_ids, topk, codes, scales, num_experts, n, k, y_bf16);
+    if (s != FP8BS_OK || m == 0) return s;
+    return moe_decode_chunks(x_bf16, m, expert_ids, topk, codes, scales, num_experts, n, k, y_bf16,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int64_t fp8bs_moe_gemv_ws_bytes(int64_t m, int64_t topk, int64_t num_experts, int64_t k) {
+    if (m < 0 || topk < 1 || num_experts < 1 || num_experts > 1024 || m >= kMaxDim || m * topk >= kMaxDim ||
+        k <= 0 || k >= kMaxDim)
+        return FP8BS_ERR_SHAPE;
+    return m <= kDecodeMaxM ? 0 : moe_route_bytes(m * topk, num_experts, k);
+}
+
+int fp8bs_moe_gemv_ws(const void *x_bf16, int64_t m, const int32_t *expert_ids, int64_t topk, const uint8_t *codes,
+                      const float *scales, int64_t num_experts, int64_t n, int64_t k, void *y_bf16, void *workspace,
+                      int64_t workspace_bytes, void *stream) {
+    const int s = moe_check(x_bf16, m, expert_ids, topk, codes, scales, num_experts, n, k, y_bf16);
+    if (s != FP8BS_OK || m == 0) return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (m <= kDecodeMaxM)
+        return moe_decode_chunks(x_bf16, m, expert_ids, topk, codes, scales, num_experts, n, k, y_bf16, st);
+    if (!workspace) return FP8BS_ERR_NULL;
+    if (!aligned(workspace, 256)) return FP8BS_ERR_ALIGN;
+    if (workspace_bytes < moe_route_bytes(m * topk, num_experts, k)) return FP8BS_ERR_SHAPE;
+    const MoeRoute r = moe_route_views(workspace, m * topk, num_experts);
+    cudaError_t e = launch_moe_route(x_bf16, k, expert_ids, m * topk, static_cast<int>(topk),
+                                     static_cast<int>(num_experts), r, st);
+    if (e != cudaSuccess) return FP8BS_ERR_CUDA;
+    const DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k, kScaleBlock, 0};
+    const MoeArgs g{expert_ids, topk, num_experts};
+    e = launch_prefill_moe(a, g, r, st);
+    if (e == cudaErrorNotSupported)
+        return moe_decode_chunks(x_bf16, m, expert_ids, topk, codes, scales, num_experts, n, k, y_bf16, st);
+    return cuda_status(e);
 }
 
 int fp8kv_append(const void *x_bf16, int64_t num_tokens, int64_t num_kv_heads, int64_t head_dim,
@@ -423,7 +466,8 @@ int fp8bs_debug_encode_f32(uint32_t first_bits, int64_t count, uint8_t *codes_u8
 
 int fp8bs_check_device_error(void *stream, uint32_t *word_out) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FP8BS_ERR_CUDA;
-    const uint32_t w = take_decode_error() | take_prefill_error() | take_w8a8_error() | take_kv_error();
+    const uint32_t w = take_decode_error() | take_prefill_error() | take_w8a8_error() | take_kv_error() |
+                       take_moe_error();
     if (word_out) *word_out = w;
     return w ? FP8BS_ERR_DEVICE : FP8BS_OK;
 }

@@ -120,6 +120,7 @@ struct BatchOp {
     const float *scales;     // block or row scales, else nullptr
     const uint8_t *e8m0;     // MX exponents, else nullptr
     __nv_bfloat16 *y;        // bf16 [m, n]
+    const float *xinv;       // prepared x: inverse factors [kblocks][32], else nullptr
     int n, kblocks, groups;
     int ntiles;              // 128-row tiles of this weight
     int unit0;               // index of its first tile in the batch's unit list
@@ -210,6 +211,7 @@ struct OpRef {
     const float *scales;     // block [ceil(n/128), kblocks] or row scales (scales[row * row_stride])
     const uint8_t *e8m0;     // MX exponents [n, groups]
     __nv_bfloat16 *y;        // [m, n]
+    const float *xinv;       // prepared x (XP): inverse factors [kblocks][32]
     int n, kblocks, groups, e8m0_vec, row_stride;
 };
 
@@ -232,7 +234,7 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     // ... and with bf16 operands and one scale per row, all of K
     constexpr bool kDirect = kWholeBlock && ROW && !F16;
     static_assert(!(MOE && BATCH), "a grouped MoE call is one launch of its own");
-    static_assert(!XP || (F16 && !MX && !MOE && !BATCH), "prepared x feeds the single-weight f16 path");
+    static_assert(!XP || (F16 && !MX && !MOE), "prepared x feeds the block-scaled f16 path");
     using C = Cfg<MT, MX, F16, XP>;
     constexpr int kStages = C::kStages;
     constexpr int kBN = C::kBN;
@@ -278,10 +280,10 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     auto op_ref = [&](int op) -> OpRef {
         if (BATCH) {
             const BatchOp &o = bp->ops[op];
-            return OpRef{&bp->tm_codes[op], &bp->tm_x[op], o.scales, o.e8m0, o.y, o.n, o.kblocks, o.groups, o.e8m0_vec,
-                         o.row_stride};
+            return OpRef{&bp->tm_codes[op], &bp->tm_x[op], o.scales, o.e8m0, o.y, o.xinv, o.n, o.kblocks, o.groups,
+                         o.e8m0_vec, o.row_stride};
         }
-        return OpRef{tm_codes, tm_x, scales, e8m0, y, n, kblocks, groups, e8m0_vec, row_stride};
+        return OpRef{tm_codes, tm_x, scales, e8m0, y, xinv_g, n, kblocks, groups, e8m0_vec, row_stride};
     };
 
     if (threadIdx.x == 0) {
@@ -418,7 +420,7 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
                     // prepared x: this K block's inverse factors, in the slot
                     // order the consumers read (xprep_kernel)
                     if (XP)
-                        bulk_load_g2s(aux + s * C::kXInvFloats, xinv_g + (kbb + kb) * 32, C::kXRows * 4, &full[s]);
+                        bulk_load_g2s(aux + s * C::kXInvFloats, o.xinv + (kbb + kb) * 32, C::kXRows * 4, &full[s]);
                 }
                 __syncwarp();
             }
@@ -690,12 +692,14 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16, XP>::kThreads,
                                              splits, ntiles, e8m0_vec, row_stride, ids, topk, num_experts);
 }
 
-// A batch of independent GEMVs with the same m in one persistent launch.
-template <int MT, int SC, bool F16>
-__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT, SC == kScaleMx, F16>::kMinBlocks)
+// A batch of independent GEMVs with the same m in one persistent launch
+// (XP: every op's x prepared, BatchOp::xinv set).
+template <int MT, int SC, bool F16, bool XP = false>
+__global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16, XP>::kThreads,
+                                  Cfg<MT, SC == kScaleMx, F16, XP>::kMinBlocks)
     gemv_batch_kernel(const __grid_constant__ BatchParams p, int m) {
-    decode_body<MT, SC, F16, false, true>(&p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, m, 0, 0, 0, 1, 0,
-                                          0, 0, nullptr, 0, 0);
+    decode_body<MT, SC, F16, false, true, XP>(&p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, m, 0, 0, 0,
+                                              1, 0, 0, 0, nullptr, 0, 0);
 }
 
 // ------------------------------------------------------------ x preparation
@@ -705,14 +709,9 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16>::kThreads, Cfg<MT
 // done once per call instead of once per CTA -- and
 // inv[kb * 32 + slot(r)] = 2^-e in the slot order the consumer warps read.
 // Padding rows r in [m, mpad) get inv = 1 (their x rows load as zeros).
-__global__ void __launch_bounds__(256) xprep_kernel(const uint16_t *__restrict__ x, int m, int mpad, int k,
-                                                    int kblocks, uint16_t *__restrict__ x16,
-                                                    float *__restrict__ inv) {
-    pdl_launch_dependents();  // the GEMV's prologue may start; it waits for this grid before reading
-    pdl_wait();               // x may come from the previous kernel in the stream
-    const int gw = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    const int r = gw / kblocks, kb = gw - r * kblocks;
+__device__ __forceinline__ void xprep_warp(const uint16_t *__restrict__ x, int m, int mpad, int k, int kblocks,
+                                           uint16_t *__restrict__ x16, float *__restrict__ inv, int w, int lane) {
+    const int r = w / kblocks, kb = w - r * kblocks;
     if (r >= mpad) return;
     const int c = kb * kKB + lane * 4;
     const bool in = r < m && c < k;  // k % 4 == 0: a lane's four values are all in or all out
@@ -737,6 +736,15 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t *__restrict__
     }
     if (lane == 0)
         inv[kb * 32 + xinv_slot(r)] = r < m ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 1.0f;
+}
+
+__global__ void __launch_bounds__(256) xprep_kernel(const uint16_t *__restrict__ x, int m, int mpad, int k,
+                                                    int kblocks, uint16_t *__restrict__ x16,
+                                                    float *__restrict__ inv) {
+    pdl_launch_dependents();  // the GEMV's prologue may start; it waits for this grid before reading
+    pdl_wait();               // x may come from the previous kernel in the stream
+    const int gw = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    xprep_warp(x, m, mpad, k, kblocks, x16, inv, gw, threadIdx.x & 31);
 }
 
 // Per-device, per-instantiation launch setup (shared-memory opt-in and the
@@ -833,12 +841,13 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream, const float *xinv
                               static_cast<const int32_t *>(nullptr), 0, 0, xinv);
 }
 
-// A batch launch: one persistent grid over the row tiles of all the ops.
-template <int MT, int SC, bool F16>
+// A batch launch: one persistent grid over the row tiles of all the ops
+// (XP: every op's x is its prepared f16 copy, with BatchItem::xinv set).
+template <int MT, int SC, bool F16, bool XP = false>
 cudaError_t launch_batch_t(const BatchItem *ops, int count, int64_t m, bool force, cudaStream_t stream) {
-    using C = Cfg<MT, SC == kScaleMx, F16>;
+    using C = Cfg<MT, SC == kScaleMx, F16, XP>;
     constexpr int kBN = C::kBN;
-    auto kern = gemv_batch_kernel<MT, SC, F16>;
+    auto kern = gemv_batch_kernel<MT, SC, F16, XP>;
     static Setup setup;
     int resident = 1;
     {
@@ -856,7 +865,7 @@ cudaError_t launch_batch_t(const BatchItem *ops, int count, int64_t m, bool forc
             DecodeArgs a{ops[i].x, ops[i].codes, SC == kScaleMx ? nullptr : static_cast<const float *>(ops[i].scales),
                          SC == kScaleMx ? static_cast<const uint8_t *>(ops[i].scales) : nullptr,
                          ops[i].y, m, ops[i].n, ops[i].k, static_cast<ScaleKind>(SC), 0};
-            const cudaError_t e = launch_t<MT, SC, F16>(a, stream);
+            const cudaError_t e = launch_t<MT, SC, F16, XP>(a, stream, ops[i].xinv);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -872,9 +881,10 @@ cudaError_t launch_batch_t(const BatchItem *ops, int count, int64_t m, bool forc
         const uint64_t n = static_cast<uint64_t>(it.n), k = static_cast<uint64_t>(it.k);
         if (!encode_tensor_map_2d(&p.tm_codes[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, it.codes, k, n, k, kKB, kBN,
                                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_tensor_map_2d(&p.tm_x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, it.x, k, static_cast<uint64_t>(m),
-                                  k * 2, 64, C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
+            !encode_tensor_map_2d(&p.tm_x[i], XP ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                  it.x, k, static_cast<uint64_t>(m), k * 2, 64, C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
+        o.xinv = it.xinv;
         o.scales = SC == kScaleMx ? nullptr : static_cast<const float *>(it.scales);
         o.e8m0 = SC == kScaleMx ? static_cast<const uint8_t *>(it.scales) : nullptr;
         o.y = static_cast<__nv_bfloat16 *>(it.y);

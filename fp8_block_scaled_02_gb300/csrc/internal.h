@@ -65,11 +65,12 @@ cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_
 // slots runs as one launch per op instead.
 constexpr int kBatchMaxOps = 96;
 struct BatchItem {
-    const void *x;           // bf16 [m, k]
+    const void *x;           // bf16 [m, k] (f16, prepared, when xinv is set)
     const uint8_t *codes;    // e4m3 [n, k]
     const void *scales;      // fp32 block scales (kScaleBlock) or e8m0 exponents (kScaleMx)
     void *y;                 // bf16 [m, n]
     int64_t n, k;
+    const float *xinv = nullptr;  // prepared x: inverse factors [ceil(k/128)][32]
 };
 cudaError_t launch_decode_batch(const BatchItem *ops, int count, int64_t m, ScaleKind kind, bool force,
                                 cudaStream_t stream);
@@ -79,11 +80,32 @@ uint32_t take_decode_error();  // reads and clears the decode kernels' error wor
 cudaError_t launch_wait_expiry_probe(cudaStream_t stream);
 cudaError_t launch_encode_probe(uint32_t first, int64_t count, uint8_t *codes, cudaStream_t stream);
 
+// moe.cu -- the routing of the grouped MoE GEMM: the (token, slot) pairs of
+// ids [pairs] grouped by expert and their x rows copied in that order, built
+// on the device in a caller workspace of moe_route_bytes(pairs, E, k) bytes.
+struct MoeRoute {
+    int32_t *counts;    // [E] pairs per expert
+    int32_t *cursor;    // [E] scatter cursors
+    int32_t *tok_off;   // [E + 1] first pair of each expert in perm
+    int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert
+    int32_t *perm;      // [pairs] t * topk + j, expert by expert
+    void *xs;           // bf16 [pairs, k]: x[perm[q] / topk] in perm's order
+};
+int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k);
+MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts);
+cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64_t pairs, int topk,
+                             int num_experts, const MoeRoute &r, cudaStream_t stream);
+uint32_t take_moe_error();
+
 // generic.cu -- plain-load kernels for any shape / alignment.
 cudaError_t launch_generic_gemv(const DecodeArgs &a, cudaStream_t stream);
 
-// prefill.cu -- tcgen05 block-FP8 / row-scaled FP8 GEMM for larger m.
+// prefill.cu -- tcgen05 block-FP8 / row-scaled / MXFP8 GEMM for larger m.
 cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream);
+// Grouped MoE GEMM over the routed experts (block scales): a.x [m, k] the
+// tokens, a.codes / a.scales the stacked experts ([E * n, k], [E, ceil(n/128),
+// ceil(k/128)]), a.y [m, topk, n]; the routing built by launch_moe_route.
+cudaError_t launch_prefill_moe(const DecodeArgs &a, const MoeArgs &g, const MoeRoute &r, cudaStream_t stream);
 uint32_t take_prefill_error();
 
 // w8a8.cu -- e4m3 activations x e4m3 weight, both scaled per tensor.

@@ -1,0 +1,177 @@
+// moe.cu -- routing for the grouped MoE GEMM on the tensor cores (large m).
+//
+// The grouped GEMM (prefill.cu, prefill_kernel<kScaleBlock, MOE = true>)
+// multiplies each selected expert's weight with the x rows of exactly the
+// tokens routed to it.  It needs the (token, slot) pairs grouped by expert,
+// which these kernels build on the device from the routing ids, with no host
+// synchronisation, in the caller's workspace:
+//   counts[e]    pairs routed to expert e
+//   tok_off[e]   exclusive prefix sum of counts (tok_off[E] = valid pairs)
+//   tile_off[e]  exclusive prefix sum of ceil(counts / 256): the first of
+//                expert e's 256-pair tiles (tile_off[E] = tiles in all)
+//   perm[...]    pair indices p = t * topk + j, expert by expert
+//                (tok_off[e] .. tok_off[e + 1]); within an expert in no
+//                particular order -- every pair's output is computed on its
+//                own, so the order changes no result.
+//   xs[q, :]     x[perm[q] / topk, :]: the x rows in the same order, so that
+//                each expert's rows are contiguous and the GEMM loads them
+//                as ordinary TMA tiles.
+// An id outside [0, E) routes nowhere and sets the error bit ERRBIT_INDEX.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8bs {
+
+__device__ uint32_t g_moe_err;
+
+namespace {
+
+constexpr int kScanThreads = 1024;  // one block scans up to 1024 experts
+
+__global__ void moe_count_kernel(const int32_t *__restrict__ ids, int64_t pairs, int num_experts,
+                                 int32_t *__restrict__ counts) {
+    pdl_launch_dependents();
+    pdl_wait();  // the ids may come from the router, the previous kernel
+    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < pairs;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int e = __ldg(ids + p);
+        if (e >= 0 && e < num_experts)
+            atomicAdd(counts + e, 1);
+        else
+            atomicOr(&g_moe_err, ERRBIT_INDEX);
+    }
+}
+
+// Exclusive prefix sums of counts and of their 256-pair tile counts; the
+// scatter cursors start at zero.
+__global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *__restrict__ counts,
+                                                                int num_experts, int32_t *__restrict__ tok_off,
+                                                                int32_t *__restrict__ tile_off,
+                                                                int32_t *__restrict__ cursor) {
+    __shared__ int32_t s_tok[kScanThreads], s_tile[kScanThreads];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int e = threadIdx.x;
+    const int32_t c = e < num_experts ? counts[e] : 0;
+    s_tok[e] = c;
+    s_tile[e] = (c + 255) >> 8;
+    __syncthreads();
+    // Hillis-Steele inclusive scan over the block
+    for (int o = 1; o < kScanThreads; o <<= 1) {
+        const int32_t a = e >= o ? s_tok[e - o] : 0, b = e >= o ? s_tile[e - o] : 0;
+        __syncthreads();
+        s_tok[e] += a;
+        s_tile[e] += b;
+        __syncthreads();
+    }
+    if (e < num_experts) {
+        tok_off[e + 1] = s_tok[e];
+        tile_off[e + 1] = s_tile[e];
+        cursor[e] = 0;
+    }
+    if (e == 0) {
+        tok_off[0] = 0;
+        tile_off[0] = 0;
+    }
+}
+
+// xs[q, :] = x[perm[q] / topk, :] for the routed pairs q < tok_off[E]; one
+// warp per row, 16-byte copies (k % 16 == 0 on this path).
+__global__ void moe_gather_kernel(const uint4 *__restrict__ x, int64_t pairs, int topk, int k,
+                                  const int32_t *__restrict__ tok_off, int num_experts,
+                                  const int32_t *__restrict__ perm, uint4 *__restrict__ xs) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t q = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (q >= pairs || q >= tok_off[num_experts]) return;
+    const int64_t t = perm[q] / topk;
+    const int chunks = k / 8;  // 16-byte chunks of a bf16 row
+    const uint4 *src = x + t * chunks;
+    uint4 *dst = xs + q * chunks;
+    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+}
+
+__global__ void moe_scatter_kernel(const int32_t *__restrict__ ids, int64_t pairs, int num_experts,
+                                   const int32_t *__restrict__ tok_off, int32_t *__restrict__ cursor,
+                                   int32_t *__restrict__ perm) {
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; p < pairs;
+         p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int e = __ldg(ids + p);
+        if (e < 0 || e >= num_experts) continue;
+        perm[tok_off[e] + atomicAdd(cursor + e, 1)] = static_cast<int32_t>(p);
+    }
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
+int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k) {
+    return 2 * align256(4 * num_experts) + 2 * align256(4 * (num_experts + 1)) + align256(4 * pairs) +
+           align256(2 * pairs * k);
+}
+
+MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts) {
+    char *p = static_cast<char *>(workspace);
+    MoeRoute r;
+    r.counts = reinterpret_cast<int32_t *>(p);
+    p += align256(4 * num_experts);
+    r.cursor = reinterpret_cast<int32_t *>(p);
+    p += align256(4 * num_experts);
+    r.tok_off = reinterpret_cast<int32_t *>(p);
+    p += align256(4 * (num_experts + 1));
+    r.tile_off = reinterpret_cast<int32_t *>(p);
+    p += align256(4 * (num_experts + 1));
+    r.perm = reinterpret_cast<int32_t *>(p);
+    p += align256(4 * pairs);
+    r.xs = p;
+    return r;
+}
+
+cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64_t pairs, int topk,
+                             int num_experts, const MoeRoute &r, cudaStream_t stream) {
+    if (num_experts < 1 || num_experts > kScanThreads || pairs < 1) return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(r.counts, 0, 4 * static_cast<size_t>(num_experts), stream);
+    const unsigned blocks = static_cast<unsigned>((pairs + 255) / 256 < 1024 ? (pairs + 255) / 256 : 1024);
+    if (e == cudaSuccess)
+        e = launch_pdl(moe_count_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts, r.counts);
+    if (e == cudaSuccess)
+        e = launch_pdl(moe_scan_kernel, dim3(1), dim3(kScanThreads), stream, static_cast<const int32_t *>(r.counts),
+                       num_experts, r.tok_off, r.tile_off, r.cursor);
+    if (e == cudaSuccess)
+        e = launch_pdl(moe_scatter_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts,
+                       static_cast<const int32_t *>(r.tok_off), r.cursor, r.perm);
+    if (e == cudaSuccess)
+        e = launch_pdl(moe_gather_kernel, dim3(static_cast<unsigned>((pairs + 7) / 8)), dim3(256), stream,
+                       static_cast<const uint4 *>(x), pairs, topk, static_cast<int>(k),
+                       static_cast<const int32_t *>(r.tok_off), num_experts, static_cast<const int32_t *>(r.perm),
+                       static_cast<uint4 *>(r.xs));
+    return e;
+}
+
+uint32_t take_moe_error() {
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_moe_err, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+    const uint32_t zero = 0;
+    cudaMemcpyToSymbol(g_moe_err, &zero, sizeof zero);
+    return v;
+}
+
+}  // namespace fp8bs

@@ -131,19 +131,39 @@ __device__ __forceinline__ void setmaxnreg_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// The grouped MoE form: the routing (moe.cu) in device memory.
+struct MoeTiles {
+    const int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert
+    const int32_t *tok_off;   // [E + 1] first pair of each expert in perm
+    const int32_t *perm;      // pairs t * topk + j, expert by expert
+    int topk, num_experts;
+};
+
 // SC: kScaleBlock (128x128 block scales, promoted per K block), kScaleRow
 // (scales[row * row_stride] per weight row, stride 0: one per tensor,
 // applied to the total) or kScaleMx (e8m0 [n, groups], folded into the
 // decoded weights).
-template <int SC>
+// MOE: grouped GEMM over routed experts (block scales).  blockIdx.y is a
+// tile of up to 256 (token, slot) pairs of one expert (CTAs past the last
+// tile leave at once), blockIdx.x a 128-row tile of that expert's weight
+// (codes [E * n, k], scales [E, ceil(n/128), kblocks]).  tm_x maps the x
+// rows copied in pair order (moe.cu: xs [pairs, k]), so a tile's rows are
+// one ordinary TMA box starting at its first pair; output row j goes to
+// y[pair_j * n + row] (y: [tokens, topk, n]).
+template <int SC, bool MOE = false>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                               const uint8_t *__restrict__ codes,
                                                               const float *__restrict__ scales,
                                                               const uint8_t *__restrict__ e8m0, int groups,
                                                               __nv_bfloat16 *__restrict__ y, int m, int n,
-                                                              int k, int kblocks, int row_stride) {
+                                                              int k, int kblocks, int row_stride, int xfast,
+                                                              MoeTiles moe) {
     constexpr bool ROW = SC == kScaleRow;
     constexpr bool MX = SC == kScaleMx;
+    static_assert(!MOE || SC == kScaleBlock, "the grouped GEMM takes block scales");
+    __shared__ int32_t s_pair[MOE ? kTileX : 1];  // MOE: this tile's pairs, -1 past its count
+    __shared__ int s_expert;
+    __shared__ int s_srow;                         // MOE: this CTA's row of block scales
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -158,8 +178,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     int *s_fail = reinterpret_cast<int *>(d_empty + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kTileW;
-    const int m0 = blockIdx.y * kTileX;
+    const bool deep_prefetch = MOE || xfast;
+    // Tile order.  xfast: blockIdx.x walks the x tiles of one weight tile, so
+    // the CTAs running at any one time share a few weight tiles and their
+    // code loads hit L2 even when the weight does not fit there; otherwise
+    // blockIdx.x walks the weight tiles of one x tile, which keeps a weight
+    // that fits in L2 together with one x tile there.
+    const int wtile = xfast ? blockIdx.y : blockIdx.x;
+    const int n0 = wtile * kTileW;
+    int m0 = (xfast ? blockIdx.x : blockIdx.y) * kTileX;  // MOE: the tile's first pair
+
+    int expert = 0;
+    if (MOE) {
+        // this CTA's expert and pairs (the routing kernels ran before it in
+        // the stream); every thread reads the same words, so the exit is
+        // uniform and happens before anything is allocated
+        const int tile = blockIdx.y;
+        if (tile >= __ldg(moe.tile_off + moe.num_experts)) return;
+        if (threadIdx.x == 0) {
+            int lo = 0, hi = moe.num_experts - 1;  // largest e with tile_off[e] <= tile
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(moe.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
+            }
+            s_expert = lo;
+            s_srow = lo * ((n + kTileW - 1) / kTileW) + wtile;
+        }
+        __syncthreads();
+        expert = s_expert;
+        const int p0 = __ldg(moe.tok_off + expert) + (tile - __ldg(moe.tile_off + expert)) * kTileX;
+        const int cnt = min(kTileX, __ldg(moe.tok_off + expert + 1) - p0);
+        m0 = p0;
+        for (int i = threadIdx.x; i < kTileX; i += blockDim.x) s_pair[i] = i < cnt ? __ldg(moe.perm + p0 + i) : -1;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kXStages; ++i) mbar_init(&x_full[i], 1);
@@ -247,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int kh = warp >> 2;
         const int row = n0 + r;
         const bool row_ok = row < n;
-        const uint8_t *rp = codes + static_cast<int64_t>(row_ok ? row : 0) * k + kh * 64;
+        // MOE: the expert's rows start at expert * n in the stacked codes
+        const uint8_t *rp = codes + (static_cast<int64_t>(expert) * n + (row_ok ? row : 0)) * k + kh * 64;
         auto load4 = [&](int kb, uint4 (&v)[4]) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -273,6 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int kb = 0; kb < kblocks; ++kb) {
             const int as = kb % kASlots;
             load4(kb + 1, c1);  // in flight while this block is converted
+            // a weight read from HBM (too large for L2, or an expert read once
+            // per tile of its pairs): ask L2 for this row's codes four K
+            // blocks ahead, beyond the one block the registers hold
+            if (deep_prefetch && row_ok && kb + 4 < kblocks)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + (kb + 4) * kKB));
             if (MX) e1 = load_e(kb + 1);
             // slot `as` was last read by the MMAs of K block kb - kASlots
             const int prev = kb - kASlots;
@@ -345,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int h = (warp - kWarpEpi0) >> 2;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
         const int row = n0 + q * 32 + lane;
-        const float *srow = (ROW || MX) ? nullptr : scales + static_cast<int64_t>(blockIdx.x) * kblocks;
+        const float *srow = (ROW || MX) ? nullptr : scales + static_cast<int64_t>(MOE ? s_srow : wtile) * kblocks;
         float tot[kHalfX];
 #pragma unroll
         for (int j = 0; j < kHalfX; ++j) tot[j] = 0.0f;
@@ -381,8 +438,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const float rs = ROW ? __ldg(scales + static_cast<int64_t>(row) * row_stride) : 1.0f;
 #pragma unroll
             for (int j = 0; j < kHalfX; ++j) {
-                const int mi = m0 + h * kHalfX + j;
-                if (mi < m) y[static_cast<int64_t>(mi) * n + row] = __float2bfloat16_rn(ROW ? tot[j] * rs : tot[j]);
+                if (MOE) {
+                    const int pr = s_pair[h * kHalfX + j];  // y row = pair index t * topk + slot
+                    if (pr >= 0) y[static_cast<int64_t>(pr) * n + row] = __float2bfloat16_rn(tot[j]);
+                } else {
+                    const int mi = m0 + h * kHalfX + j;
+                    if (mi < m) y[static_cast<int64_t>(mi) * n + row] = __float2bfloat16_rn(ROW ? tot[j] * rs : tot[j]);
+                }
             }
         }
     }
@@ -400,8 +462,10 @@ cudaError_t g_setup_err[64] = {};
 
 }  // namespace
 
-cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
-    if (a.kind != kScaleBlock && a.kind != kScaleRow && a.kind != kScaleMx) return cudaErrorNotSupported;
+// One-time set-up per device: shared-memory opt-in for every instantiation,
+// and a check that each was compiled with the registers the setmaxnreg split
+// is planned against.
+static cudaError_t prefill_setup() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     {
@@ -412,7 +476,8 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
             // fewer than the split was planned against (its epilogue warps
             // would wait forever for registers).
             cudaError_t e = cudaSuccess;
-            for (auto kern : {prefill_kernel<kScaleBlock>, prefill_kernel<kScaleRow>, prefill_kernel<kScaleMx>}) {
+            for (auto kern : {prefill_kernel<kScaleBlock>, prefill_kernel<kScaleRow>, prefill_kernel<kScaleMx>,
+                              prefill_kernel<kScaleBlock, true>}) {
                 cudaFuncAttributes fa = {};
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -424,6 +489,15 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
         }
         if (g_setup_err[dev] != cudaSuccess) return g_setup_err[dev];
     }
+    return cudaSuccess;
+}
+
+cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
+    if (a.kind != kScaleBlock && a.kind != kScaleRow && a.kind != kScaleMx) return cudaErrorNotSupported;
+    {
+        const cudaError_t e = prefill_setup();
+        if (e != cudaSuccess) return e;
+    }
     CUtensorMap tm_x;
     const uint64_t k = static_cast<uint64_t>(a.k), m = static_cast<uint64_t>(a.m);
     // one TMA box = the x rows of one MMA unit: all 256 of the CTA's rows
@@ -431,14 +505,49 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
                               static_cast<uint32_t>(kTileX), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
-    const dim3 grid(static_cast<unsigned>((a.n + kTileW - 1) / kTileW), static_cast<unsigned>((a.m + kTileX - 1) / kTileX));
+    // x tiles fastest when the codes are too large to stay in L2 (half of
+    // its 129 MB) beside the x tiles; weight tiles fastest otherwise
+    // (measured: [18432, 7168] at M = 4096 1184 us vs 1474; [12288, 4096]
+    // 386 us vs 433).  grid.y holds at most 65535 tiles: beyond that the
+    // call takes the decode kernel in chunks.
+    const int64_t wtiles = (a.n + kTileW - 1) / kTileW, xtiles = (a.m + kTileX - 1) / kTileX;
+    const int xfast = a.n * a.k > (int64_t{64} << 20) ? 1 : 0;
+    if ((xfast ? wtiles : xtiles) > 65535) return cudaErrorNotSupported;
+    const dim3 grid(static_cast<unsigned>(xfast ? xtiles : wtiles), static_cast<unsigned>(xfast ? wtiles : xtiles));
     __nv_bfloat16 *y = static_cast<__nv_bfloat16 *>(a.y);
     const int mi = static_cast<int>(a.m), ni = static_cast<int>(a.n), ki = static_cast<int>(a.k);
     auto kern = a.kind == kScaleRow ? prefill_kernel<kScaleRow>
                                     : (a.kind == kScaleMx ? prefill_kernel<kScaleMx> : prefill_kernel<kScaleBlock>);
     const int groups = static_cast<int>((a.k + 31) / 32);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, a.codes, a.scales, a.e8m0, groups, y, mi, ni, ki, kblocks,
-                                                 a.kind == kScaleRow ? a.row_stride : 0);
+                                                 a.kind == kScaleRow ? a.row_stride : 0, xfast,
+                                                 MoeTiles{nullptr, nullptr, nullptr, 0, 0});
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_moe(const DecodeArgs &a, const MoeArgs &g, const MoeRoute &r, cudaStream_t stream) {
+    {
+        const cudaError_t e = prefill_setup();
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap tm_x;
+    const int64_t pairs = a.m * g.topk;
+    const uint64_t k = static_cast<uint64_t>(a.k);
+    // the x rows in pair order (r.xs [pairs, k]); a tile is one box of 256
+    if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r.xs, k, static_cast<uint64_t>(pairs), k * 2,
+                              64, static_cast<uint32_t>(kTileX), CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t wtiles = (a.n + kTileW - 1) / kTileW;
+    // at most ceil(pairs / 256) full tiles plus one partial tile per expert;
+    // the CTAs past the routing's actual tile count leave at once
+    const int64_t tbound = (pairs + kTileX - 1) / kTileX + (g.num_experts < pairs ? g.num_experts : pairs);
+    if (tbound > 65535) return cudaErrorNotSupported;
+    const dim3 grid(static_cast<unsigned>(wtiles), static_cast<unsigned>(tbound));
+    const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
+    prefill_kernel<kScaleBlock, true><<<grid, kThreads, kSmemBytes, stream>>>(
+        tm_x, a.codes, a.scales, nullptr, 0, static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(pairs),
+        static_cast<int>(a.n), static_cast<int>(a.k), kblocks, 0, 0,
+        MoeTiles{r.tile_off, r.tok_off, r.perm, static_cast<int>(g.topk), static_cast<int>(g.num_experts)});
     return cudaGetLastError();
 }
 

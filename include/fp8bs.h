@@ -364,6 +364,40 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids,
                    void *stream);
 
 /*
+ * fp8bs_moe_gemv_ws -- fp8bs_moe_gemv with caller-provided device scratch,
+ * which lets batches of m > 32 tokens run on the 5th-generation tensor
+ * cores: four small kernels group the (token, slot) pairs by expert in the
+ * workspace (counts, prefix sums, the pairs expert by expert, and a copy of
+ * each pair's x row in that order), then one grouped GEMM multiplies each
+ * selected expert's weight, decoded to bf16 in shared memory, with exactly
+ * the x rows routed to it, in tiles of up to 256 pairs of one expert, and
+ * writes each output row to its (token, slot).  Every selected expert's weight is
+ * read once per tile of its pairs; fp8bs_moe_gemv instead runs the decode
+ * kernel per 32 tokens, reading every selected expert once per 32 tokens.
+ * Same definition, arguments and tolerance as fp8bs_moe_gemv; m <= 32
+ * takes fp8bs_moe_gemv's decode path and ignores the workspace.  In the
+ * grouped path a token that lists an expert twice has both slots computed.
+ *
+ * Defined by: Atlas spark_model/weight_map/quantize_fp8_bs.rs (module
+ * notes: the grouped MoE GEMM over block-FP8 routed experts with
+ * [N/128, K/128] fp32 scales).
+ *
+ *   workspace        device, 256-byte aligned, >= fp8bs_moe_gemv_ws_bytes(m,
+ *                    topk, num_experts, k) bytes (0 for m <= 32; about
+ *                    2 * m * topk * k for the x copy); contents on entry do
+ *                    not matter
+ *   other arguments  as fp8bs_moe_gemv (m * topk < 2^31)
+ * FP8BS_ERR_NULL / FP8BS_ERR_ALIGN / FP8BS_ERR_SHAPE for a missing,
+ * misaligned or too small workspace, before anything is launched.
+ */
+int64_t fp8bs_moe_gemv_ws_bytes(int64_t m, int64_t topk, int64_t num_experts,
+                                int64_t k);
+int fp8bs_moe_gemv_ws(const void *x_bf16, int64_t m, const int32_t *expert_ids,
+                      int64_t topk, const uint8_t *codes, const float *scales,
+                      int64_t num_experts, int64_t n, int64_t k, void *y_bf16,
+                      void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
  * FP8 E4M3 KV cache for paged decode attention.
  *
  * Defined by: InfiniLM PR #586 (Summary: an F8 cache with per-layer fp32

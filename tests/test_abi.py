@@ -188,6 +188,20 @@ def test_moe_validation(L):
     assert f(x, 1, i, 2, c, s, 8, 128, 120, y, None) == -7          # k % 16 != 0
 
 
+def test_moe_ws_validation(L):
+    x, i, c, s, y, w = P(0x10000), P(0x20000), P(0x30000), P(0x40000), P(0x50000), P(0x60000)
+    f = L.fp8bs_moe_gemv_ws
+    need = L.fp8bs_moe_gemv_ws_bytes(64, 12, 256, 4096)
+    assert need > 2 * 64 * 12 * 4096 and L.fp8bs_moe_gemv_ws_bytes(32, 12, 256, 4096) == 0  # m <= 32: decode path
+    assert L.fp8bs_moe_gemv_ws_bytes(64, 0, 256, 4096) == -2 and L.fp8bs_moe_gemv_ws_bytes(64, 2, 2000, 4096) == -2
+    assert f(x, 64, i, 12, c, s, 256, 2048, 4096, y, None, need, None) == -1      # grouped path needs it
+    assert f(x, 64, i, 12, c, s, 256, 2048, 4096, y, P(0x60010), need, None) == -4  # 256-byte aligned
+    assert f(x, 64, i, 12, c, s, 256, 2048, 4096, y, w, need - 1, None) == -2
+    assert f(x, 64, i, 0, c, s, 256, 2048, 4096, y, w, need, None) == -2
+    assert f(x, 64, i, 12, c, s, 256, 2048, 4004, y, w, need, None) == -7        # k % 16 != 0
+    assert f(None, 0, None, 12, None, None, 256, 2048, 4096, None, None, 0, None) == 0
+
+
 def test_kv_validation(L):
     x, sl, s, c = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
     a = L.fp8kv_append

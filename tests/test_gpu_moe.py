@@ -188,3 +188,105 @@ def experts_from(sample):
         codes.append(c)
         scales.append(s)
     return codes, scales
+
+
+# ------------------------------------------- grouped tensor-core GEMM (m > 32)
+def ws(pkg, m, topk, e, k):
+    """A routing workspace, pre-filled with garbage: its contents on entry
+    must not matter."""
+    return torch.full((max(1, pkg.moe_gemv_ws_bytes(m, topk, e, k)),), 0xA5, dtype=torch.uint8, device=DEV)
+
+
+@pytest.mark.parametrize("m", [33, 64, 130, 300])
+@pytest.mark.parametrize("E,n,k,topk", [(8, 256, 512, 2), (16, 320, 704, 4), (6, 130, 256, 6), (32, 128, 128, 12)])
+def test_moe_grouped_small(pkg, m, E, n, k, topk):
+    codes, scales = experts(E, n, k, 100 + E + n)
+    ids = route(m, topk, E, m + E)
+    x = inputs.activations(m, k, 3 + m)
+    y, raw = guarded_empty((m, topk, n), torch.bfloat16, DEV)
+    pkg.moe_gemv_ws(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                    torch.from_numpy(scales).to(DEV), ws(pkg, m, topk, E, k), y=y)
+    torch.cuda.synchronize()
+    assert guard_intact(raw, m * topk * n * 2)
+    check(y, bits(x), ids, codes, scales)
+    assert pkg.check_device_error() == 0
+
+
+def test_moe_grouped_many_tiles_per_expert(pkg):
+    """Skewed routing: every token picks experts 0 and 1 (300 pairs each, two
+    256-pair tiles per expert, the second partial), the other experts get
+    none and their weights are NaN codes that must never be read."""
+    E, n, k, m, topk = 4, 256, 512, 300, 2
+    codes, scales = experts(E, n, k, 77)
+    codes[2:] = 0x7F
+    ids = np.tile(np.array([[0, 1]], dtype=np.int32), (m, 1))
+    ids[::3] = ids[::3, ::-1]
+    x = inputs.activations(m, k, 9)
+    y = pkg.moe_gemv_ws(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                        torch.from_numpy(scales).to(DEV), ws(pkg, m, topk, E, k))
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(y.float()).all())
+    check(y, bits(x), ids, codes, scales)
+    assert pkg.check_device_error() == 0
+
+
+def test_moe_grouped_out_of_range_id(pkg):
+    E, n, k, m, topk = 8, 256, 256, 40, 2
+    codes, scales = experts(E, n, k, 5)
+    ids = route(m, topk, E, 3)
+    ids[7, 1] = 99
+    ids[20, 0] = -1
+    x = inputs.activations(m, k, 4)
+    y = torch.full((m, topk, n), 7.0, dtype=torch.bfloat16, device=DEV)
+    pkg.moe_gemv_ws(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                    torch.from_numpy(scales).to(DEV), ws(pkg, m, topk, E, k), y=y)
+    assert pkg.check_device_error() & 16
+    yc = y.cpu().float()
+    assert torch.all(yc[7, 1] == 7.0) and torch.all(yc[20, 0] == 7.0)
+    good = np.ones((m, topk), dtype=bool)
+    good[7, 1] = good[20, 0] = False
+    safe = np.where(good, ids, 0).astype(np.int32)
+    y64 = oracle.moe_gemv(bits(x), safe, codes, scales)
+    yb = bits(y.cpu())
+    for t, j in zip(*np.nonzero(good)):
+        e = ids[t, j]
+        wmax = np.abs(table()[codes[e]] * np.repeat(np.repeat(scales[e].astype(np.float64), 128, axis=0)[:n],
+                                                      128, axis=1)[:, :k]).max(axis=1)
+        st = tolerance.gemv_errors(yb[t, j][None, :], y64[t, j][None, :], bits(x)[t][None, :], wmax)
+        assert tolerance.gemv_ok(st), (t, j, st)
+
+
+@pytest.mark.parametrize("m", [64, 512])
+def test_moe_grouped_full_size_sampled(pkg, m):
+    """256 experts of [2048, 4096], top-12: the sampled experts' codes and
+    scales come from the oracle; every (token, slot) routed to one of them is
+    checked on 128 sampled weight rows."""
+    E, (n, k), topk = inputs.MOE_EXPERTS, inputs.MOE_SHAPE, inputs.MOE_TOPK
+    codes = torch.empty((E, n, k), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((E, n // 128, k // 128), dtype=torch.float32, device=DEV)
+    for e in range(E):
+        c, s_ = pkg.quantize(inputs.moe_expert_weight(e, device=DEV))
+        codes[e] = c
+        scales[e] = s_
+    ids = inputs.moe_routing(m, topk, E, seed=m).numpy().astype(np.int32)
+    sample = sorted(set(int(v) for v in ids[:4].ravel()))[:6]
+    rows = np.arange(640, 768)
+    oc, os_ = {}, {}
+    for e in sample:
+        w = inputs.moe_expert_weight(e)
+        c, s = oracle.block_quantize(bits(w))
+        codes[e] = torch.from_numpy(c).to(DEV)
+        scales[e] = torch.from_numpy(s).to(DEV)
+        oc[e], os_[e] = c, s
+    x = inputs.activations(m, k, 800 + m)
+    y = pkg.moe_gemv_ws(x.to(DEV), torch.from_numpy(ids).to(DEV), codes, scales, ws(pkg, m, topk, E, k))
+    torch.cuda.synchronize()
+    yb, xb = bits(y.cpu()), bits(x)
+    for e in sample:
+        pairs = np.argwhere(ids == e)
+        y64 = oracle.block_gemv(xb[pairs[:, 0]], oc[e], os_[e], rows=rows)
+        wmax = tolerance.block_wmax_rows(oc[e][rows], os_[e], rows, table())
+        got = np.stack([yb[t, j][rows] for t, j in pairs])
+        st = tolerance.gemv_errors(got, y64, xb[pairs[:, 0]], wmax)
+        assert tolerance.gemv_ok(st), (e, st)
+    assert pkg.check_device_error() == 0
