@@ -468,9 +468,13 @@ def moe_prefill_workload(torch, fp8bs, inputs, dev):
         codes[e] = c
         scales[e] = s_
     ms = [512, 2048]
-    calls = []
+    calls, hbm = [], []
     for m in ms:
         ids = inputs.moe_routing(m, topk, E, seed=m).to(dev)
+        # algorithmic bytes: every selected expert's codes and scales once,
+        # x, the routing ids and y
+        sel = int(torch.unique(ids).numel())
+        hbm.append(sel * (n * k + 4 * (n // 128) * (k // 128)) + 2 * m * k + 4 * m * topk + 2 * m * topk * n)
         x = inputs.activations(m, k, 850 + m, device=dev)
         y = torch.empty((m, topk, n), dtype=torch.bfloat16, device=dev)
         work = torch.empty((fp8bs.moe_gemv_ws_bytes(m, topk, E, k),), dtype=torch.uint8, device=dev)
@@ -480,7 +484,7 @@ def moe_prefill_workload(torch, fp8bs, inputs, dev):
                        "(fp8bs_moe_gemv_ws: routing grouped on the device, one grouped tcgen05 GEMM)",
            "experts": E, "n": n, "k": k, "topk": topk, "ms": ms,
            "l2": "inputs larger than L2 (2.1 GB of expert codes, nearly all selected)"}
-    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel<0,true>", [0, 1]), flops=True,
+    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel<0,true>", [0, 1]), flops=True, hbm_bytes=hbm,
                 call_launches=[5, 5])
 
 
@@ -793,12 +797,17 @@ def summarize(wl, per, total_ms, steps, workload):
     step_bytes = sum(b for _, _, b, _ in calls)
     value = step_bytes * steps / (total_ms * 1e-3) / scale_unit
     per_call = {}
-    for (name, m, b, _), t in zip(calls, per):
+    hbm_bytes = wl.get("hbm_bytes")   # a contraction's algorithmic HBM bytes per call, where it has them
+    for i, ((name, m, b, _), t) in enumerate(zip(calls, per)):
         lp = wl.get("gemvs_per_call", wl.get("launches_per_call", 1))   # us per GEMV / kernel call
         rate = b / (t * 1e-3) / scale_unit
         if flops:
             per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "tflop_s": round(rate, 1),
                               "frac_of_peak": round(rate / tpeak, 4)}
+            if hbm_bytes:
+                gbs = hbm_bytes[i] / (t * 1e-3) / 1e9
+                per_call[name].update(gb_s=round(gbs, 1), frac_of_measured_hbm=round(gbs / peak, 4),
+                                      bound="hbm" if hbm_bytes[i] / peak > b / 1e3 / tpeak else "tensor")
         else:
             per_call[name] = {"us_per_call": round(1e3 * t / lp, 3), "gb_s": round(rate, 1),
                               "frac_of_8TBps": round(rate / HBM_NOMINAL_GBS, 4),
@@ -807,7 +816,16 @@ def summarize(wl, per, total_ms, steps, workload):
     dom_bytes = sum(calls[i][2] for i in dom_idx)
     dom_ms = sum(per[i] for i in dom_idx)
     achieved = dom_bytes / (dom_ms * 1e-3) / scale_unit
-    if flops:
+    if flops and hbm_bytes and sum(hbm_bytes[i] for i in dom_idx) / peak > dom_bytes / 1e3 / tpeak:
+        # more time in the bytes than in the flops at the peaks: bound by HBM
+        hb = sum(hbm_bytes[i] for i in dom_idx)
+        gbs = hb / (dom_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom_name, "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(gbs / peak, 4), "peak_kind": f"hbm_gbs ({peak_kind})",
+                    "traffic": measured_traffic(dom_name, workload),
+                    "tensor": {"achieved": round(achieved, 1), "peak": tpeak, "unit": "TFLOP/s",
+                               "frac": round(achieved / tpeak, 4)}}
+    elif flops:
         roofline = {"bound": "tensor", "kernel": dom_name, "achieved": round(achieved, 1), "peak": tpeak,
                     "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
                     "peak_kind": f"bf16_tflops ({tpeak_kind})", "traffic": None,

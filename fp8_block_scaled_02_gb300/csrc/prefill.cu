@@ -3,13 +3,18 @@
 // y[M, N] = x[M, K] . dequant(W)^T.
 //
 // Design (sm_103a, one CTA per 128 weight rows x 256 rows of x, 20 warps):
-//  * Weights are the MMA's A operand.  Eight "decoder" warps stream their
-//    rows' e4m3 codes from global memory (each thread owns one weight row
-//    and one 64-wide K half, loading one K block ahead), convert them
-//    exactly to bf16 pairs in registers and store them into a
-//    double-buffered shared-memory A slot in the 128-byte-swizzled K-major
-//    layout the tensor core reads.  The decoded weight never reaches HBM,
-//    and each decoded 128 x 128 block feeds all 256 rows of x.
+//  * Weights are the MMA's A operand.  A producer thread brings each K
+//    block's 128 x 128 e4m3 codes with 2-D TMA (128-byte swizzle) into a
+//    two-stage shared-memory ring, and for weights read from HBM asks L2
+//    for the codes several K blocks further ahead.  Eight "decoder" warps
+//    (each thread one weight row and one 64-wide K half) read their codes
+//    from the ring, free the stage, convert them exactly to bf16 pairs in
+//    registers and store them into a double-buffered shared-memory A slot
+//    in the 128-byte-swizzled K-major layout the tensor core reads.  The
+//    decoded weight never reaches HBM, and each decoded 128 x 128 block
+//    feeds all 256 rows of x.  (Loading codes straight into the decoders'
+//    registers, one K block ahead, left each decoder waiting a full memory
+//    latency per K block: 16 KB in flight per SM.)
 //  * x is the B operand: one producer thread brings each K block's 256 x
 //    rows with 2-D TMA (128-byte swizzle, two 64-column panels) into a
 //    two-stage 128 KB shared-memory ring.
@@ -63,6 +68,9 @@ constexpr int kXStages = 2;
 constexpr int kXBytes = kXStages * kXStage;  // x ring: 128 KB
 constexpr int kASlots = 2;                  // decoded weight blocks in flight
 constexpr int kASlot = 2 * kPanel;          // 32 KB
+constexpr int kCStage = kTileW * kKB;      // one K block of e4m3 codes, 16 KB
+constexpr int kCStages = 2;                 // codes ring
+constexpr int kCodesAhead = 4;              // L2 prefetch distance (K blocks past the load)
 constexpr int kRing = 8;  // MMA-completion barriers, one per K block; >= every look-back
 static_assert(kXStages <= kRing && kASlots <= kRing, "a wait must never reach back a full ring");
 constexpr int kTmemCols = 512;              // partials D_0, D_1: columns [0, 256), [256, 512)
@@ -73,12 +81,14 @@ constexpr int kTmemCols = 512;              // partials D_0, D_1: columns [0, 25
 //                               K half warp / 4;
 //   warpgroups 2-3 (warps 8-15) epilogue: TMEM lane quarter warp % 4, half
 //                               (warp - 8) / 4, 128 fp32 totals per thread;
-//   warpgroup 4   (warps 16-19) MMA issuer (+ TMEM), x producer, two idle.
+//   warpgroup 4   (warps 16-19) MMA issuer (+ TMEM), x producer, codes
+//                               producer, one idle.
 constexpr int kNumDec = 8;
 constexpr int kNumEpi = 8;
 constexpr int kWarpEpi0 = kNumDec;
 constexpr int kWarpMma = kWarpEpi0 + kNumEpi;
 constexpr int kWarpTma = kWarpMma + 1;
+constexpr int kWarpCodes = kWarpMma + 2;
 constexpr int kThreads = (kWarpMma + 4) * 32;
 constexpr int kRegCtl = 40, kRegDec = 64, kRegEpi = 152;
 // The split must fit in what the block is launched with (the launcher checks
@@ -89,27 +99,39 @@ static_assert(4 * 32 * kRegCtl + kNumDec * 32 * kRegDec + kNumEpi * 32 * kRegEpi
 static_assert(kThreads * kRegLaunch <= 65536, "launch allocation exceeds the register file");
 static_assert(kRegCtl % 8 == 0 && kRegDec % 8 == 0 && kRegEpi % 8 == 0, "setmaxnreg counts are multiples of 8");
 static_assert(kNumDec % 4 == 0 && kNumEpi % 4 == 0, "roles must fill whole warpgroups");
-constexpr int kSmemBytes = 1024 + kXBytes + kASlots * kASlot + 256;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+constexpr int kSmemBytes = 1024 + kXBytes + kASlots * kASlot + kCStages * kCStage + 256;
+static_assert(kSmemBytes + 4 * kTileX + 64 <= 227 * 1024, "shared memory per CTA (with the static arrays)");
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
 // M >> 4 at bits 24-28.
-template <int N>
-__host__ __device__ constexpr uint32_t idesc_f16() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+__host__ __device__ constexpr uint32_t idesc_f16_n(int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(kTileW >> 4) << 24);
 }
-
-__device__ __forceinline__ uint4 ld_codes16(const uint8_t *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+template <int N>
+__host__ __device__ constexpr uint32_t idesc_f16() {
+    return idesc_f16_n(N);
 }
 
+// MOE: x rows per TMA box.  A tile loads only the boxes that hold its pairs
+// (an expert's tile often holds far fewer than 256); stacked at 4 KB steps
+// the boxes give the layout of one 256-row box.
+constexpr int kMoeXBox = 32;
+
 __device__ __forceinline__ void fail(uint32_t bit) { atomicOr(&g_prefill_err, bit); }
+
+// Both operands from shared memory; the instruction descriptor in a register
+// (MOE: N = the tile's pairs rounded up to 16).
+__device__ __forceinline__ void tc_mma_ss_r(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %3, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(idesc)
+        : "memory");
+}
 
 // Both operands from shared memory.
 template <uint32_t kIdesc>
@@ -147,12 +169,16 @@ struct MoeTiles {
 // tile of up to 256 (token, slot) pairs of one expert (CTAs past the last
 // tile leave at once), blockIdx.x a 128-row tile of that expert's weight
 // (codes [E * n, k], scales [E, ceil(n/128), kblocks]).  tm_x maps the x
-// rows copied in pair order (moe.cu: xs [pairs, k]), so a tile's rows are
-// one ordinary TMA box starting at its first pair; output row j goes to
-// y[pair_j * n + row] (y: [tokens, topk, n]).
+// rows copied in pair order (moe.cu: xs [pairs, k]) in boxes of kMoeXBox
+// rows, so a tile's rows are ordinary TMA boxes starting at its first pair;
+// output row j goes to y[pair_j * n + row] (y: [tokens, topk, n]).  The
+// tile's work follows its pair count: only the boxes holding its pairs are
+// loaded, the MMAs run N = pairs rounded up to 16 (at 24 pairs an expert
+// costs an eighth of the 256-wide MMA), and the epilogue reads only those
+// TMEM columns.
 template <int SC, bool MOE = false>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_x,
-                                                              const uint8_t *__restrict__ codes,
+                                                              const __grid_constant__ CUtensorMap tm_codes,
                                                               const float *__restrict__ scales,
                                                               const uint8_t *__restrict__ e8m0, int groups,
                                                               __nv_bfloat16 *__restrict__ y, int m, int n,
@@ -169,13 +195,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                                 ~static_cast<uintptr_t>(1023));
     uint8_t *xring = smem;                              // [kXStages][2 panels][256 rows][128 B]
     uint8_t *aring = smem + kXBytes;                    // [kASlots][2 panels][128 rows][128 B]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(aring + kASlots * kASlot);
+    uint8_t *cring = aring + kASlots * kASlot;          // [kCStages][128 rows][128 B] codes
+    uint64_t *bars = reinterpret_cast<uint64_t *>(cring + kCStages * kCStage);
     uint64_t *x_full = bars;                 // [kXStages]
     uint64_t *done = x_full + kXStages;      // [kRing] MMAs of K block kb finished
     uint64_t *a_full = done + kRing;         // [kASlots]
     uint64_t *d_empty = a_full + kASlots;    // [2] partial D_b read by every epilogue warp
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(d_empty + 2);
-    int *s_fail = reinterpret_cast<int *>(d_empty + 3);
+    uint64_t *c_full = d_empty + 2;          // [kCStages] codes landed
+    uint64_t *c_empty = c_full + kCStages;   // [kCStages] codes read by every decoder warp
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(c_empty + kCStages);
+    int *s_fail = reinterpret_cast<int *>(c_empty + kCStages + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool deep_prefetch = MOE || xfast;
@@ -189,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     int m0 = (xfast ? blockIdx.x : blockIdx.y) * kTileX;  // MOE: the tile's first pair
 
     int expert = 0;
+    int live = kTileX;  // MOE: this tile's pairs
     if (MOE) {
         // this CTA's expert and pairs (the routing kernels ran before it in
         // the stream); every thread reads the same words, so the exit is
@@ -209,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int p0 = __ldg(moe.tok_off + expert) + (tile - __ldg(moe.tile_off + expert)) * kTileX;
         const int cnt = min(kTileX, __ldg(moe.tok_off + expert + 1) - p0);
         m0 = p0;
+        live = cnt;
         for (int i = threadIdx.x; i < kTileX; i += blockDim.x) s_pair[i] = i < cnt ? __ldg(moe.perm + p0 + i) : -1;
     }
 
@@ -217,10 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int i = 0; i < kRing; ++i) mbar_init(&done[i], 1);  // tcgen05.commit
         for (int i = 0; i < kASlots; ++i) mbar_init(&a_full[i], kNumDec);
         for (int i = 0; i < 2; ++i) mbar_init(&d_empty[i], kNumEpi);
+        for (int i = 0; i < kCStages; ++i) {
+            mbar_init(&c_full[i], 1);
+            mbar_init(&c_empty[i], kNumDec);
+        }
         *s_fail = 0;
         fence_mbarrier_init();
     }
     if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tm_x);
+    if (warp == kWarpCodes && lane == 0) prefetch_tensormap(&tm_codes);
     if (warp == kWarpMma) tc_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -255,7 +291,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     for (int kk = 0; kk < kKB / 16; ++kk) {
                         const uint64_t aoff = static_cast<uint64_t>((kk >> 2) * (kPanel >> 4) + (kk & 3) * 2);
                         const uint64_t boff = static_cast<uint64_t>((kk >> 2) * (kXPanel >> 4) + (kk & 3) * 2);
-                        tc_mma_ss<idesc_f16<kTileX>()>(d_tmem, adesc + aoff, bdesc + boff, kk > 0 ? 1u : 0u);
+                        if (MOE)
+                            tc_mma_ss_r(d_tmem, adesc + aoff, bdesc + boff, idesc_f16_n((live + 15) & ~15),
+                                        kk > 0 ? 1u : 0u);
+                        else
+                            tc_mma_ss<idesc_f16<kTileX>()>(d_tmem, adesc + aoff, bdesc + boff, kk > 0 ? 1u : 0u);
                     }
                     tc_commit(&done[kb % kRing]);
                     issued = kb + 1;
@@ -278,9 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     }
                     if (*reinterpret_cast<volatile int *>(s_fail)) break;
                     uint8_t *st = xring + xs * kXStage;
-                    mbar_arrive_expect_tx(&x_full[xs], kXStage);
-                    tma_load_2d(st, &tm_x, &x_full[xs], kb * kKB, m0);
-                    tma_load_2d(st + kXPanel, &tm_x, &x_full[xs], kb * kKB + 64, m0);
+                    if (MOE) {
+                        // the boxes holding the tile's pairs (rows past the
+                        // pairs feed only MMA columns that are never stored)
+                        const int boxes = (live + kMoeXBox - 1) / kMoeXBox;
+                        mbar_arrive_expect_tx(&x_full[xs], boxes * 2 * kMoeXBox * 128);
+                        for (int bx = 0; bx < boxes; ++bx) {
+                            tma_load_2d(st + bx * kMoeXBox * 128, &tm_x, &x_full[xs], kb * kKB, m0 + bx * kMoeXBox);
+                            tma_load_2d(st + kXPanel + bx * kMoeXBox * 128, &tm_x, &x_full[xs], kb * kKB + 64,
+                                        m0 + bx * kMoeXBox);
+                        }
+                    } else {
+                        mbar_arrive_expect_tx(&x_full[xs], kXStage);
+                        tma_load_2d(st, &tm_x, &x_full[xs], kb * kKB, m0);
+                        tma_load_2d(st + kXPanel, &tm_x, &x_full[xs], kb * kKB + 64, m0);
+                    }
                     issued = kb + 1;
                 }
                 // never leave with copies in flight
@@ -288,27 +340,53 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     if (!mbar_wait_bounded(&x_full[u % kXStages], (u / kXStages) & 1)) fail(ERRBIT_FULL_WAIT);
             }
             __syncwarp();
+        } else if (warp == kWarpCodes) {
+            // ------------------------------------------------------ codes producer
+            if (lane == 0) {
+                // MOE: the expert's rows start at expert * n of the stacked
+                // codes (rows of a ragged last tile past n belong to the next
+                // expert or lie outside the map: they only feed TMEM lanes
+                // whose outputs are never stored)
+                const int crow0 = (MOE ? expert * n : 0) + n0;
+                int issued = 0;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const int cs = kb % kCStages;
+                    if (kb >= kCStages &&
+                        !mbar_wait_bounded(&c_empty[cs], ((kb - kCStages) / kCStages) & 1)) {
+                        fail(ERRBIT_EMPTY_WAIT);
+                        break;
+                    }
+                    if (*reinterpret_cast<volatile int *>(s_fail)) break;
+                    if (deep_prefetch) {
+                        // a weight read from HBM (too large for L2, or an
+                        // expert read once per tile of its pairs): keep L2
+                        // fetching kCodesAhead K blocks past the loads
+                        if (kb == 0)
+                            for (int p = kCStages; p < kCodesAhead && p < kblocks; ++p)
+                                tma_prefetch_l2_2d(&tm_codes, p * kKB, crow0);
+                        if (kb + kCodesAhead < kblocks) tma_prefetch_l2_2d(&tm_codes, (kb + kCodesAhead) * kKB, crow0);
+                    }
+                    mbar_arrive_expect_tx(&c_full[cs], kCStage);
+                    tma_load_2d(cring + cs * kCStage, &tm_codes, &c_full[cs], kb * kKB, crow0);
+                    issued = kb + 1;
+                }
+                for (int u = issued - kCStages < 0 ? 0 : issued - kCStages; u < issued; ++u)
+                    if (!mbar_wait_bounded(&c_full[u % kCStages], (u / kCStages) & 1)) fail(ERRBIT_FULL_WAIT);
+            }
+            __syncwarp();
         }
     } else if (wg < kWarpEpi0 / 4) {
         setmaxnreg_dec<kRegDec>();
         // ------------------------------------------------------ decoders
         // thread = one weight row r; this warp converts the K half kh of
-        // every K block, one block ahead of the conversion
+        // every K block from the codes ring
         const int r = (warp & 3) * 32 + lane;
         const int kh = warp >> 2;
         const int row = n0 + r;
         const bool row_ok = row < n;
-        // MOE: the expert's rows start at expert * n in the stacked codes
-        const uint8_t *rp = codes + (static_cast<int64_t>(expert) * n + (row_ok ? row : 0)) * k + kh * 64;
-        auto load4 = [&](int kb, uint4 (&v)[4]) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int col = kb * kKB + kh * 64 + j * 16;
-                v[j] = (kb < kblocks && row_ok && col < k) ? ld_codes16(rp + kb * kKB + j * 16) : make_uint4(0, 0, 0, 0);
-            }
-        };
         // MX: the row's exponents of the two 32-column groups of this K half
-        // (E = 127, scale 1, past the row's groups: those codes are zero)
+        // (E = 127, scale 1, past the row's groups: those codes are zero),
+        // loaded four K blocks ahead into a register queue
         const uint8_t *ep = MX ? e8m0 + static_cast<int64_t>(row_ok ? row : 0) * groups + 2 * kh : nullptr;
         auto load_e = [&](int kb) -> uint32_t {
             uint32_t e = 0x7F7Fu;
@@ -319,21 +397,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
             return e;
         };
-        uint4 c0[4], c1[4];
-        load4(0, c0);
-        uint32_t e0 = load_e(0), e1 = 0;
+        uint32_t eq0 = load_e(0), eq1 = load_e(1), eq2 = load_e(2), eq3 = load_e(3);
         for (int kb = 0; kb < kblocks; ++kb) {
-            const int as = kb % kASlots;
-            load4(kb + 1, c1);  // in flight while this block is converted
-            // a weight read from HBM (too large for L2, or an expert read once
-            // per tile of its pairs): ask L2 for this row's codes four K
-            // blocks ahead, beyond the one block the registers hold
-            if (deep_prefetch && row_ok && kb + 4 < kblocks)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(rp + (kb + 4) * kKB));
-            if (MX) e1 = load_e(kb + 1);
+            const int as = kb % kASlots, cs = kb % kCStages;
+            // this K block's codes: 16 bytes at a time from the swizzled
+            // rows (chunk c of row r sits at chunk c ^ (r & 7)), then the
+            // stage goes back to the producer
+            bool ok = mbar_wait_bounded(&c_full[cs], (kb / kCStages) & 1);
+            if (!__all_sync(0xffffffffu, ok) || *reinterpret_cast<volatile int *>(s_fail)) {
+                if (lane == 0) fail(ERRBIT_FULL_WAIT);
+                break;
+            }
+            uint4 c0[4];
+            const uint8_t *crow = cring + cs * kCStage + r * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                c0[j] = *reinterpret_cast<const uint4 *>(crow + (((4 * kh + j) ^ (r & 7)) << 4));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c_empty[cs]);
+            const uint32_t e0 = eq0;
+            if (MX) {
+                eq0 = eq1;
+                eq1 = eq2;
+                eq2 = eq3;
+                eq3 = load_e(kb + 4);
+            }
             // slot `as` was last read by the MMAs of K block kb - kASlots
             const int prev = kb - kASlots;
-            bool ok = kb < kASlots || mbar_wait_bounded(&done[prev % kRing], (prev / kRing) & 1);
+            ok = kb < kASlots || mbar_wait_bounded(&done[prev % kRing], (prev / kRing) & 1);
             if (!__all_sync(0xffffffffu, ok) || *reinterpret_cast<volatile int *>(s_fail)) {
                 if (lane == 0) fail(ERRBIT_EMPTY_WAIT);
                 break;
@@ -388,9 +479,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[as]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) c0[j] = c1[j];
-            e0 = e1;
         }
     } else {
         setmaxnreg_inc<kRegEpi>();
@@ -403,15 +491,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
         const int row = n0 + q * 32 + lane;
         const float *srow = (ROW || MX) ? nullptr : scales + static_cast<int64_t>(MOE ? s_srow : wtile) * kblocks;
+        const int live_cols = MOE ? live - h * kHalfX : kHalfX;  // MOE: TMEM columns the MMAs wrote
         float tot[kHalfX];
 #pragma unroll
         for (int j = 0; j < kHalfX; ++j) tot[j] = 0.0f;
         bool ok = true;
-        // K block scale (1 with one scale per row: the partials add unscaled)
-        float s_next = (ROW || MX) ? 1.0f : __ldg(srow);
+        // K block scale, loaded one block ahead (1 with one scale per row:
+        // the partials add unscaled).  A deeper queue spills the 128 totals.
+        auto load_s = [&](int kb) -> float { return (ROW || MX || kb >= kblocks) ? 1.0f : __ldg(srow + kb); };
+        float s_next = load_s(0);
         for (int kb = 0; kb < kblocks; ++kb) {
             const float s = s_next;
-            if (!ROW && !MX && kb + 1 < kblocks) s_next = __ldg(srow + kb + 1);
+            if (!ROW && !MX) s_next = load_s(kb + 1);
             ok = mbar_wait_bounded(&done[kb % kRing], (kb / kRing) & 1);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) fail(ERRBIT_FULL_WAIT);
@@ -422,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const uint32_t d_addr = lane_base + 256 * (kb & 1);
 #pragma unroll
             for (int c = 0; c < kHalfX / 16; ++c) {
+                if (MOE && 16 * c >= live_cols) break;
                 uint32_t dv[16];
                 tc_ld16(d_addr + 16 * c, dv);
                 tc_wait_ld();
@@ -504,6 +596,11 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
     if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64,
                               static_cast<uint32_t>(kTileX), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    // one box = one K block of the CTA's 128 weight rows
+    CUtensorMap tm_codes;
+    if (!encode_tensor_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, k, static_cast<uint64_t>(a.n), k,
+                              kKB, kTileW, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
     // x tiles fastest when the codes are too large to stay in L2 (half of
     // its 129 MB) beside the x tiles; weight tiles fastest otherwise
@@ -519,7 +616,7 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
     auto kern = a.kind == kScaleRow ? prefill_kernel<kScaleRow>
                                     : (a.kind == kScaleMx ? prefill_kernel<kScaleMx> : prefill_kernel<kScaleBlock>);
     const int groups = static_cast<int>((a.k + 31) / 32);
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, a.codes, a.scales, a.e8m0, groups, y, mi, ni, ki, kblocks,
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_x, tm_codes, a.scales, a.e8m0, groups, y, mi, ni, ki, kblocks,
                                                  a.kind == kScaleRow ? a.row_stride : 0, xfast,
                                                  MoeTiles{nullptr, nullptr, nullptr, 0, 0});
     return cudaGetLastError();
@@ -533,9 +630,15 @@ cudaError_t launch_prefill_moe(const DecodeArgs &a, const MoeArgs &g, const MoeR
     CUtensorMap tm_x;
     const int64_t pairs = a.m * g.topk;
     const uint64_t k = static_cast<uint64_t>(a.k);
-    // the x rows in pair order (r.xs [pairs, k]); a tile is one box of 256
+    // the x rows in pair order (r.xs [pairs, k]); a tile loads the boxes of
+    // kMoeXBox rows that hold its pairs
     if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r.xs, k, static_cast<uint64_t>(pairs), k * 2,
-                              64, static_cast<uint32_t>(kTileX), CU_TENSOR_MAP_SWIZZLE_128B))
+                              64, static_cast<uint32_t>(kMoeXBox), CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    CUtensorMap tm_codes;  // the stacked experts' codes [E * n, k]
+    if (!encode_tensor_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, k,
+                              static_cast<uint64_t>(g.num_experts) * static_cast<uint64_t>(a.n), k, kKB, kTileW,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int64_t wtiles = (a.n + kTileW - 1) / kTileW;
     // at most ceil(pairs / 256) full tiles plus one partial tile per expert;
@@ -545,7 +648,7 @@ cudaError_t launch_prefill_moe(const DecodeArgs &a, const MoeArgs &g, const MoeR
     const dim3 grid(static_cast<unsigned>(wtiles), static_cast<unsigned>(tbound));
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
     prefill_kernel<kScaleBlock, true><<<grid, kThreads, kSmemBytes, stream>>>(
-        tm_x, a.codes, a.scales, nullptr, 0, static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(pairs),
+        tm_x, tm_codes, a.scales, nullptr, 0, static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(pairs),
         static_cast<int>(a.n), static_cast<int>(a.k), kblocks, 0, 0,
         MoeTiles{r.tile_off, r.tok_off, r.perm, static_cast<int>(g.topk), static_cast<int>(g.num_experts)});
     return cudaGetLastError();

@@ -230,6 +230,38 @@ def test_moe_grouped_many_tiles_per_expert(pkg):
     assert pkg.check_device_error() == 0
 
 
+def test_moe_grouped_pair_counts_across_box_and_mma_edges(pkg):
+    """One routing whose experts receive 1, 15, 16, 17, 31, 32, 33, 0, 127,
+    128, 129, 255, 256, 257, 300 and 5 pairs (tokens shuffled): each expert
+    tile loads only the 32-row x boxes holding its pairs and runs its MMAs
+    at N = pairs rounded up to 16, so every count around a box, an MMA-N
+    step and a 256-pair tile edge is checked, every output in full."""
+    counts = [1, 15, 16, 17, 31, 32, 33, 0, 127, 128, 129, 255, 256, 257, 300, 5]
+    E, n, k = len(counts), 256, 512
+    codes, scales = experts(E, n, k, 41)
+    ids = np.repeat(np.arange(E, dtype=np.int32), counts)
+    np.random.default_rng(8).shuffle(ids)
+    ids = ids[:, None]
+    m = ids.shape[0]
+    x = inputs.activations(m, k, 12)
+    y, raw = guarded_empty((m, 1, n), torch.bfloat16, DEV)
+    pkg.moe_gemv_ws(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                    torch.from_numpy(scales).to(DEV), ws(pkg, m, 1, E, k), y=y)
+    torch.cuda.synchronize()
+    assert guard_intact(raw, m * n * 2)
+    yb, xb = bits(y.cpu()), bits(x)
+    for e in range(E):
+        toks = np.nonzero(ids[:, 0] == e)[0]
+        assert len(toks) == counts[e]
+        if not len(toks):
+            continue
+        y64 = oracle.block_gemv(xb[toks], codes[e], scales[e])
+        wmax = tolerance.block_wmax_rows(codes[e], scales[e], np.arange(n), table())
+        st = tolerance.gemv_errors(yb[toks, 0], y64, xb[toks], wmax)
+        assert tolerance.gemv_ok(st), (e, counts[e], st)
+    assert pkg.check_device_error() == 0
+
+
 def test_moe_grouped_out_of_range_id(pkg):
     E, n, k, m, topk = 8, 256, 256, 40, 2
     codes, scales = experts(E, n, k, 5)
