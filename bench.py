@@ -714,20 +714,38 @@ def _parallel(fn, chunks, threads):
     return time.perf_counter() - t
 
 
-def oracle_gemv_step(threads, ms=(1, 4, 8, 16)):
+ORACLE_MIN_SECONDS = 1.5     # each cpu_baseline measurement repeats its sample for at least this long
+
+
+def _repeat(once, min_seconds):
+    """Run once() (which returns its seconds) until min_seconds have passed;
+    returns (total seconds, repetitions)."""
+    total, reps = 0.0, 0
+    while reps == 0 or total < min_seconds:
+        total += once()
+        reps += 1
+    return total, reps
+
+
+def oracle_gemv_step(threads, ms=(1, 4, 8, 16), min_seconds=0.0):
     """The oracle's fp64 block GEMV on the lm_head sample, one call at each M
     (the bench step's M sweep) with its rows split over `threads` host
-    threads.  Returns (GB/s in the metric's units, seconds)."""
+    threads, repeated for at least min_seconds.  Returns (GB/s in the
+    metric's units, seconds)."""
     import oracle
     s = _oracle_samples()
     rows = s["codes"].shape[0]
     chunks = _row_chunks(rows, threads)
-    secs, nbytes = 0.0, 0
-    for m in ms:
-        x = s["xs"][m]
-        secs += _parallel(lambda r0, r1: oracle.block_gemv(x, s["codes"][r0:r1], s["scales"][r0 // 128:-(-r1 // 128)]),
-                          chunks, threads)
-        nbytes += gemv_bytes(m, rows, 4096)
+
+    def once():
+        secs = 0.0
+        for m in ms:
+            x = s["xs"][m]
+            secs += _parallel(lambda r0, r1: oracle.block_gemv(x, s["codes"][r0:r1],
+                                                               s["scales"][r0 // 128:-(-r1 // 128)]), chunks, threads)
+        return secs
+    secs, reps = _repeat(once, min_seconds)
+    nbytes = reps * sum(gemv_bytes(m, rows, 4096) for m in ms)
     return nbytes / secs / 1e9, secs
 
 
@@ -735,7 +753,8 @@ def oracle_runs(threads_list):
     """The CPU oracle as it stands, timed on the host cores: block quantize
     and MXFP8 quantize of the lm_head sample, the fp64 GEMV of the lm_head
     sample at M = 1 and of the rotation sample at M = 1, each with 1 and with
-    all host threads (rows split into contiguous 128-row ranges)."""
+    all host threads (rows split into contiguous 128-row ranges).  Each
+    measurement repeats its sample for at least ORACLE_MIN_SECONDS."""
     import oracle
     s = _oracle_samples()
     out = []
@@ -743,24 +762,24 @@ def oracle_runs(threads_list):
     qbytes = 3 * rq * 4096
     for t in threads_list:
         chunks = _row_chunks(rq, t)
-        sec = _parallel(lambda r0, r1: oracle.block_quantize(s["wq"][r0:r1]), chunks, t)
-        out.append({"op": "block_quantize", "workload": f"lm_head [{rq} of 152064 rows, 4096]", "cores": t,
-                    "gb_s": round(qbytes / sec / 1e9, 5), "seconds": round(sec, 3)})
-        sec = _parallel(lambda r0, r1: oracle.mx_quantize(s["wq"][r0:r1]), chunks, t)
-        out.append({"op": "mx_quantize", "workload": f"lm_head [{rq} of 152064 rows, 4096]", "cores": t,
-                    "gb_s": round(qbytes / sec / 1e9, 5), "seconds": round(sec, 3)})
-        v, sec = oracle_gemv_step(t, ms=(1,))
+        for op, fn in (("block_quantize", oracle.block_quantize), ("mx_quantize", oracle.mx_quantize)):
+            sec, reps = _repeat(lambda: _parallel(lambda r0, r1: fn(s["wq"][r0:r1]), chunks, t), ORACLE_MIN_SECONDS)
+            out.append({"op": op, "workload": f"lm_head [{rq} of 152064 rows, 4096]", "cores": t,
+                        "gb_s": round(reps * qbytes / sec / 1e9, 5), "seconds": round(sec, 3), "repetitions": reps})
+        v, sec = oracle_gemv_step(t, ms=(1,), min_seconds=ORACLE_MIN_SECONDS)
         out.append({"op": "block_gemv", "workload": f"lm_head M=1 [{s['codes'].shape[0]} of 152064 rows, 4096]",
                     "cores": t, "gb_s": round(v, 5), "seconds": round(sec, 3)})
-        sec, nbytes = 0.0, 0
-        for c, sc, x in s["rot"]:
-            r, k = c.shape
-            sec += _parallel(lambda r0, r1: oracle.block_gemv(x, c[r0:r1], sc[r0 // 128:-(-r1 // 128)]),
-                             _row_chunks(r, t), t)
-            nbytes += gemv_bytes(1, r, k)
-        rate = nbytes / sec
+
+        def rotation_once():
+            sec = 0.0
+            for c, sc, x in s["rot"]:
+                sec += _parallel(lambda r0, r1: oracle.block_gemv(x, c[r0:r1], sc[r0 // 128:-(-r1 // 128)]),
+                                 _row_chunks(c.shape[0], t), t)
+            return sec
+        sec, reps = _repeat(rotation_once, ORACLE_MIN_SECONDS)
+        rate = reps * sum(gemv_bytes(1, c.shape[0], c.shape[1]) for c, _, _ in s["rot"]) / sec
         out.append({"op": "block_gemv", "workload": "rotation M=1 (first 1024 rows of each projection shape)",
-                    "cores": t, "gb_s": round(rate / 1e9, 5), "seconds": round(sec, 3),
+                    "cores": t, "gb_s": round(rate / 1e9, 5), "seconds": round(sec, 3), "repetitions": reps,
                     "ms_per_rotation_step": round(1e3 * 2.5829e9 / rate, 1)})
     return out
 
@@ -768,7 +787,7 @@ def oracle_runs(threads_list):
 def oracle_sample_desc(threads):
     return (f"oracle block_gemv (plain C, fp64, as it stands) on {threads} host thread(s), rows split in 128-row "
             f"ranges: the first {ORACLE_GEMV_ROWS} of the 152064 lm_head rows, K=4096, one call at each of "
-            "M=1,4,8,16")
+            f"M=1,4,8,16, the sample repeated for at least {ORACLE_MIN_SECONDS} s")
 
 
 def host_cores():
@@ -987,7 +1006,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "lm_head":
         threads = host_cores()
-        v, _ = oracle_gemv_step(threads)
+        v, _ = oracle_gemv_step(threads, min_seconds=ORACLE_MIN_SECONDS)
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": oracle_sample_desc(threads), "runs": oracle_runs(sorted({1, threads}))}
 
