@@ -481,7 +481,7 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
                 for (int q = 0; q < 4; ++q) acc[j][q] = 0.0f;
             float s_next = (MX || ROW) ? 1.0f : __ldg(srow);
             // MX: lane l < 16 holds the e8m0 word (4 groups of this K block) of
-            // weight row 16*warp + l, fetched one K block ahead
+            // weight row 16*warp + l, fetched two K blocks ahead
             auto load_e8m0_word = [&](int kbi) -> uint32_t {
                 const int64_t row = static_cast<int64_t>(n0) + warp * 16 + lane;
                 const int g0 = (kbb + kbi) * 4;
@@ -498,13 +498,30 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
                 }
                 return w;
             };
+            // MX: ask L2 for this warp's rows' exponents of the whole unit (each
+            // row's run of 4 bytes per K block is contiguous), so the words
+            // fetched two K blocks ahead below come from L2, not HBM
+            if (MX && lane < 16) {
+                const int64_t row = static_cast<int64_t>(n0) + warp * 16 + lane;
+                const int g0 = kbb * 4;
+                const int bytes = min(nkb * 4, o.groups - g0);
+                if (row < o.n && bytes > 0) {
+                    const uint8_t *p = o.e8m0 + row * o.groups + g0;
+                    for (int off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p + bytes - 1));
+                }
+            }
             uint32_t e_next = MX ? load_e8m0_word(0) : 0u;
+            uint32_t e_next2 = (MX && nkb > 1) ? load_e8m0_word(1) : 0u;
             for (int kbi = 0; kbi < nkb; ++kbi, ++it) {
                 const int s = it % kStages;
                 const float sblk = s_next;
                 if (!MX && !ROW && kbi + 1 < nkb) s_next = __ldg(srow + kbi + 1);
                 const uint32_t e_cur = e_next;
-                if (MX && kbi + 1 < nkb) e_next = load_e8m0_word(kbi + 1);
+                if (MX) {
+                    e_next = e_next2;
+                    if (kbi + 2 < nkb) e_next2 = load_e8m0_word(kbi + 2);
+                }
                 const uint32_t ewa = MX ? __shfl_sync(0xffffffffu, e_cur, 2 * g) : 0u;
                 const uint32_t ewb = MX ? __shfl_sync(0xffffffffu, e_cur, 2 * g + 1) : 0u;
                 const uint32_t par = (it / kStages) & 1;
