@@ -184,6 +184,13 @@ __device__ __forceinline__ void dsmem_st_f32(uint32_t cluster_addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
+// Four consecutive floats (16-byte aligned cluster address).
+__device__ __forceinline__ void dsmem_st_f32x4(uint32_t cluster_addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
 // Volatile keeps it after the cluster barrier; several can still be in
 // flight when the caller issues them before using any result.
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {

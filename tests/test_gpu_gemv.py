@@ -207,6 +207,35 @@ def test_prefill_small_shapes(pkg, n, k, m):
     full_block_case(pkg, inputs.gaussian_bf16((n, k), 0.02, n * 17 + k), m, PATH_PREFILL, seed=m)
 
 
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("kind", ["block", "mx"])
+@pytest.mark.parametrize("k", [512, 1024])
+def test_prefill_split_last_wave(pkg, kind, k):
+    """A call whose tile count leaves a partial last wave of at most half the
+    SMs: those tiles run as a second launch split over K in clusters (their
+    partial sums exchanged between the CTAs), overlapping the full waves.
+    n = 2048 (16 weight tiles) and m = 256 * ceil(SMs / 16) + 1 give one more
+    ragged x tile than the full waves hold, so 16 tiles are split (with
+    k = 512 each split CTA runs a single K block).  Every output checked."""
+    n = 2048
+    m = 256 * (-(-_sms() // 16)) + 1
+    tiles = 16 * (-(-m // 256))
+    assert 0 < tiles % _sms() <= _sms() // 2
+    w = inputs.heavy_tail_weight(11, shape=(n, k), frac=0.01) if kind == "mx" else inputs.gaussian_bf16((n, k), 0.02, 5)
+    x = inputs.activations(m, k, 19)
+    if kind == "mx":
+        oc, oe = oracle.mx_quantize(bits(w))
+        y = pkg.mx_gemv(x.to(DEV), to_dev_bits(oc), to_dev_bits(oe), path=PATH_PREFILL)
+        torch.cuda.synchronize()
+        check_mx_gemv(y, bits(x), np.arange(n), oc, oe)
+    else:
+        full_block_case(pkg, w, m, PATH_PREFILL, seed=19)
+    assert pkg.check_device_error() == 0
+
+
 # ------------------------------------------------------ full-size, sampled
 def sampled_block_case(pkg, w_dev, ms, row_blocks, seed=11, path=0, x_rows=None):
     n, k = w_dev.shape
