@@ -481,10 +481,14 @@ def moe_prefill_workload(torch, fp8bs, inputs, dev):
         calls.append((f"M={m}", m, 2 * m * topk * n * k,
                       (lambda x=x, ids=ids, y=y, work=work: fp8bs.moe_gemv_ws(x, ids, codes, scales, work, y=y))))
     cfg = {"workload": "grouped MoE prefill: 256 block-FP8 experts [2048,4096], top-12 routing, M=512,2048 "
-                       "(fp8bs_moe_gemv_ws: routing grouped on the device, one grouped tcgen05 GEMM)",
+                       "(fp8bs_moe_gemv_ws: routing grouped on the device, then the decode kernel per 32-pair "
+                       "expert tile at M=512, one grouped tcgen05 GEMM at M=2048)",
            "experts": E, "n": n, "k": k, "topk": topk, "ms": ms,
            "l2": "inputs larger than L2 (2.1 GB of expert codes, nearly all selected)"}
-    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel<0,true>", [0, 1]), flops=True, hbm_bytes=hbm,
+    # M=512 (24 pairs per expert on average) takes the grouped decode path,
+    # M=2048 (96) the tensor-core grouped GEMM
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<4,0,false,true> + prefill_kernel<0,true>", [0, 1]),
+                flops=True, hbm_bytes=hbm,
                 call_launches=[5, 5])
 
 

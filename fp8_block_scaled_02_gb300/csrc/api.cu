@@ -370,6 +370,12 @@ int fp8bs_moe_gemv_ws(const void *x_bf16, int64_t m, const int32_t *expert_ids, 
     if (e != cudaSuccess) return FP8BS_ERR_CUDA;
     const DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k, kScaleBlock, 0};
     const MoeArgs g{expert_ids, topk, num_experts};
+    // few pairs per expert on average: stream each selected expert once per
+    // tile of 32 of its pairs at GEMV speed; more: the tensor-core GEMM
+    if (m * topk <= kMoeDecodeTile * num_experts) {
+        e = launch_moe_grouped(a, g, r, st);
+        if (e != cudaErrorNotSupported) return cuda_status(e);
+    }
     e = launch_prefill_moe(a, g, r, st);
     if (e == cudaErrorNotSupported)
         return moe_decode_chunks(x_bf16, m, expert_ids, topk, codes, scales, num_experts, n, k, y_bf16, st);

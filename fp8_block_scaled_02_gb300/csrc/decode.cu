@@ -203,6 +203,15 @@ __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r,
 //    streams across unit and op boundaries alike, so a sequence of GEMVs runs
 //    as one continuous weight stream instead of one launch (with its start-up
 //    and tail) per weight.
+// Grouped MoE by expert tiles (MOE with tile_off set): the routing's tiles
+// of up to kMoeDecodeTile (token, slot) pairs of one expert (moe.cu), whose
+// x rows were copied in pair order; tile_off nullptr: route by ids.
+struct MoeGroups {
+    const int32_t *tile_off;  // [E + 1] first tile of each expert (tile_off[E]: the count)
+    const int32_t *tok_off;   // [E + 1] first pair of each expert
+    const int32_t *perm;      // pair indices t * topk + j, expert by expert
+};
+
 // Per-op view of what the roles read: the tensor maps and the scale and
 // output pointers and sizes of one weight.
 struct OpRef {
@@ -218,6 +227,9 @@ struct OpRef {
 // SC: how the weight is scaled (ScaleKind: 128x128 blocks, MX groups, rows)
 // MOE: grouped expert GEMV (block scales); n is the rows of one expert, the
 // codes / scales hold num_experts such weights back to back, ids [m, topk].
+// With mg.tile_off set, blockIdx.z is an expert tile of the routing instead
+// (x: the pair-order copy, its rows from the tile's first pair; output row i
+// goes to y[pair_i * n + row], y: [tokens, topk, n]).
 // BATCH: the ops come from `bp` (the single-weight arguments are unused).
 template <int MT, int SC, bool F16, bool MOE, bool BATCH, bool XP = false>
 __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *__restrict__ xinv_g,
@@ -226,7 +238,8 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
                                             const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
                                             int m, int n, int kblocks, int groups, int splits, int ntiles,
                                             int e8m0_vec, int row_stride, const int32_t *__restrict__ ids,
-                                            int topk, int num_experts) {
+                                            int topk, int num_experts,
+                                            MoeGroups mg = MoeGroups{nullptr, nullptr, nullptr}) {
     constexpr bool MX = SC == kScaleMx;
     constexpr bool ROW = SC == kScaleRow;  // no per-K-block scale; scales[row * row_stride] at the end
     // no per-slice factor (e8m0 groups): the MMAs accumulate a whole K block
@@ -260,6 +273,7 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     __shared__ uint32_t s_bits[kMoeMaxExperts / 32];  // MOE: experts any token selected
     __shared__ int s_expert;                          // MOE: this CTA's expert
     __shared__ signed char s_route[32];               // MOE: slot j of x row mi for it, -1 if none
+    __shared__ int32_t s_pair[32];                    // MOE by tiles: pair of x row mi, -1 past the tile
 
     // Unit i of this CTA: its op (BATCH: `op` is a cursor that only moves
     // forward, units are visited in increasing order), first weight row and
@@ -327,7 +341,29 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     pdl_wait();  // inputs may be produced by the previous kernel in the stream
 
     int expert = 0;
-    if (MOE) {
+    int x_row0 = 0;  // MOE by tiles: the tile's first pair (row of the pair-order copy of x)
+    const bool by_tiles = MOE && mg.tile_off != nullptr;
+    if (by_tiles) {
+        // blockIdx.z is an expert tile; every CTA of a cluster shares it, so
+        // an idle cluster leaves whole, before anything is issued
+        const int tile = static_cast<int>(blockIdx.z);
+        if (tile >= __ldg(mg.tile_off + num_experts)) return;
+        if (threadIdx.x == 0) {
+            int lo = 0, hi = num_experts - 1;  // largest e with tile_off[e] <= tile
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (__ldg(mg.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
+            }
+            s_expert = lo;
+        }
+        __syncthreads();
+        expert = s_expert;
+        const int p0 = __ldg(mg.tok_off + expert) + (tile - __ldg(mg.tile_off + expert)) * kMoeDecodeTile;
+        const int cnt = min(kMoeDecodeTile, __ldg(mg.tok_off + expert + 1) - p0);
+        if (threadIdx.x < 32) s_pair[threadIdx.x] = threadIdx.x < cnt ? __ldg(mg.perm + p0 + threadIdx.x) : -1;
+        x_row0 = p0;
+        __syncthreads();
+    } else if (MOE) {
         for (int i = threadIdx.x; i < kMoeMaxExperts / 32; i += blockDim.x) s_bits[i] = 0;
         __syncthreads();
         for (int i = threadIdx.x; i < m * topk; i += blockDim.x) {
@@ -383,6 +419,10 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     // `nrows` rows, or -1 if not stored
     auto out_at = [&](int mi, int nn, int nrows) -> int64_t {
         if (!MOE) return static_cast<int64_t>(mi) * nrows + nn;
+        if (by_tiles) {
+            const int pr = mi < 32 ? s_pair[mi] : -1;
+            return pr < 0 ? -1 : static_cast<int64_t>(pr) * nrows + nn;
+        }
         const int j = s_route[mi];
         return j < 0 ? -1 : (static_cast<int64_t>(mi) * topk + j) * nrows + nn;
     };
@@ -415,8 +455,8 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
                     uint8_t *st = smem + s * C::kStageBytes;
                     mbar_arrive_expect_tx(&full[s], C::kStageBytes + (XP ? C::kXRows * 4 : 0));
                     tma_load_2d_hint(st, o.tm_codes, &full[s], kx, row_base + n0, stream_policy);
-                    tma_load_2d(st + C::kCodeBytes, o.tm_x, &full[s], kx, 0);
-                    tma_load_2d(st + C::kCodeBytes + C::kXPanelBytes, o.tm_x, &full[s], kx + 64, 0);
+                    tma_load_2d(st + C::kCodeBytes, o.tm_x, &full[s], kx, x_row0);
+                    tma_load_2d(st + C::kCodeBytes + C::kXPanelBytes, o.tm_x, &full[s], kx + 64, x_row0);
                     // prepared x: this K block's inverse factors, in the slot
                     // order the consumers read (xprep_kernel)
                     if (XP)
@@ -704,9 +744,10 @@ __global__ void __launch_bounds__(Cfg<MT, SC == kScaleMx, F16, XP>::kThreads,
     decode_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_x,
                   const float *__restrict__ scales, const uint8_t *__restrict__ e8m0, __nv_bfloat16 *__restrict__ y,
                   int m, int n, int kblocks, int groups, int splits, int ntiles, int e8m0_vec, int row_stride,
-                  const int32_t *__restrict__ ids, int topk, int num_experts, const float *__restrict__ xinv) {
+                  const int32_t *__restrict__ ids, int topk, int num_experts, const float *__restrict__ xinv,
+                  MoeGroups mg) {
     decode_body<MT, SC, F16, MOE, false, XP>(nullptr, xinv, &tm_codes, &tm_x, scales, e8m0, y, m, n, kblocks, groups,
-                                             splits, ntiles, e8m0_vec, row_stride, ids, topk, num_experts);
+                                             splits, ntiles, e8m0_vec, row_stride, ids, topk, num_experts, mg);
 }
 
 // A batch of independent GEMVs with the same m in one persistent launch
@@ -855,7 +896,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t stream, const float *xinv
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, a.e8m0,
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m),
                               static_cast<int>(a.n), kblocks, groups, splits, ntiles, e8m0_vec, a.row_stride,
-                              static_cast<const int32_t *>(nullptr), 0, 0, xinv);
+                              static_cast<const int32_t *>(nullptr), 0, 0, xinv, MoeGroups{nullptr, nullptr, nullptr});
 }
 
 // A batch launch: one persistent grid over the row tiles of all the ops
@@ -987,8 +1028,10 @@ cudaError_t launch_moe_t(const DecodeArgs &a, const MoeArgs &g, cudaStream_t str
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, static_cast<const uint8_t *>(nullptr),
                               static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(a.m), static_cast<int>(a.n),
                               kblocks, 0, splits, ntiles, 0, 0, g.ids, static_cast<int>(g.topk),
-                              static_cast<int>(g.num_experts), static_cast<const float *>(nullptr));
+                              static_cast<int>(g.num_experts), static_cast<const float *>(nullptr),
+                              MoeGroups{nullptr, nullptr, nullptr});
 }
+
 
 template <int SC>
 cudaError_t launch_sc(const DecodeArgs &a, cudaStream_t stream) {
@@ -1025,6 +1068,75 @@ cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_
         case 4: return launch_moe_t<4, false>(a, g, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// Grouped MoE by the routing's expert tiles (m > 32 with few pairs per
+// expert): the same kernel at 32 x rows, grid (row tiles of one expert, K
+// splits, expert tiles); each expert's weight streams once per tile of up to
+// kMoeDecodeTile of its pairs, whose x rows the routing copied in pair order.
+cudaError_t launch_moe_grouped(const DecodeArgs &a, const MoeArgs &g, const MoeRoute &r, cudaStream_t stream) {
+    constexpr int MT = kMoeDecodeTile / 8;
+    using C = Cfg<MT, false, false>;
+    static_assert(C::kXRows == kMoeDecodeTile, "one expert tile is the kernel's staged x rows");
+    constexpr int kBN = C::kBN;
+    auto kern = decode_kernel<MT, kScaleBlock, false, true>;
+    static Setup setup;
+    int resident = 1;
+    {
+        const cudaError_t e =
+            setup_once(setup, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes, resident);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t pairs = a.m * g.topk;
+    const int64_t tbound = (pairs + kMoeDecodeTile - 1) / kMoeDecodeTile + (g.num_experts < pairs ? g.num_experts : pairs);
+    if (tbound > 65535) return cudaErrorNotSupported;
+    CUtensorMap tm_codes, tm_x;
+    const uint64_t rows = static_cast<uint64_t>(g.num_experts) * static_cast<uint64_t>(a.n);
+    const uint64_t k = static_cast<uint64_t>(a.k);
+    if (!encode_tensor_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, k, rows, k, kKB, kBN,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r.xs, k, static_cast<uint64_t>(pairs), k * 2,
+                              64, C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
+    const int ntiles = static_cast<int>((a.n + kBN - 1) / kBN);
+    // size the K split for the expert tiles the routing is expected to make
+    // (one per selected expert and 32 pairs), not for the bound
+    const int64_t expect64 = (pairs + kMoeDecodeTile - 1) / kMoeDecodeTile;
+    const int expect = static_cast<int>(expect64 < g.num_experts ? g.num_experts : expect64);
+    const int capacity = device_sm_count() * resident;
+    int splits = 1;
+    if (static_cast<int64_t>(ntiles) * expect < capacity) {
+        int cap = capacity / (ntiles * expect);
+        if (cap > kMaxSplit) cap = kMaxSplit;
+        if (cap > kblocks) cap = kblocks;
+        splits = pick_split(setup.fit, reinterpret_cast<const void *>(kern), C::kThreads, C::kSmemBytes,
+                            ntiles * expect, cap);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ntiles), static_cast<unsigned>(splits), static_cast<unsigned>(tbound));
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (splits > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = static_cast<unsigned>(splits);
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, static_cast<const uint8_t *>(nullptr),
+                              static_cast<__nv_bfloat16 *>(a.y), kMoeDecodeTile, static_cast<int>(a.n), kblocks, 0,
+                              splits, ntiles, 0, 0, static_cast<const int32_t *>(nullptr), static_cast<int>(g.topk),
+                              static_cast<int>(g.num_experts), static_cast<const float *>(nullptr),
+                              MoeGroups{r.tile_off_dec, r.tok_off, r.perm});
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {

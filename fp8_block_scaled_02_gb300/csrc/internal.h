@@ -83,11 +83,14 @@ cudaError_t launch_encode_probe(uint32_t first, int64_t count, uint8_t *codes, c
 // moe.cu -- the routing of the grouped MoE GEMM: the (token, slot) pairs of
 // ids [pairs] grouped by expert and their x rows copied in that order, built
 // on the device in a caller workspace of moe_route_bytes(pairs, E, k) bytes.
+// Pairs per expert tile of the grouped decode path (the decode kernel's x rows).
+constexpr int kMoeDecodeTile = 32;
 struct MoeRoute {
     int32_t *counts;    // [E] pairs per expert
     int32_t *cursor;    // [E] scatter cursors
     int32_t *tok_off;   // [E + 1] first pair of each expert in perm
-    int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert
+    int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert (tensor-core GEMM)
+    int32_t *tile_off_dec;  // [E + 1] first kMoeDecodeTile-pair tile of each expert (decode path)
     int32_t *perm;      // [pairs] t * topk + j, expert by expert
     void *xs;           // bf16 [pairs, k]: x[perm[q] / topk] in perm's order
 };
@@ -96,6 +99,9 @@ MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts);
 cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64_t pairs, int topk,
                              int num_experts, const MoeRoute &r, cudaStream_t stream);
 uint32_t take_moe_error();
+// decode.cu: the grouped MoE GEMV by the routing's kMoeDecodeTile-pair expert
+// tiles (x rows from r.xs); cudaErrorNotSupported past the grid's bound.
+cudaError_t launch_moe_grouped(const DecodeArgs &a, const MoeArgs &g, const MoeRoute &r, cudaStream_t stream);
 
 // generic.cu -- plain-load kernels for any shape / alignment.
 cudaError_t launch_generic_gemv(const DecodeArgs &a, cudaStream_t stream);

@@ -9,6 +9,8 @@
 //   tok_off[e]   exclusive prefix sum of counts (tok_off[E] = valid pairs)
 //   tile_off[e]  exclusive prefix sum of ceil(counts / 256): the first of
 //                expert e's 256-pair tiles (tile_off[E] = tiles in all)
+//   tile_off_dec[e]  the same for tiles of kMoeDecodeTile pairs (the
+//                decode path for few pairs per expert)
 //   perm[...]    pair indices p = t * topk + j, expert by expert
 //                (tok_off[e] .. tok_off[e + 1]); within an expert in no
 //                particular order -- every pair's output is computed on its
@@ -42,36 +44,42 @@ __global__ void moe_count_kernel(const int32_t *__restrict__ ids, int64_t pairs,
     }
 }
 
-// Exclusive prefix sums of counts and of their 256-pair tile counts; the
-// scatter cursors start at zero.
+// Exclusive prefix sums of counts and of their tile counts (256 pairs and
+// kMoeDecodeTile pairs); the scatter cursors start at zero.
 __global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *__restrict__ counts,
                                                                 int num_experts, int32_t *__restrict__ tok_off,
                                                                 int32_t *__restrict__ tile_off,
+                                                                int32_t *__restrict__ tile_off_dec,
                                                                 int32_t *__restrict__ cursor) {
-    __shared__ int32_t s_tok[kScanThreads], s_tile[kScanThreads];
+    __shared__ int32_t s_tok[kScanThreads], s_tile[kScanThreads], s_dec[kScanThreads];
     pdl_launch_dependents();
     pdl_wait();
     const int e = threadIdx.x;
     const int32_t c = e < num_experts ? counts[e] : 0;
     s_tok[e] = c;
     s_tile[e] = (c + 255) >> 8;
+    s_dec[e] = (c + kMoeDecodeTile - 1) / kMoeDecodeTile;
     __syncthreads();
     // Hillis-Steele inclusive scan over the block
     for (int o = 1; o < kScanThreads; o <<= 1) {
-        const int32_t a = e >= o ? s_tok[e - o] : 0, b = e >= o ? s_tile[e - o] : 0;
+        const int32_t a = e >= o ? s_tok[e - o] : 0, b = e >= o ? s_tile[e - o] : 0,
+                      d = e >= o ? s_dec[e - o] : 0;
         __syncthreads();
         s_tok[e] += a;
         s_tile[e] += b;
+        s_dec[e] += d;
         __syncthreads();
     }
     if (e < num_experts) {
         tok_off[e + 1] = s_tok[e];
         tile_off[e + 1] = s_tile[e];
+        tile_off_dec[e + 1] = s_dec[e];
         cursor[e] = 0;
     }
     if (e == 0) {
         tok_off[0] = 0;
         tile_off[0] = 0;
+        tile_off_dec[0] = 0;
     }
 }
 
@@ -124,7 +132,7 @@ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
 }  // namespace
 
 int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k) {
-    return 2 * align256(4 * num_experts) + 2 * align256(4 * (num_experts + 1)) + align256(4 * pairs) +
+    return 2 * align256(4 * num_experts) + 3 * align256(4 * (num_experts + 1)) + align256(4 * pairs) +
            align256(2 * pairs * k);
 }
 
@@ -138,6 +146,8 @@ MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts) {
     r.tok_off = reinterpret_cast<int32_t *>(p);
     p += align256(4 * (num_experts + 1));
     r.tile_off = reinterpret_cast<int32_t *>(p);
+    p += align256(4 * (num_experts + 1));
+    r.tile_off_dec = reinterpret_cast<int32_t *>(p);
     p += align256(4 * (num_experts + 1));
     r.perm = reinterpret_cast<int32_t *>(p);
     p += align256(4 * pairs);
@@ -154,7 +164,7 @@ cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64
         e = launch_pdl(moe_count_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts, r.counts);
     if (e == cudaSuccess)
         e = launch_pdl(moe_scan_kernel, dim3(1), dim3(kScanThreads), stream, static_cast<const int32_t *>(r.counts),
-                       num_experts, r.tok_off, r.tile_off, r.cursor);
+                       num_experts, r.tok_off, r.tile_off, r.tile_off_dec, r.cursor);
     if (e == cudaSuccess)
         e = launch_pdl(moe_scatter_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts,
                        static_cast<const int32_t *>(r.tok_off), r.cursor, r.perm);

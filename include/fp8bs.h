@@ -365,15 +365,18 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids,
 
 /*
  * fp8bs_moe_gemv_ws -- fp8bs_moe_gemv with caller-provided device scratch,
- * which lets batches of m > 32 tokens run on the 5th-generation tensor
- * cores: four small kernels group the (token, slot) pairs by expert in the
- * workspace (counts, prefix sums, the pairs expert by expert, and a copy of
- * each pair's x row in that order), then one grouped GEMM multiplies each
- * selected expert's weight, decoded to bf16 in shared memory, with exactly
- * the x rows routed to it, in tiles of up to 256 pairs of one expert, and
- * writes each output row to its (token, slot).  Every selected expert's weight is
- * read once per tile of its pairs; fp8bs_moe_gemv instead runs the decode
- * kernel per 32 tokens, reading every selected expert once per 32 tokens.
+ * for batches of m > 32 tokens: four small kernels group the (token, slot)
+ * pairs by expert in the workspace (counts, prefix sums, the pairs expert by
+ * expert, and a copy of each pair's x row in that order), then each selected
+ * expert's weight is multiplied with exactly the x rows routed to it and
+ * each output row written to its (token, slot).  With at most 32 pairs per
+ * expert on average (m * topk <= 32 * num_experts) the decode kernel streams
+ * each expert once per tile of up to 32 of its pairs; otherwise one grouped
+ * GEMM on the 5th-generation tensor cores (the weight decoded to bf16 in
+ * shared memory) runs tiles of up to 256 pairs of one expert.  Every
+ * selected expert's weight is read once per tile of its pairs;
+ * fp8bs_moe_gemv instead runs the decode kernel per 32 tokens, reading
+ * every selected expert once per 32 tokens.
  * Same definition, arguments and tolerance as fp8bs_moe_gemv; m <= 32
  * takes fp8bs_moe_gemv's decode path and ignores the workspace.  In the
  * grouped path a token that lists an expert twice has both slots computed.

@@ -262,6 +262,37 @@ def test_moe_grouped_pair_counts_across_box_and_mma_edges(pkg):
     assert pkg.check_device_error() == 0
 
 
+def test_moe_grouped_decode_tile_edges(pkg):
+    """Few pairs per expert on average (pairs <= 32 * E): the call streams each
+    selected expert once per tile of up to 32 of its pairs through the decode
+    kernel.  Counts on both sides of the 32- and 64-pair tile edges, plus
+    experts nobody picked; every output checked in full."""
+    counts = [1, 31, 32, 33, 63, 64, 65, 0, 5, 96, 97] + [0] * 29
+    E, n, k = len(counts), 256, 512
+    assert sum(counts) <= 32 * E
+    codes, scales = experts(E, n, k, 43)
+    ids = np.repeat(np.arange(E, dtype=np.int32), counts)
+    np.random.default_rng(9).shuffle(ids)
+    ids = ids[:, None]
+    m = ids.shape[0]
+    x = inputs.activations(m, k, 14)
+    y, raw = guarded_empty((m, 1, n), torch.bfloat16, DEV)
+    pkg.moe_gemv_ws(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                    torch.from_numpy(scales).to(DEV), ws(pkg, m, 1, E, k), y=y)
+    torch.cuda.synchronize()
+    assert guard_intact(raw, m * n * 2)
+    yb, xb = bits(y.cpu()), bits(x)
+    for e in range(E):
+        toks = np.nonzero(ids[:, 0] == e)[0]
+        if not len(toks):
+            continue
+        y64 = oracle.block_gemv(xb[toks], codes[e], scales[e])
+        wmax = tolerance.block_wmax_rows(codes[e], scales[e], np.arange(n), table())
+        st = tolerance.gemv_errors(yb[toks, 0], y64, xb[toks], wmax)
+        assert tolerance.gemv_ok(st), (e, counts[e], st)
+    assert pkg.check_device_error() == 0
+
+
 def test_moe_grouped_out_of_range_id(pkg):
     E, n, k, m, topk = 8, 256, 256, 40, 2
     codes, scales = experts(E, n, k, 5)
@@ -288,7 +319,7 @@ def test_moe_grouped_out_of_range_id(pkg):
         assert tolerance.gemv_ok(st), (t, j, st)
 
 
-@pytest.mark.parametrize("m", [64, 512])
+@pytest.mark.parametrize("m", [64, 512, 2048])
 def test_moe_grouped_full_size_sampled(pkg, m):
     """256 experts of [2048, 4096], top-12: the sampled experts' codes and
     scales come from the oracle; every (token, slot) routed to one of them is
