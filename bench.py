@@ -332,6 +332,16 @@ def mx_workload(torch, fp8bs, inputs, dev):
     return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,1,true>", [0, 1]), launches_per_call=4)
 
 
+def prefill_launches(torch, m, n, k):
+    """Kernel launches of one tcgen05 W8A16 prefill call (prefill.cu's split
+    of the last wave): one launch of the full waves, plus one of the last
+    wave's tiles split over K when that wave fills at most half the SMs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-n // 128) * -(-m // 256)
+    rem = tiles % sms
+    return 2 if rem > 0 and 2 * rem <= sms and -(-k // 128) >= 2 else 1
+
+
 def prefill_workload(torch, fp8bs, inputs, dev, scales="block"):
     ms = [512, 2048, 4096]
     quant, gemv = quantizer(fp8bs, scales)
@@ -346,7 +356,8 @@ def prefill_workload(torch, fp8bs, inputs, dev, scales="block"):
     cfg = {"workload": f"prefill: {kind} [12288,4096] W8A16 GEMM on tcgen05, M=512,2048,4096", "n": n, "k": k,
            "ms": ms, "l2": "weight (50 MB) and x fit in L2; compute-bound"}
     dom = "prefill_kernel<0>" if scales == "block" else "prefill_kernel<2>"
-    return dict(calls=calls, cfg=cfg, dominant=(dom, [0, 1, 2]), flops=True)
+    return dict(calls=calls, cfg=cfg, dominant=(dom, [0, 1, 2]), flops=True,
+                call_launches=[prefill_launches(torch, m, n, k) for m in ms])
 
 
 def mx_prefill_workload(torch, fp8bs, inputs, dev):
@@ -364,7 +375,8 @@ def mx_prefill_workload(torch, fp8bs, inputs, dev):
         calls.append((f"M={m}", m, 2 * m * n * k, (lambda x=x, y=y: fp8bs.mx_gemv(x, codes, e8m0, y=y))))
     cfg = {"workload": "prefill: MXFP8 [18432,7168] W8A16 GEMM on tcgen05, M=512,2048,4096", "n": n, "k": k,
            "ms": ms, "l2": "weight (132 MB) about the size of L2; compute-bound"}
-    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel<1>", [0, 1, 2]), flops=True)
+    return dict(calls=calls, cfg=cfg, dominant=("prefill_kernel<1>", [0, 1, 2]), flops=True,
+                call_launches=[prefill_launches(torch, m, n, k) for m in ms])
 
 
 def rowwise_workload(torch, fp8bs, inputs, dev):
