@@ -364,18 +364,17 @@ int fp8bs_moe_gemv_ws(const void *x_bf16, int64_t m, const int32_t *expert_ids, 
     if (!workspace) return FP8BS_ERR_NULL;
     if (!aligned(workspace, 256)) return FP8BS_ERR_ALIGN;
     if (workspace_bytes < moe_route_bytes(m * topk, num_experts, k)) return FP8BS_ERR_SHAPE;
-    const MoeRoute r = moe_route_views(workspace, m * topk, num_experts);
+    const MoeRoute r = moe_route_views(workspace, m * topk, num_experts, k);
+    // few pairs per expert on average: stream each selected expert once per
+    // tile of 32 of its pairs at GEMV speed (x copied as f16 operands); more:
+    // the tensor-core GEMM (x copied as bf16)
+    const bool decode_tiles = m * topk <= kMoeDecodeTile * num_experts;
     cudaError_t e = launch_moe_route(x_bf16, k, expert_ids, m * topk, static_cast<int>(topk),
-                                     static_cast<int>(num_experts), r, st);
+                                     static_cast<int>(num_experts), r, decode_tiles, st);
     if (e != cudaSuccess) return FP8BS_ERR_CUDA;
     const DecodeArgs a{x_bf16, codes, scales, nullptr, y_bf16, m, n, k, kScaleBlock, 0};
     const MoeArgs g{expert_ids, topk, num_experts};
-    // few pairs per expert on average: stream each selected expert once per
-    // tile of 32 of its pairs at GEMV speed; more: the tensor-core GEMM
-    if (m * topk <= kMoeDecodeTile * num_experts) {
-        e = launch_moe_grouped(a, g, r, st);
-        if (e != cudaErrorNotSupported) return cuda_status(e);
-    }
+    if (decode_tiles) return cuda_status(launch_moe_grouped(a, g, r, st));
     e = launch_prefill_moe(a, g, r, st);
     if (e == cudaErrorNotSupported)
         return moe_decode_chunks(x_bf16, m, expert_ids, topk, codes, scales, num_experts, n, k, y_bf16, st);

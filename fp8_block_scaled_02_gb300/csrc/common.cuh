@@ -274,6 +274,25 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) {
     return __uint_as_float(packed & 0xFFFF0000u);
 }
 
+// Exponent e of the power of two 2^e that moves a bf16 magnitude (given as
+// its bits, m16 = |max| of a group of x values) into [2^14, 2^15): every
+// bf16 value of the group down to 2^-31 of that maximum then converts to f16
+// exactly, and nothing overflows.  Clamped to [-126, 126] so that 2^e and
+// 2^-e are both normal fp32; m16 == 0 gives 0.
+__device__ __forceinline__ int f16_rescale_exp(uint32_t m16) {
+    if (m16 == 0) return 0;
+    const int field = static_cast<int>(m16 >> 7);
+    const int lg = field ? field - 127 : -133;  // floor(log2 |max|) (subnormal: below -126)
+    return min(126, max(-126, 14 - lg));
+}
+__device__ __forceinline__ float pow2_int(int e) { return __uint_as_float(static_cast<uint32_t>(127 + e) << 23); }
+
+// Position of x row r of a 32-row x tile in the table of its per-row f16
+// inverse factors: rows 8j+t and 8j+t+4 sit next to each other, so a GEMV
+// consumer thread (which owns exactly those two rows of each 8-row group)
+// reads both with one 64-bit load.
+__device__ __forceinline__ int xinv_slot(int r) { return (r & ~7) | ((r & 3) << 1) | ((r >> 2) & 1); }
+
 // Encode 8 bf16 values (one uint4) divided by s into 8 e4m3 bytes (uint2).
 __device__ __forceinline__ uint2 encode8_div(const uint4 v, float s) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};

@@ -138,11 +138,6 @@ __device__ __forceinline__ float pow2_e8m0(uint32_t E) {
     return E ? __uint_as_float(E << 23) : __uint_as_float(0x00400000u);
 }
 
-// Position of x row r in the per-slice inverse-scale table: rows 8j+t and
-// 8j+t+4 sit next to each other, so a consumer thread reads both with one
-// 64-bit load.
-__device__ __forceinline__ int xinv_slot(int r) { return (r & ~7) | ((r & 3) << 1) | ((r >> 2) & 1); }
-
 // Rewrite one (x row r, 32-column slice sl) of a staged x tile from bf16 to
 // f16 in place with the exact power-of-two rescale described above.
 // kBlock: one power of two for the row's whole 128-column K block (the four
@@ -169,14 +164,9 @@ __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r,
         m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, 1));
         m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, 2));
     }
-    int k = 0;                                          // scale 2^k
-    if (m16 != 0) {
-        const int field = static_cast<int>(m16 >> 7);
-        const int e = field ? field - 127 : -133;       // floor(log2 |max|) (subnormal: below -126)
-        k = min(126, max(-126, 14 - e));
-    }
-    const float mult = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
-    const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+    const int k = f16_rescale_exp(m16);                 // scale 2^k
+    const float mult = pow2_int(k);
+    const float inv = pow2_int(-k);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         uint4 o;
@@ -229,7 +219,8 @@ struct OpRef {
 // codes / scales hold num_experts such weights back to back, ids [m, topk].
 // With mg.tile_off set, blockIdx.z is an expert tile of the routing instead
 // (x: the pair-order copy, its rows from the tile's first pair; output row i
-// goes to y[pair_i * n + row], y: [tokens, topk, n]).
+// goes to y[pair_i * n + row], y: [tokens, topk, n]); with XP the copy is
+// f16 and xinv_g holds each tile's inverse factors, [tile][kblocks][32]).
 // BATCH: the ops come from `bp` (the single-weight arguments are unused).
 template <int MT, int SC, bool F16, bool MOE, bool BATCH, bool XP = false>
 __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *__restrict__ xinv_g,
@@ -247,7 +238,9 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     // ... and with bf16 operands and one scale per row, all of K
     constexpr bool kDirect = kWholeBlock && ROW && !F16;
     static_assert(!(MOE && BATCH), "a grouped MoE call is one launch of its own");
-    static_assert(!XP || (F16 && !MX && !MOE), "prepared x feeds the block-scaled f16 path");
+    // prepared x feeds the block-scaled f16 path (MOE: the routing's decode
+    // tiles, whose factors are per tile)
+    static_assert(!XP || (F16 && !MX), "prepared x feeds the block-scaled f16 path");
     using C = Cfg<MT, MX, F16, XP>;
     constexpr int kStages = C::kStages;
     constexpr int kBN = C::kBN;
@@ -343,6 +336,11 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     int expert = 0;
     int x_row0 = 0;  // MOE by tiles: the tile's first pair (row of the pair-order copy of x)
     const bool by_tiles = MOE && mg.tile_off != nullptr;
+    if (MOE && XP && !by_tiles) {
+        // prepared factors exist only per routing tile: nothing was issued yet
+        if (threadIdx.x == 0) atomicOr(&g_decode_err, ERRBIT_INDEX);
+        return;
+    }
     if (by_tiles) {
         // blockIdx.z is an expert tile; every CTA of a cluster shares it, so
         // an idle cluster leaves whole, before anything is issued
@@ -362,6 +360,7 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
         const int cnt = min(kMoeDecodeTile, __ldg(mg.tok_off + expert + 1) - p0);
         if (threadIdx.x < 32) s_pair[threadIdx.x] = threadIdx.x < cnt ? __ldg(mg.perm + p0 + threadIdx.x) : -1;
         x_row0 = p0;
+        if (XP) xinv_g += static_cast<int64_t>(tile) * kblocks * 32;  // this tile's factors
         __syncthreads();
     } else if (MOE) {
         for (int i = threadIdx.x; i < kMoeMaxExperts / 32; i += blockDim.x) s_bits[i] = 0;
@@ -779,13 +778,8 @@ __device__ __forceinline__ void xprep_warp(const uint16_t *__restrict__ x, int m
     uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);  // |max| as bf16 bits
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, o));
-    int e = 0;
-    if (m16 != 0) {
-        const int field = static_cast<int>(m16 >> 7);
-        const int lg = field ? field - 127 : -133;  // floor(log2 |max|) (subnormal: below -126)
-        e = min(126, max(-126, 14 - lg));
-    }
-    const float mult = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+    const int e = f16_rescale_exp(m16);
+    const float mult = pow2_int(e);
     if (in) {
         uint2 o;
         o.x = f32x2_to_f16x2(bf16lo_to_f32(v.x) * mult, bf16hi_to_f32(v.x) * mult);
@@ -793,7 +787,7 @@ __device__ __forceinline__ void xprep_warp(const uint16_t *__restrict__ x, int m
         *reinterpret_cast<uint2 *>(x16 + static_cast<int64_t>(r) * k + c) = o;
     }
     if (lane == 0)
-        inv[kb * 32 + xinv_slot(r)] = r < m ? __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 1.0f;
+        inv[kb * 32 + xinv_slot(r)] = r < m ? pow2_int(-e) : 1.0f;
 }
 
 __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t *__restrict__ x, int m, int mpad, int k,
@@ -1076,10 +1070,12 @@ cudaError_t launch_moe_decode(const DecodeArgs &a, const MoeArgs &g, cudaStream_
 // kMoeDecodeTile of its pairs, whose x rows the routing copied in pair order.
 cudaError_t launch_moe_grouped(const DecodeArgs &a, const MoeArgs &g, const MoeRoute &r, cudaStream_t stream) {
     constexpr int MT = kMoeDecodeTile / 8;
-    using C = Cfg<MT, false, false>;
+    using C = Cfg<MT, false, true, true>;
     static_assert(C::kXRows == kMoeDecodeTile, "one expert tile is the kernel's staged x rows");
     constexpr int kBN = C::kBN;
-    auto kern = decode_kernel<MT, kScaleBlock, false, true>;
+    // f16 operands: the routing wrote the x copy rescaled, with each tile's
+    // inverse factors (one cvt per code pair instead of a 4-op bf16 decode)
+    auto kern = decode_kernel<MT, kScaleBlock, true, true, true>;
     static Setup setup;
     int resident = 1;
     {
@@ -1088,14 +1084,14 @@ cudaError_t launch_moe_grouped(const DecodeArgs &a, const MoeArgs &g, const MoeR
         if (e != cudaSuccess) return e;
     }
     const int64_t pairs = a.m * g.topk;
-    const int64_t tbound = (pairs + kMoeDecodeTile - 1) / kMoeDecodeTile + (g.num_experts < pairs ? g.num_experts : pairs);
-    if (tbound > 65535) return cudaErrorNotSupported;
+    const int64_t tbound = moe_decode_tile_bound(pairs, g.num_experts);
+    if (tbound > 65535 || r.xinv == nullptr) return cudaErrorInvalidValue;
     CUtensorMap tm_codes, tm_x;
     const uint64_t rows = static_cast<uint64_t>(g.num_experts) * static_cast<uint64_t>(a.n);
     const uint64_t k = static_cast<uint64_t>(a.k);
     if (!encode_tensor_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, k, rows, k, kKB, kBN,
                               CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r.xs, k, static_cast<uint64_t>(pairs), k * 2,
+        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, r.xs, k, static_cast<uint64_t>(pairs), k * 2,
                               64, C::kXRows, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
@@ -1135,7 +1131,7 @@ cudaError_t launch_moe_grouped(const DecodeArgs &a, const MoeArgs &g, const MoeR
     return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_x, a.scales, static_cast<const uint8_t *>(nullptr),
                               static_cast<__nv_bfloat16 *>(a.y), kMoeDecodeTile, static_cast<int>(a.n), kblocks, 0,
                               splits, ntiles, 0, 0, static_cast<const int32_t *>(nullptr), static_cast<int>(g.topk),
-                              static_cast<int>(g.num_experts), static_cast<const float *>(nullptr),
+                              static_cast<int>(g.num_experts), static_cast<const float *>(r.xinv),
                               MoeGroups{r.tile_off_dec, r.tok_off, r.perm});
 }
 

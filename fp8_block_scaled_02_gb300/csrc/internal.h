@@ -92,15 +92,24 @@ struct MoeRoute {
     int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert (tensor-core GEMM)
     int32_t *tile_off_dec;  // [E + 1] first kMoeDecodeTile-pair tile of each expert (decode path)
     int32_t *perm;      // [pairs] t * topk + j, expert by expert
-    void *xs;           // bf16 [pairs, k]: x[perm[q] / topk] in perm's order
+    float *xinv;        // decode tiles: [tile bound][kblocks][32] f16 inverse factors, slot order
+    void *xs;           // [pairs, k]: x[perm[q] / topk] in perm's order; bf16 for the
+                        // tensor-core GEMM, f16 rescaled per (row, K block) for decode tiles
 };
+// Upper bound on the kMoeDecodeTile-pair tiles of `pairs` routed pairs:
+// one partial tile per expert at most, besides the full ones.
+inline int64_t moe_decode_tile_bound(int64_t pairs, int64_t num_experts) {
+    return (pairs + kMoeDecodeTile - 1) / kMoeDecodeTile + (num_experts < pairs ? num_experts : pairs);
+}
 int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k);
-MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts);
+MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, int64_t k);
+// decode_tiles: write xs as f16 with the per-(row, K block) inverse factors
+// of each decode tile in xinv (the decode kernel's operands); else bf16.
 cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64_t pairs, int topk,
-                             int num_experts, const MoeRoute &r, cudaStream_t stream);
+                             int num_experts, const MoeRoute &r, bool decode_tiles, cudaStream_t stream);
 uint32_t take_moe_error();
 // decode.cu: the grouped MoE GEMV by the routing's kMoeDecodeTile-pair expert
-// tiles (x rows from r.xs); cudaErrorNotSupported past the grid's bound.
+// tiles (f16 x rows from r.xs, routed with decode_tiles set).
 cudaError_t launch_moe_grouped(const DecodeArgs &a, const MoeArgs &g, const MoeRoute &r, cudaStream_t stream);
 
 // generic.cu -- plain-load kernels for any shape / alignment.

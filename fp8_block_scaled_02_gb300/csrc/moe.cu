@@ -17,7 +17,10 @@
 //                own, so the order changes no result.
 //   xs[q, :]     x[perm[q] / topk, :]: the x rows in the same order, so that
 //                each expert's rows are contiguous and the GEMM loads them
-//                as ordinary TMA tiles.
+//                as ordinary TMA tiles.  For the decode tiles the copy is
+//                written as f16, rescaled per (row, 128-column K block) by a
+//                power of two, with the inverse factors of each tile in xinv
+//                (the operands of the decode kernel's f16 MMAs).
 // An id outside [0, E) routes nowhere and sets the error bit ERRBIT_INDEX.
 #include "common.cuh"
 #include "internal.h"
@@ -100,6 +103,81 @@ __global__ void moe_gather_kernel(const uint4 *__restrict__ x, int64_t pairs, in
     for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
 }
 
+// The decode-tile form of the gather.  Decode tile `tile` of expert e holds
+// pairs p0 .. p0 + cnt - 1 (p0 = tok_off[e] + kMoeDecodeTile * (tile -
+// tile_off_dec[e])); its row r < cnt becomes xs[p0 + r, :] =
+// x[perm[p0 + r] / topk, :] * 2^s per 128-column K block kb, s =
+// f16_rescale_exp(the largest |x| of that row and block), stored as f16, and
+// xinv[(tile * kblocks + kb) * 32 + xinv_slot(r)] = 2^-s.  Rows r >= cnt
+// (the next expert's pairs, whose outputs this tile never stores) read as
+// zero here and get factor 1.  Block (tile, chunk of kGatherKb K blocks);
+// warp w takes rows w, w + 8, w + 16, w + 24, all its loads in flight
+// before the first reduction.  k % 4 == 0 (a lane's 4 columns are all in or
+// all out).
+constexpr int kGatherKb = 4;
+__global__ void __launch_bounds__(256) moe_gather_f16_kernel(const uint2 *__restrict__ x, int topk, int k,
+                                                             int kblocks, const int32_t *__restrict__ tok_off,
+                                                             const int32_t *__restrict__ tile_off_dec,
+                                                             int num_experts, const int32_t *__restrict__ perm,
+                                                             uint2 *__restrict__ xs, float *__restrict__ xinv) {
+    static_assert(kMoeDecodeTile == 32, "a block covers the 32 rows of one decode tile");
+    __shared__ int s_p0, s_cnt;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tile = static_cast<int>(blockIdx.x);
+    if (tile >= tile_off_dec[num_experts]) return;
+    if (threadIdx.x == 0) {
+        int lo = 0, hi = num_experts - 1;  // largest e with tile_off_dec[e] <= tile
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tile_off_dec[mid] <= tile) lo = mid; else hi = mid - 1;
+        }
+        const int p0 = tok_off[lo] + (tile - tile_off_dec[lo]) * kMoeDecodeTile;
+        s_p0 = p0;
+        s_cnt = min(kMoeDecodeTile, tok_off[lo + 1] - p0);
+    }
+    __syncthreads();
+    const int p0 = s_p0, cnt = s_cnt;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kbase = static_cast<int>(blockIdx.y) * kGatherKb;
+    const int q4 = k >> 2;  // 4-value (8-byte) groups per row
+    int64_t src[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = warp + 8 * i;
+        src[i] = r < cnt ? static_cast<int64_t>(perm[p0 + r] / topk) : -1;
+    }
+    uint2 v[4][kGatherKb];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < kGatherKb; ++j) {
+            const int c = (kbase + j) * 32 + lane;
+            v[i][j] = (src[i] >= 0 && c < q4) ? __ldg(x + src[i] * q4 + c) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < kGatherKb; ++j) {
+            const int r = warp + 8 * i, kb = kbase + j;
+            if (kb >= kblocks) continue;  // uniform across the block
+            const uint32_t mx = max_u16x2(v[i][j].x & 0x7FFF7FFFu, v[i][j].y & 0x7FFF7FFFu);
+            uint32_t m16 = max(mx & 0xFFFFu, mx >> 16);  // |max| as bf16 bits
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, o));
+            const int e = f16_rescale_exp(m16);
+            const float mult = pow2_int(e);
+            const int c = kb * 32 + lane;
+            if (r < cnt && c < q4) {
+                uint2 o;
+                o.x = f32x2_to_f16x2(bf16lo_to_f32(v[i][j].x) * mult, bf16hi_to_f32(v[i][j].x) * mult);
+                o.y = f32x2_to_f16x2(bf16lo_to_f32(v[i][j].y) * mult, bf16hi_to_f32(v[i][j].y) * mult);
+                xs[static_cast<int64_t>(p0 + r) * q4 + c] = o;
+            }
+            if (lane == 0) xinv[(static_cast<int64_t>(tile) * kblocks + kb) * 32 + xinv_slot(r)] = pow2_int(-e);
+        }
+}
+
 __global__ void moe_scatter_kernel(const int32_t *__restrict__ ids, int64_t pairs, int num_experts,
                                    const int32_t *__restrict__ tok_off, int32_t *__restrict__ cursor,
                                    int32_t *__restrict__ perm) {
@@ -132,11 +210,12 @@ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
 }  // namespace
 
 int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k) {
+    const int64_t kblocks = (k + 127) / 128;
     return 2 * align256(4 * num_experts) + 3 * align256(4 * (num_experts + 1)) + align256(4 * pairs) +
-           align256(2 * pairs * k);
+           align256(4 * moe_decode_tile_bound(pairs, num_experts) * kblocks * 32) + align256(2 * pairs * k);
 }
 
-MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts) {
+MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, int64_t k) {
     char *p = static_cast<char *>(workspace);
     MoeRoute r;
     r.counts = reinterpret_cast<int32_t *>(p);
@@ -151,12 +230,14 @@ MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts) {
     p += align256(4 * (num_experts + 1));
     r.perm = reinterpret_cast<int32_t *>(p);
     p += align256(4 * pairs);
+    r.xinv = reinterpret_cast<float *>(p);
+    p += align256(4 * moe_decode_tile_bound(pairs, num_experts) * ((k + 127) / 128) * 32);
     r.xs = p;
     return r;
 }
 
 cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64_t pairs, int topk,
-                             int num_experts, const MoeRoute &r, cudaStream_t stream) {
+                             int num_experts, const MoeRoute &r, bool decode_tiles, cudaStream_t stream) {
     if (num_experts < 1 || num_experts > kScanThreads || pairs < 1) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(r.counts, 0, 4 * static_cast<size_t>(num_experts), stream);
     const unsigned blocks = static_cast<unsigned>((pairs + 255) / 256 < 1024 ? (pairs + 255) / 256 : 1024);
@@ -168,6 +249,16 @@ cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64
     if (e == cudaSuccess)
         e = launch_pdl(moe_scatter_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts,
                        static_cast<const int32_t *>(r.tok_off), r.cursor, r.perm);
+    if (e == cudaSuccess && decode_tiles) {
+        const int64_t tbound = moe_decode_tile_bound(pairs, num_experts);
+        const int kblocks = static_cast<int>((k + 127) / 128);
+        if (tbound > 0x7FFFFFFF || k % 4 != 0) return cudaErrorInvalidValue;
+        return launch_pdl(moe_gather_f16_kernel,
+                          dim3(static_cast<unsigned>(tbound), static_cast<unsigned>((kblocks + kGatherKb - 1) / kGatherKb)),
+                          dim3(256), stream, static_cast<const uint2 *>(x), topk, static_cast<int>(k), kblocks,
+                          static_cast<const int32_t *>(r.tok_off), static_cast<const int32_t *>(r.tile_off_dec),
+                          num_experts, static_cast<const int32_t *>(r.perm), static_cast<uint2 *>(r.xs), r.xinv);
+    }
     if (e == cudaSuccess)
         e = launch_pdl(moe_gather_kernel, dim3(static_cast<unsigned>((pairs + 7) / 8)), dim3(256), stream,
                        static_cast<const uint4 *>(x), pairs, topk, static_cast<int>(k),

@@ -371,7 +371,10 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids,
  * expert's weight is multiplied with exactly the x rows routed to it and
  * each output row written to its (token, slot).  With at most 32 pairs per
  * expert on average (m * topk <= 32 * num_experts) the decode kernel streams
- * each expert once per tile of up to 32 of its pairs; otherwise one grouped
+ * each expert once per tile of up to 32 of its pairs, on an f16 copy of the
+ * x rows with one power-of-two factor per (row, 128-column K block), as
+ * fp8bs_gemv_ws prepares x (every x within 2^-31 of its block's largest
+ * |x| converts exactly; the codes enter the tensor cores as f16); otherwise one grouped
  * GEMM on the 5th-generation tensor cores (the weight decoded to bf16 in
  * shared memory) runs tiles of up to 256 pairs of one expert.  Every
  * selected expert's weight is read once per tile of its pairs;
@@ -387,8 +390,8 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids,
  *
  *   workspace        device, 256-byte aligned, >= fp8bs_moe_gemv_ws_bytes(m,
  *                    topk, num_experts, k) bytes (0 for m <= 32; about
- *                    2 * m * topk * k for the x copy); contents on entry do
- *                    not matter
+ *                    2 * m * topk * k for the x copy, plus the factors);
+ *                    contents on entry do not matter
  *   other arguments  as fp8bs_moe_gemv (m * topk < 2^31)
  * FP8BS_ERR_NULL / FP8BS_ERR_ALIGN / FP8BS_ERR_SHAPE for a missing,
  * misaligned or too small workspace, before anything is launched.
