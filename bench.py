@@ -467,12 +467,13 @@ def moe_workload(torch, fp8bs, inputs, dev):
     return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<1,0,true,true>", [0, 1]))
 
 
-def moe_prefill_workload(torch, fp8bs, inputs, dev):
+def moe_prefill_workload(torch, fp8bs, inputs, dev, experts=None):
     """Grouped MoE at prefill sizes: 256 block-FP8 experts of [2048, 4096],
     top-12 routing, M = 512 and 2048 tokens through fp8bs_moe_gemv_ws (the
     routing grouped on the device, one grouped tcgen05 GEMM).  Work per call:
-    2 * M * topk * N * K flops."""
-    E, (n, k), topk = inputs.MOE_EXPERTS, inputs.MOE_SHAPE, inputs.MOE_TOPK
+    2 * M * topk * N * K flops.  `experts`: fewer experts (a smaller case
+    with more pairs per expert, for profiling)."""
+    E, (n, k), topk = experts or inputs.MOE_EXPERTS, inputs.MOE_SHAPE, inputs.MOE_TOPK
     codes = torch.empty((E, n, k), dtype=torch.uint8, device=dev)
     scales = torch.empty((E, n // 128, k // 128), dtype=torch.float32, device=dev)
     for e in range(E):
@@ -492,11 +493,13 @@ def moe_prefill_workload(torch, fp8bs, inputs, dev):
         work = torch.empty((fp8bs.moe_gemv_ws_bytes(m, topk, E, k),), dtype=torch.uint8, device=dev)
         calls.append((f"M={m}", m, 2 * m * topk * n * k,
                       (lambda x=x, ids=ids, y=y, work=work: fp8bs.moe_gemv_ws(x, ids, codes, scales, work, y=y))))
-    cfg = {"workload": "grouped MoE prefill: 256 block-FP8 experts [2048,4096], top-12 routing, M=512,2048 "
-                       "(fp8bs_moe_gemv_ws: routing grouped on the device, then the decode kernel per 32-pair "
-                       "expert tile at M=512, one grouped tcgen05 GEMM at M=2048)",
+    path = lambda m: ("the decode kernel per 32-pair expert tile" if m * topk <= 32 * E
+                      else "one grouped tcgen05 GEMM")
+    cfg = {"workload": f"grouped MoE prefill: {E} block-FP8 experts [{n},{k}], top-{topk} routing, M=512,2048 "
+                       f"(fp8bs_moe_gemv_ws: routing grouped on the device, then {path(512)} at M=512, "
+                       f"{path(2048)} at M=2048)",
            "experts": E, "n": n, "k": k, "topk": topk, "ms": ms,
-           "l2": "inputs larger than L2 (2.1 GB of expert codes, nearly all selected)"}
+           "l2": f"inputs larger than L2 ({E * n * k / 1e9:.1f} GB of expert codes, nearly all selected)"}
     # M=512 (24 pairs per expert on average) takes the grouped decode path,
     # M=2048 (96) the tensor-core grouped GEMM
     return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<4,0,true,true,true> + prefill_kernel<0,true>", [0, 1]),
@@ -921,6 +924,8 @@ def main():
                              "w8a8_prefill", "moe", "kv"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--layers", type=int, default=None, help="rotation: fewer layers than 48 (a smaller case)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="moe_prefill: fewer experts than 256 (a smaller case)")
     ap.add_argument("--single", action="store_true", help="rotation: one GEMV call per weight, not one batch")
     ap.add_argument("--ws", action="store_true", help="sweep: call fp8bs_gemv_ws (x prepared in a workspace)")
     ap.add_argument("--scales", default="block", choices=["block", "row", "tensor"])
@@ -988,7 +993,7 @@ def main():
     elif args.workload == "moe":
         wl = moe_workload(torch, fp8bs, inputs, dev)
     elif args.workload == "moe_prefill":
-        wl = moe_prefill_workload(torch, fp8bs, inputs, dev)
+        wl = moe_prefill_workload(torch, fp8bs, inputs, dev, experts=args.experts)
     elif args.workload == "kv":
         wl = kv_workload(torch, fp8bs, inputs, dev)
     else:

@@ -293,6 +293,61 @@ def test_moe_grouped_decode_tile_edges(pkg):
     assert pkg.check_device_error() == 0
 
 
+@pytest.mark.parametrize("case", ["wide_range", "blockwise", "tiny", "huge", "single_spike"])
+def test_moe_grouped_decode_tiles_x_dynamic_range(pkg, case):
+    """The decode tiles read an f16 copy of the routed x rows with one power
+    of two per (row, 128-column K block) and tile-local factors: activations
+    spanning 60 decades, magnitudes that jump by up to 2^80 from one K block
+    to the next, all tiny, all huge, or one spike per row stay within
+    tolerance for every (token, slot)."""
+    E, n, k, m, topk = 8, 256, 1024, 64, 2
+    assert m * topk <= 32 * E
+    codes, scales = experts(E, n, k, 61)
+    ids = route(m, topk, E, 17)
+    g = torch.Generator().manual_seed(6)
+    base = torch.randn((m, k), generator=g)
+    if case == "wide_range":
+        x = base * torch.pow(10.0, torch.randint(-30, 30, (m, k), generator=g).to(torch.float32))
+    elif case == "blockwise":
+        expo = torch.randint(-40, 40, (m, k // 128), generator=g).to(torch.float32)
+        x = base * torch.pow(2.0, expo).repeat_interleave(128, dim=1)
+    elif case == "tiny":
+        x = base * 1e-35
+    elif case == "huge":
+        x = base * 1e30
+    else:
+        x = base.clone()
+        x[:, 37] = 3e20
+    x = x.to(torch.bfloat16)
+    y = pkg.moe_gemv_ws(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(codes).to(DEV),
+                        torch.from_numpy(scales).to(DEV), ws(pkg, m, topk, E, k))
+    torch.cuda.synchronize()
+    check_call(y, bits(x), ids, codes, scales)
+    assert pkg.check_device_error() == 0
+
+
+def check_call(y_dev, x_bits, ids, codes, scales):
+    """The GEMV tolerance with its relative-L2 statistic taken over all the
+    call's outputs (as the dense tests take it) and the element bound per
+    (token, slot): in the "tiny" case above, the correctly rounded bf16 of
+    the fp64 result of output row (40, 0) alone has relative L2 error
+    2.0035e-3, so a per-row statistic of 256 outputs would reject the exact
+    answer."""
+    m, topk = ids.shape
+    y64 = oracle.moe_gemv(x_bits, ids, codes, scales)
+    yb = bits(y_dev.cpu())
+    yf = tolerance.bf16_bits_to_f64(yb)
+    for t in range(m):
+        for j in range(topk):
+            e = ids[t, j]
+            s = np.repeat(scales[e].astype(np.float64), 128, axis=0)[:codes.shape[1]]
+            wmax = np.abs(table()[codes[e]] * np.repeat(s, 128, axis=1)[:, :codes.shape[2]]).max(axis=1)
+            st = tolerance.gemv_errors(yb[t, j][None, :], y64[t, j][None, :], x_bits[t][None, :], wmax)
+            assert st["finite"] and st["max_ratio"] <= 1.0, (t, j, st)
+    rel_l2 = float(np.linalg.norm(yf - y64) / np.linalg.norm(y64))
+    assert tolerance.gemv_ok({"finite": True, "max_ratio": 0.0, "rel_l2": rel_l2, "count": yf.size}), rel_l2
+
+
 def test_moe_grouped_out_of_range_id(pkg):
     E, n, k, m, topk = 8, 256, 256, 40, 2
     codes, scales = experts(E, n, k, 5)
