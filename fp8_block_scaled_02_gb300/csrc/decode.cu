@@ -198,7 +198,7 @@ __device__ __forceinline__ void convert_x_slice(uint8_t *xs, float *xinv, int r,
 // x rows were copied in pair order; tile_off nullptr: route by ids.
 struct MoeGroups {
     const int32_t *tile_off;  // [E + 1] first tile of each expert (tile_off[E]: the count)
-    const int32_t *tok_off;   // [E + 1] first pair of each expert
+    const int4 *tile_info;    // [tile bound] {expert, first pair, pairs, 0} of each tile
     const int32_t *perm;      // pair indices t * topk + j, expert by expert
 };
 
@@ -267,6 +267,7 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     __shared__ int s_expert;                          // MOE: this CTA's expert
     __shared__ signed char s_route[32];               // MOE: slot j of x row mi for it, -1 if none
     __shared__ int32_t s_pair[32];                    // MOE by tiles: pair of x row mi, -1 past the tile
+    __shared__ int s_x_row0;                          // MOE by tiles: the tile's first pair
 
     // Unit i of this CTA: its op (BATCH: `op` is a cursor that only moves
     // forward, units are visited in increasing order), first weight row and
@@ -345,23 +346,22 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
         // blockIdx.z is an expert tile; every CTA of a cluster shares it, so
         // an idle cluster leaves whole, before anything is issued
         const int tile = static_cast<int>(blockIdx.z);
+        // the tile count and the tile's record: two independent loads (the
+        // record is in bounds, the grid's bound; used only if tile < count)
+        int4 ti = make_int4(0, 0, 0, 0);
+        if (threadIdx.x < 32) ti = __ldg(mg.tile_info + tile);
         if (tile >= __ldg(mg.tile_off + num_experts)) return;
-        if (threadIdx.x == 0) {
-            int lo = 0, hi = num_experts - 1;  // largest e with tile_off[e] <= tile
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldg(mg.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
+        if (threadIdx.x < 32) {
+            s_pair[threadIdx.x] = threadIdx.x < ti.z ? __ldg(mg.perm + ti.y + threadIdx.x) : -1;
+            if (threadIdx.x == 0) {
+                s_expert = ti.x;
+                s_x_row0 = ti.y;
             }
-            s_expert = lo;
         }
         __syncthreads();
         expert = s_expert;
-        const int p0 = __ldg(mg.tok_off + expert) + (tile - __ldg(mg.tile_off + expert)) * kMoeDecodeTile;
-        const int cnt = min(kMoeDecodeTile, __ldg(mg.tok_off + expert + 1) - p0);
-        if (threadIdx.x < 32) s_pair[threadIdx.x] = threadIdx.x < cnt ? __ldg(mg.perm + p0 + threadIdx.x) : -1;
-        x_row0 = p0;
+        x_row0 = s_x_row0;
         if (XP) xinv_g += static_cast<int64_t>(tile) * kblocks * 32;  // this tile's factors
-        __syncthreads();
     } else if (MOE) {
         for (int i = threadIdx.x; i < kMoeMaxExperts / 32; i += blockDim.x) s_bits[i] = 0;
         __syncthreads();
@@ -1132,7 +1132,7 @@ cudaError_t launch_moe_grouped(const DecodeArgs &a, const MoeArgs &g, const MoeR
                               static_cast<__nv_bfloat16 *>(a.y), kMoeDecodeTile, static_cast<int>(a.n), kblocks, 0,
                               splits, ntiles, 0, 0, static_cast<const int32_t *>(nullptr), static_cast<int>(g.topk),
                               static_cast<int>(g.num_experts), static_cast<const float *>(r.xinv),
-                              MoeGroups{r.tile_off_dec, r.tok_off, r.perm});
+                              MoeGroups{r.tile_off_dec, r.tile_info_dec, r.perm});
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream) {

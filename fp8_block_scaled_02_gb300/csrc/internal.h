@@ -91,6 +91,8 @@ struct MoeRoute {
     int32_t *tok_off;   // [E + 1] first pair of each expert in perm
     int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert (tensor-core GEMM)
     int32_t *tile_off_dec;  // [E + 1] first kMoeDecodeTile-pair tile of each expert (decode path)
+    int4 *tile_info;        // [GEMM tile bound] {expert, first pair, pairs, 0} of each 256-pair tile
+    int4 *tile_info_dec;    // [decode tile bound] the same for the kMoeDecodeTile-pair tiles
     int32_t *perm;      // [pairs] t * topk + j, expert by expert
     float *xinv;        // decode tiles: [tile bound][kblocks][32] f16 inverse factors, slot order
     void *xs;           // [pairs, k]: x[perm[q] / topk] in perm's order; bf16 for the
@@ -100,6 +102,10 @@ struct MoeRoute {
 // one partial tile per expert at most, besides the full ones.
 inline int64_t moe_decode_tile_bound(int64_t pairs, int64_t num_experts) {
     return (pairs + kMoeDecodeTile - 1) / kMoeDecodeTile + (num_experts < pairs ? num_experts : pairs);
+}
+// ... and on the 256-pair tiles of the tensor-core grouped GEMM.
+inline int64_t moe_gemm_tile_bound(int64_t pairs, int64_t num_experts) {
+    return (pairs + 255) / 256 + (num_experts < pairs ? num_experts : pairs);
 }
 int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k);
 MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, int64_t k);

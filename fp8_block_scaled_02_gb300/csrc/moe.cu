@@ -11,6 +11,9 @@
 //                expert e's 256-pair tiles (tile_off[E] = tiles in all)
 //   tile_off_dec[e]  the same for tiles of kMoeDecodeTile pairs (the
 //                decode path for few pairs per expert)
+//   tile_info[t], tile_info_dec[t]  tile t of either kind as {expert,
+//                first pair, pairs, 0}, so that a CTA finds its tile with
+//                one load instead of a search over the offsets
 //   perm[...]    pair indices p = t * topk + j, expert by expert
 //                (tok_off[e] .. tok_off[e + 1]); within an expert in no
 //                particular order -- every pair's output is computed on its
@@ -47,12 +50,35 @@ __global__ void moe_count_kernel(const int32_t *__restrict__ ids, int64_t pairs,
     }
 }
 
+// Tiles of `size` pairs from the block's inclusive scans (s_tok: pairs,
+// s_t: tiles of each expert): record t = {expert, first pair, pairs, 0},
+// the expert found by a search in shared memory.
+template <int kSize>
+__device__ __forceinline__ void write_tiles(const int32_t *s_tok, const int32_t *s_t, int num_experts,
+                                            int4 *__restrict__ info) {
+    const int ntiles = s_t[num_experts - 1];
+    for (int t = threadIdx.x; t < ntiles; t += kScanThreads) {
+        int lo = 0, hi = num_experts - 1;  // first e whose tiles end past t
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_t[mid] > t) hi = mid; else lo = mid + 1;
+        }
+        const int32_t first_pair = lo ? s_tok[lo - 1] : 0;
+        const int32_t cnt = s_tok[lo] - first_pair;
+        const int32_t i = t - (s_t[lo] - (cnt + kSize - 1) / kSize);  // tile index within the expert
+        info[t] = make_int4(lo, first_pair + kSize * i, min(kSize, cnt - kSize * i), 0);
+    }
+}
+
 // Exclusive prefix sums of counts and of their tile counts (256 pairs and
-// kMoeDecodeTile pairs); the scatter cursors start at zero.
+// kMoeDecodeTile pairs), the tile records of both kinds; the scatter
+// cursors start at zero.
 __global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *__restrict__ counts,
                                                                 int num_experts, int32_t *__restrict__ tok_off,
                                                                 int32_t *__restrict__ tile_off,
                                                                 int32_t *__restrict__ tile_off_dec,
+                                                                int4 *__restrict__ tile_info,
+                                                                int4 *__restrict__ tile_info_dec,
                                                                 int32_t *__restrict__ cursor) {
     __shared__ int32_t s_tok[kScanThreads], s_tile[kScanThreads], s_dec[kScanThreads];
     pdl_launch_dependents();
@@ -84,6 +110,8 @@ __global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *_
         tile_off[0] = 0;
         tile_off_dec[0] = 0;
     }
+    write_tiles<256>(s_tok, s_tile, num_experts, tile_info);
+    write_tiles<kMoeDecodeTile>(s_tok, s_dec, num_experts, tile_info_dec);
 }
 
 // xs[q, :] = x[perm[q] / topk, :] for the routed pairs q < tok_off[E]; one
@@ -116,28 +144,18 @@ __global__ void moe_gather_kernel(const uint4 *__restrict__ x, int64_t pairs, in
 // all out).
 constexpr int kGatherKb = 4;
 __global__ void __launch_bounds__(256) moe_gather_f16_kernel(const uint2 *__restrict__ x, int topk, int k,
-                                                             int kblocks, const int32_t *__restrict__ tok_off,
-                                                             const int32_t *__restrict__ tile_off_dec,
+                                                             int kblocks, const int32_t *__restrict__ tile_off_dec,
+                                                             const int4 *__restrict__ tile_info_dec,
                                                              int num_experts, const int32_t *__restrict__ perm,
                                                              uint2 *__restrict__ xs, float *__restrict__ xinv) {
     static_assert(kMoeDecodeTile == 32, "a block covers the 32 rows of one decode tile");
-    __shared__ int s_p0, s_cnt;
     pdl_launch_dependents();
     pdl_wait();
     const int tile = static_cast<int>(blockIdx.x);
-    if (tile >= tile_off_dec[num_experts]) return;
-    if (threadIdx.x == 0) {
-        int lo = 0, hi = num_experts - 1;  // largest e with tile_off_dec[e] <= tile
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (tile_off_dec[mid] <= tile) lo = mid; else hi = mid - 1;
-        }
-        const int p0 = tok_off[lo] + (tile - tile_off_dec[lo]) * kMoeDecodeTile;
-        s_p0 = p0;
-        s_cnt = min(kMoeDecodeTile, tok_off[lo + 1] - p0);
-    }
-    __syncthreads();
-    const int p0 = s_p0, cnt = s_cnt;
+    const int ntiles = tile_off_dec[num_experts];
+    const int4 ti = tile_info_dec[tile];  // in bounds (the grid's bound); used only if tile < ntiles
+    if (tile >= ntiles) return;
+    const int p0 = ti.y, cnt = ti.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kbase = static_cast<int>(blockIdx.y) * kGatherKb;
     const int q4 = k >> 2;  // 4-value (8-byte) groups per row
@@ -211,8 +229,10 @@ inline int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
 
 int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k) {
     const int64_t kblocks = (k + 127) / 128;
-    return 2 * align256(4 * num_experts) + 3 * align256(4 * (num_experts + 1)) + align256(4 * pairs) +
-           align256(4 * moe_decode_tile_bound(pairs, num_experts) * kblocks * 32) + align256(2 * pairs * k);
+    const int64_t dec = moe_decode_tile_bound(pairs, num_experts);
+    return 2 * align256(4 * num_experts) + 3 * align256(4 * (num_experts + 1)) +
+           align256(16 * moe_gemm_tile_bound(pairs, num_experts)) + align256(16 * dec) + align256(4 * pairs) +
+           align256(4 * dec * kblocks * 32) + align256(2 * pairs * k);
 }
 
 MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, int64_t k) {
@@ -228,6 +248,10 @@ MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, in
     p += align256(4 * (num_experts + 1));
     r.tile_off_dec = reinterpret_cast<int32_t *>(p);
     p += align256(4 * (num_experts + 1));
+    r.tile_info = reinterpret_cast<int4 *>(p);
+    p += align256(16 * moe_gemm_tile_bound(pairs, num_experts));
+    r.tile_info_dec = reinterpret_cast<int4 *>(p);
+    p += align256(16 * moe_decode_tile_bound(pairs, num_experts));
     r.perm = reinterpret_cast<int32_t *>(p);
     p += align256(4 * pairs);
     r.xinv = reinterpret_cast<float *>(p);
@@ -245,7 +269,7 @@ cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64
         e = launch_pdl(moe_count_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts, r.counts);
     if (e == cudaSuccess)
         e = launch_pdl(moe_scan_kernel, dim3(1), dim3(kScanThreads), stream, static_cast<const int32_t *>(r.counts),
-                       num_experts, r.tok_off, r.tile_off, r.tile_off_dec, r.cursor);
+                       num_experts, r.tok_off, r.tile_off, r.tile_off_dec, r.tile_info, r.tile_info_dec, r.cursor);
     if (e == cudaSuccess)
         e = launch_pdl(moe_scatter_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts,
                        static_cast<const int32_t *>(r.tok_off), r.cursor, r.perm);
@@ -256,7 +280,7 @@ cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64
         return launch_pdl(moe_gather_f16_kernel,
                           dim3(static_cast<unsigned>(tbound), static_cast<unsigned>((kblocks + kGatherKb - 1) / kGatherKb)),
                           dim3(256), stream, static_cast<const uint2 *>(x), topk, static_cast<int>(k), kblocks,
-                          static_cast<const int32_t *>(r.tok_off), static_cast<const int32_t *>(r.tile_off_dec),
+                          static_cast<const int32_t *>(r.tile_off_dec), static_cast<const int4 *>(r.tile_info_dec),
                           num_experts, static_cast<const int32_t *>(r.perm), static_cast<uint2 *>(r.xs), r.xinv);
     }
     if (e == cudaSuccess)

@@ -156,7 +156,7 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 // The grouped MoE form: the routing (moe.cu) in device memory.
 struct MoeTiles {
     const int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert
-    const int32_t *tok_off;   // [E + 1] first pair of each expert in perm
+    const int4 *tile_info;    // [tile bound] {expert, first pair, pairs, 0} of each tile
     const int32_t *perm;      // pairs t * topk + j, expert by expert
     int topk, num_experts;
 };
@@ -189,8 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     constexpr bool MX = SC == kScaleMx;
     static_assert(!MOE || SC == kScaleBlock, "the grouped GEMM takes block scales");
     __shared__ int32_t s_pair[MOE ? kTileX : 1];  // MOE: this tile's pairs, -1 past its count
-    __shared__ int s_expert;
-    __shared__ int s_srow;                         // MOE: this CTA's row of block scales
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -238,28 +236,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
     int expert = 0;
     int live = kTileX;  // MOE: this tile's pairs
+    int srow_moe = 0;   // MOE: this CTA's row of block scales
     if (MOE) {
         // this CTA's expert and pairs (the routing kernels ran before it in
-        // the stream); every thread reads the same words, so the exit is
-        // uniform and happens before anything is allocated
+        // the stream): the tile count and the tile's record, two independent
+        // loads; every thread reads the same words, so the exit is uniform
+        // and happens before anything is allocated
         const int tile = blockIdx.y;
-        if (tile >= __ldg(moe.tile_off + moe.num_experts)) return;
-        if (threadIdx.x == 0) {
-            int lo = 0, hi = moe.num_experts - 1;  // largest e with tile_off[e] <= tile
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (__ldg(moe.tile_off + mid) <= tile) lo = mid; else hi = mid - 1;
-            }
-            s_expert = lo;
-            s_srow = lo * ((n + kTileW - 1) / kTileW) + wtile;
-        }
-        __syncthreads();
-        expert = s_expert;
-        const int p0 = __ldg(moe.tok_off + expert) + (tile - __ldg(moe.tile_off + expert)) * kTileX;
-        const int cnt = min(kTileX, __ldg(moe.tok_off + expert + 1) - p0);
-        m0 = p0;
-        live = cnt;
-        for (int i = threadIdx.x; i < kTileX; i += blockDim.x) s_pair[i] = i < cnt ? __ldg(moe.perm + p0 + i) : -1;
+        const int ntiles = __ldg(moe.tile_off + moe.num_experts);
+        const int4 ti = __ldg(moe.tile_info + tile);  // in bounds (the grid's bound); used if tile < ntiles
+        if (tile >= ntiles) return;
+        expert = ti.x;
+        m0 = ti.y;
+        live = ti.z;
+        srow_moe = expert * ((n + kTileW - 1) / kTileW) + wtile;
+        for (int i = threadIdx.x; i < kTileX; i += blockDim.x) s_pair[i] = i < live ? __ldg(moe.perm + m0 + i) : -1;
     }
 
     if (threadIdx.x == 0) {
@@ -521,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int h = (warp - kWarpEpi0) >> 2;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
         const int row = n0 + q * 32 + lane;
-        const float *srow = (ROW || MX) ? nullptr : scales + static_cast<int64_t>(MOE ? s_srow : wtile) * kblocks;
+        const float *srow = (ROW || MX) ? nullptr : scales + static_cast<int64_t>(MOE ? srow_moe : wtile) * kblocks;
         const int live_cols = MOE ? live - h * kHalfX : kHalfX;  // MOE: TMEM columns the MMAs wrote
         float tot[kHalfX];
 #pragma unroll
@@ -767,14 +758,15 @@ cudaError_t launch_prefill_moe(const DecodeArgs &a, const MoeArgs &g, const MoeR
     const int64_t wtiles = (a.n + kTileW - 1) / kTileW;
     // at most ceil(pairs / 256) full tiles plus one partial tile per expert;
     // the CTAs past the routing's actual tile count leave at once
-    const int64_t tbound = (pairs + kTileX - 1) / kTileX + (g.num_experts < pairs ? g.num_experts : pairs);
+    static_assert(kTileX == 256, "the routing's tile records are of 256 pairs");
+    const int64_t tbound = moe_gemm_tile_bound(pairs, g.num_experts);
     if (tbound > 65535) return cudaErrorNotSupported;
     const dim3 grid(static_cast<unsigned>(wtiles), static_cast<unsigned>(tbound));
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
     prefill_kernel<kScaleBlock, true><<<grid, kThreads, kSmemBytes, stream>>>(
         tm_x, tm_codes, a.scales, nullptr, 0, static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(pairs),
         static_cast<int>(a.n), static_cast<int>(a.k), kblocks, 0, 0, 0, 0, 1, 0,
-        MoeTiles{r.tile_off, r.tok_off, r.perm, static_cast<int>(g.topk), static_cast<int>(g.num_experts)});
+        MoeTiles{r.tile_off, r.tile_info, r.perm, static_cast<int>(g.topk), static_cast<int>(g.num_experts)});
     return cudaGetLastError();
 }
 
