@@ -85,32 +85,37 @@ cudaError_t launch_encode_probe(uint32_t first, int64_t count, uint8_t *codes, c
 // on the device in a caller workspace of moe_route_bytes(pairs, E, k) bytes.
 // Pairs per expert tile of the grouped decode path (the decode kernel's x rows).
 constexpr int kMoeDecodeTile = 32;
+// Pairs per tile of the tensor-core grouped GEMM (prefill.cu, MOE form):
+// 128 (deeper pipeline) while the experts average few enough pairs, else 256.
+constexpr int kMoeGemmTileNarrow = 128, kMoeGemmTileWide = 256;
 struct MoeRoute {
     int32_t *counts;    // [E] pairs per expert
     int32_t *cursor;    // [E] scatter cursors
     int32_t *tok_off;   // [E + 1] first pair of each expert in perm
-    int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert (tensor-core GEMM)
+    int32_t *tile_off;  // [E + 1] first GEMM tile (gemm_tile pairs) of each expert
     int32_t *tile_off_dec;  // [E + 1] first kMoeDecodeTile-pair tile of each expert (decode path)
-    int4 *tile_info;        // [GEMM tile bound] {expert, first pair, pairs, 0} of each 256-pair tile
+    int4 *tile_info;        // [GEMM tile bound] {expert, first pair, pairs, 0} of each GEMM tile
     int4 *tile_info_dec;    // [decode tile bound] the same for the kMoeDecodeTile-pair tiles
     int32_t *perm;      // [pairs] t * topk + j, expert by expert
     float *xinv;        // decode tiles: [tile bound][kblocks][32] f16 inverse factors, slot order
     void *xs;           // [pairs, k]: x[perm[q] / topk] in perm's order; bf16 for the
                         // tensor-core GEMM, f16 rescaled per (row, K block) for decode tiles
+    int gemm_tile;      // pairs per GEMM tile of this routing (kMoeGemmTileNarrow / Wide)
 };
 // Upper bound on the kMoeDecodeTile-pair tiles of `pairs` routed pairs:
 // one partial tile per expert at most, besides the full ones.
 inline int64_t moe_decode_tile_bound(int64_t pairs, int64_t num_experts) {
     return (pairs + kMoeDecodeTile - 1) / kMoeDecodeTile + (num_experts < pairs ? num_experts : pairs);
 }
-// ... and on the 256-pair tiles of the tensor-core grouped GEMM.
-inline int64_t moe_gemm_tile_bound(int64_t pairs, int64_t num_experts) {
-    return (pairs + 255) / 256 + (num_experts < pairs ? num_experts : pairs);
+// ... and on the `tile`-pair tiles of the tensor-core grouped GEMM.
+inline int64_t moe_gemm_tile_bound(int64_t pairs, int64_t num_experts, int tile) {
+    return (pairs + tile - 1) / tile + (num_experts < pairs ? num_experts : pairs);
 }
 int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k);
 MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, int64_t k);
 // decode_tiles: write xs as f16 with the per-(row, K block) inverse factors
 // of each decode tile in xinv (the decode kernel's operands); else bf16.
+// The GEMM tiles are of r.gemm_tile pairs.
 cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64_t pairs, int topk,
                              int num_experts, const MoeRoute &r, bool decode_tiles, cudaStream_t stream);
 uint32_t take_moe_error();

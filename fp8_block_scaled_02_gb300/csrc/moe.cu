@@ -7,8 +7,8 @@
 // synchronisation, in the caller's workspace:
 //   counts[e]    pairs routed to expert e
 //   tok_off[e]   exclusive prefix sum of counts (tok_off[E] = valid pairs)
-//   tile_off[e]  exclusive prefix sum of ceil(counts / 256): the first of
-//                expert e's 256-pair tiles (tile_off[E] = tiles in all)
+//   tile_off[e]  exclusive prefix sum of ceil(counts / gemm_tile): the
+//                first of expert e's GEMM tiles (tile_off[E] = tiles in all)
 //   tile_off_dec[e]  the same for tiles of kMoeDecodeTile pairs (the
 //                decode path for few pairs per expert)
 //   tile_info[t], tile_info_dec[t]  tile t of either kind as {expert,
@@ -53,8 +53,7 @@ __global__ void moe_count_kernel(const int32_t *__restrict__ ids, int64_t pairs,
 // Tiles of `size` pairs from the block's inclusive scans (s_tok: pairs,
 // s_t: tiles of each expert): record t = {expert, first pair, pairs, 0},
 // the expert found by a search in shared memory.
-template <int kSize>
-__device__ __forceinline__ void write_tiles(const int32_t *s_tok, const int32_t *s_t, int num_experts,
+__device__ __forceinline__ void write_tiles(const int32_t *s_tok, const int32_t *s_t, int num_experts, int size,
                                             int4 *__restrict__ info) {
     const int ntiles = s_t[num_experts - 1];
     for (int t = threadIdx.x; t < ntiles; t += kScanThreads) {
@@ -65,16 +64,17 @@ __device__ __forceinline__ void write_tiles(const int32_t *s_tok, const int32_t 
         }
         const int32_t first_pair = lo ? s_tok[lo - 1] : 0;
         const int32_t cnt = s_tok[lo] - first_pair;
-        const int32_t i = t - (s_t[lo] - (cnt + kSize - 1) / kSize);  // tile index within the expert
-        info[t] = make_int4(lo, first_pair + kSize * i, min(kSize, cnt - kSize * i), 0);
+        const int32_t i = t - (s_t[lo] - (cnt + size - 1) / size);  // tile index within the expert
+        info[t] = make_int4(lo, first_pair + size * i, min(size, cnt - size * i), 0);
     }
 }
 
-// Exclusive prefix sums of counts and of their tile counts (256 pairs and
-// kMoeDecodeTile pairs), the tile records of both kinds; the scatter
+// Exclusive prefix sums of counts and of their tile counts (gemm_tile pairs
+// and kMoeDecodeTile pairs), the tile records of both kinds; the scatter
 // cursors start at zero.
 __global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *__restrict__ counts,
-                                                                int num_experts, int32_t *__restrict__ tok_off,
+                                                                int num_experts, int gemm_tile,
+                                                                int32_t *__restrict__ tok_off,
                                                                 int32_t *__restrict__ tile_off,
                                                                 int32_t *__restrict__ tile_off_dec,
                                                                 int4 *__restrict__ tile_info,
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *_
     const int e = threadIdx.x;
     const int32_t c = e < num_experts ? counts[e] : 0;
     s_tok[e] = c;
-    s_tile[e] = (c + 255) >> 8;
+    s_tile[e] = (c + gemm_tile - 1) / gemm_tile;
     s_dec[e] = (c + kMoeDecodeTile - 1) / kMoeDecodeTile;
     __syncthreads();
     // Hillis-Steele inclusive scan over the block
@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *_
         tile_off[0] = 0;
         tile_off_dec[0] = 0;
     }
-    write_tiles<256>(s_tok, s_tile, num_experts, tile_info);
-    write_tiles<kMoeDecodeTile>(s_tok, s_dec, num_experts, tile_info_dec);
+    write_tiles(s_tok, s_tile, num_experts, gemm_tile, tile_info);
+    write_tiles(s_tok, s_dec, num_experts, kMoeDecodeTile, tile_info_dec);
 }
 
 // xs[q, :] = x[perm[q] / topk, :] for the routed pairs q < tok_off[E]; one
@@ -231,7 +231,8 @@ int64_t moe_route_bytes(int64_t pairs, int64_t num_experts, int64_t k) {
     const int64_t kblocks = (k + 127) / 128;
     const int64_t dec = moe_decode_tile_bound(pairs, num_experts);
     return 2 * align256(4 * num_experts) + 3 * align256(4 * (num_experts + 1)) +
-           align256(16 * moe_gemm_tile_bound(pairs, num_experts)) + align256(16 * dec) + align256(4 * pairs) +
+           align256(16 * moe_gemm_tile_bound(pairs, num_experts, kMoeGemmTileNarrow)) + align256(16 * dec) +
+           align256(4 * pairs) +
            align256(4 * dec * kblocks * 32) + align256(2 * pairs * k);
 }
 
@@ -249,7 +250,7 @@ MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, in
     r.tile_off_dec = reinterpret_cast<int32_t *>(p);
     p += align256(4 * (num_experts + 1));
     r.tile_info = reinterpret_cast<int4 *>(p);
-    p += align256(16 * moe_gemm_tile_bound(pairs, num_experts));
+    p += align256(16 * moe_gemm_tile_bound(pairs, num_experts, kMoeGemmTileNarrow));
     r.tile_info_dec = reinterpret_cast<int4 *>(p);
     p += align256(16 * moe_decode_tile_bound(pairs, num_experts));
     r.perm = reinterpret_cast<int32_t *>(p);
@@ -257,19 +258,22 @@ MoeRoute moe_route_views(void *workspace, int64_t pairs, int64_t num_experts, in
     r.xinv = reinterpret_cast<float *>(p);
     p += align256(4 * moe_decode_tile_bound(pairs, num_experts) * ((k + 127) / 128) * 32);
     r.xs = p;
+    r.gemm_tile = kMoeGemmTileWide;
     return r;
 }
 
 cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64_t pairs, int topk,
                              int num_experts, const MoeRoute &r, bool decode_tiles, cudaStream_t stream) {
     if (num_experts < 1 || num_experts > kScanThreads || pairs < 1) return cudaErrorInvalidValue;
+    if (r.gemm_tile != kMoeGemmTileNarrow && r.gemm_tile != kMoeGemmTileWide) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(r.counts, 0, 4 * static_cast<size_t>(num_experts), stream);
     const unsigned blocks = static_cast<unsigned>((pairs + 255) / 256 < 1024 ? (pairs + 255) / 256 : 1024);
     if (e == cudaSuccess)
         e = launch_pdl(moe_count_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts, r.counts);
     if (e == cudaSuccess)
         e = launch_pdl(moe_scan_kernel, dim3(1), dim3(kScanThreads), stream, static_cast<const int32_t *>(r.counts),
-                       num_experts, r.tok_off, r.tile_off, r.tile_off_dec, r.tile_info, r.tile_info_dec, r.cursor);
+                       num_experts, r.gemm_tile, r.tok_off, r.tile_off, r.tile_off_dec, r.tile_info, r.tile_info_dec,
+                       r.cursor);
     if (e == cudaSuccess)
         e = launch_pdl(moe_scatter_kernel, dim3(blocks), dim3(256), stream, ids, pairs, num_experts,
                        static_cast<const int32_t *>(r.tok_off), r.cursor, r.perm);

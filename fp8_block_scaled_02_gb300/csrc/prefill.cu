@@ -58,22 +58,43 @@ namespace {
 __device__ uint32_t g_prefill_err;
 
 constexpr int kTileW = 128;                 // weight rows per CTA (= one scale row block, = MMA M)
-constexpr int kHalfX = 128;                 // x rows (TMEM columns) per epilogue half
-constexpr int kTileX = 2 * kHalfX;          // x rows per CTA (= MMA N)
 constexpr int kKB = 128;                    // K per block
 constexpr int kPanel = 128 * 128;           // one 64-column bf16 panel of 128 weight rows, 16 KB
-constexpr int kXPanel = kTileX * 128;       // one 64-column bf16 panel of the 256 x rows, 32 KB
-constexpr int kXStage = 2 * kXPanel;        // one K block of x, 64 KB
-constexpr int kXStages = 2;
-constexpr int kXBytes = kXStages * kXStage;  // x ring: 128 KB
 constexpr int kASlots = 2;                  // decoded weight blocks in flight
 constexpr int kASlot = 2 * kPanel;          // 32 KB
 constexpr int kCStage = kTileW * kKB;      // one K block of e4m3 codes, 16 KB
-constexpr int kCStages = 2;                 // codes ring
-constexpr int kCodesAhead = 4;              // L2 prefetch distance (K blocks past the load)
 constexpr int kRing = 8;  // MMA-completion barriers, one per K block; >= every look-back
-static_assert(kXStages <= kRing && kASlots <= kRing, "a wait must never reach back a full ring");
-constexpr int kTmemCols = 512;              // partials D_0, D_1: columns [0, 256), [256, 512)
+
+// The geometry of a CTA with TX x rows (same 225 KB of shared memory in
+// both forms).
+//  TX = 256 (dense, and the grouped MoE with many pairs per expert): the
+//  MMA's N up to 256, a two-stage x ring of 64 KB stages, a two-stage codes
+//  ring; partials D_0, D_1 in TMEM columns [0, 256) and [256, 512).
+//  TX = 128 (the grouped MoE with up to ~128 pairs per expert; its MMAs run
+//  N = pairs rounded up to 16): the x stage is 32 KB and the space buys
+//  depth, a three-stage x ring and a four-stage codes ring.  Each such CTA
+//  streams its own expert rows from HBM, which no other CTA shares, with
+//  one CTA per SM: clock stamps of the two-stage form showed each codes
+//  load landing about 2600 cycles after its issue and a K block every ~2000
+//  cycles, the codes ring's round trip.  Partials in columns [0, 128),
+//  [128, 256).
+template <int TX>
+struct Geo {
+    static_assert(TX == 256 || TX == 128, "two geometries");
+    static constexpr int kTileX = TX;                // x rows per CTA
+    static constexpr int kHalfX = kTileX / 2;        // x rows (TMEM columns) per epilogue half
+    static constexpr int kXPanel = kTileX * 128;     // one 64-column bf16 panel of the x rows
+    static constexpr int kXStage = 2 * kXPanel;      // one K block of x
+    static constexpr int kXStages = TX == 128 ? 3 : 2;
+    static constexpr int kXBytes = kXStages * kXStage;
+    static constexpr int kCStages = TX == 128 ? 4 : 2;     // codes ring
+    static constexpr int kCodesAhead = TX == 128 ? 6 : 4;  // L2 prefetch distance (K blocks past the load)
+    static constexpr int kTmemCols = 2 * kTileX;     // partials D_0, D_1
+    static constexpr int kSmemBytes = 1024 + kXBytes + kASlots * kASlot + kCStages * kCStage + 256;
+    static_assert(kXStages <= kRing && kASlots <= kRing, "a wait must never reach back a full ring");
+    static_assert(kSmemBytes + 4 * kTileX + 64 <= 227 * 1024, "shared memory per CTA (with the static arrays)");
+    static_assert(kCodesAhead >= kCStages, "the L2 prefetch runs at or past the loads");
+};
 
 // 20 warps in 5 warpgroups (a warpgroup's warps all take the same register
 // count):
@@ -99,8 +120,6 @@ static_assert(4 * 32 * kRegCtl + kNumDec * 32 * kRegDec + kNumEpi * 32 * kRegEpi
 static_assert(kThreads * kRegLaunch <= 65536, "launch allocation exceeds the register file");
 static_assert(kRegCtl % 8 == 0 && kRegDec % 8 == 0 && kRegEpi % 8 == 0, "setmaxnreg counts are multiples of 8");
 static_assert(kNumDec % 4 == 0 && kNumEpi % 4 == 0, "roles must fill whole warpgroups");
-constexpr int kSmemBytes = 1024 + kXBytes + kASlots * kASlot + kCStages * kCStage + 256;
-static_assert(kSmemBytes + 4 * kTileX + 64 <= 227 * 1024, "shared memory per CTA (with the static arrays)");
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
@@ -115,8 +134,8 @@ __host__ __device__ constexpr uint32_t idesc_f16() {
 }
 
 // MOE: x rows per TMA box.  A tile loads only the boxes that hold its pairs
-// (an expert's tile often holds far fewer than 256); stacked at 4 KB steps
-// the boxes give the layout of one 256-row box.
+// (an expert's tile often holds fewer than 128); stacked at 4 KB steps the
+// boxes give the layout of one 128-row box.
 constexpr int kMoeXBox = 32;
 
 __device__ __forceinline__ void fail(uint32_t bit) { atomicOr(&g_prefill_err, bit); }
@@ -155,7 +174,7 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 
 // The grouped MoE form: the routing (moe.cu) in device memory.
 struct MoeTiles {
-    const int32_t *tile_off;  // [E + 1] first 256-pair tile of each expert
+    const int32_t *tile_off;  // [E + 1] first GEMM tile of each expert
     const int4 *tile_info;    // [tile bound] {expert, first pair, pairs, 0} of each tile
     const int32_t *perm;      // pairs t * topk + j, expert by expert
     int topk, num_experts;
@@ -166,17 +185,16 @@ struct MoeTiles {
 // applied to the total) or kScaleMx (e8m0 [n, groups], folded into the
 // decoded weights).
 // MOE: grouped GEMM over routed experts (block scales).  blockIdx.y is a
-// tile of up to 256 (token, slot) pairs of one expert (CTAs past the last
+// tile of up to TX (token, slot) pairs of one expert (CTAs past the last
 // tile leave at once), blockIdx.x a 128-row tile of that expert's weight
 // (codes [E * n, k], scales [E, ceil(n/128), kblocks]).  tm_x maps the x
 // rows copied in pair order (moe.cu: xs [pairs, k]) in boxes of kMoeXBox
 // rows, so a tile's rows are ordinary TMA boxes starting at its first pair;
 // output row j goes to y[pair_j * n + row] (y: [tokens, topk, n]).  The
 // tile's work follows its pair count: only the boxes holding its pairs are
-// loaded, the MMAs run N = pairs rounded up to 16 (at 24 pairs an expert
-// costs an eighth of the 256-wide MMA), and the epilogue reads only those
-// TMEM columns.
-template <int SC, bool MOE = false>
+// loaded, the MMAs run N = pairs rounded up to 16, and the epilogue reads
+// only those TMEM columns.
+template <int SC, bool MOE = false, int TX = 256>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tm_x,
                                                               const __grid_constant__ CUtensorMap tm_codes,
                                                               const float *__restrict__ scales,
@@ -188,11 +206,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     constexpr bool ROW = SC == kScaleRow;
     constexpr bool MX = SC == kScaleMx;
     static_assert(!MOE || SC == kScaleBlock, "the grouped GEMM takes block scales");
+    static_assert(MOE || TX == 256, "the dense form has 256 x rows per CTA");
+    using G = Geo<TX>;
+    constexpr int kTileX = G::kTileX, kHalfX = G::kHalfX, kXPanel = G::kXPanel, kXStage = G::kXStage,
+                  kXStages = G::kXStages, kXBytes = G::kXBytes, kCStages = G::kCStages,
+                  kCodesAhead = G::kCodesAhead, kTmemCols = G::kTmemCols;
     __shared__ int32_t s_pair[MOE ? kTileX : 1];  // MOE: this tile's pairs, -1 past its count
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    uint8_t *xring = smem;                              // [kXStages][2 panels][256 rows][128 B]
+    uint8_t *xring = smem;                              // [kXStages][2 panels][kTileX rows][128 B]
     uint8_t *aring = smem + kXBytes;                    // [kASlots][2 panels][128 rows][128 B]
     uint8_t *cring = aring + kASlots * kASlot;          // [kCStages][128 rows][128 B] codes
     uint64_t *bars = reinterpret_cast<uint64_t *>(cring + kCStages * kCStage);
@@ -305,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     tc_fence_after();
                     const uint64_t adesc = sw128_desc(smem_u32(aring + as * kASlot));
                     const uint64_t bdesc = sw128_desc(smem_u32(xring + xs * kXStage));
-                    const uint32_t d_tmem = tmem + 256 * b;
+                    const uint32_t d_tmem = tmem + kTileX * b;
     #pragma unroll
                     for (int kk = 0; kk < kKB / 16; ++kk) {
                         const uint64_t aoff = static_cast<uint64_t>((kk >> 2) * (kPanel >> 4) + (kk & 3) * 2);
@@ -510,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // keeps their running totals in registers
         const int q = warp & 3;
         const int h = (warp - kWarpEpi0) >> 2;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * kHalfX;
         const int row = n0 + q * 32 + lane;
         const float *srow = (ROW || MX) ? nullptr : scales + static_cast<int64_t>(MOE ? srow_moe : wtile) * kblocks;
         const int live_cols = MOE ? live - h * kHalfX : kHalfX;  // MOE: TMEM columns the MMAs wrote
@@ -532,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 break;
             }
             tc_fence_after();
-            const uint32_t d_addr = lane_base + 256 * (kb & 1);
+            const uint32_t d_addr = lane_base + kTileX * (kb & 1);
 #pragma unroll
             for (int c = 0; c < kHalfX / 16; ++c) {
                 if (MOE && 16 * c >= live_cols) break;
@@ -642,12 +665,19 @@ static cudaError_t prefill_setup(int *sms = nullptr) {
             // fewer than the split was planned against (its epilogue warps
             // would wait forever for registers).
             cudaError_t e = cudaSuccess;
-            for (auto kern : {prefill_kernel<kScaleBlock>, prefill_kernel<kScaleRow>, prefill_kernel<kScaleMx>,
-                              prefill_kernel<kScaleBlock, true>}) {
+            using Kern = decltype(&prefill_kernel<kScaleBlock>);
+            const struct {
+                Kern kern;
+                int smem;
+            } forms[] = {{prefill_kernel<kScaleBlock>, Geo<256>::kSmemBytes},
+                         {prefill_kernel<kScaleRow>, Geo<256>::kSmemBytes},
+                         {prefill_kernel<kScaleMx>, Geo<256>::kSmemBytes},
+                         {prefill_kernel<kScaleBlock, true, 256>, Geo<256>::kSmemBytes},
+                         {prefill_kernel<kScaleBlock, true, 128>, Geo<128>::kSmemBytes}};
+            for (const auto &f : forms) {
                 cudaFuncAttributes fa = {};
-                if (e == cudaSuccess)
-                    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-                if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+                if (e == cudaSuccess) e = cudaFuncSetAttribute(f.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, f.smem);
+                if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, f.kern);
                 if (e == cudaSuccess && fa.numRegs < kRegLaunch) e = cudaErrorInvalidConfiguration;
             }
             if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms[dev], cudaDevAttrMultiProcessorCount, dev);
@@ -670,6 +700,8 @@ cudaError_t launch_prefill(const DecodeArgs &a, cudaStream_t stream) {
     CUtensorMap tm_x;
     const uint64_t k = static_cast<uint64_t>(a.k), m = static_cast<uint64_t>(a.m);
     // one TMA box = the x rows of one MMA unit: all 256 of the CTA's rows
+    constexpr int kTileX = Geo<256>::kTileX;
+    constexpr int kSmemBytes = Geo<256>::kSmemBytes;
     if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, k, m, k * 2, 64,
                               static_cast<uint32_t>(kTileX), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
@@ -756,17 +788,28 @@ cudaError_t launch_prefill_moe(const DecodeArgs &a, const MoeArgs &g, const MoeR
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int64_t wtiles = (a.n + kTileW - 1) / kTileW;
-    // at most ceil(pairs / 256) full tiles plus one partial tile per expert;
+    // at most ceil(pairs / tile) full tiles plus one partial tile per expert;
     // the CTAs past the routing's actual tile count leave at once
-    static_assert(kTileX == 256, "the routing's tile records are of 256 pairs");
-    const int64_t tbound = moe_gemm_tile_bound(pairs, g.num_experts);
+    // one routing tile is one CTA's x rows
+    static_assert(Geo<kMoeGemmTileNarrow>::kTileX == kMoeGemmTileNarrow, "narrow tiles");
+    static_assert(Geo<kMoeGemmTileWide>::kTileX == kMoeGemmTileWide, "wide tiles");
+    const bool narrow = r.gemm_tile == kMoeGemmTileNarrow;
+    if (!narrow && r.gemm_tile != kMoeGemmTileWide) return cudaErrorInvalidValue;
+    const int64_t tbound = moe_gemm_tile_bound(pairs, g.num_experts, r.gemm_tile);
     if (tbound > 65535) return cudaErrorNotSupported;
     const dim3 grid(static_cast<unsigned>(wtiles), static_cast<unsigned>(tbound));
     const int kblocks = static_cast<int>((a.k + kKB - 1) / kKB);
-    prefill_kernel<kScaleBlock, true><<<grid, kThreads, kSmemBytes, stream>>>(
-        tm_x, tm_codes, a.scales, nullptr, 0, static_cast<__nv_bfloat16 *>(a.y), static_cast<int>(pairs),
-        static_cast<int>(a.n), static_cast<int>(a.k), kblocks, 0, 0, 0, 0, 1, 0,
-        MoeTiles{r.tile_off, r.tile_info, r.perm, static_cast<int>(g.topk), static_cast<int>(g.num_experts)});
+    const MoeTiles tiles{r.tile_off, r.tile_info, r.perm, static_cast<int>(g.topk), static_cast<int>(g.num_experts)};
+    auto y = static_cast<__nv_bfloat16 *>(a.y);
+    const int pi = static_cast<int>(pairs), ni = static_cast<int>(a.n), ki = static_cast<int>(a.k);
+    if (narrow)
+        prefill_kernel<kScaleBlock, true, kMoeGemmTileNarrow>
+            <<<grid, kThreads, Geo<kMoeGemmTileNarrow>::kSmemBytes, stream>>>(
+                tm_x, tm_codes, a.scales, nullptr, 0, y, pi, ni, ki, kblocks, 0, 0, 0, 0, 1, 0, tiles);
+    else
+        prefill_kernel<kScaleBlock, true, kMoeGemmTileWide>
+            <<<grid, kThreads, Geo<kMoeGemmTileWide>::kSmemBytes, stream>>>(
+                tm_x, tm_codes, a.scales, nullptr, 0, y, pi, ni, ki, kblocks, 0, 0, 0, 0, 1, 0, tiles);
     return cudaGetLastError();
 }
 

@@ -376,7 +376,9 @@ int fp8bs_moe_gemv(const void *x_bf16, int64_t m, const int32_t *expert_ids,
  * fp8bs_gemv_ws prepares x (every x within 2^-31 of its block's largest
  * |x| converts exactly; the codes enter the tensor cores as f16); otherwise one grouped
  * GEMM on the 5th-generation tensor cores (the weight decoded to bf16 in
- * shared memory) runs tiles of up to 256 pairs of one expert.  Every
+ * shared memory) runs tiles of up to 128 pairs of one expert (a deeper
+ * pipeline) while the experts average at most 128 pairs, else of up to
+ * 256.  Every
  * selected expert's weight is read once per tile of its pairs;
  * fp8bs_moe_gemv instead runs the decode kernel per 32 tokens, reading
  * every selected expert once per 32 tokens.

@@ -232,11 +232,11 @@ def test_moe_grouped_many_tiles_per_expert(pkg):
 
 def test_moe_grouped_pair_counts_across_box_and_mma_edges(pkg):
     """One routing whose experts receive pair counts on both sides of every
-    32-row x box, 16-wide MMA-N step and 256-pair expert tile edge, and of
-    the 192-pair edge (tokens shuffled): each expert tile loads only the x
-    boxes holding its pairs and runs its MMAs at N = pairs rounded up to 16;
-    every output is checked in full."""
-    counts = [1, 15, 16, 17, 31, 32, 33, 0, 127, 128, 129, 191, 192, 193, 255, 256, 257, 383, 384, 385, 5]
+    32-row x box, 16-wide MMA-N step, 64-column epilogue half and 128-pair
+    expert tile edge (up to three tiles per expert; tokens shuffled): each
+    expert tile loads only the x boxes holding its pairs and runs its MMAs
+    at N = pairs rounded up to 16; every output is checked in full."""
+    counts = [1, 15, 16, 17, 31, 32, 33, 0, 63, 64, 65, 127, 128, 129, 191, 192, 193, 255, 256, 257, 383, 384, 385, 5]
     E, n, k = len(counts), 256, 512
     codes, scales = experts(E, n, k, 41)
     ids = np.repeat(np.arange(E, dtype=np.int32), counts)
