@@ -72,12 +72,13 @@ constexpr int kRing = 8;  // MMA-completion barriers, one per K block; >= every 
 //  ring; partials D_0, D_1 in TMEM columns [0, 256) and [256, 512).
 //  TX = 128 (the grouped MoE with up to ~128 pairs per expert; its MMAs run
 //  N = pairs rounded up to 16): the x stage is 32 KB and the space buys
-//  depth, a three-stage x ring and a four-stage codes ring.  Each such CTA
-//  streams its own expert rows from HBM, which no other CTA shares, with
-//  one CTA per SM: clock stamps of the two-stage form showed each codes
-//  load landing about 2600 cycles after its issue and a K block every ~2000
-//  cycles, the codes ring's round trip.  Partials in columns [0, 128),
-//  [128, 256).
+//  depth, a four-stage x ring.  Each such CTA streams its own expert rows
+//  from HBM, which no other CTA shares, with one CTA per SM: clock stamps of
+//  the two-stage form showed each load landing 2600-4100 cycles after its
+//  issue and a K block every ~2000 cycles, a ring's round trip.  Measured
+//  against a three-stage x ring with four codes stages: 810 vs 820 us (256
+//  experts, 96 pairs each); deeper codes rings or L2 prefetch gained
+//  nothing.  Partials in columns [0, 128), [128, 256).
 template <int TX>
 struct Geo {
     static_assert(TX == 256 || TX == 128, "two geometries");
@@ -85,9 +86,9 @@ struct Geo {
     static constexpr int kHalfX = kTileX / 2;        // x rows (TMEM columns) per epilogue half
     static constexpr int kXPanel = kTileX * 128;     // one 64-column bf16 panel of the x rows
     static constexpr int kXStage = 2 * kXPanel;      // one K block of x
-    static constexpr int kXStages = TX == 128 ? 3 : 2;
+    static constexpr int kXStages = TX == 128 ? 4 : 2;
     static constexpr int kXBytes = kXStages * kXStage;
-    static constexpr int kCStages = TX == 128 ? 4 : 2;     // codes ring
+    static constexpr int kCStages = 2;                     // codes ring
     static constexpr int kCodesAhead = TX == 128 ? 6 : 4;  // L2 prefetch distance (K blocks past the load)
     static constexpr int kTmemCols = 2 * kTileX;     // partials D_0, D_1
     static constexpr int kSmemBytes = 1024 + kXBytes + kASlots * kASlot + kCStages * kCStage + 256;
