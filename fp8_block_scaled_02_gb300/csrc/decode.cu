@@ -85,10 +85,16 @@ struct Cfg {
     // loaded by every warp, which costs shared-memory reads but no
     // cross-warp reduction and only MT x 4 accumulators per thread.
     static constexpr int kBN = 128;
-    // ring depth: a fifth stage keeps the m <= 8 stream fuller (the
-    // lm_head-sized GEMV measured 1.6% faster); wider x tiles leave room for
-    // four (m <= 16) or three stages within two CTAs per SM
-    static constexpr int kStages = MT == 1 ? 5 : (MT == 2 ? 4 : 3);
+    // ring depth.  Clock stamps on [12288, 4096] put each code tile's load
+    // at ~4700 cycles from issue to landing against 1500-2500 cycles of MMAs
+    // per K block at m = 9..32, so the ring's depth sets the K-block rate
+    // there; for m > 8 the split-K buffers reuse the drained ring to make
+    // room for a deeper one (this CTA's partials from MT = 2, the cluster's
+    // pushes too at MT = 4, which costs one more cluster barrier).  m <= 8
+    // keeps five stages (a sixth measured 1.6% slower on lm_head).
+    static constexpr int kStages = MT == 1 ? 5 : (MT == 2 ? 5 : 4);
+    static constexpr bool kRedInRing = MT >= 2;
+    static constexpr bool kRecvInRing = MT >= 4;
     static constexpr bool kConv = F16 && !XP;           // converter warp present
     static constexpr int kConvWarps = kConv ? 1 : 0;
     static constexpr int kThreads = (kConsumerWarps + 1 + kConvWarps) * 32;
@@ -104,11 +110,15 @@ struct Cfg {
     // splits * ceil(kBN / splits) <= kBN + 7 rows (even, for alignment)
     static constexpr int kRecvFloats = (kBN + kMaxSplit) * kRedStride;
     static constexpr int kRecvBytes = kRecvFloats * 4;
-    static constexpr int kSmemBytes =
-        1024 + kStages * kStageBytes + kStages * kAuxBytes + kRedBytes + kRecvBytes + 3 * kStages * 8;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kStages * kAuxBytes +
+                                      (kRedInRing ? 0 : kRedBytes) + (kRecvInRing ? 0 : kRecvBytes) +
+                                      3 * kStages * 8;
     static constexpr int kMinBlocks = 2;
     static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-    static_assert((kStages * kAuxBytes + kRedBytes + kRecvBytes) % 8 == 0, "barriers must stay 8-byte aligned");
+    static_assert(kAuxBytes % 8 == 0 && kRedBytes % 16 == 0 && kRecvBytes % 8 == 0,
+                  "the split-K buffers and the barriers stay aligned");
+    static_assert(kRedBytes + kRecvBytes <= kStages * kStageBytes, "the split-K buffers fit in the drained ring");
+    static_assert(!kRecvInRing || kRedInRing, "the receive buffer follows the partials");
     static_assert(kSmemBytes <= 113 * 1024, "two CTAs per SM");
 };
 
@@ -248,9 +258,15 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     float *aux = reinterpret_cast<float *>(smem + kStages * C::kStageBytes);
-    float *red = aux + kStages * C::kXInvFloats;
-    float *recv = red + kBN * C::kRedStride;
-    uint64_t *full = reinterpret_cast<uint64_t *>(recv + C::kRecvFloats);
+    // split-K (one unit per CTA): this CTA's partials and the cluster's
+    // pushes, in the ring once every stage is consumed (see below) or after
+    // the exponent area
+    float *own = aux + kStages * C::kXInvFloats;
+    float *red = C::kRedInRing ? reinterpret_cast<float *>(smem) : own;
+    if (!C::kRedInRing) own += kBN * C::kRedStride;
+    float *recv = C::kRecvInRing ? red + kBN * C::kRedStride : own;
+    if (!C::kRecvInRing) own += C::kRecvFloats;
+    uint64_t *full = reinterpret_cast<uint64_t *>(own);
     uint64_t *xready = full + kStages;
     uint64_t *empty = xready + kStages;
 
@@ -678,6 +694,11 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
+            // split-K: the partials go to `red`, which may overlay the ring:
+            // every consumer warp has consumed every stage of its single
+            // unit (and every TMA copy has landed) once all of them are here
+            // -- failed warps included, so that none waits for a warp that left
+            if (C::kRedInRing && splits > 1) asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             if (failed) break;
             // acc[j][q] is y[m = 8j + t + 4(q&1)][n_local = ra + (q>>1)]
 #pragma unroll
@@ -701,11 +722,16 @@ __device__ __forceinline__ void decode_body(const BatchParams *bp, const float *
     // Split-K: one row tile per CTA; reduce across the cluster in rank order.
     // CTA r finishes rows [r * rows_per, (r + 1) * rows_per) of the tile.
     // Every CTA pushes each row's partial straight into its finisher's
-    // receive buffer (DSMEM stores, slot = source rank), then one cluster
-    // barrier (release / acquire) makes all of them visible; each CTA sums
-    // its slots locally in rank order and leaves.  Nothing reads another
-    // CTA's shared memory, so no second barrier is needed before exit.
+    // receive buffer (DSMEM stores, slot = source rank; where the buffer
+    // overlays the owner's drained ring, a first cluster barrier waits for
+    // every CTA's main loop), then a cluster barrier (release / acquire) makes all
+    // of them visible; each CTA sums its slots locally in rank order and
+    // leaves.  Nothing reads another CTA's shared memory, so no further
+    // barrier is needed before exit.
     __syncthreads();  // local partials complete in red
+    // pushes into a ring: wait until every CTA of the cluster is past its
+    // main loop
+    if (C::kRecvInRing) cluster_sync_all();
     const int n0 = tile0 * kBN;
     const int rank = static_cast<int>(cluster_ctarank());
     const int rows_per = (kBN + splits - 1) / splits;
