@@ -213,3 +213,35 @@ def test_threshold_count_of_correctly_rounded_outputs_meets_the_bar():
         y = tolerance.bf16_bits_to_f64(yb)
         worst = max(worst, float(np.linalg.norm(y - y64) / np.linalg.norm(y64)))
     assert worst < 2e-3, worst
+
+
+def test_a_256_output_row_can_miss_the_bar_when_rounded_correctly():
+    """The statistic is reliable over a call's outputs, not over every row of
+    256: in the grouped-MoE case with activations near 1e-35 (8 experts of
+    [256, 1024] from the seeded generators, top-2 routing of 64 tokens), the
+    correctly rounded bf16 of the fp64 result of token 40, slot 0 alone has
+    relative L2 error just above 2e-3 while every element meets its bound;
+    over all 128 (token, slot) rows of the call the statistic is far below
+    the bar.  This is why the MoE parity tests take relative L2 over the
+    call."""
+    e_count, n, k, m, topk = 8, 256, 1024, 64, 2
+    codes, scales = [], []
+    for i in range(e_count):
+        c, s = oracle.block_quantize(inputs.bf16_bits(inputs.gaussian_bf16((n, k), 0.02, 61 + i)))
+        codes.append(c)
+        scales.append(s)
+    codes, scales = np.stack(codes), np.stack(scales)
+    rng = np.random.default_rng(17)
+    ids = np.stack([rng.choice(e_count, size=topk, replace=False) for _ in range(m)]).astype(np.int32)
+    g = torch.Generator().manual_seed(6)
+    xb = inputs.bf16_bits((torch.randn((m, k), generator=g) * 1e-35).to(torch.bfloat16))
+    y64 = oracle.moe_gemv(xb, ids, codes, scales)                 # [m, topk, n]
+    yb = oracle.to_bf16_bits(y64.reshape(m * topk, n)).reshape(m, topk, n)
+    table = oracle.e4m3_decode_table()
+    e = ids[40, 0]
+    wmax = tolerance.block_wmax_rows(codes[e], scales[e], np.arange(n), table)
+    st = tolerance.gemv_errors(yb[40, 0][None, :], y64[40, 0][None, :], xb[40][None, :], wmax)
+    assert st["count"] == tolerance.REL_L2_MIN_COUNT
+    assert st["max_ratio"] <= 1.0 and st["rel_l2"] > 2e-3, st
+    y = tolerance.bf16_bits_to_f64(yb)
+    assert float(np.linalg.norm(y - y64) / np.linalg.norm(y64)) < 1.8e-3
