@@ -502,7 +502,7 @@ def moe_prefill_workload(torch, fp8bs, inputs, dev, experts=None):
            "l2": f"inputs larger than L2 ({E * n * k / 1e9:.1f} GB of expert codes, nearly all selected)"}
     # M=512 (24 pairs per expert on average) takes the grouped decode path,
     # M=2048 (96) the tensor-core grouped GEMM
-    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<4,0,true,true,true> + prefill_kernel<0,true>", [0, 1]),
+    return dict(calls=calls, cfg=cfg, dominant=("decode_kernel<4,0,true,true,true> + prefill_kernel<0,true,TX>", [0, 1]),
                 flops=True, hbm_bytes=hbm,
                 call_launches=[5, 5])
 

@@ -280,7 +280,8 @@ cudaError_t launch_moe_route(const void *x, int64_t k, const int32_t *ids, int64
     if (e == cudaSuccess && decode_tiles) {
         const int64_t tbound = moe_decode_tile_bound(pairs, num_experts);
         const int kblocks = static_cast<int>((k + 127) / 128);
-        if (tbound > 0x7FFFFFFF || k % 4 != 0) return cudaErrorInvalidValue;
+        if (tbound > 0x7FFFFFFF || k % 4 != 0 || (kblocks + kGatherKb - 1) / kGatherKb > 65535)
+            return cudaErrorInvalidValue;
         return launch_pdl(moe_gather_f16_kernel,
                           dim3(static_cast<unsigned>(tbound), static_cast<unsigned>((kblocks + kGatherKb - 1) / kGatherKb)),
                           dim3(256), stream, static_cast<const uint2 *>(x), topk, static_cast<int>(k), kblocks,
