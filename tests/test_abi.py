@@ -202,6 +202,25 @@ def test_moe_ws_validation(L):
     assert f(None, 0, None, 12, None, None, 256, 2048, 4096, None, None, 0, None) == 0
 
 
+@pytest.mark.parametrize("m,topk,e,k", [(64, 12, 256, 4096), (512, 12, 256, 4096), (2048, 12, 256, 4096),
+                                        (33, 1, 1, 16), (300, 6, 6, 256), (40, 2, 1024, 7168)])
+def test_moe_ws_bytes_cover_every_region(L, m, topk, e, k):
+    """The workspace holds, for P = m * topk routed pairs: the x copy (2 P k
+    bytes), the pair order (4 P), the per-expert offsets, one 16-byte record
+    per tile of either size (at most ceil(P / tile) + min(E, P) tiles) and,
+    for the decode tiles, one fp32 factor per (tile, 128-column K block,
+    row of 32): a library that reserved less would let a kernel write past
+    the caller's buffer."""
+    p = m * topk
+    cdiv = lambda a, b: -(-a // b)
+    dec_tiles = cdiv(p, 32) + min(e, p)
+    gemm_tiles = cdiv(p, 128) + min(e, p)
+    floor = 2 * p * k + 4 * p + 5 * 4 * e + 16 * (dec_tiles + gemm_tiles) + 4 * dec_tiles * cdiv(k, 128) * 32
+    got = L.fp8bs_moe_gemv_ws_bytes(m, topk, e, k)
+    assert got >= floor, (got, floor)
+    assert got <= floor + 9 * 256 + 4 * e, (got, floor)   # no more than region alignment beyond it
+
+
 def test_kv_validation(L):
     x, sl, s, c = P(0x10000), P(0x20000), P(0x30000), P(0x40000)
     a = L.fp8kv_append
